@@ -1,0 +1,228 @@
+"""CPU oracle for the fused attention forward -- TEST INFRASTRUCTURE ONLY.
+
+Only ``tests/``, ``__graft_entry__.smoke()`` and the benchmark's CPU-baseline
+leg may import this package.  The CUDA library neither imports it nor shares
+any code with it; ``fl_oracle.c`` is compiled on its own by :func:`build`.
+
+Every function returns float64 results for the bf16 inputs it is given (as
+uint16 bit patterns).  The definitions followed are those of the Flashlight
+pages: an attention forward ``softmax(score_mod(scale QK^T) + mask + bias) V``
+whose online-softmax rewrite is exact over the reals (gist.science summary,
+"Methodology" item 3; talk notes, "Compiler design 2: algebraic
+transformation").  The variant formulas come from the workload statement that
+accompanies the pages; ``fl_oracle.c`` lists them.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import sys
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "fl_oracle.c")
+_LIB_DIR = os.path.join(_HERE, "_build")
+_LIB = os.path.join(_LIB_DIR, "libfloracle.so")
+
+MOD = {"none": 0, "alibi": 1, "softcap": 2}
+MASK = {"none": 0, "causal": 1, "window": 2, "prefix": 3, "doc": 4}
+
+
+class _Problem(ctypes.Structure):
+    _fields_ = [
+        ("B", ctypes.c_int32), ("Hq", ctypes.c_int32), ("Hk", ctypes.c_int32),
+        ("Sq", ctypes.c_int32), ("Sk", ctypes.c_int32), ("D", ctypes.c_int32),
+        ("Dv", ctypes.c_int32),
+        ("q_stride", ctypes.c_int64 * 3), ("k_stride", ctypes.c_int64 * 3),
+        ("v_stride", ctypes.c_int64 * 3),
+        ("score_mod", ctypes.c_int32), ("softcap", ctypes.c_double),
+        ("alibi_slopes", ctypes.c_void_p),
+        ("mask", ctypes.c_int32), ("window", ctypes.c_int32), ("prefix", ctypes.c_int32),
+        ("doc_offsets", ctypes.c_void_p), ("doc_stride", ctypes.c_int32),
+        ("scale", ctypes.c_double),
+        ("bias", ctypes.c_void_p), ("bias_stride", ctypes.c_int64 * 3),
+    ]
+
+
+def build(force: bool = False, source: str = _SRC, target: str = _LIB) -> str:
+    """Compile ``fl_oracle.c`` into a shared library (plain C11 + OpenMP)."""
+    os.makedirs(os.path.dirname(target), exist_ok=True)
+    if (not force and os.path.exists(target)
+            and os.path.getmtime(target) >= os.path.getmtime(source)):
+        return target
+    tmp = target + f".tmp{os.getpid()}"
+    cmd = ["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-fopenmp",
+           "-o", tmp, source, "-lm"]
+    subprocess.run(cmd, check=True)
+    os.replace(tmp, target)
+    return target
+
+
+_lib = None
+
+
+def load(path: str | None = None):
+    """Load (building if needed) the oracle library."""
+    global _lib
+    if path is not None:
+        lib = ctypes.CDLL(path)
+    else:
+        if _lib is not None:
+            return _lib
+        lib = ctypes.CDLL(build())
+    lib.fl_oracle_attention.restype = ctypes.c_int
+    lib.fl_oracle_attention.argtypes = [
+        ctypes.POINTER(_Problem), ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
+        ctypes.c_void_p, ctypes.c_int64, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int]
+    lib.fl_oracle_max_threads.restype = ctypes.c_int
+    if path is None:
+        _lib = lib
+    return lib
+
+
+def max_threads() -> int:
+    return int(load().fl_oracle_max_threads())
+
+
+def _bshd_strides(a: np.ndarray) -> tuple[int, int, int]:
+    """Element strides of axes (batch, position, head) of a [B, S, H, D] view."""
+    if a.dtype != np.uint16 or a.ndim != 4 or a.strides[3] != 2:
+        raise ValueError("expected a [B, S, H, D] uint16 view with contiguous features")
+    return tuple(s // 2 for s in a.strides[:3])
+
+
+def _base_and_span(a: np.ndarray):
+    """Pointer to element 0 of a possibly-strided view."""
+    return a.__array_interface__["data"][0]
+
+
+def attention(q, k, v, *, mod="none", softcap=20.0, alibi_slopes=None, mask="none",
+              window=0, prefix=0, doc_offsets=None, scale=0.0, bias=None,
+              rows=None, nthreads=0, lib=None):
+    """Attention forward of ``q [B,Sq,Hq,D]``, ``k [B,Sk,Hk,D]``, ``v [B,Sk,Hk,Dv]``.
+
+    ``bias`` (optional) is ``[Hq, Sq, Sk]`` bf16 bits.  ``doc_offsets`` is the
+    int32 ``[B, max_docs+1]`` table of document starts padded with ``Sk``.
+    ``rows`` (optional) is an ``[n, 3]`` array of ``(b, h, i)``; then the
+    result is ``O [n, Dv]`` and ``LSE [n]``, else ``O [B,Sq,Hq,Dv]`` and
+    ``LSE [B,Hq,Sq]``.
+    """
+    lib = lib or load()
+    B, Sq, Hq, D = q.shape
+    Bk, Sk, Hk, Dk = k.shape
+    Dv = v.shape[3]
+    if Bk != B or Dk != D or v.shape[:3] != (B, Sk, Hk) or Hq % Hk:
+        raise ValueError("inconsistent shapes")
+    p = _Problem()
+    p.B, p.Hq, p.Hk, p.Sq, p.Sk, p.D, p.Dv = B, Hq, Hk, Sq, Sk, D, Dv
+    p.q_stride[:] = _bshd_strides(q)
+    p.k_stride[:] = _bshd_strides(k)
+    p.v_stride[:] = _bshd_strides(v)
+    p.score_mod = MOD[mod]
+    p.softcap = float(softcap)
+    keep = []
+    if alibi_slopes is not None:
+        sl = np.ascontiguousarray(alibi_slopes, dtype=np.float64)
+        keep.append(sl)
+        p.alibi_slopes = sl.ctypes.data
+    p.mask = MASK[mask]
+    p.window = int(window)
+    p.prefix = int(prefix)
+    if doc_offsets is not None:
+        do = np.ascontiguousarray(doc_offsets, dtype=np.int32)
+        keep.append(do)
+        p.doc_offsets = do.ctypes.data
+        p.doc_stride = do.shape[1]
+    p.scale = float(scale)
+    if bias is not None:
+        if bias.dtype != np.uint16 or bias.shape != (Hq, Sq, Sk):
+            raise ValueError("bias must be [Hq, Sq, Sk] bf16 bits")
+        p.bias = _base_and_span(bias)
+        p.bias_stride[:] = tuple(s // 2 for s in bias.strides)
+    if rows is None:
+        out = np.zeros((B, Sq, Hq, Dv), dtype=np.float64)
+        lse = np.zeros((B, Hq, Sq), dtype=np.float64)
+        rp, n = None, 0
+    else:
+        r = np.ascontiguousarray(rows, dtype=np.int64).reshape(-1, 3)
+        keep.append(r)
+        out = np.zeros((r.shape[0], Dv), dtype=np.float64)
+        lse = np.zeros((r.shape[0],), dtype=np.float64)
+        rp, n = r.ctypes.data, r.shape[0]
+    rc = lib.fl_oracle_attention(ctypes.byref(p), _base_and_span(q), _base_and_span(k),
+                                 _base_and_span(v), rp, n, out.ctypes.data,
+                                 lse.ctypes.data, int(nthreads))
+    if rc != 0:
+        raise RuntimeError("oracle rejected the problem")
+    return out, lse
+
+
+def diff_attention(q, k, v, lam, *, mask="none", scale=0.0, rows=None, nthreads=0, lib=None):
+    """Differential attention: ``(softmax(Q1 K1^T s) - lam softmax(Q2 K2^T s)) V``.
+
+    ``q [2,B,S,H,D]``, ``k [2,B,S,Hk,D]``, ``v [B,S,Hk,Dv]``.  Two independent
+    softmaxes (each with its own max and sum), one shared V (the pages name
+    differential attention among the complex variants: gist.science summary,
+    "Results"; the formula is the workload statement's).  Returns O and the
+    per-stream LSE stacked on a leading axis of 2.
+    """
+    o1, l1 = attention(q[0], k[0], v, mask=mask, scale=scale, rows=rows, nthreads=nthreads,
+                       lib=lib)
+    o2, l2 = attention(q[1], k[1], v, mask=mask, scale=scale, rows=rows, nthreads=nthreads,
+                       lib=lib)
+    return o1 - lam * o2, np.stack([l1, l2])
+
+
+def sigmoid_bf16(g):
+    """sigmoid of bf16 bit patterns, in float64."""
+    x = (np.asarray(g, dtype=np.uint16).astype(np.uint32) << np.uint32(16)).view(np.float32)
+    return 1.0 / (1.0 + np.exp(-x.astype(np.float64)))
+
+
+def evo_row(q, k, v, bias, gate, *, rows=None, nthreads=0, lib=None):
+    """Evoformer row-wise gated self-attention with pair bias.
+
+    ``q, k, v, gate`` are ``[N_seq, N_res, H, c]``; ``bias`` is
+    ``[H, N_res, N_res]`` shared by every MSA row.  For each MSA row s and head
+    h, attention runs over residues with ``b[h, i, j]`` added to the logits;
+    the output is gated by ``sigmoid(g[s, i, h, :])`` (talk notes, "End-to-end:
+    AlphaFold2"; shapes from the workload statement).  With ``rows`` the triples
+    are ``(s, h, i)``.
+    """
+    o, lse = attention(q, k, v, bias=bias, rows=rows, nthreads=nthreads, lib=lib)
+    if rows is None:
+        o = o * sigmoid_bf16(gate)
+    else:
+        r = np.asarray(rows, dtype=np.int64).reshape(-1, 3)
+        o = o * sigmoid_bf16(gate[r[:, 0], r[:, 2], r[:, 1], :])
+    return o, lse
+
+
+def evo_col(q, k, v, gate, *, rows=None, nthreads=0, lib=None):
+    """Evoformer column-wise gated self-attention (no bias).
+
+    Attention for each residue r and head h runs over the MSA rows (axis 0) of
+    the same ``[N_seq, N_res, H, c]`` tensors; the gate is the same
+    ``sigmoid(g[s, r, h, :])``.  Results are laid out ``O [N_res, N_seq, H, c]``
+    and ``LSE [N_res, H, N_seq]``; with ``rows`` the triples are ``(r, h, s)``.
+    """
+    qt, kt, vt = (np.swapaxes(x, 0, 1) for x in (q, k, v))
+    o, lse = attention(qt, kt, vt, rows=rows, nthreads=nthreads, lib=lib)
+    gt = np.swapaxes(gate, 0, 1)
+    if rows is None:
+        o = o * sigmoid_bf16(gt)
+    else:
+        r = np.asarray(rows, dtype=np.int64).reshape(-1, 3)
+        o = o * sigmoid_bf16(gt[r[:, 0], r[:, 2], r[:, 1], :])
+    return o, lse
+
+
+def alibi_slopes(H: int) -> np.ndarray:
+    """``slope_h = 2^(-8 (h+1) / H)`` for 0-based h (workload statement)."""
+    return np.array([2.0 ** (-8.0 * (h + 1) / H) for h in range(H)], dtype=np.float64)
+
+
+if __name__ == "__main__":  # pragma: no cover
+    print(build(force="--force" in sys.argv))

@@ -1,0 +1,364 @@
+"""Pins of the CPU oracle against facts that do not come from the oracle itself.
+
+Each ``pin_*`` function takes an oracle library handle (``oracle.load()`` or a
+deliberately broken copy built by ``test_oracle_mutants.py``) and raises
+``AssertionError`` when the oracle disagrees with
+
+* a closed form (constant scores give the mean of V over the allowed keys and
+  LSE = ln(#allowed); ALiBi over constant scores is a geometric series; a
+  two-key softcap problem; the Evoformer gate and the differential lambda on
+  constant scores),
+* an invariant (rows of P sum to one; per-row shift of the logits leaves O
+  unchanged and moves LSE by the shift; non-causal attention is equivariant
+  under a joint permutation of keys and values; causal row 0 returns v_0),
+* a library routine (float64 ``torch.nn.functional.scaled_dot_product_attention``
+  for vanilla, causal, boolean masks, ALiBi as an additive mask and GQA), or
+* a special case that reduces to another variant.
+
+None of these restates the oracle's row loop.
+"""
+from __future__ import annotations
+
+import math
+
+import numpy as np
+import torch
+
+import oracle
+import testdata
+
+ATOL = 1e-10
+
+
+def _bf(x) -> np.ndarray:
+    """float array -> bf16 bit patterns (values chosen exactly representable)."""
+    bits = testdata.f32_to_bf16_bits(np.asarray(x, dtype=np.float32))
+    back = testdata.bf16_bits_to_f32(bits)
+    assert np.array_equal(back, np.asarray(x, dtype=np.float32)), "value not exact in bf16"
+    return bits
+
+
+def _f64(bits) -> np.ndarray:
+    return testdata.bf16_bits_to_f32(bits).astype(np.float64)
+
+
+def _rand(shape, name, wl="pins"):
+    return testdata.normal_bf16(shape, wl, name)
+
+
+def _sdpa(q, k, v, mask=None, enable_gqa=False, scale=None):
+    """float64 SDPA over [B,S,H,D] bf16-bit inputs; returns O [B,S,H,Dv]."""
+    Q, K, V = (torch.from_numpy(_f64(x)).permute(0, 2, 1, 3) for x in (q, k, v))
+    kw = {}
+    if enable_gqa:
+        kw["enable_gqa"] = True
+    if scale is not None:
+        kw["scale"] = scale
+    o = torch.nn.functional.scaled_dot_product_attention(Q, K, V, attn_mask=mask, **kw)
+    return o.permute(0, 2, 1, 3).numpy()
+
+
+def _close(a, b, atol=ATOL, what=""):
+    err = float(np.max(np.abs(np.asarray(a) - np.asarray(b)))) if np.size(a) else 0.0
+    assert err <= atol, f"{what}: max |err| {err:.3e} > {atol:.1e}"
+
+
+# --------------------------------------------------------------------------
+# closed forms on constant scores (Q = 0)
+
+
+def _allowed_range(mask, i, S, window=0, prefix=0, starts=None):
+    """[lo, hi) of keys allowed for row i, from the interval form of each mask."""
+    if mask == "none":
+        return 0, S
+    if mask == "causal":
+        return 0, i + 1
+    if mask == "window":
+        return max(0, i - window + 1), i + 1
+    if mask == "prefix":
+        return 0, max(i + 1, min(prefix, S))
+    if mask == "doc":
+        ds = max(s for s in starts if s <= i)
+        return ds, i + 1
+    raise ValueError(mask)
+
+
+def pin_constant_scores(lib):
+    """Q = 0: every allowed key has logit 0, so O_i = mean of V over the
+    allowed keys (via prefix sums) and LSE_i = ln(number allowed)."""
+    S, H, D, Dv = 300, 2, 64, 64
+    q = _bf(np.zeros((2, S, H, D)))
+    k = _rand((2, S, H, D), "k")
+    v = _rand((2, S, H, Dv), "v")
+    vf = _f64(v)
+    csum = np.concatenate([np.zeros((2, 1, H, Dv)), np.cumsum(vf, axis=1)], axis=1)
+    starts = [[0, 37, 38, 120, 260], [0, 150]]
+    doc = np.full((2, 6), S, dtype=np.int32)
+    for b, st in enumerate(starts):
+        doc[b, : len(st)] = st
+    for mask, kw in [("none", {}), ("causal", {}), ("window", {"window": 37}),
+                     ("prefix", {"prefix": 50}), ("doc", {"doc_offsets": doc})]:
+        o, lse = oracle.attention(q, k, v, mask=mask, lib=lib, **kw)
+        for b in range(2):
+            for i in range(S):
+                lo, hi = _allowed_range(mask, i, S, kw.get("window", 0), kw.get("prefix", 0),
+                                        starts[b] if mask == "doc" else None)
+                mean = (csum[b, hi] - csum[b, lo]) / (hi - lo)
+                _close(o[b, i], mean, what=f"{mask} O row {i}")
+                _close(lse[b, :, i], math.log(hi - lo), what=f"{mask} LSE row {i}")
+
+
+def pin_alibi_geometric(lib):
+    """Q = 0 with ALiBi and no mask: z_ij = -slope_h |i-j|, so with r = e^-slope
+    LSE_i = ln(1 + r(1-r^i)/(1-r) + r(1-r^(S-1-i))/(1-r)), and with V = 1 the
+    output is 1.  Default slopes must be 2^(-8(h+1)/H)."""
+    S, H, D = 40, 4, 64
+    q = _bf(np.zeros((1, S, H, D)))
+    k = _rand((1, S, H, D), "k")
+    v = _bf(np.ones((1, S, H, 8)))
+    o, lse = oracle.attention(q, k, v, mod="alibi", lib=lib)
+    _close(o, 1.0, what="alibi P row sums")
+    for h in range(H):
+        r = math.exp(-(2.0 ** (-8.0 * (h + 1) / H)))
+        for i in range(S):
+            left = r * (1 - r ** i) / (1 - r)
+            right = r * (1 - r ** (S - 1 - i)) / (1 - r)
+            _close(lse[0, h, i], math.log(1 + left + right), what=f"alibi LSE h{h} i{i}")
+    # O with V = position index: the weighted mean of j under the geometric weights
+    vpos = _bf(np.broadcast_to(np.arange(S, dtype=np.float32)[None, :, None, None],
+                               (1, S, H, 8)).copy())
+    o, _ = oracle.attention(q, k, vpos, mod="alibi", lib=lib)
+    for h in (0, H - 1):
+        r = math.exp(-(2.0 ** (-8.0 * (h + 1) / H)))
+        for i in (0, 7, S - 1):
+            w = np.array([r ** abs(i - j) for j in range(S)])
+            _close(o[0, i, h, 0], float(np.dot(w, np.arange(S)) / w.sum()),
+                   what=f"alibi mean position h{h} i{i}")
+
+
+def pin_softcap_two_keys(lib):
+    """Two keys with scores a and 0 (q = x e_0, k_0 = y e_0, k_1 = 0): the
+    logits are cap*tanh(a/cap) and 0, so LSE = ln(1 + e^(cap tanh(a/cap)))
+    and O = sigmoid(cap tanh(a/cap)) v_0 + (1 - sigmoid) v_1."""
+    D, cap = 64, 20.0
+    for x, y in [(8.0, 4.0), (32.0, 24.0), (-16.0, 12.0), (64.0, 64.0)]:
+        q = np.zeros((1, 1, 1, D)); q[..., 0] = x
+        k = np.zeros((1, 2, 1, D)); k[0, 0, 0, 0] = y
+        v = np.zeros((1, 2, 1, 2)); v[0, 0, 0] = (1.0, 0.0); v[0, 1, 0] = (0.0, 1.0)
+        o, lse = oracle.attention(_bf(q), _bf(k), _bf(v), mod="softcap", softcap=cap, lib=lib)
+        a = x * y / math.sqrt(D)
+        z = cap * math.tanh(a / cap)
+        _close(lse[0, 0, 0], math.log1p(math.exp(z)), what=f"softcap LSE a={a}")
+        sg = 1.0 / (1.0 + math.exp(-z))
+        _close(o[0, 0, 0], [sg, 1 - sg], what=f"softcap O a={a}")
+
+
+def pin_one_hot(lib):
+    """q_i = c e_t and only key j* carries e_t: with c large the softmax is
+    one-hot and O_i = v_{j*} exactly; logits near 1000 also require the max
+    to be subtracted before exponentiating."""
+    S, D = 16, 64
+    c = 8000.0
+    q = np.zeros((1, S, 1, D)); q[..., 5] = c
+    k = np.zeros((1, S, 1, D)); k[0, 11, 0, 5] = 1.0
+    v = _rand((1, S, 1, D), "v1")
+    o, lse = oracle.attention(_bf(q), _bf(k), v, lib=lib)
+    for i in range(S):
+        _close(o[0, i, 0], _f64(v)[0, 11, 0], what="one-hot O")
+        _close(lse[0, 0, i], c / 8.0, atol=1e-9, what="one-hot LSE")
+
+
+def pin_rows_sum_to_one(lib):
+    """V = 1 gives O = sum_j P_ij = 1 for every variant and mask."""
+    S, H = 130, 2
+    q, k = _rand((1, S, H, 64), "q2"), _rand((1, S, H, 64), "k2")
+    v = _bf(np.ones((1, S, H, 4)))
+    doc = np.array([[0, 64, 100, S]], dtype=np.int32)
+    for mod in ("none", "alibi", "softcap"):
+        for mask, kw in [("none", {}), ("causal", {}), ("window", {"window": 9}),
+                         ("prefix", {"prefix": 33}), ("doc", {"doc_offsets": doc})]:
+            o, _ = oracle.attention(q, k, v, mod=mod, mask=mask, lib=lib, **kw)
+            _close(o, 1.0, atol=1e-12, what=f"{mod}/{mask} row sums")
+
+
+def pin_shift_invariance(lib):
+    """A bias constant along each row (b[h,i,j] = c_{h,i}) leaves O unchanged
+    and shifts LSE by c_{h,i}; a transposed bias index would break both."""
+    S, H = 48, 2
+    q, k, v = (_rand((1, S, H, 64), n) for n in ("q3", "k3", "v3"))
+    c = np.array([[(-1) ** i * (i % 7) * 0.5 for i in range(S)] for _ in range(H)])
+    bias = _bf(np.broadcast_to(c[:, :, None], (H, S, S)).copy())
+    o0, l0 = oracle.attention(q, k, v, lib=lib)
+    o1, l1 = oracle.attention(q, k, v, bias=bias, lib=lib)
+    _close(o1, o0, atol=1e-12, what="shift O")
+    _close(l1[0], l0[0] + c, atol=1e-12, what="shift LSE")
+
+
+def pin_permutation(lib):
+    """Non-causal vanilla: permuting keys and values together leaves O and LSE
+    unchanged; permuting queries permutes the outputs."""
+    S, H = 77, 2
+    q, k, v = (_rand((1, S, H, 64), n) for n in ("q4", "k4", "v4"))
+    perm = np.random.default_rng(7).permutation(S)
+    o0, l0 = oracle.attention(q, k, v, lib=lib)
+    o1, l1 = oracle.attention(q, np.ascontiguousarray(k[:, perm]),
+                              np.ascontiguousarray(v[:, perm]), lib=lib)
+    _close(o1, o0, atol=1e-12, what="KV permutation O")
+    _close(l1, l0, atol=1e-12, what="KV permutation LSE")
+    o2, _ = oracle.attention(np.ascontiguousarray(q[:, perm]), k, v, lib=lib)
+    _close(o2, o0[:, perm], atol=1e-12, what="Q permutation")
+
+
+def pin_causal_row0(lib):
+    """Causal row 0 sees only key 0: O_0 = v_0 and LSE_0 = scale q_0 . k_0."""
+    S, H = 20, 2
+    q, k, v = (_rand((2, S, H, 64), n) for n in ("q5", "k5", "v5"))
+    o, lse = oracle.attention(q, k, v, mask="causal", lib=lib)
+    qf, kf, vf = _f64(q), _f64(k), _f64(v)
+    _close(o[:, 0], vf[:, 0], what="causal row 0 O")
+    z00 = np.einsum("bhd,bhd->bh", qf[:, 0], kf[:, 0]) / 8.0
+    _close(lse[:, :, 0], z00, what="causal row 0 LSE")
+
+
+def pin_sdpa(lib):
+    """float64 SDPA agreement: vanilla, causal, every mask as a boolean
+    attn_mask built by broadcast index comparisons, ALiBi as an additive
+    mask, GQA with enable_gqa, a custom scale and a strided (BHSD) layout."""
+    B, S, H, D = 2, 70, 4, 64
+    q, k, v = (_rand((B, S, H, D), n) for n in ("q6", "k6", "v6"))
+    o, _ = oracle.attention(q, k, v, lib=lib)
+    _close(o, _sdpa(q, k, v), what="SDPA vanilla")
+    o, _ = oracle.attention(q, k, v, scale=0.05, lib=lib)
+    _close(o, _sdpa(q, k, v, scale=0.05), what="SDPA scale")
+    ii = np.arange(S)[:, None]
+    jj = np.arange(S)[None, :]
+    doc = np.array([[0, 13, 14, 50, S], [0, 40, S, S, S]], dtype=np.int32)
+    docid = np.stack([np.searchsorted(doc[b], np.arange(S), side="right") - 1 for b in range(B)])
+    masks = {
+        "causal": ({}, np.broadcast_to(jj <= ii, (B, 1, S, S))),
+        "window": ({"window": 11}, np.broadcast_to((jj <= ii) & (ii - jj < 11), (B, 1, S, S))),
+        "prefix": ({"prefix": 23}, np.broadcast_to((jj <= ii) | (jj < 23), (B, 1, S, S))),
+        "doc": ({"doc_offsets": doc},
+                (docid[:, None, :, None] == docid[:, None, None, :]) & (jj <= ii)[None, None]),
+    }
+    for name, (kw, m) in masks.items():
+        o, _ = oracle.attention(q, k, v, mask=name, lib=lib, **kw)
+        _close(o, _sdpa(q, k, v, mask=torch.from_numpy(np.ascontiguousarray(m))),
+               what=f"SDPA {name}")
+    slopes = np.array([2.0 ** (-8.0 * (h + 1) / H) for h in range(H)])
+    add = torch.from_numpy(-slopes[None, :, None, None] * np.abs(ii - jj)[None, None])
+    o, _ = oracle.attention(q, k, v, mod="alibi", lib=lib)
+    _close(o, _sdpa(q, k, v, mask=add), what="SDPA alibi")
+    Hk = 2
+    k2, v2 = _rand((B, S, Hk, D), "k7"), _rand((B, S, Hk, D), "v7")
+    o, _ = oracle.attention(q, k2, v2, lib=lib)
+    _close(o, _sdpa(q, k2, v2, enable_gqa=True), what="SDPA GQA")
+    o, _ = oracle.attention(q, k2, v2, mask="causal", lib=lib)
+    _close(o, _sdpa(q, k2, v2, mask=torch.from_numpy(np.ascontiguousarray(
+        np.broadcast_to(jj <= ii, (B, 1, S, S)))), enable_gqa=True), what="SDPA GQA causal")
+    # BHSD storage passed as a strided BSHD view
+    qh = np.ascontiguousarray(q.transpose(0, 2, 1, 3)).transpose(0, 2, 1, 3)
+    o, _ = oracle.attention(qh, k, v, lib=lib)
+    _close(o, _sdpa(q, k, v), what="SDPA strided")
+
+
+def pin_reductions(lib):
+    """Special cases that reduce to another variant."""
+    S, H = 90, 2
+    q, k, v = (_rand((1, S, H, 64), n) for n in ("q8", "k8", "v8"))
+    van = oracle.attention(q, k, v, lib=lib)
+    cau = oracle.attention(q, k, v, mask="causal", lib=lib)
+    pairs = [
+        (oracle.attention(q, k, v, mod="softcap", softcap=1e30, lib=lib), van, "softcap inf"),
+        (oracle.attention(q, k, v, mod="alibi", alibi_slopes=np.zeros(H), lib=lib), van,
+         "alibi 0"),
+        (oracle.attention(q, k, v, mask="window", window=S, lib=lib), cau, "window S"),
+        (oracle.attention(q, k, v, mask="prefix", prefix=0, lib=lib), cau, "prefix 0"),
+        (oracle.attention(q, k, v, mask="prefix", prefix=S, lib=lib), van, "prefix S"),
+        (oracle.attention(q, k, v, mask="doc", doc_offsets=np.array([[0, S]], np.int32),
+                          lib=lib), cau, "one document"),
+    ]
+    for (o1, l1), (o0, l0), what in pairs:
+        _close(o1, o0, atol=1e-12, what=what)
+        _close(l1, l0, atol=1e-9, what=what + " LSE")
+    # GQA equals MHA on repeat-interleaved K/V
+    k2, v2 = _rand((1, S, 1, 64), "k9"), _rand((1, S, 1, 64), "v9")
+    o1, _ = oracle.attention(q, k2, v2, mask="causal", lib=lib)
+    o0, _ = oracle.attention(q, np.repeat(k2, H, axis=2), np.repeat(v2, H, axis=2),
+                             mask="causal", lib=lib)
+    _close(o1, o0, atol=1e-12, what="GQA repeat")
+
+
+def pin_rows_api(lib):
+    """Sampled rows equal the same rows of the full result."""
+    S, H = 140, 4
+    q, k = _rand((2, S, H, 64), "qa"), _rand((2, S, 2, 64), "ka")
+    v = _rand((2, S, 2, 32), "va")
+    o, lse = oracle.attention(q, k, v, mask="window", window=50, mod="alibi", lib=lib)
+    rows = np.array([[0, 0, 0], [1, 3, 139], [0, 2, 77], [1, 1, 5]])
+    o2, l2 = oracle.attention(q, k, v, mask="window", window=50, mod="alibi", rows=rows, lib=lib)
+    for n, (b, h, i) in enumerate(rows):
+        _close(o2[n], o[b, i, h], atol=0, what="rows O")
+        _close(l2[n], lse[b, h, i], atol=0, what="rows LSE")
+
+
+def pin_diff(lib):
+    """Differential attention: constant scores give (1 - lam) mean(V); lam = 0
+    is vanilla with D_v = 128; identical streams give (1 - lam) vanilla."""
+    S, H = 60, 2
+    lam = 0.8
+    qz = _bf(np.zeros((2, 1, S, H, 64)))
+    k = _rand((2, 1, S, H, 64), "kd")
+    v = _rand((1, S, H, 128), "vd")
+    o, lse = oracle.diff_attention(qz, k, v, lam, lib=lib)
+    _close(o, (1 - lam) * _f64(v).mean(axis=1, keepdims=True), what="diff closed form")
+    _close(lse, math.log(S), what="diff LSE closed form")
+    q = _rand((2, 1, S, H, 64), "qd")
+    o, _ = oracle.diff_attention(q, k, v, 0.0, mask="causal", lib=lib)
+    o0, _ = oracle.attention(q[0], k[0], v, mask="causal", lib=lib)
+    _close(o, o0, atol=1e-12, what="diff lam 0")
+    qq = np.ascontiguousarray(np.stack([q[0], q[0]]))
+    kk = np.ascontiguousarray(np.stack([k[0], k[0]]))
+    o, _ = oracle.diff_attention(qq, kk, v, lam, lib=lib)
+    o0, _ = oracle.attention(q[0], k[0], v, lib=lib)
+    _close(o, (1 - lam) * o0, atol=1e-12, what="diff identical streams")
+
+
+def pin_evo(lib):
+    """Evoformer: constant scores and zero bias give sigmoid(g) * mean(V);
+    bias 0 with g = +50 is vanilla over the residue axis; the column pass is
+    the row pass on the MSA tensor with its first two axes swapped."""
+    Ns, Nr, H, c = 6, 40, 2, 32
+    qz = _bf(np.zeros((Ns, Nr, H, c)))
+    k, v, g = (_rand((Ns, Nr, H, c), n) for n in ("ke", "ve", "ge"))
+    bias0 = _bf(np.zeros((H, Nr, Nr)))
+    o, lse = oracle.evo_row(qz, k, v, bias0, g, lib=lib)
+    sig = 1.0 / (1.0 + np.exp(-_f64(g)))
+    _close(o, sig * _f64(v).mean(axis=1, keepdims=True), what="evo row closed form")
+    _close(lse, math.log(Nr), what="evo LSE")
+    q = _rand((Ns, Nr, H, c), "qe")
+    g50 = _bf(np.full((Ns, Nr, H, c), 50.0))
+    o, _ = oracle.evo_row(q, k, v, bias0, g50, lib=lib)
+    o0, _ = oracle.attention(q, k, v, lib=lib)
+    _close(o, o0, atol=1e-12, what="evo row = vanilla")
+    oc, lc = oracle.evo_col(q, k, v, g, lib=lib)
+    sw = lambda x: np.ascontiguousarray(np.swapaxes(x, 0, 1))
+    bias_t = _bf(np.zeros((H, Ns, Ns)))
+    orow, lrow = oracle.evo_row(sw(q), sw(k), sw(v), bias_t, sw(g), lib=lib)
+    _close(oc, orow, atol=1e-12, what="evo col = row on transposed")
+    _close(lc, lrow, atol=1e-12, what="evo col LSE")
+
+
+def pin_fully_masked_row(lib):
+    """A row with no allowed key (a document table whose first document starts
+    after row 0 cannot occur in the workloads, so use prefix on Sq > Sk via a
+    window of 0) returns O = 0 and LSE = -inf."""
+    S = 10
+    q, k, v = (_rand((1, S, 1, 64), n) for n in ("qm", "km", "vm"))
+    o, lse = oracle.attention(q, k, v, mask="window", window=0, lib=lib)
+    assert np.all(o == 0.0) and np.all(np.isneginf(lse)), "fully masked rows"
+
+
+ALL_PINS = [pin_constant_scores, pin_alibi_geometric, pin_softcap_two_keys, pin_one_hot,
+            pin_rows_sum_to_one, pin_shift_invariance, pin_permutation, pin_causal_row0,
+            pin_sdpa, pin_reductions, pin_rows_api, pin_diff, pin_evo, pin_fully_masked_row]

@@ -1,0 +1,55 @@
+"""Plant plausible mistakes in a copy of the oracle and check a pin fails.
+
+Each mutant edits one expression of ``oracle/fl_oracle.c`` in a temporary
+copy (the committed oracle is never changed), builds it, and runs every pin
+of ``tests/oracle_pins.py`` against it.  A mutant that passes every pin would
+mean the pins cannot tell that mistake from the definition.
+"""
+import os
+
+import pytest
+
+import oracle
+from tests import oracle_pins
+
+SRC = os.path.join(os.path.dirname(oracle.__file__), "fl_oracle.c")
+
+MUTANTS = {
+    "causal_strict": ("return j <= i;", "return j < i;"),
+    "window_off_by_one": ("i - j < p->window", "i - j <= p->window"),
+    "prefix_inclusive": ("j <= i || j < p->prefix", "j <= i || j <= p->prefix"),
+    "doc_start_exclusive": ("if (starts[t] <= x)", "if (starts[t] < x)"),
+    "doc_no_causal": ("return j <= i && doc_of", "return doc_of"),
+    "alibi_sign": ("x += -alibi_slope(p, h)", "x += alibi_slope(p, h)"),
+    "alibi_no_abs": ("fabs((double)(i - j))", "((double)(i - j))"),
+    "alibi_slope_index": ("-8.0 * (double)(h + 1)", "-8.0 * (double)(h)"),
+    "softcap_dropped_cap": ("x = p->softcap * tanh(x / p->softcap);", "x = tanh(x);"),
+    "gqa_modulo": ("const int32_t hk = h / group;", "const int32_t hk = h % p->Hk;"),
+    "lse_log2": ("*lse = m + log(l);", "*lse = m + log2(l);"),
+    "no_max_subtraction": ("l += exp(z[j] - m);", "l += exp(z[j]);"),
+    "scale_one_over_d": ("1.0 / sqrt((double)p->D)", "1.0 / (double)p->D"),
+    "bias_transposed": ("i * p->bias_stride[1] +\n                                    j * p->bias_stride[2]",
+                        "j * p->bias_stride[1] +\n                                    i * p->bias_stride[2]"),
+    "bias_dropped": ("x += widen_bf16(p->bias[", "x += 0.0 * widen_bf16(p->bias["),
+    "k_row_uses_q_stride": ("j * p->k_stride[1]", "j * p->q_stride[1]"),
+    "v_wrong_row": ("j * p->v_stride[1] + hk", "(p->Sk - 1 - j) * p->v_stride[1] + hk"),
+    "softmax_not_normalised": ("const double pj = exp(z[j] - m) / l;", "const double pj = exp(z[j] - m);"),
+}
+
+
+@pytest.mark.parametrize("name", sorted(MUTANTS))
+def test_mutant_is_caught(name, tmp_path):
+    old, new = MUTANTS[name]
+    text = open(SRC).read()
+    assert text.count(old) == 1, f"mutation anchor for {name} not unique"
+    mutated = tmp_path / "mutant.c"
+    mutated.write_text(text.replace(old, new))
+    lib_path = oracle.build(force=True, source=str(mutated), target=str(tmp_path / "libm.so"))
+    lib = oracle.load(lib_path)
+    caught = []
+    for pin in oracle_pins.ALL_PINS:
+        try:
+            pin(lib)
+        except AssertionError:
+            caught.append(pin.__name__)
+    assert caught, f"no pin detects mutant {name}"
