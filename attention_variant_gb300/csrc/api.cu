@@ -1,0 +1,413 @@
+// api.cu -- the C ABI (include/fl_attn.h): argument validation, planning
+// (tile grid, work order, TMA descriptors) and dispatch to the kernels.
+//
+// Validation runs before any CUDA call, so a rejected request touches no
+// device state.  The library allocates no device memory: TMA descriptors are
+// passed to the kernel as __grid_constant__ parameters.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+
+#include "fl_attn.h"
+#include "launch.h"
+
+namespace {
+
+thread_local char g_last_error[512];
+
+fl_status fail(fl_status s, const char *fmt, ...)
+{
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(g_last_error, sizeof g_last_error, fmt, ap);
+    va_end(ap);
+    return s;
+}
+
+fl_status ok()
+{
+    g_last_error[0] = '\0';
+    return FL_OK;
+}
+
+// A validated, normalised copy of an fl_tensor (size-1 axes get the stride a
+// packed layout would give them, so arbitrary strides on them are accepted).
+struct View {
+    void *ptr;
+    int ndim;
+    int64_t size[5];
+    int64_t stride[5];
+};
+
+fl_status check_tensor(const fl_tensor *t, const char *name, int ndim, int dtype, View &v)
+{
+    if (!t)
+        return fail(FL_ERR_INVALID_ARG, "%s is NULL", name);
+    if (!t->ptr)
+        return fail(FL_ERR_INVALID_ARG, "%s->ptr is NULL", name);
+    if (t->ndim != ndim)
+        return fail(FL_ERR_INVALID_ARG, "%s must have %d dimensions, has %d", name, ndim, t->ndim);
+    if (t->dtype != dtype)
+        return fail(FL_ERR_INVALID_ARG, "%s must be %s", name, dtype == FL_BF16 ? "bf16" : "fp32");
+    v.ptr = t->ptr;
+    v.ndim = ndim;
+    for (int d = 0; d < ndim; ++d) {
+        if (t->sizes[d] < 1 || t->sizes[d] > (int64_t(1) << 31) - 1)
+            return fail(FL_ERR_INVALID_ARG, "%s size[%d] = %lld out of range", name, d,
+                        (long long)t->sizes[d]);
+        v.size[d] = t->sizes[d];
+        v.stride[d] = t->strides[d];
+    }
+    int64_t packed = 1;
+    for (int d = ndim - 1; d >= 0; --d) {
+        if (v.size[d] == 1)
+            v.stride[d] = packed;
+        packed *= v.size[d];
+    }
+    if (v.stride[ndim - 1] != 1)
+        return fail(FL_ERR_INVALID_ARG, "%s innermost stride must be 1", name);
+    const int elt = dtype == FL_BF16 ? 2 : 4;
+    for (int d = 0; d < ndim - 1; ++d) {
+        if (v.stride[d] <= 0)
+            return fail(FL_ERR_INVALID_ARG, "%s stride[%d] must be positive", name, d);
+        if (dtype == FL_BF16 && (v.stride[d] * elt) % 16 != 0)
+            return fail(FL_ERR_ALIGNMENT, "%s stride[%d] = %lld elements is not a multiple of 16 bytes",
+                        name, d, (long long)v.stride[d]);
+        if (v.stride[d] * elt >= (int64_t(1) << 40))
+            return fail(FL_ERR_INVALID_ARG, "%s stride[%d] too large", name, d);
+    }
+    if (reinterpret_cast<uintptr_t>(v.ptr) % (dtype == FL_BF16 ? 16 : 4) != 0)
+        return fail(FL_ERR_ALIGNMENT, "%s->ptr is not %d-byte aligned", name,
+                    dtype == FL_BF16 ? 16 : 4);
+    return FL_OK;
+}
+
+bool same(const View &v, std::initializer_list<int64_t> sizes)
+{
+    int d = 0;
+    for (int64_t s : sizes)
+        if (v.size[d++] != s)
+            return false;
+    return true;
+}
+
+// ------------------------------------------------------------------ device state
+
+struct DeviceInfo {
+    bool ready;
+    bool supported;
+    int sm_count;
+};
+
+std::mutex g_dev_mutex;
+DeviceInfo g_dev[64];
+
+fl_status device_info(int &dev, DeviceInfo &info)
+{
+    int n = 0;
+    if (cudaGetDeviceCount(&n) != cudaSuccess || n == 0) {
+        cudaGetLastError();
+        return fail(FL_ERR_NO_DEVICE, "no CUDA device");
+    }
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) {
+        cudaGetLastError();
+        return fail(FL_ERR_NO_DEVICE, "cannot query the current device");
+    }
+    std::lock_guard<std::mutex> lock(g_dev_mutex);
+    DeviceInfo &d = g_dev[dev];
+    if (!d.ready) {
+        int major = 0, minor = 0, sms = 0;
+        if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+            cudaGetLastError();
+            return fail(FL_ERR_CUDA, "cudaDeviceGetAttribute failed");
+        }
+        d.supported = (major == 10 && minor == 3);
+        d.sm_count = sms;
+        d.ready = true;
+    }
+    info = d;
+    if (!info.supported)
+        return fail(FL_ERR_NO_DEVICE, "this library is built for sm_103 (GB300) only");
+    return FL_OK;
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn()
+{
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *f = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault,
+                                             &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+        cudaGetLastError();
+    });
+    return fn;
+}
+
+// A bf16 tensor map over dims (innermost first) with byte strides of dims 1..rank-1.
+fl_status make_map(CUtensorMap &map, void *ptr, int rank, const uint64_t *dims,
+                   const uint64_t *strides_bytes, const uint32_t *box, CUtensorMapSwizzle swz,
+                   const char *what)
+{
+    auto fn = encode_fn();
+    if (!fn)
+        return fail(FL_ERR_CUDA, "cuTensorMapEncodeTiled is unavailable");
+    cuuint64_t gd[5];
+    cuuint64_t gs[4];
+    cuuint32_t bx[5], es[5];
+    for (int d = 0; d < rank; ++d) {
+        gd[d] = dims[d];
+        bx[d] = box[d];
+        es[d] = 1;
+    }
+    for (int d = 0; d < rank - 1; ++d)
+        gs[d] = strides_bytes[d];
+    CUresult r = fn(&map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, rank, ptr, gd, gs, bx, es,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS)
+        return fail(FL_ERR_CUDA, "cuTensorMapEncodeTiled(%s) failed with %d", what, (int)r);
+    return FL_OK;
+}
+
+uint64_t timeout_ns(const fl_attn_variant_desc *d)
+{
+    const uint64_t us = d->wait_timeout_us ? d->wait_timeout_us : 2000000u;
+    return us * 1000ull;
+}
+
+fl_status check_mask(const fl_attn_variant_desc *d)
+{
+    switch (d->mask) {
+    case FL_MASK_NONE:
+    case FL_MASK_CAUSAL:
+        return FL_OK;
+    case FL_MASK_WINDOW:
+        if (d->window < 1)
+            return fail(FL_ERR_INVALID_ARG, "window must be >= 1");
+        return FL_OK;
+    case FL_MASK_PREFIX:
+        if (d->prefix < 0)
+            return fail(FL_ERR_INVALID_ARG, "prefix must be >= 0");
+        return FL_OK;
+    case FL_MASK_DOC:
+        if (!d->doc_offsets || d->doc_stride < 2)
+            return fail(FL_ERR_INVALID_ARG, "doc mask needs doc_offsets and doc_stride >= 2");
+        if (reinterpret_cast<uintptr_t>(d->doc_offsets) % 4)
+            return fail(FL_ERR_ALIGNMENT, "doc_offsets is not 4-byte aligned");
+        return FL_OK;
+    default:
+        return fail(FL_ERR_INVALID_ARG, "unknown mask %d", d->mask);
+    }
+}
+
+// ------------------------------------------------------------------ standard
+
+fl_status fwd_standard(const fl_tensor *q, const fl_tensor *k, const fl_tensor *v,
+                       const fl_tensor *out, const fl_tensor *lse,
+                       const fl_attn_variant_desc *d, const fl_tensor *bias,
+                       const fl_tensor *gate, cudaStream_t stream)
+{
+    View Q, K, V, O, L{};
+    fl_status s;
+    if ((s = check_tensor(q, "q", 4, FL_BF16, Q)) != FL_OK) return s;
+    if ((s = check_tensor(k, "k", 4, FL_BF16, K)) != FL_OK) return s;
+    if ((s = check_tensor(v, "v", 4, FL_BF16, V)) != FL_OK) return s;
+    if ((s = check_tensor(out, "out", 4, FL_BF16, O)) != FL_OK) return s;
+    if (bias || gate)
+        return fail(FL_ERR_INVALID_ARG, "bias and gate are only taken by the Evoformer kinds");
+    const int64_t B = Q.size[0], S = Q.size[1], Hq = Q.size[2], D = Q.size[3];
+    const int64_t Hk = K.size[2], Dv = V.size[3];
+    if (!same(K, {B, S, Hk, D}))
+        return fail(FL_ERR_INVALID_ARG, "k must be [B, S, Hk, D] matching q");
+    if (!same(V, {B, S, Hk, Dv}))
+        return fail(FL_ERR_INVALID_ARG, "v must be [B, S, Hk, Dv] matching k");
+    if (!same(O, {B, S, Hq, Dv}))
+        return fail(FL_ERR_INVALID_ARG, "out must be [B, S, Hq, Dv]");
+    if (Hq % Hk != 0)
+        return fail(FL_ERR_INVALID_ARG, "Hq (%lld) must be a multiple of Hk (%lld)", (long long)Hq,
+                    (long long)Hk);
+    const int64_t G = Hq / Hk;
+    if (d->gqa_group != 0 && d->gqa_group != G)
+        return fail(FL_ERR_INVALID_ARG, "gqa_group %d does not match Hq / Hk = %lld", d->gqa_group,
+                    (long long)G);
+    if (lse) {
+        if ((s = check_tensor(lse, "lse", 3, FL_F32, L)) != FL_OK) return s;
+        if (!same(L, {B, Hq, S}))
+            return fail(FL_ERR_INVALID_ARG, "lse must be [B, Hq, S]");
+    }
+    if ((s = check_mask(d)) != FL_OK) return s;
+    if (d->score_mod < FL_MOD_NONE || d->score_mod > FL_MOD_SOFTCAP)
+        return fail(FL_ERR_INVALID_ARG, "unknown score_mod %d", d->score_mod);
+    if (d->score_mod == FL_MOD_SOFTCAP && !(d->softcap > 0.f && std::isfinite(d->softcap)))
+        return fail(FL_ERR_INVALID_ARG, "softcap must be positive and finite");
+    if (!std::isfinite(d->scale))
+        return fail(FL_ERR_INVALID_ARG, "scale must be finite");
+    if (d->mask == FL_MASK_DOC && d->doc_stride < 2)
+        return fail(FL_ERR_INVALID_ARG, "doc_stride must be >= 2");
+    if (D != 64 || Dv != 64)
+        return fail(FL_ERR_UNSUPPORTED, "standard kind supports D = Dv = 64 (got %lld, %lld)",
+                    (long long)D, (long long)Dv);
+
+    int dev;
+    DeviceInfo info;
+    if ((s = device_info(dev, info)) != FL_OK) return s;
+
+    CUtensorMap tq, tk, tv;
+    const uint32_t box[4] = {64, 128, 1, 1};
+    {
+        const uint64_t dims[4] = {uint64_t(D), uint64_t(S), uint64_t(Hq), uint64_t(B)};
+        const uint64_t st[3] = {uint64_t(Q.stride[1]) * 2, uint64_t(Q.stride[2]) * 2,
+                                uint64_t(Q.stride[0]) * 2};
+        if ((s = make_map(tq, Q.ptr, 4, dims, st, box, CU_TENSOR_MAP_SWIZZLE_128B, "q")) != FL_OK)
+            return s;
+    }
+    {
+        const uint64_t dims[4] = {uint64_t(D), uint64_t(S), uint64_t(Hk), uint64_t(B)};
+        const uint64_t st[3] = {uint64_t(K.stride[1]) * 2, uint64_t(K.stride[2]) * 2,
+                                uint64_t(K.stride[0]) * 2};
+        if ((s = make_map(tk, K.ptr, 4, dims, st, box, CU_TENSOR_MAP_SWIZZLE_128B, "k")) != FL_OK)
+            return s;
+    }
+    {
+        const uint64_t dims[4] = {uint64_t(Dv), uint64_t(S), uint64_t(Hk), uint64_t(B)};
+        const uint64_t st[3] = {uint64_t(V.stride[1]) * 2, uint64_t(V.stride[2]) * 2,
+                                uint64_t(V.stride[0]) * 2};
+        if ((s = make_map(tv, V.ptr, 4, dims, st, box, CU_TENSOR_MAP_SWIZZLE_128B, "v")) != FL_OK)
+            return s;
+    }
+
+    fl::StdParams p{};
+    const int nq = static_cast<int>((S + fl::BM - 1) / fl::BM);
+    p.grid.B = int(B);
+    p.grid.Hq = int(Hq);
+    p.grid.Hk = int(Hk);
+    p.grid.G = int(G);
+    p.grid.nq = nq;
+    p.grid.pair_heads = G >= 2 ? 1 : 0;
+    if (G >= 2) {
+        p.grid.R = nq;
+        p.grid.Hx = int(B * Hk * ((G + 1) / 2));
+    } else {
+        p.grid.R = (nq + 1) / 2;
+        p.grid.Hx = int(B * Hq);
+    }
+    p.grid.n_items = int64_t(p.grid.R) * p.grid.Hx;
+    p.grid.lpt = (d->mask == FL_MASK_CAUSAL || d->mask == FL_MASK_PREFIX || d->mask == FL_MASK_DOC);
+    p.grid.group = 8;
+    p.mask.kind = d->mask;
+    p.mask.S = int(S);
+    p.mask.window = d->window;
+    p.mask.prefix = d->prefix;
+    p.mask.doc = d->doc_offsets;
+    p.mask.doc_stride = d->doc_stride;
+    p.score_mod = d->score_mod;
+    const float scale = d->scale != 0.f ? d->scale : 1.0f / std::sqrt(float(D));
+    const float log2e = 1.4426950408889634f;
+    p.qk_log2 = scale * log2e;
+    if (d->score_mod == FL_MOD_SOFTCAP) {
+        p.softcap_in = 2.f * scale * log2e / d->softcap;
+        p.softcap_out = d->softcap * log2e;
+    }
+    p.alibi_slopes = d->alibi_slopes;
+    p.alibi_exp_coef = -8.0f / float(Hq);
+    p.out = static_cast<__nv_bfloat16 *>(O.ptr);
+    p.o_sb = O.stride[0];
+    p.o_ss = O.stride[1];
+    p.o_sh = O.stride[2];
+    if (lse) {
+        p.lse = static_cast<float *>(L.ptr);
+        p.l_sb = L.stride[0];
+        p.l_sh = L.stride[1];
+    }
+    p.tile_counts = d->debug_tile_counts;
+    p.err_user = d->error_word;
+    p.inject = d->debug_inject;
+    p.timeout_ns = timeout_ns(d);
+
+    const int grid = int(p.grid.n_items < info.sm_count ? p.grid.n_items : info.sm_count);
+    cudaError_t e = fl::launch_standard(tq, tk, tv, p, grid, stream);
+    if (e != cudaSuccess)
+        return fail(FL_ERR_CUDA, "kernel launch failed: %s", cudaGetErrorString(e));
+    return ok();
+}
+
+} // namespace
+
+extern "C" {
+
+fl_status fl_attn_fwd(const fl_tensor *q, const fl_tensor *k, const fl_tensor *v,
+                      const fl_tensor *out, const fl_tensor *lse,
+                      const fl_attn_variant_desc *desc, const fl_tensor *bias,
+                      const fl_tensor *gate, fl_stream_t stream)
+{
+    if (!desc)
+        return fail(FL_ERR_INVALID_ARG, "desc is NULL");
+    switch (desc->kind) {
+    case FL_KIND_STANDARD:
+        return fwd_standard(q, k, v, out, lse, desc, bias, gate, reinterpret_cast<cudaStream_t>(stream));
+    case FL_KIND_DIFF:
+    case FL_KIND_EVO_ROW:
+    case FL_KIND_EVO_COL:
+        return fail(FL_ERR_UNSUPPORTED, "kind %d is not built yet", desc->kind);
+    default:
+        return fail(FL_ERR_INVALID_ARG, "unknown kind %d", desc->kind);
+    }
+}
+
+fl_status fl_attn_tile_shape(const fl_attn_variant_desc *desc, int32_t head_dim, int32_t *block_m,
+                             int32_t *block_n)
+{
+    if (!desc || !block_m || !block_n)
+        return fail(FL_ERR_INVALID_ARG, "NULL argument");
+    switch (desc->kind) {
+    case FL_KIND_STANDARD:
+    case FL_KIND_DIFF:
+        if (head_dim != 64)
+            return fail(FL_ERR_UNSUPPORTED, "head_dim %d not supported for kind %d", head_dim,
+                        desc->kind);
+        break;
+    case FL_KIND_EVO_ROW:
+    case FL_KIND_EVO_COL:
+        if (head_dim != 32)
+            return fail(FL_ERR_UNSUPPORTED, "head_dim %d not supported for kind %d", head_dim,
+                        desc->kind);
+        break;
+    default:
+        return fail(FL_ERR_INVALID_ARG, "unknown kind %d", desc->kind);
+    }
+    *block_m = fl::BM;
+    *block_n = fl::BN;
+    return ok();
+}
+
+const char *fl_attn_status_string(fl_status s)
+{
+    switch (s) {
+    case FL_OK: return "FL_OK";
+    case FL_ERR_INVALID_ARG: return "FL_ERR_INVALID_ARG: invalid argument";
+    case FL_ERR_UNSUPPORTED: return "FL_ERR_UNSUPPORTED: outside the compiled kernel set";
+    case FL_ERR_ALIGNMENT: return "FL_ERR_ALIGNMENT: pointer or stride not 16-byte aligned";
+    case FL_ERR_CUDA: return "FL_ERR_CUDA: CUDA call failed";
+    case FL_ERR_DEVICE_TIMEOUT: return "FL_ERR_DEVICE_TIMEOUT: a device-side wait ran out";
+    case FL_ERR_NO_DEVICE: return "FL_ERR_NO_DEVICE: no sm_103 device";
+    default: return "unknown fl_status";
+    }
+}
+
+const char *fl_attn_last_error(void) { return g_last_error; }
+
+int32_t fl_attn_version(void) { return FL_ATTN_VERSION; }
+
+} // extern "C"

@@ -1,0 +1,500 @@
+// fwd_standard.cu -- fused attention forward for MHA / GQA, D = Dv = 64,
+// with the ALiBi and softcap score_mods and the causal, window, prefix and
+// document masks (sm_103a: TMA + mbarrier ring + tcgen05.mma into TMEM).
+//
+// What is computed is the single-pass online-softmax attention forward of the
+// Flashlight pages (gist.science summary, "Methodology" items 2-4; talk
+// notes, "Compiler design" 1-4): S = Q K^T per key tile, a running max m and
+// running sum l per query row, the sum and the output rescaled when the max
+// moves (e^(x-y) = e^x / e^y), O += P V, never writing S or P to memory.
+//
+// CTA organisation (persistent: one CTA per SM, 320 threads):
+//   warps 0-3  softmax warpgroup of slot 0 (one thread per query row)
+//   warps 4-7  softmax warpgroup of slot 1
+//   warp  8    TMA producer: Q tiles once per work item, K/V tiles through an
+//              NS-stage mbarrier ring
+//   warp  9    MMA issuer (one thread) and TMEM owner
+// Each work item is two 128-row query tiles ("slots") sharing every K/V tile.
+//
+// TMEM (512 columns x 128 lanes, lane = query row):
+//   S[t] fp32 at columns 128 t, O[t] fp32 at 256 + 64 t, P[t] bf16x2 at
+//   384 + 64 t, for slots t = 0, 1.
+//
+// Hand-off protocol for slot t and key tile j (all mbarriers):
+//   MMA: [wait p_full(t)] O[t] += P[t] V_{j-1}; S[t] = Q[t] K_j^T; commit s_full(t)
+//   softmax: wait s_full(t); S[t] -> registers; score_mod, mask, row max;
+//            lazily rescale O[t] and l; P = 2^(t - m) -> TMEM; arrive p_full(t)
+// s_full(t) for tile j is committed after the P V of tile j-1 was issued, so
+// when it fires O[t] already holds that product and P[t] may be overwritten.
+#include <cuda_bf16.h>
+#include <cstdint>
+
+#include "common.cuh"
+#include "launch.h"
+
+namespace fl {
+namespace {
+
+constexpr int kThreads = 320;
+constexpr int kStages = 4;
+constexpr uint32_t kTileBytes = BM * 64 * 2; // one 128 x 64 bf16 tile
+constexpr uint32_t kColS = 0, kColO = 256, kColP = 384;
+
+struct __align__(1024) StdSmem {
+    uint8_t q[2][kTileBytes];
+    uint8_t k[kStages][kTileBytes];
+    uint8_t v[kStages][kTileBytes];
+    uint64_t q_full, q_empty;
+    uint64_t kv_full[kStages], kv_empty[kStages];
+    uint64_t s_full[2], p_full[2], o_full[2];
+    uint64_t final_bar;
+    uint32_t tmem_base;
+    uint32_t abort_flag;
+};
+
+__device__ uint32_t g_lib_error_word;
+
+struct KernelCtx {
+    StdSmem *sm;
+    uint32_t tmem;
+    WaitCtl wc;
+};
+
+__device__ __forceinline__ uint32_t bar(const uint64_t &b) { return ptx::smem_u32(&b); }
+
+// ------------------------------------------------------------------ producer
+__device__ void producer_role(const KernelCtx &cx, const StdParams &p, const CUtensorMap *tm_q,
+                              const CUtensorMap *tm_k, const CUtensorMap *tm_v)
+{
+    StdSmem &sm = *cx.sm;
+    const uint32_t lane = ptx::lane_id();
+    uint32_t kv_count = 0, item_count = 0;
+    int64_t dropped = -1;
+    bool ok = true;
+    for (int64_t L = blockIdx.x; L < p.grid.n_items && ok; L += gridDim.x) {
+        const Item it = decode_item(p.grid, L);
+        int lo = 1 << 30, hi = 0;
+        int nvalid = 0;
+#pragma unroll
+        for (int t = 0; t < 2; ++t) {
+            if (!it.valid[t])
+                continue;
+            const TileRange r = q_block_range(p.mask, it.b, it.qb[t] * BM);
+            lo = min(lo, r.lo);
+            hi = max(hi, r.hi);
+            ++nvalid;
+        }
+        if (item_count > 0) {
+            ok = warp_wait(bar(sm.q_empty), (item_count - 1) & 1, cx.wc, W_Q_EMPTY);
+            if (!ok)
+                break;
+        }
+        if (lane == 0) {
+            ptx::mbar_arrive_expect_tx(bar(sm.q_full), nvalid * kTileBytes);
+#pragma unroll
+            for (int t = 0; t < 2; ++t)
+                if (it.valid[t])
+                    ptx::tma_load_4d(ptx::smem_u32(sm.q[t]), tm_q, bar(sm.q_full), 0,
+                                     it.qb[t] * BM, it.h[t], it.b);
+        }
+        __syncwarp();
+        for (int j = lo; j < hi; ++j, ++kv_count) {
+            const uint32_t s = kv_count % kStages;
+            const uint32_t ph = (kv_count / kStages) & 1;
+            ok = warp_wait(bar(sm.kv_empty[s]), ph ^ 1, cx.wc, W_KV_EMPTY);
+            if (!ok)
+                break;
+            if (lane == 0) {
+                const bool drop = p.inject == 1 && blockIdx.x == 0 && kv_count == 0;
+                if (drop) {
+                    dropped = kv_count;
+                } else {
+                    ptx::mbar_arrive_expect_tx(bar(sm.kv_full[s]), 2 * kTileBytes);
+                    ptx::tma_load_4d(ptx::smem_u32(sm.k[s]), tm_k, bar(sm.kv_full[s]), 0, j * BN,
+                                     it.kvh, it.b);
+                    ptx::tma_load_4d(ptx::smem_u32(sm.v[s]), tm_v, bar(sm.kv_full[s]), 0, j * BN,
+                                     it.kvh, it.b);
+                }
+            }
+            __syncwarp();
+        }
+        ++item_count;
+    }
+    if (!ok) {
+        // Drain: wait (bounded, ignoring the abort) for this warp's own loads in
+        // flight so that no TMA write lands after the CTA has exited.
+        dropped = __shfl_sync(0xffffffffu, dropped, 0);
+        const uint32_t first = kv_count > kStages ? kv_count - kStages : 0;
+        for (uint32_t idx = first; idx < kv_count; ++idx) {
+            if (static_cast<int64_t>(idx) == dropped)
+                continue;
+            mbar_wait_drain(bar(sm.kv_full[idx % kStages]), (idx / kStages) & 1, cx.wc, W_DRAIN);
+        }
+        if (item_count > 0)
+            mbar_wait_drain(bar(sm.q_full), (item_count - 1) & 1, cx.wc, W_DRAIN);
+    }
+}
+
+// ------------------------------------------------------------------ MMA issuer
+__device__ void mma_role(const KernelCtx &cx, const StdParams &p)
+{
+    StdSmem &sm = *cx.sm;
+    const uint32_t lane = ptx::lane_id();
+    constexpr uint32_t idesc_qk = umma_idesc_bf16(BM, BN, false);
+    constexpr uint32_t idesc_pv = umma_idesc_bf16(BM, 64, true);
+    uint32_t kv_count = 0, item_count = 0;
+    uint32_t pcount[2] = {0, 0};
+    bool ok = true;
+    for (int64_t L = blockIdx.x; L < p.grid.n_items && ok; L += gridDim.x) {
+        const Item it = decode_item(p.grid, L);
+        int lo_t[2], hi_t[2];
+        int lo = 1 << 30, hi = 0;
+#pragma unroll
+        for (int t = 0; t < 2; ++t) {
+            lo_t[t] = hi_t[t] = 0;
+            if (!it.valid[t])
+                continue;
+            const TileRange r = q_block_range(p.mask, it.b, it.qb[t] * BM);
+            lo_t[t] = r.lo;
+            hi_t[t] = r.hi;
+            lo = min(lo, r.lo);
+            hi = max(hi, r.hi);
+        }
+        ok = warp_wait(bar(sm.q_full), item_count & 1, cx.wc, W_Q_FULL);
+        if (!ok)
+            break;
+        ptx::tc_fence_after();
+        uint32_t prev_stage = 0;
+        for (int j = lo; j <= hi && ok; ++j) {
+            const uint32_t stage = kv_count % kStages;
+            if (j < hi) {
+                ok = warp_wait(bar(sm.kv_full[stage]), (kv_count / kStages) & 1, cx.wc, W_KV_FULL);
+                if (!ok)
+                    break;
+                ptx::tc_fence_after();
+            }
+#pragma unroll
+            for (int t = 0; t < 2; ++t) {
+                if (!it.valid[t])
+                    continue;
+                if (j - 1 >= lo_t[t] && j - 1 < hi_t[t]) {
+                    ok = warp_wait(bar(sm.p_full[t]), pcount[t] & 1, cx.wc, W_P_FULL);
+                    if (!ok)
+                        break;
+                    ++pcount[t];
+                    ptx::tc_fence_after();
+                    if (lane == 0) {
+                        const uint32_t vbase = ptx::smem_u32(sm.v[prev_stage]);
+#pragma unroll
+                        for (int kk = 0; kk < BN / 16; ++kk)
+                            ptx::mma_ts(cx.tmem + kColO + 64 * t, cx.tmem + kColP + 64 * t + 8 * kk,
+                                        umma_desc(vbase + kk * 2048, kTileBytes, 1024, kSwizzle128B),
+                                        idesc_pv, (j - 1 > lo_t[t] || kk > 0) ? 1u : 0u);
+                        if (j == hi_t[t])
+                            ptx::mma_commit(bar(sm.o_full[t]));
+                    }
+                    __syncwarp();
+                }
+                if (j < hi && j >= lo_t[t] && j < hi_t[t]) {
+                    if (lane == 0) {
+                        const uint32_t qbase = ptx::smem_u32(sm.q[t]);
+                        const uint32_t kbase = ptx::smem_u32(sm.k[stage]);
+#pragma unroll
+                        for (int kk = 0; kk < 64 / 16; ++kk)
+                            ptx::mma_ss(cx.tmem + kColS + 128 * t,
+                                        umma_desc(qbase + kk * 32, 16, 1024, kSwizzle128B),
+                                        umma_desc(kbase + kk * 32, 16, 1024, kSwizzle128B),
+                                        idesc_qk, kk > 0 ? 1u : 0u);
+                        ptx::mma_commit(bar(sm.s_full[t]));
+                    }
+                    __syncwarp();
+                }
+            }
+            if (!ok)
+                break;
+            if (lane == 0) {
+                if (j > lo)
+                    ptx::mma_commit(bar(sm.kv_empty[prev_stage]));
+                if (j == hi - 1)
+                    ptx::mma_commit(bar(sm.q_empty));
+            }
+            __syncwarp();
+            if (j < hi) {
+                prev_stage = stage;
+                ++kv_count;
+            }
+        }
+        ++item_count;
+    }
+    // Every MMA this thread issued has completed before TMEM is released.
+    if (lane == 0)
+        ptx::mma_commit(bar(sm.final_bar));
+    __syncwarp();
+    mbar_wait_drain(bar(sm.final_bar), 0, cx.wc, W_FINAL);
+}
+
+// ------------------------------------------------------------------ softmax
+template <int MOD>
+__device__ void softmax_role(const KernelCtx &cx, const StdParams &p, int t)
+{
+    StdSmem &sm = *cx.sm;
+    const int r = threadIdx.x & 127;             // row of the query tile = TMEM lane
+    const uint32_t wq = (threadIdx.x >> 5) & 3;  // warp's quarter of the lanes
+    const uint32_t lane_off = (wq * 32u) << 16;
+    const uint32_t tS = cx.tmem + lane_off + kColS + 128 * t;
+    const uint32_t tO = cx.tmem + lane_off + kColO + 64 * t;
+    const uint32_t tP = cx.tmem + lane_off + kColP + 64 * t;
+    uint32_t scount = 0, ocount = 0;
+
+    for (int64_t L = blockIdx.x; L < p.grid.n_items; L += gridDim.x) {
+        const Item it = decode_item(p.grid, L);
+        if (!it.valid[t])
+            continue;
+        const int b = it.b, h = it.h[t], qb = it.qb[t];
+        const int i = qb * BM + r;
+        const TileRange tr = q_block_range(p.mask, b, qb * BM);
+        int row_lo, row_hi;
+        row_interval(p.mask, b, i, row_lo, row_hi);
+
+        float alibi_c = 0.f;
+        if constexpr (MOD == MOD_ALIBI) {
+            const float slope = p.alibi_slopes ? __ldg(p.alibi_slopes + h)
+                                               : exp2f(p.alibi_exp_coef * static_cast<float>(h + 1));
+            alibi_c = slope * kLog2e;
+        }
+
+        float m_ref = kNegInf, l = 0.f;
+        int ntiles = 0;
+        for (int j = tr.lo; j < tr.hi; ++j) {
+            if (!warp_wait(bar(sm.s_full[t]), scount & 1, cx.wc, W_S_FULL))
+                return;
+            ++scount;
+            ptx::tc_fence_after();
+
+            float x[BN];
+            {
+                uint32_t raw[BN];
+#pragma unroll
+                for (int c = 0; c < BN / 32; ++c)
+                    ptx::tmem_ld32(tS + 32 * c, raw + 32 * c);
+                ptx::tmem_wait_ld();
+                ptx::reg_fence<BN>(raw);
+#pragma unroll
+                for (int e = 0; e < BN; ++e)
+                    x[e] = __uint_as_float(raw[e]);
+            }
+            const int j0 = j * BN;
+            // logits in log2 units
+            if constexpr (MOD == MOD_NONE) {
+#pragma unroll
+                for (int e = 0; e < BN; ++e)
+                    x[e] *= p.qk_log2;
+            } else if constexpr (MOD == MOD_ALIBI) {
+                const float d0 = static_cast<float>(j0 - i);
+#pragma unroll
+                for (int e = 0; e < BN; ++e)
+                    x[e] = fmaf(x[e], p.qk_log2, -alibi_c * fabsf(d0 + static_cast<float>(e)));
+            } else {
+                // cap * tanh(u), tanh(u) = 1 - 2 / (1 + e^(2u)), in log2 units
+#pragma unroll
+                for (int e = 0; e < BN; ++e) {
+                    const float ex = ptx::ex2(x[e] * p.softcap_in);
+                    x[e] = p.softcap_out * (1.f - 2.f * ptx::rcp_approx(1.f + ex));
+                }
+            }
+            const bool full = (j0 >= tr.full_lo) && (j0 + BN <= tr.full_hi);
+            if (!full) {
+                const int a = row_lo - j0, z = row_hi - j0;
+#pragma unroll
+                for (int e = 0; e < BN; ++e)
+                    if (e < a || e >= z)
+                        x[e] = kNegInf;
+            }
+            float mx = x[0];
+#pragma unroll
+            for (int e = 1; e < BN; ++e)
+                mx = fmaxf(mx, x[e]);
+
+            if (j == tr.lo) {
+                m_ref = mx;
+            } else {
+                const bool need = mx > m_ref + 8.f;
+                if (__any_sync(0xffffffffu, need)) {
+                    const float m_new = fmaxf(m_ref, mx);
+                    const float alpha = (m_new == kNegInf) ? 1.f : ptx::ex2(m_ref - m_new);
+                    uint32_t o[32];
+#pragma unroll
+                    for (int c = 0; c < 2; ++c) {
+                        ptx::tmem_ld32(tO + 32 * c, o);
+                        ptx::tmem_wait_ld();
+                        ptx::reg_fence<32>(o);
+#pragma unroll
+                        for (int e = 0; e < 32; ++e)
+                            o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
+                        ptx::tmem_st32(tO + 32 * c, o);
+                    }
+                    ptx::tmem_wait_st();
+                    l *= alpha;
+                    m_ref = m_new;
+                }
+            }
+            const float mu = (m_ref == kNegInf) ? 0.f : m_ref;
+            float rs = 0.f;
+#pragma unroll
+            for (int c = 0; c < BN / 32; ++c) {
+                uint32_t pk[16];
+#pragma unroll
+                for (int e = 0; e < 16; ++e) {
+                    const float p0 = ptx::ex2(x[32 * c + 2 * e] - mu);
+                    const float p1 = ptx::ex2(x[32 * c + 2 * e + 1] - mu);
+                    rs += p0 + p1;
+                    pk[e] = ptx::pack_bf16(p0, p1);
+                }
+                ptx::tmem_st16(tP + 16 * c, pk);
+            }
+            l += rs;
+            ptx::tmem_wait_st();
+            ptx::tc_fence_before();
+            ptx::mbar_arrive(bar(sm.p_full[t]));
+            ++ntiles;
+        }
+
+        // epilogue: O / l -> bf16, LSE
+        if (!warp_wait(bar(sm.o_full[t]), ocount & 1, cx.wc, W_O_FULL))
+            return;
+        ++ocount;
+        ptx::tc_fence_after();
+        uint32_t o[64];
+        {
+            uint32_t lo32[32], hi32[32];
+            ptx::tmem_ld32(tO, lo32);
+            ptx::tmem_ld32(tO + 32, hi32);
+            ptx::tmem_wait_ld();
+            ptx::reg_fence<32>(lo32);
+            ptx::reg_fence<32>(hi32);
+#pragma unroll
+            for (int e = 0; e < 32; ++e) {
+                o[e] = lo32[e];
+                o[32 + e] = hi32[e];
+            }
+        }
+        const float inv = l > 0.f ? 1.f / l : 0.f;
+        if (i < p.mask.S) {
+            __nv_bfloat16 *dst = p.out + b * p.o_sb + static_cast<int64_t>(i) * p.o_ss + h * p.o_sh;
+            uint4 *d4 = reinterpret_cast<uint4 *>(dst);
+#pragma unroll
+            for (int c = 0; c < 8; ++c) {
+                uint4 w;
+                w.x = ptx::pack_bf16(__uint_as_float(o[8 * c + 0]) * inv, __uint_as_float(o[8 * c + 1]) * inv);
+                w.y = ptx::pack_bf16(__uint_as_float(o[8 * c + 2]) * inv, __uint_as_float(o[8 * c + 3]) * inv);
+                w.z = ptx::pack_bf16(__uint_as_float(o[8 * c + 4]) * inv, __uint_as_float(o[8 * c + 5]) * inv);
+                w.w = ptx::pack_bf16(__uint_as_float(o[8 * c + 6]) * inv, __uint_as_float(o[8 * c + 7]) * inv);
+                d4[c] = w;
+            }
+            if (p.lse)
+                p.lse[b * p.l_sb + h * p.l_sh + i] = l > 0.f ? (m_ref + log2f(l)) * kLn2 : kNegInf;
+        }
+        if (p.tile_counts && r == 0)
+            p.tile_counts[(static_cast<int64_t>(b) * p.grid.Hq + h) * p.grid.nq + qb] = ntiles;
+    }
+}
+
+template <int MOD>
+__global__ void __launch_bounds__(kThreads, 1)
+    std_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                   const __grid_constant__ CUtensorMap tm_v, const StdParams p)
+{
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t base = ptx::smem_u32(smem_raw);
+    StdSmem *sm = reinterpret_cast<StdSmem *>(smem_raw + ((1024u - (base & 1023u)) & 1023u));
+    const int warp = threadIdx.x >> 5;
+
+    if (threadIdx.x == 0) {
+        ptx::mbar_init(bar(sm->q_full), 1);
+        ptx::mbar_init(bar(sm->q_empty), 1);
+        for (int s = 0; s < kStages; ++s) {
+            ptx::mbar_init(bar(sm->kv_full[s]), 1);
+            ptx::mbar_init(bar(sm->kv_empty[s]), 1);
+        }
+        for (int t = 0; t < 2; ++t) {
+            ptx::mbar_init(bar(sm->s_full[t]), 1);
+            ptx::mbar_init(bar(sm->p_full[t]), 128);
+            ptx::mbar_init(bar(sm->o_full[t]), 1);
+        }
+        ptx::mbar_init(bar(sm->final_bar), 1);
+        sm->abort_flag = 0;
+        ptx::fence_mbarrier_init();
+        ptx::fence_proxy_async_smem();
+    }
+    if (warp == 8 && ptx::lane_id() == 0) {
+        ptx::prefetch_tensormap(&tm_q);
+        ptx::prefetch_tensormap(&tm_k);
+        ptx::prefetch_tensormap(&tm_v);
+    }
+    if (warp == 9) {
+        ptx::tmem_alloc(ptx::smem_u32(&sm->tmem_base), 512);
+        ptx::tmem_relinquish();
+    }
+    ptx::tc_fence_before();
+    __syncthreads();
+    ptx::tc_fence_after();
+
+    KernelCtx cx;
+    cx.sm = sm;
+    cx.tmem = sm->tmem_base;
+    cx.wc.abort_flag = &sm->abort_flag;
+    cx.wc.timeout_ns = p.timeout_ns;
+    cx.wc.err_user = p.err_user;
+    cx.wc.err_lib = &g_lib_error_word;
+
+    if (warp < 8)
+        softmax_role<MOD>(cx, p, warp >> 2);
+    else if (warp == 8)
+        producer_role(cx, p, &tm_q, &tm_k, &tm_v);
+    else
+        mma_role(cx, p);
+
+    ptx::tc_fence_before();
+    __syncthreads();
+    if (warp == 9) {
+        ptx::tc_fence_after();
+        ptx::tmem_dealloc(cx.tmem, 512);
+    }
+}
+
+template <int MOD>
+cudaError_t launch_mod(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
+                       const StdParams &p, int grid, cudaStream_t stream)
+{
+    const size_t smem = sizeof(StdSmem) + 1024;
+    static bool configured = false; // benign race: the attribute call is idempotent
+    if (!configured) {
+        cudaError_t e = cudaFuncSetAttribute(std_fwd_kernel<MOD>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             static_cast<int>(smem));
+        if (e != cudaSuccess)
+            return e;
+        configured = true;
+    }
+    std_fwd_kernel<MOD><<<grid, kThreads, smem, stream>>>(tq, tk, tv, p);
+    return cudaGetLastError();
+}
+
+} // namespace
+
+cudaError_t launch_standard(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
+                            const StdParams &p, int grid, cudaStream_t stream)
+{
+    switch (p.score_mod) {
+    case MOD_ALIBI:
+        return launch_mod<MOD_ALIBI>(tq, tk, tv, p, grid, stream);
+    case MOD_SOFTCAP:
+        return launch_mod<MOD_SOFTCAP>(tq, tk, tv, p, grid, stream);
+    default:
+        return launch_mod<MOD_NONE>(tq, tk, tv, p, grid, stream);
+    }
+}
+
+size_t standard_smem_bytes() { return sizeof(StdSmem) + 1024; }
+
+} // namespace fl

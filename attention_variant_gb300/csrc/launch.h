@@ -1,0 +1,39 @@
+// launch.h -- host-side interface between the C-ABI layer (api.cu) and the
+// kernel translation units.  Internal to the library; every file including it
+// is compiled by nvcc.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <cstdint>
+
+#include "common.cuh"
+
+namespace fl {
+
+// Parameters of the standard (MHA / GQA) kernel.  Strides are in elements.
+struct StdParams {
+    GridSpec grid;
+    MaskSpec mask;
+    int score_mod;
+    float qk_log2;        // scale * log2(e)
+    float softcap_in;     // 2 * scale * log2(e) / cap
+    float softcap_out;    // cap * log2(e)
+    const float *alibi_slopes;
+    float alibi_exp_coef; // default slopes: 2^(alibi_exp_coef * (h + 1)), coef = -8 / Hq
+    __nv_bfloat16 *out;
+    int64_t o_sb, o_ss, o_sh;
+    float *lse;
+    int64_t l_sb, l_sh;
+    int32_t *tile_counts; // [B][Hq][nq] or null
+    uint32_t *err_user;
+    int inject;
+    uint64_t timeout_ns;
+};
+
+cudaError_t launch_standard(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
+                            const StdParams &p, int grid, cudaStream_t stream);
+size_t standard_smem_bytes();
+
+}  // namespace fl

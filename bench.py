@@ -1,0 +1,456 @@
+#!/usr/bin/env python
+"""Fused attention forward throughput on GB300: TFLOP/s and fraction of peak.
+
+Headline workload: the MHA score_mod sweep at S = 2048 (B = 8, H = 16, D = 64,
+bf16 inputs drawn N(0,1) from the shared seeded generator), vanilla
+non-causal.  A step is one fused forward (O and LSE) over that batch, with the
+inputs already resident in HBM.  L2 is flushed (a 256 MiB write) before every
+timed step, and each step is timed with CUDA events on the launching stream.
+
+Flops are algorithmic: 4 * D per unmasked (query, key) pair.  The per-variant
+table ("variants") repeats the measurement for every variant and sequence
+length of the MHA sweep and the GQA mask sweep.
+
+--impl reference times the CPU oracle (the plain double-precision definition)
+on the host cores on a bounded sample of the same workload.
+
+For N > 1 (torchrun), every rank runs the same per-GPU workload on its own
+GPU with no collective on the data path (independent shards: weak scaling);
+value = all ranks' flops / the slowest rank's time.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import testdata  # noqa: E402
+from testdata import workloads  # noqa: E402
+
+HEADLINE = dict(S=2048, variant="vanilla")
+METRIC = "fused attention fwd TFLOP/s (bf16) and % of GB300 dense BF16 peak per variant"
+L2_FLUSH_BYTES = 256 << 20
+KERNEL_SOURCES = ["attention_variant_gb300/csrc/fwd_standard.cu",
+                  "attention_variant_gb300/csrc/common.cuh",
+                  "attention_variant_gb300/csrc/ptx.cuh"]
+
+
+# ---------------------------------------------------------------- workload accounting
+
+def row_intervals(mask, S, window=0, prefix=0, starts=None):
+    """Allowed keys [lo_i, hi_i) of every query row (the masks' definitions)."""
+    i = np.arange(S, dtype=np.int64)
+    if mask == "none":
+        return np.zeros(S, np.int64), np.full(S, S, np.int64)
+    if mask == "causal":
+        return np.zeros(S, np.int64), i + 1
+    if mask == "window":
+        return np.maximum(0, i - window + 1), i + 1
+    if mask == "prefix":
+        return np.zeros(S, np.int64), np.minimum(S, np.maximum(i + 1, prefix))
+    if mask == "doc":
+        st = np.asarray(starts)
+        st = st[st < S]
+        ds = st[np.searchsorted(st, i, side="right") - 1]
+        return ds, i + 1
+    raise ValueError(mask)
+
+
+def unmasked_pairs(mask, B, H, S, window=0, prefix=0, doc=None):
+    total = 0
+    for b in range(B):
+        lo, hi = row_intervals(mask, S, window, prefix, None if doc is None else doc[b])
+        total += int((hi - lo).sum()) * H
+    return total
+
+
+def entry(kind, S, variant):
+    """One benchmark entry of the MHA sweep ("mha") or GQA mask sweep ("gqa")."""
+    if kind == "mha":
+        w = workloads.mha_workload(S)
+        B, Hq, Hk = w["B"], w["H"], w["H"]
+    else:
+        B = dict(workloads.GQA_SHAPES)[S]
+        w = workloads.gqa_workload(S, B)
+        Hq, Hk = w["Hq"], w["Hk"]
+    D = workloads.HEAD_DIM
+    mod = {"vanilla": "none", "alibi": "alibi", "softcap": "softcap"}.get(variant, "none")
+    mask = variant if variant in ("causal", "window", "prefix", "doc") else "none"
+    kw = {}
+    doc = None
+    if mask == "window":
+        kw["window"] = workloads.WINDOW
+    elif mask == "prefix":
+        kw["prefix"] = workloads.PREFIX
+    elif mask == "doc":
+        doc = testdata.doc_offsets(S, B, w["name"], *workloads.DOC_LEN_RANGE)
+    pairs = unmasked_pairs(mask, B, Hq, S, kw.get("window", 0), kw.get("prefix", 0), doc)
+    return dict(name=w["name"], kind=kind, B=B, Hq=Hq, Hk=Hk, S=S, D=D, variant=variant,
+                mod=mod, mask=mask, kw=kw, doc=doc, pairs=pairs, flops=4 * D * pairs,
+                bytes=2 * B * S * D * (2 * Hq + 2 * Hk) + 4 * B * Hq * S)
+
+
+def all_entries():
+    out = [entry("mha", S, v) for S in workloads.MHA_SEQ_LENS for v in workloads.MHA_VARIANTS]
+    out += [entry("gqa", S, m) for S, _ in workloads.GQA_SHAPES for m in workloads.GQA_MASKS]
+    return out
+
+
+# ---------------------------------------------------------------- environment
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return dict(bf16_tflops=d["bf16_tflops"], bf16_tflops_sustained=d["bf16_tflops_sustained"],
+                    hbm_gbs=d["hbm_gbs"], source="measured")
+    return dict(bf16_tflops=1900.0, bf16_tflops_sustained=1700.0, hbm_gbs=6800.0,
+                source="fallback")
+
+
+def kernel_source_hash():
+    h = hashlib.sha256()
+    for rel in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, rel), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(workload):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken
+    on the current kernel source; else None."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(path):
+        return None
+    with open(path) as f:
+        d = json.load(f)
+    rec = d.get(workload)
+    if not rec or rec.get("source_hash") != kernel_source_hash():
+        return None
+    return rec.get("dram_bytes_per_launch")
+
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons during the timed region."""
+
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_rank{gpu_index}.csv")
+
+    def __enter__(self):
+        try:
+            os.makedirs(os.path.dirname(self.path), exist_ok=True)
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.QUERY}",
+                 "--format=csv,noheader,nounits", "-lms", "200"], stdout=self.f,
+                stderr=subprocess.DEVNULL)
+            time.sleep(0.5)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            self.f.close()
+
+    def summary(self):
+        if self.proc is None or not os.path.exists(self.path):
+            return None
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in open(self.path):
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx = float(f[2])
+            except ValueError:
+                continue
+            for n, flag in zip(names, f[5:9]):
+                if flag.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return None
+        busy = [x for x in sm if x >= 0.5 * (mx or 1)] or sm
+        return dict(sm_mhz=statistics.median(busy), sm_max_mhz=mx, reasons=sorted(reasons),
+                    samples=len(sm))
+
+
+# ---------------------------------------------------------------- GPU arm
+
+def gpu_inputs(e, torch, device):
+    q = testdata.normal_bf16((e["B"], e["S"], e["Hq"], e["D"]), e["name"], "q")
+    k = testdata.normal_bf16((e["B"], e["S"], e["Hk"], e["D"]), e["name"], "k")
+    v = testdata.normal_bf16((e["B"], e["S"], e["Hk"], e["D"]), e["name"], "v")
+    to = lambda b: torch.from_numpy(b.view(np.int16)).view(torch.bfloat16)
+    return [to(x) for x in (q, k, v)]
+
+
+def time_entry(e, host, torch, fa, device, steps, warmup, flush, stream):
+    q, k, v = (x.to(device) for x in host)
+    out = torch.empty((e["B"], e["S"], e["Hq"], e["D"]), dtype=torch.bfloat16, device=device)
+    lse = torch.empty((e["B"], e["Hq"], e["S"]), dtype=torch.float32, device=device)
+    doc_t = torch.from_numpy(e["doc"]).to(device) if e["doc"] is not None else None
+    desc = fa.make_desc(score_mod=e["mod"], mask=e["mask"], doc_offsets=doc_t,
+                        softcap=workloads.SOFTCAP, **e["kw"])
+    with torch.cuda.stream(stream):
+        for _ in range(warmup):
+            flush.zero_()
+            fa.fl_attn_fwd(q, k, v, out, lse, desc, stream=stream)
+        torch.cuda.synchronize()
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(steps)]
+        for s, t in evs:
+            flush.zero_()
+            s.record(stream)
+            fa.fl_attn_fwd(q, k, v, out, lse, desc, stream=stream)
+            t.record(stream)
+        torch.cuda.synchronize()
+    ms = [s.elapsed_time(t) for s, t in evs]
+    return ms, (q, k, v, out, lse, desc)
+
+
+def time_e2e(e, host, torch, fa, device, steps, warmup, stream):
+    """Same metric end to end: pinned host inputs -> device -> fused forward
+    -> O and LSE back to pinned host memory, every step."""
+    hq, hk, hv = (x.pin_memory() for x in host)
+    q, k, v = (torch.empty_like(x, device=device) for x in host)
+    out = torch.empty((e["B"], e["S"], e["Hq"], e["D"]), dtype=torch.bfloat16, device=device)
+    lse = torch.empty((e["B"], e["Hq"], e["S"]), dtype=torch.float32, device=device)
+    ho = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    hl = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
+    desc = fa.make_desc(score_mod=e["mod"], mask=e["mask"], softcap=workloads.SOFTCAP, **e["kw"])
+
+    def step():
+        q.copy_(hq, non_blocking=True)
+        k.copy_(hk, non_blocking=True)
+        v.copy_(hv, non_blocking=True)
+        fa.fl_attn_fwd(q, k, v, out, lse, desc, stream=stream)
+        ho.copy_(out, non_blocking=True)
+        hl.copy_(lse, non_blocking=True)
+
+    with torch.cuda.stream(stream):
+        for _ in range(warmup):
+            step()
+        torch.cuda.synchronize()
+        s, t = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        s.record(stream)
+        for _ in range(steps):
+            step()
+        t.record(stream)
+        torch.cuda.synchronize()
+    ms = s.elapsed_time(t) / steps
+    h2d = sum(x.numel() * x.element_size() for x in (hq, hk, hv))
+    d2h = ho.numel() * ho.element_size() + hl.numel() * hl.element_size()
+    return ms, h2d, d2h
+
+
+def cpu_baseline(e, seconds=12.0):
+    """The oracle as it stands, on a bounded sample of query rows of the
+    workload, on all host cores; returns TFLOP/s in the same algorithmic unit."""
+    import oracle
+    q, k, v = (testdata.normal_bf16((e["B"], e["S"], h, e["D"]), e["name"], n)
+               for n, h in (("q", e["Hq"]), ("k", e["Hk"]), ("v", e["Hk"])))
+    rng = np.random.default_rng(0)
+
+    def run(n):
+        rows = np.stack([rng.integers(0, e["B"], n), rng.integers(0, e["Hq"], n),
+                         rng.integers(0, e["S"], n)], axis=1)
+        t0 = time.perf_counter()
+        oracle.attention(q, k, v, mod=e["mod"], mask=e["mask"], softcap=workloads.SOFTCAP,
+                         rows=rows, **e["kw"])
+        dt = time.perf_counter() - t0
+        pairs = 0
+        for b, h, i in rows:
+            lo, hi = row_intervals(e["mask"], e["S"], e["kw"].get("window", 0),
+                                   e["kw"].get("prefix", 0))
+            pairs += int(hi[i] - lo[i])
+        return dt, 4 * e["D"] * pairs, n
+
+    dt, fl, n = run(256)
+    n2 = int(min(200000, max(256, 256 * seconds / max(dt, 1e-3))))
+    dt, fl, n = run(n2)
+    return dict(value=fl / dt / 1e12, unit="TFLOP/s", cores=oracle.max_threads(), kind="oracle",
+                sample=f"{n} random query rows (full key range each) of {e['name']} "
+                       f"{e['variant']}, {dt:.1f} s")
+
+
+def run_ours(args):
+    import torch
+    import attention_variant_gb300 as fa
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    fa.load_library()
+    stream = torch.cuda.Stream(device)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=device)
+
+    head = entry("mha", HEADLINE["S"], HEADLINE["variant"])
+    host = gpu_inputs(head, torch, device)
+
+    def barrier():
+        if world > 1:
+            torch.distributed.barrier()
+        torch.cuda.synchronize()
+
+    # headline, timed under the clock sampler
+    barrier()
+    with ClockSampler(local) as clk:
+        t0 = time.perf_counter()
+        ms, _ = time_entry(head, host, torch, fa, device, args.steps, args.warmup, flush, stream)
+        barrier()
+        wall = time.perf_counter() - t0
+    clocks = clk.summary()
+    step_ms = statistics.mean(ms)
+    if world > 1:
+        t = torch.tensor([step_ms], device=device)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        step_ms = float(t.item())
+    value = head["flops"] * world / (step_ms * 1e-3) / 1e12
+    peaks = measured_peaks()
+    achieved = head["flops"] / (statistics.mean(ms) * 1e-3) / 1e12
+
+    e2e_ms, h2d, d2h = time_e2e(head, host, torch, fa, device, max(3, args.steps // 4),
+                                args.warmup, stream)
+    e2e = dict(value=head["flops"] * world / (e2e_ms * 1e-3) / 1e12, unit="TFLOP/s",
+               h2d_bytes_per_step=h2d, d2h_bytes_per_step=d2h)
+
+    variants = {}
+    if not args.headline_only:
+        for e in all_entries():
+            h = gpu_inputs(e, torch, device) if (e["S"], e["kind"]) != (head["S"], "mha") else host
+            vms, _ = time_entry(e, h, torch, fa, device, args.variant_steps, 2, flush, stream)
+            vm = statistics.mean(vms)
+            tf = e["flops"] / (vm * 1e-3) / 1e12
+            variants[f"{e['name']}/{e['variant']}"] = dict(
+                tflops=round(tf, 1), frac_peak=round(tf / peaks["bf16_tflops"], 4),
+                ms=round(vm, 4), gbs=round(e["bytes"] / (vm * 1e-3) / 1e9, 1))
+
+    if rank != 0:
+        return
+    line = {
+        "metric": METRIC,
+        "value": round(value, 2),
+        "unit": "TFLOP/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(step_ms, 4),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic (seeded N(0,1) bf16)",
+        "config": {"workload": head["name"] + "/vanilla", "B": head["B"], "H": head["Hq"],
+                   "S": head["S"], "D": head["D"], "variant": "vanilla non-causal",
+                   "l2": "flushed before every timed step (256 MiB write)",
+                   "parallelism": f"independent replicas x{world}"},
+        "roofline": {"bound": "tensor", "achieved": round(achieved, 1),
+                     "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+                     "frac": round(achieved / peaks["bf16_tflops"], 4),
+                     "traffic": recorded_traffic(head["name"] + "/vanilla"),
+                     "peak_source": peaks["source"] + " bf16 burst"},
+        "e2e": e2e,
+        "gpu_launches": args.steps,
+        "clocks": clocks,
+        "wall_s_timed_region": round(wall, 3),
+        "variants": variants,
+    }
+    if not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(head, seconds=args.cpu_seconds)
+    print(json.dumps(line), flush=True)
+
+
+# ---------------------------------------------------------------- reference arm
+
+def run_reference(args):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    import oracle
+    head = entry("mha", HEADLINE["S"], HEADLINE["variant"])
+    q, k, v = (testdata.normal_bf16((head["B"], head["S"], h, head["D"]), head["name"], n)
+               for n, h in (("q", head["Hq"]), ("k", head["Hk"]), ("v", head["Hk"])))
+    rng = np.random.default_rng(1)
+    rows_per_step = 512
+
+    def step():
+        rows = np.stack([rng.integers(0, head["B"], rows_per_step),
+                         rng.integers(0, head["Hq"], rows_per_step),
+                         rng.integers(0, head["S"], rows_per_step)], axis=1)
+        oracle.attention(q, k, v, rows=rows)
+
+    for _ in range(args.warmup):
+        step()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        step()
+    dt = (time.perf_counter() - t0) / args.steps
+    flops = 4 * head["D"] * head["S"] * rows_per_step
+    value = flops / dt / 1e12
+    print(json.dumps({
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": dt * 1e3, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded N(0,1) bf16)",
+        "config": {"workload": head["name"] + "/vanilla", "B": head["B"], "H": head["Hq"],
+                   "S": head["S"], "D": head["D"], "variant": "vanilla non-causal"},
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": oracle.max_threads(),
+                         "kind": "oracle",
+                         "sample": f"{rows_per_step} random query rows per step"},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--variant-steps", type=int, default=5)
+    ap.add_argument("--headline-only", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

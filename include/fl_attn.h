@@ -1,0 +1,175 @@
+/*
+ * fl_attn.h -- C ABI of the GB300 fused attention-variant forward.
+ *
+ * One call computes, for every (batch, query head, query row i),
+ *
+ *     O_i   = sum_j softmax_j( z_ij ) v_j
+ *     LSE_i = ln sum_j exp( z_ij )
+ *     z_ij  = score_mod( scale * q_i . k_j ) + bias_ij    (or -inf where masked)
+ *
+ * in a single pass over the keys with an online softmax: a running maximum and
+ * a running sum per query row, the sum (and the output accumulator) rescaled
+ * whenever the maximum moves, so that no S x S score or probability tensor is
+ * ever written to device memory.  This is the fused kernel shape the
+ * Flashlight pages describe (gist.science summary, "Methodology" items 2-4:
+ * dimension demotion fuses max() into QK^T, the homomorphism
+ * e^(x-y) = e^x / e^y turns the two-pass stable softmax into a one-pass
+ * online one, and tiling-aware dimension elimination fuses softmax(QK^T)V;
+ * talk notes, "Compiler design" 1-4).  The variants are the ones the talk
+ * notes evaluate ("Evaluation: FlexAttention-supported variants" and
+ * "Evaluation: complex variants"): vanilla, ALiBi, softcap, causal, sliding
+ * window, PrefixLM, document mask, MHA and GQA, differential attention, and
+ * the AlphaFold Evoformer row- and column-wise gated self-attention with pair
+ * bias.  The pages give no formula for these; the ones used are stated at
+ * each enum below.
+ *
+ * Conventions shared by every entry point
+ *  - Every tensor is a caller-owned DEVICE buffer of the current CUDA device
+ *    (e.g. a torch tensor).  The library never allocates, frees or retains
+ *    caller memory.
+ *  - Calls are asynchronous on `stream` (a cudaStream_t; NULL is the legacy
+ *    default stream).  A returned FL_OK means the work was enqueued.
+ *  - Functions never throw.  Argument validation happens before any CUDA
+ *    call; a failed validation launches nothing and leaves outputs
+ *    untouched.  fl_attn_last_error() then describes the failure.
+ *  - The library is thread-safe for concurrent calls on different streams.
+ */
+#ifndef FL_ATTN_H
+#define FL_ATTN_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define FL_ATTN_VERSION 1
+
+typedef struct CUstream_st *fl_stream_t; /* identical to cudaStream_t */
+
+typedef enum {
+    FL_OK = 0,
+    FL_ERR_INVALID_ARG = 1,    /* null pointer, bad rank/shape/dtype, bad parameter */
+    FL_ERR_UNSUPPORTED = 2,    /* valid request outside the compiled kernel set */
+    FL_ERR_ALIGNMENT = 3,      /* base pointer or stride not 16-byte aligned */
+    FL_ERR_CUDA = 4,           /* a CUDA runtime/driver call failed */
+    FL_ERR_DEVICE_TIMEOUT = 5, /* reported through error_word: a device wait ran out */
+    FL_ERR_NO_DEVICE = 6       /* no CUDA device, or not an sm_103 (GB300) device */
+} fl_status;
+
+typedef enum { FL_BF16 = 0, FL_F32 = 1 } fl_dtype;
+
+/* A strided view.  sizes/strides are in ELEMENTS, outermost first; the
+ * innermost stride must be 1.  All other strides of bf16 tensors must be
+ * multiples of 8 elements (16 bytes) and every ptr 16-byte aligned. */
+typedef struct {
+    void *ptr;
+    int32_t dtype; /* fl_dtype */
+    int32_t ndim;
+    int64_t sizes[5];
+    int64_t strides[5];
+} fl_tensor;
+
+typedef enum {
+    FL_KIND_STANDARD = 0, /* MHA / GQA with score_mod and mask */
+    FL_KIND_DIFF = 1,     /* differential attention, two softmax streams, one V */
+    FL_KIND_EVO_ROW = 2,  /* Evoformer MSA row-wise gated attention + pair bias */
+    FL_KIND_EVO_COL = 3   /* Evoformer MSA column-wise gated attention */
+} fl_kind;
+
+typedef enum {
+    FL_MOD_NONE = 0,
+    FL_MOD_ALIBI = 1,  /* z += -slope_h * |i - j|, slope_h = 2^(-8 (h+1) / Hq) by default */
+    FL_MOD_SOFTCAP = 2 /* z = cap * tanh(z / cap) */
+} fl_score_mod;
+
+typedef enum {
+    FL_MASK_NONE = 0,
+    FL_MASK_CAUSAL = 1, /* key j allowed for query i iff j <= i */
+    FL_MASK_WINDOW = 2, /* j <= i and i - j < window */
+    FL_MASK_PREFIX = 3, /* j <= i or j < prefix (bidirectional over the first prefix keys) */
+    FL_MASK_DOC = 4     /* same document and j <= i */
+} fl_mask;
+
+/* Test-only fault injection: the library itself never sets these. */
+typedef enum {
+    FL_INJECT_NONE = 0,
+    FL_INJECT_DROP_KV_LOAD = 1 /* one K/V tile load of CTA 0 is never issued, so the
+                                  consumer's bounded wait runs out */
+} fl_inject;
+
+/* Bits the kernel ORs into error_word. */
+#define FL_DEVERR_TIMEOUT 0x1u        /* a bounded wait ran out; the CTA quit cleanly */
+#define FL_DEVERR_WHERE_SHIFT 8       /* bits 8..15: which wait (diagnostic) */
+
+typedef struct {
+    int32_t kind;            /* fl_kind */
+    int32_t score_mod;       /* fl_score_mod (FL_KIND_STANDARD only) */
+    float softcap;           /* cap > 0 for FL_MOD_SOFTCAP */
+    int32_t mask;            /* fl_mask (STANDARD and DIFF; DIFF takes NONE or CAUSAL) */
+    int32_t window;          /* FL_MASK_WINDOW, >= 1 */
+    int32_t prefix;          /* FL_MASK_PREFIX, >= 0 */
+    const int32_t *doc_offsets; /* FL_MASK_DOC: device int32 [B][doc_stride]; row b holds the
+                                   ascending document starts of batch b (first 0), padded
+                                   with S */
+    int32_t doc_stride;      /* entries per row of doc_offsets (max documents + 1) */
+    int32_t gqa_group;       /* Hq / Hk; 0 derives it from the shapes, else must match */
+    float diff_lambda;       /* FL_KIND_DIFF: O = O_1 - lambda O_2 */
+    float scale;             /* 0 means 1 / sqrt(D) */
+    const float *alibi_slopes; /* device float [Hq], or NULL for 2^(-8 (h+1) / Hq) */
+    int32_t *debug_tile_counts; /* NULL, or device int32 [batch][heads][ceil(S/128)]: the
+                                   number of 128-key tiles each 128-row query block visited */
+    uint32_t *error_word;    /* NULL, or a device word the kernel ORs FL_DEVERR_* into */
+    int32_t debug_inject;    /* fl_inject; 0 in normal use */
+    uint32_t wait_timeout_us; /* bound of every device-side wait; 0 means 2,000,000 */
+} fl_attn_variant_desc;
+
+/*
+ * fl_attn_fwd -- fused attention forward.
+ *
+ * Layouts (sizes in this logical order; any strides subject to the fl_tensor
+ * rules), all bf16 except lse (fp32):
+ *   FL_KIND_STANDARD  q [B,S,Hq,D]  k [B,S,Hk,D]  v [B,S,Hk,Dv]  out [B,S,Hq,Dv]
+ *                     lse [B,Hq,S] or NULL.        bias, gate: NULL.
+ *   FL_KIND_DIFF      q [2,B,S,H,D] k [2,B,S,Hk,D] v [B,S,Hk,Dv] out [B,S,H,Dv]
+ *                     lse [2,B,H,S] or NULL (one LSE per softmax stream).
+ *                     out = softmax(scale Q1 K1^T) V - lambda softmax(scale Q2 K2^T) V.
+ *   FL_KIND_EVO_ROW   q,k,v,gate,out [N_seq,N_res,H,c]; bias [H,N_res,N_res];
+ *                     attention over residues for each MSA row:
+ *                     out = sigmoid(gate) * softmax(scale q k^T + bias) v;
+ *                     lse [N_seq,H,N_res] or NULL.
+ *   FL_KIND_EVO_COL   q,k,v,gate,out [N_seq,N_res,H,c]; bias NULL;
+ *                     attention over MSA rows for each residue (axis 0);
+ *                     lse [N_res,H,N_seq] or NULL.
+ * lse is natural-log; its innermost stride must be 1.
+ *
+ * Supported shapes: STANDARD D = Dv = 64; DIFF D = 64, Dv = 128;
+ * EVO c = 32.  Other head dimensions return FL_ERR_UNSUPPORTED.
+ *
+ * Returns FL_OK when enqueued.  Device-side failures (a wait that ran out)
+ * are reported asynchronously through desc->error_word.
+ */
+fl_status fl_attn_fwd(const fl_tensor *q, const fl_tensor *k, const fl_tensor *v,
+                      const fl_tensor *out, const fl_tensor *lse,
+                      const fl_attn_variant_desc *desc, const fl_tensor *bias,
+                      const fl_tensor *gate, fl_stream_t stream);
+
+/* Query-block and key-tile sizes the kernel for `desc` uses (for the
+ * visited-tile accounting).  Never touches the device. */
+fl_status fl_attn_tile_shape(const fl_attn_variant_desc *desc, int32_t head_dim,
+                             int32_t *block_m, int32_t *block_n);
+
+/* Static text for a status code. */
+const char *fl_attn_status_string(fl_status status);
+
+/* Detail of the last failure on the calling thread ("" if none). */
+const char *fl_attn_last_error(void);
+
+/* FL_ATTN_VERSION of the loaded library. */
+int32_t fl_attn_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FL_ATTN_H */

@@ -1,0 +1,170 @@
+"""GPU parity of the standard (MHA / GQA) kernel against the CPU oracle.
+
+Every case runs the CUDA library through its C ABI on seeded bf16 inputs and
+compares element by element with the float64 oracle: O max |err| <= 1e-2 and
+mean |err| <= 1e-3, LSE max |err| <= 1e-3, visited-tile counts bit-exact.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import testdata
+from testdata import workloads
+from tests import gpu_util as gu
+from tests.golden import make_golden
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from attention_variant_gb300 import build
+    build.build()
+
+
+def _inputs(tag, B, S, Hq, Hk=None, D=64, Dv=64):
+    Hk = Hk or Hq
+    q = testdata.normal_bf16((B, S, Hq, D), tag, "q")
+    k = testdata.normal_bf16((B, S, Hk, D), tag, "k")
+    v = testdata.normal_bf16((B, S, Hk, Dv), tag, "v")
+    return q, k, v
+
+
+def _doc_table(B, S, tag):
+    return testdata.doc_offsets(S, B, tag, lo=37, hi=300)
+
+
+MASK_ARGS = {
+    "none": {},
+    "causal": {},
+    "window": {"window": 200},
+    "prefix": {"prefix": 300},
+    "doc": {},
+}
+
+
+def _check(q, k, v, mod, mask, tag, **extra):
+    B, S, Hq, _ = q.shape
+    kw = dict(MASK_ARGS[mask])
+    if mask == "doc":
+        kw["doc_offsets"] = _doc_table(B, S, tag)
+    o, lse, cnt, err = gu.run_standard(q, k, v, score_mod=mod, mask=mask, softcap=20.0,
+                                       **dict(kw), **extra)
+    assert err == 0
+    oref, lref = oracle.attention(q, k, v, mod=mod, mask=mask, softcap=20.0, **kw)
+    gu.compare(o, lse, oref, lref, what=f"{tag} {mod}/{mask}")
+    exp = gu.expected_tile_counts(mask, B, Hq, S, kw.get("window", 0), kw.get("prefix", 0),
+                                  kw.get("doc_offsets"))
+    assert np.array_equal(cnt, exp), f"{tag}: tile counts differ"
+
+
+def test_small_vanilla_and_golden():
+    q, k, v = make_golden.small_vanilla_inputs()
+    o, lse, cnt, err = gu.run_standard(q, k, v)
+    oref, lref = oracle.attention(q, k, v)
+    gu.compare(o, lse, oref, lref, what="small vanilla")
+    from tests.test_golden import load_rows
+    rows, glse, gout = load_rows()
+    for n, (b, h, i) in enumerate(rows):
+        assert np.abs(o[b, i, h] - gout[n]).max() <= gu.O_MAX
+        assert abs(lse[b, h, i] - glse[n]) <= gu.LSE_MAX
+    assert np.all(cnt == 2)
+
+
+@pytest.mark.parametrize("S", [640, 333])
+@pytest.mark.parametrize("mask", ["none", "causal", "window", "prefix", "doc"])
+@pytest.mark.parametrize("mod", ["none", "alibi", "softcap"])
+def test_mha_variants(mod, mask, S):
+    q, k, v = _inputs(f"mha{S}", 2, S, 4)
+    _check(q, k, v, mod, mask, f"mha{S}")
+
+
+@pytest.mark.parametrize("Hq,Hk", [(8, 2), (6, 2), (3, 1)])
+@pytest.mark.parametrize("mask", ["none", "causal", "window", "doc"])
+def test_gqa(Hq, Hk, mask):
+    q, k, v = _inputs(f"gqa{Hq}_{Hk}", 2, 300, Hq, Hk)
+    _check(q, k, v, "none", mask, f"gqa{Hq}_{Hk}")
+
+
+@pytest.mark.parametrize("S", [1, 127, 128, 129, 257])
+def test_edge_lengths(S):
+    q, k, v = _inputs(f"edge{S}", 1, S, 2)
+    for mask in ("none", "causal"):
+        _check(q, k, v, "alibi", mask, f"edge{S}")
+
+
+def test_strided_layout_and_no_lse():
+    q, k, v = _inputs("strided", 2, 384, 4)
+    o, lse, _, err = gu.run_standard(q, k, v, layout="bhsd", lse=False, counts=False,
+                                     mask="causal")
+    oref, _ = oracle.attention(q, k, v, mask="causal")
+    gu.compare(o, None, oref, None, what="bhsd")
+
+
+def test_custom_scale_and_slopes():
+    q, k, v = _inputs("scale", 1, 256, 4)
+    slopes = np.array([0.5, 0.25, 0.0, 1.0], dtype=np.float32)
+    o, lse, _, _ = gu.run_standard(q, k, v, scale=0.07, score_mod="alibi",
+                                   alibi_slopes=torch.from_numpy(slopes).cuda())
+    oref, lref = oracle.attention(q, k, v, scale=0.07, mod="alibi",
+                                  alibi_slopes=slopes.astype(np.float64))
+    gu.compare(o, lse, oref, lref, what="custom scale/slopes")
+
+
+# ------------------------------------------------------------------ full sizes
+
+def _full_size(S, B, Hq, Hk, mod, mask, tag, n_rows=96, **kw):
+    q, k, v = _inputs(tag, B, S, Hq, Hk)
+    okw = dict(kw)
+    o, lse, cnt, err = gu.run_standard(q, k, v, score_mod=mod, mask=mask, **kw)
+    assert err == 0
+    rows = gu.sample_rows(B, Hq, S, n_rows, seed=S)
+    oref, lref = oracle.attention(q, k, v, mod=mod, mask=mask, rows=rows, **okw)
+    o_s = np.stack([o[b, i, h] for b, h, i in rows])
+    l_s = np.array([lse[b, h, i] for b, h, i in rows])
+    gu.compare(o_s, l_s, oref, lref, what=f"{tag} {mod}/{mask}")
+    exp = gu.expected_tile_counts(mask, B, Hq, S, kw.get("window", 0), kw.get("prefix", 0),
+                                  kw.get("doc_offsets"))
+    assert np.array_equal(cnt, exp), f"{tag}: tile counts differ"
+    # properties that hold everywhere: finite outputs
+    assert np.all(np.isfinite(o)) and np.all(np.isfinite(lse))
+
+
+@pytest.mark.parametrize("mod,mask", [("none", "none"), ("alibi", "none"), ("softcap", "none"),
+                                      ("none", "causal")])
+@pytest.mark.parametrize("S", workloads.MHA_SEQ_LENS)
+def test_mha_sweep_full_size(S, mod, mask):
+    w = workloads.mha_workload(S)
+    _full_size(S, w["B"], w["H"], w["H"], mod, mask, w["name"], n_rows=48)
+
+
+@pytest.mark.parametrize("S,B", workloads.GQA_SHAPES)
+@pytest.mark.parametrize("mask", workloads.GQA_MASKS)
+def test_gqa_sweep_full_size(S, B, mask):
+    w = workloads.gqa_workload(S, B)
+    kw = {}
+    if mask == "window":
+        kw["window"] = workloads.WINDOW
+    elif mask == "prefix":
+        kw["prefix"] = workloads.PREFIX
+    else:
+        kw["doc_offsets"] = testdata.doc_offsets(S, B, w["name"], *workloads.DOC_LEN_RANGE)
+    _full_size(S, B, w["Hq"], w["Hk"], "none", mask, w["name"], n_rows=48, **kw)
+
+
+# ------------------------------------------------------------------ failure path
+
+def test_device_timeout_is_reported_and_context_survives():
+    """A K/V load that never arrives makes the consumer's bounded wait run out:
+    the kernel records FL_DEVERR_TIMEOUT and every CTA exits; the context stays
+    usable for the next call."""
+    q, k, v = _inputs("inject", 1, 512, 2)
+    o, lse, cnt, err = gu.run_standard(q, k, v, debug_inject=1, wait_timeout_us=20000)
+    assert err & 0x1, "timeout not reported"
+    o, lse, cnt, err = gu.run_standard(q, k, v)
+    assert err == 0
+    oref, lref = oracle.attention(q, k, v)
+    gu.compare(o, lse, oref, lref, what="after injected timeout")
