@@ -190,7 +190,7 @@ struct WaitCtl {
     uint32_t *err_lib;             // the library's own word
 };
 
-static __device__ __noinline__ bool mbar_wait_slow(uint32_t bar, uint32_t parity, const WaitCtl &c,
+static __device__ __forceinline__ bool mbar_wait_slow(uint32_t bar, uint32_t parity, const WaitCtl &c,
                                             uint32_t where, bool honour_abort)
 {
     const uint64_t t0 = ptx::globaltimer_ns();

@@ -8,12 +8,18 @@
 // running sum l per query row, the sum and the output rescaled when the max
 // moves (e^(x-y) = e^x / e^y), O += P V, never writing S or P to memory.
 //
-// CTA organisation (persistent: one CTA per SM, 320 threads):
+// CTA organisation (persistent: one CTA per SM, 384 threads):
 //   warps 0-3  softmax warpgroup of slot 0 (one thread per query row)
 //   warps 4-7  softmax warpgroup of slot 1
 //   warp  8    TMA producer: Q tiles once per work item, K/V tiles through an
 //              NS-stage mbarrier ring
 //   warp  9    MMA issuer (one thread) and TMEM owner
+//   warps 10-11 idle (they complete the third warpgroup)
+// The kernel is compiled for 168 registers per thread; after set-up the two
+// softmax warpgroups raise their limit to kRegsSoftmax and the third lowers
+// its own to kRegsOther, with 2*128*kRegsSoftmax + 128*kRegsOther equal to
+// 384*168 so the raise is always satisfiable (the host checks the compiled
+// register count before launching).
 // Each work item is two 128-row query tiles ("slots") sharing every K/V tile.
 //
 // TMEM (512 columns x 128 lanes, lane = query row):
@@ -35,7 +41,12 @@
 namespace fl {
 namespace {
 
-constexpr int kThreads = 320;
+constexpr int kThreads = 384;
+constexpr uint32_t kRegsLaunch = 168;
+constexpr uint32_t kRegsSoftmax = 216;
+constexpr uint32_t kRegsOther = 72;
+static_assert(2 * 128 * kRegsSoftmax + 128 * kRegsOther == kThreads * kRegsLaunch,
+              "register split must equal the launch allocation");
 constexpr int kStages = 4;
 constexpr uint32_t kTileBytes = BM * 64 * 2; // one 128 x 64 bf16 tile
 constexpr uint32_t kColS = 0, kColO = 256, kColP = 384;
@@ -278,7 +289,9 @@ __device__ void softmax_role(const KernelCtx &cx, const StdParams &p, int t)
                 for (int c = 0; c < BN / 32; ++c)
                     ptx::tmem_ld32(tS + 32 * c, raw + 32 * c);
                 ptx::tmem_wait_ld();
-                ptx::reg_fence<BN>(raw);
+#pragma unroll
+                for (int c = 0; c < BN / 32; ++c)
+                    ptx::reg_fence<32>(raw + 32 * c);
 #pragma unroll
                 for (int e = 0; e < BN; ++e)
                     x[e] = __uint_as_float(raw[e]);
@@ -322,37 +335,41 @@ __device__ void softmax_role(const KernelCtx &cx, const StdParams &p, int t)
                 if (__any_sync(0xffffffffu, need)) {
                     const float m_new = fmaxf(m_ref, mx);
                     const float alpha = (m_new == kNegInf) ? 1.f : ptx::ex2(m_ref - m_new);
-                    uint32_t o[32];
-#pragma unroll
-                    for (int c = 0; c < 2; ++c) {
-                        ptx::tmem_ld32(tO + 32 * c, o);
+#pragma unroll 1
+                    for (int c = 0; c < 64 / 16; ++c) {
+                        uint32_t o[16];
+                        ptx::tmem_ld16(tO + 16 * c, o);
                         ptx::tmem_wait_ld();
-                        ptx::reg_fence<32>(o);
+                        ptx::reg_fence<16>(o);
 #pragma unroll
-                        for (int e = 0; e < 32; ++e)
+                        for (int e = 0; e < 16; ++e)
                             o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
-                        ptx::tmem_st32(tO + 32 * c, o);
+                        ptx::tmem_st16(tO + 16 * c, o);
                     }
                     ptx::tmem_wait_st();
                     l *= alpha;
                     m_ref = m_new;
                 }
             }
+            // P = 2^(t - m) rounded to bf16 for the tensor core.  The row sum
+            // adds the ROUNDED values, so O / l is an exact convex combination
+            // of V rows with the weights the P V product actually used.
             const float mu = (m_ref == kNegInf) ? 0.f : m_ref;
-            float rs = 0.f;
+            float rs0 = 0.f, rs1 = 0.f;
 #pragma unroll
-            for (int c = 0; c < BN / 32; ++c) {
-                uint32_t pk[16];
+            for (int c = 0; c < BN / 16; ++c) {
+                uint32_t pk[8];
 #pragma unroll
-                for (int e = 0; e < 16; ++e) {
-                    const float p0 = ptx::ex2(x[32 * c + 2 * e] - mu);
-                    const float p1 = ptx::ex2(x[32 * c + 2 * e + 1] - mu);
-                    rs += p0 + p1;
+                for (int e = 0; e < 8; ++e) {
+                    const float p0 = ptx::ex2(x[16 * c + 2 * e] - mu);
+                    const float p1 = ptx::ex2(x[16 * c + 2 * e + 1] - mu);
                     pk[e] = ptx::pack_bf16(p0, p1);
+                    rs0 += __uint_as_float(pk[e] << 16);
+                    rs1 += __uint_as_float(pk[e] & 0xFFFF0000u);
                 }
-                ptx::tmem_st16(tP + 16 * c, pk);
+                ptx::tmem_st8(tP + 8 * c, pk);
             }
-            l += rs;
+            l += rs0 + rs1;
             ptx::tmem_wait_st();
             ptx::tc_fence_before();
             ptx::mbar_arrive(bar(sm.p_full[t]));
@@ -365,19 +382,11 @@ __device__ void softmax_role(const KernelCtx &cx, const StdParams &p, int t)
         ++ocount;
         ptx::tc_fence_after();
         uint32_t o[64];
-        {
-            uint32_t lo32[32], hi32[32];
-            ptx::tmem_ld32(tO, lo32);
-            ptx::tmem_ld32(tO + 32, hi32);
-            ptx::tmem_wait_ld();
-            ptx::reg_fence<32>(lo32);
-            ptx::reg_fence<32>(hi32);
-#pragma unroll
-            for (int e = 0; e < 32; ++e) {
-                o[e] = lo32[e];
-                o[32 + e] = hi32[e];
-            }
-        }
+        ptx::tmem_ld32(tO, o);
+        ptx::tmem_ld32(tO + 32, o + 32);
+        ptx::tmem_wait_ld();
+        ptx::reg_fence<32>(o);
+        ptx::reg_fence<32>(o + 32);
         const float inv = l > 0.f ? 1.f / l : 0.f;
         if (i < p.mask.S) {
             __nv_bfloat16 *dst = p.out + b * p.o_sb + static_cast<int64_t>(i) * p.o_ss + h * p.o_sh;
@@ -447,18 +456,25 @@ __global__ void __launch_bounds__(kThreads, 1)
     cx.wc.err_user = p.err_user;
     cx.wc.err_lib = &g_lib_error_word;
 
-    if (warp < 8)
+    // Each branch ends with its own copy of the teardown barrier, so no code
+    // runs under both register limits.
+    if (warp < 8) {
+        ptx::setmaxnreg_inc<kRegsSoftmax>();
         softmax_role<MOD>(cx, p, warp >> 2);
-    else if (warp == 8)
-        producer_role(cx, p, &tm_q, &tm_k, &tm_v);
-    else
-        mma_role(cx, p);
-
-    ptx::tc_fence_before();
-    __syncthreads();
-    if (warp == 9) {
-        ptx::tc_fence_after();
-        ptx::tmem_dealloc(cx.tmem, 512);
+        ptx::tc_fence_before();
+        ptx::named_barrier_sync(1, kThreads);
+    } else {
+        ptx::setmaxnreg_dec<kRegsOther>();
+        if (warp == 8)
+            producer_role(cx, p, &tm_q, &tm_k, &tm_v);
+        else if (warp == 9)
+            mma_role(cx, p);
+        ptx::tc_fence_before();
+        ptx::named_barrier_sync(1, kThreads);
+        if (warp == 9) {
+            ptx::tc_fence_after();
+            ptx::tmem_dealloc(cx.tmem, 512);
+        }
     }
 }
 
@@ -467,11 +483,17 @@ cudaError_t launch_mod(const CUtensorMap &tq, const CUtensorMap &tk, const CUten
                        const StdParams &p, int grid, cudaStream_t stream)
 {
     const size_t smem = sizeof(StdSmem) + 1024;
-    static bool configured = false; // benign race: the attribute call is idempotent
+    static bool configured = false; // benign race: both calls are idempotent
     if (!configured) {
-        cudaError_t e = cudaFuncSetAttribute(std_fwd_kernel<MOD>,
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             static_cast<int>(smem));
+        cudaFuncAttributes attr;
+        cudaError_t e = cudaFuncGetAttributes(&attr, std_fwd_kernel<MOD>);
+        if (e != cudaSuccess)
+            return e;
+        // The setmaxnreg split assumes exactly kRegsLaunch registers at launch.
+        if (attr.numRegs != static_cast<int>(kRegsLaunch))
+            return cudaErrorInvalidConfiguration;
+        e = cudaFuncSetAttribute(std_fwd_kernel<MOD>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 static_cast<int>(smem));
         if (e != cudaSuccess)
             return e;
         configured = true;
