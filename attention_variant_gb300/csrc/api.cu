@@ -252,8 +252,8 @@ fl_status fwd_standard(const fl_tensor *q, const fl_tensor *k, const fl_tensor *
         return fail(FL_ERR_INVALID_ARG, "unknown score_mod %d", d->score_mod);
     if (d->score_mod == FL_MOD_SOFTCAP && !(d->softcap > 0.f && std::isfinite(d->softcap)))
         return fail(FL_ERR_INVALID_ARG, "softcap must be positive and finite");
-    if (!std::isfinite(d->scale))
-        return fail(FL_ERR_INVALID_ARG, "scale must be finite");
+    if (!std::isfinite(d->scale) || d->scale < 0.f)
+        return fail(FL_ERR_INVALID_ARG, "scale must be finite and positive (0 selects 1/sqrt(D))");
     if (d->mask == FL_MASK_DOC && d->doc_stride < 2)
         return fail(FL_ERR_INVALID_ARG, "doc_stride must be >= 2");
     if (D != 64 || Dv != 64)
@@ -343,6 +343,109 @@ fl_status fwd_standard(const fl_tensor *q, const fl_tensor *k, const fl_tensor *
     return ok();
 }
 
+// ------------------------------------------------------------------ differential
+
+fl_status fwd_diff(const fl_tensor *q, const fl_tensor *k, const fl_tensor *v,
+                   const fl_tensor *out, const fl_tensor *lse, const fl_attn_variant_desc *d,
+                   const fl_tensor *bias, const fl_tensor *gate, cudaStream_t stream)
+{
+    View Q, K, V, O, L{};
+    fl_status s;
+    if ((s = check_tensor(q, "q", 5, FL_BF16, Q)) != FL_OK) return s;
+    if ((s = check_tensor(k, "k", 5, FL_BF16, K)) != FL_OK) return s;
+    if ((s = check_tensor(v, "v", 4, FL_BF16, V)) != FL_OK) return s;
+    if ((s = check_tensor(out, "out", 4, FL_BF16, O)) != FL_OK) return s;
+    if (bias || gate)
+        return fail(FL_ERR_INVALID_ARG, "bias and gate are only taken by the Evoformer kinds");
+    if (Q.size[0] != 2 || K.size[0] != 2)
+        return fail(FL_ERR_INVALID_ARG, "q and k need a leading stream axis of size 2");
+    const int64_t B = Q.size[1], S = Q.size[2], H = Q.size[3], D = Q.size[4];
+    const int64_t Hk = K.size[3], Dv = V.size[3];
+    if (!(K.size[1] == B && K.size[2] == S && K.size[4] == D))
+        return fail(FL_ERR_INVALID_ARG, "k must be [2, B, S, Hk, D] matching q");
+    if (!same(V, {B, S, Hk, Dv}))
+        return fail(FL_ERR_INVALID_ARG, "v must be [B, S, Hk, Dv]");
+    if (!same(O, {B, S, H, Dv}))
+        return fail(FL_ERR_INVALID_ARG, "out must be [B, S, H, Dv]");
+    if (H % Hk != 0)
+        return fail(FL_ERR_INVALID_ARG, "H must be a multiple of Hk");
+    if (d->gqa_group != 0 && d->gqa_group != H / Hk)
+        return fail(FL_ERR_INVALID_ARG, "gqa_group does not match H / Hk");
+    if (lse) {
+        if ((s = check_tensor(lse, "lse", 4, FL_F32, L)) != FL_OK) return s;
+        if (!same(L, {2, B, H, S}))
+            return fail(FL_ERR_INVALID_ARG, "lse must be [2, B, H, S]");
+    }
+    if (d->mask != FL_MASK_NONE && d->mask != FL_MASK_CAUSAL)
+        return fail(FL_ERR_UNSUPPORTED, "differential attention takes no mask or causal");
+    if (d->score_mod != FL_MOD_NONE)
+        return fail(FL_ERR_UNSUPPORTED, "differential attention takes no score_mod");
+    if (!std::isfinite(d->scale) || d->scale < 0.f || !std::isfinite(d->diff_lambda))
+        return fail(FL_ERR_INVALID_ARG, "scale must be finite and positive, diff_lambda finite");
+    if (D != 64 || Dv != 128)
+        return fail(FL_ERR_UNSUPPORTED, "differential kind supports D = 64, Dv = 128");
+
+    int dev;
+    DeviceInfo info;
+    if ((s = device_info(dev, info)) != FL_OK) return s;
+    CUtensorMap tq, tk, tv;
+    {
+        const uint64_t dims[5] = {uint64_t(D), uint64_t(S), uint64_t(H), uint64_t(B), 2};
+        const uint64_t st[4] = {uint64_t(Q.stride[2]) * 2, uint64_t(Q.stride[3]) * 2,
+                                uint64_t(Q.stride[1]) * 2, uint64_t(Q.stride[0]) * 2};
+        const uint32_t box[5] = {64, 128, 1, 1, 1};
+        if ((s = make_map(tq, Q.ptr, 5, dims, st, box, CU_TENSOR_MAP_SWIZZLE_128B, "q")) != FL_OK)
+            return s;
+    }
+    {
+        const uint64_t dims[5] = {uint64_t(D), uint64_t(S), uint64_t(Hk), uint64_t(B), 2};
+        const uint64_t st[4] = {uint64_t(K.stride[2]) * 2, uint64_t(K.stride[3]) * 2,
+                                uint64_t(K.stride[1]) * 2, uint64_t(K.stride[0]) * 2};
+        const uint32_t box[5] = {64, 128, 1, 1, 1};
+        if ((s = make_map(tk, K.ptr, 5, dims, st, box, CU_TENSOR_MAP_SWIZZLE_128B, "k")) != FL_OK)
+            return s;
+    }
+    {
+        const uint64_t dims[4] = {uint64_t(Dv), uint64_t(S), uint64_t(Hk), uint64_t(B)};
+        const uint64_t st[3] = {uint64_t(V.stride[1]) * 2, uint64_t(V.stride[2]) * 2,
+                                uint64_t(V.stride[0]) * 2};
+        const uint32_t box[4] = {64, 128, 1, 1};
+        if ((s = make_map(tv, V.ptr, 4, dims, st, box, CU_TENSOR_MAP_SWIZZLE_128B, "v")) != FL_OK)
+            return s;
+    }
+    fl::DiffParams p{};
+    p.B = int(B);
+    p.H = int(H);
+    p.Hk = int(Hk);
+    p.G = int(H / Hk);
+    p.nq = int((S + fl::BM - 1) / fl::BM);
+    p.n_items = int64_t(p.B) * p.H * p.nq;
+    p.lpt = d->mask == FL_MASK_CAUSAL;
+    p.group = 8;
+    p.mask.kind = d->mask;
+    p.mask.S = int(S);
+    p.qk_log2 = (d->scale != 0.f ? d->scale : 1.0f / std::sqrt(float(D))) * 1.4426950408889634f;
+    p.lambda = d->diff_lambda;
+    p.out = static_cast<__nv_bfloat16 *>(O.ptr);
+    p.o_sb = O.stride[0];
+    p.o_ss = O.stride[1];
+    p.o_sh = O.stride[2];
+    if (lse) {
+        p.lse = static_cast<float *>(L.ptr);
+        p.l_s2 = L.stride[0];
+        p.l_sb = L.stride[1];
+        p.l_sh = L.stride[2];
+    }
+    p.tile_counts = d->debug_tile_counts;
+    p.err_user = d->error_word;
+    p.timeout_ns = timeout_ns(d);
+    const int grid = int(p.n_items < info.sm_count ? p.n_items : info.sm_count);
+    cudaError_t e = fl::launch_diff(tq, tk, tv, p, grid, stream);
+    if (e != cudaSuccess)
+        return fail(FL_ERR_CUDA, "kernel launch failed: %s", cudaGetErrorString(e));
+    return ok();
+}
+
 } // namespace
 
 extern "C" {
@@ -358,6 +461,7 @@ fl_status fl_attn_fwd(const fl_tensor *q, const fl_tensor *k, const fl_tensor *v
     case FL_KIND_STANDARD:
         return fwd_standard(q, k, v, out, lse, desc, bias, gate, reinterpret_cast<cudaStream_t>(stream));
     case FL_KIND_DIFF:
+        return fwd_diff(q, k, v, out, lse, desc, bias, gate, reinterpret_cast<cudaStream_t>(stream));
     case FL_KIND_EVO_ROW:
     case FL_KIND_EVO_COL:
         return fail(FL_ERR_UNSUPPORTED, "kind %d is not built yet", desc->kind);

@@ -37,6 +37,7 @@
 
 #include "common.cuh"
 #include "launch.h"
+#include "softmax_tile.cuh"
 
 namespace fl {
 namespace {
@@ -267,110 +268,31 @@ __device__ void softmax_role(const KernelCtx &cx, const StdParams &p, int t)
         int row_lo, row_hi;
         row_interval(p.mask, b, i, row_lo, row_hi);
 
-        float alibi_c = 0.f;
+        ScoreMod smod;
+        smod.qk_log2 = p.qk_log2;
+        smod.softcap_in = p.softcap_in;
+        smod.softcap_out = p.softcap_out;
+        smod.alibi_c = 0.f;
         if constexpr (MOD == MOD_ALIBI) {
             const float slope = p.alibi_slopes ? __ldg(p.alibi_slopes + h)
                                                : exp2f(p.alibi_exp_coef * static_cast<float>(h + 1));
-            alibi_c = slope * kLog2e;
+            smod.alibi_c = slope * kLog2e;
         }
 
-        float m_ref = kNegInf, l = 0.f;
+        RowState st{kNegInf, 0.f, 0.f};
         int ntiles = 0;
         for (int j = tr.lo; j < tr.hi; ++j) {
             if (!warp_wait(bar(sm.s_full[t]), scount & 1, cx.wc, W_S_FULL))
                 return;
             ++scount;
             ptx::tc_fence_after();
-
             float x[BN];
-            {
-                uint32_t raw[BN];
-#pragma unroll
-                for (int c = 0; c < BN / 32; ++c)
-                    ptx::tmem_ld32(tS + 32 * c, raw + 32 * c);
-                ptx::tmem_wait_ld();
-#pragma unroll
-                for (int c = 0; c < BN / 32; ++c)
-                    ptx::reg_fence<32>(raw + 32 * c);
-#pragma unroll
-                for (int e = 0; e < BN; ++e)
-                    x[e] = __uint_as_float(raw[e]);
-            }
+            load_scores(tS, x);
             const int j0 = j * BN;
-            // logits in log2 units
-            if constexpr (MOD == MOD_NONE) {
-#pragma unroll
-                for (int e = 0; e < BN; ++e)
-                    x[e] *= p.qk_log2;
-            } else if constexpr (MOD == MOD_ALIBI) {
-                const float d0 = static_cast<float>(j0 - i);
-#pragma unroll
-                for (int e = 0; e < BN; ++e)
-                    x[e] = fmaf(x[e], p.qk_log2, -alibi_c * fabsf(d0 + static_cast<float>(e)));
-            } else {
-                // cap * tanh(u), tanh(u) = 1 - 2 / (1 + e^(2u)), in log2 units
-#pragma unroll
-                for (int e = 0; e < BN; ++e) {
-                    const float ex = ptx::ex2(x[e] * p.softcap_in);
-                    x[e] = p.softcap_out * (1.f - 2.f * ptx::rcp_approx(1.f + ex));
-                }
-            }
-            const bool full = (j0 >= tr.full_lo) && (j0 + BN <= tr.full_hi);
-            if (!full) {
-                const int a = row_lo - j0, z = row_hi - j0;
-#pragma unroll
-                for (int e = 0; e < BN; ++e)
-                    if (e < a || e >= z)
-                        x[e] = kNegInf;
-            }
-            float mx = x[0];
-#pragma unroll
-            for (int e = 1; e < BN; ++e)
-                mx = fmaxf(mx, x[e]);
-
-            if (j == tr.lo) {
-                m_ref = mx;
-            } else {
-                const bool need = mx > m_ref + 8.f;
-                if (__any_sync(0xffffffffu, need)) {
-                    const float m_new = fmaxf(m_ref, mx);
-                    const float alpha = (m_new == kNegInf) ? 1.f : ptx::ex2(m_ref - m_new);
-#pragma unroll 1
-                    for (int c = 0; c < 64 / 16; ++c) {
-                        uint32_t o[16];
-                        ptx::tmem_ld16(tO + 16 * c, o);
-                        ptx::tmem_wait_ld();
-                        ptx::reg_fence<16>(o);
-#pragma unroll
-                        for (int e = 0; e < 16; ++e)
-                            o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
-                        ptx::tmem_st16(tO + 16 * c, o);
-                    }
-                    ptx::tmem_wait_st();
-                    l *= alpha;
-                    m_ref = m_new;
-                }
-            }
-            // P = 2^(t - m) rounded to bf16 for the tensor core.  The row sum
-            // adds the ROUNDED values, so O / l is an exact convex combination
-            // of V rows with the weights the P V product actually used.
-            const float mu = (m_ref == kNegInf) ? 0.f : m_ref;
-            float rs0 = 0.f, rs1 = 0.f;
-#pragma unroll
-            for (int c = 0; c < BN / 16; ++c) {
-                uint32_t pk[8];
-#pragma unroll
-                for (int e = 0; e < 8; ++e) {
-                    const float p0 = ptx::ex2(x[16 * c + 2 * e] - mu);
-                    const float p1 = ptx::ex2(x[16 * c + 2 * e + 1] - mu);
-                    pk[e] = ptx::pack_bf16(p0, p1);
-                    rs0 += __uint_as_float(pk[e] << 16);
-                    rs1 += __uint_as_float(pk[e] & 0xFFFF0000u);
-                }
-                ptx::tmem_st8(tP + 8 * c, pk);
-            }
-            l += rs0 + rs1;
-            ptx::tmem_wait_st();
+            apply_score_mod<MOD>(x, smod, i, j0);
+            if (!((j0 >= tr.full_lo) && (j0 + BN <= tr.full_hi)))
+                apply_row_mask(x, j0, row_lo, row_hi);
+            online_update_and_store_p<64>(x, MOD == MOD_NONE ? p.qk_log2 : 1.f, st, j == tr.lo, tO, tP);
             ptx::tc_fence_before();
             ptx::mbar_arrive(bar(sm.p_full[t]));
             ++ntiles;
@@ -387,7 +309,7 @@ __device__ void softmax_role(const KernelCtx &cx, const StdParams &p, int t)
         ptx::tmem_wait_ld();
         ptx::reg_fence<32>(o);
         ptx::reg_fence<32>(o + 32);
-        const float inv = l > 0.f ? 1.f / l : 0.f;
+        const float inv = row_inv_norm(st);
         if (i < p.mask.S) {
             __nv_bfloat16 *dst = p.out + b * p.o_sb + static_cast<int64_t>(i) * p.o_ss + h * p.o_sh;
             uint4 *d4 = reinterpret_cast<uint4 *>(dst);
@@ -401,7 +323,7 @@ __device__ void softmax_role(const KernelCtx &cx, const StdParams &p, int t)
                 d4[c] = w;
             }
             if (p.lse)
-                p.lse[b * p.l_sb + h * p.l_sh + i] = l > 0.f ? (m_ref + log2f(l)) * kLn2 : kNegInf;
+                p.lse[b * p.l_sb + h * p.l_sh + i] = row_lse(st);
         }
         if (p.tile_counts && r == 0)
             p.tile_counts[(static_cast<int64_t>(b) * p.grid.Hq + h) * p.grid.nq + qb] = ntiles;

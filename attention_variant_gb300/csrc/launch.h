@@ -32,6 +32,26 @@ struct StdParams {
     uint64_t timeout_ns;
 };
 
+// Parameters of the differential-attention kernel (D = 64, Dv = 128).
+struct DiffParams {
+    int B, H, Hk, G, nq;
+    int64_t n_items;
+    int lpt, group;
+    MaskSpec mask;        // none or causal
+    float qk_log2;        // scale * log2(e)
+    float lambda;
+    __nv_bfloat16 *out;   // [B, S, H, 128]
+    int64_t o_sb, o_ss, o_sh;
+    float *lse;           // [2, B, H, S] or null
+    int64_t l_s2, l_sb, l_sh;
+    int32_t *tile_counts; // [B][H][nq] or null
+    uint32_t *err_user;
+    uint64_t timeout_ns;
+};
+
+cudaError_t launch_diff(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
+                        const DiffParams &p, int grid, cudaStream_t stream);
+
 cudaError_t launch_standard(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
                             const StdParams &p, int grid, cudaStream_t stream);
 size_t standard_smem_bytes();

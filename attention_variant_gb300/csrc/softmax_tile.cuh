@@ -1,0 +1,165 @@
+// softmax_tile.cuh -- the per-row online-softmax step on one 128-key tile,
+// shared by every fused attention kernel.
+//
+// One thread owns one query row (= one TMEM lane).  For key tile j it reads
+// the fp32 scores S from TMEM, forms log2-domain logits t (scale * log2 e is
+// folded into the exponent's multiply-add for the plain score, or applied
+// with the score_mod), masks them, takes the row max, lazily rescales the
+// running output O and sums when the max has grown by more than
+// kRescaleThreshold (2^8), and writes P = 2^(t - m) as bf16 into TMEM for the
+// P V product.  This is the running-max / running-sum recurrence of the
+// online softmax (Flashlight gist.science summary, "Methodology" item 3; talk
+// notes, "Compiler design 2"); keeping a stale reference max m is exact in
+// real arithmetic because every term and both sums carry the same factor.
+//
+// Two sums are kept: `l` adds the exact P (it gives the log-sum-exp), and
+// `l_round` adds the bf16-rounded P the tensor core actually multiplies V
+// by (it normalises O, so O / l_round is an exact convex combination of V
+// rows with those weights).
+#pragma once
+
+#include "common.cuh"
+
+namespace fl {
+
+constexpr float kRescaleThreshold = 8.f; // log2 units
+
+struct RowState {
+    float m_ref;   // reference max (log2 units) every P of this row is relative to
+    float l;       // sum of the exact P
+    float l_round; // sum of the bf16-rounded P
+};
+
+struct ScoreMod {
+    float qk_log2;     // scale * log2(e) (> 0)
+    float alibi_c;     // slope_h * log2(e)                 (ALiBi)
+    float softcap_in;  // 2 * scale * log2(e) / cap           (softcap)
+    float softcap_out; // cap * log2(e)                       (softcap)
+};
+
+// Loads the 128 scores of this thread's row from TMEM columns [tS, tS + 128).
+__device__ __forceinline__ void load_scores(uint32_t tS, float (&x)[BN])
+{
+    uint32_t raw[BN];
+#pragma unroll
+    for (int c = 0; c < BN / 32; ++c)
+        ptx::tmem_ld32(tS + 32 * c, raw + 32 * c);
+    ptx::tmem_wait_ld();
+#pragma unroll
+    for (int c = 0; c < BN / 32; ++c)
+        ptx::reg_fence<32>(raw + 32 * c);
+#pragma unroll
+    for (int e = 0; e < BN; ++e)
+        x[e] = __uint_as_float(raw[e]);
+}
+
+// Scores -> logits for query row i and keys j0 .. j0 + 127.  For MOD_NONE the
+// scores stay unscaled (the scale is applied in the exponent); the other
+// score_mods produce log2-domain logits.
+template <int MOD>
+__device__ __forceinline__ void apply_score_mod(float (&x)[BN], const ScoreMod &sm, int i, int j0)
+{
+    if constexpr (MOD == MOD_ALIBI) {
+        // z - slope |i - j|, in log2 units
+        const float d0 = static_cast<float>(j0 - i);
+#pragma unroll
+        for (int e = 0; e < BN; ++e)
+            x[e] = fmaf(x[e], sm.qk_log2, -sm.alibi_c * fabsf(d0 + static_cast<float>(e)));
+    } else if constexpr (MOD == MOD_SOFTCAP) {
+        // cap * tanh(z / cap) with tanh(u) = 1 - 2 / (1 + e^(2u)), in log2 units
+#pragma unroll
+        for (int e = 0; e < BN; ++e) {
+            const float ex = ptx::ex2(x[e] * sm.softcap_in);
+            x[e] = sm.softcap_out * (1.f - 2.f * ptx::rcp_approx(1.f + ex));
+        }
+    }
+}
+
+// Keys outside [row_lo, row_hi) -> -inf (only on tiles that hold masked pairs).
+__device__ __forceinline__ void apply_row_mask(float (&x)[BN], int j0, int row_lo, int row_hi)
+{
+    const int a = row_lo - j0, z = row_hi - j0;
+#pragma unroll
+    for (int e = 0; e < BN; ++e)
+        if (e < a || e >= z)
+            x[e] = kNegInf;
+}
+
+// Max update with lazy rescale of the DV fp32 output columns at tO, then
+// P = 2^(t - m) -> bf16 at tP (64 columns) and both sums.  `first` marks the
+// first tile of the row's range (O is not yet written: the P V product of that
+// tile overwrites it).  For MOD_NONE, x holds raw scores and `c` = scale *
+// log2 e; otherwise x holds log2-domain logits and `c` = 1.
+template <int DV>
+__device__ __forceinline__ void online_update_and_store_p(float (&x)[BN], float c, RowState &st,
+                                                          bool first, uint32_t tO, uint32_t tP)
+{
+    float m0 = ptx::max3(x[0], x[1], x[2]);
+    float m1 = ptx::max3(x[3], x[4], x[5]);
+#pragma unroll
+    for (int e = 6; e + 3 < BN; e += 4) {
+        m0 = ptx::max3(m0, x[e], x[e + 1]);
+        m1 = ptx::max3(m1, x[e + 2], x[e + 3]);
+    }
+    m0 = ptx::max3(m0, m1, x[BN - 2]);
+    const float mx = fmaxf(m0, x[BN - 1]) * c; // c > 0: scaling commutes with max
+
+    if (first) {
+        st.m_ref = mx;
+    } else {
+        const bool need = mx > st.m_ref + kRescaleThreshold;
+        if (__any_sync(0xffffffffu, need)) {
+            const float m_new = fmaxf(st.m_ref, mx);
+            const float alpha = (m_new == kNegInf) ? 1.f : ptx::ex2(st.m_ref - m_new);
+#pragma unroll 1
+            for (int k = 0; k < DV / 16; ++k) {
+                uint32_t o[16];
+                ptx::tmem_ld16(tO + 16 * k, o);
+                ptx::tmem_wait_ld();
+                ptx::reg_fence<16>(o);
+#pragma unroll
+                for (int e = 0; e < 16; ++e)
+                    o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
+                ptx::tmem_st16(tO + 16 * k, o);
+            }
+            ptx::tmem_wait_st();
+            st.l *= alpha;
+            st.l_round *= alpha;
+            st.m_ref = m_new;
+        }
+    }
+    const float nmu = (st.m_ref == kNegInf) ? 0.f : -st.m_ref;
+    float le0 = 0.f, le1 = 0.f, lr0 = 0.f, lr1 = 0.f;
+#pragma unroll
+    for (int k = 0; k < BN / 16; ++k) {
+        uint32_t pk[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+            float a0, a1;
+            ptx::fma2(a0, a1, x[16 * k + 2 * e], x[16 * k + 2 * e + 1], c, c, nmu, nmu);
+            const float p0 = ptx::ex2(a0);
+            const float p1 = ptx::ex2(a1);
+            pk[e] = ptx::pack_bf16(p0, p1);
+            ptx::add2(le0, le1, p0, p1);
+            ptx::add2(lr0, lr1, __uint_as_float(pk[e] << 16), __uint_as_float(pk[e] & 0xFFFF0000u));
+        }
+        ptx::tmem_st8(tP + 8 * k, pk);
+    }
+    st.l += le0 + le1;
+    st.l_round += lr0 + lr1;
+    ptx::tmem_wait_st();
+}
+
+// Natural-log LSE of a finished row (from the exact sum).
+__device__ __forceinline__ float row_lse(const RowState &st)
+{
+    return st.l > 0.f ? (st.m_ref + log2f(st.l)) * kLn2 : kNegInf;
+}
+
+// 1 / (the normaliser of O), 0 for a row with no allowed key.
+__device__ __forceinline__ float row_inv_norm(const RowState &st)
+{
+    return st.l_round > 0.f ? 1.f / st.l_round : 0.f;
+}
+
+} // namespace fl
