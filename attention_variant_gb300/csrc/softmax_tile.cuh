@@ -94,15 +94,18 @@ template <int DV>
 __device__ __forceinline__ void online_update_and_store_p(float (&x)[BN], float c, RowState &st,
                                                           bool first, uint32_t tO, uint32_t tP)
 {
-    float m0 = ptx::max3(x[0], x[1], x[2]);
-    float m1 = ptx::max3(x[3], x[4], x[5]);
+    // four independent max chains (3-input max), then combine
+    float mc[4];
 #pragma unroll
-    for (int e = 6; e + 3 < BN; e += 4) {
-        m0 = ptx::max3(m0, x[e], x[e + 1]);
-        m1 = ptx::max3(m1, x[e + 2], x[e + 3]);
+    for (int q = 0; q < 4; ++q)
+        mc[q] = fmaxf(x[2 * q], x[2 * q + 1]);
+#pragma unroll
+    for (int e = 8; e < BN; e += 8) {
+#pragma unroll
+        for (int q = 0; q < 4; ++q)
+            mc[q] = ptx::max3(mc[q], x[e + 2 * q], x[e + 2 * q + 1]);
     }
-    m0 = ptx::max3(m0, m1, x[BN - 2]);
-    const float mx = fmaxf(m0, x[BN - 1]) * c; // c > 0: scaling commutes with max
+    const float mx = fmaxf(fmaxf(mc[0], mc[1]), fmaxf(mc[2], mc[3])) * c; // c > 0
 
     if (first) {
         st.m_ref = mx;
@@ -129,7 +132,9 @@ __device__ __forceinline__ void online_update_and_store_p(float (&x)[BN], float 
         }
     }
     const float nmu = (st.m_ref == kNegInf) ? 0.f : -st.m_ref;
-    float le0 = 0.f, le1 = 0.f, lr0 = 0.f, lr1 = 0.f;
+    // four independent packed accumulators per sum keep the add chains short
+    float le[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+    float lr[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
 #pragma unroll
     for (int k = 0; k < BN / 16; ++k) {
         uint32_t pk[8];
@@ -140,13 +145,15 @@ __device__ __forceinline__ void online_update_and_store_p(float (&x)[BN], float 
             const float p0 = ptx::ex2(a0);
             const float p1 = ptx::ex2(a1);
             pk[e] = ptx::pack_bf16(p0, p1);
-            ptx::add2(le0, le1, p0, p1);
-            ptx::add2(lr0, lr1, __uint_as_float(pk[e] << 16), __uint_as_float(pk[e] & 0xFFFF0000u));
+            const int q = 2 * (e & 3);
+            ptx::add2(le[q], le[q + 1], p0, p1);
+            ptx::add2(lr[q], lr[q + 1], __uint_as_float(pk[e] << 16),
+                      __uint_as_float(pk[e] & 0xFFFF0000u));
         }
         ptx::tmem_st8(tP + 8 * k, pk);
     }
-    st.l += le0 + le1;
-    st.l_round += lr0 + lr1;
+    st.l += ((le[0] + le[1]) + (le[2] + le[3])) + ((le[4] + le[5]) + (le[6] + le[7]));
+    st.l_round += ((lr[0] + lr[1]) + (lr[2] + lr[3])) + ((lr[4] + lr[5]) + (lr[6] + lr[7]));
     ptx::tmem_wait_st();
 }
 
