@@ -27,11 +27,17 @@
 //   384 + 64 t, for slots t = 0, 1.
 //
 // Hand-off protocol for slot t and key tile j (all mbarriers):
-//   MMA: [wait p_full(t)] O[t] += P[t] V_{j-1}; S[t] = Q[t] K_j^T; commit s_full(t)
-//   softmax: wait s_full(t); S[t] -> registers; score_mod, mask, row max;
-//            lazily rescale O[t] and l; P = 2^(t - m) -> TMEM; arrive p_full(t)
-// s_full(t) for tile j is committed after the P V of tile j-1 was issued, so
-// when it fires O[t] already holds that product and P[t] may be overwritten.
+//   MMA:     wait p_full(t) [P(t, j) written, O(t) rescaled]; issue
+//            S[t] = Q[t] K_{j+1}^T and commit s_full(t); then issue
+//            O[t] += P[t] V_j and commit pv_done(t).
+//   softmax: wait s_full(t); S[t] -> registers; score_mod, mask, row max,
+//            P in registers; wait pv_done(t) [the P V of tile j-1 has read
+//            P[t] and landed in O[t]]; lazily rescale O[t]; P -> TMEM; arrive
+//            p_full(t).
+// Issuing the next QK^T before the current P V lets the softmax of tile j+1
+// start after one MMA instead of two, and P has its own columns so the next
+// S never overwrites a P still being read.  Q is double-buffered across work
+// items so the next item's Q arrives while the current one finishes.
 #include <cuda_bf16.h>
 #include <cstdint>
 
@@ -44,8 +50,8 @@ namespace {
 
 constexpr int kThreads = 384;
 constexpr uint32_t kRegsLaunch = 168;
-constexpr uint32_t kRegsSoftmax = 216;
-constexpr uint32_t kRegsOther = 72;
+constexpr uint32_t kRegsSoftmax = 208;
+constexpr uint32_t kRegsOther = 88;
 static_assert(2 * 128 * kRegsSoftmax + 128 * kRegsOther == kThreads * kRegsLaunch,
               "register split must equal the launch allocation");
 constexpr int kStages = 4;
@@ -53,12 +59,12 @@ constexpr uint32_t kTileBytes = BM * 64 * 2; // one 128 x 64 bf16 tile
 constexpr uint32_t kColS = 0, kColO = 256, kColP = 384;
 
 struct __align__(1024) StdSmem {
-    uint8_t q[2][kTileBytes];
+    uint8_t q[2][2][kTileBytes]; // [Q buffer][slot]
     uint8_t k[kStages][kTileBytes];
     uint8_t v[kStages][kTileBytes];
-    uint64_t q_full, q_empty;
+    uint64_t q_full[2], q_empty[2];
     uint64_t kv_full[kStages], kv_empty[kStages];
-    uint64_t s_full[2], p_full[2], o_full[2];
+    uint64_t s_full[2], p_full[2], pv_done[2];
     uint64_t final_bar;
     uint32_t tmem_base;
     uint32_t abort_flag;
@@ -96,17 +102,18 @@ __device__ void producer_role(const KernelCtx &cx, const StdParams &p, const CUt
             hi = max(hi, r.hi);
             ++nvalid;
         }
-        if (item_count > 0) {
-            ok = warp_wait(bar(sm.q_empty), (item_count - 1) & 1, cx.wc, W_Q_EMPTY);
+        const uint32_t qbuf = item_count & 1;
+        if (item_count >= 2) {
+            ok = warp_wait(bar(sm.q_empty[qbuf]), ((item_count - 2) >> 1) & 1, cx.wc, W_Q_EMPTY);
             if (!ok)
                 break;
         }
         if (lane == 0) {
-            ptx::mbar_arrive_expect_tx(bar(sm.q_full), nvalid * kTileBytes);
+            ptx::mbar_arrive_expect_tx(bar(sm.q_full[qbuf]), nvalid * kTileBytes);
 #pragma unroll
             for (int t = 0; t < 2; ++t)
                 if (it.valid[t])
-                    ptx::tma_load_4d(ptx::smem_u32(sm.q[t]), tm_q, bar(sm.q_full), 0,
+                    ptx::tma_load_4d(ptx::smem_u32(sm.q[qbuf][t]), tm_q, bar(sm.q_full[qbuf]), 0,
                                      it.qb[t] * BM, it.h[t], it.b);
         }
         __syncwarp();
@@ -142,8 +149,8 @@ __device__ void producer_role(const KernelCtx &cx, const StdParams &p, const CUt
                 continue;
             mbar_wait_drain(bar(sm.kv_full[idx % kStages]), (idx / kStages) & 1, cx.wc, W_DRAIN);
         }
-        if (item_count > 0)
-            mbar_wait_drain(bar(sm.q_full), (item_count - 1) & 1, cx.wc, W_DRAIN);
+        for (uint32_t n = item_count > 2 ? item_count - 2 : 0; n < item_count; ++n)
+            mbar_wait_drain(bar(sm.q_full[n & 1]), (n >> 1) & 1, cx.wc, W_DRAIN);
     }
 }
 
@@ -154,13 +161,14 @@ __device__ void mma_role(const KernelCtx &cx, const StdParams &p)
     const uint32_t lane = ptx::lane_id();
     constexpr uint32_t idesc_qk = umma_idesc_bf16(BM, BN, false);
     constexpr uint32_t idesc_pv = umma_idesc_bf16(BM, 64, true);
-    uint32_t kv_count = 0, item_count = 0;
+    uint32_t kv_base = 0, item_count = 0;
     uint32_t pcount[2] = {0, 0};
     bool ok = true;
+
     for (int64_t L = blockIdx.x; L < p.grid.n_items && ok; L += gridDim.x) {
         const Item it = decode_item(p.grid, L);
         int lo_t[2], hi_t[2];
-        int lo = 1 << 30, hi = 0;
+        int lo = 1 << 30, hi = 0, s_total = 0;
 #pragma unroll
         for (int t = 0; t < 2; ++t) {
             lo_t[t] = hi_t[t] = 0;
@@ -171,71 +179,91 @@ __device__ void mma_role(const KernelCtx &cx, const StdParams &p)
             hi_t[t] = r.hi;
             lo = min(lo, r.lo);
             hi = max(hi, r.hi);
+            s_total += r.hi - r.lo;
         }
-        ok = warp_wait(bar(sm.q_full), item_count & 1, cx.wc, W_Q_FULL);
+        const uint32_t qbuf = item_count & 1;
+        ok = warp_wait(bar(sm.q_full[qbuf]), (item_count >> 1) & 1, cx.wc, W_Q_FULL);
         if (!ok)
             break;
         ptx::tc_fence_after();
-        uint32_t prev_stage = 0;
-        for (int j = lo; j <= hi && ok; ++j) {
-            const uint32_t stage = kv_count % kStages;
-            if (j < hi) {
-                ok = warp_wait(bar(sm.kv_full[stage]), (kv_count / kStages) & 1, cx.wc, W_KV_FULL);
-                if (!ok)
-                    break;
-                ptx::tc_fence_after();
+        int s_issued = 0;
+        uint32_t waited = 0; // ring entries of this item whose kv_full has been waited
+
+        // S[t] = Q[t] K_j^T for key tile j (its ring entry already waited)
+        auto issue_s = [&](int t, int j) {
+            const uint32_t stage = (kv_base + (j - lo)) % kStages;
+            if (lane == 0) {
+                const uint32_t qbase = ptx::smem_u32(sm.q[qbuf][t]);
+                const uint32_t kbase = ptx::smem_u32(sm.k[stage]);
+#pragma unroll
+                for (int kk = 0; kk < 64 / 16; ++kk)
+                    ptx::mma_ss(cx.tmem + kColS + 128 * t,
+                                umma_desc(qbase + kk * 32, 16, 1024, kSwizzle128B),
+                                umma_desc(kbase + kk * 32, 16, 1024, kSwizzle128B), idesc_qk,
+                                kk > 0 ? 1u : 0u);
+                ptx::mma_commit(bar(sm.s_full[t]));
+                if (++s_issued == s_total)
+                    ptx::mma_commit(bar(sm.q_empty[qbuf])); // last read of this Q buffer
             }
+            __syncwarp();
+        };
+        // make sure key tile j's K/V have landed
+        auto need_tile = [&](int j) -> bool {
+            while (waited <= static_cast<uint32_t>(j - lo)) {
+                const uint32_t idx = kv_base + waited;
+                if (!warp_wait(bar(sm.kv_full[idx % kStages]), (idx / kStages) & 1, cx.wc, W_KV_FULL))
+                    return false;
+                ++waited;
+            }
+            ptx::tc_fence_after();
+            return true;
+        };
+
+        for (int j = lo; j < hi && ok; ++j) {
+            // slots whose range starts at this tile get their first S here
 #pragma unroll
             for (int t = 0; t < 2; ++t) {
-                if (!it.valid[t])
-                    continue;
-                if (j - 1 >= lo_t[t] && j - 1 < hi_t[t]) {
-                    ok = warp_wait(bar(sm.p_full[t]), pcount[t] & 1, cx.wc, W_P_FULL);
-                    if (!ok)
+                if (it.valid[t] && lo_t[t] == j) {
+                    if (!(ok = need_tile(j)))
                         break;
-                    ++pcount[t];
-                    ptx::tc_fence_after();
-                    if (lane == 0) {
-                        const uint32_t vbase = ptx::smem_u32(sm.v[prev_stage]);
-#pragma unroll
-                        for (int kk = 0; kk < BN / 16; ++kk)
-                            ptx::mma_ts(cx.tmem + kColO + 64 * t, cx.tmem + kColP + 64 * t + 8 * kk,
-                                        umma_desc(vbase + kk * 2048, kTileBytes, 1024, kSwizzle128B),
-                                        idesc_pv, (j - 1 > lo_t[t] || kk > 0) ? 1u : 0u);
-                        if (j == hi_t[t])
-                            ptx::mma_commit(bar(sm.o_full[t]));
-                    }
-                    __syncwarp();
-                }
-                if (j < hi && j >= lo_t[t] && j < hi_t[t]) {
-                    if (lane == 0) {
-                        const uint32_t qbase = ptx::smem_u32(sm.q[t]);
-                        const uint32_t kbase = ptx::smem_u32(sm.k[stage]);
-#pragma unroll
-                        for (int kk = 0; kk < 64 / 16; ++kk)
-                            ptx::mma_ss(cx.tmem + kColS + 128 * t,
-                                        umma_desc(qbase + kk * 32, 16, 1024, kSwizzle128B),
-                                        umma_desc(kbase + kk * 32, 16, 1024, kSwizzle128B),
-                                        idesc_qk, kk > 0 ? 1u : 0u);
-                        ptx::mma_commit(bar(sm.s_full[t]));
-                    }
-                    __syncwarp();
+                    issue_s(t, j);
                 }
             }
             if (!ok)
                 break;
-            if (lane == 0) {
-                if (j > lo)
-                    ptx::mma_commit(bar(sm.kv_empty[prev_stage]));
-                if (j == hi - 1)
-                    ptx::mma_commit(bar(sm.q_empty));
+#pragma unroll
+            for (int t = 0; t < 2; ++t) {
+                if (!it.valid[t] || j < lo_t[t] || j >= hi_t[t])
+                    continue;
+                ok = warp_wait(bar(sm.p_full[t]), pcount[t] & 1, cx.wc, W_P_FULL);
+                if (!ok)
+                    break;
+                ++pcount[t];
+                ptx::tc_fence_after();
+                if (j + 1 < hi_t[t]) {
+                    if (!(ok = need_tile(j + 1)))
+                        break;
+                    issue_s(t, j + 1);
+                }
+                if (lane == 0) {
+                    const uint32_t vbase = ptx::smem_u32(sm.v[(kv_base + (j - lo)) % kStages]);
+#pragma unroll
+                    for (int kk = 0; kk < BN / 16; ++kk)
+                        ptx::mma_ts(cx.tmem + kColO + 64 * t, cx.tmem + kColP + 64 * t + 8 * kk,
+                                    umma_desc(vbase + kk * 2048, kTileBytes, 1024, kSwizzle128B),
+                                    idesc_pv, (j > lo_t[t] || kk > 0) ? 1u : 0u);
+                    ptx::mma_commit(bar(sm.pv_done[t]));
+                }
+                __syncwarp();
             }
+            if (!ok)
+                break;
+            // every S and P V reading key tile j has been issued
+            if (lane == 0)
+                ptx::mma_commit(bar(sm.kv_empty[(kv_base + (j - lo)) % kStages]));
             __syncwarp();
-            if (j < hi) {
-                prev_stage = stage;
-                ++kv_count;
-            }
         }
+        kv_base += static_cast<uint32_t>(hi - lo);
         ++item_count;
     }
     // Every MMA this thread issued has completed before TMEM is released.
@@ -256,7 +284,7 @@ __device__ void softmax_role(const KernelCtx &cx, const StdParams &p, int t)
     const uint32_t tS = cx.tmem + lane_off + kColS + 128 * t;
     const uint32_t tO = cx.tmem + lane_off + kColO + 64 * t;
     const uint32_t tP = cx.tmem + lane_off + kColP + 64 * t;
-    uint32_t scount = 0, ocount = 0;
+    uint32_t scount = 0, pvcount = 0;
 
     for (int64_t L = blockIdx.x; L < p.grid.n_items; L += gridDim.x) {
         const Item it = decode_item(p.grid, L);
@@ -292,16 +320,29 @@ __device__ void softmax_role(const KernelCtx &cx, const StdParams &p, int t)
             apply_score_mod<MOD>(x, smod, i, j0);
             if (!((j0 >= tr.full_lo) && (j0 + BN <= tr.full_hi)))
                 apply_row_mask(x, j0, row_lo, row_hi);
-            online_update_and_store_p<64>(x, MOD == MOD_NONE ? p.qk_log2 : 1.f, st, j == tr.lo, tO, tP);
+            uint32_t pk[BN / 2];
+            bool rescale;
+            const float alpha =
+                softmax_compute_p(x, MOD == MOD_NONE ? p.qk_log2 : 1.f, st, j == tr.lo, pk, rescale);
+            if (j > tr.lo) {
+                // the previous tile's P V has consumed P[t] and landed in O[t]
+                if (!warp_wait(bar(sm.pv_done[t]), pvcount & 1, cx.wc, W_O_FULL))
+                    return;
+                ++pvcount;
+                ptx::tc_fence_after();
+                if (rescale)
+                    rescale_o<64>(tO, alpha);
+            }
+            store_p(tP, pk);
             ptx::tc_fence_before();
             ptx::mbar_arrive(bar(sm.p_full[t]));
             ++ntiles;
         }
 
         // epilogue: O / l -> bf16, LSE
-        if (!warp_wait(bar(sm.o_full[t]), ocount & 1, cx.wc, W_O_FULL))
+        if (!warp_wait(bar(sm.pv_done[t]), pvcount & 1, cx.wc, W_O_FULL))
             return;
-        ++ocount;
+        ++pvcount;
         ptx::tc_fence_after();
         uint32_t o[64];
         ptx::tmem_ld32(tO, o);
@@ -341,8 +382,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int warp = threadIdx.x >> 5;
 
     if (threadIdx.x == 0) {
-        ptx::mbar_init(bar(sm->q_full), 1);
-        ptx::mbar_init(bar(sm->q_empty), 1);
+        for (int b = 0; b < 2; ++b) {
+            ptx::mbar_init(bar(sm->q_full[b]), 1);
+            ptx::mbar_init(bar(sm->q_empty[b]), 1);
+        }
         for (int s = 0; s < kStages; ++s) {
             ptx::mbar_init(bar(sm->kv_full[s]), 1);
             ptx::mbar_init(bar(sm->kv_empty[s]), 1);
@@ -350,7 +393,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int t = 0; t < 2; ++t) {
             ptx::mbar_init(bar(sm->s_full[t]), 1);
             ptx::mbar_init(bar(sm->p_full[t]), 128);
-            ptx::mbar_init(bar(sm->o_full[t]), 1);
+            ptx::mbar_init(bar(sm->pv_done[t]), 1);
         }
         ptx::mbar_init(bar(sm->final_bar), 1);
         sm->abort_flag = 0;
