@@ -185,21 +185,25 @@ __device__ __forceinline__ Item decode_item(const GridSpec &g, int64_t L)
 // own copies in flight, TMEM release) instead of hanging.
 struct WaitCtl {
     volatile uint32_t *abort_flag; // shared memory
-    uint64_t timeout_ns;
+    uint64_t timeout_cycles;
     uint32_t *err_user;            // may be null
     uint32_t *err_lib;             // the library's own word
 };
 
-static __device__ __forceinline__ bool mbar_wait_slow(uint32_t bar, uint32_t parity, const WaitCtl &c,
-                                            uint32_t where, bool honour_abort)
+static __device__ __forceinline__ bool mbar_wait_slow(uint32_t bar, uint32_t parity,
+                                                      const WaitCtl &c, uint32_t where,
+                                                      bool honour_abort)
 {
-    const uint64_t t0 = ptx::globaltimer_ns();
+    // The bound is kept in SM clock cycles (clock64 is a cheap register read;
+    // the global timer is not): timeout_cycles assumes the maximum SM clock,
+    // so at lower clocks the wait only lasts longer in wall time.
+    const long long t0 = clock64();
     for (uint32_t n = 1;; ++n) {
         if (ptx::mbar_try_wait(bar, parity))
             return true;
         if (honour_abort && *c.abort_flag)
             return false;
-        if ((n & 63u) == 0 && ptx::globaltimer_ns() - t0 > c.timeout_ns) {
+        if ((n & 15u) == 0 && static_cast<uint64_t>(clock64() - t0) > c.timeout_cycles) {
             *c.abort_flag = 1u;
             const uint32_t code = 0x1u | ((where & 0xFFu) << 8);
             if (c.err_user)

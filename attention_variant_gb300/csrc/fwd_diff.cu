@@ -346,7 +346,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     cx.sm = sm;
     cx.tmem = sm->tmem_base;
     cx.wc.abort_flag = &sm->abort_flag;
-    cx.wc.timeout_ns = p.timeout_ns;
+    cx.wc.timeout_cycles = p.timeout_ns * 21 / 10; // 2.1 cycles per ns at the maximum clock
     cx.wc.err_user = p.err_user;
     cx.wc.err_lib = &g_lib_error_word;
     if (warp < 8) {

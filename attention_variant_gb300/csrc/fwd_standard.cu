@@ -50,8 +50,8 @@ namespace {
 
 constexpr int kThreads = 384;
 constexpr uint32_t kRegsLaunch = 168;
-constexpr uint32_t kRegsSoftmax = 208;
-constexpr uint32_t kRegsOther = 88;
+constexpr uint32_t kRegsSoftmax = 200;
+constexpr uint32_t kRegsOther = 104;
 static_assert(2 * 128 * kRegsSoftmax + 128 * kRegsOther == kThreads * kRegsLaunch,
               "register split must equal the launch allocation");
 constexpr int kStages = 4;
@@ -155,104 +155,132 @@ __device__ void producer_role(const KernelCtx &cx, const StdParams &p, const CUt
 }
 
 // ------------------------------------------------------------------ MMA issuer
+
+// Waits until the item's key tiles 0 .. rel (relative to the item's first
+// tile) have landed; `waited` counts the tiles already waited for.
+__device__ __forceinline__ bool wait_kv_tiles(const KernelCtx &cx, uint32_t bar_kvf0,
+                                              uint32_t kv_base, int rel, int &waited)
+{
+    while (waited <= rel) {
+        const uint32_t idx = kv_base + static_cast<uint32_t>(waited);
+        if (!warp_wait(bar_kvf0 + (idx % kStages) * static_cast<uint32_t>(sizeof(uint64_t)),
+                       (idx / kStages) & 1, cx.wc, W_KV_FULL))
+            return false;
+        ++waited;
+    }
+    return true;
+}
+
+//
+// One thread issues every MMA.  The loop keeps all of its state in registers
+// and builds descriptors as (constant high word) | (14-bit start address),
+// so an MMA issues in a few instructions and the tensor core is never left
+// waiting for its issuer.
 __device__ void mma_role(const KernelCtx &cx, const StdParams &p)
 {
     StdSmem &sm = *cx.sm;
     const uint32_t lane = ptx::lane_id();
     constexpr uint32_t idesc_qk = umma_idesc_bf16(BM, BN, false);
     constexpr uint32_t idesc_pv = umma_idesc_bf16(BM, 64, true);
-    uint32_t kv_base = 0, item_count = 0;
-    uint32_t pcount[2] = {0, 0};
-    bool ok = true;
+    constexpr uint64_t kHiK = umma_desc_hi(16, 1024, kSwizzle128B);          // Q, K: K-major
+    constexpr uint64_t kHiV = umma_desc_hi(kTileBytes, 1024, kSwizzle128B);  // V: MN-major
+    // start-address fields (address >> 4) of every tile
+    const uint32_t q_lo0 = ptx::smem_u32(sm.q[0][0]) >> 4;
+    const uint32_t k_lo0 = ptx::smem_u32(sm.k[0]) >> 4;
+    const uint32_t v_lo0 = ptx::smem_u32(sm.v[0]) >> 4;
+    constexpr uint32_t kTileLo = kTileBytes >> 4;
+    const uint32_t tS0 = cx.tmem + kColS, tO0 = cx.tmem + kColO, tP0 = cx.tmem + kColP;
+    const uint32_t bar_s0 = bar(sm.s_full[0]), bar_p0 = bar(sm.p_full[0]);
+    const uint32_t bar_pv0 = bar(sm.pv_done[0]);
+    const uint32_t bar_kvf0 = bar(sm.kv_full[0]), bar_kve0 = bar(sm.kv_empty[0]);
+    constexpr uint32_t kBarStride = sizeof(uint64_t);
 
+    uint32_t kv_base = 0, item_count = 0, pc0 = 0, pc1 = 0;
+    bool ok = true;
     for (int64_t L = blockIdx.x; L < p.grid.n_items && ok; L += gridDim.x) {
         const Item it = decode_item(p.grid, L);
-        int lo_t[2], hi_t[2];
-        int lo = 1 << 30, hi = 0, s_total = 0;
-#pragma unroll
-        for (int t = 0; t < 2; ++t) {
-            lo_t[t] = hi_t[t] = 0;
-            if (!it.valid[t])
-                continue;
-            const TileRange r = q_block_range(p.mask, it.b, it.qb[t] * BM);
-            lo_t[t] = r.lo;
-            hi_t[t] = r.hi;
-            lo = min(lo, r.lo);
-            hi = max(hi, r.hi);
-            s_total += r.hi - r.lo;
+        int lo0 = 0, hi0 = 0, lo1 = 0, hi1 = 0;
+        if (it.valid[0]) {
+            const TileRange r = q_block_range(p.mask, it.b, it.qb[0] * BM);
+            lo0 = r.lo;
+            hi0 = r.hi;
         }
+        if (it.valid[1]) {
+            const TileRange r = q_block_range(p.mask, it.b, it.qb[1] * BM);
+            lo1 = r.lo;
+            hi1 = r.hi;
+        }
+        const int lo = it.valid[0] ? (it.valid[1] ? min(lo0, lo1) : lo0) : lo1;
+        const int hi = max(hi0, hi1);
+        const int s_total = (hi0 - lo0) + (hi1 - lo1);
         const uint32_t qbuf = item_count & 1;
         ok = warp_wait(bar(sm.q_full[qbuf]), (item_count >> 1) & 1, cx.wc, W_Q_FULL);
         if (!ok)
             break;
         ptx::tc_fence_after();
+        const uint32_t qlo = q_lo0 + qbuf * 2 * kTileLo;
+        const uint32_t bar_qe = bar(sm.q_empty[qbuf]);
         int s_issued = 0;
-        uint32_t waited = 0; // ring entries of this item whose kv_full has been waited
-
-        // S[t] = Q[t] K_j^T for key tile j (its ring entry already waited)
-        auto issue_s = [&](int t, int j) {
-            const uint32_t stage = (kv_base + (j - lo)) % kStages;
-            if (lane == 0) {
-                const uint32_t qbase = ptx::smem_u32(sm.q[qbuf][t]);
-                const uint32_t kbase = ptx::smem_u32(sm.k[stage]);
-#pragma unroll
-                for (int kk = 0; kk < 64 / 16; ++kk)
-                    ptx::mma_ss(cx.tmem + kColS + 128 * t,
-                                umma_desc(qbase + kk * 32, 16, 1024, kSwizzle128B),
-                                umma_desc(kbase + kk * 32, 16, 1024, kSwizzle128B), idesc_qk,
-                                kk > 0 ? 1u : 0u);
-                ptx::mma_commit(bar(sm.s_full[t]));
-                if (++s_issued == s_total)
-                    ptx::mma_commit(bar(sm.q_empty[qbuf])); // last read of this Q buffer
-            }
-            __syncwarp();
-        };
-        // make sure key tile j's K/V have landed
-        auto need_tile = [&](int j) -> bool {
-            while (waited <= static_cast<uint32_t>(j - lo)) {
-                const uint32_t idx = kv_base + waited;
-                if (!warp_wait(bar(sm.kv_full[idx % kStages]), (idx / kStages) & 1, cx.wc, W_KV_FULL))
-                    return false;
-                ++waited;
-            }
-            ptx::tc_fence_after();
-            return true;
-        };
+        int waited = 0; // tiles lo .. lo + waited - 1 of this item have landed
 
         for (int j = lo; j < hi && ok; ++j) {
-            // slots whose range starts at this tile get their first S here
+            // phase A: the first S of every slot whose range starts at tile j
 #pragma unroll
             for (int t = 0; t < 2; ++t) {
-                if (it.valid[t] && lo_t[t] == j) {
-                    if (!(ok = need_tile(j)))
-                        break;
-                    issue_s(t, j);
+                const int lot = t ? lo1 : lo0;
+                if (!it.valid[t] || j != lot)
+                    continue;
+                if (!(ok = wait_kv_tiles(cx, bar_kvf0, kv_base, j - lo, waited)))
+                    break;
+                if (lane == 0) {
+                    const uint32_t klo = k_lo0 + ((kv_base + (j - lo)) % kStages) * kTileLo;
+#pragma unroll
+                    for (int kk = 0; kk < 4; ++kk)
+                        ptx::mma_ss(tS0 + 128 * t, kHiK | (qlo + t * kTileLo + 2 * kk),
+                                    kHiK | (klo + 2 * kk), idesc_qk, kk > 0 ? 1u : 0u);
+                    ptx::mma_commit(bar_s0 + t * kBarStride);
+                    if (++s_issued == s_total)
+                        ptx::mma_commit(bar_qe);
                 }
+                __syncwarp();
             }
             if (!ok)
                 break;
+            // phase B: per active slot, once its softmax of tile j is done,
+            // the next S and then this tile's P V
 #pragma unroll
             for (int t = 0; t < 2; ++t) {
-                if (!it.valid[t] || j < lo_t[t] || j >= hi_t[t])
+                const int lot = t ? lo1 : lo0, hit = t ? hi1 : hi0;
+                if (!it.valid[t] || j < lot || j >= hit)
                     continue;
-                ok = warp_wait(bar(sm.p_full[t]), pcount[t] & 1, cx.wc, W_P_FULL);
+                ok = warp_wait(bar_p0 + t * kBarStride, (t ? pc1 : pc0) & 1, cx.wc, W_P_FULL);
                 if (!ok)
                     break;
-                ++pcount[t];
+                if (t)
+                    ++pc1;
+                else
+                    ++pc0;
+                const bool next = j + 1 < hit;
+                if (next && !(ok = wait_kv_tiles(cx, bar_kvf0, kv_base, j + 1 - lo, waited)))
+                    break;
                 ptx::tc_fence_after();
-                if (j + 1 < hi_t[t]) {
-                    if (!(ok = need_tile(j + 1)))
-                        break;
-                    issue_s(t, j + 1);
-                }
                 if (lane == 0) {
-                    const uint32_t vbase = ptx::smem_u32(sm.v[(kv_base + (j - lo)) % kStages]);
+                    if (next) {
+                        const uint32_t klo = k_lo0 + ((kv_base + (j + 1 - lo)) % kStages) * kTileLo;
+#pragma unroll
+                        for (int kk = 0; kk < 4; ++kk)
+                            ptx::mma_ss(tS0 + 128 * t, kHiK | (qlo + t * kTileLo + 2 * kk),
+                                        kHiK | (klo + 2 * kk), idesc_qk, kk > 0 ? 1u : 0u);
+                        ptx::mma_commit(bar_s0 + t * kBarStride);
+                        if (++s_issued == s_total)
+                            ptx::mma_commit(bar_qe);
+                    }
+                    const uint32_t vlo = v_lo0 + ((kv_base + (j - lo)) % kStages) * kTileLo;
 #pragma unroll
                     for (int kk = 0; kk < BN / 16; ++kk)
-                        ptx::mma_ts(cx.tmem + kColO + 64 * t, cx.tmem + kColP + 64 * t + 8 * kk,
-                                    umma_desc(vbase + kk * 2048, kTileBytes, 1024, kSwizzle128B),
-                                    idesc_pv, (j > lo_t[t] || kk > 0) ? 1u : 0u);
-                    ptx::mma_commit(bar(sm.pv_done[t]));
+                        ptx::mma_ts(tO0 + 64 * t, tP0 + 64 * t + 8 * kk, kHiV | (vlo + 128 * kk),
+                                    idesc_pv, (j > lot || kk > 0) ? 1u : 0u);
+                    ptx::mma_commit(bar_pv0 + t * kBarStride);
                 }
                 __syncwarp();
             }
@@ -260,7 +288,7 @@ __device__ void mma_role(const KernelCtx &cx, const StdParams &p)
                 break;
             // every S and P V reading key tile j has been issued
             if (lane == 0)
-                ptx::mma_commit(bar(sm.kv_empty[(kv_base + (j - lo)) % kStages]));
+                ptx::mma_commit(bar_kve0 + ((kv_base + (j - lo)) % kStages) * kBarStride);
             __syncwarp();
         }
         kv_base += static_cast<uint32_t>(hi - lo);
@@ -417,7 +445,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     cx.sm = sm;
     cx.tmem = sm->tmem_base;
     cx.wc.abort_flag = &sm->abort_flag;
-    cx.wc.timeout_ns = p.timeout_ns;
+    cx.wc.timeout_cycles = p.timeout_ns * 21 / 10; // 2.1 cycles per ns at the maximum clock
     cx.wc.err_user = p.err_user;
     cx.wc.err_lib = &g_lib_error_word;
 
