@@ -183,6 +183,10 @@ __device__ __forceinline__ Item decode_item(const GridSpec &g, int64_t L)
 // the error word(s); every other wait in the CTA then returns false at once,
 // each role leaves its loop, and the CTA reaches its teardown (drain of its
 // own copies in flight, TMEM release) instead of hanging.
+// A blocked waiter sleeps in hardware for at most this long between checks of
+// the abort flag and the timeout (the phase completing wakes it at once).
+constexpr uint32_t kWaitSuspendNs = 20000;
+
 struct WaitCtl {
     volatile uint32_t *abort_flag; // shared memory
     uint64_t timeout_cycles;
@@ -199,11 +203,11 @@ static __device__ __forceinline__ bool mbar_wait_slow(uint32_t bar, uint32_t par
     // so at lower clocks the wait only lasts longer in wall time.
     const long long t0 = clock64();
     for (uint32_t n = 1;; ++n) {
-        if (ptx::mbar_try_wait(bar, parity))
+        if (ptx::mbar_try_wait_sleep(bar, parity, kWaitSuspendNs))
             return true;
         if (honour_abort && *c.abort_flag)
             return false;
-        if ((n & 15u) == 0 && static_cast<uint64_t>(clock64() - t0) > c.timeout_cycles) {
+        if (static_cast<uint64_t>(clock64() - t0) > c.timeout_cycles) {
             *c.abort_flag = 1u;
             const uint32_t code = 0x1u | ((where & 0xFFu) << 8);
             if (c.err_user)

@@ -27,17 +27,17 @@
 //   384 + 64 t, for slots t = 0, 1.
 //
 // Hand-off protocol for slot t and key tile j (all mbarriers):
-//   MMA:     wait p_full(t) [P(t, j) written, O(t) rescaled]; issue
-//            S[t] = Q[t] K_{j+1}^T and commit s_full(t); then issue
-//            O[t] += P[t] V_j and commit pv_done(t).
-//   softmax: wait s_full(t); S[t] -> registers; score_mod, mask, row max,
-//            P in registers; wait pv_done(t) [the P V of tile j-1 has read
-//            P[t] and landed in O[t]]; lazily rescale O[t]; P -> TMEM; arrive
-//            p_full(t).
-// Issuing the next QK^T before the current P V lets the softmax of tile j+1
-// start after one MMA instead of two, and P has its own columns so the next
-// S never overwrites a P still being read.  Q is double-buffered across work
-// items so the next item's Q arrives while the current one finishes.
+//   softmax: wait s_full(t); S[t] -> registers; arrive s_free(t);
+//            score_mod, mask, row max, P in registers; wait pv_done(t) [the
+//            P V of tile j-1 has read P[t] and landed in O[t]]; lazily rescale
+//            O[t]; P -> TMEM; arrive p_full(t).
+//   MMA:     wait s_free(t), issue S[t] = Q[t] K_{j+1}^T, commit s_full(t);
+//            later wait p_full(t), issue O[t] += P[t] V_j, commit pv_done(t).
+// The next QK^T starts as soon as the softmax has copied the scores out of
+// TMEM, so its latency hides behind the exponentials, and P has its own TMEM
+// columns so the next S never overwrites a P still being read.  Q is
+// double-buffered across work items so the next item's Q arrives while the
+// current one finishes.
 #include <cuda_bf16.h>
 #include <cstdint>
 
@@ -64,7 +64,7 @@ struct __align__(1024) StdSmem {
     uint8_t v[kStages][kTileBytes];
     uint64_t q_full[2], q_empty[2];
     uint64_t kv_full[kStages], kv_empty[kStages];
-    uint64_t s_full[2], p_full[2], pv_done[2];
+    uint64_t s_full[2], s_free[2], p_full[2], pv_done[2];
     uint64_t final_bar;
     uint32_t tmem_base;
     uint32_t abort_flag;
@@ -191,11 +191,12 @@ __device__ void mma_role(const KernelCtx &cx, const StdParams &p)
     constexpr uint32_t kTileLo = kTileBytes >> 4;
     const uint32_t tS0 = cx.tmem + kColS, tO0 = cx.tmem + kColO, tP0 = cx.tmem + kColP;
     const uint32_t bar_s0 = bar(sm.s_full[0]), bar_p0 = bar(sm.p_full[0]);
+    const uint32_t bar_sf0 = bar(sm.s_free[0]);
     const uint32_t bar_pv0 = bar(sm.pv_done[0]);
     const uint32_t bar_kvf0 = bar(sm.kv_full[0]), bar_kve0 = bar(sm.kv_empty[0]);
     constexpr uint32_t kBarStride = sizeof(uint64_t);
 
-    uint32_t kv_base = 0, item_count = 0, pc0 = 0, pc1 = 0;
+    uint32_t kv_base = 0, item_count = 0, pc0 = 0, pc1 = 0, fc0 = 0, fc1 = 0;
     bool ok = true;
     for (int64_t L = blockIdx.x; L < p.grid.n_items && ok; L += gridDim.x) {
         const Item it = decode_item(p.grid, L);
@@ -246,8 +247,40 @@ __device__ void mma_role(const KernelCtx &cx, const StdParams &p)
             }
             if (!ok)
                 break;
-            // phase B: per active slot, once its softmax of tile j is done,
-            // the next S and then this tile's P V
+            // phase B1: once the softmax has copied S(t, j) out of TMEM, the next S
+#pragma unroll
+            for (int t = 0; t < 2; ++t) {
+                const int lot = t ? lo1 : lo0, hit = t ? hi1 : hi0;
+                if (!it.valid[t] || j < lot || j >= hit)
+                    continue;
+                ok = warp_wait(bar_sf0 + t * kBarStride, (t ? fc1 : fc0) & 1, cx.wc, W_S_FULL);
+                if (!ok)
+                    break;
+                if (t)
+                    ++fc1;
+                else
+                    ++fc0;
+                if (j + 1 >= hit)
+                    continue;
+                if (!(ok = wait_kv_tiles(cx, bar_kvf0, kv_base, j + 1 - lo, waited)))
+                    break;
+                ptx::tc_fence_after();
+                if (lane == 0) {
+                    const uint32_t klo = k_lo0 + ((kv_base + (j + 1 - lo)) % kStages) * kTileLo;
+#pragma unroll
+                    for (int kk = 0; kk < 4; ++kk)
+                        ptx::mma_ss(tS0 + 128 * t, kHiK | (qlo + t * kTileLo + 2 * kk),
+                                    kHiK | (klo + 2 * kk), idesc_qk, kk > 0 ? 1u : 0u);
+                    ptx::mma_commit(bar_s0 + t * kBarStride);
+                    if (++s_issued == s_total)
+                        ptx::mma_commit(bar_qe);
+                }
+                __syncwarp();
+            }
+            if (!ok)
+                break;
+            // phase B2: once the softmax of (t, j) has written P and rescaled O,
+            // this tile's P V
 #pragma unroll
             for (int t = 0; t < 2; ++t) {
                 const int lot = t ? lo1 : lo0, hit = t ? hi1 : hi0;
@@ -260,21 +293,8 @@ __device__ void mma_role(const KernelCtx &cx, const StdParams &p)
                     ++pc1;
                 else
                     ++pc0;
-                const bool next = j + 1 < hit;
-                if (next && !(ok = wait_kv_tiles(cx, bar_kvf0, kv_base, j + 1 - lo, waited)))
-                    break;
                 ptx::tc_fence_after();
                 if (lane == 0) {
-                    if (next) {
-                        const uint32_t klo = k_lo0 + ((kv_base + (j + 1 - lo)) % kStages) * kTileLo;
-#pragma unroll
-                        for (int kk = 0; kk < 4; ++kk)
-                            ptx::mma_ss(tS0 + 128 * t, kHiK | (qlo + t * kTileLo + 2 * kk),
-                                        kHiK | (klo + 2 * kk), idesc_qk, kk > 0 ? 1u : 0u);
-                        ptx::mma_commit(bar_s0 + t * kBarStride);
-                        if (++s_issued == s_total)
-                            ptx::mma_commit(bar_qe);
-                    }
                     const uint32_t vlo = v_lo0 + ((kv_base + (j - lo)) % kStages) * kTileLo;
 #pragma unroll
                     for (int kk = 0; kk < BN / 16; ++kk)
@@ -344,6 +364,8 @@ __device__ void softmax_role(const KernelCtx &cx, const StdParams &p, int t)
             ptx::tc_fence_after();
             float x[BN];
             load_scores(tS, x);
+            ptx::tc_fence_before();
+            ptx::mbar_arrive(bar(sm.s_free[t])); // S[t] may be overwritten
             const int j0 = j * BN;
             apply_score_mod<MOD>(x, smod, i, j0);
             if (!((j0 >= tr.full_lo) && (j0 + BN <= tr.full_hi)))
@@ -421,6 +443,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int t = 0; t < 2; ++t) {
             ptx::mbar_init(bar(sm->s_full[t]), 1);
             ptx::mbar_init(bar(sm->p_full[t]), 128);
+            ptx::mbar_init(bar(sm->s_free[t]), 128);
             ptx::mbar_init(bar(sm->pv_done[t]), 1);
         }
         ptx::mbar_init(bar(sm->final_bar), 1);
