@@ -13,8 +13,9 @@
 //   warps 4-7  softmax warpgroup of slot 1
 //   warp  8    TMA producer: Q tiles once per work item, K/V tiles through an
 //              NS-stage mbarrier ring
-//   warp  9    MMA issuer (one thread) and TMEM owner
-//   warps 10-11 idle (they complete the third warpgroup)
+//   warp  9    MMA issuer of slot 0 (one thread) and TMEM owner
+//   warp  10   MMA issuer of slot 1
+//   warp  11   idle (it completes the third warpgroup)
 // The kernel is compiled for 168 registers per thread; after set-up the two
 // softmax warpgroups raise their limit to kRegsSoftmax and the third lowers
 // its own to kRegsOther, with 2*128*kRegsSoftmax + 128*kRegsOther equal to
@@ -65,7 +66,7 @@ struct __align__(1024) StdSmem {
     uint64_t q_full[2], q_empty[2];
     uint64_t kv_full[kStages], kv_empty[kStages];
     uint64_t s_full[2], s_free[2], p_full[2], pv_done[2];
-    uint64_t final_bar;
+    uint64_t final_bar[2];
     uint32_t tmem_base;
     uint32_t abort_flag;
 };
@@ -154,10 +155,15 @@ __device__ void producer_role(const KernelCtx &cx, const StdParams &p, const CUt
     }
 }
 
-// ------------------------------------------------------------------ MMA issuer
-
-// Waits until the item's key tiles 0 .. rel (relative to the item's first
-// tile) have landed; `waited` counts the tiles already waited for.
+// ------------------------------------------------------------------ MMA issuers
+//
+// Two MMA warps, one per slot, so each slot's S -> softmax -> P V chain moves
+// independently and the tensor core interleaves the two.  Each keeps its state
+// in registers and builds descriptors as (constant high word) | (14-bit start
+// address).  kv_empty and q_empty take one arrival from each warp: a warp
+// commits after its last MMA reading the tile (or Q buffer), or -- for a tile
+// its slot does not use -- arrives once the tile has landed, which proves the
+// stage's previous phase is complete.
 __device__ __forceinline__ bool wait_kv_tiles(const KernelCtx &cx, uint32_t bar_kvf0,
                                               uint32_t kv_base, int rel, int &waited)
 {
@@ -171,12 +177,7 @@ __device__ __forceinline__ bool wait_kv_tiles(const KernelCtx &cx, uint32_t bar_
     return true;
 }
 
-//
-// One thread issues every MMA.  The loop keeps all of its state in registers
-// and builds descriptors as (constant high word) | (14-bit start address),
-// so an MMA issues in a few instructions and the tensor core is never left
-// waiting for its issuer.
-__device__ void mma_role(const KernelCtx &cx, const StdParams &p)
+__device__ void mma_role(const KernelCtx &cx, const StdParams &p, int t)
 {
     StdSmem &sm = *cx.sm;
     const uint32_t lane = ptx::lane_id();
@@ -184,141 +185,126 @@ __device__ void mma_role(const KernelCtx &cx, const StdParams &p)
     constexpr uint32_t idesc_pv = umma_idesc_bf16(BM, 64, true);
     constexpr uint64_t kHiK = umma_desc_hi(16, 1024, kSwizzle128B);          // Q, K: K-major
     constexpr uint64_t kHiV = umma_desc_hi(kTileBytes, 1024, kSwizzle128B);  // V: MN-major
-    // start-address fields (address >> 4) of every tile
-    const uint32_t q_lo0 = ptx::smem_u32(sm.q[0][0]) >> 4;
+    constexpr uint32_t kTileLo = kTileBytes >> 4;
+    constexpr uint32_t kBarStride = sizeof(uint64_t);
+    const uint32_t q_lo0 = ptx::smem_u32(sm.q[0][t]) >> 4;
     const uint32_t k_lo0 = ptx::smem_u32(sm.k[0]) >> 4;
     const uint32_t v_lo0 = ptx::smem_u32(sm.v[0]) >> 4;
-    constexpr uint32_t kTileLo = kTileBytes >> 4;
-    const uint32_t tS0 = cx.tmem + kColS, tO0 = cx.tmem + kColO, tP0 = cx.tmem + kColP;
-    const uint32_t bar_s0 = bar(sm.s_full[0]), bar_p0 = bar(sm.p_full[0]);
-    const uint32_t bar_sf0 = bar(sm.s_free[0]);
-    const uint32_t bar_pv0 = bar(sm.pv_done[0]);
-    const uint32_t bar_kvf0 = bar(sm.kv_full[0]), bar_kve0 = bar(sm.kv_empty[0]);
-    constexpr uint32_t kBarStride = sizeof(uint64_t);
+    const uint32_t tS = cx.tmem + kColS + 128 * t, tO = cx.tmem + kColO + 64 * t;
+    const uint32_t tP = cx.tmem + kColP + 64 * t;
+    const uint32_t b_sfull = bar(sm.s_full[t]), b_sfree = bar(sm.s_free[t]);
+    const uint32_t b_pfull = bar(sm.p_full[t]), b_pvdone = bar(sm.pv_done[t]);
+    const uint32_t b_kvf0 = bar(sm.kv_full[0]), b_kve0 = bar(sm.kv_empty[0]);
 
-    uint32_t kv_base = 0, item_count = 0, pc0 = 0, pc1 = 0, fc0 = 0, fc1 = 0;
+    uint32_t kv_base = 0, item_count = 0, fcount = 0, pcount = 0;
     bool ok = true;
     for (int64_t L = blockIdx.x; L < p.grid.n_items && ok; L += gridDim.x) {
         const Item it = decode_item(p.grid, L);
-        int lo0 = 0, hi0 = 0, lo1 = 0, hi1 = 0;
-        if (it.valid[0]) {
-            const TileRange r = q_block_range(p.mask, it.b, it.qb[0] * BM);
-            lo0 = r.lo;
-            hi0 = r.hi;
+        int lo = 1 << 30, hi = 0, lot = 0, hit = 0;
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+            if (!it.valid[u])
+                continue;
+            const TileRange r = q_block_range(p.mask, it.b, it.qb[u] * BM);
+            lo = min(lo, r.lo);
+            hi = max(hi, r.hi);
+            if (u == t) {
+                lot = r.lo;
+                hit = r.hi;
+            }
         }
-        if (it.valid[1]) {
-            const TileRange r = q_block_range(p.mask, it.b, it.qb[1] * BM);
-            lo1 = r.lo;
-            hi1 = r.hi;
-        }
-        const int lo = it.valid[0] ? (it.valid[1] ? min(lo0, lo1) : lo0) : lo1;
-        const int hi = max(hi0, hi1);
-        const int s_total = (hi0 - lo0) + (hi1 - lo1);
+        const bool active = it.valid[t];
         const uint32_t qbuf = item_count & 1;
+        const uint32_t b_qe = bar(sm.q_empty[qbuf]);
         ok = warp_wait(bar(sm.q_full[qbuf]), (item_count >> 1) & 1, cx.wc, W_Q_FULL);
         if (!ok)
             break;
         ptx::tc_fence_after();
         const uint32_t qlo = q_lo0 + qbuf * 2 * kTileLo;
-        const uint32_t bar_qe = bar(sm.q_empty[qbuf]);
-        int s_issued = 0;
-        int waited = 0; // tiles lo .. lo + waited - 1 of this item have landed
+        int waited = 0;
 
         for (int j = lo; j < hi && ok; ++j) {
-            // phase A: the first S of every slot whose range starts at tile j
-#pragma unroll
-            for (int t = 0; t < 2; ++t) {
-                const int lot = t ? lo1 : lo0;
-                if (!it.valid[t] || j != lot)
-                    continue;
-                if (!(ok = wait_kv_tiles(cx, bar_kvf0, kv_base, j - lo, waited)))
+            const uint32_t stage_j = (kv_base + (j - lo)) % kStages;
+            if (!active || j < lot || j >= hit) {
+                // tile not used by this slot: release it once it has landed
+                if (!(ok = wait_kv_tiles(cx, b_kvf0, kv_base, j - lo, waited)))
                     break;
+                if (lane == 0)
+                    ptx::mbar_arrive(b_kve0 + stage_j * kBarStride);
+                __syncwarp();
+                continue;
+            }
+            if (j == lot) {
+                // first S of the item for this slot
+                if (!(ok = wait_kv_tiles(cx, b_kvf0, kv_base, j - lo, waited)))
+                    break;
+                ptx::tc_fence_after();
                 if (lane == 0) {
-                    const uint32_t klo = k_lo0 + ((kv_base + (j - lo)) % kStages) * kTileLo;
+                    const uint32_t klo = k_lo0 + stage_j * kTileLo;
 #pragma unroll
                     for (int kk = 0; kk < 4; ++kk)
-                        ptx::mma_ss(tS0 + 128 * t, kHiK | (qlo + t * kTileLo + 2 * kk),
-                                    kHiK | (klo + 2 * kk), idesc_qk, kk > 0 ? 1u : 0u);
-                    ptx::mma_commit(bar_s0 + t * kBarStride);
-                    if (++s_issued == s_total)
-                        ptx::mma_commit(bar_qe);
+                        ptx::mma_ss(tS, kHiK | (qlo + 2 * kk), kHiK | (klo + 2 * kk), idesc_qk,
+                                    kk > 0 ? 1u : 0u);
+                    ptx::mma_commit(b_sfull);
+                    if (j + 1 == hit)
+                        ptx::mma_commit(b_qe); // last read of this Q buffer
                 }
                 __syncwarp();
             }
+            // the softmax has copied S(j) out of TMEM: issue S(j + 1)
+            ok = warp_wait(b_sfree, fcount & 1, cx.wc, W_S_FULL);
             if (!ok)
                 break;
-            // phase B1: once the softmax has copied S(t, j) out of TMEM, the next S
-#pragma unroll
-            for (int t = 0; t < 2; ++t) {
-                const int lot = t ? lo1 : lo0, hit = t ? hi1 : hi0;
-                if (!it.valid[t] || j < lot || j >= hit)
-                    continue;
-                ok = warp_wait(bar_sf0 + t * kBarStride, (t ? fc1 : fc0) & 1, cx.wc, W_S_FULL);
-                if (!ok)
-                    break;
-                if (t)
-                    ++fc1;
-                else
-                    ++fc0;
-                if (j + 1 >= hit)
-                    continue;
-                if (!(ok = wait_kv_tiles(cx, bar_kvf0, kv_base, j + 1 - lo, waited)))
+            ++fcount;
+            if (j + 1 < hit) {
+                if (!(ok = wait_kv_tiles(cx, b_kvf0, kv_base, j + 1 - lo, waited)))
                     break;
                 ptx::tc_fence_after();
                 if (lane == 0) {
                     const uint32_t klo = k_lo0 + ((kv_base + (j + 1 - lo)) % kStages) * kTileLo;
 #pragma unroll
                     for (int kk = 0; kk < 4; ++kk)
-                        ptx::mma_ss(tS0 + 128 * t, kHiK | (qlo + t * kTileLo + 2 * kk),
-                                    kHiK | (klo + 2 * kk), idesc_qk, kk > 0 ? 1u : 0u);
-                    ptx::mma_commit(bar_s0 + t * kBarStride);
-                    if (++s_issued == s_total)
-                        ptx::mma_commit(bar_qe);
+                        ptx::mma_ss(tS, kHiK | (qlo + 2 * kk), kHiK | (klo + 2 * kk), idesc_qk,
+                                    kk > 0 ? 1u : 0u);
+                    ptx::mma_commit(b_sfull);
+                    if (j + 2 == hit)
+                        ptx::mma_commit(b_qe);
                 }
                 __syncwarp();
             }
+            // the softmax has written P(j) and rescaled O: issue P V(j)
+            ok = warp_wait(b_pfull, pcount & 1, cx.wc, W_P_FULL);
             if (!ok)
                 break;
-            // phase B2: once the softmax of (t, j) has written P and rescaled O,
-            // this tile's P V
+            ++pcount;
+            ptx::tc_fence_after();
+            if (lane == 0) {
+                const uint32_t vlo = v_lo0 + stage_j * kTileLo;
 #pragma unroll
-            for (int t = 0; t < 2; ++t) {
-                const int lot = t ? lo1 : lo0, hit = t ? hi1 : hi0;
-                if (!it.valid[t] || j < lot || j >= hit)
-                    continue;
-                ok = warp_wait(bar_p0 + t * kBarStride, (t ? pc1 : pc0) & 1, cx.wc, W_P_FULL);
-                if (!ok)
-                    break;
-                if (t)
-                    ++pc1;
-                else
-                    ++pc0;
-                ptx::tc_fence_after();
-                if (lane == 0) {
-                    const uint32_t vlo = v_lo0 + ((kv_base + (j - lo)) % kStages) * kTileLo;
-#pragma unroll
-                    for (int kk = 0; kk < BN / 16; ++kk)
-                        ptx::mma_ts(tO0 + 64 * t, tP0 + 64 * t + 8 * kk, kHiV | (vlo + 128 * kk),
-                                    idesc_pv, (j > lot || kk > 0) ? 1u : 0u);
-                    ptx::mma_commit(bar_pv0 + t * kBarStride);
-                }
-                __syncwarp();
+                for (int kk = 0; kk < BN / 16; ++kk)
+                    ptx::mma_ts(tO, tP + 8 * kk, kHiV | (vlo + 128 * kk), idesc_pv,
+                                (j > lot || kk > 0) ? 1u : 0u);
+                ptx::mma_commit(b_pvdone);
+                ptx::mma_commit(b_kve0 + stage_j * kBarStride); // this slot is done with tile j
             }
-            if (!ok)
-                break;
-            // every S and P V reading key tile j has been issued
+            __syncwarp();
+        }
+        if (!ok)
+            break;
+        if (!active) {
             if (lane == 0)
-                ptx::mma_commit(bar_kve0 + ((kv_base + (j - lo)) % kStages) * kBarStride);
+                ptx::mbar_arrive(b_qe);
             __syncwarp();
         }
         kv_base += static_cast<uint32_t>(hi - lo);
         ++item_count;
     }
     // Every MMA this thread issued has completed before TMEM is released.
+    const uint32_t b_final = bar(sm.final_bar[t]);
     if (lane == 0)
-        ptx::mma_commit(bar(sm.final_bar));
+        ptx::mma_commit(b_final);
     __syncwarp();
-    mbar_wait_drain(bar(sm.final_bar), 0, cx.wc, W_FINAL);
+    mbar_wait_drain(b_final, 0, cx.wc, W_FINAL);
 }
 
 // ------------------------------------------------------------------ softmax
@@ -434,11 +420,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (threadIdx.x == 0) {
         for (int b = 0; b < 2; ++b) {
             ptx::mbar_init(bar(sm->q_full[b]), 1);
-            ptx::mbar_init(bar(sm->q_empty[b]), 1);
+            ptx::mbar_init(bar(sm->q_empty[b]), 2); // one arrival per MMA warp
         }
         for (int s = 0; s < kStages; ++s) {
             ptx::mbar_init(bar(sm->kv_full[s]), 1);
-            ptx::mbar_init(bar(sm->kv_empty[s]), 1);
+            ptx::mbar_init(bar(sm->kv_empty[s]), 2); // one arrival per MMA warp
         }
         for (int t = 0; t < 2; ++t) {
             ptx::mbar_init(bar(sm->s_full[t]), 1);
@@ -446,7 +432,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             ptx::mbar_init(bar(sm->s_free[t]), 128);
             ptx::mbar_init(bar(sm->pv_done[t]), 1);
         }
-        ptx::mbar_init(bar(sm->final_bar), 1);
+        ptx::mbar_init(bar(sm->final_bar[0]), 1);
+        ptx::mbar_init(bar(sm->final_bar[1]), 1);
         sm->abort_flag = 0;
         ptx::fence_mbarrier_init();
         ptx::fence_proxy_async_smem();
@@ -483,8 +470,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         ptx::setmaxnreg_dec<kRegsOther>();
         if (warp == 8)
             producer_role(cx, p, &tm_q, &tm_k, &tm_v);
-        else if (warp == 9)
-            mma_role(cx, p);
+        else if (warp == 9 || warp == 10)
+            mma_role(cx, p, warp - 9);
         ptx::tc_fence_before();
         ptx::named_barrier_sync(1, kThreads);
         if (warp == 9) {
