@@ -320,6 +320,15 @@ __device__ __forceinline__ void add2(float &d0, float &d1, float a0, float a1)
         : "f"(a0), "f"(a1));
 }
 
+// acc0 += (float)low bf16 of w, acc1 += (float)high bf16 of w (exact widening).
+__device__ __forceinline__ void add_bf16x2_to_f32(float &acc0, float &acc1, uint32_t w)
+{
+    asm("{\n\t.reg .b16 lo, hi;\n\tmov.b32 {lo, hi}, %2;\n\t"
+        "add.rn.f32.bf16 %0, lo, %0;\n\tadd.rn.f32.bf16 %1, hi, %1;\n\t}"
+        : "+f"(acc0), "+f"(acc1)
+        : "r"(w));
+}
+
 __device__ __forceinline__ float max3(float a, float b, float c)
 {
     float d;
