@@ -308,50 +308,6 @@ __device__ void mma_role(const KernelCtx &cx, const StdParams &p, int t)
 }
 
 // ------------------------------------------------------------------ softmax
-
-// What the deferred epilogue of a finished query tile needs.
-struct PendingTile {
-    int b, h, qb, i, ntiles;
-    RowState st;
-};
-
-// O / l -> bf16 row, natural-log LSE, visited-tile count.  O[t] must hold the
-// tile's complete output (its last P V has completed).
-__device__ __forceinline__ void store_tile_output(const StdParams &p, uint32_t tO,
-                                                  const PendingTile &pt, int r)
-{
-    uint32_t o[64];
-    ptx::tmem_ld32(tO, o);
-    ptx::tmem_ld32(tO + 32, o + 32);
-    ptx::tmem_wait_ld();
-    ptx::reg_fence<32>(o);
-    ptx::reg_fence<32>(o + 32);
-    const float inv = row_inv_norm(pt.st);
-    if (pt.i < p.mask.S) {
-        __nv_bfloat16 *dst =
-            p.out + pt.b * p.o_sb + static_cast<int64_t>(pt.i) * p.o_ss + pt.h * p.o_sh;
-        uint4 *d4 = reinterpret_cast<uint4 *>(dst);
-#pragma unroll
-        for (int c = 0; c < 8; ++c) {
-            uint4 w;
-            w.x = ptx::pack_bf16(__uint_as_float(o[8 * c + 0]) * inv, __uint_as_float(o[8 * c + 1]) * inv);
-            w.y = ptx::pack_bf16(__uint_as_float(o[8 * c + 2]) * inv, __uint_as_float(o[8 * c + 3]) * inv);
-            w.z = ptx::pack_bf16(__uint_as_float(o[8 * c + 4]) * inv, __uint_as_float(o[8 * c + 5]) * inv);
-            w.w = ptx::pack_bf16(__uint_as_float(o[8 * c + 6]) * inv, __uint_as_float(o[8 * c + 7]) * inv);
-            d4[c] = w;
-        }
-        if (p.lse)
-            p.lse[pt.b * p.l_sb + pt.h * p.l_sh + pt.i] = row_lse(pt.st);
-    }
-    if (p.tile_counts && r == 0)
-        p.tile_counts[(static_cast<int64_t>(pt.b) * p.grid.Hq + pt.h) * p.grid.nq + pt.qb] = pt.ntiles;
-}
-
-// The epilogue of a query tile is deferred into the first key tile of the
-// slot's next work item: after that tile's P is computed (in registers) and
-// before it is handed to the MMA warp, which is the last moment O[t] still
-// holds the previous tile's result.  The latency of the previous tile's last
-// P V is thereby hidden behind the new tile's exponentials.
 template <int MOD>
 __device__ void softmax_role(const KernelCtx &cx, const StdParams &p, int t)
 {
@@ -363,8 +319,6 @@ __device__ void softmax_role(const KernelCtx &cx, const StdParams &p, int t)
     const uint32_t tO = cx.tmem + lane_off + kColO + 64 * t;
     const uint32_t tP = cx.tmem + lane_off + kColP + 64 * t;
     uint32_t scount = 0, pvcount = 0;
-    bool pending = false;
-    PendingTile prev{};
 
     for (int64_t L = blockIdx.x; L < p.grid.n_items; L += gridDim.x) {
         const Item it = decode_item(p.grid, L);
@@ -406,39 +360,50 @@ __device__ void softmax_role(const KernelCtx &cx, const StdParams &p, int t)
             bool rescale;
             const float alpha =
                 softmax_compute_p(x, MOD == MOD_NONE ? p.qk_log2 : 1.f, st, j == tr.lo, pk, rescale);
-            if (j > tr.lo || pending) {
-                // the previous P V (of this tile or of the previous work item)
-                // has consumed P[t] and landed in O[t]
+            if (j > tr.lo) {
+                // the previous tile's P V has consumed P[t] and landed in O[t]
                 if (!warp_wait(bar(sm.pv_done[t]), pvcount & 1, cx.wc, W_O_FULL))
                     return;
                 ++pvcount;
                 ptx::tc_fence_after();
-                if (j > tr.lo) {
-                    if (rescale)
-                        rescale_o<64>(tO, alpha);
-                } else {
-                    store_tile_output(p, tO, prev, r);
-                    pending = false;
-                }
+                if (rescale)
+                    rescale_o<64>(tO, alpha);
             }
             store_p(tP, pk);
             ptx::tc_fence_before();
             ptx::mbar_arrive(bar(sm.p_full[t]));
             ++ntiles;
         }
-        prev.b = b;
-        prev.h = h;
-        prev.qb = qb;
-        prev.i = i;
-        prev.ntiles = ntiles;
-        prev.st = st;
-        pending = true;
-    }
-    if (pending) {
+
+        // epilogue: O / l -> bf16, LSE
         if (!warp_wait(bar(sm.pv_done[t]), pvcount & 1, cx.wc, W_O_FULL))
             return;
+        ++pvcount;
         ptx::tc_fence_after();
-        store_tile_output(p, tO, prev, r);
+        uint32_t o[64];
+        ptx::tmem_ld32(tO, o);
+        ptx::tmem_ld32(tO + 32, o + 32);
+        ptx::tmem_wait_ld();
+        ptx::reg_fence<32>(o);
+        ptx::reg_fence<32>(o + 32);
+        const float inv = row_inv_norm(st);
+        if (i < p.mask.S) {
+            __nv_bfloat16 *dst = p.out + b * p.o_sb + static_cast<int64_t>(i) * p.o_ss + h * p.o_sh;
+            uint4 *d4 = reinterpret_cast<uint4 *>(dst);
+#pragma unroll
+            for (int c = 0; c < 8; ++c) {
+                uint4 w;
+                w.x = ptx::pack_bf16(__uint_as_float(o[8 * c + 0]) * inv, __uint_as_float(o[8 * c + 1]) * inv);
+                w.y = ptx::pack_bf16(__uint_as_float(o[8 * c + 2]) * inv, __uint_as_float(o[8 * c + 3]) * inv);
+                w.z = ptx::pack_bf16(__uint_as_float(o[8 * c + 4]) * inv, __uint_as_float(o[8 * c + 5]) * inv);
+                w.w = ptx::pack_bf16(__uint_as_float(o[8 * c + 6]) * inv, __uint_as_float(o[8 * c + 7]) * inv);
+                d4[c] = w;
+            }
+            if (p.lse)
+                p.lse[b * p.l_sb + h * p.l_sh + i] = row_lse(st);
+        }
+        if (p.tile_counts && r == 0)
+            p.tile_counts[(static_cast<int64_t>(b) * p.grid.Hq + h) * p.grid.nq + qb] = ntiles;
     }
 }
 

@@ -219,6 +219,11 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t *r)
         : "r"(taddr));
 }
 
+__device__ __forceinline__ void tmem_ld1(uint32_t taddr, uint32_t *r)
+{
+    asm volatile("tcgen05.ld.sync.aligned.32x32b.x1.b32 {%0}, [%1];" : "=r"(r[0]) : "r"(taddr));
+}
+
 __device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t *r)
 {
     asm volatile(

@@ -205,10 +205,59 @@ __device__ __forceinline__ float softmax_compute_p(float (&x)[BN], float c, RowS
         pk[e] = ptx::pack_bf16(p0, p1);
         const int q = 2 * (e & 3);
         ptx::add2(le[q], le[q + 1], p0, p1);
-        ptx::add_bf16x2_to_f32(lr[q], lr[q + 1], pk[e]);
+        ptx::add2(lr[q], lr[q + 1], __uint_as_float(pk[e] << 16),
+                  __uint_as_float(pk[e] & 0xFFFF0000u));
     }
     st.l += ((le[0] + le[1]) + (le[2] + le[3])) + ((le[4] + le[5]) + (le[6] + le[7]));
     st.l_round += ((lr[0] + lr[1]) + (lr[2] + lr[3])) + ((lr[4] + lr[5]) + (lr[6] + lr[7]));
+    return alpha;
+}
+
+// As softmax_compute_p, for kernels whose P V product also produces the sum
+// of the rounded P (an extra output column multiplied by ones): only the
+// exact sum `l` is kept here; st.l_round is left untouched.
+__device__ __forceinline__ float softmax_compute_p_exact_sum(float (&x)[BN], float c, RowState &st,
+                                                             bool first, uint32_t (&pk)[BN / 2],
+                                                             bool &rescale)
+{
+    float mc[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q)
+        mc[q] = fmaxf(x[2 * q], x[2 * q + 1]);
+#pragma unroll
+    for (int e = 8; e < BN; e += 8) {
+#pragma unroll
+        for (int q = 0; q < 4; ++q)
+            mc[q] = ptx::max3(mc[q], x[e + 2 * q], x[e + 2 * q + 1]);
+    }
+    const float mx = fmaxf(fmaxf(mc[0], mc[1]), fmaxf(mc[2], mc[3])) * c; // c > 0
+    float alpha = 1.f;
+    rescale = false;
+    if (first) {
+        st.m_ref = mx;
+    } else {
+        const bool need = mx > st.m_ref + kRescaleThreshold;
+        if (__any_sync(0xffffffffu, need)) {
+            const float m_new = fmaxf(st.m_ref, mx);
+            alpha = (m_new == kNegInf) ? 1.f : ptx::ex2(st.m_ref - m_new);
+            st.l *= alpha;
+            st.m_ref = m_new;
+            rescale = true;
+        }
+    }
+    const float nmu = (st.m_ref == kNegInf) ? 0.f : -st.m_ref;
+    float le[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int e = 0; e < BN / 2; ++e) {
+        float a0, a1;
+        ptx::fma2(a0, a1, x[2 * e], x[2 * e + 1], c, c, nmu, nmu);
+        const float p0 = ptx::ex2(a0);
+        const float p1 = ptx::ex2(a1);
+        pk[e] = ptx::pack_bf16(p0, p1);
+        const int q = 2 * (e & 3);
+        ptx::add2(le[q], le[q + 1], p0, p1);
+    }
+    st.l += ((le[0] + le[1]) + (le[2] + le[3])) + ((le[4] + le[5]) + (le[6] + le[7]));
     return alpha;
 }
 
