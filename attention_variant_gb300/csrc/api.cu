@@ -446,6 +446,110 @@ fl_status fwd_diff(const fl_tensor *q, const fl_tensor *k, const fl_tensor *v,
     return ok();
 }
 
+// ------------------------------------------------------------------ Evoformer
+
+fl_status fwd_evo(bool row_pass, const fl_tensor *q, const fl_tensor *k, const fl_tensor *v,
+                  const fl_tensor *out, const fl_tensor *lse, const fl_attn_variant_desc *d,
+                  const fl_tensor *bias, const fl_tensor *gate, cudaStream_t stream)
+{
+    View Q, K, V, O, G, Bz{}, L{};
+    fl_status s;
+    if ((s = check_tensor(q, "q", 4, FL_BF16, Q)) != FL_OK) return s;
+    if ((s = check_tensor(k, "k", 4, FL_BF16, K)) != FL_OK) return s;
+    if ((s = check_tensor(v, "v", 4, FL_BF16, V)) != FL_OK) return s;
+    if ((s = check_tensor(out, "out", 4, FL_BF16, O)) != FL_OK) return s;
+    if ((s = check_tensor(gate, "gate", 4, FL_BF16, G)) != FL_OK) return s;
+    const int64_t Ns = Q.size[0], Nr = Q.size[1], H = Q.size[2], C = Q.size[3];
+    for (const View *t : {&K, &V, &O, &G})
+        if (!same(*t, {Ns, Nr, H, C}))
+            return fail(FL_ERR_INVALID_ARG, "q, k, v, gate and out must all be [N_seq, N_res, H, c]");
+    if (row_pass) {
+        if ((s = check_tensor(bias, "bias", 3, FL_BF16, Bz)) != FL_OK) return s;
+        if (!same(Bz, {H, Nr, Nr}))
+            return fail(FL_ERR_INVALID_ARG, "bias must be [H, N_res, N_res]");
+    } else if (bias) {
+        return fail(FL_ERR_INVALID_ARG, "the column pass takes no bias");
+    }
+    const int64_t B = row_pass ? Ns : Nr, S = row_pass ? Nr : Ns;
+    if (lse) {
+        if ((s = check_tensor(lse, "lse", 3, FL_F32, L)) != FL_OK) return s;
+        if (!same(L, {B, H, S}))
+            return fail(FL_ERR_INVALID_ARG, row_pass ? "lse must be [N_seq, H, N_res]"
+                                                     : "lse must be [N_res, H, N_seq]");
+    }
+    if (d->mask != FL_MASK_NONE || d->score_mod != FL_MOD_NONE)
+        return fail(FL_ERR_UNSUPPORTED, "the Evoformer kinds take no mask and no score_mod");
+    if (!std::isfinite(d->scale) || d->scale < 0.f)
+        return fail(FL_ERR_INVALID_ARG, "scale must be finite and positive (0 selects 1/sqrt(c))");
+    if (C != 32)
+        return fail(FL_ERR_UNSUPPORTED, "the Evoformer kinds support c = 32 (got %lld)", (long long)C);
+
+    int dev;
+    DeviceInfo info;
+    if ((s = device_info(dev, info)) != FL_OK) return s;
+
+    // [batch, sequence, head, c] view: which tensor axis plays batch and sequence
+    const int ab = row_pass ? 0 : 1, ai = row_pass ? 1 : 0;
+    CUtensorMap tq, tk, tv;
+    const uint32_t box[4] = {32, 128, 1, 1};
+    const View *src[3] = {&Q, &K, &V};
+    CUtensorMap *dst[3] = {&tq, &tk, &tv};
+    const char *names[3] = {"q", "k", "v"};
+    for (int m = 0; m < 3; ++m) {
+        const View &T = *src[m];
+        const uint64_t dims[4] = {uint64_t(C), uint64_t(S), uint64_t(H), uint64_t(B)};
+        const uint64_t st[3] = {uint64_t(T.stride[ai]) * 2, uint64_t(T.stride[2]) * 2,
+                                uint64_t(T.stride[ab]) * 2};
+        if ((s = make_map(*dst[m], T.ptr, 4, dims, st, box, CU_TENSOR_MAP_SWIZZLE_64B, names[m])) != FL_OK)
+            return s;
+    }
+    fl::EvoParams p{};
+    const int nq = int((S + fl::BM - 1) / fl::BM);
+    p.grid.B = int(B);
+    p.grid.Hq = int(H);
+    p.grid.Hk = int(H);
+    p.grid.G = 1;
+    p.grid.nq = nq;
+    p.grid.pair_heads = 0;
+    p.grid.R = (nq + 1) / 2;
+    p.grid.Hx = int(B * H);
+    p.grid.n_items = int64_t(p.grid.R) * p.grid.Hx;
+    p.grid.lpt = 0;
+    p.grid.group = 8;
+    p.mask.kind = FL_MASK_NONE;
+    p.mask.S = int(S);
+    const float scale = d->scale != 0.f ? d->scale : 1.0f / std::sqrt(float(C));
+    p.qk_scale = scale;
+    p.qk_log2 = scale * 1.4426950408889634f;
+    if (row_pass) {
+        p.bias = static_cast<const __nv_bfloat16 *>(Bz.ptr);
+        p.bias_sh = Bz.stride[0];
+        p.bias_si = Bz.stride[1];
+    }
+    p.gate = static_cast<const __nv_bfloat16 *>(G.ptr);
+    p.g_sb = G.stride[ab];
+    p.g_si = G.stride[ai];
+    p.g_sh = G.stride[2];
+    p.out = static_cast<__nv_bfloat16 *>(O.ptr);
+    p.o_sb = O.stride[ab];
+    p.o_si = O.stride[ai];
+    p.o_sh = O.stride[2];
+    if (lse) {
+        p.lse = static_cast<float *>(L.ptr);
+        p.l_sb = L.stride[0];
+        p.l_sh = L.stride[1];
+    }
+    p.tile_counts = d->debug_tile_counts;
+    p.err_user = d->error_word;
+    p.inject = d->debug_inject;
+    p.timeout_ns = timeout_ns(d);
+    const int grid = int(p.grid.n_items < info.sm_count ? p.grid.n_items : info.sm_count);
+    cudaError_t e = fl::launch_evo(tq, tk, tv, p, grid, stream);
+    if (e != cudaSuccess)
+        return fail(FL_ERR_CUDA, "kernel launch failed: %s", cudaGetErrorString(e));
+    return ok();
+}
+
 } // namespace
 
 extern "C" {
@@ -464,7 +568,8 @@ fl_status fl_attn_fwd(const fl_tensor *q, const fl_tensor *k, const fl_tensor *v
         return fwd_diff(q, k, v, out, lse, desc, bias, gate, reinterpret_cast<cudaStream_t>(stream));
     case FL_KIND_EVO_ROW:
     case FL_KIND_EVO_COL:
-        return fail(FL_ERR_UNSUPPORTED, "kind %d is not built yet", desc->kind);
+        return fwd_evo(desc->kind == FL_KIND_EVO_ROW, q, k, v, out, lse, desc, bias, gate,
+                       reinterpret_cast<cudaStream_t>(stream));
     default:
         return fail(FL_ERR_INVALID_ARG, "unknown kind %d", desc->kind);
     }

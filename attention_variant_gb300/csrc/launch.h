@@ -52,6 +52,30 @@ struct DiffParams {
 cudaError_t launch_diff(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
                         const DiffParams &p, int grid, cudaStream_t stream);
 
+// Parameters of the Evoformer kernel (c = 32) over a [batch, sequence, head, c]
+// view: row pass batch = MSA row, sequence = residue; column pass the reverse.
+struct EvoParams {
+    GridSpec grid;
+    MaskSpec mask;          // kind NONE; S = length of the attended axis
+    float qk_log2;          // scale * log2(e)
+    float qk_scale;         // scale
+    const __nv_bfloat16 *bias; // row pass: bias[h, i, j]; null for the column pass
+    int64_t bias_sh, bias_si;
+    const __nv_bfloat16 *gate;
+    int64_t g_sb, g_si, g_sh;
+    __nv_bfloat16 *out;
+    int64_t o_sb, o_si, o_sh;
+    float *lse;             // [batch, head, sequence] or null
+    int64_t l_sb, l_sh;
+    int32_t *tile_counts;   // [batch][head][nq] or null
+    uint32_t *err_user;
+    int inject;
+    uint64_t timeout_ns;
+};
+
+cudaError_t launch_evo(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
+                       const EvoParams &p, int grid, cudaStream_t stream);
+
 cudaError_t launch_standard(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
                             const StdParams &p, int grid, cudaStream_t stream);
 size_t standard_smem_bytes();
