@@ -191,6 +191,12 @@ int fl_oracle_attention(const fl_oracle_problem *p, const uint16_t *q, const uin
         return -1;
     if (p->mask == FL_ORACLE_MASK_DOC && (!p->doc_offsets || p->doc_stride <= 0))
         return -1;
+    if (rows) {
+        for (int64_t r = 0; r < n_rows; ++r)
+            if (rows[3 * r] < 0 || rows[3 * r] >= p->B || rows[3 * r + 1] < 0 ||
+                rows[3 * r + 1] >= p->Hq || rows[3 * r + 2] < 0 || rows[3 * r + 2] >= p->Sq)
+                return -1;
+    }
     const int64_t total = rows ? n_rows : (int64_t)p->B * p->Hq * p->Sq;
 #ifdef _OPENMP
     if (nthreads > 0)
