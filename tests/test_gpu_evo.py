@@ -28,7 +28,7 @@ def _inputs(tag, Ns, Nr, H, c=32):
     return q, k, v, g, bias
 
 
-def run_evo(row, q, k, v, g, bias):
+def run_evo(row, q, k, v, g, bias, bias_pitch=None):
     Ns, Nr, H, c = q.shape
     B, S = (Ns, Nr) if row else (Nr, Ns)
     out = torch.full((Ns, Nr, H, c), float("nan"), dtype=torch.bfloat16, device="cuda")
@@ -36,13 +36,21 @@ def run_evo(row, q, k, v, g, bias):
     cnt = torch.full((B, H, (S + 127) // 128), -1, dtype=torch.int32, device="cuda")
     err = torch.zeros(1, dtype=torch.int32, device="cuda")
     d = fa.make_desc(kind="evo_row" if row else "evo_col", debug_tile_counts=cnt, error_word=err)
-    fa.fl_attn_fwd(gu.dev(q), gu.dev(k), gu.dev(v), out, lse, d,
-                   bias=gu.dev(bias) if row else None, gate=gu.dev(g))
+    bias_t = None
+    if row:
+        if bias_pitch is None:
+            bias_t = gu.dev(bias)
+        else:  # rows padded to bias_pitch elements (a strided, 16-byte aligned view)
+            H = bias.shape[0]
+            padded = np.zeros((H, Nr, bias_pitch), dtype=np.uint16)
+            padded[:, :, :Nr] = bias
+            bias_t = gu.dev(padded)[:, :, :Nr]
+    fa.fl_attn_fwd(gu.dev(q), gu.dev(k), gu.dev(v), out, lse, d, bias=bias_t, gate=gu.dev(g))
     torch.cuda.synchronize()
     return gu.f64(out), gu.f64(lse), cnt.cpu().numpy(), int(err.item())
 
 
-@pytest.mark.parametrize("Ns,Nr", [(4, 200), (3, 384), (5, 130)])
+@pytest.mark.parametrize("Ns,Nr", [(4, 200), (3, 384), (5, 136)])
 def test_evo_row_small(Ns, Nr):
     q, k, v, g, bias = _inputs(f"evo{Ns}_{Nr}", Ns, Nr, 2)
     o, lse, cnt, err = run_evo(True, q, k, v, g, bias)
@@ -50,6 +58,23 @@ def test_evo_row_small(Ns, Nr):
     oref, lref = oracle.evo_row(q, k, v, bias, g)
     gu.compare(o, lse, oref, lref, what=f"evo row {Ns}x{Nr}")
     assert np.array_equal(cnt, gu.expected_tile_counts("none", Ns, 2, Nr))
+
+
+def test_evo_row_ragged_padded_bias():
+    """N_res = 130: the bias rows are padded to a 16-byte multiple (pitch 136)
+    and passed as a strided view; the last key tile is ragged."""
+    q, k, v, g, bias = _inputs("evopad", 3, 130, 2)
+    o, lse, cnt, err = run_evo(True, q, k, v, g, bias, bias_pitch=136)
+    assert err == 0
+    oref, lref = oracle.evo_row(q, k, v, bias, g)
+    gu.compare(o, lse, oref, lref, what="evo row padded bias")
+
+
+def test_evo_rejects_unaligned_bias():
+    q, k, v, g, bias = _inputs("evobad", 2, 130, 2)
+    with pytest.raises(fa.FlAttnError) as e:
+        run_evo(True, q, k, v, g, bias)
+    assert e.value.status == fa.FL_ERR_ALIGNMENT
 
 
 @pytest.mark.parametrize("Ns,Nr", [(200, 4), (512, 3), (130, 5)])
