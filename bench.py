@@ -41,6 +41,7 @@ HEADLINE = dict(S=2048, variant="vanilla")
 METRIC = "fused attention fwd TFLOP/s (bf16) and % of GB300 dense BF16 peak per variant"
 L2_FLUSH_BYTES = 256 << 20
 KERNEL_SOURCES = ["attention_variant_gb300/csrc/fwd_standard.cu",
+                  "attention_variant_gb300/csrc/softmax_tile.cuh",
                   "attention_variant_gb300/csrc/common.cuh",
                   "attention_variant_gb300/csrc/ptx.cuh"]
 
@@ -98,6 +99,28 @@ def entry(kind, S, variant):
     return dict(name=w["name"], kind=kind, B=B, Hq=Hq, Hk=Hk, S=S, D=D, variant=variant,
                 mod=mod, mask=mask, kw=kw, doc=doc, pairs=pairs, flops=4 * D * pairs,
                 bytes=2 * B * S * D * (2 * Hq + 2 * Hk) + 4 * B * Hq * S)
+
+
+def diff_entry(mask):
+    w = workloads.DIFF
+    B, S, H, D, Dv = w["B"], w["S"], w["H"], w["D"], w["Dv"]
+    pairs = unmasked_pairs(mask, B, H, S)
+    # per pair: two Q K^T (2 D each) and two P V (2 Dv each)
+    return dict(name=w["name"], kind="diff", B=B, S=S, H=H, D=D, Dv=Dv, mask=mask,
+                variant="causal" if mask == "causal" else "non-causal", pairs=pairs,
+                flops=pairs * (2 * 2 * D + 2 * 2 * Dv),
+                bytes=2 * (2 * 2 * B * S * H * D + B * S * H * Dv + B * S * H * Dv) + 4 * 2 * B * H * S)
+
+
+def evo_entry(row):
+    w = workloads.EVO
+    Ns, Nr, H, c = w["N_seq"], w["N_res"], w["H"], w["c"]
+    B, S = (Ns, Nr) if row else (Nr, Ns)
+    pairs = B * H * S * S
+    tensor_bytes = Ns * Nr * H * c * 2
+    return dict(name=w["name"], kind="evo_row" if row else "evo_col", variant="row" if row else "col",
+                Ns=Ns, Nr=Nr, H=H, c=c, pairs=pairs, flops=pairs * 4 * c,
+                bytes=5 * tensor_bytes + (H * Nr * Nr * 2 if row else 0))
 
 
 def all_entries():
@@ -233,6 +256,44 @@ def time_entry(e, host, torch, fa, device, steps, warmup, flush, stream):
     return ms, (q, k, v, out, lse, desc)
 
 
+def time_other(e, torch, fa, device, steps, warmup, flush, stream):
+    """Device time of the differential or Evoformer kernel on its workload."""
+    to = lambda b: torch.from_numpy(b.view(np.int16)).view(torch.bfloat16).to(device)
+    if e["kind"] == "diff":
+        B, S, H, D, Dv = e["B"], e["S"], e["H"], e["D"], e["Dv"]
+        q = to(testdata.normal_bf16((2, B, S, H, D), e["name"], "q"))
+        k = to(testdata.normal_bf16((2, B, S, H, D), e["name"], "k"))
+        v = to(testdata.normal_bf16((B, S, H, Dv), e["name"], "v"))
+        out = torch.empty((B, S, H, Dv), dtype=torch.bfloat16, device=device)
+        lse = torch.empty((2, B, H, S), dtype=torch.float32, device=device)
+        desc = fa.make_desc(kind="diff", mask=e["mask"], diff_lambda=workloads.DIFF["lam"])
+        args = (q, k, v, out, lse, desc)
+        kw = {}
+    else:
+        Ns, Nr, H, c = e["Ns"], e["Nr"], e["H"], e["c"]
+        q, k, v, g = (to(testdata.normal_bf16((Ns, Nr, H, c), e["name"], n)) for n in "qkvg")
+        out = torch.empty_like(q)
+        row = e["kind"] == "evo_row"
+        bias = to(testdata.normal_bf16((H, Nr, Nr), e["name"], "bias")) if row else None
+        desc = fa.make_desc(kind=e["kind"])
+        args = (q, k, v, out, None, desc)
+        kw = dict(bias=bias, gate=g)
+    with torch.cuda.stream(stream):
+        for _ in range(warmup):
+            flush.zero_()
+            fa.fl_attn_fwd(*args, stream=stream, **kw)
+        torch.cuda.synchronize()
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(steps)]
+        for a, b in evs:
+            flush.zero_()
+            a.record(stream)
+            fa.fl_attn_fwd(*args, stream=stream, **kw)
+            b.record(stream)
+        torch.cuda.synchronize()
+    return [a.elapsed_time(b) for a, b in evs]
+
+
 def time_e2e(e, host, torch, fa, device, steps, warmup, stream):
     """Same metric end to end: pinned host inputs -> device -> fused forward
     -> O and LSE back to pinned host memory, every step."""
@@ -346,6 +407,16 @@ def run_ours(args):
 
     variants = {}
     if not args.headline_only:
+        for e in [diff_entry("none"), diff_entry("causal"), evo_entry(True), evo_entry(False)]:
+            vms = time_other(e, torch, fa, device, args.variant_steps, 2, flush, stream)
+            vm = statistics.mean(vms)
+            tf = e["flops"] / (vm * 1e-3) / 1e12
+            gbs = e["bytes"] / (vm * 1e-3) / 1e9
+            rec = dict(tflops=round(tf, 1), frac_peak=round(tf / peaks["bf16_tflops"], 4),
+                       ms=round(vm, 4), gbs=round(gbs, 1))
+            if e["kind"].startswith("evo"):
+                rec["frac_hbm"] = round(gbs / peaks["hbm_gbs"], 4)
+            variants[f"{e['name']}/{e['variant']}"] = rec
         for e in all_entries():
             h = gpu_inputs(e, torch, device) if (e["S"], e["kind"]) != (head["S"], "mha") else host
             vms, _ = time_entry(e, h, torch, fa, device, args.variant_steps, 2, flush, stream)
