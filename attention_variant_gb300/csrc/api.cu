@@ -503,6 +503,20 @@ fl_status fwd_evo(bool row_pass, const fl_tensor *q, const fl_tensor *k, const f
         if ((s = make_map(*dst[m], T.ptr, 4, dims, st, box, CU_TENSOR_MAP_SWIZZLE_64B, names[m])) != FL_OK)
             return s;
     }
+    CUtensorMap tb;
+    std::memset(&tb, 0, sizeof tb);
+    if (row_pass) {
+        if (Nr > fl::evo_max_bias_keys())
+            return fail(FL_ERR_UNSUPPORTED, "the row pass keeps the bias rows of a query block in "
+                        "shared memory: N_res <= %d", fl::evo_max_bias_keys());
+        // bias[h, i, j] as (j, i, h, 1); boxes of 64 keys x 128 query rows
+        const uint64_t dims[4] = {uint64_t(Nr), uint64_t(Nr), uint64_t(H), 1};
+        const uint64_t st[3] = {uint64_t(Bz.stride[1]) * 2, uint64_t(Bz.stride[0]) * 2,
+                                uint64_t(Bz.stride[0]) * 2 * uint64_t(H)};
+        const uint32_t bbox[4] = {64, 128, 1, 1};
+        if ((s = make_map(tb, Bz.ptr, 4, dims, st, bbox, CU_TENSOR_MAP_SWIZZLE_128B, "bias")) != FL_OK)
+            return s;
+    }
     fl::EvoParams p{};
     const int nq = int((S + fl::BM - 1) / fl::BM);
     p.grid.B = int(B);
@@ -510,22 +524,30 @@ fl_status fwd_evo(bool row_pass, const fl_tensor *q, const fl_tensor *k, const f
     p.grid.Hk = int(H);
     p.grid.G = 1;
     p.grid.nq = nq;
-    p.grid.pair_heads = 0;
-    p.grid.R = (nq + 1) / 2;
-    p.grid.Hx = int(B * H);
-    p.grid.n_items = int64_t(p.grid.R) * p.grid.Hx;
-    p.grid.lpt = 0;
-    p.grid.group = 8;
+    // chunk of batch indices per work item: minimise (waves x chunk) over the SMs
+    {
+        int64_t best_cost = -1;
+        int best_chunk = int(B);
+        for (int64_t nch = 1; nch <= B; ++nch) {
+            const int64_t chunk = (B + nch - 1) / nch;
+            const int64_t items = ((B + chunk - 1) / chunk) * H * nq;
+            const int64_t waves = (items + info.sm_count - 1) / info.sm_count;
+            const int64_t cost = waves * chunk;
+            if (best_cost < 0 || cost < best_cost) {
+                best_cost = cost;
+                best_chunk = int(chunk);
+            }
+        }
+        p.chunk = best_chunk;
+        p.n_items = ((B + best_chunk - 1) / best_chunk) * H * nq;
+    }
     p.mask.kind = FL_MASK_NONE;
     p.mask.S = int(S);
     const float scale = d->scale != 0.f ? d->scale : 1.0f / std::sqrt(float(C));
     p.qk_scale = scale;
     p.qk_log2 = scale * 1.4426950408889634f;
-    if (row_pass) {
+    if (row_pass)
         p.bias = static_cast<const __nv_bfloat16 *>(Bz.ptr);
-        p.bias_sh = Bz.stride[0];
-        p.bias_si = Bz.stride[1];
-    }
     p.gate = static_cast<const __nv_bfloat16 *>(G.ptr);
     p.g_sb = G.stride[ab];
     p.g_si = G.stride[ai];
@@ -541,10 +563,9 @@ fl_status fwd_evo(bool row_pass, const fl_tensor *q, const fl_tensor *k, const f
     }
     p.tile_counts = d->debug_tile_counts;
     p.err_user = d->error_word;
-    p.inject = d->debug_inject;
     p.timeout_ns = timeout_ns(d);
-    const int grid = int(p.grid.n_items < info.sm_count ? p.grid.n_items : info.sm_count);
-    cudaError_t e = fl::launch_evo(tq, tk, tv, p, grid, stream);
+    const int grid = int(p.n_items < info.sm_count ? p.n_items : info.sm_count);
+    cudaError_t e = fl::launch_evo(tq, tk, tv, tb, p, grid, stream);
     if (e != cudaSuccess)
         return fail(FL_ERR_CUDA, "kernel launch failed: %s", cudaGetErrorString(e));
     return ok();

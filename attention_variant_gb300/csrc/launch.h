@@ -54,13 +54,15 @@ cudaError_t launch_diff(const CUtensorMap &tq, const CUtensorMap &tk, const CUte
 
 // Parameters of the Evoformer kernel (c = 32) over a [batch, sequence, head, c]
 // view: row pass batch = MSA row, sequence = residue; column pass the reverse.
+// Work items are (head, query block, chunk of `chunk` batch indices).
 struct EvoParams {
-    GridSpec grid;
+    GridSpec grid;          // B, Hq (= heads), nq used
     MaskSpec mask;          // kind NONE; S = length of the attended axis
+    int64_t n_items;
+    int chunk;
     float qk_log2;          // scale * log2(e)
     float qk_scale;         // scale
-    const __nv_bfloat16 *bias; // row pass: bias[h, i, j]; null for the column pass
-    int64_t bias_sh, bias_si;
+    const __nv_bfloat16 *bias; // row pass only (its TMA map is passed separately)
     const __nv_bfloat16 *gate;
     int64_t g_sb, g_si, g_sh;
     __nv_bfloat16 *out;
@@ -69,12 +71,12 @@ struct EvoParams {
     int64_t l_sb, l_sh;
     int32_t *tile_counts;   // [batch][head][nq] or null
     uint32_t *err_user;
-    int inject;
     uint64_t timeout_ns;
 };
 
 cudaError_t launch_evo(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
-                       const EvoParams &p, int grid, cudaStream_t stream);
+                       const CUtensorMap &tb, const EvoParams &p, int grid, cudaStream_t stream);
+int evo_max_bias_keys();
 
 cudaError_t launch_standard(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
                             const StdParams &p, int grid, cudaStream_t stream);

@@ -261,6 +261,46 @@ __device__ __forceinline__ float softmax_compute_p_exact_sum(float (&x)[BN], flo
     return alpha;
 }
 
+// As softmax_compute_p_exact_sum, without any row sum (for kernels whose P V
+// product produces the rounded sum and whose caller needs no log-sum-exp).
+__device__ __forceinline__ float softmax_compute_p_no_sum(float (&x)[BN], float c, RowState &st,
+                                                          bool first, uint32_t (&pk)[BN / 2],
+                                                          bool &rescale)
+{
+    float mc[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q)
+        mc[q] = fmaxf(x[2 * q], x[2 * q + 1]);
+#pragma unroll
+    for (int e = 8; e < BN; e += 8) {
+#pragma unroll
+        for (int q = 0; q < 4; ++q)
+            mc[q] = ptx::max3(mc[q], x[e + 2 * q], x[e + 2 * q + 1]);
+    }
+    const float mx = fmaxf(fmaxf(mc[0], mc[1]), fmaxf(mc[2], mc[3])) * c; // c > 0
+    float alpha = 1.f;
+    rescale = false;
+    if (first) {
+        st.m_ref = mx;
+    } else {
+        const bool need = mx > st.m_ref + kRescaleThreshold;
+        if (__any_sync(0xffffffffu, need)) {
+            const float m_new = fmaxf(st.m_ref, mx);
+            alpha = (m_new == kNegInf) ? 1.f : ptx::ex2(st.m_ref - m_new);
+            st.m_ref = m_new;
+            rescale = true;
+        }
+    }
+    const float nmu = (st.m_ref == kNegInf) ? 0.f : -st.m_ref;
+#pragma unroll
+    for (int e = 0; e < BN / 2; ++e) {
+        float a0, a1;
+        ptx::fma2(a0, a1, x[2 * e], x[2 * e + 1], c, c, nmu, nmu);
+        pk[e] = ptx::pack_bf16(ptx::ex2(a0), ptx::ex2(a1));
+    }
+    return alpha;
+}
+
 // O *= alpha over DV fp32 columns at tO (this thread's row).
 template <int DV>
 __device__ __forceinline__ void rescale_o(uint32_t tO, float alpha)
