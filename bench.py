@@ -357,6 +357,26 @@ def cpu_baseline(e, seconds=12.0):
                        f"{e['variant']}, {dt:.1f} s")
 
 
+ONLY = {"diff": lambda: diff_entry("none"), "diff_causal": lambda: diff_entry("causal"),
+        "evo_row": lambda: evo_entry(True), "evo_col": lambda: evo_entry(False)}
+
+
+def run_only(args):
+    """Time one differential or Evoformer workload alone (for profiling)."""
+    import torch
+    import attention_variant_gb300 as fa
+    torch.cuda.set_device(0)
+    device = torch.device("cuda", 0)
+    fa.load_library()
+    stream = torch.cuda.Stream(device)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=device)
+    e = ONLY[args.only]()
+    ms = statistics.mean(time_other(e, torch, fa, device, args.steps, args.warmup, flush, stream))
+    print(json.dumps({"only": args.only, "ms": round(ms, 4),
+                      "tflops": round(e["flops"] / (ms * 1e-3) / 1e12, 1),
+                      "gbs": round(e["bytes"] / (ms * 1e-3) / 1e9, 1)}), flush=True)
+
+
 def run_ours(args):
     import torch
     import attention_variant_gb300 as fa
@@ -514,6 +534,8 @@ def main():
     ap.add_argument("--headline-only", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--only", choices=sorted(ONLY), default=None,
+                    help="time only this differential/Evoformer workload (profiling aid)")
     ap.add_argument("--clock-steps", type=int, default=3000,
                     help="untimed steps run under the clock sampler before the timed ones")
     args = ap.parse_args()
@@ -521,6 +543,8 @@ def main():
         args.warmup = 3
     if args.impl == "reference":
         run_reference(args)
+    elif args.only:
+        run_only(args)
     else:
         run_ours(args)
 
