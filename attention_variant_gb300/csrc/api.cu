@@ -266,6 +266,7 @@ fl_status fwd_standard(const fl_tensor *q, const fl_tensor *k, const fl_tensor *
 
     CUtensorMap tq, tk, tv;
     const uint32_t box[4] = {64, 128, 1, 1};
+    const uint32_t kvbox[4] = {64, uint32_t(fl::kStdKeyTile), 1, 1};
     {
         const uint64_t dims[4] = {uint64_t(D), uint64_t(S), uint64_t(Hq), uint64_t(B)};
         const uint64_t st[3] = {uint64_t(Q.stride[1]) * 2, uint64_t(Q.stride[2]) * 2,
@@ -277,14 +278,14 @@ fl_status fwd_standard(const fl_tensor *q, const fl_tensor *k, const fl_tensor *
         const uint64_t dims[4] = {uint64_t(D), uint64_t(S), uint64_t(Hk), uint64_t(B)};
         const uint64_t st[3] = {uint64_t(K.stride[1]) * 2, uint64_t(K.stride[2]) * 2,
                                 uint64_t(K.stride[0]) * 2};
-        if ((s = make_map(tk, K.ptr, 4, dims, st, box, CU_TENSOR_MAP_SWIZZLE_128B, "k")) != FL_OK)
+        if ((s = make_map(tk, K.ptr, 4, dims, st, kvbox, CU_TENSOR_MAP_SWIZZLE_128B, "k")) != FL_OK)
             return s;
     }
     {
         const uint64_t dims[4] = {uint64_t(Dv), uint64_t(S), uint64_t(Hk), uint64_t(B)};
         const uint64_t st[3] = {uint64_t(V.stride[1]) * 2, uint64_t(V.stride[2]) * 2,
                                 uint64_t(V.stride[0]) * 2};
-        if ((s = make_map(tv, V.ptr, 4, dims, st, box, CU_TENSOR_MAP_SWIZZLE_128B, "v")) != FL_OK)
+        if ((s = make_map(tv, V.ptr, 4, dims, st, kvbox, CU_TENSOR_MAP_SWIZZLE_128B, "v")) != FL_OK)
             return s;
     }
 
@@ -618,7 +619,7 @@ fl_status fl_attn_tile_shape(const fl_attn_variant_desc *desc, int32_t head_dim,
         return fail(FL_ERR_INVALID_ARG, "unknown kind %d", desc->kind);
     }
     *block_m = fl::BM;
-    *block_n = fl::BN;
+    *block_n = desc->kind == FL_KIND_STANDARD ? fl::kStdKeyTile : fl::BN;
     return ok();
 }
 

@@ -81,9 +81,12 @@ __device__ __forceinline__ void row_interval(const MaskSpec &m, int b, int i, in
 
 struct TileRange {
     int lo, hi;            // KV tiles [lo, hi) this query block visits
-    int full_lo, full_hi;  // a tile [j0, j0 + BN) needs no mask iff full_lo <= j0, j0 + BN <= full_hi
+    int full_lo, full_hi;  // a tile [j0, j0 + width) needs no mask iff full_lo <= j0 and
+                           // j0 + width <= full_hi
 };
 
+// TBN: the kernel's key-tile width (128 unless it says otherwise).
+template <int TBN = BN>
 __device__ __forceinline__ TileRange q_block_range(const MaskSpec &m, int b, int q0)
 {
     const int i_first = q0;
@@ -92,8 +95,8 @@ __device__ __forceinline__ TileRange q_block_range(const MaskSpec &m, int b, int
     row_interval(m, b, i_first, lo_f, hi_f);
     row_interval(m, b, i_last, lo_l, hi_l);
     TileRange r;
-    r.lo = lo_f / BN;
-    r.hi = (hi_l + BN - 1) / BN;
+    r.lo = lo_f / TBN;
+    r.hi = (hi_l + TBN - 1) / TBN;
     r.full_lo = lo_l;
     r.full_hi = hi_f;
     return r;

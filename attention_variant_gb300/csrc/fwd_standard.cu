@@ -23,9 +23,12 @@
 // register count before launching).
 // Each work item is two 128-row query tiles ("slots") sharing every K/V tile.
 //
-// TMEM (512 columns x 128 lanes, lane = query row):
-//   S[t] fp32 at columns 128 t, O[t] fp32 at 256 + 64 t, P[t] bf16x2 at
-//   384 + 64 t, for slots t = 0, 1.
+// Key tiles are kBN = 112 keys wide, so that TMEM (512 columns x 128 lanes,
+// lane = query row) holds, for slots t = 0, 1: S[t] fp32 at 112 t, O[t] fp32 at
+// 224 + 80 t with 80 columns -- 64 output columns and 16 columns of sum_j P_j
+// (P V multiplies P by V extended with a tile of ones, so the tensor core sums
+// the exact bf16 P it used: the normaliser of O) -- and P[t] bf16 pairs at
+// 384 + 64 t.  The softmax then keeps only the exact sum (for the LSE).
 //
 // Hand-off protocol for slot t and key tile j (all mbarriers):
 //   softmax: wait s_full(t); S[t] -> registers; arrive s_free(t);
@@ -56,13 +59,20 @@ constexpr uint32_t kRegsOther = 104;
 static_assert(2 * 128 * kRegsSoftmax + 128 * kRegsOther == kThreads * kRegsLaunch,
               "register split must equal the launch allocation");
 constexpr int kStages = 4;
-constexpr uint32_t kTileBytes = BM * 64 * 2; // one 128 x 64 bf16 tile
-constexpr uint32_t kColS = 0, kColO = 256, kColP = 384;
+constexpr int kBN = 112;                        // keys per K/V tile
+constexpr uint32_t kTileBytes = BM * 64 * 2;    // one 128 x 64 bf16 Q tile
+constexpr uint32_t kKVBytes = kBN * 64 * 2;     // one 112 x 64 bf16 K or V tile
+constexpr uint32_t kDvExt = 80;                 // 64 output columns + 16 sum columns
+constexpr uint32_t kColSum = 64;
+static_assert(kBN == kStdKeyTile, "the host encodes K/V tensor maps with kStdKeyTile rows");
+constexpr uint32_t kColS = 0, kColO = 224, kColP = 384;
+constexpr uint32_t kStrideS = kBN, kStrideO = kDvExt, kStrideP = 64;
 
 struct __align__(1024) StdSmem {
     uint8_t q[2][2][kTileBytes]; // [Q buffer][slot]
-    uint8_t k[kStages][kTileBytes];
-    uint8_t v[kStages][kTileBytes];
+    uint8_t k[kStages][kKVBytes];
+    uint8_t v[kStages][kKVBytes];
+    uint8_t ones[kTileBytes];    // bf16 1.0 everywhere: V's extra columns (after every V stage)
     uint64_t q_full[2], q_empty[2];
     uint64_t kv_full[kStages], kv_empty[kStages];
     uint64_t s_full[2], s_free[2], p_full[2], pv_done[2];
@@ -98,7 +108,7 @@ __device__ void producer_role(const KernelCtx &cx, const StdParams &p, const CUt
         for (int t = 0; t < 2; ++t) {
             if (!it.valid[t])
                 continue;
-            const TileRange r = q_block_range(p.mask, it.b, it.qb[t] * BM);
+            const TileRange r = q_block_range<kBN>(p.mask, it.b, it.qb[t] * BM);
             lo = min(lo, r.lo);
             hi = max(hi, r.hi);
             ++nvalid;
@@ -129,10 +139,10 @@ __device__ void producer_role(const KernelCtx &cx, const StdParams &p, const CUt
                 if (drop) {
                     dropped = kv_count;
                 } else {
-                    ptx::mbar_arrive_expect_tx(bar(sm.kv_full[s]), 2 * kTileBytes);
-                    ptx::tma_load_4d(ptx::smem_u32(sm.k[s]), tm_k, bar(sm.kv_full[s]), 0, j * BN,
+                    ptx::mbar_arrive_expect_tx(bar(sm.kv_full[s]), 2 * kKVBytes);
+                    ptx::tma_load_4d(ptx::smem_u32(sm.k[s]), tm_k, bar(sm.kv_full[s]), 0, j * kBN,
                                      it.kvh, it.b);
-                    ptx::tma_load_4d(ptx::smem_u32(sm.v[s]), tm_v, bar(sm.kv_full[s]), 0, j * BN,
+                    ptx::tma_load_4d(ptx::smem_u32(sm.v[s]), tm_v, bar(sm.kv_full[s]), 0, j * kBN,
                                      it.kvh, it.b);
                 }
             }
@@ -181,17 +191,17 @@ __device__ void mma_role(const KernelCtx &cx, const StdParams &p, int t)
 {
     StdSmem &sm = *cx.sm;
     const uint32_t lane = ptx::lane_id();
-    constexpr uint32_t idesc_qk = umma_idesc_bf16(BM, BN, false);
-    constexpr uint32_t idesc_pv = umma_idesc_bf16(BM, 64, true);
-    constexpr uint64_t kHiK = umma_desc_hi(16, 1024, kSwizzle128B);          // Q, K: K-major
-    constexpr uint64_t kHiV = umma_desc_hi(kTileBytes, 1024, kSwizzle128B);  // V: MN-major
-    constexpr uint32_t kTileLo = kTileBytes >> 4;
+    constexpr uint32_t idesc_qk = umma_idesc_bf16(BM, kBN, false);
+    constexpr uint32_t idesc_pv = umma_idesc_bf16(BM, kDvExt, true);
+    constexpr uint64_t kHiK = umma_desc_hi(16, 1024, kSwizzle128B); // Q, K: K-major
+    constexpr uint32_t kTileLo = kTileBytes >> 4, kKVLo = kKVBytes >> 4;
     constexpr uint32_t kBarStride = sizeof(uint64_t);
     const uint32_t q_lo0 = ptx::smem_u32(sm.q[0][t]) >> 4;
     const uint32_t k_lo0 = ptx::smem_u32(sm.k[0]) >> 4;
     const uint32_t v_lo0 = ptx::smem_u32(sm.v[0]) >> 4;
-    const uint32_t tS = cx.tmem + kColS + 128 * t, tO = cx.tmem + kColO + 64 * t;
-    const uint32_t tP = cx.tmem + kColP + 64 * t;
+    const uint32_t ones_lo = ptx::smem_u32(sm.ones) >> 4;
+    const uint32_t tS = cx.tmem + kColS + kStrideS * t, tO = cx.tmem + kColO + kStrideO * t;
+    const uint32_t tP = cx.tmem + kColP + kStrideP * t;
     const uint32_t b_sfull = bar(sm.s_full[t]), b_sfree = bar(sm.s_free[t]);
     const uint32_t b_pfull = bar(sm.p_full[t]), b_pvdone = bar(sm.pv_done[t]);
     const uint32_t b_kvf0 = bar(sm.kv_full[0]), b_kve0 = bar(sm.kv_empty[0]);
@@ -205,7 +215,7 @@ __device__ void mma_role(const KernelCtx &cx, const StdParams &p, int t)
         for (int u = 0; u < 2; ++u) {
             if (!it.valid[u])
                 continue;
-            const TileRange r = q_block_range(p.mask, it.b, it.qb[u] * BM);
+            const TileRange r = q_block_range<kBN>(p.mask, it.b, it.qb[u] * BM);
             lo = min(lo, r.lo);
             hi = max(hi, r.hi);
             if (u == t) {
@@ -240,7 +250,7 @@ __device__ void mma_role(const KernelCtx &cx, const StdParams &p, int t)
                     break;
                 ptx::tc_fence_after();
                 if (lane == 0) {
-                    const uint32_t klo = k_lo0 + stage_j * kTileLo;
+                    const uint32_t klo = k_lo0 + stage_j * kKVLo;
 #pragma unroll
                     for (int kk = 0; kk < 4; ++kk)
                         ptx::mma_ss(tS, kHiK | (qlo + 2 * kk), kHiK | (klo + 2 * kk), idesc_qk,
@@ -261,7 +271,7 @@ __device__ void mma_role(const KernelCtx &cx, const StdParams &p, int t)
                     break;
                 ptx::tc_fence_after();
                 if (lane == 0) {
-                    const uint32_t klo = k_lo0 + ((kv_base + (j + 1 - lo)) % kStages) * kTileLo;
+                    const uint32_t klo = k_lo0 + ((kv_base + (j + 1 - lo)) % kStages) * kKVLo;
 #pragma unroll
                     for (int kk = 0; kk < 4; ++kk)
                         ptx::mma_ss(tS, kHiK | (qlo + 2 * kk), kHiK | (klo + 2 * kk), idesc_qk,
@@ -279,10 +289,13 @@ __device__ void mma_role(const KernelCtx &cx, const StdParams &p, int t)
             ++pcount;
             ptx::tc_fence_after();
             if (lane == 0) {
-                const uint32_t vlo = v_lo0 + stage_j * kTileLo;
+                // O += P [V_j | 1]: V's second 64-column block (of which the
+                // MMA reads 16 columns) is the ones tile, LBO bytes away
+                const uint32_t vlo = v_lo0 + stage_j * kKVLo;
+                const uint64_t hi_v = umma_desc_hi((ones_lo - vlo) << 4, 1024, kSwizzle128B);
 #pragma unroll
-                for (int kk = 0; kk < BN / 16; ++kk)
-                    ptx::mma_ts(tO, tP + 8 * kk, kHiV | (vlo + 128 * kk), idesc_pv,
+                for (int kk = 0; kk < kBN / 16; ++kk)
+                    ptx::mma_ts(tO, tP + 8 * kk, hi_v | (vlo + 128 * kk), idesc_pv,
                                 (j > lot || kk > 0) ? 1u : 0u);
                 ptx::mma_commit(b_pvdone);
                 ptx::mma_commit(b_kve0 + stage_j * kBarStride); // this slot is done with tile j
@@ -315,9 +328,9 @@ __device__ void softmax_role(const KernelCtx &cx, const StdParams &p, int t)
     const int r = threadIdx.x & 127;             // row of the query tile = TMEM lane
     const uint32_t wq = (threadIdx.x >> 5) & 3;  // warp's quarter of the lanes
     const uint32_t lane_off = (wq * 32u) << 16;
-    const uint32_t tS = cx.tmem + lane_off + kColS + 128 * t;
-    const uint32_t tO = cx.tmem + lane_off + kColO + 64 * t;
-    const uint32_t tP = cx.tmem + lane_off + kColP + 64 * t;
+    const uint32_t tS = cx.tmem + lane_off + kColS + kStrideS * t;
+    const uint32_t tO = cx.tmem + lane_off + kColO + kStrideO * t;
+    const uint32_t tP = cx.tmem + lane_off + kColP + kStrideP * t;
     uint32_t scount = 0, pvcount = 0;
 
     for (int64_t L = blockIdx.x; L < p.grid.n_items; L += gridDim.x) {
@@ -326,7 +339,7 @@ __device__ void softmax_role(const KernelCtx &cx, const StdParams &p, int t)
             continue;
         const int b = it.b, h = it.h[t], qb = it.qb[t];
         const int i = qb * BM + r;
-        const TileRange tr = q_block_range(p.mask, b, qb * BM);
+        const TileRange tr = q_block_range<kBN>(p.mask, b, qb * BM);
         int row_lo, row_hi;
         row_interval(p.mask, b, i, row_lo, row_hi);
 
@@ -348,18 +361,18 @@ __device__ void softmax_role(const KernelCtx &cx, const StdParams &p, int t)
                 return;
             ++scount;
             ptx::tc_fence_after();
-            float x[BN];
-            load_scores(tS, x);
+            float x[kBN];
+            load_scores<kBN>(tS, x);
             ptx::tc_fence_before();
             ptx::mbar_arrive(bar(sm.s_free[t])); // S[t] may be overwritten
-            const int j0 = j * BN;
-            apply_score_mod<MOD>(x, smod, i, j0);
-            if (!((j0 >= tr.full_lo) && (j0 + BN <= tr.full_hi)))
-                apply_row_mask(x, j0, row_lo, row_hi);
-            uint32_t pk[BN / 2];
+            const int j0 = j * kBN;
+            apply_score_mod<MOD, kBN>(x, smod, i, j0);
+            if (!((j0 >= tr.full_lo) && (j0 + kBN <= tr.full_hi)))
+                apply_row_mask<kBN>(x, j0, row_lo, row_hi);
+            uint32_t pk[kBN / 2];
             bool rescale;
-            const float alpha =
-                softmax_compute_p(x, MOD == MOD_NONE ? p.qk_log2 : 1.f, st, j == tr.lo, pk, rescale);
+            const float alpha = softmax_compute_p_exact_sum<kBN>(
+                x, MOD == MOD_NONE ? p.qk_log2 : 1.f, st, j == tr.lo, pk, rescale);
             if (j > tr.lo) {
                 // the previous tile's P V has consumed P[t] and landed in O[t]
                 if (!warp_wait(bar(sm.pv_done[t]), pvcount & 1, cx.wc, W_O_FULL))
@@ -367,9 +380,9 @@ __device__ void softmax_role(const KernelCtx &cx, const StdParams &p, int t)
                 ++pvcount;
                 ptx::tc_fence_after();
                 if (rescale)
-                    rescale_o<64>(tO, alpha);
+                    rescale_o<kDvExt>(tO, alpha);
             }
-            store_p(tP, pk);
+            store_p<kBN>(tP, pk);
             ptx::tc_fence_before();
             ptx::mbar_arrive(bar(sm.p_full[t]));
             ++ntiles;
@@ -380,13 +393,16 @@ __device__ void softmax_role(const KernelCtx &cx, const StdParams &p, int t)
             return;
         ++pvcount;
         ptx::tc_fence_after();
-        uint32_t o[64];
+        uint32_t o[64], sum[1];
         ptx::tmem_ld32(tO, o);
         ptx::tmem_ld32(tO + 32, o + 32);
+        ptx::tmem_ld1(tO + kColSum, sum);
         ptx::tmem_wait_ld();
         ptx::reg_fence<32>(o);
         ptx::reg_fence<32>(o + 32);
-        const float inv = row_inv_norm(st);
+        ptx::reg_fence<1>(sum);
+        const float l_round = __uint_as_float(sum[0]);
+        const float inv = l_round > 0.f ? 1.f / l_round : 0.f;
         if (i < p.mask.S) {
             __nv_bfloat16 *dst = p.out + b * p.o_sb + static_cast<int64_t>(i) * p.o_ss + h * p.o_sh;
             uint4 *d4 = reinterpret_cast<uint4 *>(dst);
@@ -417,6 +433,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     StdSmem *sm = reinterpret_cast<StdSmem *>(smem_raw + ((1024u - (base & 1023u)) & 1023u));
     const int warp = threadIdx.x >> 5;
 
+    // the ones tile (bf16 1.0 pairs), read by the tensor core through the async proxy
+    for (uint32_t w = threadIdx.x; w < kTileBytes / 4; w += kThreads)
+        reinterpret_cast<uint32_t *>(sm->ones)[w] = 0x3F803F80u;
+    ptx::fence_proxy_async_smem();
     if (threadIdx.x == 0) {
         for (int b = 0; b < 2; ++b) {
             ptx::mbar_init(bar(sm->q_full[b]), 1);

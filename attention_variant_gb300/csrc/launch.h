@@ -78,6 +78,9 @@ cudaError_t launch_evo(const CUtensorMap &tq, const CUtensorMap &tk, const CUten
                        const CUtensorMap &tb, const EvoParams &p, int grid, cudaStream_t stream);
 int evo_max_bias_keys();
 
+// Keys per K/V tile of the standard kernel (its TMEM budget: see fwd_standard.cu).
+constexpr int kStdKeyTile = 112;
+
 cudaError_t launch_standard(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
                             const StdParams &p, int grid, cudaStream_t stream);
 size_t standard_smem_bytes();

@@ -37,38 +37,43 @@ struct ScoreMod {
     float softcap_out; // cap * log2(e)                       (softcap)
 };
 
-// Loads the 128 scores of this thread's row from TMEM columns [tS, tS + 128).
-__device__ __forceinline__ void load_scores(uint32_t tS, float (&x)[BN])
+// Loads the N scores (N a multiple of 16) of this thread's row from TMEM
+// columns [tS, tS + N).
+template <int N = BN>
+__device__ __forceinline__ void load_scores(uint32_t tS, float (&x)[N])
 {
-    uint32_t raw[BN];
+    static_assert(N % 16 == 0, "tile width must be a multiple of 16");
+    uint32_t raw[N];
 #pragma unroll
-    for (int c = 0; c < BN / 32; ++c)
+    for (int c = 0; c < N / 32; ++c)
         ptx::tmem_ld32(tS + 32 * c, raw + 32 * c);
+    if constexpr (N % 32 != 0)
+        ptx::tmem_ld16(tS + 32 * (N / 32), raw + 32 * (N / 32));
     ptx::tmem_wait_ld();
 #pragma unroll
-    for (int c = 0; c < BN / 32; ++c)
-        ptx::reg_fence<32>(raw + 32 * c);
+    for (int c = 0; c < N / 16; ++c)
+        ptx::reg_fence<16>(raw + 16 * c);
 #pragma unroll
-    for (int e = 0; e < BN; ++e)
+    for (int e = 0; e < N; ++e)
         x[e] = __uint_as_float(raw[e]);
 }
 
 // Scores -> logits for query row i and keys j0 .. j0 + 127.  For MOD_NONE the
 // scores stay unscaled (the scale is applied in the exponent); the other
 // score_mods produce log2-domain logits.
-template <int MOD>
-__device__ __forceinline__ void apply_score_mod(float (&x)[BN], const ScoreMod &sm, int i, int j0)
+template <int MOD, int N = BN>
+__device__ __forceinline__ void apply_score_mod(float (&x)[N], const ScoreMod &sm, int i, int j0)
 {
     if constexpr (MOD == MOD_ALIBI) {
         // z - slope |i - j|, in log2 units
         const float d0 = static_cast<float>(j0 - i);
 #pragma unroll
-        for (int e = 0; e < BN; ++e)
+        for (int e = 0; e < N; ++e)
             x[e] = fmaf(x[e], sm.qk_log2, -sm.alibi_c * fabsf(d0 + static_cast<float>(e)));
     } else if constexpr (MOD == MOD_SOFTCAP) {
         // cap * tanh(z / cap) with tanh(u) = 1 - 2 / (1 + e^(2u)), in log2 units
 #pragma unroll
-        for (int e = 0; e < BN; ++e) {
+        for (int e = 0; e < N; ++e) {
             const float ex = ptx::ex2(x[e] * sm.softcap_in);
             x[e] = sm.softcap_out * (1.f - 2.f * ptx::rcp_approx(1.f + ex));
         }
@@ -76,11 +81,12 @@ __device__ __forceinline__ void apply_score_mod(float (&x)[BN], const ScoreMod &
 }
 
 // Keys outside [row_lo, row_hi) -> -inf (only on tiles that hold masked pairs).
-__device__ __forceinline__ void apply_row_mask(float (&x)[BN], int j0, int row_lo, int row_hi)
+template <int N = BN>
+__device__ __forceinline__ void apply_row_mask(float (&x)[N], int j0, int row_lo, int row_hi)
 {
     const int a = row_lo - j0, z = row_hi - j0;
 #pragma unroll
-    for (int e = 0; e < BN; ++e)
+    for (int e = 0; e < N; ++e)
         if (e < a || e >= z)
             x[e] = kNegInf;
 }
@@ -216,8 +222,9 @@ __device__ __forceinline__ float softmax_compute_p(float (&x)[BN], float c, RowS
 // As softmax_compute_p, for kernels whose P V product also produces the sum
 // of the rounded P (an extra output column multiplied by ones): only the
 // exact sum `l` is kept here; st.l_round is left untouched.
-__device__ __forceinline__ float softmax_compute_p_exact_sum(float (&x)[BN], float c, RowState &st,
-                                                             bool first, uint32_t (&pk)[BN / 2],
+template <int N = BN>
+__device__ __forceinline__ float softmax_compute_p_exact_sum(float (&x)[N], float c, RowState &st,
+                                                             bool first, uint32_t (&pk)[N / 2],
                                                              bool &rescale)
 {
     float mc[4];
@@ -225,7 +232,7 @@ __device__ __forceinline__ float softmax_compute_p_exact_sum(float (&x)[BN], flo
     for (int q = 0; q < 4; ++q)
         mc[q] = fmaxf(x[2 * q], x[2 * q + 1]);
 #pragma unroll
-    for (int e = 8; e < BN; e += 8) {
+    for (int e = 8; e < N; e += 8) {
 #pragma unroll
         for (int q = 0; q < 4; ++q)
             mc[q] = ptx::max3(mc[q], x[e + 2 * q], x[e + 2 * q + 1]);
@@ -248,7 +255,7 @@ __device__ __forceinline__ float softmax_compute_p_exact_sum(float (&x)[BN], flo
     const float nmu = (st.m_ref == kNegInf) ? 0.f : -st.m_ref;
     float le[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-    for (int e = 0; e < BN / 2; ++e) {
+    for (int e = 0; e < N / 2; ++e) {
         float a0, a1;
         ptx::fma2(a0, a1, x[2 * e], x[2 * e + 1], c, c, nmu, nmu);
         const float p0 = ptx::ex2(a0);
@@ -263,8 +270,9 @@ __device__ __forceinline__ float softmax_compute_p_exact_sum(float (&x)[BN], flo
 
 // As softmax_compute_p_exact_sum, without any row sum (for kernels whose P V
 // product produces the rounded sum and whose caller needs no log-sum-exp).
-__device__ __forceinline__ float softmax_compute_p_no_sum(float (&x)[BN], float c, RowState &st,
-                                                          bool first, uint32_t (&pk)[BN / 2],
+template <int N = BN>
+__device__ __forceinline__ float softmax_compute_p_no_sum(float (&x)[N], float c, RowState &st,
+                                                          bool first, uint32_t (&pk)[N / 2],
                                                           bool &rescale)
 {
     float mc[4];
@@ -272,7 +280,7 @@ __device__ __forceinline__ float softmax_compute_p_no_sum(float (&x)[BN], float 
     for (int q = 0; q < 4; ++q)
         mc[q] = fmaxf(x[2 * q], x[2 * q + 1]);
 #pragma unroll
-    for (int e = 8; e < BN; e += 8) {
+    for (int e = 8; e < N; e += 8) {
 #pragma unroll
         for (int q = 0; q < 4; ++q)
             mc[q] = ptx::max3(mc[q], x[e + 2 * q], x[e + 2 * q + 1]);
@@ -293,7 +301,7 @@ __device__ __forceinline__ float softmax_compute_p_no_sum(float (&x)[BN], float 
     }
     const float nmu = (st.m_ref == kNegInf) ? 0.f : -st.m_ref;
 #pragma unroll
-    for (int e = 0; e < BN / 2; ++e) {
+    for (int e = 0; e < N / 2; ++e) {
         float a0, a1;
         ptx::fma2(a0, a1, x[2 * e], x[2 * e + 1], c, c, nmu, nmu);
         pk[e] = ptx::pack_bf16(ptx::ex2(a0), ptx::ex2(a1));
@@ -318,12 +326,15 @@ __device__ __forceinline__ void rescale_o(uint32_t tO, float alpha)
     }
 }
 
-// P (packed bf16, 64 columns) -> TMEM at tP; completes the stores.
-__device__ __forceinline__ void store_p(uint32_t tP, const uint32_t (&pk)[BN / 2])
+// P (packed bf16, N / 2 columns) -> TMEM at tP; completes the stores.
+template <int N = BN>
+__device__ __forceinline__ void store_p(uint32_t tP, const uint32_t (&pk)[N / 2])
 {
 #pragma unroll
-    for (int k = 0; k < BN / 32; ++k)
+    for (int k = 0; k < N / 32; ++k)
         ptx::tmem_st16(tP + 16 * k, pk + 16 * k);
+    if constexpr (N % 32 != 0)
+        ptx::tmem_st8(tP + 16 * (N / 32), pk + 16 * (N / 32));
     ptx::tmem_wait_st();
 }
 
