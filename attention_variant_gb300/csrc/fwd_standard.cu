@@ -9,15 +9,15 @@
 // moves (e^(x-y) = e^x / e^y), O += P V, never writing S or P to memory.
 //
 // CTA organisation (persistent: one CTA per SM, 384 threads):
-//   warps 0-3  softmax warpgroup of slot 0 (one thread per query row)
-//   warps 4-7  softmax warpgroup of slot 1
-//   warp  8    TMA producer: Q tiles once per work item, K/V tiles through an
+//   warp  0    TMA producer: Q tiles once per work item, K/V tiles through an
 //              NS-stage mbarrier ring
-//   warp  9    MMA issuer of slot 0 (one thread) and TMEM owner
-//   warp  10   MMA issuer of slot 1
-//   warp  11   idle (it completes the third warpgroup)
+//   warp  1    issues S = Q K^T for both slots (one thread); TMEM owner
+//   warp  2    issues O += P V for slot 0
+//   warp  3    issues O += P V for slot 1
+//   warps 4-7  softmax warpgroup of slot 0 (one thread per query row)
+//   warps 8-11 softmax warpgroup of slot 1
 // The kernel is compiled for 168 registers per thread; after set-up the two
-// softmax warpgroups raise their limit to kRegsSoftmax and the third lowers
+// softmax warpgroups raise their limit to kRegsSoftmax and the first lowers
 // its own to kRegsOther, with 2*128*kRegsSoftmax + 128*kRegsOther equal to
 // 384*168 so the raise is always satisfiable (the host checks the compiled
 // register count before launching).
@@ -31,12 +31,13 @@
 // 384 + 64 t.  The softmax then keeps only the exact sum (for the LSE).
 //
 // Hand-off protocol for slot t and key tile j (all mbarriers):
-//   softmax: wait s_full(t); S[t] -> registers; arrive s_free(t);
-//            score_mod, mask, row max, P in registers; wait pv_done(t) [the
-//            P V of tile j-1 has read P[t] and landed in O[t]]; lazily rescale
-//            O[t]; P -> TMEM; arrive p_full(t).
-//   MMA:     wait s_free(t), issue S[t] = Q[t] K_{j+1}^T, commit s_full(t);
-//            later wait p_full(t), issue O[t] += P[t] V_j, commit pv_done(t).
+//   softmax: wait s_full(t); S[t] -> registers; arrive s_free(t); take the
+//            turn; score_mod, mask, row max, P in registers; pass the turn;
+//            wait pv_done(t) [the P V of tile j-1 has read P[t] and landed in
+//            O[t]]; lazily rescale O[t]; P -> TMEM; arrive p_full(t).
+//   S warp:  wait s_free(t) [S(j) copied out], issue S[t] = Q[t] K_{j+1}^T,
+//            commit s_full(t).
+//   P V warp t: wait p_full(t), issue O[t] += P[t] V_j, commit pv_done(t).
 // The next QK^T starts as soon as the softmax has copied the scores out of
 // TMEM, so its latency hides behind the exponentials, and P has its own TMEM
 // columns so the next S never overwrites a P still being read.  Q is
@@ -76,7 +77,8 @@ struct __align__(1024) StdSmem {
     uint64_t q_full[2], q_empty[2];
     uint64_t kv_full[kStages], kv_empty[kStages];
     uint64_t s_full[2], s_free[2], p_full[2], pv_done[2];
-    uint64_t final_bar[2];
+    uint64_t turn[2];            // exponential-phase token of each softmax warpgroup
+    uint64_t final_bar[3];
     uint32_t tmem_base;
     uint32_t abort_flag;
 };
@@ -167,46 +169,126 @@ __device__ void producer_role(const KernelCtx &cx, const StdParams &p, const CUt
 
 // ------------------------------------------------------------------ MMA issuers
 //
-// Two MMA warps, one per slot, so each slot's S -> softmax -> P V chain moves
-// independently and the tensor core interleaves the two.  Each keeps its state
-// in registers and builds descriptors as (constant high word) | (14-bit start
-// address).  kv_empty and q_empty take one arrival from each warp: a warp
-// commits after its last MMA reading the tile (or Q buffer), or -- for a tile
-// its slot does not use -- arrives once the tile has landed, which proves the
-// stage's previous phase is complete.
-__device__ __forceinline__ bool wait_kv_tiles(const KernelCtx &cx, uint32_t bar_kvf0,
-                                              uint32_t kv_base, int rel, int &waited)
-{
-    while (waited <= rel) {
-        const uint32_t idx = kv_base + static_cast<uint32_t>(waited);
-        if (!warp_wait(bar_kvf0 + (idx % kStages) * static_cast<uint32_t>(sizeof(uint64_t)),
-                       (idx / kStages) & 1, cx.wc, W_KV_FULL))
-            return false;
-        ++waited;
-    }
-    return true;
-}
+// A tcgen05.mma returns to its issuing thread only once the tensor core has
+// accepted it, and the MMAs of one accumulation chain advance ~110-150 cycles
+// apart (measured), so one thread issuing a slot's Q K^T and P V chains one
+// after the other spends most of a tile blocked in issue.  Each chain kind
+// therefore has its own issuing warp: warp 1 issues S = Q K^T for both slots
+// (in tile order, slot 0 then slot 1), warps 2 and 3 issue O += P V for slot
+// 0 and slot 1.  Descriptors are (constant high word) | (14-bit start
+// address).
+//
+// Buffer release: a K/V stage is free once both slots are done with it.  S(j)
+// of a slot completes before its softmax can publish P(j) and so before P V(j)
+// is issued, hence the P V warp's commit after P V(j) also covers the K read;
+// kv_empty takes one arrival per P V warp (a commit, or -- for a tile its slot
+// does not use -- an arrival once the tile has landed, which proves the
+// stage's previous phase complete).  q_empty takes one arrival per slot from
+// the S warp (a commit after the slot's last S of the item, or an arrival for
+// an absent slot).
+__device__ __forceinline__ uint32_t kv_stage(uint32_t idx) { return idx % kStages; }
+__device__ __forceinline__ uint32_t kv_parity(uint32_t idx) { return (idx / kStages) & 1; }
 
-__device__ void mma_role(const KernelCtx &cx, const StdParams &p, int t)
+__device__ void s_role(const KernelCtx &cx, const StdParams &p)
 {
     StdSmem &sm = *cx.sm;
     const uint32_t lane = ptx::lane_id();
     constexpr uint32_t idesc_qk = umma_idesc_bf16(BM, kBN, false);
-    constexpr uint32_t idesc_pv = umma_idesc_bf16(BM, kDvExt, true);
     constexpr uint64_t kHiK = umma_desc_hi(16, 1024, kSwizzle128B); // Q, K: K-major
     constexpr uint32_t kTileLo = kTileBytes >> 4, kKVLo = kKVBytes >> 4;
     constexpr uint32_t kBarStride = sizeof(uint64_t);
-    const uint32_t q_lo0 = ptx::smem_u32(sm.q[0][t]) >> 4;
+    const uint32_t q_lo0 = ptx::smem_u32(sm.q[0][0]) >> 4;
     const uint32_t k_lo0 = ptx::smem_u32(sm.k[0]) >> 4;
+    const uint32_t b_kvf0 = bar(sm.kv_full[0]);
+
+    uint32_t kv_base = 0, item_count = 0;
+    uint32_t issued[2] = {0u, 0u};
+    bool ok = true;
+    for (int64_t L = blockIdx.x; L < p.grid.n_items && ok; L += gridDim.x) {
+        const Item it = decode_item(p.grid, L);
+        int lo = 1 << 30, hi = 0, rlo[2] = {0, 0}, rhi[2] = {0, 0};
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+            if (!it.valid[u])
+                continue;
+            const TileRange r = q_block_range<kBN>(p.mask, it.b, it.qb[u] * BM);
+            rlo[u] = r.lo;
+            rhi[u] = r.hi;
+            lo = min(lo, r.lo);
+            hi = max(hi, r.hi);
+        }
+        const uint32_t qbuf = item_count & 1;
+        const uint32_t b_qe = bar(sm.q_empty[qbuf]);
+        ok = warp_wait(bar(sm.q_full[qbuf]), (item_count >> 1) & 1, cx.wc, W_Q_FULL);
+        if (!ok)
+            break;
+        for (int j = lo; j < hi && ok; ++j) {
+            const uint32_t idx = kv_base + static_cast<uint32_t>(j - lo);
+            ok = warp_wait(b_kvf0 + kv_stage(idx) * kBarStride, kv_parity(idx), cx.wc, W_KV_FULL);
+            if (!ok)
+                break;
+            const uint32_t klo = k_lo0 + kv_stage(idx) * kKVLo;
+#pragma unroll
+            for (int t = 0; t < 2; ++t) {
+                if (!it.valid[t] || j < rlo[t] || j >= rhi[t])
+                    continue;
+                if (issued[t] > 0) {
+                    // the softmax has copied the slot's previous S out of TMEM
+                    ok = warp_wait(bar(sm.s_free[t]), (issued[t] - 1) & 1, cx.wc, W_S_FULL);
+                    if (!ok)
+                        break;
+                }
+                ++issued[t];
+                ptx::tc_fence_after();
+                if (lane == 0) {
+                    const uint32_t qlo = q_lo0 + (2 * qbuf + t) * kTileLo;
+                    const uint32_t tS = cx.tmem + kColS + kStrideS * t;
+#pragma unroll
+                    for (int kk = 0; kk < 4; ++kk)
+                        ptx::mma_ss(tS, kHiK | (qlo + 2 * kk), kHiK | (klo + 2 * kk), idesc_qk,
+                                    kk > 0 ? 1u : 0u);
+                    ptx::mma_commit(bar(sm.s_full[t]));
+                    if (j + 1 == rhi[t])
+                        ptx::mma_commit(b_qe); // the slot's last read of this Q buffer
+                }
+                __syncwarp();
+            }
+        }
+        if (!ok)
+            break;
+#pragma unroll
+        for (int t = 0; t < 2; ++t)
+            if (!it.valid[t]) {
+                if (lane == 0)
+                    ptx::mbar_arrive(b_qe);
+                __syncwarp();
+            }
+        kv_base += static_cast<uint32_t>(hi - lo);
+        ++item_count;
+    }
+    // Every MMA this thread issued has completed before TMEM is released.
+    const uint32_t b_final = bar(sm.final_bar[0]);
+    if (lane == 0)
+        ptx::mma_commit(b_final);
+    __syncwarp();
+    mbar_wait_drain(b_final, 0, cx.wc, W_FINAL);
+}
+
+__device__ void pv_role(const KernelCtx &cx, const StdParams &p, int t)
+{
+    StdSmem &sm = *cx.sm;
+    const uint32_t lane = ptx::lane_id();
+    constexpr uint32_t idesc_pv = umma_idesc_bf16(BM, kDvExt, true);
+    constexpr uint32_t kKVLo = kKVBytes >> 4;
+    constexpr uint32_t kBarStride = sizeof(uint64_t);
     const uint32_t v_lo0 = ptx::smem_u32(sm.v[0]) >> 4;
     const uint32_t ones_lo = ptx::smem_u32(sm.ones) >> 4;
-    const uint32_t tS = cx.tmem + kColS + kStrideS * t, tO = cx.tmem + kColO + kStrideO * t;
+    const uint32_t tO = cx.tmem + kColO + kStrideO * t;
     const uint32_t tP = cx.tmem + kColP + kStrideP * t;
-    const uint32_t b_sfull = bar(sm.s_full[t]), b_sfree = bar(sm.s_free[t]);
     const uint32_t b_pfull = bar(sm.p_full[t]), b_pvdone = bar(sm.pv_done[t]);
     const uint32_t b_kvf0 = bar(sm.kv_full[0]), b_kve0 = bar(sm.kv_empty[0]);
 
-    uint32_t kv_base = 0, item_count = 0, fcount = 0, pcount = 0;
+    uint32_t kv_base = 0, pcount = 0;
     bool ok = true;
     for (int64_t L = blockIdx.x; L < p.grid.n_items && ok; L += gridDim.x) {
         const Item it = decode_item(p.grid, L);
@@ -224,63 +306,18 @@ __device__ void mma_role(const KernelCtx &cx, const StdParams &p, int t)
             }
         }
         const bool active = it.valid[t];
-        const uint32_t qbuf = item_count & 1;
-        const uint32_t b_qe = bar(sm.q_empty[qbuf]);
-        ok = warp_wait(bar(sm.q_full[qbuf]), (item_count >> 1) & 1, cx.wc, W_Q_FULL);
-        if (!ok)
-            break;
-        ptx::tc_fence_after();
-        const uint32_t qlo = q_lo0 + qbuf * 2 * kTileLo;
-        int waited = 0;
-
         for (int j = lo; j < hi && ok; ++j) {
-            const uint32_t stage_j = (kv_base + (j - lo)) % kStages;
+            const uint32_t idx = kv_base + static_cast<uint32_t>(j - lo);
+            const uint32_t stage = kv_stage(idx);
             if (!active || j < lot || j >= hit) {
                 // tile not used by this slot: release it once it has landed
-                if (!(ok = wait_kv_tiles(cx, b_kvf0, kv_base, j - lo, waited)))
+                ok = warp_wait(b_kvf0 + stage * kBarStride, kv_parity(idx), cx.wc, W_KV_FULL);
+                if (!ok)
                     break;
                 if (lane == 0)
-                    ptx::mbar_arrive(b_kve0 + stage_j * kBarStride);
+                    ptx::mbar_arrive(b_kve0 + stage * kBarStride);
                 __syncwarp();
                 continue;
-            }
-            if (j == lot) {
-                // first S of the item for this slot
-                if (!(ok = wait_kv_tiles(cx, b_kvf0, kv_base, j - lo, waited)))
-                    break;
-                ptx::tc_fence_after();
-                if (lane == 0) {
-                    const uint32_t klo = k_lo0 + stage_j * kKVLo;
-#pragma unroll
-                    for (int kk = 0; kk < 4; ++kk)
-                        ptx::mma_ss(tS, kHiK | (qlo + 2 * kk), kHiK | (klo + 2 * kk), idesc_qk,
-                                    kk > 0 ? 1u : 0u);
-                    ptx::mma_commit(b_sfull);
-                    if (j + 1 == hit)
-                        ptx::mma_commit(b_qe); // last read of this Q buffer
-                }
-                __syncwarp();
-            }
-            // the softmax has copied S(j) out of TMEM: issue S(j + 1)
-            ok = warp_wait(b_sfree, fcount & 1, cx.wc, W_S_FULL);
-            if (!ok)
-                break;
-            ++fcount;
-            if (j + 1 < hit) {
-                if (!(ok = wait_kv_tiles(cx, b_kvf0, kv_base, j + 1 - lo, waited)))
-                    break;
-                ptx::tc_fence_after();
-                if (lane == 0) {
-                    const uint32_t klo = k_lo0 + ((kv_base + (j + 1 - lo)) % kStages) * kKVLo;
-#pragma unroll
-                    for (int kk = 0; kk < 4; ++kk)
-                        ptx::mma_ss(tS, kHiK | (qlo + 2 * kk), kHiK | (klo + 2 * kk), idesc_qk,
-                                    kk > 0 ? 1u : 0u);
-                    ptx::mma_commit(b_sfull);
-                    if (j + 2 == hit)
-                        ptx::mma_commit(b_qe);
-                }
-                __syncwarp();
             }
             // the softmax has written P(j) and rescaled O: issue P V(j)
             ok = warp_wait(b_pfull, pcount & 1, cx.wc, W_P_FULL);
@@ -291,29 +328,20 @@ __device__ void mma_role(const KernelCtx &cx, const StdParams &p, int t)
             if (lane == 0) {
                 // O += P [V_j | 1]: V's second 64-column block (of which the
                 // MMA reads 16 columns) is the ones tile, LBO bytes away
-                const uint32_t vlo = v_lo0 + stage_j * kKVLo;
+                const uint32_t vlo = v_lo0 + stage * kKVLo;
                 const uint64_t hi_v = umma_desc_hi((ones_lo - vlo) << 4, 1024, kSwizzle128B);
 #pragma unroll
                 for (int kk = 0; kk < kBN / 16; ++kk)
                     ptx::mma_ts(tO, tP + 8 * kk, hi_v | (vlo + 128 * kk), idesc_pv,
                                 (j > lot || kk > 0) ? 1u : 0u);
                 ptx::mma_commit(b_pvdone);
-                ptx::mma_commit(b_kve0 + stage_j * kBarStride); // this slot is done with tile j
+                ptx::mma_commit(b_kve0 + stage * kBarStride); // this slot is done with tile j
             }
             __syncwarp();
         }
-        if (!ok)
-            break;
-        if (!active) {
-            if (lane == 0)
-                ptx::mbar_arrive(b_qe);
-            __syncwarp();
-        }
         kv_base += static_cast<uint32_t>(hi - lo);
-        ++item_count;
     }
-    // Every MMA this thread issued has completed before TMEM is released.
-    const uint32_t b_final = bar(sm.final_bar[t]);
+    const uint32_t b_final = bar(sm.final_bar[1 + t]);
     if (lane == 0)
         ptx::mma_commit(b_final);
     __syncwarp();
@@ -321,6 +349,19 @@ __device__ void mma_role(const KernelCtx &cx, const StdParams &p, int t)
 }
 
 // ------------------------------------------------------------------ softmax
+//
+// The two softmax warpgroups take turns on the exponential phase (score_mod,
+// mask, max, P and the sum): warpgroup t computes P only while it holds the
+// turn, then hands it to the other one.  Without the turns both warpgroups
+// run their exponentials at the same time on the same SM sub-partitions and
+// then both wait for their tensor-core chains; with them one slot's
+// exponentials overlap the other slot's Q K^T and P V (ping-pong).  Every work
+// item takes max(n_0, n_1) turns, n_t being slot t's tile count (0 for an
+// absent slot): the slot with fewer tiles takes empty turns, so both
+// warpgroups pass the turn the same number of times.  The turn is an mbarrier
+// pair (a bounded wait, like every other wait of the kernel): turn k of
+// warpgroup 1 waits for warpgroup 0's k-th pass, turn k > 0 of warpgroup 0 for
+// warpgroup 1's (k-1)-th; warpgroup 0's first turn is free.
 template <int MOD>
 __device__ void softmax_role(const KernelCtx &cx, const StdParams &p, int t)
 {
@@ -331,17 +372,25 @@ __device__ void softmax_role(const KernelCtx &cx, const StdParams &p, int t)
     const uint32_t tS = cx.tmem + lane_off + kColS + kStrideS * t;
     const uint32_t tO = cx.tmem + lane_off + kColO + kStrideO * t;
     const uint32_t tP = cx.tmem + lane_off + kColP + kStrideP * t;
-    uint32_t scount = 0, pvcount = 0;
+    const uint32_t b_turn_mine = bar(sm.turn[t]), b_turn_other = bar(sm.turn[t ^ 1]);
+    uint32_t scount = 0, pvcount = 0, turns = 0;
 
     for (int64_t L = blockIdx.x; L < p.grid.n_items; L += gridDim.x) {
         const Item it = decode_item(p.grid, L);
-        if (!it.valid[t])
-            continue;
+        const bool mine = it.valid[t];
         const int b = it.b, h = it.h[t], qb = it.qb[t];
         const int i = qb * BM + r;
         const TileRange tr = q_block_range<kBN>(p.mask, b, qb * BM);
-        int row_lo, row_hi;
-        row_interval(p.mask, b, i, row_lo, row_hi);
+        const int n_mine = mine ? tr.hi - tr.lo : 0;
+        int n_other = 0;
+        if (it.valid[t ^ 1]) {
+            const TileRange to = q_block_range<kBN>(p.mask, b, it.qb[t ^ 1] * BM);
+            n_other = to.hi - to.lo;
+        }
+        const int n_turns = max(n_mine, n_other);
+        int row_lo = 0, row_hi = 0;
+        if (mine)
+            row_interval(p.mask, b, i, row_lo, row_hi);
 
         ScoreMod smod;
         smod.qk_log2 = p.qk_log2;
@@ -349,14 +398,26 @@ __device__ void softmax_role(const KernelCtx &cx, const StdParams &p, int t)
         smod.softcap_out = p.softcap_out;
         smod.alibi_c = 0.f;
         if constexpr (MOD == MOD_ALIBI) {
-            const float slope = p.alibi_slopes ? __ldg(p.alibi_slopes + h)
-                                               : exp2f(p.alibi_exp_coef * static_cast<float>(h + 1));
-            smod.alibi_c = slope * kLog2e;
+            if (mine) {
+                const float slope = p.alibi_slopes
+                                        ? __ldg(p.alibi_slopes + h)
+                                        : exp2f(p.alibi_exp_coef * static_cast<float>(h + 1));
+                smod.alibi_c = slope * kLog2e;
+            }
         }
 
         RowState st{kNegInf, 0.f, 0.f};
-        int ntiles = 0;
-        for (int j = tr.lo; j < tr.hi; ++j) {
+        for (int k = 0; k < n_turns; ++k, ++turns) {
+            const uint32_t phase = t == 1 ? turns : turns - 1;
+            const bool free_turn = t == 0 && turns == 0; // warpgroup 0's first turn
+            if (k >= n_mine) {
+                // empty turn: pass the token on
+                if (!free_turn && !warp_wait(b_turn_mine, phase & 1, cx.wc, W_TURN))
+                    return;
+                ptx::mbar_arrive(b_turn_other);
+                continue;
+            }
+            const int j = tr.lo + k;
             if (!warp_wait(bar(sm.s_full[t]), scount & 1, cx.wc, W_S_FULL))
                 return;
             ++scount;
@@ -365,6 +426,8 @@ __device__ void softmax_role(const KernelCtx &cx, const StdParams &p, int t)
             load_scores<kBN>(tS, x);
             ptx::tc_fence_before();
             ptx::mbar_arrive(bar(sm.s_free[t])); // S[t] may be overwritten
+            if (!free_turn && !warp_wait(b_turn_mine, phase & 1, cx.wc, W_TURN))
+                return;
             const int j0 = j * kBN;
             apply_score_mod<MOD, kBN>(x, smod, i, j0);
             if (!((j0 >= tr.full_lo) && (j0 + kBN <= tr.full_hi)))
@@ -372,8 +435,9 @@ __device__ void softmax_role(const KernelCtx &cx, const StdParams &p, int t)
             uint32_t pk[kBN / 2];
             bool rescale;
             const float alpha = softmax_compute_p_exact_sum<kBN>(
-                x, MOD == MOD_NONE ? p.qk_log2 : 1.f, st, j == tr.lo, pk, rescale);
-            if (j > tr.lo) {
+                x, MOD == MOD_NONE ? p.qk_log2 : 1.f, st, k == 0, pk, rescale);
+            ptx::mbar_arrive(b_turn_other); // hand the turn over
+            if (k > 0) {
                 // the previous tile's P V has consumed P[t] and landed in O[t]
                 if (!warp_wait(bar(sm.pv_done[t]), pvcount & 1, cx.wc, W_O_FULL))
                     return;
@@ -385,8 +449,9 @@ __device__ void softmax_role(const KernelCtx &cx, const StdParams &p, int t)
             store_p<kBN>(tP, pk);
             ptx::tc_fence_before();
             ptx::mbar_arrive(bar(sm.p_full[t]));
-            ++ntiles;
         }
+        if (!mine)
+            continue;
 
         // epilogue: O / l -> bf16, LSE
         if (!warp_wait(bar(sm.pv_done[t]), pvcount & 1, cx.wc, W_O_FULL))
@@ -419,7 +484,7 @@ __device__ void softmax_role(const KernelCtx &cx, const StdParams &p, int t)
                 p.lse[b * p.l_sb + h * p.l_sh + i] = row_lse(st);
         }
         if (p.tile_counts && r == 0)
-            p.tile_counts[(static_cast<int64_t>(b) * p.grid.Hq + h) * p.grid.nq + qb] = ntiles;
+            p.tile_counts[(static_cast<int64_t>(b) * p.grid.Hq + h) * p.grid.nq + qb] = n_mine;
     }
 }
 
@@ -440,30 +505,31 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (threadIdx.x == 0) {
         for (int b = 0; b < 2; ++b) {
             ptx::mbar_init(bar(sm->q_full[b]), 1);
-            ptx::mbar_init(bar(sm->q_empty[b]), 2); // one arrival per MMA warp
+            ptx::mbar_init(bar(sm->q_empty[b]), 2); // one arrival per slot (S warp)
         }
         for (int s = 0; s < kStages; ++s) {
             ptx::mbar_init(bar(sm->kv_full[s]), 1);
-            ptx::mbar_init(bar(sm->kv_empty[s]), 2); // one arrival per MMA warp
+            ptx::mbar_init(bar(sm->kv_empty[s]), 2); // one arrival per P V warp
         }
         for (int t = 0; t < 2; ++t) {
             ptx::mbar_init(bar(sm->s_full[t]), 1);
             ptx::mbar_init(bar(sm->p_full[t]), 128);
             ptx::mbar_init(bar(sm->s_free[t]), 128);
             ptx::mbar_init(bar(sm->pv_done[t]), 1);
+            ptx::mbar_init(bar(sm->turn[t]), 128);  // arrived by the other warpgroup
         }
-        ptx::mbar_init(bar(sm->final_bar[0]), 1);
-        ptx::mbar_init(bar(sm->final_bar[1]), 1);
+        for (int b = 0; b < 3; ++b)
+            ptx::mbar_init(bar(sm->final_bar[b]), 1);
         sm->abort_flag = 0;
         ptx::fence_mbarrier_init();
         ptx::fence_proxy_async_smem();
     }
-    if (warp == 8 && ptx::lane_id() == 0) {
+    if (warp == 0 && ptx::lane_id() == 0) {
         ptx::prefetch_tensormap(&tm_q);
         ptx::prefetch_tensormap(&tm_k);
         ptx::prefetch_tensormap(&tm_v);
     }
-    if (warp == 9) {
+    if (warp == 1) {
         ptx::tmem_alloc(ptx::smem_u32(&sm->tmem_base), 512);
         ptx::tmem_relinquish();
     }
@@ -481,20 +547,22 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     // Each branch ends with its own copy of the teardown barrier, so no code
     // runs under both register limits.
-    if (warp < 8) {
+    if (warp >= 4) {
         ptx::setmaxnreg_inc<kRegsSoftmax>();
-        softmax_role<MOD>(cx, p, warp >> 2);
+        softmax_role<MOD>(cx, p, (warp >> 2) - 1);
         ptx::tc_fence_before();
         ptx::named_barrier_sync(1, kThreads);
     } else {
         ptx::setmaxnreg_dec<kRegsOther>();
-        if (warp == 8)
+        if (warp == 0)
             producer_role(cx, p, &tm_q, &tm_k, &tm_v);
-        else if (warp == 9 || warp == 10)
-            mma_role(cx, p, warp - 9);
+        else if (warp == 1)
+            s_role(cx, p);
+        else
+            pv_role(cx, p, warp - 2);
         ptx::tc_fence_before();
         ptx::named_barrier_sync(1, kThreads);
-        if (warp == 9) {
+        if (warp == 1) {
             ptx::tc_fence_after();
             ptx::tmem_dealloc(cx.tmem, 512);
         }

@@ -200,6 +200,16 @@ __device__ __forceinline__ void reg_fence(uint32_t *r)
     for (int i = 0; i < N; ++i)
         asm volatile("" : "+r"(r[i]));
 }
+// The same for float values: pins them to a point in the volatile-asm order
+// (used to keep register-only arithmetic between two barrier instructions).
+template <int N>
+__device__ __forceinline__ void reg_fence_f(float *r)
+{
+#pragma unroll
+    for (int i = 0; i < N; ++i)
+        asm volatile("" : "+f"(r[i]));
+}
+
 __device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
 // 32 lanes x 32 consecutive 32-bit columns: thread t of the warp receives
@@ -274,6 +284,12 @@ __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t *r)
 __device__ __forceinline__ void named_barrier_sync(uint32_t id, uint32_t count)
 {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
+
+// Arrive on named CTA barrier `id` (counted towards `count`) without waiting.
+__device__ __forceinline__ void named_barrier_arrive(uint32_t id, uint32_t count)
+{
+    asm volatile("bar.arrive %0, %1;" ::"r"(id), "r"(count) : "memory");
 }
 
 // Warpgroup-wide register re-allocation (all 128 threads of the warpgroup).
