@@ -358,13 +358,64 @@ __device__ void pv_role(const KernelCtx &cx, const StdParams &p, int t)
 // exponentials overlap the other slot's Q K^T and P V (ping-pong).  Every work
 // item takes max(n_0, n_1) turns, n_t being slot t's tile count (0 for an
 // absent slot): the slot with fewer tiles takes empty turns, so both
-// warpgroups pass the turn the same number of times.  The turn is an mbarrier
-// pair (a bounded wait, like every other wait of the kernel): turn k of
-// warpgroup 1 waits for warpgroup 0's k-th pass, turn k > 0 of warpgroup 0 for
-// warpgroup 1's (k-1)-th; warpgroup 0's first turn is free.
+// warpgroups pass the turn the same number of times.  Turn k of warpgroup 1
+// follows warpgroup 0's turn k, turn k > 0 of warpgroup 0 follows warpgroup
+// 1's turn k - 1, and warpgroup 0's first turn is free.
+//
+// How the turn is passed depends on the score_mod (chosen by measurement):
+//  * plain scores: an mbarrier pair (a bounded wait, like every other wait);
+//  * ALiBi and softcap, whose longer exponential phase gains from a faster
+//    hand-off: two named barriers (a woken barrier.sync resumes within a few
+//    cycles, an mbarrier wait took ~250).  Warpgroup 0 waits on barrier 2
+//    before each turn and warpgroup 1 arrives there once at the start and
+//    after each turn; warpgroup 1 waits on barrier 3 and warpgroup 0 arrives
+//    there after each turn; warpgroup 0 consumes warpgroup 1's last arrival
+//    at the end.  The non-aligned forms are used because the take and the
+//    pass appear on several paths (measured: the aligned forms, duplicated on
+//    short branches, stopped ordering the turns).  Named barriers cannot time
+//    out, so termination is by construction: a warp whose bounded mbarrier
+//    wait fails (the CTA is aborting) jumps out of its loops and takes and
+//    passes every remaining turn (drain_turns), so both warpgroups always
+//    execute the same sequence of barrier operations.  Register fences pin
+//    the scores after the take and P and the sum before the pass: barrier
+//    instructions have no register operands, so the compiler could otherwise
+//    move the arithmetic across them.
+__device__ __forceinline__ void nb_take(int t)
+{
+    asm volatile("barrier.sync %0, 256;" ::"r"(2 + t) : "memory");
+}
+
+__device__ __forceinline__ void nb_pass(int t)
+{
+    asm volatile("barrier.arrive %0, 256;" ::"r"(2 + (t ^ 1)) : "memory");
+}
+
+// Abort path (named-barrier turns): take and pass every turn of the CTA that
+// remains, from turn k_from of item L on, then (warpgroup 0) the final take.
+__device__ __forceinline__ void drain_turns(const StdParams &p, int t, int64_t L, int k_from)
+{
+    for (; L < p.grid.n_items; L += gridDim.x, k_from = 0) {
+        const Item it = decode_item(p.grid, L);
+        int n_turns = 0;
+#pragma unroll
+        for (int u = 0; u < 2; ++u)
+            if (it.valid[u]) {
+                const TileRange r = q_block_range<kBN>(p.mask, it.b, it.qb[u] * BM);
+                n_turns = max(n_turns, r.hi - r.lo);
+            }
+        for (int k = k_from; k < n_turns; ++k) {
+            nb_take(t);
+            nb_pass(t);
+        }
+    }
+    if (t == 0)
+        nb_take(t);
+}
+
 template <int MOD>
 __device__ void softmax_role(const KernelCtx &cx, const StdParams &p, int t)
 {
+    constexpr bool kNamed = MOD != MOD_NONE; // how the turn is passed (see above)
     StdSmem &sm = *cx.sm;
     const int r = threadIdx.x & 127;             // row of the query tile = TMEM lane
     const uint32_t wq = (threadIdx.x >> 5) & 3;  // warp's quarter of the lanes
@@ -374,6 +425,11 @@ __device__ void softmax_role(const KernelCtx &cx, const StdParams &p, int t)
     const uint32_t tP = cx.tmem + lane_off + kColP + kStrideP * t;
     const uint32_t b_turn_mine = bar(sm.turn[t]), b_turn_other = bar(sm.turn[t ^ 1]);
     uint32_t scount = 0, pvcount = 0, turns = 0;
+    int64_t fail_L = 0;
+    int fail_k = 0;
+    if constexpr (kNamed)
+        if (t == 1)
+            nb_pass(t); // warpgroup 0 takes the first turn
 
     for (int64_t L = blockIdx.x; L < p.grid.n_items; L += gridDim.x) {
         const Item it = decode_item(p.grid, L);
@@ -412,22 +468,37 @@ __device__ void softmax_role(const KernelCtx &cx, const StdParams &p, int t)
             const bool free_turn = t == 0 && turns == 0; // warpgroup 0's first turn
             if (k >= n_mine) {
                 // empty turn: pass the token on
-                if (!free_turn && !warp_wait(b_turn_mine, phase & 1, cx.wc, W_TURN))
-                    return;
-                ptx::mbar_arrive(b_turn_other);
+                if constexpr (kNamed) {
+                    nb_take(t);
+                    nb_pass(t);
+                } else {
+                    if (!free_turn && !warp_wait(b_turn_mine, phase & 1, cx.wc, W_TURN))
+                        return;
+                    ptx::mbar_arrive(b_turn_other);
+                }
                 continue;
             }
             const int j = tr.lo + k;
-            if (!warp_wait(bar(sm.s_full[t]), scount & 1, cx.wc, W_S_FULL))
-                return;
+            if (!warp_wait(bar(sm.s_full[t]), scount & 1, cx.wc, W_S_FULL)) {
+                if constexpr (!kNamed)
+                    return;
+                fail_L = L;
+                fail_k = k;
+                goto aborted;
+            }
             ++scount;
             ptx::tc_fence_after();
             float x[kBN];
             load_scores<kBN>(tS, x);
             ptx::tc_fence_before();
             ptx::mbar_arrive(bar(sm.s_free[t])); // S[t] may be overwritten
-            if (!free_turn && !warp_wait(b_turn_mine, phase & 1, cx.wc, W_TURN))
-                return;
+            if constexpr (kNamed) {
+                nb_take(t);
+                ptx::reg_fence_f<kBN>(x);
+            } else {
+                if (!free_turn && !warp_wait(b_turn_mine, phase & 1, cx.wc, W_TURN))
+                    return;
+            }
             const int j0 = j * kBN;
             apply_score_mod<MOD, kBN>(x, smod, i, j0);
             if (!((j0 >= tr.full_lo) && (j0 + kBN <= tr.full_hi)))
@@ -436,11 +507,22 @@ __device__ void softmax_role(const KernelCtx &cx, const StdParams &p, int t)
             bool rescale;
             const float alpha = softmax_compute_p_exact_sum<kBN>(
                 x, MOD == MOD_NONE ? p.qk_log2 : 1.f, st, k == 0, pk, rescale);
-            ptx::mbar_arrive(b_turn_other); // hand the turn over
+            if constexpr (kNamed) {
+                ptx::reg_fence<kBN / 2>(pk);
+                ptx::reg_fence_f<1>(&st.l);
+                nb_pass(t);
+            } else {
+                ptx::mbar_arrive(b_turn_other); // hand the turn over
+            }
             if (k > 0) {
                 // the previous tile's P V has consumed P[t] and landed in O[t]
-                if (!warp_wait(bar(sm.pv_done[t]), pvcount & 1, cx.wc, W_O_FULL))
-                    return;
+                if (!warp_wait(bar(sm.pv_done[t]), pvcount & 1, cx.wc, W_O_FULL)) {
+                    if constexpr (!kNamed)
+                        return;
+                    fail_L = L;
+                    fail_k = k + 1;
+                    goto aborted;
+                }
                 ++pvcount;
                 ptx::tc_fence_after();
                 if (rescale)
@@ -454,8 +536,13 @@ __device__ void softmax_role(const KernelCtx &cx, const StdParams &p, int t)
             continue;
 
         // epilogue: O / l -> bf16, LSE
-        if (!warp_wait(bar(sm.pv_done[t]), pvcount & 1, cx.wc, W_O_FULL))
-            return;
+        if (!warp_wait(bar(sm.pv_done[t]), pvcount & 1, cx.wc, W_O_FULL)) {
+            if constexpr (!kNamed)
+                return;
+            fail_L = L + gridDim.x;
+            fail_k = 0;
+            goto aborted;
+        }
         ++pvcount;
         ptx::tc_fence_after();
         uint32_t o[64], sum[1];
@@ -486,6 +573,13 @@ __device__ void softmax_role(const KernelCtx &cx, const StdParams &p, int t)
         if (p.tile_counts && r == 0)
             p.tile_counts[(static_cast<int64_t>(b) * p.grid.Hq + h) * p.grid.nq + qb] = n_mine;
     }
+    if constexpr (kNamed)
+        if (t == 0)
+            nb_take(t); // warpgroup 1's last arrival
+    return;
+aborted:
+    // (named-barrier turns only) match the other warpgroup's remaining turns
+    drain_turns(p, t, fail_L, fail_k);
 }
 
 template <int MOD>
