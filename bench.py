@@ -153,7 +153,7 @@ def kernel_source_hash():
 def recorded_traffic(workload):
     """DRAM bytes per launch from the committed ncu summary, if it was taken
     on the current kernel source; else None."""
-    path = os.path.join(ROOT, "profiles", "traffic.json")
+    path = os.path.join(ROOT, "profiles", "std_fwd_mha_s2048_vanilla_traffic.txt")
     if not os.path.exists(path):
         return None
     with open(path) as f:
