@@ -525,15 +525,19 @@ fl_status fwd_evo(bool row_pass, const fl_tensor *q, const fl_tensor *k, const f
     p.grid.Hk = int(H);
     p.grid.G = 1;
     p.grid.nq = nq;
-    // chunk of batch indices per work item: minimise (waves x chunk) over the SMs
+    // chunk of batch indices per work item: the CTA's two slots run a chunk's
+    // batch indices two at a time, so an item costs ceil(chunk / 2) row times
+    // plus about half a row time of start-up (the item's bias rows and first
+    // Q tiles, loaded once the previous item is done with them); minimise
+    // waves x (2 ceil(chunk / 2) + 1) over the SMs, on a tie the smaller chunk
+    // (more items to spread over the SMs)
     {
         int64_t best_cost = -1;
         int best_chunk = int(B);
-        for (int64_t nch = 1; nch <= B; ++nch) {
-            const int64_t chunk = (B + nch - 1) / nch;
+        for (int64_t chunk = 1; chunk <= B; ++chunk) {
             const int64_t items = ((B + chunk - 1) / chunk) * H * nq;
             const int64_t waves = (items + info.sm_count - 1) / info.sm_count;
-            const int64_t cost = waves * chunk;
+            const int64_t cost = waves * (2 * ((chunk + 1) / 2) + 1);
             if (best_cost < 0 || cost < best_cost) {
                 best_cost = cost;
                 best_chunk = int(chunk);

@@ -12,17 +12,22 @@
 // host swaps the two strides).
 //
 // Work item = (head h, query block qb, a chunk of batch indices).  The CTA's
-// two slots take alternate batch indices of the chunk; each slot is a complete
-// pipeline of its own -- a TMA producer warp (Q double-buffered, K/V through a
-// ring), an MMA warp and a softmax warpgroup -- so the two never wait for each
-// other.  In the row pass the bias rows of (h, qb) are loaded once per item
-// into shared memory (128 rows x up to 384 keys) and read by every MSA row of
-// the chunk: the pair-bias tile is reused across MSA rows instead of being
-// re-read from L2 for each of them.
+// two slots take alternate batch indices of the chunk; a slot's "steps" are
+// its (batch index, key tile) pairs in order.  In the row pass the bias rows
+// of (h, qb) are loaded once per item into shared memory (128 rows x up to
+// 384 keys) and read by every MSA row of the chunk: the pair-bias tile is
+// reused across MSA rows instead of being re-read from L2 for each of them.
 //
-// Warps: 0-3 softmax slot 0, 4-7 softmax slot 1, 8 producer slot 0 (also
-// loads the bias), 9 MMA slot 0 (TMEM owner), 10 MMA slot 1, 11 producer slot 1.
-//
+// Warps: 0 TMA producer for both slots (Q double-buffered per slot, K/V
+// through one ring per slot, and the bias), 1 issues S = Q K^T for both slots
+// (TMEM owner), 2 and 3 issue O += P V for slot 0 and slot 1, 4-7 softmax of
+// slot 0, 8-11 softmax of slot 1.  The producer and the S warp walk the steps
+// of both slots interleaved (step s of slot 0, then of slot 1), the order in
+// which the slots consume them.  Q K^T and P V are issued by different warps
+// because a tcgen05.mma returns to its issuing thread only once the tensor
+// core has accepted it: one thread issuing both chains of a slot spends most
+// of a tile blocked in issue.
+
 // TMEM per slot t: S[t] fp32 at 128 t; O[t] at 256 + 64 t with 48 columns:
 // 32 output columns and 16 columns of sum_j P_j (P V multiplies P by V
 // extended with a tile of ones, so the tensor core also sums the exact bf16 P
@@ -58,6 +63,7 @@ constexpr uint32_t kColS = 0, kColO = 256, kColP = 384;
 constexpr uint32_t kDvExt = 48;               // 32 output columns + 16 sum columns
 constexpr uint32_t kColSum = 32;
 
+
 template <bool BIAS>
 struct EvoCfg {
     static constexpr int kStages = BIAS ? 2 : 4; // K/V ring depth per slot
@@ -74,7 +80,7 @@ struct __align__(1024) EvoSmem {
                                     // follow every V stage (the descriptor offset is unsigned)
     uint64_t q_full[2][2], q_empty[2][2];
     uint64_t kv_full[2][NS], kv_empty[2][NS];
-    uint64_t s_full[2], s_free[2], p_full[2], pv_done[2], o_final[2];
+    uint64_t s_full[2], s_free[2], p_full[2], pv_done[2], o_final[2], s_final;
     uint64_t bias_full, bias_empty;
     uint32_t tmem_base;
     uint32_t abort_flag;
@@ -108,22 +114,28 @@ __device__ __forceinline__ EvoItem decode_evo(const EvoParams &p, int64_t L)
     return it;
 }
 
-// ------------------------------------------------------------------ producers
+// Batch indices of slot t in an item: b0 + t, b0 + t + 2, ... < b1.
+__device__ __forceinline__ int slot_rows(const EvoItem &it, int t)
+{
+    return it.b1 - it.b0 > t ? (it.b1 - it.b0 - t + 1) / 2 : 0;
+}
+
+// ------------------------------------------------------------------ producer
 template <bool BIAS>
-__device__ void producer_role(const Ctx<BIAS> &cx, const EvoParams &p, int t,
-                              const CUtensorMap *tm_q, const CUtensorMap *tm_k,
-                              const CUtensorMap *tm_v, const CUtensorMap *tm_b)
+__device__ void producer_role(const Ctx<BIAS> &cx, const EvoParams &p, const CUtensorMap *tm_q,
+                              const CUtensorMap *tm_k, const CUtensorMap *tm_v,
+                              const CUtensorMap *tm_b)
 {
     constexpr int NS = EvoCfg<BIAS>::kStages;
     EvoSmem<BIAS> &sm = *cx.sm;
     const uint32_t lane = ptx::lane_id();
     const int nkv = (p.mask.S + BN - 1) / BN;
     const int nbox = (p.mask.S + 63) / 64;
-    uint32_t kv_count = 0, q_count = 0, item_count = 0;
+    uint32_t kv_count[2] = {0u, 0u}, q_count[2] = {0u, 0u}, item_count = 0;
     bool ok = true;
     for (int64_t L = blockIdx.x; L < p.n_items && ok; L += gridDim.x, ++item_count) {
         const EvoItem it = decode_evo(p, L);
-        if (BIAS && t == 0) {
+        if (BIAS) {
             if (item_count > 0) {
                 ok = warp_wait(bar(sm.bias_empty), (item_count - 1) & 1, cx.wc, W_BIAS);
                 if (!ok)
@@ -137,143 +149,173 @@ __device__ void producer_role(const Ctx<BIAS> &cx, const EvoParams &p, int t,
             }
             __syncwarp();
         }
-        for (int b = it.b0 + t; b < it.b1 && ok; b += 2, ++q_count) {
-            const uint32_t qbuf = q_count & 1;
-            if (q_count >= 2) {
-                ok = warp_wait(bar(sm.q_empty[t][qbuf]), ((q_count - 2) >> 1) & 1, cx.wc, W_Q_EMPTY);
-                if (!ok)
-                    break;
-            }
-            if (lane == 0) {
-                ptx::mbar_arrive_expect_tx(bar(sm.q_full[t][qbuf]), kTile);
-                ptx::tma_load_4d(ptx::smem_u32(sm.q[t][qbuf]), tm_q, bar(sm.q_full[t][qbuf]), 0,
-                                 it.qb * BM, it.h, b);
-            }
-            __syncwarp();
-            for (int j = 0; j < nkv; ++j, ++kv_count) {
-                const uint32_t s = kv_count % NS;
-                ok = warp_wait(bar(sm.kv_empty[t][s]), ((kv_count / NS) & 1) ^ 1, cx.wc, W_KV_EMPTY);
+        const int steps[2] = {slot_rows(it, 0) * nkv, slot_rows(it, 1) * nkv};
+        const int n_steps = max(steps[0], steps[1]);
+        for (int st = 0; st < n_steps && ok; ++st) {
+            const int j = st % nkv;
+#pragma unroll
+            for (int t = 0; t < 2; ++t) {
+                if (st >= steps[t])
+                    continue;
+                const int b = it.b0 + t + 2 * (st / nkv);
+                if (j == 0) {
+                    const uint32_t qbuf = q_count[t] & 1;
+                    if (q_count[t] >= 2) {
+                        ok = warp_wait(bar(sm.q_empty[t][qbuf]), ((q_count[t] - 2) >> 1) & 1, cx.wc,
+                                       W_Q_EMPTY);
+                        if (!ok)
+                            break;
+                    }
+                    if (lane == 0) {
+                        ptx::mbar_arrive_expect_tx(bar(sm.q_full[t][qbuf]), kTile);
+                        ptx::tma_load_4d(ptx::smem_u32(sm.q[t][qbuf]), tm_q, bar(sm.q_full[t][qbuf]), 0,
+                                         it.qb * BM, it.h, b);
+                    }
+                    __syncwarp();
+                    ++q_count[t];
+                }
+                const uint32_t stage = kv_count[t] % NS;
+                ok = warp_wait(bar(sm.kv_empty[t][stage]), ((kv_count[t] / NS) & 1) ^ 1, cx.wc,
+                               W_KV_EMPTY);
                 if (!ok)
                     break;
                 if (lane == 0) {
-                    ptx::mbar_arrive_expect_tx(bar(sm.kv_full[t][s]), 2 * kTile);
-                    ptx::tma_load_4d(ptx::smem_u32(sm.k[t][s]), tm_k, bar(sm.kv_full[t][s]), 0,
+                    ptx::mbar_arrive_expect_tx(bar(sm.kv_full[t][stage]), 2 * kTile);
+                    ptx::tma_load_4d(ptx::smem_u32(sm.k[t][stage]), tm_k, bar(sm.kv_full[t][stage]), 0,
                                      j * BN, it.h, b);
-                    ptx::tma_load_4d(ptx::smem_u32(sm.v[t][s]), tm_v, bar(sm.kv_full[t][s]), 0,
+                    ptx::tma_load_4d(ptx::smem_u32(sm.v[t][stage]), tm_v, bar(sm.kv_full[t][stage]), 0,
                                      j * BN, it.h, b);
                 }
                 __syncwarp();
+                ++kv_count[t];
             }
         }
     }
     if (!ok) {
         // wait (bounded, ignoring the abort) for this warp's own loads in flight
-        const uint32_t first = kv_count > NS ? kv_count - NS : 0;
-        for (uint32_t idx = first; idx < kv_count; ++idx)
-            mbar_wait_drain(bar(sm.kv_full[t][idx % NS]), (idx / NS) & 1, cx.wc, W_DRAIN);
-        for (uint32_t n = q_count > 2 ? q_count - 2 : 0; n < q_count; ++n)
-            mbar_wait_drain(bar(sm.q_full[t][n & 1]), (n >> 1) & 1, cx.wc, W_DRAIN);
-        if (BIAS && t == 0 && item_count > 0)
+#pragma unroll
+        for (int t = 0; t < 2; ++t) {
+            const uint32_t first = kv_count[t] > NS ? kv_count[t] - NS : 0;
+            for (uint32_t idx = first; idx < kv_count[t]; ++idx)
+                mbar_wait_drain(bar(sm.kv_full[t][idx % NS]), (idx / NS) & 1, cx.wc, W_DRAIN);
+            for (uint32_t n = q_count[t] > 2 ? q_count[t] - 2 : 0; n < q_count[t]; ++n)
+                mbar_wait_drain(bar(sm.q_full[t][n & 1]), (n >> 1) & 1, cx.wc, W_DRAIN);
+        }
+        if (BIAS && item_count > 0)
             mbar_wait_drain(bar(sm.bias_full), (item_count - 1) & 1, cx.wc, W_DRAIN);
     }
 }
 
 // ------------------------------------------------------------------ MMA issuers
+constexpr uint64_t kHiK = umma_desc_hi(16, 512, kSwizzle64B); // Q, K: K-major, 64-byte rows
+
+// S = Q K^T for both slots, steps interleaved like the producer's.  q_empty
+// (one arrival) is committed after a batch index's last S; S(t, s) waits for
+// the softmax to have copied S(t, s-1) out of TMEM.
 template <bool BIAS>
-__device__ void mma_role(const Ctx<BIAS> &cx, const EvoParams &p, int t)
+__device__ void s_role(const Ctx<BIAS> &cx, const EvoParams &p)
 {
     constexpr int NS = EvoCfg<BIAS>::kStages;
     EvoSmem<BIAS> &sm = *cx.sm;
     const uint32_t lane = ptx::lane_id();
     constexpr uint32_t idesc_qk = umma_idesc_bf16(BM, BN, false);
-    constexpr uint32_t idesc_pv = umma_idesc_bf16(BM, kDvExt, true);
-    constexpr uint64_t kHiK = umma_desc_hi(16, 512, kSwizzle64B); // Q, K: K-major, 64-byte rows
     constexpr uint32_t kTileLo = kTile >> 4;
-    constexpr uint32_t kBarStride = sizeof(uint64_t);
-    const uint32_t q_lo0 = ptx::smem_u32(sm.q[t][0]) >> 4;
-    const uint32_t k_lo0 = ptx::smem_u32(sm.k[t][0]) >> 4;
-    const uint32_t v_lo0 = ptx::smem_u32(sm.v[t][0]) >> 4;
-    const uint32_t ones_lo = ptx::smem_u32(sm.ones) >> 4;
-    const uint32_t tS = cx.tmem + kColS + 128 * t, tO = cx.tmem + kColO + 64 * t;
-    const uint32_t tP = cx.tmem + kColP + 64 * t;
-    const uint32_t b_sfull = bar(sm.s_full[t]), b_sfree = bar(sm.s_free[t]);
-    const uint32_t b_pfull = bar(sm.p_full[t]), b_pvdone = bar(sm.pv_done[t]);
-    const uint32_t b_kvf0 = bar(sm.kv_full[t][0]), b_kve0 = bar(sm.kv_empty[t][0]);
     const int nkv = (p.mask.S + BN - 1) / BN;
-
-    uint32_t kv_count = 0, q_count = 0, fcount = 0, pcount = 0;
+    uint32_t kv_count[2] = {0u, 0u}, q_count[2] = {0u, 0u}, issued[2] = {0u, 0u};
     bool ok = true;
     for (int64_t L = blockIdx.x; L < p.n_items && ok; L += gridDim.x) {
         const EvoItem it = decode_evo(p, L);
-        for (int b = it.b0 + t; b < it.b1 && ok; b += 2, ++q_count) {
-            const uint32_t qbuf = q_count & 1;
-            const uint32_t b_qe = bar(sm.q_empty[t][qbuf]);
-            ok = warp_wait(bar(sm.q_full[t][qbuf]), (q_count >> 1) & 1, cx.wc, W_Q_FULL);
-            if (!ok)
-                break;
-            const uint32_t qlo = q_lo0 + qbuf * kTileLo;
-            // first S of this batch index
-            ok = warp_wait(b_kvf0 + (kv_count % NS) * kBarStride, (kv_count / NS) & 1, cx.wc,
-                           W_KV_FULL);
-            if (!ok)
-                break;
-            ptx::tc_fence_after();
-            if (lane == 0) {
-                const uint32_t klo = k_lo0 + (kv_count % NS) * kTileLo;
+        const int steps[2] = {slot_rows(it, 0) * nkv, slot_rows(it, 1) * nkv};
+        const int n_steps = max(steps[0], steps[1]);
+        for (int st = 0; st < n_steps && ok; ++st) {
+            const int j = st % nkv;
 #pragma unroll
-                for (int kk = 0; kk < 2; ++kk)
-                    ptx::mma_ss(tS, kHiK | (qlo + 2 * kk), kHiK | (klo + 2 * kk), idesc_qk,
-                                kk > 0 ? 1u : 0u);
-                ptx::mma_commit(b_sfull);
-                if (nkv == 1)
-                    ptx::mma_commit(b_qe);
-            }
-            __syncwarp();
-            for (int j = 0; j < nkv && ok; ++j) {
-                const uint32_t idx = kv_count + j;
-                // the softmax has copied S(j) out of TMEM: issue S(j + 1)
-                ok = warp_wait(b_sfree, fcount & 1, cx.wc, W_S_FULL);
-                if (!ok)
-                    break;
-                ++fcount;
-                if (j + 1 < nkv) {
-                    const uint32_t nidx = idx + 1;
-                    ok = warp_wait(b_kvf0 + (nidx % NS) * kBarStride, (nidx / NS) & 1, cx.wc,
-                                   W_KV_FULL);
+            for (int t = 0; t < 2; ++t) {
+                if (st >= steps[t])
+                    continue;
+                const uint32_t qbuf = q_count[t] & 1;
+                if (j == 0) {
+                    ok = warp_wait(bar(sm.q_full[t][qbuf]), (q_count[t] >> 1) & 1, cx.wc, W_Q_FULL);
                     if (!ok)
                         break;
-                    ptx::tc_fence_after();
-                    if (lane == 0) {
-                        const uint32_t klo = k_lo0 + (nidx % NS) * kTileLo;
-#pragma unroll
-                        for (int kk = 0; kk < 2; ++kk)
-                            ptx::mma_ss(tS, kHiK | (qlo + 2 * kk), kHiK | (klo + 2 * kk), idesc_qk,
-                                        kk > 0 ? 1u : 0u);
-                        ptx::mma_commit(b_sfull);
-                        if (j + 2 == nkv)
-                            ptx::mma_commit(b_qe); // last read of this Q buffer
-                    }
-                    __syncwarp();
                 }
-                // the softmax has written P(j) and rescaled O: O += P [V_j | 1]
-                ok = warp_wait(b_pfull, pcount & 1, cx.wc, W_P_FULL);
+                if (issued[t] > 0) {
+                    ok = warp_wait(bar(sm.s_free[t]), (issued[t] - 1) & 1, cx.wc, W_S_FULL);
+                    if (!ok)
+                        break;
+                }
+                const uint32_t stage = kv_count[t] % NS;
+                ok = warp_wait(bar(sm.kv_full[t][stage]), (kv_count[t] / NS) & 1, cx.wc, W_KV_FULL);
                 if (!ok)
                     break;
-                ++pcount;
                 ptx::tc_fence_after();
                 if (lane == 0) {
-                    const uint32_t vlo = v_lo0 + (idx % NS) * kTileLo;
-                    const uint64_t hi_v = umma_desc_hi((ones_lo - vlo) << 4, 512, kSwizzle64B);
+                    const uint32_t qlo = (ptx::smem_u32(sm.q[t][qbuf]) >> 4);
+                    const uint32_t klo = (ptx::smem_u32(sm.k[t][0]) >> 4) + stage * kTileLo;
+                    const uint32_t tS = cx.tmem + kColS + 128 * t;
 #pragma unroll
-                    for (int kk = 0; kk < BN / 16; ++kk)
-                        ptx::mma_ts(tO, tP + 8 * kk, hi_v | (vlo + 64 * kk), idesc_pv,
-                                    (j > 0 || kk > 0) ? 1u : 0u);
-                    ptx::mma_commit(b_pvdone);
-                    ptx::mma_commit(b_kve0 + (idx % NS) * kBarStride);
+                    for (int kk = 0; kk < 2; ++kk)
+                        ptx::mma_ss(tS, kHiK | (qlo + 2 * kk), kHiK | (klo + 2 * kk), idesc_qk,
+                                    kk > 0 ? 1u : 0u);
+                    ptx::mma_commit(bar(sm.s_full[t]));
+                    if (j + 1 == nkv)
+                        ptx::mma_commit(bar(sm.q_empty[t][qbuf])); // last read of this Q buffer
                 }
                 __syncwarp();
+                ++issued[t];
+                ++kv_count[t];
+                if (j + 1 == nkv)
+                    ++q_count[t];
             }
-            kv_count += nkv;
+        }
+    }
+    // Every MMA this thread issued has completed before TMEM is released.
+    if (lane == 0)
+        ptx::mma_commit(bar(sm.s_final));
+    __syncwarp();
+    mbar_wait_drain(bar(sm.s_final), 0, cx.wc, W_FINAL);
+}
+
+// O += P [V | 1] for slot t.  S(j) of a step completes before its softmax can
+// publish P(j), so the commit after P V also covers the K read: kv_empty has
+// one arrival (this warp's).
+template <bool BIAS>
+__device__ void pv_role(const Ctx<BIAS> &cx, const EvoParams &p, int t)
+{
+    constexpr int NS = EvoCfg<BIAS>::kStages;
+    EvoSmem<BIAS> &sm = *cx.sm;
+    const uint32_t lane = ptx::lane_id();
+    constexpr uint32_t idesc_pv = umma_idesc_bf16(BM, kDvExt, true);
+    constexpr uint32_t kTileLo = kTile >> 4;
+    const uint32_t v_lo0 = ptx::smem_u32(sm.v[t][0]) >> 4;
+    const uint32_t ones_lo = ptx::smem_u32(sm.ones) >> 4;
+    const uint32_t tO = cx.tmem + kColO + 64 * t, tP = cx.tmem + kColP + 64 * t;
+    const int nkv = (p.mask.S + BN - 1) / BN;
+    uint32_t kv_count = 0, pcount = 0;
+    bool ok = true;
+    for (int64_t L = blockIdx.x; L < p.n_items && ok; L += gridDim.x) {
+        const EvoItem it = decode_evo(p, L);
+        const int steps = slot_rows(it, t) * nkv;
+        for (int st = 0; st < steps && ok; ++st, ++kv_count) {
+            const int j = st % nkv;
+            // the softmax has written P(j) and rescaled O: O += P [V_j | 1]
+            ok = warp_wait(bar(sm.p_full[t]), pcount & 1, cx.wc, W_P_FULL);
+            if (!ok)
+                break;
+            ++pcount;
+            ptx::tc_fence_after();
+            if (lane == 0) {
+                const uint32_t stage = kv_count % NS;
+                const uint32_t vlo = v_lo0 + stage * kTileLo;
+                const uint64_t hi_v = umma_desc_hi((ones_lo - vlo) << 4, 512, kSwizzle64B);
+#pragma unroll
+                for (int kk = 0; kk < BN / 16; ++kk)
+                    ptx::mma_ts(tO, tP + 8 * kk, hi_v | (vlo + 64 * kk), idesc_pv,
+                                (j > 0 || kk > 0) ? 1u : 0u);
+                ptx::mma_commit(bar(sm.pv_done[t]));
+                ptx::mma_commit(bar(sm.kv_empty[t][stage]));
+            }
+            __syncwarp();
         }
     }
     const uint32_t b_final = bar(sm.o_final[t]);
@@ -289,6 +331,13 @@ struct PendingRow {
     int b, h, qb, i;
     RowState st;
 };
+
+__device__ __forceinline__ float tanh_approx(float x)
+{
+    float y;
+    asm("tanh.approx.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
 
 // sigmoid(g) * O / sum(P) -> bf16 row, LSE, visited-tile count.  O[t] must
 // hold the finished output of `pr` (its last P V has completed).
@@ -316,11 +365,11 @@ __device__ __forceinline__ void store_row_output(const EvoParams &p, uint32_t tO
             uint32_t ov[4];
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
-                // sigmoid(g) = 1 / (1 + 2^(-g log2 e))
+                // sigmoid(g) = 1/2 + tanh(g / 2) / 2 (one special-function op)
                 const float g0 = __uint_as_float(gv[q] << 16);
                 const float g1 = __uint_as_float(gv[q] & 0xFFFF0000u);
-                const float s0 = ptx::rcp_approx(1.f + ptx::ex2(-g0 * kLog2e));
-                const float s1 = ptx::rcp_approx(1.f + ptx::ex2(-g1 * kLog2e));
+                const float s0 = fmaf(0.5f, tanh_approx(0.5f * g0), 0.5f);
+                const float s1 = fmaf(0.5f, tanh_approx(0.5f * g1), 0.5f);
                 ov[q] = ptx::pack_bf16(__uint_as_float(o[8 * c4 + 2 * q]) * inv * s0,
                                        __uint_as_float(o[8 * c4 + 2 * q + 1]) * inv * s1);
             }
@@ -478,20 +527,21 @@ __global__ void __launch_bounds__(kThreads, 1)
             ptx::mbar_init(bar(sm->pv_done[t]), 1);
             ptx::mbar_init(bar(sm->o_final[t]), 1);
         }
+        ptx::mbar_init(bar(sm->s_final), 1);
         ptx::mbar_init(bar(sm->bias_full), 1);
         ptx::mbar_init(bar(sm->bias_empty), 256);
         sm->abort_flag = 0;
         ptx::fence_mbarrier_init();
         ptx::fence_proxy_async_smem();
     }
-    if ((warp == 8 || warp == 11) && ptx::lane_id() == 0) {
+    if (warp == 0 && ptx::lane_id() == 0) {
         ptx::prefetch_tensormap(&tm_q);
         ptx::prefetch_tensormap(&tm_k);
         ptx::prefetch_tensormap(&tm_v);
         if (BIAS)
             ptx::prefetch_tensormap(&tm_b);
     }
-    if (warp == 9) {
+    if (warp == 1) {
         ptx::tmem_alloc(ptx::smem_u32(&sm->tmem_base), 512);
         ptx::tmem_relinquish();
     }
@@ -509,20 +559,22 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     // Each branch ends with its own copy of the teardown barrier, so no code
     // runs under both register limits.
-    if (warp < 8) {
+    if (warp >= 4) {
         ptx::setmaxnreg_inc<kRegsSoftmax>();
-        softmax_role<BIAS, LSE>(cx, p, warp >> 2);
+        softmax_role<BIAS, LSE>(cx, p, (warp >> 2) - 1);
         ptx::tc_fence_before();
         ptx::named_barrier_sync(1, kThreads);
     } else {
         ptx::setmaxnreg_dec<kRegsOther>();
-        if (warp == 8 || warp == 11)
-            producer_role<BIAS>(cx, p, warp == 8 ? 0 : 1, &tm_q, &tm_k, &tm_v, &tm_b);
+        if (warp == 0)
+            producer_role<BIAS>(cx, p, &tm_q, &tm_k, &tm_v, &tm_b);
+        else if (warp == 1)
+            s_role<BIAS>(cx, p);
         else
-            mma_role<BIAS>(cx, p, warp - 9);
+            pv_role<BIAS>(cx, p, warp - 2);
         ptx::tc_fence_before();
         ptx::named_barrier_sync(1, kThreads);
-        if (warp == 9) {
+        if (warp == 1) {
             ptx::tc_fence_after();
             ptx::tmem_dealloc(cx.tmem, 512);
         }
