@@ -164,6 +164,38 @@ def recorded_traffic(workload):
     return rec.get("dram_bytes_per_launch")
 
 
+# ---------------------------------------------------------------- ranks
+
+def init_ranks():
+    """(world, rank, local rank) from the torchrun environment; joins the
+    process group when world > 1 (NCCL with a GPU, gloo otherwise)."""
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        if not dist.is_initialized():
+            dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+    return world, rank, local
+
+
+def max_over_ranks(value, world, device):
+    """The largest of every rank's value (the slowest rank's step time)."""
+    if world <= 1:
+        return float(value)
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(units_per_rank, world, step_ms):
+    """Whole-job rate: every rank's units over the slowest rank's time (per second)."""
+    return units_per_rank * world / (step_ms * 1e-3)
+
+
 class ClockSampler:
     """nvidia-smi samples of SM clock and throttle reasons during the timed region."""
 
@@ -381,12 +413,7 @@ def run_ours(args):
     import torch
     import attention_variant_gb300 as fa
 
-    world = int(os.environ.get("WORLD_SIZE", "1"))
-    rank = int(os.environ.get("RANK", "0"))
-    local = int(os.environ.get("LOCAL_RANK", "0"))
-    if world > 1:
-        import torch.distributed as dist
-        dist.init_process_group("nccl")
+    world, rank, local = init_ranks()
     torch.cuda.set_device(local)
     device = torch.device("cuda", local)
     fa.load_library()
@@ -411,18 +438,15 @@ def run_ours(args):
         barrier()
         wall = time.perf_counter() - t0
     clocks = clk.summary()
-    step_ms = statistics.mean(ms)
-    if world > 1:
-        t = torch.tensor([step_ms], device=device)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        step_ms = float(t.item())
-    value = head["flops"] * world / (step_ms * 1e-3) / 1e12
+    step_ms = max_over_ranks(statistics.mean(ms), world, device)
+    value = job_throughput(head["flops"], world, step_ms) / 1e12
     peaks = measured_peaks()
     achieved = head["flops"] / (statistics.mean(ms) * 1e-3) / 1e12
 
     e2e_ms, h2d, d2h = time_e2e(head, host, torch, fa, device, max(3, args.steps // 4),
                                 args.warmup, stream)
-    e2e = dict(value=head["flops"] * world / (e2e_ms * 1e-3) / 1e12, unit="TFLOP/s",
+    e2e_ms = max_over_ranks(e2e_ms, world, device)
+    e2e = dict(value=job_throughput(head["flops"], world, e2e_ms) / 1e12, unit="TFLOP/s",
                h2d_bytes_per_step=h2d, d2h_bytes_per_step=d2h)
 
     variants = {}
