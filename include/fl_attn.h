@@ -118,7 +118,9 @@ typedef struct {
     float scale;             /* 0 means 1 / sqrt(D) */
     const float *alibi_slopes; /* device float [Hq], or NULL for 2^(-8 (h+1) / Hq) */
     int32_t *debug_tile_counts; /* NULL, or device int32 [batch][heads][ceil(S/128)]: the
-                                   number of 128-key tiles each 128-row query block visited */
+                                   number of key tiles each 128-row query block visited
+                                   (key-tile width from fl_attn_tile_shape: 112 for the
+                                   standard kind, 128 for the others) */
     uint32_t *error_word;    /* NULL, or a device word the kernel ORs FL_DEVERR_* into */
     int32_t debug_inject;    /* fl_inject; 0 in normal use */
     uint32_t wait_timeout_us; /* bound of every device-side wait; 0 means 2,000,000 */
@@ -143,8 +145,14 @@ typedef struct {
  *                     lse [N_res,H,N_seq] or NULL.
  * lse is natural-log; its innermost stride must be 1.
  *
- * Supported shapes: STANDARD D = Dv = 64; DIFF D = 64, Dv = 128;
- * EVO c = 32.  Other head dimensions return FL_ERR_UNSUPPORTED.
+ * Supported shapes: STANDARD D = Dv = 64; DIFF D = 64, Dv = 128 with mask
+ * none or causal; EVO c = 32, and for FL_KIND_EVO_ROW N_res <= 384 (the bias
+ * rows of a query block are kept in shared memory).  Other shapes return
+ * FL_ERR_UNSUPPORTED.  The bias may be passed with any strides obeying the
+ * fl_tensor rules (for example a [N_res,N_res,H] tensor viewed as
+ * [H,N_res,N_res]).  Evoformer sequence lengths must keep every stride a
+ * multiple of 16 bytes (c = 32 bf16 rows always do; the bias row stride must
+ * be a multiple of 8 elements: pad N_res or the bias rows otherwise).
  *
  * Returns FL_OK when enqueued.  Device-side failures (a wait that ran out)
  * are reported asynchronously through desc->error_word.
