@@ -327,35 +327,61 @@ def time_other(e, torch, fa, device, steps, warmup, flush, stream):
 
 
 def time_e2e(e, host, torch, fa, device, steps, warmup, stream):
-    """Same metric end to end: pinned host inputs -> device -> fused forward
-    -> O and LSE back to pinned host memory, every step."""
+    """Same metric end to end: every step copies its inputs from pinned host
+    memory to the device, runs the fused forward and reads O and LSE back to
+    pinned host memory.  Steps are pipelined over two device buffer sets and
+    three streams (copy in, compute, copy out), so step n+1's upload overlaps
+    step n's forward; the timed region runs from the first upload to the last
+    download."""
     hq, hk, hv = (x.pin_memory() for x in host)
-    q, k, v = (torch.empty_like(x, device=device) for x in host)
-    out = torch.empty((e["B"], e["S"], e["Hq"], e["D"]), dtype=torch.bfloat16, device=device)
-    lse = torch.empty((e["B"], e["Hq"], e["S"]), dtype=torch.float32, device=device)
-    ho = torch.empty(out.shape, dtype=out.dtype).pin_memory()
-    hl = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
+    sets = []
+    for _ in range(2):
+        q, k, v = (torch.empty_like(x, device=device) for x in host)
+        out = torch.empty((e["B"], e["S"], e["Hq"], e["D"]), dtype=torch.bfloat16, device=device)
+        lse = torch.empty((e["B"], e["Hq"], e["S"]), dtype=torch.float32, device=device)
+        sets.append((q, k, v, out, lse))
+    ho = torch.empty(sets[0][3].shape, dtype=torch.bfloat16).pin_memory()
+    hl = torch.empty(sets[0][4].shape, dtype=torch.float32).pin_memory()
     desc = fa.make_desc(score_mod=e["mod"], mask=e["mask"], softcap=workloads.SOFTCAP, **e["kw"])
+    s_in, s_out = torch.cuda.Stream(device), torch.cuda.Stream(device)
+    ev = lambda: torch.cuda.Event()
+    in_done = [ev(), ev()]
+    comp_done = [ev(), ev()]
+    out_done = [ev(), ev()]
+    used = [False, False]
 
-    def step():
-        q.copy_(hq, non_blocking=True)
-        k.copy_(hk, non_blocking=True)
-        v.copy_(hv, non_blocking=True)
+    def step(n):
+        i = n & 1
+        q, k, v, out, lse = sets[i]
+        with torch.cuda.stream(s_in):
+            if used[i]:
+                s_in.wait_event(comp_done[i])   # step n-2's forward has read this set
+            q.copy_(hq, non_blocking=True)
+            k.copy_(hk, non_blocking=True)
+            v.copy_(hv, non_blocking=True)
+            in_done[i].record(s_in)
+        stream.wait_event(in_done[i])
+        if used[i]:
+            stream.wait_event(out_done[i])      # step n-2's outputs have been read back
         fa.fl_attn_fwd(q, k, v, out, lse, desc, stream=stream)
-        ho.copy_(out, non_blocking=True)
-        hl.copy_(lse, non_blocking=True)
+        comp_done[i].record(stream)
+        with torch.cuda.stream(s_out):
+            s_out.wait_event(comp_done[i])
+            ho.copy_(out, non_blocking=True)
+            hl.copy_(lse, non_blocking=True)
+            out_done[i].record(s_out)
+        used[i] = True
 
-    with torch.cuda.stream(stream):
-        for _ in range(warmup):
-            step()
-        torch.cuda.synchronize()
-        s, t = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        s.record(stream)
-        for _ in range(steps):
-            step()
-        t.record(stream)
-        torch.cuda.synchronize()
-    ms = s.elapsed_time(t) / steps
+    for n in range(warmup):
+        step(n)
+    torch.cuda.synchronize()
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t0.record(s_in)
+    for n in range(warmup, warmup + steps):
+        step(n)
+    t1.record(s_out)
+    torch.cuda.synchronize()
+    ms = t0.elapsed_time(t1) / steps
     h2d = sum(x.numel() * x.element_size() for x in (hq, hk, hv))
     d2h = ho.numel() * ho.element_size() + hl.numel() * hl.element_size()
     return ms, h2d, d2h
