@@ -27,7 +27,7 @@ _LIB_DIR = os.path.join(_HERE, "_build")
 _LIB = os.path.join(_LIB_DIR, "libfloracle.so")
 
 MOD = {"none": 0, "alibi": 1, "softcap": 2}
-MASK = {"none": 0, "causal": 1, "window": 2, "prefix": 3, "doc": 4}
+MASK = {"none": 0, "causal": 1, "window": 2, "prefix": 3, "doc": 4, "kv_len": 5, "decode": 6}
 
 
 class _Problem(ctypes.Structure):
@@ -43,6 +43,7 @@ class _Problem(ctypes.Structure):
         ("doc_offsets", ctypes.c_void_p), ("doc_stride", ctypes.c_int32),
         ("scale", ctypes.c_double),
         ("bias", ctypes.c_void_p), ("bias_stride", ctypes.c_int64 * 3),
+        ("kv_len", ctypes.c_void_p),
     ]
 
 
@@ -99,12 +100,15 @@ def _base_and_span(a: np.ndarray):
 
 
 def attention(q, k, v, *, mod="none", softcap=20.0, alibi_slopes=None, mask="none",
-              window=0, prefix=0, doc_offsets=None, scale=0.0, bias=None,
+              window=0, prefix=0, doc_offsets=None, scale=0.0, bias=None, kv_len=None,
               rows=None, nthreads=0, lib=None):
     """Attention forward of ``q [B,Sq,Hq,D]``, ``k [B,Sk,Hk,D]``, ``v [B,Sk,Hk,Dv]``.
 
     ``bias`` (optional) is ``[Hq, Sq, Sk]`` bf16 bits.  ``doc_offsets`` is the
     int32 ``[B, max_docs+1]`` table of document starts padded with ``Sk``.
+    ``kv_len`` (masks ``kv_len`` and ``decode``) holds each batch element's
+    cache length; the decode mask puts the ``Sq`` query rows at the last
+    ``Sq`` positions of that length.
     ``rows`` (optional) is an ``[n, 3]`` array of ``(b, h, i)``; then the
     result is ``O [n, Dv]`` and ``LSE [n]``, else ``O [B,Sq,Hq,Dv]`` and
     ``LSE [B,Hq,Sq]``.
@@ -136,6 +140,12 @@ def attention(q, k, v, *, mod="none", softcap=20.0, alibi_slopes=None, mask="non
         p.doc_offsets = do.ctypes.data
         p.doc_stride = do.shape[1]
     p.scale = float(scale)
+    if kv_len is not None:
+        kl = np.ascontiguousarray(kv_len, dtype=np.int32)
+        if kl.shape != (B,):
+            raise ValueError("kv_len must have one entry per batch element")
+        keep.append(kl)
+        p.kv_len = kl.ctypes.data
     if bias is not None:
         if bias.dtype != np.uint16 or bias.shape != (Hq, Sq, Sk):
             raise ValueError("bias must be [Hq, Sq, Sk] bf16 bits")

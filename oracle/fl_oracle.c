@@ -33,6 +33,11 @@
  *   window   allowed iff j <= i and i - j < W
  *   prefix   allowed iff j <= i or j < P   (bidirectional over the first P)
  *   document allowed iff doc(i) == doc(j) and j <= i
+ *   KV length  allowed iff j < kv_len[b]            (a cache of kv_len[b] keys)
+ *   decode     allowed iff j < kv_len[b] and j <= kv_len[b] - Sq + i
+ *              (the Sq query rows are the last Sq positions of a sequence of
+ *              kv_len[b] tokens: serving with a KV cache, talk notes,
+ *              "End-to-end: LLaMA-3.2-1B (vLLM / Mooncake)", causal variant)
  * Query head h reads key/value head h / (Hq / Hk) (contiguous GQA groups).
  */
 #include <math.h>
@@ -52,6 +57,8 @@
 #define FL_ORACLE_MASK_WINDOW 2
 #define FL_ORACLE_MASK_PREFIX 3
 #define FL_ORACLE_MASK_DOC 4
+#define FL_ORACLE_MASK_KVLEN 5
+#define FL_ORACLE_MASK_DECODE 6
 
 typedef struct {
     int32_t B, Hq, Hk, Sq, Sk, D, Dv;
@@ -70,6 +77,7 @@ typedef struct {
     double scale;               /* 0 means 1 / sqrt(D) */
     const uint16_t *bias;       /* NULL, or bias[h, i, j] with the strides below */
     int64_t bias_stride[3];
+    const int32_t *kv_len;      /* [B] cache lengths (KV-length and decode masks) */
 } fl_oracle_problem;
 
 static double widen_bf16(uint16_t bits)
@@ -107,6 +115,10 @@ static int allowed(const fl_oracle_problem *p, int32_t b, int64_t i, int64_t j)
         return j <= i && doc_of(starts, p->doc_stride, (int32_t)i) ==
                              doc_of(starts, p->doc_stride, (int32_t)j);
     }
+    case FL_ORACLE_MASK_KVLEN:
+        return j < p->kv_len[b];
+    case FL_ORACLE_MASK_DECODE:
+        return j < p->kv_len[b] && j <= (int64_t)p->kv_len[b] - p->Sq + i;
     default:
         return 0;
     }
@@ -191,6 +203,14 @@ int fl_oracle_attention(const fl_oracle_problem *p, const uint16_t *q, const uin
         return -1;
     if (p->mask == FL_ORACLE_MASK_DOC && (!p->doc_offsets || p->doc_stride <= 0))
         return -1;
+    if (p->mask == FL_ORACLE_MASK_KVLEN || p->mask == FL_ORACLE_MASK_DECODE) {
+        if (!p->kv_len)
+            return -1;
+        for (int32_t b = 0; b < p->B; ++b)
+            if (p->kv_len[b] < 0 || p->kv_len[b] > p->Sk ||
+                (p->mask == FL_ORACLE_MASK_DECODE && p->kv_len[b] < p->Sq))
+                return -1;
+    }
     if (rows) {
         for (int64_t r = 0; r < n_rows; ++r)
             if (rows[3 * r] < 0 || rows[3 * r] >= p->B || rows[3 * r + 1] < 0 ||

@@ -17,6 +17,8 @@ Recipe (every tensor is reproducible from the global seed alone):
 * document lengths: uniform integers in [256, 4096] drawn from the stream of
   ``"<workload>/doc_lengths/<batch>"`` until the running total reaches the
   sequence length; the last document is cut to fit.
+* KV-cache lengths (serving workload): uniform integers in [lo, hi] drawn from
+  the stream of ``"<workload>/kv_lengths/0"``, one per sequence.
 
 The workloads themselves (shapes, variants) live in :mod:`testdata.workloads`.
 """
@@ -143,6 +145,14 @@ def doc_lengths(seq_len: int, workload: str, batch_index: int,
         lengths.append(length)
         total += length
     return lengths
+
+
+def kv_lengths(batch: int, workload: str, lo: int, hi: int, seed: int = GLOBAL_SEED) -> np.ndarray:
+    """Per-sequence cache lengths, int32 ``[batch]``: ``lo + draw % (hi - lo + 1)``
+    from the stream of ``"<workload>/kv_lengths/0"``."""
+    key = sub_seed(workload, "kv_lengths", 0, seed)
+    d = draws(key, 0, batch)
+    return (lo + (d % np.uint64(hi - lo + 1)).astype(np.int64)).astype(np.int32)
 
 
 def doc_offsets(seq_len: int, batch: int, workload: str,

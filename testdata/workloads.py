@@ -3,8 +3,9 @@
 They stand in for the pages' evaluation workloads (Flashlight talk notes,
 "Evaluation: FlexAttention-supported variants": 16 heads, head dim 64,
 sequence 512-16k at a constant 16k tokens, GQA 16/2; "Evaluation: complex
-variants" and "End-to-end": differential attention and the AlphaFold Evoformer
-MSA gated self-attention).  No dataset items are reproduced; every tensor is
+variants" and "End-to-end": differential attention, the AlphaFold Evoformer
+MSA gated self-attention, and LLaMA-3.2-1B served by vLLM with causal and
+softcap attention).  No dataset items are reproduced; every tensor is
 drawn by :mod:`testdata`.
 """
 from __future__ import annotations
@@ -42,3 +43,13 @@ def mha_workload(S: int) -> dict:
 
 def gqa_workload(S: int, B: int) -> dict:
     return dict(name=f"gqa_s{S}_b{B}", B=B, Hq=GQA_HQ, Hk=GQA_HK, S=S, D=HEAD_DIM)
+
+
+# Serving with a KV cache (decode): LLaMA-3.2-1B attention shapes -- 32 query
+# heads over 8 KV heads, head dimension 64 -- one new token per sequence,
+# 64 sequences whose cache lengths are uniform in [512, 8192] (a synthetic
+# stand-in for a conversation trace; no trace item is reproduced), paged in
+# 256-token pages.  Variants: causal (the new token sees its whole cache) and
+# softcap (cap 20, as in the MHA sweep).
+DECODE = dict(name="decode_llama1b_b64", B=64, Sq=1, Hq=32, Hk=8, D=64, kv_lo=512,
+              kv_hi=8192, page=256, softcap=20.0)

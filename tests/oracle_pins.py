@@ -359,6 +359,62 @@ def pin_fully_masked_row(lib):
     assert np.all(o == 0.0) and np.all(np.isneginf(lse)), "fully masked rows"
 
 
+def pin_decode(lib):
+    """Serving with a KV cache: float64 SDPA with the boolean mask built from
+    the definitions (query row i of a batch element with a cache of L keys sits
+    at position L - Sq + i; KV-length: every key j < L), GQA, ragged lengths
+    and Sq > 1; constant scores give the mean of V over keys 0..L-Sq+i and
+    LSE ln(L-Sq+i+1); a cache of L keys equals attention over the first L keys
+    alone; the decode mask with L = Sq = Sk is the causal mask; softcap."""
+    B, Sq, Sk, Hq, Hk, D = 3, 4, 90, 8, 2, 64
+    q = _rand((B, Sq, Hq, D), "qd")
+    k, v = _rand((B, Sk, Hk, D), "kd"), _rand((B, Sk, Hk, D), "vd")
+    L = np.array([90, 37, 4], dtype=np.int32)
+    ii = np.arange(Sq)[None, :, None]
+    jj = np.arange(Sk)[None, None, :]
+    Lb = L[:, None, None]
+    dec = (jj < Lb) & (jj <= Lb - Sq + ii)            # [B, Sq, Sk]
+    kvl = np.broadcast_to(jj < Lb, (B, Sq, Sk))
+    for name, m in (("decode", dec), ("kv_len", kvl)):
+        o, _ = oracle.attention(q, k, v, mask=name, kv_len=L, lib=lib)
+        ref = _sdpa(q, k, v, mask=torch.from_numpy(np.ascontiguousarray(m[:, None])),
+                    enable_gqa=True)
+        _close(o, ref, what=f"SDPA {name}")
+    # closed form on constant scores
+    q0 = _bf(np.zeros((B, Sq, Hq, D)))
+    o, lse = oracle.attention(q0, k, v, mask="decode", kv_len=L, lib=lib)
+    vf = _f64(v)
+    for b in range(B):
+        for i in range(Sq):
+            n = int(L[b]) - Sq + i + 1
+            for h in range(Hq):
+                _close(o[b, i, h], vf[b, :n, h // (Hq // Hk)].mean(axis=0), what="decode mean")
+                _close(lse[b, h, i], math.log(n), what="decode LSE")
+    # a cache of L keys is attention over those L keys alone (per batch element)
+    o, lse = oracle.attention(q, k, v, mask="kv_len", kv_len=L, lib=lib)
+    for b in range(B):
+        n = int(L[b])
+        ob, lb = oracle.attention(q[b:b + 1], k[b:b + 1, :n], v[b:b + 1, :n], lib=lib)
+        _close(o[b], ob[0], what="kv_len truncation")
+        _close(lse[b], lb[0], what="kv_len truncation LSE")
+    # decode with L = Sq = Sk is causal
+    qs, ks, vs = _rand((2, 33, 2, D), "qs"), _rand((2, 33, 2, D), "ks"), _rand((2, 33, 2, D), "vs")
+    o1, l1 = oracle.attention(qs, ks, vs, mask="decode", kv_len=np.array([33, 33]), lib=lib)
+    o2, l2 = oracle.attention(qs, ks, vs, mask="causal", lib=lib)
+    _close(o1, o2, what="decode = causal")
+    _close(l1, l2, what="decode = causal LSE")
+    # softcap on the decode mask against SDPA with the capped scores as an
+    # additive term (scores computed in float64 from the same bits)
+    cap = 20.0
+    Q, K = _f64(q), _f64(k)
+    z = np.einsum("bihd,bjhd->bhij", Q, np.repeat(K, Hq // Hk, axis=2)) / math.sqrt(D)
+    add = cap * np.tanh(z / cap) - z + np.where(dec[:, None], 0.0, -np.inf)
+    o, _ = oracle.attention(q, k, v, mod="softcap", softcap=cap, mask="decode", kv_len=L, lib=lib)
+    _close(o, _sdpa(q, k, v, mask=torch.from_numpy(add), enable_gqa=True), atol=1e-9,
+           what="SDPA decode softcap")
+
+
 ALL_PINS = [pin_constant_scores, pin_alibi_geometric, pin_softcap_two_keys, pin_one_hot,
             pin_rows_sum_to_one, pin_shift_invariance, pin_permutation, pin_causal_row0,
-            pin_sdpa, pin_reductions, pin_rows_api, pin_diff, pin_evo, pin_fully_masked_row]
+            pin_sdpa, pin_reductions, pin_rows_api, pin_diff, pin_evo, pin_fully_masked_row,
+            pin_decode]

@@ -34,6 +34,9 @@ MUTANTS = {
     "k_row_uses_q_stride": ("j * p->k_stride[1]", "j * p->q_stride[1]"),
     "v_wrong_row": ("j * p->v_stride[1] + hk", "(p->Sk - 1 - j) * p->v_stride[1] + hk"),
     "softmax_not_normalised": ("const double pj = exp(z[j] - m) / l;", "const double pj = exp(z[j] - m);"),
+    "kv_len_inclusive": ("return j < p->kv_len[b];", "return j <= p->kv_len[b];"),
+    "decode_position_off_by_one": ("j <= (int64_t)p->kv_len[b] - p->Sq + i", "j < (int64_t)p->kv_len[b] - p->Sq + i"),
+    "decode_rows_from_start": ("j <= (int64_t)p->kv_len[b] - p->Sq + i", "j <= i"),
 }
 
 
