@@ -6,7 +6,8 @@ is missing, importing the binding's entry points raises.
 
 The names mirror the C ABI: :func:`fl_attn_fwd`, :func:`fl_attn_tile_shape`,
 :func:`fl_attn_status_string`, :func:`fl_attn_last_error`,
-:func:`fl_attn_version`.  Tensors are torch tensors on the current CUDA device
+:func:`fl_attn_version`, :func:`fl_attn_decode_workspace_size`,
+:func:`fl_attn_decode`.  Tensors are torch tensors on the current CUDA device
 (PyTorch provides device memory and streams; nothing else).
 """
 from __future__ import annotations
@@ -74,6 +75,15 @@ class FlDesc(ctypes.Structure):
     ]
 
 
+class FlDecodeDesc(ctypes.Structure):
+    _fields_ = [
+        ("score_mod", ctypes.c_int32), ("softcap", ctypes.c_float), ("causal", ctypes.c_int32),
+        ("scale", ctypes.c_float), ("kv_lens", ctypes.c_void_p), ("max_kv_len", ctypes.c_int32),
+        ("block_table", ctypes.c_void_p), ("block_table_stride", ctypes.c_int32),
+        ("error_word", ctypes.c_void_p), ("wait_timeout_us", ctypes.c_uint32),
+    ]
+
+
 class FlAttnError(RuntimeError):
     def __init__(self, status: int, detail: str):
         super().__init__(f"{fl_attn_status_string(status)} ({detail})")
@@ -105,6 +115,13 @@ def load_library(path: str = LIB_PATH):
     lib.fl_attn_last_error.restype = ctypes.c_char_p
     lib.fl_attn_last_error.argtypes = []
     lib.fl_attn_version.restype = ctypes.c_int32
+    lib.fl_attn_decode_workspace_size.restype = ctypes.c_int
+    lib.fl_attn_decode_workspace_size.argtypes = [P(FlTensor), P(FlTensor), P(FlDecodeDesc),
+                                                  P(ctypes.c_size_t)]
+    lib.fl_attn_decode.restype = ctypes.c_int
+    lib.fl_attn_decode.argtypes = [P(FlTensor), P(FlTensor), P(FlTensor), P(FlTensor), P(FlTensor),
+                                   P(FlDecodeDesc), ctypes.c_void_p, ctypes.c_size_t,
+                                   ctypes.c_void_p]
     _lib = lib
     return lib
 
@@ -205,6 +222,56 @@ def fl_attn_last_error() -> str:
 
 def fl_attn_version() -> int:
     return int(load_library().fl_attn_version())
+
+
+def make_decode_desc(kv_lens, max_kv_len: int, *, score_mod="none", softcap=20.0, causal=True,
+                     scale=0.0, block_table=None, error_word=None,
+                     wait_timeout_us=0) -> FlDecodeDesc:
+    """Build an fl_decode_desc; kv_lens and block_table are device int32 torch tensors."""
+    d = FlDecodeDesc()
+    d.score_mod = MODS[score_mod] if isinstance(score_mod, str) else int(score_mod)
+    d.softcap = float(softcap)
+    d.causal = 1 if causal else 0
+    d.scale = float(scale)
+    d.kv_lens = kv_lens.data_ptr()
+    d.max_kv_len = int(max_kv_len)
+    if block_table is not None:
+        d.block_table = block_table.data_ptr()
+        d.block_table_stride = int(block_table.stride(0))
+    d.error_word = error_word.data_ptr() if error_word is not None else None
+    d.wait_timeout_us = int(wait_timeout_us)
+    d._keep = (kv_lens, block_table, error_word)
+    return d
+
+
+def fl_attn_decode_workspace_size(q, k_cache, desc: FlDecodeDesc) -> int:
+    """Bytes of workspace fl_attn_decode needs for these shapes."""
+    lib = load_library()
+    n = ctypes.c_size_t()
+    st = lib.fl_attn_decode_workspace_size(ctypes.byref(as_fl_tensor(q)),
+                                           ctypes.byref(as_fl_tensor(k_cache)), ctypes.byref(desc),
+                                           ctypes.byref(n))
+    if st != FL_OK:
+        raise FlAttnError(st, fl_attn_last_error())
+    return n.value
+
+
+def fl_attn_decode(q, k_cache, v_cache, out, lse, desc: FlDecodeDesc, workspace, stream=None) -> None:
+    """Enqueue attention against a KV cache (see include/fl_attn.h); workspace is a
+    device torch tensor of at least fl_attn_decode_workspace_size bytes."""
+    lib = load_library()
+    if stream is None:
+        import torch
+        stream = torch.cuda.current_stream().cuda_stream
+    elif hasattr(stream, "cuda_stream"):
+        stream = stream.cuda_stream
+    tensors = [as_fl_tensor(x) for x in (q, k_cache, v_cache, out, lse)]
+    nbytes = workspace.numel() * workspace.element_size()
+    st = lib.fl_attn_decode(_ref(tensors[0]), _ref(tensors[1]), _ref(tensors[2]), _ref(tensors[3]),
+                            _ref(tensors[4]), ctypes.byref(desc), ctypes.c_void_p(workspace.data_ptr()),
+                            nbytes, ctypes.c_void_p(stream))
+    if st != FL_OK:
+        raise FlAttnError(st, fl_attn_last_error())
 
 
 def default_scale(head_dim: int) -> float:

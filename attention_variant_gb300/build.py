@@ -17,7 +17,7 @@ ROOT = os.path.dirname(HERE)
 CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(BUILD, "libflattn.so")
-SOURCES = ["api.cu", "fwd_standard.cu", "fwd_diff.cu", "fwd_evo.cu"]
+SOURCES = ["api.cu", "fwd_standard.cu", "fwd_diff.cu", "fwd_evo.cu", "fwd_decode.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC = os.environ.get("NVCC", "nvcc")
 

@@ -576,9 +576,195 @@ fl_status fwd_evo(bool row_pass, const fl_tensor *q, const fl_tensor *k, const f
     return ok();
 }
 
+// ------------------------------------------------------------------ decode
+
+constexpr size_t kWsAlign = 256;
+size_t align_up(size_t x) { return (x + kWsAlign - 1) / kWsAlign * kWsAlign; }
+
+struct DecodePlan {
+    View Q, K, V;
+    int64_t B, Sq, Hq, Hk, P, T;
+    int G, R, max_chunks;
+    size_t o_bytes, ml_bytes, cnt_bytes, total;
+};
+
+// Validates the shapes common to the workspace query and the call.
+fl_status decode_plan(const fl_tensor *q, const fl_tensor *k_cache, const fl_tensor *v_cache,
+                      const fl_decode_desc *d, DecodePlan &pl)
+{
+    fl_status s;
+    if (!d)
+        return fail(FL_ERR_INVALID_ARG, "desc is NULL");
+    if ((s = check_tensor(q, "q", 4, FL_BF16, pl.Q)) != FL_OK) return s;
+    if ((s = check_tensor(k_cache, "k_cache", 4, FL_BF16, pl.K)) != FL_OK) return s;
+    if (v_cache) {
+        if ((s = check_tensor(v_cache, "v_cache", 4, FL_BF16, pl.V)) != FL_OK) return s;
+        if (!same(pl.V, {pl.K.size[0], pl.K.size[1], pl.K.size[2], pl.K.size[3]}))
+            return fail(FL_ERR_INVALID_ARG, "v_cache must have the shape of k_cache");
+    }
+    pl.B = pl.Q.size[0];
+    pl.Sq = pl.Q.size[1];
+    pl.Hq = pl.Q.size[2];
+    pl.P = pl.K.size[0];
+    pl.T = pl.K.size[1];
+    pl.Hk = pl.K.size[2];
+    if (pl.Q.size[3] != 64 || pl.K.size[3] != 64)
+        return fail(FL_ERR_UNSUPPORTED, "decode supports head dimension 64");
+    if (pl.Hq % pl.Hk != 0)
+        return fail(FL_ERR_INVALID_ARG, "Hq (%lld) must be a multiple of Hk (%lld)",
+                    (long long)pl.Hq, (long long)pl.Hk);
+    pl.G = int(pl.Hq / pl.Hk);
+    if (int64_t(pl.G) * pl.Sq > fl::kDecodeMaxRows)
+        return fail(FL_ERR_UNSUPPORTED, "(Hq / Hk) * Sq = %lld exceeds %d",
+                    (long long)(int64_t(pl.G) * pl.Sq), fl::kDecodeMaxRows);
+    pl.R = int(pl.G * pl.Sq);
+    if (d->max_kv_len < 1)
+        return fail(FL_ERR_INVALID_ARG, "max_kv_len must be >= 1");
+    if (d->score_mod != FL_MOD_NONE && d->score_mod != FL_MOD_SOFTCAP)
+        return fail(FL_ERR_UNSUPPORTED, "decode supports score_mod none or softcap");
+    if (d->score_mod == FL_MOD_SOFTCAP && !(d->softcap > 0.f && std::isfinite(d->softcap)))
+        return fail(FL_ERR_INVALID_ARG, "softcap must be positive and finite");
+    if (!std::isfinite(d->scale) || d->scale < 0.f)
+        return fail(FL_ERR_INVALID_ARG, "scale must be finite and positive (0 selects 1/sqrt(D))");
+    if (!d->block_table) {
+        if (pl.P != pl.B)
+            return fail(FL_ERR_INVALID_ARG, "a contiguous cache is [B, S_max, Hk, 64]");
+        if (d->max_kv_len > pl.T)
+            return fail(FL_ERR_INVALID_ARG, "max_kv_len %d exceeds the cache length %lld",
+                        d->max_kv_len, (long long)pl.T);
+    } else {
+        if (pl.T != 16 && pl.T != 32 && pl.T != 64 && pl.T != 128 && pl.T != 256)
+            return fail(FL_ERR_UNSUPPORTED, "page size %lld: must be 16, 32, 64, 128 or 256",
+                        (long long)pl.T);
+        if (int64_t(d->block_table_stride) * pl.T < d->max_kv_len)
+            return fail(FL_ERR_INVALID_ARG, "block_table_stride %d pages cannot hold %d keys",
+                        d->block_table_stride, d->max_kv_len);
+        if (reinterpret_cast<uintptr_t>(d->block_table) % 4)
+            return fail(FL_ERR_ALIGNMENT, "block_table is not 4-byte aligned");
+    }
+    pl.max_chunks = (d->max_kv_len + fl::kDecodeChunk - 1) / fl::kDecodeChunk;
+    const size_t units = size_t(pl.B) * size_t(pl.Hk) * size_t(pl.max_chunks) * size_t(pl.R);
+    pl.o_bytes = align_up(units * 64 * sizeof(float));
+    pl.ml_bytes = align_up(units * 2 * sizeof(float));
+    pl.cnt_bytes = align_up(size_t(pl.B) * size_t(pl.Hk) * sizeof(int));
+    pl.total = pl.o_bytes + pl.ml_bytes + pl.cnt_bytes;
+    return FL_OK;
+}
+
+fl_status decode_run(const DecodePlan &pl, const fl_tensor *out, const fl_tensor *lse,
+                     const fl_decode_desc *d, void *workspace, cudaStream_t stream)
+{
+    View O, L{};
+    fl_status s;
+    if ((s = check_tensor(out, "out", 4, FL_BF16, O)) != FL_OK) return s;
+    if (!same(O, {pl.B, pl.Sq, pl.Hq, 64}))
+        return fail(FL_ERR_INVALID_ARG, "out must be [B, Sq, Hq, 64]");
+    if (lse) {
+        if ((s = check_tensor(lse, "lse", 3, FL_F32, L)) != FL_OK) return s;
+        if (!same(L, {pl.B, pl.Hq, pl.Sq}))
+            return fail(FL_ERR_INVALID_ARG, "lse must be [B, Hq, Sq]");
+    }
+    if (!d->kv_lens)
+        return fail(FL_ERR_INVALID_ARG, "kv_lens is NULL");
+    if (reinterpret_cast<uintptr_t>(d->kv_lens) % 4)
+        return fail(FL_ERR_ALIGNMENT, "kv_lens is not 4-byte aligned");
+    int dev;
+    DeviceInfo info;
+    if ((s = device_info(dev, info)) != FL_OK) return s;
+
+    CUtensorMap tk, tv;
+    const uint32_t box[4] = {64, uint32_t(pl.T < fl::kDecodeChunk ? pl.T : fl::kDecodeChunk), 1, 1};
+    const View *src[2] = {&pl.K, &pl.V};
+    CUtensorMap *dst[2] = {&tk, &tv};
+    const char *names[2] = {"k_cache", "v_cache"};
+    for (int m = 0; m < 2; ++m) {
+        const View &T = *src[m];
+        const uint64_t dims[4] = {64, uint64_t(pl.T), uint64_t(pl.Hk), uint64_t(pl.P)};
+        const uint64_t st[3] = {uint64_t(T.stride[1]) * 2, uint64_t(T.stride[2]) * 2,
+                                uint64_t(T.stride[0]) * 2};
+        if ((s = make_map(*dst[m], T.ptr, 4, dims, st, box, CU_TENSOR_MAP_SWIZZLE_128B, names[m])) != FL_OK)
+            return s;
+    }
+    fl::DecodeParams p{};
+    p.B = int(pl.B);
+    p.Hk = int(pl.Hk);
+    p.G = pl.G;
+    p.Sq = int(pl.Sq);
+    p.max_kv = d->max_kv_len;
+    p.max_chunks = pl.max_chunks;
+    p.page = int(pl.T);
+    p.bt_stride = d->block_table_stride;
+    p.kv_lens = d->kv_lens;
+    p.block_table = d->block_table;
+    p.q = static_cast<const __nv_bfloat16 *>(pl.Q.ptr);
+    p.q_sb = pl.Q.stride[0];
+    p.q_ss = pl.Q.stride[1];
+    p.q_sh = pl.Q.stride[2];
+    p.out = static_cast<__nv_bfloat16 *>(O.ptr);
+    p.o_sb = O.stride[0];
+    p.o_ss = O.stride[1];
+    p.o_sh = O.stride[2];
+    if (lse) {
+        p.lse = static_cast<float *>(L.ptr);
+        p.l_sb = L.stride[0];
+        p.l_sh = L.stride[1];
+    }
+    p.scale = d->scale != 0.f ? d->scale : 0.125f; // 1 / sqrt(64)
+    p.softcap = d->score_mod == FL_MOD_SOFTCAP ? d->softcap : 0.f;
+    p.causal = d->causal ? 1 : 0;
+    uint8_t *ws = static_cast<uint8_t *>(workspace);
+    p.ws_o = reinterpret_cast<float *>(ws);
+    p.ws_ml = reinterpret_cast<float *>(ws + pl.o_bytes);
+    p.ws_cnt = reinterpret_cast<int *>(ws + pl.o_bytes + pl.ml_bytes);
+    p.err_user = d->error_word;
+    p.timeout_ns = uint64_t(d->wait_timeout_us ? d->wait_timeout_us : 2000000u) * 1000ull;
+
+    // the per-(sequence, KV head) tickets must start at zero
+    cudaError_t e = cudaMemsetAsync(p.ws_cnt, 0, size_t(pl.B) * size_t(pl.Hk) * sizeof(int), stream);
+    if (e != cudaSuccess)
+        return fail(FL_ERR_CUDA, "clearing the workspace counters failed: %s", cudaGetErrorString(e));
+    e = fl::launch_decode(tk, tv, p, stream);
+    if (e != cudaSuccess)
+        return fail(FL_ERR_CUDA, "kernel launch failed: %s", cudaGetErrorString(e));
+    return ok();
+}
+
 } // namespace
 
 extern "C" {
+
+fl_status fl_attn_decode_workspace_size(const fl_tensor *q, const fl_tensor *k_cache,
+                                        const fl_decode_desc *desc, size_t *bytes)
+{
+    if (!bytes)
+        return fail(FL_ERR_INVALID_ARG, "bytes is NULL");
+    DecodePlan pl;
+    fl_status s = decode_plan(q, k_cache, nullptr, desc, pl);
+    if (s != FL_OK)
+        return s;
+    *bytes = pl.total;
+    return ok();
+}
+
+fl_status fl_attn_decode(const fl_tensor *q, const fl_tensor *k_cache, const fl_tensor *v_cache,
+                         const fl_tensor *out, const fl_tensor *lse, const fl_decode_desc *desc,
+                         void *workspace, size_t workspace_bytes, fl_stream_t stream)
+{
+    if (!v_cache)
+        return fail(FL_ERR_INVALID_ARG, "v_cache is NULL");
+    DecodePlan pl;
+    fl_status s = decode_plan(q, k_cache, v_cache, desc, pl);
+    if (s != FL_OK)
+        return s;
+    if (!workspace)
+        return fail(FL_ERR_INVALID_ARG, "workspace is NULL");
+    if (reinterpret_cast<uintptr_t>(workspace) % kWsAlign)
+        return fail(FL_ERR_ALIGNMENT, "workspace is not %zu-byte aligned", kWsAlign);
+    if (workspace_bytes < pl.total)
+        return fail(FL_ERR_INVALID_ARG, "workspace holds %zu bytes, %zu needed", workspace_bytes,
+                    pl.total);
+    return decode_run(pl, out, lse, desc, workspace, reinterpret_cast<cudaStream_t>(stream));
+}
 
 fl_status fl_attn_fwd(const fl_tensor *q, const fl_tensor *k, const fl_tensor *v,
                       const fl_tensor *out, const fl_tensor *lse,

@@ -74,6 +74,36 @@ struct EvoParams {
     uint64_t timeout_ns;
 };
 
+// ---- serving with a KV cache (fwd_decode.cu)
+constexpr int kDecodeChunk = 128; // keys per CTA (and per workspace partial)
+constexpr int kDecodeMaxRows = 64; // G * Sq query rows per (sequence, KV head)
+
+struct DecodeParams {
+    int B, Hk, G, Sq;
+    int max_kv, max_chunks;
+    int page;                     // keys per page (paged cache)
+    int64_t bt_stride;            // block_table row stride
+    const int32_t *kv_lens;       // [B]
+    const int32_t *block_table;   // [B][bt_stride] or null (contiguous cache)
+    const __nv_bfloat16 *q;       // [B, Sq, Hq, 64] element strides:
+    int64_t q_sb, q_ss, q_sh;
+    __nv_bfloat16 *out;
+    int64_t o_sb, o_ss, o_sh;
+    float *lse;                   // [B, Hq, Sq] or null
+    int64_t l_sb, l_sh;
+    float scale, softcap;         // softcap 0: none
+    int causal;
+    float *ws_o;                  // [B][Hk][max_chunks][R][64]
+    float *ws_ml;                 // [B][Hk][max_chunks][R][2]
+    int *ws_cnt;                  // [B][Hk], zero before the launch
+    uint32_t *err_user;
+    uint64_t timeout_ns;
+};
+
+cudaError_t launch_decode(const CUtensorMap &tk, const CUtensorMap &tv, const DecodeParams &p,
+                          cudaStream_t stream);
+size_t decode_smem_bytes(int R);
+
 cudaError_t launch_evo(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
                        const CUtensorMap &tb, const EvoParams &p, int grid, cudaStream_t stream);
 int evo_max_bias_keys();

@@ -124,6 +124,18 @@ def evo_entry(row):
                 bytes=5 * tensor_bytes + (H * Nr * Nr * 2 if row else 0))
 
 
+def decode_entry(mod):
+    """The serving workload: one new token per sequence against a paged cache."""
+    w = workloads.DECODE
+    B, Sq, Hq, Hk, D = w["B"], w["Sq"], w["Hq"], w["Hk"], w["D"]
+    lens = testdata.kv_lengths(B, w["name"], w["kv_lo"], w["kv_hi"]).astype(np.int64)
+    keys = int(lens.sum())
+    return dict(name=w["name"], kind="decode", variant="causal" if mod == "none" else "softcap",
+                mod=mod, B=B, Sq=Sq, Hq=Hq, Hk=Hk, D=D, lens=lens, page=w["page"],
+                flops=4 * D * Sq * Hq * keys,
+                bytes=2 * 2 * keys * Hk * D + 2 * 2 * B * Sq * Hq * D + 4 * B * Hq * Sq)
+
+
 def all_entries():
     out = [entry("mha", S, v) for S in workloads.MHA_SEQ_LENS for v in workloads.MHA_VARIANTS]
     out += [entry("gqa", S, m) for S, _ in workloads.GQA_SHAPES for m in workloads.GQA_MASKS]
@@ -326,6 +338,45 @@ def time_other(e, torch, fa, device, steps, warmup, flush, stream):
     return [a.elapsed_time(b) for a, b in evs]
 
 
+def time_decode(e, torch, fa, device, steps, warmup, flush, stream):
+    """Device time of the decode kernel on its workload (paged cache, pages of
+    each sequence scattered over the pool)."""
+    B, Sq, Hq, Hk, D, page = e["B"], e["Sq"], e["Hq"], e["Hk"], e["D"], e["page"]
+    per = [-(-int(L) // page) for L in e["lens"]]
+    n_pages = sum(per)
+    perm = np.random.default_rng(7).permutation(n_pages).astype(np.int32)
+    table = np.full((B, max(per)), -1, dtype=np.int32)
+    at = 0
+    for b in range(B):
+        table[b, : per[b]] = perm[at: at + per[b]]
+        at += per[b]
+    to = lambda x: torch.from_numpy(x.view(np.int16)).view(torch.bfloat16).to(device)
+    q = to(testdata.normal_bf16((B, Sq, Hq, D), e["name"], "q"))
+    kp = to(testdata.normal_bf16((n_pages, page, Hk, D), e["name"], "kpool"))
+    vp = to(testdata.normal_bf16((n_pages, page, Hk, D), e["name"], "vpool"))
+    out = torch.empty((B, Sq, Hq, D), dtype=torch.bfloat16, device=device)
+    lse = torch.empty((B, Hq, Sq), dtype=torch.float32, device=device)
+    lens_t = torch.from_numpy(e["lens"].astype(np.int32)).to(device)
+    table_t = torch.from_numpy(table).to(device)
+    d = fa.make_decode_desc(lens_t, int(e["lens"].max()), score_mod=e["mod"], softcap=workloads.SOFTCAP,
+                            causal=True, block_table=table_t)
+    ws = torch.empty(fa.fl_attn_decode_workspace_size(q, kp, d), dtype=torch.uint8, device=device)
+    with torch.cuda.stream(stream):
+        for _ in range(warmup):
+            flush.zero_()
+            fa.fl_attn_decode(q, kp, vp, out, lse, d, ws, stream=stream)
+        torch.cuda.synchronize()
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(steps)]
+        for a, b in evs:
+            flush.zero_()
+            a.record(stream)
+            fa.fl_attn_decode(q, kp, vp, out, lse, d, ws, stream=stream)
+            b.record(stream)
+        torch.cuda.synchronize()
+    return [a.elapsed_time(b) for a, b in evs]
+
+
 def time_e2e(e, host, torch, fa, device, steps, warmup, stream):
     """Same metric end to end: every step copies its inputs from pinned host
     memory to the device, runs the fused forward and reads O and LSE back to
@@ -416,7 +467,8 @@ def cpu_baseline(e, seconds=12.0):
 
 
 ONLY = {"diff": lambda: diff_entry("none"), "diff_causal": lambda: diff_entry("causal"),
-        "evo_row": lambda: evo_entry(True), "evo_col": lambda: evo_entry(False)}
+        "evo_row": lambda: evo_entry(True), "evo_col": lambda: evo_entry(False),
+        "decode": lambda: decode_entry("none"), "decode_softcap": lambda: decode_entry("softcap")}
 
 
 def run_only(args):
@@ -429,7 +481,8 @@ def run_only(args):
     stream = torch.cuda.Stream(device)
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=device)
     e = ONLY[args.only]()
-    ms = statistics.mean(time_other(e, torch, fa, device, args.steps, args.warmup, flush, stream))
+    timer = time_decode if e["kind"] == "decode" else time_other
+    ms = statistics.mean(timer(e, torch, fa, device, args.steps, args.warmup, flush, stream))
     print(json.dumps({"only": args.only, "ms": round(ms, 4),
                       "tflops": round(e["flops"] / (ms * 1e-3) / 1e12, 1),
                       "gbs": round(e["bytes"] / (ms * 1e-3) / 1e9, 1)}), flush=True)
@@ -487,6 +540,12 @@ def run_ours(args):
             if e["kind"].startswith("evo"):
                 rec["frac_hbm"] = round(gbs / peaks["hbm_gbs"], 4)
             variants[f"{e['name']}/{e['variant']}"] = rec
+        for e in (decode_entry("none"), decode_entry("softcap")):
+            vm = statistics.mean(time_decode(e, torch, fa, device, args.variant_steps, 2, flush, stream))
+            gbs = e["bytes"] / (vm * 1e-3) / 1e9
+            variants[f"{e['name']}/{e['variant']}"] = dict(
+                tflops=round(e["flops"] / (vm * 1e-3) / 1e12, 1), ms=round(vm, 4), gbs=round(gbs, 1),
+                frac_hbm=round(gbs / peaks["hbm_gbs"], 4))
         for e in all_entries():
             h = gpu_inputs(e, torch, device) if (e["S"], e["kind"]) != (head["S"], "mha") else host
             vms, _ = time_entry(e, h, torch, fa, device, args.variant_steps, 2, flush, stream)

@@ -176,6 +176,57 @@ const char *fl_attn_last_error(void);
 /* FL_ATTN_VERSION of the loaded library. */
 int32_t fl_attn_version(void);
 
+/* ------------------------------------------------------------------------
+ * Serving with a KV cache (decode).
+ *
+ * A few new query tokens per sequence attend to that sequence's cached keys
+ * and values: the LLaMA-3.2-1B serving workload of the talk notes ("End-to-end:
+ * LLaMA-3.2-1B (vLLM / Mooncake)"), whose attention is made causal or
+ * softcapped.  out = softmax(score_mod(scale q k^T) + mask) v over the keys
+ * 0 .. kv_lens[b] - 1 of sequence b; with `causal`, new token s of a sequence
+ * of L cached keys (the new tokens included) sits at position L - Sq + s and
+ * sees the keys up to it.
+ */
+typedef struct {
+    int32_t score_mod;          /* FL_MOD_NONE or FL_MOD_SOFTCAP */
+    float softcap;              /* FL_MOD_SOFTCAP: the cap (> 0) */
+    int32_t causal;             /* 1: decode-causal as above; 0: every cached key */
+    float scale;                /* 0 means 1 / sqrt(D) */
+    const int32_t *kv_lens;     /* device int32 [B]: cache length of each sequence */
+    int32_t max_kv_len;         /* host bound on kv_lens[] (sizes the launch and the workspace);
+                                   larger entries are clamped to it */
+    const int32_t *block_table; /* NULL: contiguous cache; else device int32
+                                   [B][block_table_stride]: page index of each page of a
+                                   sequence */
+    int32_t block_table_stride; /* entries per row of block_table */
+    uint32_t *error_word;       /* NULL, or a device word the kernel ORs FL_DEVERR_* into */
+    uint32_t wait_timeout_us;   /* bound of every device-side wait; 0 means 2,000,000 */
+} fl_decode_desc;
+
+/*
+ * Layouts (bf16 except lse):
+ *   q        [B, Sq, Hq, 64]
+ *   k_cache, v_cache
+ *            contiguous (block_table NULL): [B, S_max, Hk, 64], S_max >= max_kv_len;
+ *            paged: [num_pages, page_size, Hk, 64] with page_size in
+ *            {16, 32, 64, 128, 256}; key p of sequence b is row p % page_size of
+ *            page block_table[b][p / page_size]
+ *   out      [B, Sq, Hq, 64]
+ *   lse      [B, Hq, Sq] fp32 (natural log) or NULL
+ * Hq must be a multiple of Hk, and (Hq / Hk) * Sq <= 64.  The kernel splits
+ * every sequence's keys into chunks of 128 and merges the chunks' partial
+ * results through `workspace`: device memory of at least the size
+ * fl_attn_decode_workspace_size reports, 256-byte aligned, owned by the
+ * caller; its contents need no initialisation (the call clears what must
+ * start at zero).  Calls sharing one workspace must not overlap on the GPU.
+ */
+fl_status fl_attn_decode_workspace_size(const fl_tensor *q, const fl_tensor *k_cache,
+                                        const fl_decode_desc *desc, size_t *bytes);
+
+fl_status fl_attn_decode(const fl_tensor *q, const fl_tensor *k_cache, const fl_tensor *v_cache,
+                         const fl_tensor *out, const fl_tensor *lse, const fl_decode_desc *desc,
+                         void *workspace, size_t workspace_bytes, fl_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

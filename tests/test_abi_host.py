@@ -106,3 +106,67 @@ def test_tile_shape(lib):
     assert fa.fl_attn_tile_shape(fa.make_desc(kind="evo_row"), 32) == (128, 128)
     with pytest.raises(fa.FlAttnError):
         fa.fl_attn_tile_shape(fa.make_desc(), 48)
+
+
+def _ddesc(max_kv=1000, kv_lens=0x20000, block_table=None, bt_stride=0, score_mod=0, softcap=0.0):
+    d = fa.FlDecodeDesc()
+    d.score_mod = score_mod
+    d.softcap = softcap
+    d.causal = 1
+    d.kv_lens = kv_lens
+    d.max_kv_len = max_kv
+    d.block_table = block_table
+    d.block_table_stride = bt_stride
+    return d
+
+
+def _ws_bytes(lib, q, kc, d):
+    n = ctypes.c_size_t()
+    st = lib.fl_attn_decode_workspace_size(ctypes.byref(q), ctypes.byref(kc), ctypes.byref(d),
+                                           ctypes.byref(n))
+    return st, n.value
+
+
+def test_decode_workspace_size(lib):
+    B, Sq, Hq, Hk, Smax = 3, 2, 8, 2, 1000
+    st, n = _ws_bytes(lib, _t((B, Sq, Hq, 64)), _t((B, Smax, Hk, 64)), _ddesc(max_kv=1000))
+    assert st == fa.FL_OK, fa.fl_attn_last_error()
+    R, chunks = (Hq // Hk) * Sq, -(-1000 // 128)
+    up = lambda x: -(-x // 256) * 256
+    units = B * Hk * chunks * R
+    assert n == up(units * 64 * 4) + up(units * 2 * 4) + up(B * Hk * 4)
+
+
+def test_decode_validation_before_device(lib):
+    B, Sq, Hq, Hk, Smax = 2, 1, 8, 2, 512
+    q, kc = _t((B, Sq, Hq, 64)), _t((B, Smax, Hk, 64))
+    r = lambda x: ctypes.byref(x) if x is not None else None
+
+    def call(q=q, kc=kc, vc=None, o=None, lse=None, d=None, ws=0x40000, nbytes=1 << 30):
+        vc = vc if vc is not None else _t((B, Smax, Hk, 64))
+        o = o if o is not None else _t((B, Sq, Hq, 64))
+        d = d if d is not None else _ddesc(max_kv=500)
+        return lib.fl_attn_decode(r(q), r(kc), r(vc), r(o), r(lse), ctypes.byref(d), ws, nbytes,
+                                  None)
+
+    assert _ws_bytes(lib, _t((B, Sq, Hq, 128)), _t((B, Smax, Hk, 128)), _ddesc())[0] == \
+        fa.FL_ERR_UNSUPPORTED                                        # head dimension
+    assert _ws_bytes(lib, _t((B, 17, Hq, 64)), kc, _ddesc(max_kv=500))[0] == \
+        fa.FL_ERR_UNSUPPORTED                                        # (Hq/Hk) * Sq > 64
+    assert _ws_bytes(lib, q, kc, _ddesc(max_kv=513))[0] == fa.FL_ERR_INVALID_ARG  # > S_max
+    assert _ws_bytes(lib, q, _t((5, 48, Hk, 64)), _ddesc(max_kv=500, block_table=0x30000,
+                                                         bt_stride=11))[0] == fa.FL_ERR_UNSUPPORTED
+    assert _ws_bytes(lib, q, _t((5, 64, Hk, 64)), _ddesc(max_kv=500, block_table=0x30000,
+                                                         bt_stride=7))[0] == fa.FL_ERR_INVALID_ARG
+    assert _ws_bytes(lib, q, kc, _ddesc(max_kv=500, score_mod=fa.FL_MOD_ALIBI))[0] == \
+        fa.FL_ERR_UNSUPPORTED
+    assert _ws_bytes(lib, q, kc, _ddesc(max_kv=500, score_mod=fa.FL_MOD_SOFTCAP))[0] == \
+        fa.FL_ERR_INVALID_ARG                                        # softcap 0
+    assert call(vc=_t((B, Smax, Hk + 1, 64))) == fa.FL_ERR_INVALID_ARG
+    assert call(ws=0) == fa.FL_ERR_INVALID_ARG
+    assert call(ws=0x40010) == fa.FL_ERR_ALIGNMENT
+    assert call(nbytes=1024) == fa.FL_ERR_INVALID_ARG
+    assert "workspace holds" in fa.fl_attn_last_error()
+    assert call(o=_t((B, Sq, Hq + 1, 64))) == fa.FL_ERR_INVALID_ARG
+    assert call(lse=_t((B, Hq, Sq + 1), fa.FL_F32)) == fa.FL_ERR_INVALID_ARG
+    assert call(d=_ddesc(max_kv=500, kv_lens=None)) == fa.FL_ERR_INVALID_ARG
