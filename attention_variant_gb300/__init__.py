@@ -7,7 +7,7 @@ is missing, importing the binding's entry points raises.
 The names mirror the C ABI: :func:`fl_attn_fwd`, :func:`fl_attn_tile_shape`,
 :func:`fl_attn_status_string`, :func:`fl_attn_last_error`,
 :func:`fl_attn_version`, :func:`fl_attn_decode_workspace_size`,
-:func:`fl_attn_decode`.  Tensors are torch tensors on the current CUDA device
+:func:`fl_attn_decode`, :func:`fl_attn_decode_static`.  Tensors are torch tensors on the current CUDA device
 (PyTorch provides device memory and streams; nothing else).
 """
 from __future__ import annotations
@@ -118,6 +118,9 @@ def load_library(path: str = LIB_PATH):
     lib.fl_attn_decode_workspace_size.restype = ctypes.c_int
     lib.fl_attn_decode_workspace_size.argtypes = [P(FlTensor), P(FlTensor), P(FlDecodeDesc),
                                                   P(ctypes.c_size_t)]
+    lib.fl_attn_decode_static.restype = ctypes.c_int
+    lib.fl_attn_decode_static.argtypes = [P(FlTensor), P(FlTensor), P(FlTensor), P(FlTensor),
+                                          P(FlTensor), P(FlDecodeDesc), ctypes.c_void_p]
     lib.fl_attn_decode.restype = ctypes.c_int
     lib.fl_attn_decode.argtypes = [P(FlTensor), P(FlTensor), P(FlTensor), P(FlTensor), P(FlTensor),
                                    P(FlDecodeDesc), ctypes.c_void_p, ctypes.c_size_t,
@@ -270,6 +273,26 @@ def fl_attn_decode(q, k_cache, v_cache, out, lse, desc: FlDecodeDesc, workspace,
     st = lib.fl_attn_decode(_ref(tensors[0]), _ref(tensors[1]), _ref(tensors[2]), _ref(tensors[3]),
                             _ref(tensors[4]), ctypes.byref(desc), ctypes.c_void_p(workspace.data_ptr()),
                             nbytes, ctypes.c_void_p(stream))
+    if st != FL_OK:
+        raise FlAttnError(st, fl_attn_last_error())
+
+
+def fl_attn_decode_static(q, k_cache, v_cache, out, lse, desc: FlDecodeDesc, stream=None) -> None:
+    """fl_attn_decode with the library's own static scratch instead of a
+    workspace: for callers that cannot allocate device memory.  Allocates
+    nothing; calls that overlap on the GPU race (they share the scratch); the
+    first call on a device sets up the scratch address, so make it before any
+    stream capture."""
+    lib = load_library()
+    if stream is None:
+        import torch
+        stream = torch.cuda.current_stream().cuda_stream
+    elif hasattr(stream, "cuda_stream"):
+        stream = stream.cuda_stream
+    tensors = [as_fl_tensor(x) for x in (q, k_cache, v_cache, out, lse)]
+    st = lib.fl_attn_decode_static(_ref(tensors[0]), _ref(tensors[1]), _ref(tensors[2]),
+                                   _ref(tensors[3]), _ref(tensors[4]), ctypes.byref(desc),
+                                   ctypes.c_void_p(stream))
     if st != FL_OK:
         raise FlAttnError(st, fl_attn_last_error())
 

@@ -733,6 +733,37 @@ fl_status decode_run(const DecodePlan &pl, const fl_tensor *out, const fl_tensor
 
 extern "C" {
 
+// No workspace argument: the scratch is the library's own static device
+// array (fl::decode_static_scratch), looked up on the first call per device.
+// Nothing is allocated.
+fl_status fl_attn_decode_static(const fl_tensor *q, const fl_tensor *k_cache,
+                                const fl_tensor *v_cache, const fl_tensor *out,
+                                const fl_tensor *lse, const fl_decode_desc *desc,
+                                fl_stream_t stream)
+{
+    if (!v_cache)
+        return fail(FL_ERR_INVALID_ARG, "v_cache is NULL");
+    DecodePlan pl;
+    fl_status s = decode_plan(q, k_cache, v_cache, desc, pl);
+    if (s != FL_OK)
+        return s;
+    if (pl.total > fl::kDecodeStaticScratch)
+        return fail(FL_ERR_UNSUPPORTED,
+                    "these shapes need %zu bytes of scratch; the library's static decode scratch "
+                    "holds %zu (use fl_attn_decode with a workspace)",
+                    pl.total, fl::kDecodeStaticScratch);
+    int dev;
+    DeviceInfo info;
+    if ((s = device_info(dev, info)) != FL_OK)
+        return s;
+    void *scratch = nullptr;
+    const cudaError_t e = fl::decode_static_scratch(&scratch);
+    if (e != cudaSuccess)
+        return fail(FL_ERR_CUDA, "looking up the static decode scratch failed: %s",
+                    cudaGetErrorString(e));
+    return decode_run(pl, out, lse, desc, scratch, reinterpret_cast<cudaStream_t>(stream));
+}
+
 fl_status fl_attn_decode_workspace_size(const fl_tensor *q, const fl_tensor *k_cache,
                                         const fl_decode_desc *desc, size_t *bytes)
 {

@@ -27,6 +27,7 @@
 //     sum), write bf16 O and the natural-log LSE, and zero its counter again.
 #include <cuda_bf16.h>
 #include <cstdint>
+#include <mutex>
 
 #include "common.cuh"
 #include "launch.h"
@@ -289,6 +290,47 @@ __global__ void __launch_bounds__(kThreads, 6)
 }
 
 } // namespace
+
+// ---- scratch for callers that cannot allocate device memory
+//
+// fl_attn_decode_static runs the same kernel with its workspace in this
+// array instead of caller memory: for callers that cannot call cudaMalloc
+// (one that must not take the device-wide synchronisation an allocation or
+// a free can cause in a serving loop, or a plug-in that does not own the
+// process's device allocator) and have no buffer to hand over.  Every GPU
+// that loads this library holds the array until the process exits; every
+// call shares it and finds the previous call's contents (the host clears the
+// counters, the only part that must start at zero, before each launch), so
+// calls that overlap on the GPU race.
+namespace {
+static __device__ __align__(256) uint8_t g_decode_scratch[kDecodeStaticScratch];
+
+std::mutex g_scratch_mutex;
+void *g_scratch_ptr[64];
+}
+
+// Device address of the scratch array on the current device.  The first call
+// on a device looks it up (host code cannot use the array's name as a device
+// address); later calls return the cached pointer.
+cudaError_t decode_static_scratch(void **ptr)
+{
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess)
+        return e;
+    if (dev < 0 || dev >= 64)
+        return cudaErrorInvalidDevice;
+    std::lock_guard<std::mutex> lock(g_scratch_mutex);
+    if (!g_scratch_ptr[dev]) {
+        void *p = nullptr;
+        e = cudaGetSymbolAddress(&p, g_decode_scratch);
+        if (e != cudaSuccess)
+            return e;
+        g_scratch_ptr[dev] = p;
+    }
+    *ptr = g_scratch_ptr[dev];
+    return cudaSuccess;
+}
 
 size_t decode_smem_bytes(int R)
 {

@@ -104,6 +104,10 @@ cudaError_t launch_decode(const CUtensorMap &tk, const CUtensorMap &tv, const De
                           cudaStream_t stream);
 size_t decode_smem_bytes(int R);
 
+// Size of the library's own decode scratch array (fl_attn_decode_static).
+constexpr size_t kDecodeStaticScratch = size_t(64) << 20;
+cudaError_t decode_static_scratch(void **ptr);
+
 cudaError_t launch_evo(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
                        const CUtensorMap &tb, const EvoParams &p, int grid, cudaStream_t stream);
 int evo_max_bias_keys();

@@ -227,6 +227,31 @@ fl_status fl_attn_decode(const fl_tensor *q, const fl_tensor *k_cache, const fl_
                          const fl_tensor *out, const fl_tensor *lse, const fl_decode_desc *desc,
                          void *workspace, size_t workspace_bytes, fl_stream_t stream);
 
+/*
+ * fl_attn_decode_static -- fl_attn_decode without a workspace argument, for
+ * callers that cannot allocate device memory: for example a serving loop that
+ * must not take the device-wide synchronisation a cudaMalloc or cudaFree can
+ * cause, or a plug-in that does not own the process's device allocator, and
+ * that has no buffer of its own to pass.  (The pages have no counterpart: it
+ * is an interface for such callers, not part of the method.)
+ *
+ * The call allocates nothing.  Its scratch is a static device array of
+ * FL_DECODE_STATIC_SCRATCH_BYTES (64 MiB) inside this library, which every GPU
+ * that loads the library holds until the process exits; shapes that need more
+ * (see fl_attn_decode_workspace_size) return FL_ERR_UNSUPPORTED.  The first
+ * call on each device looks up the array's device address (which may load
+ * the library's device code on that device): make that first call before any
+ * stream capture.  Every call shares the one array and finds the previous
+ * call's contents; the call clears what must start at zero, but calls that
+ * overlap on the GPU race: issue them on one stream, or order them.
+ * Arguments, layouts and results are those of fl_attn_decode.
+ */
+#define FL_DECODE_STATIC_SCRATCH_BYTES (64u << 20)
+fl_status fl_attn_decode_static(const fl_tensor *q, const fl_tensor *k_cache,
+                                const fl_tensor *v_cache, const fl_tensor *out,
+                                const fl_tensor *lse, const fl_decode_desc *desc,
+                                fl_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif
