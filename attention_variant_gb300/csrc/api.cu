@@ -584,7 +584,7 @@ size_t align_up(size_t x) { return (x + kWsAlign - 1) / kWsAlign * kWsAlign; }
 struct DecodePlan {
     View Q, K, V;
     int64_t B, Sq, Hq, Hk, P, T;
-    int G, R, max_chunks;
+    int G, R, split_chunks, max_splits;
     size_t o_bytes, ml_bytes, cnt_bytes, total;
 };
 
@@ -642,8 +642,19 @@ fl_status decode_plan(const fl_tensor *q, const fl_tensor *k_cache, const fl_ten
         if (reinterpret_cast<uintptr_t>(d->block_table) % 4)
             return fail(FL_ERR_ALIGNMENT, "block_table is not 4-byte aligned");
     }
-    pl.max_chunks = (d->max_kv_len + fl::kDecodeChunk - 1) / fl::kDecodeChunk;
-    const size_t units = size_t(pl.B) * size_t(pl.Hk) * size_t(pl.max_chunks) * size_t(pl.R);
+    // Keys per CTA: the longest split (fewest partials to merge) that still
+    // leaves about 2048 CTAs for the longest sequences' work, so that the GPU
+    // stays full; a function of the shapes alone, so that the workspace query
+    // and the call agree.
+    const int64_t max_chunks = (d->max_kv_len + fl::kDecodeChunk - 1) / fl::kDecodeChunk;
+    pl.split_chunks = 1;
+    for (int sc = fl::kDecodeMaxSplitChunks; sc > 1; sc /= 2)
+        if (pl.B * pl.Hk * ((max_chunks + sc - 1) / sc) >= 2048) {
+            pl.split_chunks = sc;
+            break;
+        }
+    pl.max_splits = int((max_chunks + pl.split_chunks - 1) / pl.split_chunks);
+    const size_t units = size_t(pl.B) * size_t(pl.Hk) * size_t(pl.max_splits) * size_t(pl.R);
     pl.o_bytes = align_up(units * 64 * sizeof(float));
     pl.ml_bytes = align_up(units * 2 * sizeof(float));
     pl.cnt_bytes = align_up(size_t(pl.B) * size_t(pl.Hk) * sizeof(int));
@@ -691,7 +702,8 @@ fl_status decode_run(const DecodePlan &pl, const fl_tensor *out, const fl_tensor
     p.G = pl.G;
     p.Sq = int(pl.Sq);
     p.max_kv = d->max_kv_len;
-    p.max_chunks = pl.max_chunks;
+    p.split_chunks = pl.split_chunks;
+    p.max_splits = pl.max_splits;
     p.page = int(pl.T);
     p.bt_stride = d->block_table_stride;
     p.kv_lens = d->kv_lens;

@@ -75,12 +75,14 @@ struct EvoParams {
 };
 
 // ---- serving with a KV cache (fwd_decode.cu)
-constexpr int kDecodeChunk = 128; // keys per CTA (and per workspace partial)
+constexpr int kDecodeChunk = 128; // keys per pipeline stage
+constexpr int kDecodeMaxSplitChunks = 8; // chunks per CTA (split) at most
 constexpr int kDecodeMaxRows = 64; // G * Sq query rows per (sequence, KV head)
 
 struct DecodeParams {
     int B, Hk, G, Sq;
-    int max_kv, max_chunks;
+    int max_kv;
+    int split_chunks, max_splits; // chunks per split; splits of the longest sequence
     int page;                     // keys per page (paged cache)
     int64_t bt_stride;            // block_table row stride
     const int32_t *kv_lens;       // [B]
@@ -93,8 +95,8 @@ struct DecodeParams {
     int64_t l_sb, l_sh;
     float scale, softcap;         // softcap 0: none
     int causal;
-    float *ws_o;                  // [B][Hk][max_chunks][R][64]
-    float *ws_ml;                 // [B][Hk][max_chunks][R][2]
+    float *ws_o;                  // [B][Hk][max_splits][R][64]
+    float *ws_ml;                 // [B][Hk][max_splits][R][2]: base-2 max, sum
     int *ws_cnt;                  // [B][Hk], zero before the launch
     uint32_t *err_user;
     uint64_t timeout_ns;

@@ -214,8 +214,10 @@ typedef struct {
  *   out      [B, Sq, Hq, 64]
  *   lse      [B, Hq, Sq] fp32 (natural log) or NULL
  * Hq must be a multiple of Hk, and (Hq / Hk) * Sq <= 64.  The kernel splits
- * every sequence's keys into chunks of 128 and merges the chunks' partial
- * results through `workspace`: device memory of at least the size
+ * every sequence's keys into splits of 128, 256, 512 or 1024 keys (the
+ * longest that leaves B * Hk * splits-of-max_kv_len >= 2048, else 128) and
+ * merges the splits' partial results through `workspace`: device memory of
+ * at least the size
  * fl_attn_decode_workspace_size reports, 256-byte aligned, owned by the
  * caller; its contents need no initialisation (the call clears what must
  * start at zero).  Calls sharing one workspace must not overlap on the GPU.

@@ -127,13 +127,20 @@ def _ws_bytes(lib, q, kc, d):
     return st, n.value
 
 
-def test_decode_workspace_size(lib):
-    B, Sq, Hq, Hk, Smax = 3, 2, 8, 2, 1000
-    st, n = _ws_bytes(lib, _t((B, Sq, Hq, 64)), _t((B, Smax, Hk, 64)), _ddesc(max_kv=1000))
+@pytest.mark.parametrize("B,Sq,Hq,Hk,Smax,split_keys", [
+    (3, 2, 8, 2, 1000, 128),     # few sequences: the shortest splits
+    (64, 1, 32, 8, 8192, 1024),  # 512 (sequence, KV head) pairs x 8 splits of 1024 >= 2048
+    (16, 1, 32, 8, 8192, 512),   # 128 pairs x 8 splits of 1024 < 2048; x 16 of 512 = 2048
+    (4, 1, 32, 8, 8192, 128),    # 32 pairs x 64 splits of 128 = 2048
+])
+def test_decode_workspace_size(lib, B, Sq, Hq, Hk, Smax, split_keys):
+    # one fp32 partial (64 outputs, max, sum) per (sequence, KV head, split,
+    # query row) and one counter per (sequence, KV head), each 256-byte aligned
+    st, n = _ws_bytes(lib, _t((B, Sq, Hq, 64)), _t((B, Smax, Hk, 64)), _ddesc(max_kv=Smax))
     assert st == fa.FL_OK, fa.fl_attn_last_error()
-    R, chunks = (Hq // Hk) * Sq, -(-1000 // 128)
+    R, splits = (Hq // Hk) * Sq, -(-Smax // split_keys)
     up = lambda x: -(-x // 256) * 256
-    units = B * Hk * chunks * R
+    units = B * Hk * splits * R
     assert n == up(units * 64 * 4) + up(units * 2 * 4) + up(B * Hk * 4)
 
 

@@ -89,6 +89,17 @@ def test_contiguous_cache(Sq, mod, causal):
     gu.compare(o, lse, oref, lref, what=f"decode contiguous Sq={Sq} {mod} causal={causal}")
 
 
+@pytest.mark.parametrize("causal,lens", [(True, [100, 37, 1]), (False, [100, 37, 0])])
+def test_cache_shorter_than_one_chunk(causal, lens):
+    # the cache holds fewer keys than a chunk (a box of 100 rows), and an
+    # empty cache (no causal mask: a row with no key gives O = 0, LSE = -inf)
+    B, Sq, Hq, Hk, S = 3, 1, 8, 2, 100
+    q, k, v = _inputs(f"short{int(causal)}", B, Sq, Hq, Hk, S)
+    (o, lse), = _run(q, k, v, lens, S, causal=causal)
+    oref, lref = _ref(q, k, v, lens, "none", causal)
+    gu.compare(o, lse, oref, lref, what=f"decode short cache causal={causal}")
+
+
 @pytest.mark.parametrize("page", [16, 64, 256])
 def test_paged_cache(page):
     B, Sq, Hq, Hk = 4, 2, 8, 2
@@ -97,6 +108,31 @@ def test_paged_cache(page):
     (o, lse), = _run(q, kp, vp, lens, max(lens), table=table, mod="softcap")
     oref, lref = _ref(q, k, v, lens, "softcap", True)
     gu.compare(o, lse, oref, lref, what=f"decode paged page={page}")
+
+
+@pytest.mark.parametrize("Hq,Hk,Sq", [(32, 2, 2), (6, 2, 7), (16, 2, 5), (32, 2, 4)])
+def test_many_query_rows(Hq, Hk, Sq):
+    # G * Sq query rows per KV head: 32, 21, 40 and 64 (two to four groups
+    # of 16 rows, the last one ragged or empty)
+    B, S = 2, 450
+    q, k, v = _inputs(f"rows{Hq}_{Sq}", B, Sq, Hq, Hk, S)
+    lens = [450, 200]
+    for mod in ("none", "softcap"):
+        (o, lse), = _run(q, k, v, lens, S, mod=mod)
+        oref, lref = _ref(q, k, v, lens, mod, True)
+        gu.compare(o, lse, oref, lref, what=f"decode rows={Hq // Hk * Sq} {mod}")
+
+
+def test_splits_of_several_chunks():
+    # 256 sequences x 1 KV head with caches of up to 4096 keys: splits of 512
+    # keys (four chunks, so the three-stage ring wraps), ragged last splits
+    B, Sq, Hq, Hk, S = 256, 2, 4, 1, 4096
+    q, k, v = _inputs("splits", B, Sq, Hq, Hk, S)
+    lens = testdata.kv_lengths(B, "dec_splits", Sq, S)
+    for causal in (True, False):
+        (o, lse), = _run(q, k, v, lens, S, causal=causal)
+        oref, lref = _ref(q, k, v, lens, "none", causal)
+        gu.compare(o, lse, oref, lref, what=f"decode splits causal={causal}")
 
 
 def test_two_calls_share_one_workspace():
