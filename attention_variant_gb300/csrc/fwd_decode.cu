@@ -52,6 +52,8 @@ constexpr int kThreads = 32 * (kConsumerWarps + 1); // + the producer warp
 constexpr int kStages = 3;
 constexpr uint32_t kKVBytes = kDecodeChunk * 64 * 2; // one chunk of K (or V), 16 KB
 constexpr uint32_t kStageBytes = 2 * kKVBytes;
+// block-table entries one split touches at most (pages of 16 keys)
+constexpr int kSplitPages = kDecodeMaxSplitChunks * kDecodeChunk / 16;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 
@@ -95,11 +97,13 @@ __device__ __forceinline__ uint32_t bf16_bits(const __nv_bfloat16 &x)
 }
 
 // Thread 0 of the producer: start the loads of chunk c of (b, hk) into stage
-// (sk, sv), completing on `bar`.  A box is always written whole (rows past the
+// (sk, sv), completing on `bar`.  `pages` holds the block-table entries of the
+// split from page `pg_first` on.  A box is always written whole (rows past the
 // tensor's end are zero-filled), so the expected bytes count whole boxes.
 __device__ __forceinline__ void issue_chunk(const DecodeParams &p, const CUtensorMap *tm_k,
                                             const CUtensorMap *tm_v, int b, int hk, int c, int L,
-                                            uint32_t sk, uint32_t sv, uint32_t bar)
+                                            const int *pages, int pg_first, uint32_t sk, uint32_t sv,
+                                            uint32_t bar)
 {
     const int k0 = c * kDecodeChunk;
     if (!p.block_table) {
@@ -110,7 +114,7 @@ __device__ __forceinline__ void issue_chunk(const DecodeParams &p, const CUtenso
         ptx::tma_load_4d(sv, tm_v, bar, 0, k0, hk, b);
     } else if (p.page >= kDecodeChunk) {
         // the chunk is a slice of one page
-        const int page = __ldg(p.block_table + static_cast<int64_t>(b) * p.bt_stride + k0 / p.page);
+        const int page = pages[k0 / p.page - pg_first];
         ptx::mbar_arrive_expect_tx(bar, 2 * kKVBytes);
         ptx::tma_load_4d(sk, tm_k, bar, 0, k0 % p.page, hk, page);
         ptx::tma_load_4d(sv, tm_v, bar, 0, k0 % p.page, hk, page);
@@ -120,7 +124,7 @@ __device__ __forceinline__ void issue_chunk(const DecodeParams &p, const CUtenso
         const uint32_t pbytes = static_cast<uint32_t>(p.page) * 128u;
         ptx::mbar_arrive_expect_tx(bar, 2u * pbytes * static_cast<uint32_t>(npg));
         for (int g = 0; g < npg; ++g) {
-            const int page = __ldg(p.block_table + static_cast<int64_t>(b) * p.bt_stride + pg0 + g);
+            const int page = pages[pg0 + g - pg_first];
             ptx::tma_load_4d(sk + g * pbytes, tm_k, bar, 0, 0, hk, page);
             ptx::tma_load_4d(sv + g * pbytes, tm_v, bar, 0, 0, hk, page);
         }
@@ -177,6 +181,7 @@ __global__ void __launch_bounds__(kThreads, 2)
     uint64_t *empty = full + kStages;
     int *s_ticket = reinterpret_cast<int *>(empty + kStages);
     volatile uint32_t *s_abort = reinterpret_cast<volatile uint32_t *>(s_ticket + 1);
+    int *s_pages = s_ticket + 2; // [kSplitPages] block-table entries of the split
 
     if (tid == 0) {
         for (int s = 0; s < kStages; ++s) {
@@ -212,7 +217,15 @@ __global__ void __launch_bounds__(kThreads, 2)
         o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.f;
 
     if (warp == kConsumerWarps) {
-        // ---- producer
+        // ---- producer: the split's block-table entries first (one load per
+        // lane instead of one dependent load before every chunk's copies)
+        const int pg_first = p.block_table ? c_lo * kDecodeChunk / p.page : 0;
+        if (p.block_table) {
+            const int pg_last = (min(L, (c_lo + n_ch) * kDecodeChunk) - 1) / p.page;
+            for (int e = lane; e <= pg_last - pg_first; e += 32)
+                s_pages[e] = __ldg(p.block_table + static_cast<int64_t>(b) * p.bt_stride + pg_first + e);
+            __syncwarp();
+        }
         if (lane == 0)
             for (int i = 0; i < n_ch; ++i) {
                 const int s = i % kStages;
@@ -221,8 +234,9 @@ __global__ void __launch_bounds__(kThreads, 2)
                     ok = false;
                     break;
                 }
-                issue_chunk(p, &tm_k, &tm_v, b, hk, c_lo + i, L, s_stage + s * kStageBytes,
-                            s_stage + s * kStageBytes + kKVBytes, ptx::smem_u32(&full[s]));
+                issue_chunk(p, &tm_k, &tm_v, b, hk, c_lo + i, L, s_pages, pg_first,
+                            s_stage + s * kStageBytes, s_stage + s * kStageBytes + kKVBytes,
+                            ptx::smem_u32(&full[s]));
                 issued = i + 1;
             }
     } else {
@@ -522,8 +536,8 @@ size_t decode_smem_bytes(int)
 {
     // the stages (reused at the end for the warps' partials: at most 4 x 16
     // rows x 66 floats, 17 KB), the barriers, the ticket and the abort flag,
-    // and up to 1 KB of alignment padding
-    return kStages * static_cast<size_t>(kStageBytes) + 2 * kStages * 8 + 8 + 1024;
+    // the split's block-table entries, and up to 1 KB of alignment padding
+    return kStages * static_cast<size_t>(kStageBytes) + 2 * kStages * 8 + 8 + kSplitPages * 4 + 1024;
 }
 
 cudaError_t launch_decode(const CUtensorMap &tk, const CUtensorMap &tv, const DecodeParams &p,
