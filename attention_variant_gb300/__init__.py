@@ -39,6 +39,7 @@ FL_KIND_EVO_COL = 3
 FL_MOD_NONE = 0
 FL_MOD_ALIBI = 1
 FL_MOD_SOFTCAP = 2
+FL_MOD_EXPR = 3
 # fl_mask
 FL_MASK_NONE = 0
 FL_MASK_CAUSAL = 1
@@ -51,7 +52,7 @@ FL_INJECT_DROP_KV_LOAD = 1
 FL_DEVERR_TIMEOUT = 0x1
 
 MODS = {"none": FL_MOD_NONE, "vanilla": FL_MOD_NONE, "alibi": FL_MOD_ALIBI,
-        "softcap": FL_MOD_SOFTCAP}
+        "softcap": FL_MOD_SOFTCAP, "expr": FL_MOD_EXPR}
 MASKS = {"none": FL_MASK_NONE, "causal": FL_MASK_CAUSAL, "window": FL_MASK_WINDOW,
          "prefix": FL_MASK_PREFIX, "doc": FL_MASK_DOC}
 KINDS = {"standard": FL_KIND_STANDARD, "diff": FL_KIND_DIFF, "evo_row": FL_KIND_EVO_ROW,
@@ -71,7 +72,7 @@ class FlDesc(ctypes.Structure):
         ("gqa_group", ctypes.c_int32), ("diff_lambda", ctypes.c_float), ("scale", ctypes.c_float),
         ("alibi_slopes", ctypes.c_void_p), ("debug_tile_counts", ctypes.c_void_p),
         ("error_word", ctypes.c_void_p), ("debug_inject", ctypes.c_int32),
-        ("wait_timeout_us", ctypes.c_uint32),
+        ("wait_timeout_us", ctypes.c_uint32), ("score_mod_expr", ctypes.c_char_p),
     ]
 
 
@@ -115,6 +116,8 @@ def load_library(path: str = LIB_PATH):
     lib.fl_attn_last_error.restype = ctypes.c_char_p
     lib.fl_attn_last_error.argtypes = []
     lib.fl_attn_version.restype = ctypes.c_int32
+    lib.fl_attn_score_expr_check.restype = ctypes.c_int
+    lib.fl_attn_score_expr_check.argtypes = [ctypes.c_char_p, ctypes.c_int32]
     lib.fl_attn_decode_workspace_size.restype = ctypes.c_int
     lib.fl_attn_decode_workspace_size.argtypes = [P(FlTensor), P(FlTensor), P(FlDecodeDesc),
                                                   P(ctypes.c_size_t)]
@@ -155,9 +158,14 @@ def as_fl_tensor(t) -> FlTensor | None:
 def make_desc(kind="standard", score_mod="none", softcap=20.0, mask="none", window=0, prefix=0,
               doc_offsets=None, gqa_group=0, diff_lambda=0.0, scale=0.0, alibi_slopes=None,
               debug_tile_counts=None, error_word=None, debug_inject=0,
-              wait_timeout_us=0) -> FlDesc:
-    """Build an fl_attn_variant_desc; tensor arguments are device torch tensors."""
+              wait_timeout_us=0, score_expr=None) -> FlDesc:
+    """Build an fl_attn_variant_desc; tensor arguments are device torch tensors.
+    ``score_expr`` (a string in the grammar of include/fl_attn.h) selects
+    FL_MOD_EXPR."""
     d = FlDesc()
+    if score_expr is not None:
+        score_mod = "expr"
+        d.score_mod_expr = score_expr.encode()
     d.kind = KINDS[kind] if isinstance(kind, str) else int(kind)
     d.score_mod = MODS[score_mod] if isinstance(score_mod, str) else int(score_mod)
     d.softcap = float(softcap)
@@ -180,6 +188,15 @@ def make_desc(kind="standard", score_mod="none", softcap=20.0, mask="none", wind
 
 def _ref(x):
     return ctypes.byref(x) if x is not None else None
+
+
+def fl_attn_score_expr_check(expr: str, compile: bool = False) -> None:
+    """Check a score_mod expression against the grammar (and, with ``compile``,
+    run its runtime compilation, which needs no GPU); raises FlAttnError."""
+    lib = load_library()
+    st = lib.fl_attn_score_expr_check(expr.encode(), int(bool(compile)))
+    if st != FL_OK:
+        raise FlAttnError(st, fl_attn_last_error())
 
 
 def fl_attn_fwd(q, k, v, out, lse=None, desc: FlDesc | None = None, bias=None, gate=None,

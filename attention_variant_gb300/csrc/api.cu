@@ -19,7 +19,11 @@
 
 namespace {
 
-thread_local char g_last_error[512];
+thread_local char g_last_error[2048];
+
+// Room for a translated score_mod expression (the grammar caps the source at
+// 4096 characters; the translation adds parentheses and helper names).
+constexpr size_t kExprCudaMax = 16384;
 
 fl_status fail(fl_status s, const char *fmt, ...)
 {
@@ -248,10 +252,16 @@ fl_status fwd_standard(const fl_tensor *q, const fl_tensor *k, const fl_tensor *
             return fail(FL_ERR_INVALID_ARG, "lse must be [B, Hq, S]");
     }
     if ((s = check_mask(d)) != FL_OK) return s;
-    if (d->score_mod < FL_MOD_NONE || d->score_mod > FL_MOD_SOFTCAP)
+    if (d->score_mod < FL_MOD_NONE || d->score_mod > FL_MOD_EXPR)
         return fail(FL_ERR_INVALID_ARG, "unknown score_mod %d", d->score_mod);
     if (d->score_mod == FL_MOD_SOFTCAP && !(d->softcap > 0.f && std::isfinite(d->softcap)))
         return fail(FL_ERR_INVALID_ARG, "softcap must be positive and finite");
+    char expr_cuda[kExprCudaMax];
+    if (d->score_mod == FL_MOD_EXPR) {
+        char err[256];
+        if (!fl::score_expr_translate(d->score_mod_expr, expr_cuda, sizeof expr_cuda, err, sizeof err))
+            return fail(FL_ERR_INVALID_ARG, "score_mod_expr: %s", err);
+    }
     if (!std::isfinite(d->scale) || d->scale < 0.f)
         return fail(FL_ERR_INVALID_ARG, "scale must be finite and positive (0 selects 1/sqrt(D))");
     if (d->mask == FL_MASK_DOC && d->doc_stride < 2)
@@ -317,6 +327,7 @@ fl_status fwd_standard(const fl_tensor *q, const fl_tensor *k, const fl_tensor *
     const float scale = d->scale != 0.f ? d->scale : 1.0f / std::sqrt(float(D));
     const float log2e = 1.4426950408889634f;
     p.qk_log2 = scale * log2e;
+    p.scale = scale;
     if (d->score_mod == FL_MOD_SOFTCAP) {
         p.softcap_in = 2.f * scale * log2e / d->softcap;
         p.softcap_out = d->softcap * log2e;
@@ -338,6 +349,19 @@ fl_status fwd_standard(const fl_tensor *q, const fl_tensor *k, const fl_tensor *
     p.timeout_ns = timeout_ns(d);
 
     const int grid = int(p.grid.n_items < info.sm_count ? p.grid.n_items : info.sm_count);
+    if (d->score_mod == FL_MOD_EXPR) {
+        char err[1024] = "";
+        const cudaError_t e = fl::launch_standard_expr(tq, tk, tv, p, grid, stream, expr_cuda, err,
+                                                       sizeof err);
+        if (e == cudaErrorInvalidSource)
+            return fail(FL_ERR_INVALID_ARG, "score_mod_expr: %s", err);
+        if (e == cudaErrorNotSupported)
+            return fail(FL_ERR_UNSUPPORTED, "score_mod_expr: %s", err);
+        if (e != cudaSuccess)
+            return fail(FL_ERR_CUDA, "score_mod_expr kernel: %s%s%s", cudaGetErrorString(e),
+                        err[0] ? ": " : "", err);
+        return ok();
+    }
     cudaError_t e = fl::launch_standard(tq, tk, tv, p, grid, stream);
     if (e != cudaSuccess)
         return fail(FL_ERR_CUDA, "kernel launch failed: %s", cudaGetErrorString(e));
@@ -744,6 +768,17 @@ fl_status decode_run(const DecodePlan &pl, const fl_tensor *out, const fl_tensor
 } // namespace
 
 extern "C" {
+
+fl_status fl_attn_score_expr_check(const char *expr, int32_t compile)
+{
+    char cuda[kExprCudaMax], err[1024];
+    if (!fl::score_expr_translate(expr, cuda, sizeof cuda, err, sizeof err))
+        return fail(FL_ERR_INVALID_ARG, "score_mod_expr: %s", err);
+    if (compile && !fl::score_expr_compile_only(cuda, err, sizeof err))
+        return fail(strstr(err, "not found") ? FL_ERR_UNSUPPORTED : FL_ERR_INVALID_ARG,
+                    "score_mod_expr: %s", err);
+    return ok();
+}
 
 // No workspace argument: the scratch is the library's own static device
 // array (fl::decode_static_scratch), looked up on the first call per device.

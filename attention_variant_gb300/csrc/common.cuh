@@ -3,8 +3,7 @@
 // bounded mbarrier waits every role uses.
 #pragma once
 
-#include <cstdint>
-#include <cuda.h>
+#include "rtc_compat.cuh"
 
 #include "ptx.cuh"
 
@@ -15,9 +14,10 @@ constexpr int BN = 128; // keys per KV tile
 
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
-constexpr float kNegInf = -__builtin_huge_valf();
+constexpr float kNegInf = -__builtin_bit_cast(float, 0x7f800000u); // -infinity
 
-enum : int { MOD_NONE = 0, MOD_ALIBI = 1, MOD_SOFTCAP = 2 };
+// MOD_EXPR: a score_mod expression compiled into the kernel at run time
+enum : int { MOD_NONE = 0, MOD_ALIBI = 1, MOD_SOFTCAP = 2, MOD_EXPR = 3 };
 enum : int { MASK_NONE = 0, MASK_CAUSAL = 1, MASK_WINDOW = 2, MASK_PREFIX = 3, MASK_DOC = 4 };
 
 // ---------------------------------------------------------------- masks

@@ -275,7 +275,9 @@ __global__ void __launch_bounds__(kThreads, 2)
         const int lim_b = p.causal ? min(L - 1, L - p.Sq + r_b / p.G) : L - 1;
         const float sl2 = p.scale * kLog2e;
         const bool capped = p.softcap > 0.f;
-        const float cap_in = capped ? p.scale / p.softcap : 0.f, cap_out = p.softcap * kLog2e;
+        // cap * tanh(u), u = scale * z / cap, as cap (1 - 2 / (1 + e^(2u))), in log2 units
+        const float cap_in = capped ? 2.f * p.scale * kLog2e / p.softcap : 0.f;
+        const float cap_out = p.softcap * kLog2e;
 
         for (int i = 0; i < n_ch; ++i) {
             const int s = i % kStages;
@@ -310,7 +312,8 @@ __global__ void __launch_bounds__(kThreads, 2)
                 for (int n = 0; n < 4; ++n)
 #pragma unroll
                     for (int e = 0; e < 4; ++e)
-                        sc[n][e] = capped ? cap_out * tanhf(sc[n][e] * cap_in) : sc[n][e] * sl2;
+                        sc[n][e] = capped ? cap_out * (1.f - 2.f * ptx::rcp_approx(1.f + ptx::ex2(sc[n][e] * cap_in)))
+                                          : sc[n][e] * sl2;
                 if (k0 + kb + 31 > lim_all) {
                     // keys past the cache or the causal limit of a row
 #pragma unroll

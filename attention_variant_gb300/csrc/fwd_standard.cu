@@ -44,7 +44,6 @@
 // double-buffered across work items so the next item's Q arrives while the
 // current one finishes.
 #include <cuda_bf16.h>
-#include <cstdint>
 
 #include "common.cuh"
 #include "launch.h"
@@ -53,8 +52,8 @@
 namespace fl {
 namespace {
 
-constexpr int kThreads = 384;
-constexpr uint32_t kRegsLaunch = 168;
+constexpr int kThreads = kStdThreads;
+constexpr uint32_t kRegsLaunch = kStdRegs;
 constexpr uint32_t kRegsSoftmax = 200;
 constexpr uint32_t kRegsOther = 104;
 static_assert(2 * 128 * kRegsSoftmax + 128 * kRegsOther == kThreads * kRegsLaunch,
@@ -453,6 +452,9 @@ __device__ void softmax_role(const KernelCtx &cx, const StdParams &p, int t)
         smod.softcap_in = p.softcap_in;
         smod.softcap_out = p.softcap_out;
         smod.alibi_c = 0.f;
+        smod.scale = p.scale;
+        smod.b = static_cast<float>(b);
+        smod.h = static_cast<float>(h);
         if constexpr (MOD == MOD_ALIBI) {
             if (mine) {
                 const float slope = p.alibi_slopes
@@ -663,6 +665,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 }
 
+#ifndef __CUDACC_RTC__
 template <int MOD>
 cudaError_t launch_mod(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
                        const StdParams &p, int grid, cudaStream_t stream)
@@ -686,9 +689,11 @@ cudaError_t launch_mod(const CUtensorMap &tq, const CUtensorMap &tk, const CUten
     std_fwd_kernel<MOD><<<grid, kThreads, smem, stream>>>(tq, tk, tv, p);
     return cudaGetLastError();
 }
+#endif // !__CUDACC_RTC__
 
 } // namespace
 
+#ifndef __CUDACC_RTC__
 cudaError_t launch_standard(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
                             const StdParams &p, int grid, cudaStream_t stream)
 {
@@ -703,5 +708,6 @@ cudaError_t launch_standard(const CUtensorMap &tq, const CUtensorMap &tk, const 
 }
 
 size_t standard_smem_bytes() { return sizeof(StdSmem) + 1024; }
+#endif // !__CUDACC_RTC__
 
 } // namespace fl

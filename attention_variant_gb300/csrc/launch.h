@@ -1,12 +1,13 @@
 // launch.h -- host-side interface between the C-ABI layer (api.cu) and the
-// kernel translation units.  Internal to the library; every file including it
-// is compiled by nvcc.
+// kernel translation units.  Internal to the library.  Under the runtime
+// compiler (NVRTC) only the parameter structs are seen.
 #pragma once
 
-#include <cuda.h>
 #include <cuda_bf16.h>
+#ifndef __CUDACC_RTC__
+#include <cuda.h>
 #include <cuda_runtime.h>
-#include <cstdint>
+#endif
 
 #include "common.cuh"
 
@@ -20,6 +21,7 @@ struct StdParams {
     float qk_log2;        // scale * log2(e)
     float softcap_in;     // 2 * scale * log2(e) / cap
     float softcap_out;    // cap * log2(e)
+    float scale;          // scale (the `score` of a score_mod expression is scale * q.k)
     const float *alibi_slopes;
     float alibi_exp_coef; // default slopes: 2^(alibi_exp_coef * (h + 1)), coef = -8 / Hq
     __nv_bfloat16 *out;
@@ -49,8 +51,10 @@ struct DiffParams {
     uint64_t timeout_ns;
 };
 
+#ifndef __CUDACC_RTC__
 cudaError_t launch_diff(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
                         const DiffParams &p, int grid, cudaStream_t stream);
+#endif
 
 // Parameters of the Evoformer kernel (c = 32) over a [batch, sequence, head, c]
 // view: row pass batch = MSA row, sequence = residue; column pass the reverse.
@@ -102,6 +106,7 @@ struct DecodeParams {
     uint64_t timeout_ns;
 };
 
+#ifndef __CUDACC_RTC__
 cudaError_t launch_decode(const CUtensorMap &tk, const CUtensorMap &tv, const DecodeParams &p,
                           cudaStream_t stream);
 size_t decode_smem_bytes(int R);
@@ -113,12 +118,34 @@ cudaError_t decode_static_scratch(void **ptr);
 cudaError_t launch_evo(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
                        const CUtensorMap &tb, const EvoParams &p, int grid, cudaStream_t stream);
 int evo_max_bias_keys();
+#endif
 
-// Keys per K/V tile of the standard kernel (its TMEM budget: see fwd_standard.cu).
+// Keys per K/V tile of the standard kernel (its TMEM budget: see fwd_standard.cu),
+// its threads per CTA and the registers per thread it must be compiled to.
 constexpr int kStdKeyTile = 112;
+constexpr int kStdThreads = 384;
+constexpr int kStdRegs = 168;
 
+#ifndef __CUDACC_RTC__
 cudaError_t launch_standard(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
                             const StdParams &p, int grid, cudaStream_t stream);
 size_t standard_smem_bytes();
+
+// ---- score_mod expressions (score_expr.cu)
+// Checks `expr` against the expression grammar of fl_attn.h and writes the
+// equivalent fp32 CUDA expression to `cuda` (NUL-terminated, at most `n`
+// bytes); false with a message in `err` otherwise.
+bool score_expr_translate(const char *expr, char *cuda, size_t n, char *err, size_t err_n);
+// Runs the runtime compilation of the standard kernel for the translated
+// expression `cuda` without loading it (needs no device).
+bool score_expr_compile_only(const char *cuda, char *err, size_t err_n);
+// The standard kernel specialised for the translated expression `cuda`:
+// compiled at run time on first use (per device and expression), then
+// launched like launch_standard.  Errors other than CUDA ones are described
+// in `err`.
+cudaError_t launch_standard_expr(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
+                                 const StdParams &p, int grid, cudaStream_t stream, const char *cuda,
+                                 char *err, size_t err_n);
+#endif
 
 }  // namespace fl

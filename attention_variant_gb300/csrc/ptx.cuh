@@ -5,7 +5,7 @@
 // wait,fence}).  Shared-memory operands are 32-bit shared-window addresses.
 #pragma once
 
-#include <cstdint>
+#include "rtc_compat.cuh"
 
 namespace fl {
 namespace ptx {

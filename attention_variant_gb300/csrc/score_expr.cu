@@ -1,0 +1,571 @@
+// score_expr.cu -- score_mod expressions compiled into the fused kernel at
+// run time.
+//
+// The Flashlight pages' central point is that an attention variant written as
+// a plain elementwise expression over the score and its indices is fused into
+// the same single-pass kernel as the built-in variants, with no per-variant
+// template written by hand (talk notes, "Compiler design" 1-4 and the
+// comparison with FlexAttention's score_mod/mask_mod interface; gist.science
+// summary, "Methodology").  Here the expression is a string in a small grammar
+// (fl_attn.h, FL_MOD_EXPR).  The library
+//   1. parses it and writes the equivalent fp32 CUDA expression
+//      (score_expr_translate): numbers become float literals, names map to
+//      fixed helper functions, anything outside the grammar is refused, so
+//      what is compiled is exactly what the grammar means;
+//   2. on the first use of an expression on a device, compiles the standard
+//      kernel's own source (embedded in the library at build time) with that
+//      expression as its score_mod using NVRTC, for sm_103a, into a cubin;
+//   3. loads the cubin into the current context and launches it exactly like
+//      the built-in standard kernel (same parameters, same tensor maps).
+// NVRTC is loaded on first use (dlopen), so the library has no link-time
+// dependency on it; without it FL_MOD_EXPR returns FL_ERR_UNSUPPORTED.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+#include <dlfcn.h>
+
+#include <cstdarg>
+#include <cstdio>
+#include <cstdlib>
+#include <cstring>
+#include <map>
+#include <mutex>
+#include <string>
+#include <type_traits>
+#include <vector>
+
+#include "launch.h"
+#include "jit_sources.inc" // kJitSources: {file name, text} of the kernel sources
+
+namespace fl {
+namespace {
+
+void put(char *dst, size_t n, const char *fmt, ...)
+{
+    if (!dst || n == 0)
+        return;
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(dst, n, fmt, ap);
+    va_end(ap);
+}
+
+// ------------------------------------------------------------------ grammar
+//
+//   expr    := sum [ relop sum ]          relop: < <= > >= == !=  (no chaining)
+//   sum     := term { (+|-) term }
+//   term    := unary { (*|/) unary }
+//   unary   := (-|+) unary | primary
+//   primary := number | variable | inf | func ( expr {, expr} ) | ( expr )
+//   variable: score b h q_idx kv_idx      func: see kFuncs
+// A comparison yields 1 or 0.  Every value is fp32.
+
+struct Func {
+    const char *name;
+    int arity;
+};
+constexpr Func kFuncs[] = {{"tanh", 1}, {"exp", 1},  {"exp2", 1}, {"log", 1},
+                           {"log2", 1}, {"sqrt", 1}, {"abs", 1},  {"floor", 1},
+                           {"min", 2},  {"max", 2},  {"where", 3}};
+constexpr const char *kVars[] = {"score", "b", "h", "q_idx", "kv_idx"};
+constexpr int kMaxDepth = 64;
+constexpr size_t kMaxLen = 4096;
+
+class Translator {
+  public:
+    explicit Translator(const char *src) : s_(src) {}
+
+    bool run(std::string &out, std::string &err)
+    {
+        if (strlen(s_) > kMaxLen) {
+            err = "expression longer than 4096 characters";
+            return false;
+        }
+        std::string o;
+        if (expr(o)) {
+            skip();
+            if (s_[i_] == '\0') {
+                out = o;
+                return true;
+            }
+            fail("unexpected character");
+        }
+        err = err_;
+        return false;
+    }
+
+  private:
+    const char *s_;
+    size_t i_ = 0;
+    int depth_ = 0;
+    std::string err_;
+
+    void skip()
+    {
+        while (s_[i_] == ' ' || s_[i_] == '\t' || s_[i_] == '\n' || s_[i_] == '\r')
+            ++i_;
+    }
+    bool fail(const char *what)
+    {
+        if (err_.empty()) {
+            char buf[160];
+            snprintf(buf, sizeof buf, "%s at offset %zu", what, i_);
+            err_ = buf;
+        }
+        return false;
+    }
+    static bool is_alpha(char c) { return (c >= 'a' && c <= 'z') || (c >= 'A' && c <= 'Z') || c == '_'; }
+    static bool is_digit(char c) { return c >= '0' && c <= '9'; }
+
+    // which relational operator starts at i_ (0 if none)
+    const char *relop() const
+    {
+        static const char *ops[] = {"<=", ">=", "==", "!=", "<", ">"};
+        for (const char *op : ops)
+            if (strncmp(s_ + i_, op, strlen(op)) == 0)
+                return op;
+        return nullptr;
+    }
+
+    bool expr(std::string &o)
+    {
+        if (++depth_ > kMaxDepth)
+            return fail("expression nested too deeply");
+        std::string a;
+        if (!sum(a))
+            return false;
+        skip();
+        if (const char *op = relop()) {
+            i_ += strlen(op);
+            std::string b;
+            if (!sum(b))
+                return false;
+            skip();
+            if (relop())
+                return fail("comparisons do not chain (parenthesise one side)");
+            o = "fl_x_bool(" + a + " " + op + " " + b + ")";
+        } else {
+            o = a;
+        }
+        --depth_;
+        return true;
+    }
+
+    bool sum(std::string &o)
+    {
+        if (!term(o))
+            return false;
+        for (;;) {
+            skip();
+            const char c = s_[i_];
+            if (c != '+' && c != '-')
+                return true;
+            ++i_;
+            std::string b;
+            if (!term(b))
+                return false;
+            o = "(" + o + " " + c + " " + b + ")";
+        }
+    }
+
+    bool term(std::string &o)
+    {
+        if (!unary(o))
+            return false;
+        for (;;) {
+            skip();
+            const char c = s_[i_];
+            if (c != '*' && c != '/')
+                return true;
+            if (s_[i_ + 1] == '*' || s_[i_ + 1] == '/')
+                return fail("'**', '//' and comments are not part of the grammar");
+            ++i_;
+            std::string b;
+            if (!unary(b))
+                return false;
+            o = "(" + o + " " + c + " " + b + ")";
+        }
+    }
+
+    bool unary(std::string &o)
+    {
+        skip();
+        const char c = s_[i_];
+        if (c == '-' || c == '+') {
+            ++i_;
+            if (++depth_ > kMaxDepth)
+                return fail("expression nested too deeply");
+            std::string a;
+            if (!unary(a))
+                return false;
+            --depth_;
+            o = std::string("(") + c + a + ")";
+            return true;
+        }
+        return primary(o);
+    }
+
+    bool number(std::string &o)
+    {
+        const size_t start = i_;
+        bool dot = false, exp = false;
+        while (is_digit(s_[i_]))
+            ++i_;
+        if (s_[i_] == '.') {
+            dot = true;
+            ++i_;
+            while (is_digit(s_[i_]))
+                ++i_;
+        }
+        if (i_ == start + (dot ? 1 : 0))
+            return fail("malformed number");
+        if (s_[i_] == 'e' || s_[i_] == 'E') {
+            exp = true;
+            ++i_;
+            if (s_[i_] == '+' || s_[i_] == '-')
+                ++i_;
+            if (!is_digit(s_[i_]))
+                return fail("malformed exponent");
+            while (is_digit(s_[i_]))
+                ++i_;
+        }
+        if (is_alpha(s_[i_]) || s_[i_] == '.')
+            return fail("malformed number");
+        o.assign(s_ + start, i_ - start);
+        if (!dot && !exp)
+            o += ".0";
+        else if (o.back() == '.')
+            o += "0";
+        o = "(" + o + "f)";
+        return true;
+    }
+
+    bool primary(std::string &o)
+    {
+        skip();
+        const char c = s_[i_];
+        if (is_digit(c) || (c == '.' && is_digit(s_[i_ + 1])))
+            return number(o);
+        if (c == '(') {
+            ++i_;
+            std::string a;
+            if (!expr(a))
+                return false;
+            skip();
+            if (s_[i_] != ')')
+                return fail("expected ')'");
+            ++i_;
+            o = "(" + a + ")";
+            return true;
+        }
+        if (!is_alpha(c))
+            return fail(c ? "unexpected character" : "unexpected end of expression");
+        const size_t start = i_;
+        while (is_alpha(s_[i_]) || is_digit(s_[i_]))
+            ++i_;
+        const std::string name(s_ + start, i_ - start);
+        for (const char *v : kVars)
+            if (name == v) {
+                o = name;
+                return true;
+            }
+        if (name == "inf") {
+            o = "fl_x_inf()";
+            return true;
+        }
+        for (const Func &f : kFuncs) {
+            if (name != f.name)
+                continue;
+            skip();
+            if (s_[i_] != '(')
+                return fail("expected '(' after a function name");
+            ++i_;
+            o = std::string("fl_x_") + f.name + "(";
+            for (int a = 0; a < f.arity; ++a) {
+                std::string arg;
+                if (!expr(arg))
+                    return false;
+                skip();
+                if (s_[i_] != (a + 1 < f.arity ? ',' : ')'))
+                    return fail(a + 1 < f.arity ? "expected ',' (too few arguments)"
+                                                : "expected ')' (too many arguments)");
+                ++i_;
+                o += arg + (a + 1 < f.arity ? ", " : ")");
+            }
+            return true;
+        }
+        i_ = start;
+        return fail("unknown name");
+    }
+};
+
+// ------------------------------------------------------------------ NVRTC
+
+typedef int nvrtcResult_t;
+typedef struct _nvrtcProgram *nvrtcProgram_t;
+struct Nvrtc {
+    nvrtcResult_t (*create)(nvrtcProgram_t *, const char *, const char *, int, const char *const *,
+                            const char *const *);
+    nvrtcResult_t (*destroy)(nvrtcProgram_t *);
+    nvrtcResult_t (*compile)(nvrtcProgram_t, int, const char *const *);
+    nvrtcResult_t (*log_size)(nvrtcProgram_t, size_t *);
+    nvrtcResult_t (*log)(nvrtcProgram_t, char *);
+    nvrtcResult_t (*cubin_size)(nvrtcProgram_t, size_t *);
+    nvrtcResult_t (*cubin)(nvrtcProgram_t, char *);
+    nvrtcResult_t (*add_name)(nvrtcProgram_t, const char *);
+    nvrtcResult_t (*lowered)(nvrtcProgram_t, const char *, const char **);
+    bool ok = false;
+};
+
+std::string cuda_home()
+{
+    for (const char *v : {"CUDA_HOME", "CUDA_PATH"})
+        if (const char *e = getenv(v))
+            if (*e)
+                return e;
+    return "/usr/local/cuda";
+}
+
+const Nvrtc &nvrtc()
+{
+    static Nvrtc n;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        const std::string home = cuda_home();
+        const std::string cands[] = {"libnvrtc.so.13", home + "/lib64/libnvrtc.so.13",
+                                     home + "/lib64/libnvrtc.so", "libnvrtc.so"};
+        void *h = nullptr;
+        for (const std::string &c : cands)
+            if ((h = dlopen(c.c_str(), RTLD_NOW | RTLD_LOCAL)))
+                break;
+        if (!h)
+            return;
+        bool all = true;
+        auto sym = [&](auto &fn, const char *name) {
+            fn = reinterpret_cast<std::remove_reference_t<decltype(fn)>>(dlsym(h, name));
+            all = all && fn;
+        };
+        sym(n.create, "nvrtcCreateProgram");
+        sym(n.destroy, "nvrtcDestroyProgram");
+        sym(n.compile, "nvrtcCompileProgram");
+        sym(n.log_size, "nvrtcGetProgramLogSize");
+        sym(n.log, "nvrtcGetProgramLog");
+        sym(n.cubin_size, "nvrtcGetCUBINSize");
+        sym(n.cubin, "nvrtcGetCUBIN");
+        sym(n.add_name, "nvrtcAddNameExpression");
+        sym(n.lowered, "nvrtcGetLoweredName");
+        n.ok = all;
+    });
+    return n;
+}
+
+// The helpers every translated expression calls, then the expression as the
+// score_mod the kernel source applies when FL_SCORE_EXPR is defined.
+std::string program_source(const std::string &cuda)
+{
+    return "#define FL_SCORE_EXPR 1\n"
+           "__device__ __forceinline__ float fl_x_bool(bool c) { return c ? 1.f : 0.f; }\n"
+           "__device__ __forceinline__ float fl_x_inf() { return __int_as_float(0x7f800000); }\n"
+           // tanh(x) = 1 - 2 / (1 + e^(2x)) on the fast exponential and
+           // division (absolute error ~1e-7; +-1 at the extremes)
+           "__device__ __forceinline__ float fl_x_tanh(float x)\n"
+           "{ return 1.f - __fdividef(2.f, 1.f + exp2f(x * 2.8853900817779268f)); }\n"
+           "__device__ __forceinline__ float fl_x_exp(float x) { return expf(x); }\n"
+           "__device__ __forceinline__ float fl_x_exp2(float x) { return exp2f(x); }\n"
+           "__device__ __forceinline__ float fl_x_log(float x) { return logf(x); }\n"
+           "__device__ __forceinline__ float fl_x_log2(float x) { return log2f(x); }\n"
+           "__device__ __forceinline__ float fl_x_sqrt(float x) { return sqrtf(x); }\n"
+           "__device__ __forceinline__ float fl_x_abs(float x) { return fabsf(x); }\n"
+           "__device__ __forceinline__ float fl_x_floor(float x) { return floorf(x); }\n"
+           "__device__ __forceinline__ float fl_x_min(float x, float y) { return fminf(x, y); }\n"
+           "__device__ __forceinline__ float fl_x_max(float x, float y) { return fmaxf(x, y); }\n"
+           "__device__ __forceinline__ float fl_x_where(float c, float x, float y) { return c != 0.f ? x : y; }\n"
+           "__device__ __forceinline__ float fl_score_expr(float score, float b, float h, float q_idx,\n"
+           "                                               float kv_idx)\n"
+           "{\n"
+           "    (void)score; (void)b; (void)h; (void)q_idx; (void)kv_idx;\n"
+           "    return " + cuda + ";\n"
+           "}\n"
+           "#include \"fwd_standard.cu\"\n";
+}
+
+constexpr const char *kKernelName = "fl::std_fwd_kernel<3>"; // MOD_EXPR
+
+// Compiles the standard kernel for the translated expression; the cubin and
+// the kernel's mangled name on success.
+bool compile(const std::string &cuda, std::vector<char> &cubin, std::string &name, char *err,
+             size_t err_n)
+{
+    const Nvrtc &n = nvrtc();
+    if (!n.ok) {
+        put(err, err_n, "the runtime compiler (libnvrtc.so.13) was not found");
+        return false;
+    }
+    std::vector<const char *> hnames, htexts;
+    for (const auto &s : kJitSources) {
+        hnames.push_back(s.name);
+        htexts.push_back(s.text);
+    }
+    const std::string src = program_source(cuda);
+    nvrtcProgram_t prog = nullptr;
+    if (n.create(&prog, src.c_str(), "score_expr_kernel.cu", int(hnames.size()), htexts.data(),
+                 hnames.data()) != 0) {
+        put(err, err_n, "nvrtcCreateProgram failed");
+        return false;
+    }
+    n.add_name(prog, kKernelName);
+    const std::string inc = "--include-path=" + cuda_home() + "/include";
+    // --prec-div=false: '/' is the fast division (within 2 ulp), not the
+    // IEEE-rounded one, whose slow path would cost ~10 instructions a score
+    const char *opts[] = {"--gpu-architecture=sm_103a", "-std=c++17", "-lineinfo", "--prec-div=false",
+                          inc.c_str()};
+    const int rc = n.compile(prog, 5, opts);
+    bool good = rc == 0;
+    if (!good) {
+        size_t ls = 0;
+        n.log_size(prog, &ls);
+        std::string log(ls, '\0');
+        if (ls)
+            n.log(prog, &log[0]);
+        put(err, err_n, "runtime compilation failed: %.900s", log.c_str());
+    } else {
+        size_t cs = 0;
+        const char *lowered = nullptr;
+        good = n.cubin_size(prog, &cs) == 0 && cs > 0 && n.lowered(prog, kKernelName, &lowered) == 0 &&
+               lowered;
+        if (good) {
+            cubin.resize(cs);
+            good = n.cubin(prog, cubin.data()) == 0;
+            name = lowered;
+        }
+        if (!good)
+            put(err, err_n, "reading the compiled kernel failed");
+    }
+    n.destroy(&prog);
+    return good;
+}
+
+// ------------------------------------------------------------------ modules
+
+struct Driver {
+    PFN_cuModuleLoadData_v2000 load = nullptr;
+    PFN_cuModuleGetFunction_v2000 get = nullptr;
+    PFN_cuFuncGetAttribute_v2020 attr = nullptr;
+    PFN_cuFuncSetAttribute_v9000 set = nullptr;
+    PFN_cuLaunchKernel_v4000 launch = nullptr;
+    bool ok = false;
+};
+
+const Driver &driver()
+{
+    static Driver d;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        auto entry = [](const char *name, int ver) -> void * {
+            void *f = nullptr;
+            cudaDriverEntryPointQueryResult q;
+            if (cudaGetDriverEntryPointByVersion(name, &f, ver, cudaEnableDefault, &q) != cudaSuccess ||
+                q != cudaDriverEntryPointSuccess)
+                return nullptr;
+            return f;
+        };
+        d.load = reinterpret_cast<PFN_cuModuleLoadData_v2000>(entry("cuModuleLoadData", 2000));
+        d.get = reinterpret_cast<PFN_cuModuleGetFunction_v2000>(entry("cuModuleGetFunction", 2000));
+        d.attr = reinterpret_cast<PFN_cuFuncGetAttribute_v2020>(entry("cuFuncGetAttribute", 2020));
+        d.set = reinterpret_cast<PFN_cuFuncSetAttribute_v9000>(entry("cuFuncSetAttribute", 9000));
+        d.launch = reinterpret_cast<PFN_cuLaunchKernel_v4000>(entry("cuLaunchKernel", 4000));
+        d.ok = d.load && d.get && d.attr && d.set && d.launch;
+    });
+    return d;
+}
+
+// One loaded kernel per (device, translated expression); modules stay loaded
+// until the process exits.
+std::mutex g_mutex;
+std::map<std::pair<int, std::string>, CUfunction> g_kernels;
+
+} // namespace
+
+bool score_expr_translate(const char *expr, char *cuda, size_t n, char *err, size_t err_n)
+{
+    if (!expr) {
+        put(err, err_n, "no expression");
+        return false;
+    }
+    std::string out, e;
+    if (!Translator(expr).run(out, e)) {
+        put(err, err_n, "%s", e.c_str());
+        return false;
+    }
+    if (out.size() + 1 > n) {
+        put(err, err_n, "translated expression too long");
+        return false;
+    }
+    memcpy(cuda, out.c_str(), out.size() + 1);
+    return true;
+}
+
+bool score_expr_compile_only(const char *cuda, char *err, size_t err_n)
+{
+    std::vector<char> cubin;
+    std::string name;
+    return compile(cuda, cubin, name, err, err_n);
+}
+
+cudaError_t launch_standard_expr(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
+                                 const StdParams &p, int grid, cudaStream_t stream, const char *cuda,
+                                 char *err, size_t err_n)
+{
+    const Driver &d = driver();
+    if (!d.ok) {
+        put(err, err_n, "driver entry points for module loading are unavailable");
+        return cudaErrorNotSupported;
+    }
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess)
+        return e;
+    const size_t smem = standard_smem_bytes();
+    CUfunction fn = nullptr;
+    {
+        std::lock_guard<std::mutex> lock(g_mutex);
+        auto it = g_kernels.find({dev, cuda});
+        if (it != g_kernels.end()) {
+            fn = it->second;
+        } else {
+            std::vector<char> cubin;
+            std::string name;
+            if (!compile(cuda, cubin, name, err, err_n))
+                return cudaErrorInvalidSource;
+            // the runtime has made the device's primary context current
+            if ((e = cudaFree(nullptr)) != cudaSuccess)
+                return e;
+            CUmodule mod = nullptr;
+            if (d.load(&mod, cubin.data()) != CUDA_SUCCESS || d.get(&fn, mod, name.c_str()) != CUDA_SUCCESS) {
+                put(err, err_n, "loading the compiled kernel failed");
+                return cudaErrorInvalidKernelImage;
+            }
+            // the setmaxnreg split assumes exactly kStdRegs registers at launch
+            int regs = 0;
+            if (d.attr(&regs, CU_FUNC_ATTRIBUTE_NUM_REGS, fn) != CUDA_SUCCESS || regs != kStdRegs) {
+                put(err, err_n, "the compiled kernel uses %d registers per thread, not %d", regs, kStdRegs);
+                return cudaErrorInvalidConfiguration;
+            }
+            if (d.set(fn, CU_FUNC_ATTRIBUTE_MAX_DYNAMIC_SHARED_SIZE_BYTES, int(smem)) != CUDA_SUCCESS) {
+                put(err, err_n, "setting the kernel's shared-memory size failed");
+                return cudaErrorInvalidConfiguration;
+            }
+            g_kernels[{dev, cuda}] = fn;
+        }
+    }
+    void *args[] = {const_cast<CUtensorMap *>(&tq), const_cast<CUtensorMap *>(&tk),
+                    const_cast<CUtensorMap *>(&tv), const_cast<StdParams *>(&p)};
+    if (d.launch(fn, unsigned(grid), 1, 1, unsigned(kStdThreads), 1, 1, unsigned(smem),
+                 reinterpret_cast<CUstream>(stream), args, nullptr) != CUDA_SUCCESS) {
+        put(err, err_n, "launching the compiled kernel failed");
+        return cudaErrorLaunchFailure;
+    }
+    return cudaSuccess;
+}
+
+} // namespace fl

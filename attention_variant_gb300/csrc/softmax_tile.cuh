@@ -35,6 +35,8 @@ struct ScoreMod {
     float alibi_c;     // slope_h * log2(e)                 (ALiBi)
     float softcap_in;  // 2 * scale * log2(e) / cap           (softcap)
     float softcap_out; // cap * log2(e)                       (softcap)
+    float scale;       // scale                               (expression)
+    float b, h;        // batch index and query head          (expression)
 };
 
 // Loads the N scores (N a multiple of 16) of this thread's row from TMEM
@@ -77,6 +79,16 @@ __device__ __forceinline__ void apply_score_mod(float (&x)[N], const ScoreMod &s
             const float ex = ptx::ex2(x[e] * sm.softcap_in);
             x[e] = sm.softcap_out * (1.f - 2.f * ptx::rcp_approx(1.f + ex));
         }
+    } else if constexpr (MOD == MOD_EXPR) {
+#ifdef FL_SCORE_EXPR
+        // the run-time expression fl_score_expr(score, b, h, q_idx, kv_idx)
+        // (defined ahead of this file by the runtime compilation), in log2 units
+        // (indices below 2^24 are exact in fp32; j0 + e as one add per score)
+        const float fi = static_cast<float>(i), fj0 = static_cast<float>(j0);
+#pragma unroll
+        for (int e = 0; e < N; ++e)
+            x[e] = kLog2e * fl_score_expr(x[e] * sm.scale, sm.b, sm.h, fi, fj0 + static_cast<float>(e));
+#endif
     }
 }
 

@@ -114,6 +114,21 @@ def entry(kind, S, variant):
                 bytes=2 * B * S * D * (2 * Hq + 2 * Hk) + 4 * B * Hq * S)
 
 
+# Score_mod expressions compiled at run time, on the same workload as the
+# built-in variant each one restates (the pages' generic-variant interface).
+EXPR_VARIANTS = {
+    "expr_softcap": ("softcap", "20 * tanh(score / 20)"),
+    "expr_alibi": ("alibi", "score - exp2(-8 * (h + 1) / 16) * abs(q_idx - kv_idx)"),
+}
+
+
+def expr_entry(S, name):
+    builtin, expr = EXPR_VARIANTS[name]
+    e = entry("mha", S, builtin)
+    e.update(variant=name, mod="expr", kw={"score_expr": expr})
+    return e
+
+
 def diff_entry(mask):
     w = workloads.DIFF
     B, S, H, D, Dv = w["B"], w["S"], w["H"], w["D"], w["Dv"]
@@ -295,6 +310,9 @@ def time_entry(e, host, torch, fa, device, steps, warmup, flush, stream):
     doc_t = torch.from_numpy(e["doc"]).to(device) if e["doc"] is not None else None
     desc = fa.make_desc(score_mod=e["mod"], mask=e["mask"], doc_offsets=doc_t,
                         softcap=workloads.SOFTCAP, **e["kw"])
+    if e["mod"] == "expr":
+        fa.fl_attn_fwd(q, k, v, out, lse, desc, stream=stream)  # the run-time compilation
+        torch.cuda.synchronize()
     with torch.cuda.stream(stream):
         for _ in range(warmup):
             flush.zero_()
@@ -565,7 +583,7 @@ def run_ours(args):
             variants[f"{e['name']}/{e['variant']}"] = dict(
                 tflops=round(e["flops"] / (vm * 1e-3) / 1e12, 1), ms=round(vm, 4), gbs=round(gbs, 1),
                 frac_hbm=round(gbs / peaks["hbm_gbs"], 4), l2=l2_policy(e))
-        for e in all_entries():
+        for e in all_entries() + [expr_entry(head["S"], n) for n in EXPR_VARIANTS]:
             h = gpu_inputs(e, torch, device) if (e["S"], e["kind"]) != (head["S"], "mha") else host
             vms, _ = time_entry(e, h, torch, fa, device, args.variant_steps, 2, flush, stream)
             vm = statistics.mean(vms)

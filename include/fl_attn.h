@@ -79,9 +79,40 @@ typedef enum {
 
 typedef enum {
     FL_MOD_NONE = 0,
-    FL_MOD_ALIBI = 1,  /* z += -slope_h * |i - j|, slope_h = 2^(-8 (h+1) / Hq) by default */
-    FL_MOD_SOFTCAP = 2 /* z = cap * tanh(z / cap) */
+    FL_MOD_ALIBI = 1,   /* z += -slope_h * |i - j|, slope_h = 2^(-8 (h+1) / Hq) by default */
+    FL_MOD_SOFTCAP = 2, /* z = cap * tanh(z / cap) */
+    FL_MOD_EXPR = 3     /* z = the expression desc->score_mod_expr (FL_KIND_STANDARD) */
 } fl_score_mod;
+
+/*
+ * score_mod expressions (FL_MOD_EXPR).  The logit of (query row q_idx, key
+ * kv_idx) of batch b and query head h is the value of a user expression over
+ *     score   scale * q . k (the scaled dot product)
+ *     b, h, q_idx, kv_idx
+ * in this grammar (every value fp32; a comparison gives 1 or 0; '/' is the
+ * fast division, within 2 ulp, and tanh is 1 - 2 / (1 + e^(2x)) on the fast
+ * exponential, absolute error about 1e-7):
+ *     expr    := sum [ relop sum ]        relop: < <= > >= == !=  (no chains)
+ *     sum     := term { (+ | -) term }
+ *     term    := unary { (* | /) unary }
+ *     unary   := (- | +) unary | primary
+ *     primary := number | score | b | h | q_idx | kv_idx | inf
+ *              | tanh(e) | exp(e) | exp2(e) | log(e) | log2(e) | sqrt(e)
+ *              | abs(e) | floor(e) | min(e, e) | max(e, e)
+ *              | where(c, x, y)           (x where c != 0, else y)
+ *              | ( expr )
+ * e.g. "20 * tanh(score / 20)" (softcap), "score - 0.5 * abs(q_idx - kv_idx)"
+ * (ALiBi with slope 0.5), "where(kv_idx <= q_idx, score, -inf)" (a causal
+ * mask written as a score_mod).  -inf removes the pair; the mask in the desc
+ * still applies on top.  This is the pages' generic-variant interface: the
+ * expression is fused into the same single-pass kernel as the built-in
+ * variants (talk notes, "Compiler design" and the comparison with
+ * FlexAttention).  The first call with a new expression on a device compiles
+ * the kernel for it at run time (NVRTC, about two seconds; the CUDA toolkit's
+ * libnvrtc.so.13 and include directory -- $CUDA_HOME, else /usr/local/cuda --
+ * must be present, or the call returns FL_ERR_UNSUPPORTED); later calls reuse
+ * it.  A string outside the grammar returns FL_ERR_INVALID_ARG.
+ */
 
 typedef enum {
     FL_MASK_NONE = 0,
@@ -124,6 +155,7 @@ typedef struct {
     uint32_t *error_word;    /* NULL, or a device word the kernel ORs FL_DEVERR_* into */
     int32_t debug_inject;    /* fl_inject; 0 in normal use */
     uint32_t wait_timeout_us; /* bound of every device-side wait; 0 means 2,000,000 */
+    const char *score_mod_expr; /* FL_MOD_EXPR: the expression (host string), else unused */
 } fl_attn_variant_desc;
 
 /*
@@ -166,6 +198,12 @@ fl_status fl_attn_fwd(const fl_tensor *q, const fl_tensor *k, const fl_tensor *v
  * visited-tile accounting).  Never touches the device. */
 fl_status fl_attn_tile_shape(const fl_attn_variant_desc *desc, int32_t head_dim,
                              int32_t *block_m, int32_t *block_n);
+
+/* Checks a score_mod expression against the FL_MOD_EXPR grammar (FL_OK or
+ * FL_ERR_INVALID_ARG, with the position in fl_attn_last_error()).  With
+ * `compile` nonzero it also runs the runtime compilation of the kernel for it
+ * (no device needed; FL_ERR_UNSUPPORTED without NVRTC). */
+fl_status fl_attn_score_expr_check(const char *expr, int32_t compile);
 
 /* Static text for a status code. */
 const char *fl_attn_status_string(fl_status status);

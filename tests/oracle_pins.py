@@ -414,7 +414,52 @@ def pin_decode(lib):
            what="SDPA decode softcap")
 
 
+def pin_score_expr(lib):
+    """The score_mod-expression oracle (numpy, float64) against the C oracle's
+    built-in variants written as expressions, against a closed form, on rows
+    the expression removes entirely, and on the strings the grammar refuses."""
+    from oracle import score_expr as se
+
+    B, S, Hq, Hk, D = 2, 70, 4, 2, 64
+    q, k, v = _rand((B, S, Hq, D), "xq"), _rand((B, S, Hk, D), "xk"), _rand((B, S, Hk, D), "xv")
+    cases = [
+        ("score", "none", dict(mod="none", mask="none")),
+        ("score", "causal", dict(mod="none", mask="causal")),
+        ("20 * tanh(score / 20)", "none", dict(mod="softcap", softcap=20.0, mask="none")),
+        # default ALiBi slopes 2^(-8 (h + 1) / Hq) with Hq = 4
+        ("score - exp2(-8 * (h + 1) / 4) * abs(q_idx - kv_idx)", "causal",
+         dict(mod="alibi", mask="causal")),
+        ("where(kv_idx <= q_idx, score, -inf)", "none", dict(mod="none", mask="causal")),
+        ("where(kv_idx > q_idx, -inf, score)", "none", dict(mod="none", mask="causal")),
+    ]
+    for expr, mask, kw in cases:
+        o, l = se.attention_expr(q, k, v, expr, mask=mask)
+        o2, l2 = oracle.attention(q, k, v, lib=lib, **kw)
+        _close(o, o2, atol=1e-9, what=f"expr {expr!r} O")
+        _close(l, l2, atol=1e-9, what=f"expr {expr!r} LSE")
+    # a constant logit c: O_i = mean of v over the allowed keys, LSE_i = c + ln(count)
+    vf = _f64(v)
+    csum = np.cumsum(vf, axis=1)
+    o, l = se.attention_expr(q, k, v, "0 * score + 3", mask="causal")
+    for h in range(Hq):
+        cnt = np.arange(1, S + 1)[None, :, None]
+        _close(o[:, :, h], csum[:, :, h // (Hq // Hk)] / cnt, what="constant logit O")
+        _close(l[:, h], 3.0 + np.log(np.arange(1, S + 1))[None, :], what="constant logit LSE")
+    # rows the expression removes entirely: O = 0, LSE = -inf; the others unchanged
+    o, l = se.attention_expr(q, k, v, "where(q_idx < 5, -inf, score)")
+    o2, l2 = se.attention_expr(q, k, v, "score")
+    assert np.all(o[:, :5] == 0) and np.all(np.isneginf(l[:, :, :5]))
+    _close(o[:, 5:], o2[:, 5:], what="unmasked rows")
+    for bad in ["score ** 2", "score // 2", "a + 1", "1 < score < 3", "tanh(score, 1)", "tanh",
+                "__import__('os')", "score if b else h", "[score]", "score.real", "True + score"]:
+        try:
+            se.parse(bad)
+        except ValueError:
+            continue
+        raise AssertionError(f"the grammar accepted {bad!r}")
+
+
 ALL_PINS = [pin_constant_scores, pin_alibi_geometric, pin_softcap_two_keys, pin_one_hot,
             pin_rows_sum_to_one, pin_shift_invariance, pin_permutation, pin_causal_row0,
             pin_sdpa, pin_reductions, pin_rows_api, pin_diff, pin_evo, pin_fully_masked_row,
-            pin_decode]
+            pin_decode, pin_score_expr]

@@ -177,3 +177,60 @@ def test_decode_validation_before_device(lib):
     assert call(o=_t((B, Sq, Hq + 1, 64))) == fa.FL_ERR_INVALID_ARG
     assert call(lse=_t((B, Hq, Sq + 1), fa.FL_F32)) == fa.FL_ERR_INVALID_ARG
     assert call(d=_ddesc(max_kv=500, kv_lens=None)) == fa.FL_ERR_INVALID_ARG
+
+
+# ---- score_mod expressions (FL_MOD_EXPR)
+
+GOOD_EXPRS = ["score", "20 * tanh(score / 20)", "score - 0.5 * abs(q_idx - kv_idx)",
+              "where(kv_idx <= q_idx, score, -inf)", "max(score, .5e1) + (q_idx >= kv_idx) * 2",
+              "exp2(-(h + 1) / 2) * floor(kv_idx / 64) + log(1 + exp(score)) - sqrt(b + 1) + log2(4)",
+              "min(score, 3.) / 2 - +score * -1"]
+BAD_EXPRS = ["", "score +", "score ** 2", "score // 2", "score /* c */", "a + 1", "1 < score < 3",
+             "tanh(score, 1)", "tanh", "where(score, 1)", "20f", "1e", "0x10", "score; score",
+             "score = 1", "(score", "score)", "score & 1", "score ? 1 : 0", "pi * score"]
+
+
+@pytest.mark.parametrize("expr", GOOD_EXPRS)
+def test_score_expr_grammar_accepts(lib, expr):
+    assert lib.fl_attn_score_expr_check(expr.encode(), 0) == fa.FL_OK, fa.fl_attn_last_error()
+
+
+@pytest.mark.parametrize("expr", BAD_EXPRS)
+def test_score_expr_grammar_refuses(lib, expr):
+    assert lib.fl_attn_score_expr_check(expr.encode(), 0) == fa.FL_ERR_INVALID_ARG
+    assert "score_mod_expr" in fa.fl_attn_last_error()
+
+
+def test_score_expr_grammar_matches_the_oracle_grammar():
+    # the CUDA translator and the oracle's parser are separate code; every
+    # string one accepts the other accepts, and the same for refusals
+    from oracle import score_expr as se
+
+    for expr in GOOD_EXPRS:
+        se.parse(expr)
+    for expr in BAD_EXPRS:
+        if expr in ("0x10",):  # a Python literal the CUDA side refuses: stricter there
+            continue
+        with pytest.raises(ValueError):
+            se.parse(expr)
+
+
+def test_score_expr_runtime_compilation_needs_no_device(lib):
+    # the whole standard kernel is compiled for sm_103a with the expression
+    # as its score_mod (NVRTC; no GPU involved)
+    st = lib.fl_attn_score_expr_check(b"score - 0.25 * abs(q_idx - kv_idx) + h * b", 1)
+    assert st == fa.FL_OK, fa.fl_attn_last_error()
+
+
+def test_score_expr_refused_before_device(lib):
+    B, S, H, D = 2, 256, 4, 64
+    t = lambda: _t((B, S, H, D))
+    d = fa.make_desc(score_expr="score ** 2")
+    assert _call(lib, t(), t(), t(), t(), desc=d) == fa.FL_ERR_INVALID_ARG
+    assert "score_mod_expr" in fa.fl_attn_last_error()
+    d = fa.make_desc(score_mod="expr")  # no string
+    assert _call(lib, t(), t(), t(), t(), desc=d) == fa.FL_ERR_INVALID_ARG
+    # the other kinds take no expression
+    d = fa.make_desc(kind="evo_row", score_expr="score")
+    assert _call(lib, _t((4, 64, 8, 32)), _t((4, 64, 8, 32)), _t((4, 64, 8, 32)),
+                 _t((4, 64, 8, 32)), desc=d) != fa.FL_OK

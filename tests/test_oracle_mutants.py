@@ -56,3 +56,32 @@ def test_mutant_is_caught(name, tmp_path):
         except AssertionError:
             caught.append(pin.__name__)
     assert caught, f"no pin detects mutant {name}"
+
+
+# Mistakes planted in the score_mod-expression oracle (oracle/score_expr.py):
+# each replaces one entry of its operator or function tables for the duration
+# of the test; the expression pin must fail.
+def _expr_mutants():
+    import ast
+
+    import numpy as np
+
+    return {
+        "expr_tanh_is_sinh": ("_FUNCS", "tanh", (1, np.sinh)),
+        "expr_le_is_lt": ("_CMP", ast.LtE, np.less),
+        "expr_gt_is_ge": ("_CMP", ast.Gt, np.greater_equal),
+        "expr_sub_reversed": ("_BIN", ast.Sub, lambda a, b: b - a),
+        "expr_div_is_mul": ("_BIN", ast.Div, np.multiply),
+        "expr_exp2_is_exp": ("_FUNCS", "exp2", (1, np.exp)),
+        "expr_where_swapped": ("_FUNCS", "where", (3, lambda c, x, y: np.where(np.asarray(c) != 0, y, x))),
+    }
+
+
+@pytest.mark.parametrize("name", sorted(_expr_mutants()))
+def test_expr_mutant_is_caught(name, monkeypatch):
+    from oracle import score_expr as se
+
+    table, key, value = _expr_mutants()[name]
+    monkeypatch.setitem(getattr(se, table), key, value)
+    with pytest.raises(AssertionError):
+        oracle_pins.pin_score_expr(oracle.load())
