@@ -366,12 +366,18 @@ std::string program_source(const std::string &cuda)
     return "#define FL_SCORE_EXPR 1\n"
            "__device__ __forceinline__ float fl_x_bool(bool c) { return c ? 1.f : 0.f; }\n"
            "__device__ __forceinline__ float fl_x_inf() { return __int_as_float(0x7f800000); }\n"
-           // tanh(x) = 1 - 2 / (1 + e^(2x)) on the fast exponential and
-           // division (absolute error ~1e-7; +-1 at the extremes)
+           // exponentials on the hardware 2^x (relative error ~2^-22);
+           // tanh(x) = 1 - 2 / (1 + e^(2x)) on it and the hardware
+           // reciprocal (absolute error ~1e-7; +-1 at the extremes)
+           "__device__ __forceinline__ float fl_x_exp2(float x)\n"
+           "{ float y; asm(\"ex2.approx.ftz.f32 %0, %1;\" : \"=f\"(y) : \"f\"(x)); return y; }\n"
+           "__device__ __forceinline__ float fl_x_exp(float x) { return fl_x_exp2(x * 1.4426950408889634f); }\n"
            "__device__ __forceinline__ float fl_x_tanh(float x)\n"
-           "{ return 1.f - __fdividef(2.f, 1.f + exp2f(x * 2.8853900817779268f)); }\n"
-           "__device__ __forceinline__ float fl_x_exp(float x) { return expf(x); }\n"
-           "__device__ __forceinline__ float fl_x_exp2(float x) { return exp2f(x); }\n"
+           "{\n"
+           "    float r;\n"
+           "    asm(\"rcp.approx.ftz.f32 %0, %1;\" : \"=f\"(r) : \"f\"(1.f + fl_x_exp2(x * 2.8853900817779268f)));\n"
+           "    return 1.f - 2.f * r;\n"
+           "}\n"
            "__device__ __forceinline__ float fl_x_log(float x) { return logf(x); }\n"
            "__device__ __forceinline__ float fl_x_log2(float x) { return log2f(x); }\n"
            "__device__ __forceinline__ float fl_x_sqrt(float x) { return sqrtf(x); }\n"

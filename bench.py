@@ -504,11 +504,14 @@ def cpu_baseline(e, seconds=12.0):
 
 ONLY = {"diff": lambda: diff_entry("none"), "diff_causal": lambda: diff_entry("causal"),
         "evo_row": lambda: evo_entry(True), "evo_col": lambda: evo_entry(False),
-        "decode": lambda: decode_entry("none"), "decode_softcap": lambda: decode_entry("softcap")}
+        "decode": lambda: decode_entry("none"), "decode_softcap": lambda: decode_entry("softcap"),
+        "softcap": lambda: entry("mha", 2048, "softcap"), "alibi": lambda: entry("mha", 2048, "alibi"),
+        "expr_softcap": lambda: expr_entry(2048, "expr_softcap"),
+        "expr_alibi": lambda: expr_entry(2048, "expr_alibi")}
 
 
 def run_only(args):
-    """Time one differential or Evoformer workload alone (for profiling)."""
+    """Time one workload alone (for profiling)."""
     import torch
     import attention_variant_gb300 as fa
     torch.cuda.set_device(0)
@@ -517,8 +520,12 @@ def run_only(args):
     stream = torch.cuda.Stream(device)
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=device)
     e = ONLY[args.only]()
-    timer = time_decode if e["kind"] == "decode" else time_other
-    ms = statistics.mean(timer(e, torch, fa, device, args.steps, args.warmup, flush, stream))
+    if e["kind"] in ("mha", "gqa"):
+        ms = statistics.mean(time_entry(e, gpu_inputs(e, torch, device), torch, fa, device, args.steps,
+                                        args.warmup, flush, stream)[0])
+    else:
+        timer = time_decode if e["kind"] == "decode" else time_other
+        ms = statistics.mean(timer(e, torch, fa, device, args.steps, args.warmup, flush, stream))
     print(json.dumps({"only": args.only, "ms": round(ms, 4),
                       "tflops": round(e["flops"] / (ms * 1e-3) / 1e12, 1),
                       "gbs": round(e["bytes"] / (ms * 1e-3) / 1e9, 1)}), flush=True)
@@ -681,7 +688,7 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--only", choices=sorted(ONLY), default=None,
-                    help="time only this differential/Evoformer workload (profiling aid)")
+                    help="time only this workload (profiling aid)")
     ap.add_argument("--clock-steps", type=int, default=3000,
                     help="untimed steps run under the clock sampler before the timed ones")
     args = ap.parse_args()

@@ -90,8 +90,9 @@ typedef enum {
  *     score   scale * q . k (the scaled dot product)
  *     b, h, q_idx, kv_idx
  * in this grammar (every value fp32; a comparison gives 1 or 0; '/' is the
- * fast division, within 2 ulp, and tanh is 1 - 2 / (1 + e^(2x)) on the fast
- * exponential, absolute error about 1e-7):
+ * fast division, within 2 ulp; exp and exp2 use the hardware 2^x, relative
+ * error about 2^-22; tanh is 1 - 2 / (1 + e^(2x)) on it, absolute error
+ * about 1e-7):
  *     expr    := sum [ relop sum ]        relop: < <= > >= == !=  (no chains)
  *     sum     := term { (+ | -) term }
  *     term    := unary { (* | /) unary }
