@@ -116,6 +116,9 @@ def load_library(path: str = LIB_PATH):
     lib.fl_attn_last_error.restype = ctypes.c_char_p
     lib.fl_attn_last_error.argtypes = []
     lib.fl_attn_version.restype = ctypes.c_int32
+    lib.fl_attn_evoformer.restype = ctypes.c_int
+    lib.fl_attn_evoformer.argtypes = [P(FlTensor), P(FlTensor), P(FlTensor), P(FlTensor), P(FlTensor),
+                                      P(FlDesc), P(FlTensor), P(FlTensor), P(FlTensor), ctypes.c_void_p]
     lib.fl_attn_score_expr_check.restype = ctypes.c_int
     lib.fl_attn_score_expr_check.argtypes = [ctypes.c_char_p, ctypes.c_int32]
     lib.fl_attn_decode_workspace_size.restype = ctypes.c_int
@@ -188,6 +191,24 @@ def make_desc(kind="standard", score_mod="none", softcap=20.0, mask="none", wind
 
 def _ref(x):
     return ctypes.byref(x) if x is not None else None
+
+
+def fl_attn_evoformer(q, k, v, out, lse, desc: FlDesc, bias=None, gate=None, msa_mask=None,
+                      stream=None) -> None:
+    """The Evoformer kinds over a batch of MSA stacks (5-D tensors) with an
+    optional MSA mask (see include/fl_attn.h); raises FlAttnError."""
+    lib = load_library()
+    if stream is None:
+        import torch
+        stream = torch.cuda.current_stream().cuda_stream
+    elif hasattr(stream, "cuda_stream"):
+        stream = stream.cuda_stream
+    t = [as_fl_tensor(x) if x is not None else None for x in (q, k, v, out, lse, bias, gate, msa_mask)]
+    st = lib.fl_attn_evoformer(_ref(t[0]), _ref(t[1]), _ref(t[2]), _ref(t[3]), _ref(t[4]),
+                               ctypes.byref(desc), _ref(t[5]), _ref(t[6]), _ref(t[7]),
+                               ctypes.c_void_p(stream))
+    if st != FL_OK:
+        raise FlAttnError(st, fl_attn_last_error())
 
 
 def fl_attn_score_expr_check(expr: str, compile: bool = False) -> None:

@@ -475,9 +475,10 @@ fl_status fwd_diff(const fl_tensor *q, const fl_tensor *k, const fl_tensor *v,
 
 fl_status fwd_evo(bool row_pass, const fl_tensor *q, const fl_tensor *k, const fl_tensor *v,
                   const fl_tensor *out, const fl_tensor *lse, const fl_attn_variant_desc *d,
-                  const fl_tensor *bias, const fl_tensor *gate, cudaStream_t stream)
+                  const fl_tensor *bias, const fl_tensor *gate, const fl_tensor *msa_mask,
+                  cudaStream_t stream)
 {
-    View Q, K, V, O, G, Bz{}, L{};
+    View Q, K, V, O, G, Bz{}, L{}, M{};
     fl_status s;
     if ((s = check_tensor(q, "q", 4, FL_BF16, Q)) != FL_OK) return s;
     if ((s = check_tensor(k, "k", 4, FL_BF16, K)) != FL_OK) return s;
@@ -501,6 +502,13 @@ fl_status fwd_evo(bool row_pass, const fl_tensor *q, const fl_tensor *k, const f
         if (!same(L, {B, H, S}))
             return fail(FL_ERR_INVALID_ARG, row_pass ? "lse must be [N_seq, H, N_res]"
                                                      : "lse must be [N_res, H, N_seq]");
+    }
+    if (msa_mask) {
+        if (msa_mask->dtype != FL_BF16 && msa_mask->dtype != FL_F32)
+            return fail(FL_ERR_INVALID_ARG, "msa_mask must be bf16 or fp32");
+        if ((s = check_tensor(msa_mask, "msa_mask", 2, msa_mask->dtype, M)) != FL_OK) return s;
+        if (!same(M, {Ns, Nr}))
+            return fail(FL_ERR_INVALID_ARG, "msa_mask must be [N_seq, N_res]");
     }
     if (d->mask != FL_MASK_NONE || d->score_mod != FL_MOD_NONE)
         return fail(FL_ERR_UNSUPPORTED, "the Evoformer kinds take no mask and no score_mod");
@@ -591,6 +599,14 @@ fl_status fwd_evo(bool row_pass, const fl_tensor *q, const fl_tensor *k, const f
         p.l_sh = L.stride[1];
     }
     p.tile_counts = d->debug_tile_counts;
+    if (msa_mask) {
+        // key j of batch index b: row pass b = MSA row, j = residue; column
+        // pass b = residue, j = MSA row
+        p.kmask = M.ptr;
+        p.km_f32 = msa_mask->dtype == FL_F32;
+        p.km_sb = M.stride[ab];
+        p.km_sk = M.stride[ai];
+    }
     p.err_user = d->error_word;
     p.timeout_ns = timeout_ns(d);
     const int grid = int(p.n_items < info.sm_count ? p.n_items : info.sm_count);
@@ -769,6 +785,89 @@ fl_status decode_run(const DecodePlan &pl, const fl_tensor *out, const fl_tensor
 
 extern "C" {
 
+// Stacks of a batch run one launch each (every launch alone fills the GPU at
+// AlphaFold2 sizes: N_seq x H x ceil(N_res / 128) work items for the row pass).
+// The per-stack tensors are views of the caller's: only the base pointer moves
+// by the stack stride, so validating the stack-stride rules and the first
+// stack validates them all before anything is launched.
+fl_status fl_attn_evoformer(const fl_tensor *q, const fl_tensor *k, const fl_tensor *v,
+                            const fl_tensor *out, const fl_tensor *lse,
+                            const fl_attn_variant_desc *desc, const fl_tensor *bias,
+                            const fl_tensor *gate, const fl_tensor *msa_mask, fl_stream_t stream)
+{
+    if (!desc)
+        return fail(FL_ERR_INVALID_ARG, "desc is NULL");
+    if (desc->kind != FL_KIND_EVO_ROW && desc->kind != FL_KIND_EVO_COL)
+        return fail(FL_ERR_INVALID_ARG, "fl_attn_evoformer takes FL_KIND_EVO_ROW or FL_KIND_EVO_COL");
+    const bool row = desc->kind == FL_KIND_EVO_ROW;
+    const cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    if (!q)
+        return fail(FL_ERR_INVALID_ARG, "q is NULL");
+    if (q->ndim == 4)
+        return fwd_evo(row, q, k, v, out, lse, desc, bias, gate, msa_mask, st);
+    if (q->ndim != 5)
+        return fail(FL_ERR_INVALID_ARG, "q must be [N_seq, N_res, H, c] or [B, N_seq, N_res, H, c]");
+    const int64_t Bt = q->sizes[0];
+    if (Bt < 1)
+        return fail(FL_ERR_INVALID_ARG, "batch of stacks must be >= 1");
+    // every batched tensor has one more leading axis of size Bt, whose stride
+    // keeps the per-stack views aligned; bias and msa_mask may instead have
+    // one axis fewer (one tensor shared by every stack)
+    struct Arg {
+        const fl_tensor *t;
+        const char *name;
+        int batched_rank;
+        bool shared_ok;
+    };
+    const Arg args[] = {{q, "q", 5, false},       {k, "k", 5, false},
+                        {v, "v", 5, false},       {out, "out", 5, false},
+                        {gate, "gate", 5, false}, {lse, "lse", 4, false},
+                        {bias, "bias", 4, true},  {msa_mask, "msa_mask", 3, true}};
+    fl_tensor views[8];
+    const fl_tensor *per_stack[8];
+    bool batched[8];
+    for (int a = 0; a < 8; ++a) {
+        per_stack[a] = args[a].t;
+        batched[a] = false;
+        if (!args[a].t)
+            continue;
+        const fl_tensor &t = *args[a].t;
+        if (t.ndim == args[a].batched_rank) {
+            if (t.sizes[0] != Bt)
+                return fail(FL_ERR_INVALID_ARG, "%s has %lld stacks, q has %lld", args[a].name,
+                            (long long)t.sizes[0], (long long)Bt);
+            const int elt = t.dtype == FL_F32 ? 4 : 2;
+            if (Bt > 1 && (t.strides[0] <= 0 || (t.strides[0] * elt) % 16 != 0))
+                return fail(FL_ERR_ALIGNMENT, "%s stack stride must be a positive multiple of 16 bytes",
+                            args[a].name);
+            views[a] = t;
+            views[a].ndim = t.ndim - 1;
+            for (int d = 0; d < 4; ++d) {
+                views[a].sizes[d] = t.sizes[d + 1];
+                views[a].strides[d] = t.strides[d + 1];
+            }
+            per_stack[a] = &views[a];
+            batched[a] = true;
+        } else if (!(args[a].shared_ok && t.ndim == args[a].batched_rank - 1)) {
+            return fail(FL_ERR_INVALID_ARG, "%s must have %d dimensions%s", args[a].name,
+                        args[a].batched_rank, args[a].shared_ok ? " (or one fewer, shared)" : "");
+        }
+    }
+    for (int64_t b = 0; b < Bt; ++b) {
+        for (int a = 0; a < 8; ++a)
+            if (batched[a]) {
+                const fl_tensor &t = *args[a].t;
+                const int elt = t.dtype == FL_F32 ? 4 : 2;
+                views[a].ptr = static_cast<char *>(t.ptr) + b * t.strides[0] * elt;
+            }
+        const fl_status s = fwd_evo(row, per_stack[0], per_stack[1], per_stack[2], per_stack[3],
+                                    per_stack[5], desc, per_stack[6], per_stack[4], per_stack[7], st);
+        if (s != FL_OK)
+            return s;
+    }
+    return ok();
+}
+
 fl_status fl_attn_score_expr_check(const char *expr, int32_t compile)
 {
     char cuda[kExprCudaMax], err[1024];
@@ -858,7 +957,7 @@ fl_status fl_attn_fwd(const fl_tensor *q, const fl_tensor *k, const fl_tensor *v
         return fwd_diff(q, k, v, out, lse, desc, bias, gate, reinterpret_cast<cudaStream_t>(stream));
     case FL_KIND_EVO_ROW:
     case FL_KIND_EVO_COL:
-        return fwd_evo(desc->kind == FL_KIND_EVO_ROW, q, k, v, out, lse, desc, bias, gate,
+        return fwd_evo(desc->kind == FL_KIND_EVO_ROW, q, k, v, out, lse, desc, bias, gate, nullptr,
                        reinterpret_cast<cudaStream_t>(stream));
     default:
         return fail(FL_ERR_INVALID_ARG, "unknown kind %d", desc->kind);

@@ -382,7 +382,18 @@ __device__ __forceinline__ void store_row_output(const EvoParams &p, uint32_t tO
         p.tile_counts[(static_cast<int64_t>(pr.b) * p.grid.Hq + pr.h) * p.grid.nq + pr.qb] = nkv;
 }
 
-template <bool BIAS, bool LSE>
+// Whether the MSA mask keeps key `key` of batch index b (a nonzero entry;
+// keys past the sequence count as removed).
+__device__ __forceinline__ uint32_t mask_keeps(const EvoParams &p, int b, int key, int S)
+{
+    if (key >= S)
+        return 0u;
+    const int64_t off = b * p.km_sb + static_cast<int64_t>(key) * p.km_sk;
+    return p.km_f32 ? (__ldg(static_cast<const uint32_t *>(p.kmask) + off) & 0x7FFFFFFFu)
+                    : (__ldg(static_cast<const uint16_t *>(p.kmask) + off) & 0x7FFFu);
+}
+
+template <bool BIAS, bool LSE, bool KMASK>
 __device__ void softmax_role(const Ctx<BIAS> &cx, const EvoParams &p, int t)
 {
     EvoSmem<BIAS> &sm = *cx.sm;
@@ -412,6 +423,15 @@ __device__ void softmax_role(const Ctx<BIAS> &cx, const EvoParams &p, int t)
         for (int b = it.b0 + t; b < it.b1; b += 2) {
             RowState st{kNegInf, 0.f, 0.f};
             for (int j = 0; j < nkv; ++j) {
+                // MSA mask of this batch index and key tile: lane l reads keys
+                // j0 + 32 w + l (issued before the wait, used after it)
+                uint32_t keep[4];
+                if constexpr (KMASK) {
+                    const int lane = threadIdx.x & 31;
+#pragma unroll
+                    for (int w = 0; w < 4; ++w)
+                        keep[w] = mask_keeps(p, b, j * BN + 32 * w + lane, S);
+                }
                 if (!warp_wait(bar(sm.s_full[t]), scount & 1, cx.wc, W_S_FULL))
                     return;
                 ++scount;
@@ -447,6 +467,21 @@ __device__ void softmax_role(const Ctx<BIAS> &cx, const EvoParams &p, int t)
                 }
                 if (!((j0 >= tr.full_lo) && (j0 + BN <= tr.full_hi)))
                     apply_row_mask(x, j0, row_lo, row_hi);
+                if constexpr (KMASK) {
+                    // word w bit l: key j0 + 32 w + l is kept
+                    uint32_t bits[4], all = ~0u;
+#pragma unroll
+                    for (int w = 0; w < 4; ++w) {
+                        bits[w] = __ballot_sync(0xffffffffu, keep[w] != 0u);
+                        all &= bits[w];
+                    }
+                    if (all != ~0u) {
+#pragma unroll
+                        for (int e = 0; e < BN; ++e)
+                            if (!((bits[e >> 5] >> (e & 31)) & 1u))
+                                x[e] = kNegInf;
+                    }
+                }
                 uint32_t pk[BN / 2];
                 bool rescale;
                 const float alpha =
@@ -495,7 +530,7 @@ __device__ void softmax_role(const Ctx<BIAS> &cx, const EvoParams &p, int t)
     }
 }
 
-template <bool BIAS, bool LSE>
+template <bool BIAS, bool LSE, bool KMASK>
 __global__ void __launch_bounds__(kThreads, 1)
     evo_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                    const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_b,
@@ -561,7 +596,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // runs under both register limits.
     if (warp >= 4) {
         ptx::setmaxnreg_inc<kRegsSoftmax>();
-        softmax_role<BIAS, LSE>(cx, p, (warp >> 2) - 1);
+        softmax_role<BIAS, LSE, KMASK>(cx, p, (warp >> 2) - 1);
         ptx::tc_fence_before();
         ptx::named_barrier_sync(1, kThreads);
     } else {
@@ -581,7 +616,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 }
 
-template <bool BIAS, bool LSE>
+template <bool BIAS, bool LSE, bool KMASK>
 cudaError_t launch_variant(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
                            const CUtensorMap &tb, const EvoParams &p, int grid, cudaStream_t stream)
 {
@@ -589,19 +624,19 @@ cudaError_t launch_variant(const CUtensorMap &tq, const CUtensorMap &tk, const C
     static bool configured = false; // benign race: both calls are idempotent
     if (!configured) {
         cudaFuncAttributes attr;
-        cudaError_t e = cudaFuncGetAttributes(&attr, evo_fwd_kernel<BIAS, LSE>);
+        cudaError_t e = cudaFuncGetAttributes(&attr, evo_fwd_kernel<BIAS, LSE, KMASK>);
         if (e != cudaSuccess)
             return e;
         // The setmaxnreg split assumes exactly kRegsLaunch registers at launch.
         if (attr.numRegs != static_cast<int>(kRegsLaunch))
             return cudaErrorInvalidConfiguration;
-        e = cudaFuncSetAttribute(evo_fwd_kernel<BIAS, LSE>,
+        e = cudaFuncSetAttribute(evo_fwd_kernel<BIAS, LSE, KMASK>,
                                  cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
         if (e != cudaSuccess)
             return e;
         configured = true;
     }
-    evo_fwd_kernel<BIAS, LSE><<<grid, kThreads, smem, stream>>>(tq, tk, tv, tb, p);
+    evo_fwd_kernel<BIAS, LSE, KMASK><<<grid, kThreads, smem, stream>>>(tq, tk, tv, tb, p);
     return cudaGetLastError();
 }
 
@@ -610,11 +645,18 @@ cudaError_t launch_variant(const CUtensorMap &tq, const CUtensorMap &tk, const C
 cudaError_t launch_evo(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
                        const CUtensorMap &tb, const EvoParams &p, int grid, cudaStream_t stream)
 {
+    if (p.kmask) {
+        if (p.bias)
+            return p.lse ? launch_variant<true, true, true>(tq, tk, tv, tb, p, grid, stream)
+                         : launch_variant<true, false, true>(tq, tk, tv, tb, p, grid, stream);
+        return p.lse ? launch_variant<false, true, true>(tq, tk, tv, tb, p, grid, stream)
+                     : launch_variant<false, false, true>(tq, tk, tv, tb, p, grid, stream);
+    }
     if (p.bias)
-        return p.lse ? launch_variant<true, true>(tq, tk, tv, tb, p, grid, stream)
-                     : launch_variant<true, false>(tq, tk, tv, tb, p, grid, stream);
-    return p.lse ? launch_variant<false, true>(tq, tk, tv, tb, p, grid, stream)
-                 : launch_variant<false, false>(tq, tk, tv, tb, p, grid, stream);
+        return p.lse ? launch_variant<true, true, false>(tq, tk, tv, tb, p, grid, stream)
+                     : launch_variant<true, false, false>(tq, tk, tv, tb, p, grid, stream);
+    return p.lse ? launch_variant<false, true, false>(tq, tk, tv, tb, p, grid, stream)
+                 : launch_variant<false, false, false>(tq, tk, tv, tb, p, grid, stream);
 }
 
 int evo_max_bias_keys() { return kMaxBiasBoxes * 64; }

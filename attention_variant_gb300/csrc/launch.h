@@ -74,6 +74,9 @@ struct EvoParams {
     float *lse;             // [batch, head, sequence] or null
     int64_t l_sb, l_sh;
     int32_t *tile_counts;   // [batch][head][nq] or null
+    const void *kmask;      // MSA mask or null: key j of batch index b is removed where
+    int64_t km_sb, km_sk;   //   kmask[b * km_sb + j * km_sk] is zero (element strides)
+    int km_f32;             //   fp32 entries (else bf16)
     uint32_t *err_user;
     uint64_t timeout_ns;
 };

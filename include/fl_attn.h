@@ -195,6 +195,29 @@ fl_status fl_attn_fwd(const fl_tensor *q, const fl_tensor *k, const fl_tensor *v
                       const fl_attn_variant_desc *desc, const fl_tensor *bias,
                       const fl_tensor *gate, fl_stream_t stream);
 
+/*
+ * fl_attn_evoformer -- the Evoformer kinds over a batch of MSA stacks, with an
+ * optional MSA mask (AlphaFold2 context: talk notes, "End-to-end: AlphaFold2").
+ *
+ * desc->kind is FL_KIND_EVO_ROW or FL_KIND_EVO_COL; everything fl_attn_fwd
+ * says of those kinds holds per stack.  Shapes (bf16 unless noted):
+ *   q, k, v, gate, out  [B, N_seq, N_res, H, c]   (or [N_seq, N_res, H, c]: B = 1)
+ *   bias (row pass)     [B, H, N_res, N_res], or [H, N_res, N_res] shared by all stacks
+ *   msa_mask            NULL, or [B, N_seq, N_res] / [N_seq, N_res] shared, bf16 or
+ *                       fp32: where msa_mask[s, r] is 0 the entry is removed as a key --
+ *                       residue r for MSA row s in the row pass, MSA row s for residue
+ *                       r in the column pass.  A query row left with no key gives
+ *                       O = 0 and LSE = -inf.
+ *   lse                 NULL, or [B, N_seq, H, N_res] (row) / [B, N_res, H, N_seq] (col)
+ * The stack axis may have any stride that is a positive multiple of 16 bytes.
+ * Each stack is one kernel launch on `stream`.  Every argument is validated
+ * before the first launch.
+ */
+fl_status fl_attn_evoformer(const fl_tensor *q, const fl_tensor *k, const fl_tensor *v,
+                            const fl_tensor *out, const fl_tensor *lse,
+                            const fl_attn_variant_desc *desc, const fl_tensor *bias,
+                            const fl_tensor *gate, const fl_tensor *msa_mask, fl_stream_t stream);
+
 /* Query-block and key-tile sizes the kernel for `desc` uses (for the
  * visited-tile accounting).  Never touches the device. */
 fl_status fl_attn_tile_shape(const fl_attn_variant_desc *desc, int32_t head_dim,

@@ -44,6 +44,7 @@ class _Problem(ctypes.Structure):
         ("scale", ctypes.c_double),
         ("bias", ctypes.c_void_p), ("bias_stride", ctypes.c_int64 * 3),
         ("kv_len", ctypes.c_void_p),
+        ("key_mask", ctypes.c_void_p), ("key_mask_stride", ctypes.c_int64 * 2),
     ]
 
 
@@ -101,7 +102,7 @@ def _base_and_span(a: np.ndarray):
 
 def attention(q, k, v, *, mod="none", softcap=20.0, alibi_slopes=None, mask="none",
               window=0, prefix=0, doc_offsets=None, scale=0.0, bias=None, kv_len=None,
-              rows=None, nthreads=0, lib=None):
+              key_mask=None, rows=None, nthreads=0, lib=None):
     """Attention forward of ``q [B,Sq,Hq,D]``, ``k [B,Sk,Hk,D]``, ``v [B,Sk,Hk,Dv]``.
 
     ``bias`` (optional) is ``[Hq, Sq, Sk]`` bf16 bits.  ``doc_offsets`` is the
@@ -109,6 +110,8 @@ def attention(q, k, v, *, mod="none", softcap=20.0, alibi_slopes=None, mask="non
     ``kv_len`` (masks ``kv_len`` and ``decode``) holds each batch element's
     cache length; the decode mask puts the ``Sq`` query rows at the last
     ``Sq`` positions of that length.
+    ``key_mask`` (optional, ``[B, Sk]``) removes key j of batch element b
+    where it is zero, on top of ``mask``.
     ``rows`` (optional) is an ``[n, 3]`` array of ``(b, h, i)``; then the
     result is ``O [n, Dv]`` and ``LSE [n]``, else ``O [B,Sq,Hq,Dv]`` and
     ``LSE [B,Hq,Sq]``.
@@ -146,6 +149,13 @@ def attention(q, k, v, *, mod="none", softcap=20.0, alibi_slopes=None, mask="non
             raise ValueError("kv_len must have one entry per batch element")
         keep.append(kl)
         p.kv_len = kl.ctypes.data
+    if key_mask is not None:
+        km = np.ascontiguousarray(np.asarray(key_mask) != 0, dtype=np.uint8)
+        if km.shape != (B, Sk):
+            raise ValueError("key_mask must be [B, Sk]")
+        keep.append(km)
+        p.key_mask = km.ctypes.data
+        p.key_mask_stride[:] = (Sk, 1)
     if bias is not None:
         if bias.dtype != np.uint16 or bias.shape != (Hq, Sq, Sk):
             raise ValueError("bias must be [Hq, Sq, Sk] bf16 bits")
@@ -191,17 +201,19 @@ def sigmoid_bf16(g):
     return 1.0 / (1.0 + np.exp(-x.astype(np.float64)))
 
 
-def evo_row(q, k, v, bias, gate, *, rows=None, nthreads=0, lib=None):
+def evo_row(q, k, v, bias, gate, *, msa_mask=None, rows=None, nthreads=0, lib=None):
     """Evoformer row-wise gated self-attention with pair bias.
 
     ``q, k, v, gate`` are ``[N_seq, N_res, H, c]``; ``bias`` is
     ``[H, N_res, N_res]`` shared by every MSA row.  For each MSA row s and head
     h, attention runs over residues with ``b[h, i, j]`` added to the logits;
     the output is gated by ``sigmoid(g[s, i, h, :])`` (talk notes, "End-to-end:
-    AlphaFold2"; shapes from the workload statement).  With ``rows`` the triples
-    are ``(s, h, i)``.
+    AlphaFold2"; shapes from the workload statement).  ``msa_mask``
+    (optional, ``[N_seq, N_res]``) removes residue j as a key of MSA row s
+    where it is zero.  With ``rows`` the triples are ``(s, h, i)``.
     """
-    o, lse = attention(q, k, v, bias=bias, rows=rows, nthreads=nthreads, lib=lib)
+    o, lse = attention(q, k, v, bias=bias, key_mask=msa_mask, rows=rows, nthreads=nthreads,
+                       lib=lib)
     if rows is None:
         o = o * sigmoid_bf16(gate)
     else:
@@ -210,16 +222,19 @@ def evo_row(q, k, v, bias, gate, *, rows=None, nthreads=0, lib=None):
     return o, lse
 
 
-def evo_col(q, k, v, gate, *, rows=None, nthreads=0, lib=None):
+def evo_col(q, k, v, gate, *, msa_mask=None, rows=None, nthreads=0, lib=None):
     """Evoformer column-wise gated self-attention (no bias).
 
     Attention for each residue r and head h runs over the MSA rows (axis 0) of
     the same ``[N_seq, N_res, H, c]`` tensors; the gate is the same
-    ``sigmoid(g[s, r, h, :])``.  Results are laid out ``O [N_res, N_seq, H, c]``
-    and ``LSE [N_res, H, N_seq]``; with ``rows`` the triples are ``(r, h, s)``.
+    ``sigmoid(g[s, r, h, :])``.  ``msa_mask`` (optional, ``[N_seq, N_res]``)
+    removes MSA row t as a key of residue r where ``msa_mask[t, r]`` is zero.
+    Results are laid out ``O [N_res, N_seq, H, c]`` and ``LSE [N_res, H, N_seq]``;
+    with ``rows`` the triples are ``(r, h, s)``.
     """
     qt, kt, vt = (np.swapaxes(x, 0, 1) for x in (q, k, v))
-    o, lse = attention(qt, kt, vt, rows=rows, nthreads=nthreads, lib=lib)
+    km = None if msa_mask is None else np.swapaxes(np.asarray(msa_mask), 0, 1)
+    o, lse = attention(qt, kt, vt, key_mask=km, rows=rows, nthreads=nthreads, lib=lib)
     gt = np.swapaxes(gate, 0, 1)
     if rows is None:
         o = o * sigmoid_bf16(gt)

@@ -38,6 +38,10 @@
  *              (the Sq query rows are the last Sq positions of a sequence of
  *              kv_len[b] tokens: serving with a KV cache, talk notes,
  *              "End-to-end: LLaMA-3.2-1B (vLLM / Mooncake)", causal variant)
+ *   key mask (any of the above, and)  key j of batch element b allowed only if
+ *              key_mask[b][j] != 0  (the Evoformer MSA mask: a masked residue or
+ *              sequence is removed as a key; AlphaFold2 context, talk notes,
+ *              "End-to-end: AlphaFold2")
  * Query head h reads key/value head h / (Hq / Hk) (contiguous GQA groups).
  */
 #include <math.h>
@@ -78,6 +82,8 @@ typedef struct {
     const uint16_t *bias;       /* NULL, or bias[h, i, j] with the strides below */
     int64_t bias_stride[3];
     const int32_t *kv_len;      /* [B] cache lengths (KV-length and decode masks) */
+    const uint8_t *key_mask;    /* NULL, or key_mask[b, j] with the strides below */
+    int64_t key_mask_stride[2];
 } fl_oracle_problem;
 
 static double widen_bf16(uint16_t bits)
@@ -101,6 +107,8 @@ static int32_t doc_of(const int32_t *starts, int32_t n, int32_t x)
 
 static int allowed(const fl_oracle_problem *p, int32_t b, int64_t i, int64_t j)
 {
+    if (p->key_mask && !p->key_mask[b * p->key_mask_stride[0] + j * p->key_mask_stride[1]])
+        return 0;
     switch (p->mask) {
     case FL_ORACLE_MASK_NONE:
         return 1;

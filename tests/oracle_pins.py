@@ -414,6 +414,53 @@ def pin_decode(lib):
            what="SDPA decode softcap")
 
 
+def pin_key_mask(lib):
+    """The MSA key mask: removing a key by the mask equals deleting it from K,
+    V and the bias (row and column passes), constant scores average V over the
+    kept keys, an all-ones mask changes nothing, and a row with every key
+    removed gives O = 0 and LSE = -inf."""
+    Ns, Nr, H, c = 3, 90, 2, 32
+    q, k, v = _rand((Ns, Nr, H, c), "mq"), _rand((Ns, Nr, H, c), "mk"), _rand((Ns, Nr, H, c), "mv")
+    bias = _rand((H, Nr, Nr), "mb")
+    rng = np.random.default_rng(5)
+    mask = (rng.random((Ns, Nr)) > 0.3).astype(np.float32)
+    mask[:, 0] = 1.0  # every MSA row keeps a residue
+    mask[0, :] = 1.0  # every residue keeps an MSA row
+    o, l = oracle.attention(q, k, v, bias=bias, key_mask=mask, lib=lib)
+    for s in range(Ns):
+        keep = np.nonzero(mask[s])[0]
+        o2, l2 = oracle.attention(q[s:s + 1], np.ascontiguousarray(k[s:s + 1, keep]),
+                                  np.ascontiguousarray(v[s:s + 1, keep]),
+                                  bias=np.ascontiguousarray(bias[:, :, keep]), lib=lib)
+        _close(o[s], o2[0], what=f"row pass, masked keys deleted (row {s})")
+        _close(l[s], l2[0], what=f"row pass LSE (row {s})")
+    # column pass: residue r attends over MSA rows t with mask[t, r] != 0
+    g = _bf(np.zeros((Ns, Nr, H, c)))  # sigmoid(0) = 1/2 everywhere
+    oc, lc = oracle.evo_col(q, k, v, g, msa_mask=mask, lib=lib)
+    for r in (0, 7, 50, 89):
+        keep = np.nonzero(mask[:, r])[0]
+        o2, l2 = oracle.attention(np.ascontiguousarray(q[:, r:r + 1].swapaxes(0, 1)),
+                                  np.ascontiguousarray(k[keep, r:r + 1].swapaxes(0, 1)),
+                                  np.ascontiguousarray(v[keep, r:r + 1].swapaxes(0, 1)), lib=lib)
+        _close(oc[r], 0.5 * o2[0], what=f"column pass, masked rows deleted (residue {r})")
+        _close(lc[r], l2[0], what=f"column pass LSE (residue {r})")
+    # constant scores: the mean of V over the kept keys
+    z = _bf(np.zeros((Ns, Nr, H, c)))
+    o, l = oracle.attention(z, k, v, key_mask=mask, lib=lib)
+    vf = _f64(v)
+    for s in range(Ns):
+        keep = mask[s] != 0
+        _close(o[s], np.broadcast_to(vf[s, keep].mean(axis=0), o[s].shape), what="constant scores")
+        _close(l[s], math.log(keep.sum()), what="constant scores LSE")
+    # all ones = no mask; a row with every key removed
+    o1, l1 = oracle.attention(q, k, v, bias=bias, key_mask=np.ones((Ns, Nr)), lib=lib)
+    o0, l0 = oracle.attention(q, k, v, bias=bias, lib=lib)
+    _close(o1, o0, what="all-ones mask")
+    mask[1] = 0.0
+    o, l = oracle.attention(q, k, v, bias=bias, key_mask=mask, lib=lib)
+    assert np.all(o[1] == 0.0) and np.all(np.isneginf(l[1])), "fully removed row"
+
+
 def pin_score_expr(lib):
     """The score_mod-expression oracle (numpy, float64) against the C oracle's
     built-in variants written as expressions, against a closed form, on rows
@@ -462,4 +509,4 @@ def pin_score_expr(lib):
 ALL_PINS = [pin_constant_scores, pin_alibi_geometric, pin_softcap_two_keys, pin_one_hot,
             pin_rows_sum_to_one, pin_shift_invariance, pin_permutation, pin_causal_row0,
             pin_sdpa, pin_reductions, pin_rows_api, pin_diff, pin_evo, pin_fully_masked_row,
-            pin_decode, pin_score_expr]
+            pin_decode, pin_key_mask, pin_score_expr]

@@ -234,3 +234,25 @@ def test_score_expr_refused_before_device(lib):
     d = fa.make_desc(kind="evo_row", score_expr="score")
     assert _call(lib, _t((4, 64, 8, 32)), _t((4, 64, 8, 32)), _t((4, 64, 8, 32)),
                  _t((4, 64, 8, 32)), desc=d) != fa.FL_OK
+
+
+def test_evoformer_batched_validation_before_device(lib):
+    Bt, Ns, Nr, H, c = 2, 4, 64, 2, 32
+    t5 = lambda: _t((Bt, Ns, Nr, H, c))
+    r = lambda x: ctypes.byref(x) if x is not None else None
+
+    def call(q=None, k=None, bias=None, mask=None, kind="evo_row"):
+        d = fa.make_desc(kind=kind)
+        q, k = q or t5(), k or t5()
+        return lib.fl_attn_evoformer(r(q), r(k), r(t5()), r(t5()), None, ctypes.byref(d), r(bias),
+                                     r(t5()), r(mask), None)
+
+    assert call(kind="standard") == fa.FL_ERR_INVALID_ARG
+    assert call(k=_t((Bt + 1, Ns, Nr, H, c))) == fa.FL_ERR_INVALID_ARG
+    assert "stacks" in fa.fl_attn_last_error()
+    assert call(bias=_t((Bt, H, Nr, Nr)), mask=_t((Bt, Ns, Nr + 1), dtype=fa.FL_F32)) == \
+        fa.FL_ERR_INVALID_ARG
+    assert call(bias=_t((H, Nr, Nr)), mask=_t((Ns, Nr, 1, 1), dtype=fa.FL_F32)) == \
+        fa.FL_ERR_INVALID_ARG
+    odd = _t((Bt, Ns, Nr, H, c), strides=(Ns * Nr * H * c + 4, Nr * H * c, H * c, c, 1))
+    assert call(q=odd) == fa.FL_ERR_ALIGNMENT

@@ -37,6 +37,9 @@ MUTANTS = {
     "kv_len_inclusive": ("return j < p->kv_len[b];", "return j <= p->kv_len[b];"),
     "decode_position_off_by_one": ("j <= (int64_t)p->kv_len[b] - p->Sq + i", "j < (int64_t)p->kv_len[b] - p->Sq + i"),
     "decode_rows_from_start": ("j <= (int64_t)p->kv_len[b] - p->Sq + i", "j <= i"),
+    "key_mask_inverted": ("if (p->key_mask && !p->key_mask[", "if (p->key_mask && p->key_mask["),
+    "key_mask_axes_swapped": ("b * p->key_mask_stride[0] + j * p->key_mask_stride[1]",
+                              "j * p->key_mask_stride[0] + b * p->key_mask_stride[1]"),
 }
 
 
