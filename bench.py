@@ -151,6 +151,22 @@ def evo_entry(row):
                 bytes=5 * tensor_bytes + (H * Nr * Nr * 2 if row else 0))
 
 
+def evo_batched_entry(row):
+    """A batch of MSA stacks with an MSA mask, through fl_attn_evoformer."""
+    w = workloads.EVO_AF2
+    Bt, Ns, Nr, H, c = w["B"], w["N_seq"], w["N_res"], w["H"], w["c"]
+    mask = np.ones((Bt, Ns, Nr), dtype=np.float32)
+    mask[:, :, Nr - w["pad_res"]:] = 0.0  # padding residues
+    mask[:, Ns - w["pad_seq"]:, :] = 0.0  # padding MSA rows
+    kept = mask.sum(axis=2) if row else mask.sum(axis=1)  # keys per (stack, batch index)
+    q_rows = Nr if row else Ns
+    pairs = int(kept.sum()) * H * q_rows
+    tensor_bytes = Bt * Ns * Nr * H * c * 2
+    return dict(name=w["name"], kind="evo_batched", row=row, variant="row_masked" if row else "col_masked",
+                Bt=Bt, Ns=Ns, Nr=Nr, H=H, c=c, mask=mask, pairs=pairs, flops=pairs * 4 * c,
+                bytes=5 * tensor_bytes + (Bt * H * Nr * Nr * 2 if row else 0) + mask.size * 4)
+
+
 def decode_entry(mod):
     """The serving workload: one new token per sequence against a paged cache."""
     w = workloads.DECODE
@@ -371,6 +387,38 @@ def time_other(e, torch, fa, device, steps, warmup, flush, stream):
     return [a.elapsed_time(b) for a, b in evs]
 
 
+def time_evo_batched(e, torch, fa, device, steps, warmup, flush, stream):
+    """Device time of fl_attn_evoformer over the batch of masked stacks (one
+    launch per stack, all inside the timed region)."""
+    to = lambda b: torch.from_numpy(b.view(np.int16)).view(torch.bfloat16).to(device)
+    shape = (e["Bt"], e["Ns"], e["Nr"], e["H"], e["c"])
+    q, k, v, g = (to(testdata.normal_bf16(shape, e["name"], n)) for n in "qkvg")
+    bias = to(testdata.normal_bf16((e["Bt"], e["H"], e["Nr"], e["Nr"]), e["name"], "bias")) \
+        if e["row"] else None
+    mask = torch.from_numpy(e["mask"]).to(device)
+    out = torch.empty_like(q)
+    desc = fa.make_desc(kind="evo_row" if e["row"] else "evo_col")
+    flushed = l2_policy(e).startswith("flushed")
+    with torch.cuda.stream(stream):
+        for _ in range(warmup):
+            if flushed:
+                flush.zero_()
+            fa.fl_attn_evoformer(q, k, v, out, None, desc, bias=bias, gate=g, msa_mask=mask,
+                                 stream=stream)
+        torch.cuda.synchronize()
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(steps)]
+        for a, b in evs:
+            if flushed:
+                flush.zero_()
+            a.record(stream)
+            fa.fl_attn_evoformer(q, k, v, out, None, desc, bias=bias, gate=g, msa_mask=mask,
+                                 stream=stream)
+            b.record(stream)
+        torch.cuda.synchronize()
+    return [a.elapsed_time(b) for a, b in evs]
+
+
 def time_decode(e, torch, fa, device, steps, warmup, flush, stream):
     """Device time of the decode kernel on its workload (paged cache, pages of
     each sequence scattered over the pool)."""
@@ -507,7 +555,8 @@ ONLY = {"diff": lambda: diff_entry("none"), "diff_causal": lambda: diff_entry("c
         "decode": lambda: decode_entry("none"), "decode_softcap": lambda: decode_entry("softcap"),
         "softcap": lambda: entry("mha", 2048, "softcap"), "alibi": lambda: entry("mha", 2048, "alibi"),
         "expr_softcap": lambda: expr_entry(2048, "expr_softcap"),
-        "expr_alibi": lambda: expr_entry(2048, "expr_alibi")}
+        "expr_alibi": lambda: expr_entry(2048, "expr_alibi"),
+        "evo_af2_row": lambda: evo_batched_entry(True), "evo_af2_col": lambda: evo_batched_entry(False)}
 
 
 def run_only(args):
@@ -524,7 +573,7 @@ def run_only(args):
         ms = statistics.mean(time_entry(e, gpu_inputs(e, torch, device), torch, fa, device, args.steps,
                                         args.warmup, flush, stream)[0])
     else:
-        timer = time_decode if e["kind"] == "decode" else time_other
+        timer = {"decode": time_decode, "evo_batched": time_evo_batched}.get(e["kind"], time_other)
         ms = statistics.mean(timer(e, torch, fa, device, args.steps, args.warmup, flush, stream))
     print(json.dumps({"only": args.only, "ms": round(ms, 4),
                       "tflops": round(e["flops"] / (ms * 1e-3) / 1e12, 1),
@@ -584,6 +633,13 @@ def run_ours(args):
                 rec["frac_hbm"] = round(gbs / peaks["hbm_gbs"], 4)
             rec["l2"] = l2_policy(e)
             variants[f"{e['name']}/{e['variant']}"] = rec
+        for e in (evo_batched_entry(True), evo_batched_entry(False)):
+            vm = statistics.mean(time_evo_batched(e, torch, fa, device, args.variant_steps, 2, flush,
+                                                  stream))
+            gbs = e["bytes"] / (vm * 1e-3) / 1e9
+            variants[f"{e['name']}/{e['variant']}"] = dict(
+                tflops=round(e["flops"] / (vm * 1e-3) / 1e12, 1), ms=round(vm, 4), gbs=round(gbs, 1),
+                frac_hbm=round(gbs / peaks["hbm_gbs"], 4), l2=l2_policy(e))
         for e in (decode_entry("none"), decode_entry("softcap")):
             vm = statistics.mean(time_decode(e, torch, fa, device, args.variant_steps, 2, flush, stream))
             gbs = e["bytes"] / (vm * 1e-3) / 1e9

@@ -116,3 +116,30 @@ def test_batched_shape_errors_launch_nothing():
                              gate=gu.dev(g))
     torch.cuda.synchronize()
     assert bool((out == 7.0).all()), "a rejected call wrote the output"
+
+
+@pytest.mark.parametrize("row", [True, False])
+def test_af2_batched_workload_sampled_rows(row):
+    # the benchmark's batch of masked AlphaFold2-sized stacks, at full size;
+    # sampled rows of two stacks against the oracle
+    import bench
+
+    e = bench.evo_batched_entry(row)
+    Bt, Ns, Nr, H, c = e["Bt"], e["Ns"], e["Nr"], e["H"], e["c"]
+    shape = (Bt, Ns, Nr, H, c)
+    q, k, v, g = (testdata.normal_bf16(shape, e["name"], n) for n in "qkvg")
+    bias = testdata.normal_bf16((Bt, H, Nr, Nr), e["name"], "bias") if row else None
+    o, lse = _run(row, q, k, v, g, bias, e["mask"])
+    B, S = (Ns, Nr) if row else (Nr, Ns)
+    rng = np.random.default_rng(3)
+    for b in (0, Bt - 1):
+        rows = np.stack([rng.integers(0, B, 48), rng.integers(0, H, 48), rng.integers(0, S, 48)], 1)
+        if row:
+            oref, lref = oracle.evo_row(q[b], k[b], v[b], bias[b], g[b], msa_mask=e["mask"][b],
+                                        rows=rows)
+            og = o[b][rows[:, 0], rows[:, 2], rows[:, 1]]
+        else:
+            oref, lref = oracle.evo_col(q[b], k[b], v[b], g[b], msa_mask=e["mask"][b], rows=rows)
+            og = o[b][rows[:, 2], rows[:, 0], rows[:, 1]]
+        lg = lse[b][rows[:, 0], rows[:, 1], rows[:, 2]]
+        gu.compare(og, lg, oref, lref, what=f"af2 {'row' if row else 'col'} stack {b}")
