@@ -116,6 +116,12 @@ def load_library(path: str = LIB_PATH):
     lib.fl_attn_last_error.restype = ctypes.c_char_p
     lib.fl_attn_last_error.argtypes = []
     lib.fl_attn_version.restype = ctypes.c_int32
+    lib.fl_attn_bwd_workspace_size.restype = ctypes.c_int
+    lib.fl_attn_bwd_workspace_size.argtypes = [P(FlTensor), P(FlTensor), P(FlDesc),
+                                               P(ctypes.c_size_t)]
+    lib.fl_attn_bwd.restype = ctypes.c_int
+    lib.fl_attn_bwd.argtypes = [P(FlTensor)] * 9 + [P(FlDesc), ctypes.c_void_p, ctypes.c_size_t,
+                                                    ctypes.c_void_p]
     lib.fl_attn_evoformer.restype = ctypes.c_int
     lib.fl_attn_evoformer.argtypes = [P(FlTensor), P(FlTensor), P(FlTensor), P(FlTensor), P(FlTensor),
                                       P(FlDesc), P(FlTensor), P(FlTensor), P(FlTensor), ctypes.c_void_p]
@@ -191,6 +197,34 @@ def make_desc(kind="standard", score_mod="none", softcap=20.0, mask="none", wind
 
 def _ref(x):
     return ctypes.byref(x) if x is not None else None
+
+
+def fl_attn_bwd_workspace_size(q, k, desc: FlDesc) -> int:
+    """Bytes of workspace fl_attn_bwd needs for these shapes."""
+    lib = load_library()
+    n = ctypes.c_size_t()
+    st = lib.fl_attn_bwd_workspace_size(_ref(as_fl_tensor(q)), _ref(as_fl_tensor(k)), ctypes.byref(desc),
+                                        ctypes.byref(n))
+    if st != FL_OK:
+        raise FlAttnError(st, fl_attn_last_error())
+    return n.value
+
+
+def fl_attn_bwd(q, k, v, out, lse, dout, dq, dk, dv, desc: FlDesc, workspace, stream=None) -> None:
+    """Enqueue the backward (see include/fl_attn.h); workspace is a device torch
+    tensor of at least fl_attn_bwd_workspace_size bytes."""
+    lib = load_library()
+    if stream is None:
+        import torch
+        stream = torch.cuda.current_stream().cuda_stream
+    elif hasattr(stream, "cuda_stream"):
+        stream = stream.cuda_stream
+    t = [as_fl_tensor(x) for x in (q, k, v, out, lse, dout, dq, dk, dv)]
+    st = lib.fl_attn_bwd(*[_ref(x) for x in t], ctypes.byref(desc),
+                         ctypes.c_void_p(workspace.data_ptr()),
+                         workspace.numel() * workspace.element_size(), ctypes.c_void_p(stream))
+    if st != FL_OK:
+        raise FlAttnError(st, fl_attn_last_error())
 
 
 def fl_attn_evoformer(q, k, v, out, lse, desc: FlDesc, bias=None, gate=None, msa_mask=None,

@@ -781,9 +781,161 @@ fl_status decode_run(const DecodePlan &pl, const fl_tensor *out, const fl_tensor
     return ok();
 }
 
+// ------------------------------------------------------------------ backward
+
+struct BwdPlan {
+    View Q, K, V;
+    int64_t B, S, Hq, Hk, S_pad;
+    size_t total;
+};
+
+fl_status bwd_plan(const fl_tensor *q, const fl_tensor *k, const fl_tensor *v,
+                   const fl_attn_variant_desc *d, BwdPlan &pl)
+{
+    fl_status s;
+    if (!d)
+        return fail(FL_ERR_INVALID_ARG, "desc is NULL");
+    if ((s = check_tensor(q, "q", 4, FL_BF16, pl.Q)) != FL_OK) return s;
+    if ((s = check_tensor(k, "k", 4, FL_BF16, pl.K)) != FL_OK) return s;
+    if (v) {
+        if ((s = check_tensor(v, "v", 4, FL_BF16, pl.V)) != FL_OK) return s;
+        if (!same(pl.V, {pl.K.size[0], pl.K.size[1], pl.K.size[2], pl.K.size[3]}))
+            return fail(FL_ERR_INVALID_ARG, "v must have the shape of k");
+    }
+    pl.B = pl.Q.size[0];
+    pl.S = pl.Q.size[1];
+    pl.Hq = pl.Q.size[2];
+    pl.Hk = pl.K.size[2];
+    if (pl.K.size[0] != pl.B || pl.K.size[1] != pl.S)
+        return fail(FL_ERR_INVALID_ARG, "k must be [B, S, Hk, D] matching q");
+    if (pl.Q.size[3] != 64 || pl.K.size[3] != 64)
+        return fail(FL_ERR_UNSUPPORTED, "the backward supports head dimension 64");
+    if (pl.Hq % pl.Hk != 0)
+        return fail(FL_ERR_INVALID_ARG, "Hq (%lld) must be a multiple of Hk (%lld)",
+                    (long long)pl.Hq, (long long)pl.Hk);
+    if (d->kind != FL_KIND_STANDARD)
+        return fail(FL_ERR_UNSUPPORTED, "the backward supports the standard kind");
+    if (d->score_mod != FL_MOD_NONE)
+        return fail(FL_ERR_UNSUPPORTED, "the backward supports score_mod none");
+    if (d->mask != FL_MASK_NONE && d->mask != FL_MASK_CAUSAL)
+        return fail(FL_ERR_UNSUPPORTED, "the backward supports mask none or causal");
+    if (d->gqa_group != 0 && d->gqa_group != pl.Hq / pl.Hk)
+        return fail(FL_ERR_INVALID_ARG, "gqa_group does not match Hq / Hk");
+    if (!std::isfinite(d->scale) || d->scale < 0.f)
+        return fail(FL_ERR_INVALID_ARG, "scale must be finite and positive (0 selects 1/sqrt(D))");
+    pl.S_pad = (pl.S + fl::kBwdBlock - 1) / fl::kBwdBlock * fl::kBwdBlock;
+    pl.total = (size_t(pl.B) * size_t(pl.Hq) * size_t(pl.S_pad) * 8 + 255) / 256 * 256;
+    return FL_OK;
+}
+
 } // namespace
 
 extern "C" {
+
+fl_status fl_attn_bwd_workspace_size(const fl_tensor *q, const fl_tensor *k,
+                                     const fl_attn_variant_desc *desc, size_t *bytes)
+{
+    if (!bytes)
+        return fail(FL_ERR_INVALID_ARG, "bytes is NULL");
+    BwdPlan pl;
+    const fl_status s = bwd_plan(q, k, nullptr, desc, pl);
+    if (s != FL_OK)
+        return s;
+    *bytes = pl.total;
+    return ok();
+}
+
+fl_status fl_attn_bwd(const fl_tensor *q, const fl_tensor *k, const fl_tensor *v,
+                      const fl_tensor *out, const fl_tensor *lse, const fl_tensor *dout,
+                      const fl_tensor *dq, const fl_tensor *dk, const fl_tensor *dv,
+                      const fl_attn_variant_desc *desc, void *workspace, size_t workspace_bytes,
+                      fl_stream_t stream)
+{
+    if (!v)
+        return fail(FL_ERR_INVALID_ARG, "v is NULL");
+    BwdPlan pl;
+    fl_status s = bwd_plan(q, k, v, desc, pl);
+    if (s != FL_OK)
+        return s;
+    View O, DO, DQ, DK, DV, L;
+    if ((s = check_tensor(out, "out", 4, FL_BF16, O)) != FL_OK) return s;
+    if ((s = check_tensor(dout, "dout", 4, FL_BF16, DO)) != FL_OK) return s;
+    if ((s = check_tensor(dq, "dq", 4, FL_BF16, DQ)) != FL_OK) return s;
+    if ((s = check_tensor(dk, "dk", 4, FL_BF16, DK)) != FL_OK) return s;
+    if ((s = check_tensor(dv, "dv", 4, FL_BF16, DV)) != FL_OK) return s;
+    if ((s = check_tensor(lse, "lse", 3, FL_F32, L)) != FL_OK) return s;
+    for (const View *t : {&O, &DO, &DQ})
+        if (!same(*t, {pl.B, pl.S, pl.Hq, 64}))
+            return fail(FL_ERR_INVALID_ARG, "out, dout and dq must be [B, S, Hq, 64]");
+    for (const View *t : {&DK, &DV})
+        if (!same(*t, {pl.B, pl.S, pl.Hk, 64}))
+            return fail(FL_ERR_INVALID_ARG, "dk and dv must be [B, S, Hk, 64]");
+    if (!same(L, {pl.B, pl.Hq, pl.S}))
+        return fail(FL_ERR_INVALID_ARG, "lse must be [B, Hq, S]");
+    if (!workspace)
+        return fail(FL_ERR_INVALID_ARG, "workspace is NULL");
+    if (reinterpret_cast<uintptr_t>(workspace) % kWsAlign)
+        return fail(FL_ERR_ALIGNMENT, "workspace is not %zu-byte aligned", kWsAlign);
+    if (workspace_bytes < pl.total)
+        return fail(FL_ERR_INVALID_ARG, "workspace holds %zu bytes, %zu needed", workspace_bytes, pl.total);
+    int dev;
+    DeviceInfo info;
+    if ((s = device_info(dev, info)) != FL_OK) return s;
+
+    // [64 features, S, heads, B] maps, boxes of 64 rows
+    CUtensorMap tq, tdo, tk, tv;
+    const uint32_t box[4] = {64, uint32_t(fl::kBwdBlock), 1, 1};
+    const View *src[4] = {&pl.Q, &DO, &pl.K, &pl.V};
+    CUtensorMap *dst[4] = {&tq, &tdo, &tk, &tv};
+    const char *names[4] = {"q", "dout", "k", "v"};
+    for (int m = 0; m < 4; ++m) {
+        const View &T = *src[m];
+        const uint64_t dims[4] = {64, uint64_t(pl.S), uint64_t(T.size[2]), uint64_t(pl.B)};
+        const uint64_t st[3] = {uint64_t(T.stride[1]) * 2, uint64_t(T.stride[2]) * 2,
+                                uint64_t(T.stride[0]) * 2};
+        if ((s = make_map(*dst[m], T.ptr, 4, dims, st, box, CU_TENSOR_MAP_SWIZZLE_128B, names[m])) != FL_OK)
+            return s;
+    }
+    fl::BwdParams p{};
+    p.B = int(pl.B);
+    p.Hq = int(pl.Hq);
+    p.Hk = int(pl.Hk);
+    p.S = int(pl.S);
+    p.S_pad = int(pl.S_pad);
+    p.causal = desc->mask == FL_MASK_CAUSAL;
+    p.scale = desc->scale != 0.f ? desc->scale : 0.125f; // 1 / sqrt(64)
+    auto strides3 = [](const View &t, int64_t &sb, int64_t &ss, int64_t &sh) {
+        sb = t.stride[0];
+        ss = t.stride[1];
+        sh = t.stride[2];
+    };
+    p.q = static_cast<const __nv_bfloat16 *>(pl.Q.ptr);
+    strides3(pl.Q, p.q_sb, p.q_ss, p.q_sh);
+    p.k = static_cast<const __nv_bfloat16 *>(pl.K.ptr);
+    strides3(pl.K, p.k_sb, p.k_ss, p.k_sh);
+    p.v = static_cast<const __nv_bfloat16 *>(pl.V.ptr);
+    strides3(pl.V, p.v_sb, p.v_ss, p.v_sh);
+    p.o = static_cast<const __nv_bfloat16 *>(O.ptr);
+    strides3(O, p.o_sb, p.o_ss, p.o_sh);
+    p.dout = static_cast<const __nv_bfloat16 *>(DO.ptr);
+    strides3(DO, p.do_sb, p.do_ss, p.do_sh);
+    p.lse = static_cast<const float *>(L.ptr);
+    p.l_sb = L.stride[0];
+    p.l_sh = L.stride[1];
+    p.dq = static_cast<__nv_bfloat16 *>(DQ.ptr);
+    strides3(DQ, p.dq_sb, p.dq_ss, p.dq_sh);
+    p.dk = static_cast<__nv_bfloat16 *>(DK.ptr);
+    strides3(DK, p.dk_sb, p.dk_ss, p.dk_sh);
+    p.dv = static_cast<__nv_bfloat16 *>(DV.ptr);
+    strides3(DV, p.dv_sb, p.dv_ss, p.dv_sh);
+    p.ws_stats = static_cast<float *>(workspace);
+    p.err_user = desc->error_word;
+    p.timeout_ns = timeout_ns(desc);
+    const cudaError_t e = fl::launch_bwd(tq, tdo, tk, tv, p, reinterpret_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess)
+        return fail(FL_ERR_CUDA, "kernel launch failed: %s", cudaGetErrorString(e));
+    return ok();
+}
 
 // Stacks of a batch run one launch each (every launch alone fills the GPU at
 // AlphaFold2 sizes: N_seq x H x ceil(N_res / 128) work items for the row pass).

@@ -81,6 +81,25 @@ struct EvoParams {
     uint64_t timeout_ns;
 };
 
+// ---- backward of the standard kind (bwd_standard.cu)
+constexpr int kBwdBlock = 64; // query / key rows per tile
+
+struct BwdParams {
+    int B, Hq, Hk, S, S_pad;      // S_pad: S rounded up to kBwdBlock
+    int causal;
+    float scale;
+    const __nv_bfloat16 *q, *k, *v, *o, *dout; // element strides (batch, position, head):
+    int64_t q_sb, q_ss, q_sh, k_sb, k_ss, k_sh, v_sb, v_ss, v_sh;
+    int64_t o_sb, o_ss, o_sh, do_sb, do_ss, do_sh;
+    const float *lse;             // [B, Hq, S] natural log
+    int64_t l_sb, l_sh;
+    __nv_bfloat16 *dq, *dk, *dv;
+    int64_t dq_sb, dq_ss, dq_sh, dk_sb, dk_ss, dk_sh, dv_sb, dv_ss, dv_sh;
+    float *ws_stats;              // [B][Hq][S_pad] x (LSE log2 e, rowsum(dO O))
+    uint32_t *err_user;
+    uint64_t timeout_ns;
+};
+
 // ---- serving with a KV cache (fwd_decode.cu)
 constexpr int kDecodeChunk = 128; // keys per pipeline stage
 constexpr int kDecodeMaxSplitChunks = 8; // chunks per CTA (split) at most
@@ -121,6 +140,8 @@ cudaError_t decode_static_scratch(void **ptr);
 cudaError_t launch_evo(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
                        const CUtensorMap &tb, const EvoParams &p, int grid, cudaStream_t stream);
 int evo_max_bias_keys();
+cudaError_t launch_bwd(const CUtensorMap &tq, const CUtensorMap &tdo, const CUtensorMap &tk,
+                       const CUtensorMap &tv, const BwdParams &p, cudaStream_t stream);
 #endif
 
 // Keys per K/V tile of the standard kernel (its TMEM budget: see fwd_standard.cu),

@@ -167,6 +167,45 @@ def evo_batched_entry(row):
                 bytes=5 * tensor_bytes + (Bt * H * Nr * Nr * 2 if row else 0) + mask.size * 4)
 
 
+def bwd_entry(mask):
+    """The backward (dQ, dK, dV) on the headline MHA workload; algorithmic
+    flops 10 D per unmasked pair (the five products of the gradient)."""
+    e = entry("mha", HEADLINE["S"], "causal" if mask == "causal" else "vanilla")
+    e.update(kind="bwd", variant="bwd_" + ("causal" if mask == "causal" else "vanilla"),
+             flops=10 * e["D"] * e["pairs"],
+             bytes=2 * e["B"] * e["S"] * e["D"] * (4 * e["Hq"] + 4 * e["Hk"]) + 4 * e["B"] * e["Hq"] * e["S"])
+    return e
+
+
+def time_bwd(e, torch, fa, device, steps, warmup, flush, stream):
+    """Device time of fl_attn_bwd (its three launches) on the workload."""
+    B, S, Hq, Hk, D = e["B"], e["S"], e["Hq"], e["Hk"], e["D"]
+    q, k, v = gpu_inputs(e, torch, device)
+    q, k, v = q.to(device), k.to(device), v.to(device)
+    do = torch.from_numpy(testdata.normal_bf16((B, S, Hq, D), e["name"], "do").view(np.int16)) \
+        .view(torch.bfloat16).to(device)
+    out = torch.empty_like(q)
+    lse = torch.empty((B, Hq, S), dtype=torch.float32, device=device)
+    desc = fa.make_desc(mask=e["mask"])
+    fa.fl_attn_fwd(q, k, v, out, lse, desc)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    ws = torch.empty(fa.fl_attn_bwd_workspace_size(q, k, desc), dtype=torch.uint8, device=device)
+    with torch.cuda.stream(stream):
+        for _ in range(warmup):
+            flush.zero_()
+            fa.fl_attn_bwd(q, k, v, out, lse, do, dq, dk, dv, desc, ws, stream=stream)
+        torch.cuda.synchronize()
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(steps)]
+        for a, b in evs:
+            flush.zero_()
+            a.record(stream)
+            fa.fl_attn_bwd(q, k, v, out, lse, do, dq, dk, dv, desc, ws, stream=stream)
+            b.record(stream)
+        torch.cuda.synchronize()
+    return [a.elapsed_time(b) for a, b in evs]
+
+
 def decode_entry(mod):
     """The serving workload: one new token per sequence against a paged cache."""
     w = workloads.DECODE
@@ -556,7 +595,8 @@ ONLY = {"diff": lambda: diff_entry("none"), "diff_causal": lambda: diff_entry("c
         "softcap": lambda: entry("mha", 2048, "softcap"), "alibi": lambda: entry("mha", 2048, "alibi"),
         "expr_softcap": lambda: expr_entry(2048, "expr_softcap"),
         "expr_alibi": lambda: expr_entry(2048, "expr_alibi"),
-        "evo_af2_row": lambda: evo_batched_entry(True), "evo_af2_col": lambda: evo_batched_entry(False)}
+        "evo_af2_row": lambda: evo_batched_entry(True), "evo_af2_col": lambda: evo_batched_entry(False),
+        "bwd": lambda: bwd_entry("none"), "bwd_causal": lambda: bwd_entry("causal")}
 
 
 def run_only(args):
@@ -573,7 +613,8 @@ def run_only(args):
         ms = statistics.mean(time_entry(e, gpu_inputs(e, torch, device), torch, fa, device, args.steps,
                                         args.warmup, flush, stream)[0])
     else:
-        timer = {"decode": time_decode, "evo_batched": time_evo_batched}.get(e["kind"], time_other)
+        timer = {"decode": time_decode, "evo_batched": time_evo_batched,
+                 "bwd": time_bwd}.get(e["kind"], time_other)
         ms = statistics.mean(timer(e, torch, fa, device, args.steps, args.warmup, flush, stream))
     print(json.dumps({"only": args.only, "ms": round(ms, 4),
                       "tflops": round(e["flops"] / (ms * 1e-3) / 1e12, 1),
@@ -640,6 +681,12 @@ def run_ours(args):
             variants[f"{e['name']}/{e['variant']}"] = dict(
                 tflops=round(e["flops"] / (vm * 1e-3) / 1e12, 1), ms=round(vm, 4), gbs=round(gbs, 1),
                 frac_hbm=round(gbs / peaks["hbm_gbs"], 4), l2=l2_policy(e))
+        for e in (bwd_entry("none"), bwd_entry("causal")):
+            vm = statistics.mean(time_bwd(e, torch, fa, device, args.variant_steps, 2, flush, stream))
+            tf = e["flops"] / (vm * 1e-3) / 1e12
+            variants[f"{e['name']}/{e['variant']}"] = dict(
+                tflops=round(tf, 1), frac_peak=round(tf / peaks["bf16_tflops"], 4), ms=round(vm, 4),
+                gbs=round(e["bytes"] / (vm * 1e-3) / 1e9, 1), l2="flushed before every timed step (256 MiB write)")
         for e in (decode_entry("none"), decode_entry("softcap")):
             vm = statistics.mean(time_decode(e, torch, fa, device, args.variant_steps, 2, flush, stream))
             gbs = e["bytes"] / (vm * 1e-3) / 1e9

@@ -218,6 +218,29 @@ fl_status fl_attn_evoformer(const fl_tensor *q, const fl_tensor *k, const fl_ten
                             const fl_attn_variant_desc *desc, const fl_tensor *bias,
                             const fl_tensor *gate, const fl_tensor *msa_mask, fl_stream_t stream);
 
+/*
+ * fl_attn_bwd -- backward of the standard kind: dQ, dK, dV of
+ *     O = softmax(scale Q K^T + mask) V
+ * given the forward's out and (natural-log) lse and the output gradient
+ * dout.  The pages name the backward pass as the fused kernels' next step
+ * (gist.science summary, "Limitations and future work").  P is recomputed
+ * from Q, K and the LSE; dS = P (dP - D) with D_i = sum_d dout_id out_id.
+ *   q, out, dout, dq [B, S, Hq, 64]; k, v, dk, dv [B, S, Hk, 64]; lse [B, Hq, S] fp32
+ *   desc: kind FL_KIND_STANDARD, score_mod FL_MOD_NONE, mask FL_MASK_NONE or
+ *   FL_MASK_CAUSAL, scale (0: 1/8).  GQA heads are summed into dk, dv.
+ * `workspace`: device memory of at least fl_attn_bwd_workspace_size bytes,
+ * 256-byte aligned, owned by the caller, no initialisation needed.  Three
+ * kernel launches on `stream`; every output element is written once (no
+ * atomics: the result does not depend on scheduling).
+ */
+fl_status fl_attn_bwd_workspace_size(const fl_tensor *q, const fl_tensor *k,
+                                     const fl_attn_variant_desc *desc, size_t *bytes);
+fl_status fl_attn_bwd(const fl_tensor *q, const fl_tensor *k, const fl_tensor *v,
+                      const fl_tensor *out, const fl_tensor *lse, const fl_tensor *dout,
+                      const fl_tensor *dq, const fl_tensor *dk, const fl_tensor *dv,
+                      const fl_attn_variant_desc *desc, void *workspace, size_t workspace_bytes,
+                      fl_stream_t stream);
+
 /* Query-block and key-tile sizes the kernel for `desc` uses (for the
  * visited-tile accounting).  Never touches the device. */
 fl_status fl_attn_tile_shape(const fl_attn_variant_desc *desc, int32_t head_dim,

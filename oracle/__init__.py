@@ -251,3 +251,44 @@ def alibi_slopes(H: int) -> np.ndarray:
 
 if __name__ == "__main__":  # pragma: no cover
     print(build(force="--force" in sys.argv))
+
+
+def attention_bwd(q, k, v, dout, *, mask="none", scale=0.0):
+    """Gradients dQ, dK, dV (float64) of ``O = softmax(scale Q K^T + mask) V``
+    for ``q [B,S,Hq,D]``, ``k, v [B,S,Hk,D]`` and the output gradient
+    ``dout [B,S,Hq,D]`` (all bf16 bits), mask ``none`` or ``causal``.
+
+    The plain definition per (batch, query head): the full probability matrix
+    P (two-pass softmax), dV = P^T dO, dP = dO V^T, dS_ij = P_ij (dP_ij -
+    sum_l P_il dP_il), dQ = scale dS K, dK = scale dS^T Q; query heads sharing
+    a K/V head add their dK and dV (gist.science summary, "Limitations and
+    future work": the backward pass is the fused kernels' next step).
+    """
+    if mask not in ("none", "causal"):
+        raise ValueError("mask must be none or causal")
+    wid = lambda x: (np.asarray(x, dtype=np.uint16).astype(np.uint32) << 16).view(np.float32) \
+        .astype(np.float64)
+    Q, K, V, dO = wid(q), wid(k), wid(v), wid(dout)
+    B, S, Hq, D = Q.shape
+    Hk = K.shape[2]
+    G = Hq // Hk
+    s = scale if scale else 1.0 / np.sqrt(D)
+    dQ = np.zeros_like(Q)
+    dK = np.zeros_like(K)
+    dV = np.zeros_like(V)
+    causal = np.tril(np.ones((S, S), dtype=bool))
+    for b in range(B):
+        for h in range(Hq):
+            kh = h // G
+            z = s * (Q[b, :, h] @ K[b, :, kh].T)
+            if mask == "causal":
+                z = np.where(causal, z, -np.inf)
+            m = z.max(axis=1, keepdims=True)
+            e = np.exp(z - m)
+            P = e / e.sum(axis=1, keepdims=True)
+            dV[b, :, kh] += P.T @ dO[b, :, h]
+            dP = dO[b, :, h] @ V[b, :, kh].T
+            dS = P * (dP - (P * dP).sum(axis=1, keepdims=True))
+            dQ[b, :, h] = s * (dS @ K[b, :, kh])
+            dK[b, :, kh] += s * (dS.T @ Q[b, :, h])
+    return dQ, dK, dV

@@ -461,6 +461,50 @@ def pin_key_mask(lib):
     assert np.all(o[1] == 0.0) and np.all(np.isneginf(l[1])), "fully removed row"
 
 
+def pin_backward(lib):
+    """The backward oracle against float64 autograd of torch's
+    scaled_dot_product_attention (MHA and GQA, with and without the causal
+    mask, a non-default scale) and against central finite differences of the
+    loss sum(dO * O) on a tiny problem."""
+    for (B, S, Hq, Hk, D, mask, scale) in [(2, 37, 2, 2, 64, "none", 0.0), (1, 50, 4, 2, 64, "causal", 0.0),
+                                           (1, 20, 2, 1, 16, "causal", 0.3)]:
+        q, k, v = _rand((B, S, Hq, D), "bq"), _rand((B, S, Hk, D), "bk"), _rand((B, S, Hk, D), "bv")
+        do = _rand((B, S, Hq, D), "bdo")
+        dq, dk, dv = oracle.attention_bwd(q, k, v, do, mask=mask, scale=scale)
+        Q, K, V = (torch.from_numpy(_f64(x)).permute(0, 2, 1, 3).requires_grad_(True) for x in (q, k, v))
+        o = torch.nn.functional.scaled_dot_product_attention(
+            Q, K, V, is_causal=mask == "causal", enable_gqa=Hq != Hk, scale=scale or None)
+        o.backward(torch.from_numpy(_f64(do)).permute(0, 2, 1, 3))
+        for name, mine, ref in (("dQ", dq, Q.grad), ("dK", dk, K.grad), ("dV", dv, V.grad)):
+            _close(mine, ref.permute(0, 2, 1, 3).numpy(), atol=1e-10, what=f"backward {name} {mask}")
+    # finite differences of L = sum(dO * O) with respect to one entry of each input
+    B, S, Hq, Hk, D = 1, 6, 2, 1, 8
+    q, k, v = _rand((B, S, Hq, D), "fq"), _rand((B, S, Hk, D), "fk"), _rand((B, S, Hk, D), "fv")
+    do = _rand((B, S, Hq, D), "fdo")
+    dq, dk, dv = oracle.attention_bwd(q, k, v, do, mask="causal")
+    Qf, Kf, Vf, dOf = _f64(q), _f64(k), _f64(v), _f64(do)
+
+    def loss(Qx, Kx, Vx):
+        tot = 0.0
+        for h in range(Hq):
+            z = (Qx[0, :, h] @ Kx[0, :, 0].T) / math.sqrt(D)
+            z = np.where(np.tril(np.ones((S, S), dtype=bool)), z, -np.inf)
+            p = np.exp(z - z.max(axis=1, keepdims=True))
+            p /= p.sum(axis=1, keepdims=True)
+            tot += float((dOf[0, :, h] * (p @ Vx[0, :, 0])).sum())
+        return tot
+
+    eps = 1e-6
+    for name, grad, idx in (("dQ", dq, (0, 3, 1, 2)), ("dK", dk, (0, 2, 0, 5)), ("dV", dv, (0, 1, 0, 7))):
+        args = [Qf.copy(), Kf.copy(), Vf.copy()]
+        which = {"dQ": 0, "dK": 1, "dV": 2}[name]
+        args[which][idx] += eps
+        up = loss(*args)
+        args[which][idx] -= 2 * eps
+        down = loss(*args)
+        _close(grad[idx], (up - down) / (2 * eps), atol=1e-7, what=f"finite difference {name}")
+
+
 def pin_score_expr(lib):
     """The score_mod-expression oracle (numpy, float64) against the C oracle's
     built-in variants written as expressions, against a closed form, on rows
@@ -509,4 +553,4 @@ def pin_score_expr(lib):
 ALL_PINS = [pin_constant_scores, pin_alibi_geometric, pin_softcap_two_keys, pin_one_hot,
             pin_rows_sum_to_one, pin_shift_invariance, pin_permutation, pin_causal_row0,
             pin_sdpa, pin_reductions, pin_rows_api, pin_diff, pin_evo, pin_fully_masked_row,
-            pin_decode, pin_key_mask, pin_score_expr]
+            pin_decode, pin_key_mask, pin_score_expr, pin_backward]

@@ -88,3 +88,29 @@ def test_expr_mutant_is_caught(name, monkeypatch):
     monkeypatch.setitem(getattr(se, table), key, value)
     with pytest.raises(AssertionError):
         oracle_pins.pin_score_expr(oracle.load())
+
+
+# Mistakes planted in the backward oracle (oracle.attention_bwd): its source
+# is edited in memory, compiled, and swapped in for the duration of the test.
+BWD_MUTANTS = {
+    "bwd_no_D_term": ("dS = P * (dP - (P * dP).sum(axis=1, keepdims=True))", "dS = P * dP"),
+    "bwd_dk_no_scale": ("dK[b, :, kh] += s * (dS.T @ Q[b, :, h])", "dK[b, :, kh] += dS.T @ Q[b, :, h]"),
+    "bwd_dv_overwritten": ("dV[b, :, kh] += P.T @ dO[b, :, h]", "dV[b, :, kh] = P.T @ dO[b, :, h]"),
+    "bwd_gqa_modulo": ("kh = h // G", "kh = h % Hk"),
+    "bwd_dq_transposed_ds": ("dQ[b, :, h] = s * (dS @ K[b, :, kh])", "dQ[b, :, h] = s * (dS.T @ K[b, :, kh])"),
+}
+
+
+@pytest.mark.parametrize("name", sorted(BWD_MUTANTS))
+def test_bwd_mutant_is_caught(name, monkeypatch):
+    import inspect
+    import textwrap
+
+    src = textwrap.dedent(inspect.getsource(oracle.attention_bwd))
+    a, b = BWD_MUTANTS[name]
+    assert a in src, name
+    ns = dict(vars(oracle))
+    exec(compile(src.replace(a, b), "<mutant>", "exec"), ns)
+    monkeypatch.setattr(oracle, "attention_bwd", ns["attention_bwd"])
+    with pytest.raises((AssertionError, ValueError, IndexError)):
+        oracle_pins.pin_backward(oracle.load())
