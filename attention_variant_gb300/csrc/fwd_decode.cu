@@ -43,6 +43,7 @@
 
 #include "common.cuh"
 #include "launch.h"
+#include "warp_mma.cuh"
 
 namespace fl {
 namespace {
@@ -54,42 +55,12 @@ constexpr uint32_t kKVBytes = kDecodeChunk * 64 * 2; // one chunk of K (or V), 1
 constexpr uint32_t kStageBytes = 2 * kKVBytes;
 // block-table entries one split touches at most (pages of 16 keys)
 constexpr int kSplitPages = kDecodeMaxSplitChunks * kDecodeChunk / 16;
-constexpr float kLog2e = 1.4426950408889634f;
-constexpr float kLn2 = 0.6931471805599453f;
-
 __device__ uint32_t g_lib_error_word;
 
-// Byte offset of 16-byte unit u of key row t inside a stage: unit u of row t
-// sits at u ^ (t mod 8) (the 128-byte swizzle the TMA wrote the rows with).
-__device__ __forceinline__ uint32_t swz(int t, int u)
-{
-    return static_cast<uint32_t>(t * 128 + ((u ^ (t & 7)) << 4));
-}
-
-__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t &r0, uint32_t &r1, uint32_t &r2,
-                                        uint32_t &r3)
-{
-    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
-                 : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
-                 : "r"(addr));
-}
-
-__device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t &r0, uint32_t &r1, uint32_t &r2,
-                                          uint32_t &r3)
-{
-    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
-                 : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
-                 : "r"(addr));
-}
-
-// d += a b for one 16 x 8 tile, K = 16 (bf16 in, fp32 accumulate)
-__device__ __forceinline__ void mma16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1)
-{
-    asm volatile("mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 "
-                 "{%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
-                 : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-                 : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
-}
+using wm::ldsm_x4;
+using wm::ldsm_x4_t;
+using wm::mma16816;
+using wm::swz;
 
 __device__ __forceinline__ uint32_t bf16_bits(const __nv_bfloat16 &x)
 {
