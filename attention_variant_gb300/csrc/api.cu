@@ -823,7 +823,8 @@ fl_status bwd_plan(const fl_tensor *q, const fl_tensor *k, const fl_tensor *v,
         return fail(FL_ERR_INVALID_ARG, "gqa_group does not match Hq / Hk");
     if (!std::isfinite(d->scale) || d->scale < 0.f)
         return fail(FL_ERR_INVALID_ARG, "scale must be finite and positive (0 selects 1/sqrt(D))");
-    pl.S_pad = (pl.S + fl::kBwdBlock - 1) / fl::kBwdBlock * fl::kBwdBlock;
+    // padded to the dQ kernel's 128-row query tiles (a multiple of kBwdBlock)
+    pl.S_pad = (pl.S + 127) / 128 * 128;
     pl.total = (size_t(pl.B) * size_t(pl.Hq) * size_t(pl.S_pad) * 8 + 255) / 256 * 256;
     return FL_OK;
 }
@@ -931,7 +932,20 @@ fl_status fl_attn_bwd(const fl_tensor *q, const fl_tensor *k, const fl_tensor *v
     p.ws_stats = static_cast<float *>(workspace);
     p.err_user = desc->error_word;
     p.timeout_ns = timeout_ns(desc);
-    const cudaError_t e = fl::launch_bwd(tq, tdo, tk, tv, p, reinterpret_cast<cudaStream_t>(stream));
+    // Q and dO again with 128-row boxes (the dQ kernel's query tiles)
+    CUtensorMap tq128, tdo128;
+    const uint32_t box128[4] = {64, 128, 1, 1};
+    for (int m = 0; m < 2; ++m) {
+        const View &T = *src[m];
+        const uint64_t dims[4] = {64, uint64_t(pl.S), uint64_t(T.size[2]), uint64_t(pl.B)};
+        const uint64_t st[3] = {uint64_t(T.stride[1]) * 2, uint64_t(T.stride[2]) * 2,
+                                uint64_t(T.stride[0]) * 2};
+        if ((s = make_map(m == 0 ? tq128 : tdo128, T.ptr, 4, dims, st, box128, CU_TENSOR_MAP_SWIZZLE_128B,
+                          names[m])) != FL_OK)
+            return s;
+    }
+    const cudaError_t e = fl::launch_bwd(tq, tdo, tk, tv, tq128, tdo128, p,
+                                         reinterpret_cast<cudaStream_t>(stream));
     if (e != cudaSuccess)
         return fail(FL_ERR_CUDA, "kernel launch failed: %s", cudaGetErrorString(e));
     return ok();

@@ -19,15 +19,16 @@
 //                    the CTA walks every query block of every query head of
 //                    the group (query blocks wholly before the key block are
 //                    skipped under the causal mask);
-//   bwd_dq_kernel    one CTA per (64-row query block, query head, batch):
-//                    four warps own 16 query rows each and keep dQ in
-//                    registers while the CTA walks the key blocks.
-// In both main kernels a producer warp streams the 64-row tiles the loop
-// needs (Q and dO, or K and V; 128-byte swizzle) through a 3-stage TMA ring,
-// and the consumer warps recompute S and P and form the products with
-// warp-level bf16 MMAs (m16n8k16, fp32 accumulate) on ldmatrix fragments;
-// P and dS go from accumulators straight into A operands.  Recomputing S in
-// the dQ kernel costs two more of the seven products than an atomic dQ
+//   bwd_dq_kernel    one CTA per (128-row query tile, query head, batch) on
+//                    the tcgen05 tensor cores: S, dP and the dQ accumulator
+//                    in TMEM, dS computed by one thread per query row
+//                    (described at the kernel).
+// In the dK/dV kernel a producer warp streams the 64-row Q and dO tiles
+// (128-byte swizzle) through a 3-stage TMA ring and the consumer warps
+// recompute S and P and form the products with warp-level bf16 MMAs
+// (m16n8k16, fp32 accumulate) on ldmatrix fragments; P and dS go from
+// accumulators straight into A operands.  Recomputing S and dP in the dQ
+// kernel costs two more of the seven products than an atomic dQ
 // accumulation would, and buys determinism and no dQ workspace.
 #include <cuda_bf16.h>
 #include <cstdint>
@@ -347,125 +348,277 @@ __global__ void __launch_bounds__(kThreads, 2)
     }
 }
 
-// ---------------------------------------------------------------- dQ
+// ---------------------------------------------------------------- dQ (tcgen05)
+//
+// One CTA per (128-row query tile, query head, batch), eight warps:
+//   warp 0     TMA producer: the Q and dO tiles once, then the K and V tiles
+//              of 64 keys through a kDqStages ring;
+//   warps 1-3  MMA issuers (one thread each; warp 1 also owns TMEM): per key
+//              tile j, warp 1 issues S(j) = Q K_j^T and warp 2 dP(j) =
+//              dO V_j^T into TMEM buffer j % 2 (smem x smem, K-major
+//              operands); once the softmax has written dS(j), warp 3 issues
+//              dQ += dS(j) K_j (dS from TMEM, K as an MN-major smem operand).
+//              A tcgen05.mma returns to its thread only when the tensor core
+//              accepts it, so one issuer per chain lets the chains interleave;
+//              the S and dP of tile j + 1 run while the softmax works on j;
+//   warps 4-11 two warpgroups, one thread per query row (TMEM lane), taking
+//              alternate key tiles: dS = P (dP - D) with
+//              P = 2^(S scale log2 e - LSE log2 e), packed to bf16 into TMEM;
+//              at the end dQ (fp32, TMEM) * scale -> bf16.
+// TMEM columns: S[2] at 0 / 64, dP[2] at 128 / 192, dS[2] (bf16 pairs) at
+// 256 / 288, dQ at 320.
+constexpr int kDqRows = 128, kDqKeys = 64, kDqStages = 4, kDqThreads = 384;
+constexpr uint32_t kDqTile = kDqRows * 64 * 2;   // Q or dO tile, 16 KB
+constexpr uint32_t kColDqS = 0, kColDqP = 128, kColDqDs = 256, kColDq = 320;
 
-__global__ void __launch_bounds__(kThreads, 2)
-    bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
+struct __align__(1024) DqSmem {
+    uint8_t q[kDqTile];
+    uint8_t dout[kDqTile];
+    uint8_t k[kDqStages][kTileBytes];
+    uint8_t v[kDqStages][kTileBytes];
+    uint64_t q_full, kv_full[kDqStages], kv_empty[kDqStages];
+    uint64_t s_full[2], s_free[2], ds_full[2], dq_done[2], mma_done;
+    uint32_t tmem_base;
+    uint32_t abort_flag;
+};
+
+__global__ void __launch_bounds__(kDqThreads, 1)
+    bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_do,
+                  const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
                   const BwdParams p)
 {
-    const int qb = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int g = lane >> 2, t = lane & 3;
-    const int q0 = qb * kBlk;
+    const int qt = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int q0 = qt * kDqRows;
     const int hk = h / (p.Hq / p.Hk);
-    const int nkb = (p.S + kBlk - 1) / kBlk;
-    const int n_it = p.causal ? min(qb + 1, nkb) : nkb; // key blocks past the query block see none
+    const int nkb = (p.S + kDqKeys - 1) / kDqKeys;
+    // causal: key tiles wholly after the last row of the query tile see none
+    const int n_it = p.causal ? min(nkb, (q0 + kDqRows + kDqKeys - 1) / kDqKeys) : nkb;
 
     extern __shared__ uint8_t smem_raw[];
-    const Ring ring = make_ring(smem_raw);
-    init_ring(ring);
+    const uint32_t base = ptx::smem_u32(smem_raw);
+    DqSmem &sm = *reinterpret_cast<DqSmem *>(smem_raw + ((1024u - (base & 1023u)) & 1023u));
+    auto bar = [](const uint64_t &x) { return ptx::smem_u32(&x); };
+
+    if (threadIdx.x == 0) {
+        ptx::mbar_init(bar(sm.q_full), 1);
+        for (int s = 0; s < kDqStages; ++s) {
+            ptx::mbar_init(bar(sm.kv_full[s]), 1);
+            ptx::mbar_init(bar(sm.kv_empty[s]), 2); // the dP and the dQ issuer
+        }
+        for (int u = 0; u < 2; ++u) {
+            ptx::mbar_init(bar(sm.s_full[u]), 2);   // the S and the dP issuer
+            ptx::mbar_init(bar(sm.s_free[u]), 128);
+            ptx::mbar_init(bar(sm.ds_full[u]), 128);
+            ptx::mbar_init(bar(sm.dq_done[u]), 1);
+        }
+        ptx::mbar_init(bar(sm.mma_done), 3);        // every issuer
+        sm.abort_flag = 0;
+        ptx::fence_mbarrier_init();
+    }
+    if (warp == 1) {
+        ptx::tmem_alloc(ptx::smem_u32(&sm.tmem_base), 512);
+        ptx::tmem_relinquish();
+    }
+    ptx::tc_fence_before();
+    __syncthreads();
+    ptx::tc_fence_after();
+    const uint32_t tmem = sm.tmem_base;
+
     WaitCtl wc;
-    wc.abort_flag = ring.abort;
+    wc.abort_flag = &sm.abort_flag;
     wc.timeout_cycles = p.timeout_ns * 21 / 10;
     wc.err_user = p.err_user;
     wc.err_lib = &g_lib_error_word;
-
     bool ok = true;
-    int issued = 0;
-    float dq[8][4];
-    zero(dq);
 
-    if (warp == kConsumerWarps) {
-        if (lane == 0)
-            for (int it = 0; it < n_it; ++it) {
-                const int s = it % kStages;
-                if (it >= kStages &&
-                    !mbar_wait(ptx::smem_u32(&ring.empty[s]), ((it / kStages) - 1) & 1, wc, W_KV_EMPTY)) {
-                    ok = false;
-                    break;
-                }
-                const uint32_t bar = ptx::smem_u32(&ring.full[s]);
-                ptx::mbar_arrive_expect_tx(bar, 2 * kTileBytes);
-                ptx::tma_load_4d(ring.tile(s, 0), &tm_k, bar, 0, it * kBlk, hk, b);
-                ptx::tma_load_4d(ring.tile(s, 1), &tm_v, bar, 0, it * kBlk, hk, b);
-                issued = it + 1;
-            }
-    } else {
-        // ---- consumers: query rows q0 + 16 warp .. + 15
-        const int row_a = q0 + 16 * warp + g, row_b = row_a + 8;
-        uint32_t qa[4][4], doa[4][4];
-        load_a_rows(p.q + b * p.q_sb + h * p.q_sh, p.q_ss, q0 + 16 * warp, p.S, qa);
-        load_a_rows(p.dout + b * p.do_sb + h * p.do_sh, p.do_ss, q0 + 16 * warp, p.S, doa);
-        const float2 *stats = reinterpret_cast<const float2 *>(p.ws_stats) +
-                              (static_cast<int64_t>(b) * p.Hq + h) * p.S_pad;
-        const float2 st_a = stats[row_a], st_b = stats[row_b]; // rows < S_pad
-        const float sl2 = p.scale * kLog2e;
-        for (int it = 0; it < n_it; ++it) {
-            const int s = it % kStages;
-            if (!warp_wait(ptx::smem_u32(&ring.full[s]), (it / kStages) & 1, wc, W_KV_FULL)) {
+    if (warp == 0) {
+        // ---- producer
+        int issued = 0;
+        if (lane == 0) {
+            ptx::mbar_arrive_expect_tx(bar(sm.q_full), 2 * kDqTile);
+            ptx::tma_load_4d(ptx::smem_u32(sm.q), &tm_q, bar(sm.q_full), 0, q0, h, b);
+            ptx::tma_load_4d(ptx::smem_u32(sm.dout), &tm_do, bar(sm.q_full), 0, q0, h, b);
+        }
+        for (int j = 0; j < n_it; ++j) {
+            const int s = j % kDqStages;
+            if (j >= kDqStages && !warp_wait(bar(sm.kv_empty[s]), ((j / kDqStages) - 1) & 1, wc, W_KV_EMPTY)) {
                 ok = false;
                 break;
             }
-            const uint32_t sk = ring.tile(s, 0), sv = ring.tile(s, 1);
-            const int j0 = it * kBlk;
-            // P = exp2(sl2 Q K^T - lse2)
-            float pr[8][4];
-            zero(pr);
-            mma_a_tile_rows(pr, qa, sk);
-            const bool edge = j0 + kBlk > p.S || (p.causal && j0 + kBlk > q0);
-#pragma unroll
-            for (int n = 0; n < 8; ++n)
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const int key = j0 + 8 * n + 2 * t + (e & 1);
-                    const int row = e < 2 ? row_a : row_b;
-                    const float pv = ptx::ex2(fmaf(pr[n][e], sl2, -(e < 2 ? st_a.x : st_b.x)));
-                    pr[n][e] = (edge && (key >= p.S || (p.causal && key > row))) ? 0.f : pv;
-                }
-            // dP = dO V^T, dS = P (dP - D)
-            float dp[8][4];
-            zero(dp);
-            mma_a_tile_rows(dp, doa, sv);
-#pragma unroll
-            for (int n = 0; n < 8; ++n)
-#pragma unroll
-                for (int e = 0; e < 4; ++e)
-                    dp[n][e] = pr[n][e] * (dp[n][e] - (e < 2 ? st_a.y : st_b.y));
-            uint32_t dsa[4][4];
-            acc_to_a(dp, dsa);
-            // dQ += dS K
-            mma_a_tile_cols(dq, dsa, sk);
+            if (lane == 0) {
+                ptx::mbar_arrive_expect_tx(bar(sm.kv_full[s]), 2 * kTileBytes);
+                ptx::tma_load_4d(ptx::smem_u32(sm.k[s]), &tm_k, bar(sm.kv_full[s]), 0, j * kDqKeys, hk, b);
+                ptx::tma_load_4d(ptx::smem_u32(sm.v[s]), &tm_v, bar(sm.kv_full[s]), 0, j * kDqKeys, hk, b);
+            }
             __syncwarp();
-            if (lane == 0)
-                ptx::mbar_arrive(ptx::smem_u32(&ring.empty[s]));
+            issued = j + 1;
+        }
+        if (!ok) {
+            // the last copies into each stage, and Q / dO, may still land
+            for (int s = 0; s < kDqStages; ++s) {
+                const int last = issued - 1 - ((issued - 1 - s) % kDqStages + kDqStages) % kDqStages;
+                if (last >= 0)
+                    mbar_wait_drain(bar(sm.kv_full[s]), (last / kDqStages) & 1, wc, W_DRAIN);
+            }
+            mbar_wait_drain(bar(sm.q_full), 0, wc, W_DRAIN);
+        }
+    } else if (warp <= 3) {
+        // ---- MMA issuers, one chain kind per warp so the chains interleave
+        // on the tensor core: warp 1 S(j), warp 2 dP(j), warp 3 dQ += dS(j) K
+        constexpr uint32_t idesc_s = umma_idesc_bf16(kDqRows, kDqKeys, false);
+        constexpr uint32_t idesc_dq = umma_idesc_bf16(kDqRows, 64, true);
+        constexpr uint64_t kHiKmaj = umma_desc_hi(16, 1024, kSwizzle128B);
+        constexpr uint64_t kHiMN = umma_desc_hi(16, 1024, kSwizzle128B);
+        if (warp < 3) {
+            const uint32_t a_lo = ptx::smem_u32(warp == 1 ? sm.q : sm.dout) >> 4;
+            const uint32_t col = warp == 1 ? kColDqS : kColDqP;
+            ok = warp_wait(bar(sm.q_full), 0, wc, W_Q_FULL);
+            for (int j = 0; j < n_it && ok; ++j) {
+                const int s = j % kDqStages, u = j & 1;
+                if (!warp_wait(bar(sm.kv_full[s]), (j / kDqStages) & 1, wc, W_KV_FULL) ||
+                    (j >= 2 && !warp_wait(bar(sm.s_free[u]), ((j - 2) >> 1) & 1, wc, W_S_FULL))) {
+                    ok = false;
+                    break;
+                }
+                ptx::tc_fence_after();
+                if (lane == 0) {
+                    // S = Q K^T (warp 1) or dP = dO V^T (warp 2)
+                    const uint32_t b_lo = ptx::smem_u32(warp == 1 ? sm.k[s] : sm.v[s]) >> 4;
+#pragma unroll
+                    for (int kk = 0; kk < 4; ++kk)
+                        ptx::mma_ss(tmem + col + 64 * u, kHiKmaj | (a_lo + 2 * kk), kHiKmaj | (b_lo + 2 * kk),
+                                    idesc_s, kk > 0 ? 1u : 0u);
+                    ptx::mma_commit(bar(sm.s_full[u]));
+                    if (warp == 2)
+                        ptx::mma_commit(bar(sm.kv_empty[s])); // the last read of V_j
+                }
+                __syncwarp();
+            }
+        } else {
+            for (int j = 0; j < n_it; ++j) {
+                const int s = j % kDqStages, u = j & 1;
+                if (!warp_wait(bar(sm.ds_full[u]), (j >> 1) & 1, wc, W_P_FULL)) {
+                    ok = false;
+                    break;
+                }
+                ptx::tc_fence_after();
+                if (lane == 0) {
+                    const uint32_t k_lo = ptx::smem_u32(sm.k[s]) >> 4;
+#pragma unroll
+                    for (int kk = 0; kk < kDqKeys / 16; ++kk)
+                        ptx::mma_ts(tmem + kColDq, tmem + kColDqDs + 32 * u + 8 * kk, kHiMN | (k_lo + 128 * kk),
+                                    idesc_dq, (j > 0 || kk > 0) ? 1u : 0u);
+                    ptx::mma_commit(bar(sm.dq_done[u]));
+                    // the last read of K_j (S(j) completed before dS(j) existed)
+                    ptx::mma_commit(bar(sm.kv_empty[s]));
+                }
+                __syncwarp();
+            }
+        }
+        // every MMA the issuers started has completed before TMEM is read or freed
+        if (lane == 0)
+            ptx::mma_commit(bar(sm.mma_done));
+        __syncwarp();
+        mbar_wait_drain(bar(sm.mma_done), 0, wc, W_FINAL);
+    } else {
+        // ---- softmax warpgroups (warps 4-7 take the even key tiles, 8-11 the
+        // odd ones: TMEM buffer u = j % 2 belongs to warpgroup u); a warp
+        // reaches TMEM lanes 32 (warp % 4) ..
+        const int wg = (warp >> 2) - 1;
+        const int r = 32 * (warp & 3) + lane;
+        const int row = q0 + r;
+        const uint32_t lane_off = static_cast<uint32_t>(32 * (warp & 3)) << 16;
+        const float2 st = reinterpret_cast<const float2 *>(p.ws_stats)[(static_cast<int64_t>(b) * p.Hq + h) * p.S_pad + row];
+        const float sl2 = p.scale * kLog2e;
+        for (int j = wg; j < n_it; j += 2) {
+            const int u = j & 1;
+            if (!warp_wait(bar(sm.s_full[u]), (j >> 1) & 1, wc, W_S_FULL)) {
+                ok = false;
+                break;
+            }
+            ptx::tc_fence_after();
+            uint32_t sv[64], pv[64];
+            ptx::tmem_ld32(tmem + lane_off + kColDqS + 64 * u, sv);
+            ptx::tmem_ld32(tmem + lane_off + kColDqS + 64 * u + 32, sv + 32);
+            ptx::tmem_ld32(tmem + lane_off + kColDqP + 64 * u, pv);
+            ptx::tmem_ld32(tmem + lane_off + kColDqP + 64 * u + 32, pv + 32);
+            ptx::tmem_wait_ld();
+            ptx::reg_fence<64>(sv);
+            ptx::reg_fence<64>(pv);
+            ptx::tc_fence_before();
+            ptx::mbar_arrive(bar(sm.s_free[u]));
+            const int j0 = j * kDqKeys;
+            const bool edge = j0 + kDqKeys > p.S || (p.causal && j0 + kDqKeys - 1 > q0);
+            uint32_t ds[32];
+#pragma unroll
+            for (int c = 0; c < 32; ++c) {
+                float d2[2];
+#pragma unroll
+                for (int e = 0; e < 2; ++e) {
+                    const int col = 2 * c + e;
+                    const float pr = ptx::ex2(fmaf(__uint_as_float(sv[col]), sl2, -st.x));
+                    float dsv = pr * (__uint_as_float(pv[col]) - st.y);
+                    if (edge && (j0 + col >= p.S || (p.causal && j0 + col > row)))
+                        dsv = 0.f;
+                    d2[e] = dsv;
+                }
+                ds[c] = ptx::pack_bf16(d2[0], d2[1]);
+            }
+            // dQ(j - 2) has read dS buffer u
+            if (j >= 2 && !warp_wait(bar(sm.dq_done[u]), ((j - 2) >> 1) & 1, wc, W_O_FULL)) {
+                ok = false;
+                break;
+            }
+            ptx::tc_fence_after();
+            ptx::tmem_st32(tmem + lane_off + kColDqDs + 32 * u, ds);
+            ptx::tmem_wait_st();
+            ptx::tc_fence_before();
+            ptx::mbar_arrive(bar(sm.ds_full[u]));
+        }
+        if (ok)
+            ok = warp_wait(bar(sm.mma_done), 0, wc, W_FINAL);
+        // warpgroup wg writes output columns 32 wg .. 32 wg + 31 of its row;
+        // the TMEM load is warp-collective, so every lane takes it (`ok` is
+        // warp-uniform) and only the store depends on the row
+        if (ok) {
+            uint32_t o[32];
+            ptx::tc_fence_after();
+            ptx::tmem_ld32(tmem + lane_off + kColDq + 32 * wg, o);
+            ptx::tmem_wait_ld();
+            ptx::reg_fence<32>(o);
+            uint4 *dst = reinterpret_cast<uint4 *>(p.dq + b * p.dq_sb + static_cast<int64_t>(row) * p.dq_ss +
+                                                   h * p.dq_sh + 32 * wg);
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+                uint32_t w[4];
+#pragma unroll
+                for (int q = 0; q < 4; ++q)
+                    w[q] = ptx::pack_bf16(__uint_as_float(o[8 * c + 2 * q]) * p.scale,
+                                          __uint_as_float(o[8 * c + 2 * q + 1]) * p.scale);
+                if (row < p.S)
+                    dst[c] = make_uint4(w[0], w[1], w[2], w[3]);
+            }
         }
     }
-    if (!__syncthreads_and(ok)) {
-        if (warp == kConsumerWarps && lane == 0)
-            drain(ring, issued, wc);
-        return;
-    }
-    if (warp < kConsumerWarps) {
-#pragma unroll
-        for (int half = 0; half < 2; ++half) {
-            const int row = q0 + 16 * warp + g + 8 * half;
-            if (row >= p.S)
-                continue;
-            __nv_bfloat16 *pq = p.dq + b * p.dq_sb + row * p.dq_ss + h * p.dq_sh;
-#pragma unroll
-            for (int n = 0; n < 8; ++n)
-                *reinterpret_cast<uint32_t *>(pq + 8 * n + 2 * t) =
-                    ptx::pack_bf16(dq[n][2 * half] * p.scale, dq[n][2 * half + 1] * p.scale);
-        }
+    ptx::tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        ptx::tc_fence_after();
+        ptx::tmem_dealloc(tmem, 512);
     }
 }
 
 constexpr size_t kSmemBytes = kStages * (2 * kTileBytes + kStatBytes) + 2 * kStages * 8 + 8 + 1024;
+// more than half an SM's shared memory: one dQ CTA per SM, so that no second
+// CTA waits in tcgen05.alloc for the 512 TMEM columns the first one holds
+constexpr size_t kDqSmemBytes = sizeof(DqSmem) + 1024 > 120 * 1024 ? sizeof(DqSmem) + 1024 : 120 * 1024;
 
 } // namespace
 
 cudaError_t launch_bwd(const CUtensorMap &tq, const CUtensorMap &tdo, const CUtensorMap &tk,
-                       const CUtensorMap &tv, const BwdParams &p, cudaStream_t stream)
+                       const CUtensorMap &tv, const CUtensorMap &tq128, const CUtensorMap &tdo128,
+                       const BwdParams &p, cudaStream_t stream)
 {
     const int64_t rows = static_cast<int64_t>(p.B) * p.Hq * p.S_pad;
     bwd_prep_kernel<<<static_cast<unsigned>((rows + 127) / 128), 128, 0, stream>>>(p);
@@ -477,7 +630,7 @@ cudaError_t launch_bwd(const CUtensorMap &tq, const CUtensorMap &tdo, const CUte
         if ((e = cudaFuncSetAttribute(bwd_dkdv_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                       static_cast<int>(kSmemBytes))) != cudaSuccess ||
             (e = cudaFuncSetAttribute(bwd_dq_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                      static_cast<int>(kSmemBytes))) != cudaSuccess)
+                                      static_cast<int>(kDqSmemBytes))) != cudaSuccess)
             return e;
         configured = true;
     }
@@ -485,7 +638,8 @@ cudaError_t launch_bwd(const CUtensorMap &tq, const CUtensorMap &tdo, const CUte
     bwd_dkdv_kernel<<<dim3(nb, p.Hk, p.B), kThreads, kSmemBytes, stream>>>(tq, tdo, p);
     if ((e = cudaGetLastError()) != cudaSuccess)
         return e;
-    bwd_dq_kernel<<<dim3(nb, p.Hq, p.B), kThreads, kSmemBytes, stream>>>(tk, tv, p);
+    bwd_dq_kernel<<<dim3((p.S + kDqRows - 1) / kDqRows, p.Hq, p.B), kDqThreads, kDqSmemBytes, stream>>>(
+        tq128, tdo128, tk, tv, p);
     return cudaGetLastError();
 }
 

@@ -85,7 +85,7 @@ struct EvoParams {
 constexpr int kBwdBlock = 64; // query / key rows per tile
 
 struct BwdParams {
-    int B, Hq, Hk, S, S_pad;      // S_pad: S rounded up to kBwdBlock
+    int B, Hq, Hk, S, S_pad;      // S_pad: S rounded up to 128 (a multiple of kBwdBlock)
     int causal;
     float scale;
     const __nv_bfloat16 *q, *k, *v, *o, *dout; // element strides (batch, position, head):
@@ -141,7 +141,8 @@ cudaError_t launch_evo(const CUtensorMap &tq, const CUtensorMap &tk, const CUten
                        const CUtensorMap &tb, const EvoParams &p, int grid, cudaStream_t stream);
 int evo_max_bias_keys();
 cudaError_t launch_bwd(const CUtensorMap &tq, const CUtensorMap &tdo, const CUtensorMap &tk,
-                       const CUtensorMap &tv, const BwdParams &p, cudaStream_t stream);
+                       const CUtensorMap &tv, const CUtensorMap &tq128, const CUtensorMap &tdo128,
+                       const BwdParams &p, cudaStream_t stream);
 #endif
 
 // Keys per K/V tile of the standard kernel (its TMEM budget: see fwd_standard.cu),
