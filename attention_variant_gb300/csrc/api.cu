@@ -932,19 +932,21 @@ fl_status fl_attn_bwd(const fl_tensor *q, const fl_tensor *k, const fl_tensor *v
     p.ws_stats = static_cast<float *>(workspace);
     p.err_user = desc->error_word;
     p.timeout_ns = timeout_ns(desc);
-    // Q and dO again with 128-row boxes (the dQ kernel's query tiles)
-    CUtensorMap tq128, tdo128;
+    // all four again with 128-row boxes (the dQ kernel's query tiles, the
+    // dK/dV kernel's key tiles)
+    CUtensorMap tq128, tdo128, tk128, tv128;
+    CUtensorMap *dst128[4] = {&tq128, &tdo128, &tk128, &tv128};
     const uint32_t box128[4] = {64, 128, 1, 1};
-    for (int m = 0; m < 2; ++m) {
+    for (int m = 0; m < 4; ++m) {
         const View &T = *src[m];
         const uint64_t dims[4] = {64, uint64_t(pl.S), uint64_t(T.size[2]), uint64_t(pl.B)};
         const uint64_t st[3] = {uint64_t(T.stride[1]) * 2, uint64_t(T.stride[2]) * 2,
                                 uint64_t(T.stride[0]) * 2};
-        if ((s = make_map(m == 0 ? tq128 : tdo128, T.ptr, 4, dims, st, box128, CU_TENSOR_MAP_SWIZZLE_128B,
-                          names[m])) != FL_OK)
+        if ((s = make_map(*dst128[m], T.ptr, 4, dims, st, box128, CU_TENSOR_MAP_SWIZZLE_128B, names[m])) !=
+            FL_OK)
             return s;
     }
-    const cudaError_t e = fl::launch_bwd(tq, tdo, tk, tv, tq128, tdo128, p,
+    const cudaError_t e = fl::launch_bwd(tq, tdo, tk, tv, tq128, tdo128, tk128, tv128, p,
                                          reinterpret_cast<cudaStream_t>(stream));
     if (e != cudaSuccess)
         return fail(FL_ERR_CUDA, "kernel launch failed: %s", cudaGetErrorString(e));

@@ -14,169 +14,31 @@
 // Three kernels, no atomics (every output element has one writer):
 //   bwd_prep_kernel  per query row: D_i and LSE_i * log2 e into the workspace
 //                    (padded rows get +inf, so their P is 0);
-//   bwd_dkdv_kernel  one CTA per (64-key block, KV head, batch): four warps
-//                    own 16 keys each and keep dK and dV in registers while
-//                    the CTA walks every query block of every query head of
-//                    the group (query blocks wholly before the key block are
-//                    skipped under the causal mask);
-//   bwd_dq_kernel    one CTA per (128-row query tile, query head, batch) on
-//                    the tcgen05 tensor cores: S, dP and the dQ accumulator
-//                    in TMEM, dS computed by one thread per query row
-//                    (described at the kernel).
-// In the dK/dV kernel a producer warp streams the 64-row Q and dO tiles
-// (128-byte swizzle) through a 3-stage TMA ring and the consumer warps
-// recompute S and P and form the products with warp-level bf16 MMAs
-// (m16n8k16, fp32 accumulate) on ldmatrix fragments; P and dS go from
-// accumulators straight into A operands.  Recomputing S and dP in the dQ
-// kernel costs two more of the seven products than an atomic dQ
-// accumulation would, and buys determinism and no dQ workspace.
+//   bwd_dkdv_kernel  one CTA per (128-key tile, KV head, batch): dK and dV
+//                    accumulate in TMEM over every 64-row query tile of every
+//                    query head of the group (causal: from the diagonal on);
+//   bwd_dq_kernel    one CTA per (128-row query tile, query head, batch): dQ
+//                    accumulates in TMEM over the 64-key tiles.
+// Both main kernels run on the tcgen05 tensor cores with the same layout of
+// roles: a TMA producer warp, one MMA-issuing warp per product chain (an MMA
+// returns to its thread only when the tensor core accepts it, so separate
+// issuers let independent chains interleave), and two warpgroups of one
+// thread per TMEM lane taking alternate tiles for the elementwise step, which
+// writes bf16 operands back into TMEM for the next products.  Recomputing S
+// and dP in the dQ kernel costs two more of the seven products than an atomic
+// dQ accumulation would, and buys determinism and no dQ workspace.
 #include <cuda_bf16.h>
 #include <cstdint>
 
 #include "common.cuh"
 #include "launch.h"
-#include "warp_mma.cuh"
 
 namespace fl {
 namespace {
 
-constexpr int kBlk = kBwdBlock;              // rows per tile (queries or keys)
-constexpr int kConsumerWarps = 4;            // 16 rows each
-constexpr int kThreads = 32 * (kConsumerWarps + 1);
-constexpr int kStages = 3;
-constexpr uint32_t kTileBytes = kBlk * 64 * 2; // 8 KB
-constexpr uint32_t kStatBytes = kBlk * 8;      // (lse2, D) per row
+constexpr uint32_t kTileBytes = kBwdBlock * 64 * 2; // one 64-row tile, 8 KB
 
 __device__ uint32_t g_lib_error_word;
-
-__device__ __forceinline__ uint32_t bf16_bits(const __nv_bfloat16 &x)
-{
-    return static_cast<uint32_t>(__bfloat16_as_ushort(x));
-}
-
-// A fragments of 16 consecutive rows (r0 .. r0+15) of a [.., 64] bf16 row
-// block in global memory, k-steps 0..3; rows >= n are zero.
-__device__ __forceinline__ void load_a_rows(const __nv_bfloat16 *base, int64_t row_stride, int r0, int n,
-                                            uint32_t (&a)[4][4])
-{
-    const int lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
-#pragma unroll
-    for (int k = 0; k < 4; ++k)
-        a[k][0] = a[k][1] = a[k][2] = a[k][3] = 0u;
-#pragma unroll
-    for (int half = 0; half < 2; ++half) {
-        const int r = r0 + g + 8 * half;
-        if (r >= n)
-            continue;
-        const __nv_bfloat16 *p = base + r * row_stride;
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-            a[k][half] = bf16_bits(p[16 * k + 2 * t]) | (bf16_bits(p[16 * k + 2 * t + 1]) << 16);
-            a[k][2 + half] = bf16_bits(p[16 * k + 8 + 2 * t]) | (bf16_bits(p[16 * k + 9 + 2 * t]) << 16);
-        }
-    }
-}
-
-// Accumulators (16 rows x 64 columns as eight n-tiles) of one warp -> bf16 A
-// fragments over those 64 columns as k (four k-steps).
-__device__ __forceinline__ void acc_to_a(const float (&c)[8][4], uint32_t (&a)[4][4])
-{
-#pragma unroll
-    for (int kk = 0; kk < 4; ++kk) {
-        a[kk][0] = ptx::pack_bf16(c[2 * kk][0], c[2 * kk][1]);
-        a[kk][1] = ptx::pack_bf16(c[2 * kk][2], c[2 * kk][3]);
-        a[kk][2] = ptx::pack_bf16(c[2 * kk + 1][0], c[2 * kk + 1][1]);
-        a[kk][3] = ptx::pack_bf16(c[2 * kk + 1][2], c[2 * kk + 1][3]);
-    }
-}
-
-__device__ __forceinline__ void zero(float (&c)[8][4])
-{
-#pragma unroll
-    for (int n = 0; n < 8; ++n)
-        c[n][0] = c[n][1] = c[n][2] = c[n][3] = 0.f;
-}
-
-// c += A (16 x 64, as k) times the 64 x 64 tile `tile`, read as B with k along
-// the tile's rows and n along its columns (P V form).
-__device__ __forceinline__ void mma_a_tile_cols(float (&c)[8][4], const uint32_t (&a)[4][4], uint32_t tile)
-{
-#pragma unroll
-    for (int kk = 0; kk < 4; ++kk)
-#pragma unroll
-        for (int u2 = 0; u2 < 4; ++u2) {
-            uint32_t b[4];
-            wm::ldsm_b_cols(tile, 16 * kk, u2, b);
-            wm::mma16816(c[2 * u2], a[kk], b[0], b[1]);
-            wm::mma16816(c[2 * u2 + 1], a[kk], b[2], b[3]);
-        }
-}
-
-// c += A (16 x 64 dims) times tile^T: n along the tile's rows (Q K^T form).
-__device__ __forceinline__ void mma_a_tile_rows(float (&c)[8][4], const uint32_t (&a)[4][4], uint32_t tile)
-{
-#pragma unroll
-    for (int kk = 0; kk < 4; ++kk)
-#pragma unroll
-        for (int n2 = 0; n2 < 4; ++n2) {
-            uint32_t b[4];
-            wm::ldsm_b_rows(tile, 16 * n2, kk, b);
-            wm::mma16816(c[2 * n2], a[kk], b[0], b[1]);
-            wm::mma16816(c[2 * n2 + 1], a[kk], b[2], b[3]);
-        }
-}
-
-// Shared memory of both main kernels: the stages' tiles (each 1024-byte
-// aligned, as the 128-byte swizzle pattern assumes), the stages' row
-// statistics, then the barriers.
-struct Ring {
-    uint8_t *base;
-    uint64_t *full, *empty;
-    volatile uint32_t *abort;
-    __device__ uint32_t tile(int s, int which) const
-    {
-        return ptx::smem_u32(base) + (2 * s + which) * kTileBytes;
-    }
-    __device__ float *stats(int s) const
-    {
-        return reinterpret_cast<float *>(base + kStages * 2 * kTileBytes + s * kStatBytes);
-    }
-};
-
-__device__ __forceinline__ Ring make_ring(uint8_t *smem_raw)
-{
-    const uint32_t b = ptx::smem_u32(smem_raw);
-    Ring r;
-    r.base = smem_raw + ((1024u - (b & 1023u)) & 1023u);
-    r.full = reinterpret_cast<uint64_t *>(r.base + kStages * (2 * kTileBytes + kStatBytes));
-    r.empty = r.full + kStages;
-    r.abort = reinterpret_cast<volatile uint32_t *>(r.empty + kStages);
-    return r;
-}
-
-__device__ __forceinline__ void init_ring(const Ring &r)
-{
-    if (threadIdx.x == 0) {
-        for (int s = 0; s < kStages; ++s) {
-            ptx::mbar_init(ptx::smem_u32(&r.full[s]), 1);
-            ptx::mbar_init(ptx::smem_u32(&r.empty[s]), kConsumerWarps);
-        }
-        *r.abort = 0;
-        ptx::fence_mbarrier_init();
-    }
-    __syncthreads();
-}
-
-// The last copy issued into each stage may still be landing after a failed
-// wait: wait for it (bounded) before the CTA exits.
-__device__ __forceinline__ void drain(const Ring &r, int issued, const WaitCtl &wc)
-{
-    for (int s = 0; s < kStages; ++s) {
-        const int last = issued - 1 - ((issued - 1 - s) % kStages + kStages) % kStages;
-        if (last >= 0)
-            mbar_wait_drain(ptx::smem_u32(&r.full[s]), (last / kStages) & 1, wc, W_DRAIN);
-    }
-}
 
 // ---------------------------------------------------------------- prep
 
@@ -210,142 +72,6 @@ __global__ void __launch_bounds__(128) bwd_prep_kernel(const BwdParams p)
         st = make_float2(lse == kNegInf ? __int_as_float(0x7f800000) : lse * kLog2e, acc);
     }
     reinterpret_cast<float2 *>(p.ws_stats)[idx] = st;
-}
-
-// ---------------------------------------------------------------- dK, dV
-
-__global__ void __launch_bounds__(kThreads, 2)
-    bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_do,
-                    const BwdParams p)
-{
-    const int kb = blockIdx.x, hk = blockIdx.y, b = blockIdx.z;
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int g = lane >> 2, t = lane & 3;
-    const int k0 = kb * kBlk;
-    const int G = p.Hq / p.Hk;
-    const int nqb = p.S_pad / kBlk;
-    const int qb0 = p.causal ? kb : 0; // query blocks before the key block see none of its keys
-    const int n_it = G * (nqb - qb0);
-
-    extern __shared__ uint8_t smem_raw[];
-    const Ring ring = make_ring(smem_raw);
-    init_ring(ring);
-    WaitCtl wc;
-    wc.abort_flag = ring.abort;
-    wc.timeout_cycles = p.timeout_ns * 21 / 10;
-    wc.err_user = p.err_user;
-    wc.err_lib = &g_lib_error_word;
-
-    bool ok = true;
-    int issued = 0;
-    float dk[8][4], dv[8][4];
-    zero(dk);
-    zero(dv);
-
-    if (warp == kConsumerWarps) {
-        // ---- producer: per iteration (head h of the group, query block qb)
-        // the Q and dO tiles by TMA and the rows' (lse2, D) by the warp's lanes
-        for (int it = 0; it < n_it; ++it) {
-            const int s = it % kStages;
-            const int h = hk * G + it / (nqb - qb0), qb = qb0 + it % (nqb - qb0);
-            if (it >= kStages &&
-                !__all_sync(0xffffffffu, mbar_wait(ptx::smem_u32(&ring.empty[s]), ((it / kStages) - 1) & 1, wc,
-                                                   W_KV_EMPTY))) {
-                ok = false;
-                break;
-            }
-            const float2 *src = reinterpret_cast<const float2 *>(p.ws_stats) +
-                                (static_cast<int64_t>(b) * p.Hq + h) * p.S_pad + qb * kBlk;
-            float2 *dst = reinterpret_cast<float2 *>(ring.stats(s));
-            dst[lane] = src[lane];
-            dst[lane + 32] = src[lane + 32];
-            __syncwarp();
-            if (lane == 0) {
-                const uint32_t bar = ptx::smem_u32(&ring.full[s]);
-                ptx::mbar_arrive_expect_tx(bar, 2 * kTileBytes);
-                ptx::tma_load_4d(ring.tile(s, 0), &tm_q, bar, 0, qb * kBlk, h, b);
-                ptx::tma_load_4d(ring.tile(s, 1), &tm_do, bar, 0, qb * kBlk, h, b);
-            }
-            issued = it + 1;
-        }
-    } else {
-        // ---- consumers: keys k0 + 16 warp .. + 15
-        const int key_a = k0 + 16 * warp + g, key_b = key_a + 8;
-        uint32_t ka[4][4], va[4][4];
-        load_a_rows(p.k + b * p.k_sb + hk * p.k_sh, p.k_ss, k0 + 16 * warp, p.S, ka);
-        load_a_rows(p.v + b * p.v_sb + hk * p.v_sh, p.v_ss, k0 + 16 * warp, p.S, va);
-        const float sl2 = p.scale * kLog2e;
-        for (int it = 0; it < n_it; ++it) {
-            const int s = it % kStages;
-            const int qb = qb0 + it % (nqb - qb0);
-            if (!warp_wait(ptx::smem_u32(&ring.full[s]), (it / kStages) & 1, wc, W_KV_FULL)) {
-                ok = false;
-                break;
-            }
-            const uint32_t sq = ring.tile(s, 0), sdo = ring.tile(s, 1);
-            const float2 *st = reinterpret_cast<const float2 *>(ring.stats(s));
-            const int q0 = qb * kBlk;
-            // P^T (keys x queries) = exp2(sl2 K Q^T - lse2)
-            float pt[8][4];
-            zero(pt);
-            mma_a_tile_rows(pt, ka, sq);
-            const bool masked = p.causal && q0 < k0 + kBlk; // the diagonal block
-#pragma unroll
-            for (int n = 0; n < 8; ++n)
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const int qc = 8 * n + 2 * t + (e & 1);
-                    const float pv = ptx::ex2(fmaf(pt[n][e], sl2, -st[qc].x));
-                    const int key = e < 2 ? key_a : key_b;
-                    pt[n][e] = (masked && key > q0 + qc) ? 0.f : pv;
-                }
-            uint32_t pa[4][4];
-            acc_to_a(pt, pa);
-            // dV += P^T dO
-            mma_a_tile_cols(dv, pa, sdo);
-            // dP^T = V dO^T, then dS^T = P^T (dP^T - D)
-            float dpt[8][4];
-            zero(dpt);
-            mma_a_tile_rows(dpt, va, sdo);
-#pragma unroll
-            for (int n = 0; n < 8; ++n)
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const int qc = 8 * n + 2 * t + (e & 1);
-                    dpt[n][e] = pt[n][e] * (dpt[n][e] - st[qc].y);
-                }
-            uint32_t dsa[4][4];
-            acc_to_a(dpt, dsa);
-            // dK += dS^T Q
-            mma_a_tile_cols(dk, dsa, sq);
-            __syncwarp();
-            if (lane == 0)
-                ptx::mbar_arrive(ptx::smem_u32(&ring.empty[s]));
-        }
-    }
-    if (!__syncthreads_and(ok)) {
-        if (warp == kConsumerWarps && lane == 0)
-            drain(ring, issued, wc);
-        return; // recorded in the error words; this block's dK, dV stay unwritten
-    }
-    if (warp < kConsumerWarps) {
-        const int key_a = k0 + 16 * warp + g, key_b = key_a + 8;
-#pragma unroll
-        for (int half = 0; half < 2; ++half) {
-            const int key = half ? key_b : key_a;
-            if (key >= p.S)
-                continue;
-            __nv_bfloat16 *pk = p.dk + b * p.dk_sb + key * p.dk_ss + hk * p.dk_sh;
-            __nv_bfloat16 *pv = p.dv + b * p.dv_sb + key * p.dv_ss + hk * p.dv_sh;
-#pragma unroll
-            for (int n = 0; n < 8; ++n) {
-                *reinterpret_cast<uint32_t *>(pk + 8 * n + 2 * t) =
-                    ptx::pack_bf16(dk[n][2 * half] * p.scale, dk[n][2 * half + 1] * p.scale);
-                *reinterpret_cast<uint32_t *>(pv + 8 * n + 2 * t) =
-                    ptx::pack_bf16(dv[n][2 * half], dv[n][2 * half + 1]);
-            }
-        }
-    }
 }
 
 // ---------------------------------------------------------------- dQ (tcgen05)
@@ -609,16 +335,290 @@ __global__ void __launch_bounds__(kDqThreads, 1)
     }
 }
 
-constexpr size_t kSmemBytes = kStages * (2 * kTileBytes + kStatBytes) + 2 * kStages * 8 + 8 + 1024;
+// ---------------------------------------------------------------- dK, dV (tcgen05)
+//
+// One CTA per (128-key tile, KV head, batch), twelve warps; the key tile is
+// the MMA's M side (TMEM lane = key):
+//   warp 0     TMA producer: the K and V tiles once, then for every query
+//              tile of 64 rows of every query head of the group (causal:
+//              from the key tile's diagonal on) the Q and dO tiles through a
+//              kKvStages ring, with the rows' (LSE log2 e, D) copied by the
+//              warp's lanes;
+//   warps 1-3  MMA issuers: warp 1 S^T(i) = K Q_i^T, warp 2 dP^T(i) =
+//              V dO_i^T into TMEM buffer i % 2; warp 3, once P^T(i) and
+//              dS^T(i) are in TMEM, dV += P^T(i) dO_i and dK += dS^T(i) Q_i
+//              (TMEM x MN-major smem operands), accumulating over the whole
+//              loop;
+//   warps 4-11 two warpgroups taking alternate query tiles, one thread per
+//              key: P^T = 2^(S^T scale log2 e - LSE log2 e) and
+//              dS^T = P^T (dP^T - D), both packed to bf16 into TMEM; at the
+//              end warpgroup 0 writes dV and warpgroup 1 scale * dK.
+// TMEM columns: S^T[2] at 0 / 64, dP^T[2] at 128 / 192, P^T[2] at 256 / 288,
+// dS^T[2] at 320 / 352, dV at 384, dK at 448.
+constexpr int kKvKeys = 128, kKvQ = 64, kKvStages = 4, kKvThreads = 384;
+constexpr uint32_t kKvTile = kKvKeys * 64 * 2;   // K or V tile, 16 KB
+constexpr uint32_t kColTS = 0, kColTP = 128, kColTPb = 256, kColTDs = 320, kColDv = 384, kColDk = 448;
+
+struct __align__(1024) DkvSmem {
+    uint8_t k[kKvTile];
+    uint8_t v[kKvTile];
+    uint8_t q[kKvStages][kTileBytes];
+    uint8_t dout[kKvStages][kTileBytes];
+    float2 stats[kKvStages][kKvQ];
+    uint64_t kv_full, st_full[kKvStages], st_empty[kKvStages];
+    uint64_t s_full[2], s_free[2], pds_full[2], acc_done[2], mma_done;
+    uint32_t tmem_base;
+    uint32_t abort_flag;
+};
+
+__global__ void __launch_bounds__(kKvThreads, 1)
+    bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
+                    const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_do,
+                    const BwdParams p)
+{
+    const int kt = blockIdx.x, hk = blockIdx.y, b = blockIdx.z;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int k0 = kt * kKvKeys;
+    const int G = p.Hq / p.Hk;
+    const int nq = p.S_pad / kKvQ;
+    const int qj0 = p.causal ? k0 / kKvQ : 0; // earlier query tiles see none of these keys
+    const int n_qt = nq - qj0;
+    const int n_it = G * n_qt;
+
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t base = ptx::smem_u32(smem_raw);
+    DkvSmem &sm = *reinterpret_cast<DkvSmem *>(smem_raw + ((1024u - (base & 1023u)) & 1023u));
+    auto bar = [](const uint64_t &x) { return ptx::smem_u32(&x); };
+
+    if (threadIdx.x == 0) {
+        ptx::mbar_init(bar(sm.kv_full), 1);
+        for (int s = 0; s < kKvStages; ++s) {
+            ptx::mbar_init(bar(sm.st_full[s]), 1);
+            ptx::mbar_init(bar(sm.st_empty[s]), 1); // the dV / dK issuer
+        }
+        for (int u = 0; u < 2; ++u) {
+            ptx::mbar_init(bar(sm.s_full[u]), 2);   // the S^T and the dP^T issuer
+            ptx::mbar_init(bar(sm.s_free[u]), 128);
+            ptx::mbar_init(bar(sm.pds_full[u]), 128);
+            ptx::mbar_init(bar(sm.acc_done[u]), 1);
+        }
+        ptx::mbar_init(bar(sm.mma_done), 3);
+        sm.abort_flag = 0;
+        ptx::fence_mbarrier_init();
+    }
+    if (warp == 1) {
+        ptx::tmem_alloc(ptx::smem_u32(&sm.tmem_base), 512);
+        ptx::tmem_relinquish();
+    }
+    ptx::tc_fence_before();
+    __syncthreads();
+    ptx::tc_fence_after();
+    const uint32_t tmem = sm.tmem_base;
+
+    WaitCtl wc;
+    wc.abort_flag = &sm.abort_flag;
+    wc.timeout_cycles = p.timeout_ns * 21 / 10;
+    wc.err_user = p.err_user;
+    wc.err_lib = &g_lib_error_word;
+    bool ok = true;
+
+    if (warp == 0) {
+        // ---- producer
+        int issued = 0;
+        if (lane == 0) {
+            ptx::mbar_arrive_expect_tx(bar(sm.kv_full), 2 * kKvTile);
+            ptx::tma_load_4d(ptx::smem_u32(sm.k), &tm_k, bar(sm.kv_full), 0, k0, hk, b);
+            ptx::tma_load_4d(ptx::smem_u32(sm.v), &tm_v, bar(sm.kv_full), 0, k0, hk, b);
+        }
+        for (int i = 0; i < n_it; ++i) {
+            const int s = i % kKvStages;
+            const int h = hk * G + i / n_qt, q0 = (qj0 + i % n_qt) * kKvQ;
+            if (i >= kKvStages && !warp_wait(bar(sm.st_empty[s]), ((i / kKvStages) - 1) & 1, wc, W_KV_EMPTY)) {
+                ok = false;
+                break;
+            }
+            const float2 *src = reinterpret_cast<const float2 *>(p.ws_stats) +
+                                (static_cast<int64_t>(b) * p.Hq + h) * p.S_pad + q0;
+            sm.stats[s][lane] = src[lane];
+            sm.stats[s][lane + 32] = src[lane + 32];
+            __syncwarp();
+            if (lane == 0) {
+                ptx::mbar_arrive_expect_tx(bar(sm.st_full[s]), 2 * kTileBytes);
+                ptx::tma_load_4d(ptx::smem_u32(sm.q[s]), &tm_q, bar(sm.st_full[s]), 0, q0, h, b);
+                ptx::tma_load_4d(ptx::smem_u32(sm.dout[s]), &tm_do, bar(sm.st_full[s]), 0, q0, h, b);
+            }
+            __syncwarp();
+            issued = i + 1;
+        }
+        if (!ok) {
+            for (int s = 0; s < kKvStages; ++s) {
+                const int last = issued - 1 - ((issued - 1 - s) % kKvStages + kKvStages) % kKvStages;
+                if (last >= 0)
+                    mbar_wait_drain(bar(sm.st_full[s]), (last / kKvStages) & 1, wc, W_DRAIN);
+            }
+            mbar_wait_drain(bar(sm.kv_full), 0, wc, W_DRAIN);
+        }
+    } else if (warp <= 3) {
+        // ---- MMA issuers
+        constexpr uint32_t idesc_s = umma_idesc_bf16(kKvKeys, kKvQ, false);
+        constexpr uint32_t idesc_acc = umma_idesc_bf16(kKvKeys, 64, true);
+        constexpr uint64_t kHiKmaj = umma_desc_hi(16, 1024, kSwizzle128B);
+        constexpr uint64_t kHiMN = umma_desc_hi(16, 1024, kSwizzle128B);
+        if (warp < 3) {
+            // S^T = K Q_i^T (warp 1) or dP^T = V dO_i^T (warp 2)
+            const uint32_t a_lo = ptx::smem_u32(warp == 1 ? sm.k : sm.v) >> 4;
+            const uint32_t col = warp == 1 ? kColTS : kColTP;
+            ok = warp_wait(bar(sm.kv_full), 0, wc, W_Q_FULL);
+            for (int i = 0; i < n_it && ok; ++i) {
+                const int s = i % kKvStages, u = i & 1;
+                if (!warp_wait(bar(sm.st_full[s]), (i / kKvStages) & 1, wc, W_KV_FULL) ||
+                    (i >= 2 && !warp_wait(bar(sm.s_free[u]), ((i - 2) >> 1) & 1, wc, W_S_FULL))) {
+                    ok = false;
+                    break;
+                }
+                ptx::tc_fence_after();
+                if (lane == 0) {
+                    const uint32_t b_lo = ptx::smem_u32(warp == 1 ? sm.q[s] : sm.dout[s]) >> 4;
+#pragma unroll
+                    for (int kk = 0; kk < 4; ++kk)
+                        ptx::mma_ss(tmem + col + 64 * u, kHiKmaj | (a_lo + 2 * kk), kHiKmaj | (b_lo + 2 * kk),
+                                    idesc_s, kk > 0 ? 1u : 0u);
+                    ptx::mma_commit(bar(sm.s_full[u]));
+                }
+                __syncwarp();
+            }
+        } else {
+            for (int i = 0; i < n_it; ++i) {
+                const int s = i % kKvStages, u = i & 1;
+                if (!warp_wait(bar(sm.pds_full[u]), (i >> 1) & 1, wc, W_P_FULL)) {
+                    ok = false;
+                    break;
+                }
+                ptx::tc_fence_after();
+                if (lane == 0) {
+                    const uint32_t do_lo = ptx::smem_u32(sm.dout[s]) >> 4, q_lo = ptx::smem_u32(sm.q[s]) >> 4;
+#pragma unroll
+                    for (int kk = 0; kk < kKvQ / 16; ++kk)
+                        ptx::mma_ts(tmem + kColDv, tmem + kColTPb + 32 * u + 8 * kk, kHiMN | (do_lo + 128 * kk),
+                                    idesc_acc, (i > 0 || kk > 0) ? 1u : 0u);
+#pragma unroll
+                    for (int kk = 0; kk < kKvQ / 16; ++kk)
+                        ptx::mma_ts(tmem + kColDk, tmem + kColTDs + 32 * u + 8 * kk, kHiMN | (q_lo + 128 * kk),
+                                    idesc_acc, (i > 0 || kk > 0) ? 1u : 0u);
+                    ptx::mma_commit(bar(sm.acc_done[u]));
+                    // the stage's last readers (S^T(i), dP^T(i) completed before P^T(i) existed)
+                    ptx::mma_commit(bar(sm.st_empty[s]));
+                }
+                __syncwarp();
+            }
+        }
+        if (lane == 0)
+            ptx::mma_commit(bar(sm.mma_done));
+        __syncwarp();
+        mbar_wait_drain(bar(sm.mma_done), 0, wc, W_FINAL);
+    } else {
+        // ---- two softmax warpgroups (warps 4-7: even i, 8-11: odd i); a warp
+        // reaches TMEM lanes 32 (warp % 4) ..
+        const int wg = (warp >> 2) - 1;
+        const int r = 32 * (warp & 3) + lane;
+        const int key = k0 + r;
+        const uint32_t lane_off = static_cast<uint32_t>(32 * (warp & 3)) << 16;
+        const float sl2 = p.scale * kLog2e;
+        for (int i = wg; i < n_it; i += 2) {
+            const int s = i % kKvStages, u = i & 1;
+            const int q0 = (qj0 + i % n_qt) * kKvQ;
+            if (!warp_wait(bar(sm.s_full[u]), (i >> 1) & 1, wc, W_S_FULL)) {
+                ok = false;
+                break;
+            }
+            ptx::tc_fence_after();
+            const bool edge = p.causal && q0 < k0 + kKvKeys; // holds pairs with query < key
+            uint32_t pa[32], da[32];
+#pragma unroll
+            for (int half = 0; half < 2; ++half) {
+                uint32_t sv[32], pv[32];
+                ptx::tmem_ld32(tmem + lane_off + kColTS + 64 * u + 32 * half, sv);
+                ptx::tmem_ld32(tmem + lane_off + kColTP + 64 * u + 32 * half, pv);
+                ptx::tmem_wait_ld();
+                ptx::reg_fence<32>(sv);
+                ptx::reg_fence<32>(pv);
+#pragma unroll
+                for (int c2 = 0; c2 < 16; ++c2) {
+                    float pp[2], dd[2];
+#pragma unroll
+                    for (int e = 0; e < 2; ++e) {
+                        const int c = 32 * half + 2 * c2 + e;
+                        const float2 st = sm.stats[s][c];
+                        float pr = ptx::ex2(fmaf(__uint_as_float(sv[2 * c2 + e]), sl2, -st.x));
+                        if (edge && q0 + c < key)
+                            pr = 0.f;
+                        pp[e] = pr;
+                        dd[e] = pr * (__uint_as_float(pv[2 * c2 + e]) - st.y);
+                    }
+                    pa[16 * half + c2] = ptx::pack_bf16(pp[0], pp[1]);
+                    da[16 * half + c2] = ptx::pack_bf16(dd[0], dd[1]);
+                }
+            }
+            ptx::tc_fence_before();
+            ptx::mbar_arrive(bar(sm.s_free[u]));
+            // dV / dK of tile i - 2 have read P^T / dS^T buffer u
+            if (i >= 2 && !warp_wait(bar(sm.acc_done[u]), ((i - 2) >> 1) & 1, wc, W_O_FULL)) {
+                ok = false;
+                break;
+            }
+            ptx::tc_fence_after();
+            ptx::tmem_st32(tmem + lane_off + kColTPb + 32 * u, pa);
+            ptx::tmem_st32(tmem + lane_off + kColTDs + 32 * u, da);
+            ptx::tmem_wait_st();
+            ptx::tc_fence_before();
+            ptx::mbar_arrive(bar(sm.pds_full[u]));
+        }
+        if (ok)
+            ok = warp_wait(bar(sm.mma_done), 0, wc, W_FINAL);
+        // warpgroup 0 writes dV, warpgroup 1 scale * dK (the TMEM loads are
+        // warp-collective: every lane takes them; only the stores test the key)
+        if (ok) {
+            ptx::tc_fence_after();
+            uint32_t o[64];
+            const uint32_t col = wg == 0 ? kColDv : kColDk;
+            ptx::tmem_ld32(tmem + lane_off + col, o);
+            ptx::tmem_ld32(tmem + lane_off + col + 32, o + 32);
+            ptx::tmem_wait_ld();
+            ptx::reg_fence<64>(o);
+            const float f = wg == 0 ? 1.f : p.scale;
+            __nv_bfloat16 *dst = wg == 0 ? p.dv + b * p.dv_sb + static_cast<int64_t>(key) * p.dv_ss + hk * p.dv_sh
+                                         : p.dk + b * p.dk_sb + static_cast<int64_t>(key) * p.dk_ss + hk * p.dk_sh;
+#pragma unroll
+            for (int c = 0; c < 8; ++c) {
+                uint32_t w[4];
+#pragma unroll
+                for (int q = 0; q < 4; ++q)
+                    w[q] = ptx::pack_bf16(__uint_as_float(o[8 * c + 2 * q]) * f,
+                                          __uint_as_float(o[8 * c + 2 * q + 1]) * f);
+                if (key < p.S)
+                    reinterpret_cast<uint4 *>(dst)[c] = make_uint4(w[0], w[1], w[2], w[3]);
+            }
+        }
+    }
+    ptx::tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        ptx::tc_fence_after();
+        ptx::tmem_dealloc(tmem, 512);
+    }
+}
+
 // more than half an SM's shared memory: one dQ CTA per SM, so that no second
 // CTA waits in tcgen05.alloc for the 512 TMEM columns the first one holds
 constexpr size_t kDqSmemBytes = sizeof(DqSmem) + 1024 > 120 * 1024 ? sizeof(DqSmem) + 1024 : 120 * 1024;
+constexpr size_t kKvSmemBytes = sizeof(DkvSmem) + 1024 > 120 * 1024 ? sizeof(DkvSmem) + 1024 : 120 * 1024;
 
 } // namespace
 
 cudaError_t launch_bwd(const CUtensorMap &tq, const CUtensorMap &tdo, const CUtensorMap &tk,
                        const CUtensorMap &tv, const CUtensorMap &tq128, const CUtensorMap &tdo128,
-                       const BwdParams &p, cudaStream_t stream)
+                       const CUtensorMap &tk128, const CUtensorMap &tv128, const BwdParams &p,
+                       cudaStream_t stream)
 {
     const int64_t rows = static_cast<int64_t>(p.B) * p.Hq * p.S_pad;
     bwd_prep_kernel<<<static_cast<unsigned>((rows + 127) / 128), 128, 0, stream>>>(p);
@@ -628,14 +628,14 @@ cudaError_t launch_bwd(const CUtensorMap &tq, const CUtensorMap &tdo, const CUte
     static bool configured = false; // benign race: the calls are idempotent
     if (!configured) {
         if ((e = cudaFuncSetAttribute(bwd_dkdv_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                      static_cast<int>(kSmemBytes))) != cudaSuccess ||
+                                      static_cast<int>(kKvSmemBytes))) != cudaSuccess ||
             (e = cudaFuncSetAttribute(bwd_dq_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                       static_cast<int>(kDqSmemBytes))) != cudaSuccess)
             return e;
         configured = true;
     }
-    const int nb = p.S_pad / kBlk;
-    bwd_dkdv_kernel<<<dim3(nb, p.Hk, p.B), kThreads, kSmemBytes, stream>>>(tq, tdo, p);
+    bwd_dkdv_kernel<<<dim3((p.S + kKvKeys - 1) / kKvKeys, p.Hk, p.B), kKvThreads, kKvSmemBytes, stream>>>(
+        tk128, tv128, tq, tdo, p);
     if ((e = cudaGetLastError()) != cudaSuccess)
         return e;
     bwd_dq_kernel<<<dim3((p.S + kDqRows - 1) / kDqRows, p.Hq, p.B), kDqThreads, kDqSmemBytes, stream>>>(

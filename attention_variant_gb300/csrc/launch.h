@@ -142,7 +142,8 @@ cudaError_t launch_evo(const CUtensorMap &tq, const CUtensorMap &tk, const CUten
 int evo_max_bias_keys();
 cudaError_t launch_bwd(const CUtensorMap &tq, const CUtensorMap &tdo, const CUtensorMap &tk,
                        const CUtensorMap &tv, const CUtensorMap &tq128, const CUtensorMap &tdo128,
-                       const BwdParams &p, cudaStream_t stream);
+                       const CUtensorMap &tk128, const CUtensorMap &tv128, const BwdParams &p,
+                       cudaStream_t stream);
 #endif
 
 // Keys per K/V tile of the standard kernel (its TMEM budget: see fwd_standard.cu),

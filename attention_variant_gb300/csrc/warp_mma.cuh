@@ -1,5 +1,5 @@
-// warp_mma.cuh -- warp-level bf16 tensor-core helpers for the kernels whose
-// contractions are a few rows per warp (decode, backward): ldmatrix fragment
+// warp_mma.cuh -- warp-level bf16 tensor-core helpers for kernels whose
+// contractions are a few rows per warp (the decode kernel): ldmatrix fragment
 // loads from 128-byte-swizzled shared-memory tiles and the m16n8k16 MMA with
 // fp32 accumulation.
 //
