@@ -817,15 +817,15 @@ fl_status bwd_plan(const fl_tensor *q, const fl_tensor *k, const fl_tensor *v,
         return fail(FL_ERR_UNSUPPORTED, "the backward supports the standard kind");
     if (d->score_mod != FL_MOD_NONE)
         return fail(FL_ERR_UNSUPPORTED, "the backward supports score_mod none");
-    if (d->mask != FL_MASK_NONE && d->mask != FL_MASK_CAUSAL)
-        return fail(FL_ERR_UNSUPPORTED, "the backward supports mask none or causal");
+    if ((s = check_mask(d)) != FL_OK)
+        return s;
     if (d->gqa_group != 0 && d->gqa_group != pl.Hq / pl.Hk)
         return fail(FL_ERR_INVALID_ARG, "gqa_group does not match Hq / Hk");
     if (!std::isfinite(d->scale) || d->scale < 0.f)
         return fail(FL_ERR_INVALID_ARG, "scale must be finite and positive (0 selects 1/sqrt(D))");
     // padded to the dQ kernel's 128-row query tiles (a multiple of kBwdBlock)
     pl.S_pad = (pl.S + 127) / 128 * 128;
-    pl.total = (size_t(pl.B) * size_t(pl.Hq) * size_t(pl.S_pad) * 8 + 255) / 256 * 256;
+    pl.total = (size_t(pl.B) * size_t(pl.Hq) * size_t(pl.S_pad) * sizeof(fl::BwdRowStat) + 255) / 256 * 256;
     return FL_OK;
 }
 
@@ -903,7 +903,12 @@ fl_status fl_attn_bwd(const fl_tensor *q, const fl_tensor *k, const fl_tensor *v
     p.Hk = int(pl.Hk);
     p.S = int(pl.S);
     p.S_pad = int(pl.S_pad);
-    p.causal = desc->mask == FL_MASK_CAUSAL;
+    p.mask.kind = desc->mask;
+    p.mask.S = int(pl.S);
+    p.mask.window = desc->window;
+    p.mask.prefix = desc->prefix;
+    p.mask.doc = desc->doc_offsets;
+    p.mask.doc_stride = desc->doc_stride;
     p.scale = desc->scale != 0.f ? desc->scale : 0.125f; // 1 / sqrt(64)
     auto strides3 = [](const View &t, int64_t &sb, int64_t &ss, int64_t &sh) {
         sb = t.stride[0];
@@ -929,7 +934,7 @@ fl_status fl_attn_bwd(const fl_tensor *q, const fl_tensor *k, const fl_tensor *v
     strides3(DK, p.dk_sb, p.dk_ss, p.dk_sh);
     p.dv = static_cast<__nv_bfloat16 *>(DV.ptr);
     strides3(DV, p.dv_sb, p.dv_ss, p.dv_sh);
-    p.ws_stats = static_cast<float *>(workspace);
+    p.ws_stats = static_cast<fl::BwdRowStat *>(workspace);
     p.err_user = desc->error_word;
     p.timeout_ns = timeout_ns(desc);
     // all four again with 128-row boxes (the dQ kernel's query tiles, the

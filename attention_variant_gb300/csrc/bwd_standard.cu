@@ -1,5 +1,5 @@
 // bwd_standard.cu -- attention backward for the standard kind (MHA / GQA,
-// D = Dv = 64, no mask or causal): dQ, dK, dV from Q, K, V, the forward's O
+// D = Dv = 64, every mask of the forward): dQ, dK, dV from Q, K, V, the forward's O
 // and natural-log LSE, and dO.  The pages name training (the backward pass)
 // as the next step for the fused kernels (gist.science summary, "Limitations
 // and future work"); the gradients are those of
@@ -12,11 +12,14 @@
 // with GQA heads summed into their shared K/V head.
 //
 // Three kernels, no atomics (every output element has one writer):
-//   bwd_prep_kernel  per query row: D_i and LSE_i * log2 e into the workspace
-//                    (padded rows get +inf, so their P is 0);
+//   bwd_prep_kernel  per query row: D_i, LSE_i * log2 e and the row's allowed
+//                    key interval [lo_i, hi_i) into the workspace (padded
+//                    rows get LSE +inf, so their P is 0, and the empty
+//                    interval [S, S));
 //   bwd_dkdv_kernel  one CTA per (128-key tile, KV head, batch): dK and dV
 //                    accumulate in TMEM over every 64-row query tile of every
-//                    query head of the group (causal: from the diagonal on);
+//                    query head of the group whose rows allow a key of the
+//                    tile;
 //   bwd_dq_kernel    one CTA per (128-row query tile, query head, batch): dQ
 //                    accumulates in TMEM over the 64-key tiles.
 // Both main kernels run on the tcgen05 tensor cores with the same layout of
@@ -40,6 +43,42 @@ constexpr uint32_t kTileBytes = kBwdBlock * 64 * 2; // one 64-row tile, 8 KB
 
 __device__ uint32_t g_lib_error_word;
 
+// Query rows [qa, qb) that allow at least one key of [k0, k1) (k0 < k1 <= S).
+// Row i allows [lo_i, hi_i) with both bounds non-decreasing in i, so the rows
+// are those with hi_i > k0 and lo_i < k1: from the first row whose interval
+// reaches k0 to the first row whose interval starts at or after k1.
+__device__ __forceinline__ void key_block_query_range(const MaskSpec &m, int b, int k0, int k1, int &qa, int &qb)
+{
+    qa = 0;
+    qb = m.S;
+    switch (m.kind) {
+    case MASK_NONE:
+        break;
+    case MASK_CAUSAL:
+        qa = k0;
+        break;
+    case MASK_WINDOW:
+        qa = k0;
+        qb = min(m.S, k1 - 1 + m.window);
+        break;
+    case MASK_PREFIX:
+        qa = k0 < m.prefix ? 0 : k0;
+        break;
+    default: { // MASK_DOC: up to the first document start at or after k1
+        qa = k0;
+        const int32_t *st = m.doc + static_cast<int64_t>(b) * m.doc_stride;
+        for (int t = 0; t < m.doc_stride; ++t) {
+            const int s0 = __ldg(st + t);
+            if (s0 >= k1) {
+                qb = min(qb, s0);
+                break;
+            }
+        }
+        break;
+    }
+    }
+}
+
 // ---------------------------------------------------------------- prep
 
 __global__ void __launch_bounds__(128) bwd_prep_kernel(const BwdParams p)
@@ -52,7 +91,9 @@ __global__ void __launch_bounds__(128) bwd_prep_kernel(const BwdParams p)
     const int i = static_cast<int>(idx % p.S_pad);
     const int64_t bh = idx / p.S_pad;
     const int h = static_cast<int>(bh % p.Hq), b = static_cast<int>(bh / p.Hq);
-    float2 st = make_float2(__int_as_float(0x7f800000), 0.f); // padded: P = 0
+    // padded rows: P = 0 and the empty key interval [S, S), which keeps both
+    // interval bounds non-decreasing over the rows (tile tests rely on it)
+    BwdRowStat st{__int_as_float(0x7f800000), 0.f, p.S, p.S};
     if (i < p.S) {
         const uint4 *o4 = reinterpret_cast<const uint4 *>(p.o + b * p.o_sb + i * p.o_ss + h * p.o_sh);
         const uint4 *d4 = reinterpret_cast<const uint4 *>(p.dout + b * p.do_sb + i * p.do_ss + h * p.do_sh);
@@ -69,9 +110,11 @@ __global__ void __launch_bounds__(128) bwd_prep_kernel(const BwdParams p)
         }
         const float lse = p.lse[b * p.l_sb + h * p.l_sh + i];
         // a row with no allowed key (LSE = -inf) has P = 0 everywhere
-        st = make_float2(lse == kNegInf ? __int_as_float(0x7f800000) : lse * kLog2e, acc);
+        st.lse2 = lse == kNegInf ? __int_as_float(0x7f800000) : lse * kLog2e;
+        st.d = acc;
+        row_interval(p.mask, b, i, st.lo, st.hi);
     }
-    reinterpret_cast<float2 *>(p.ws_stats)[idx] = st;
+    p.ws_stats[idx] = st;
 }
 
 // ---------------------------------------------------------------- dQ (tcgen05)
@@ -117,9 +160,10 @@ __global__ void __launch_bounds__(kDqThreads, 1)
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int q0 = qt * kDqRows;
     const int hk = h / (p.Hq / p.Hk);
-    const int nkb = (p.S + kDqKeys - 1) / kDqKeys;
-    // causal: key tiles wholly after the last row of the query tile see none
-    const int n_it = p.causal ? min(nkb, (q0 + kDqRows + kDqKeys - 1) / kDqKeys) : nkb;
+    // the key tiles holding an allowed pair of the tile's rows, and the span
+    // of keys every row allows (tiles inside it need no mask)
+    const TileRange tr = q_block_range<kDqKeys>(p.mask, b, q0);
+    const int n_it = max(tr.hi - tr.lo, 0);
 
     extern __shared__ uint8_t smem_raw[];
     const uint32_t base = ptx::smem_u32(smem_raw);
@@ -174,8 +218,8 @@ __global__ void __launch_bounds__(kDqThreads, 1)
             }
             if (lane == 0) {
                 ptx::mbar_arrive_expect_tx(bar(sm.kv_full[s]), 2 * kTileBytes);
-                ptx::tma_load_4d(ptx::smem_u32(sm.k[s]), &tm_k, bar(sm.kv_full[s]), 0, j * kDqKeys, hk, b);
-                ptx::tma_load_4d(ptx::smem_u32(sm.v[s]), &tm_v, bar(sm.kv_full[s]), 0, j * kDqKeys, hk, b);
+                ptx::tma_load_4d(ptx::smem_u32(sm.k[s]), &tm_k, bar(sm.kv_full[s]), 0, (tr.lo + j) * kDqKeys, hk, b);
+                ptx::tma_load_4d(ptx::smem_u32(sm.v[s]), &tm_v, bar(sm.kv_full[s]), 0, (tr.lo + j) * kDqKeys, hk, b);
             }
             __syncwarp();
             issued = j + 1;
@@ -255,7 +299,7 @@ __global__ void __launch_bounds__(kDqThreads, 1)
         const int r = 32 * (warp & 3) + lane;
         const int row = q0 + r;
         const uint32_t lane_off = static_cast<uint32_t>(32 * (warp & 3)) << 16;
-        const float2 st = reinterpret_cast<const float2 *>(p.ws_stats)[(static_cast<int64_t>(b) * p.Hq + h) * p.S_pad + row];
+        const BwdRowStat st = p.ws_stats[(static_cast<int64_t>(b) * p.Hq + h) * p.S_pad + row];
         const float sl2 = p.scale * kLog2e;
         for (int j = wg; j < n_it; j += 2) {
             const int u = j & 1;
@@ -274,8 +318,8 @@ __global__ void __launch_bounds__(kDqThreads, 1)
             ptx::reg_fence<64>(pv);
             ptx::tc_fence_before();
             ptx::mbar_arrive(bar(sm.s_free[u]));
-            const int j0 = j * kDqKeys;
-            const bool edge = j0 + kDqKeys > p.S || (p.causal && j0 + kDqKeys - 1 > q0);
+            const int j0 = (tr.lo + j) * kDqKeys;
+            const bool edge = !(j0 >= tr.full_lo && j0 + kDqKeys <= tr.full_hi);
             uint32_t ds[32];
 #pragma unroll
             for (int c = 0; c < 32; ++c) {
@@ -283,9 +327,9 @@ __global__ void __launch_bounds__(kDqThreads, 1)
 #pragma unroll
                 for (int e = 0; e < 2; ++e) {
                     const int col = 2 * c + e;
-                    const float pr = ptx::ex2(fmaf(__uint_as_float(sv[col]), sl2, -st.x));
-                    float dsv = pr * (__uint_as_float(pv[col]) - st.y);
-                    if (edge && (j0 + col >= p.S || (p.causal && j0 + col > row)))
+                    const float pr = ptx::ex2(fmaf(__uint_as_float(sv[col]), sl2, -st.lse2));
+                    float dsv = pr * (__uint_as_float(pv[col]) - st.d);
+                    if (edge && (j0 + col < st.lo || j0 + col >= st.hi))
                         dsv = 0.f;
                     d2[e] = dsv;
                 }
@@ -313,6 +357,7 @@ __global__ void __launch_bounds__(kDqThreads, 1)
             ptx::tmem_ld32(tmem + lane_off + kColDq + 32 * wg, o);
             ptx::tmem_wait_ld();
             ptx::reg_fence<32>(o);
+            const float f = n_it > 0 ? p.scale : 0.f; // no visited tile: dQ = 0
             uint4 *dst = reinterpret_cast<uint4 *>(p.dq + b * p.dq_sb + static_cast<int64_t>(row) * p.dq_ss +
                                                    h * p.dq_sh + 32 * wg);
 #pragma unroll
@@ -320,8 +365,8 @@ __global__ void __launch_bounds__(kDqThreads, 1)
                 uint32_t w[4];
 #pragma unroll
                 for (int q = 0; q < 4; ++q)
-                    w[q] = ptx::pack_bf16(__uint_as_float(o[8 * c + 2 * q]) * p.scale,
-                                          __uint_as_float(o[8 * c + 2 * q + 1]) * p.scale);
+                    w[q] = ptx::pack_bf16(__uint_as_float(o[8 * c + 2 * q]) * f,
+                                          __uint_as_float(o[8 * c + 2 * q + 1]) * f);
                 if (row < p.S)
                     dst[c] = make_uint4(w[0], w[1], w[2], w[3]);
             }
@@ -340,8 +385,8 @@ __global__ void __launch_bounds__(kDqThreads, 1)
 // One CTA per (128-key tile, KV head, batch), twelve warps; the key tile is
 // the MMA's M side (TMEM lane = key):
 //   warp 0     TMA producer: the K and V tiles once, then for every query
-//              tile of 64 rows of every query head of the group (causal:
-//              from the key tile's diagonal on) the Q and dO tiles through a
+//              tile of 64 rows of every query head of the group that holds
+//              an allowed pair with the key tile, the Q and dO tiles through a
 //              kKvStages ring, with the rows' (LSE log2 e, D) copied by the
 //              warp's lanes;
 //   warps 1-3  MMA issuers: warp 1 S^T(i) = K Q_i^T, warp 2 dP^T(i) =
@@ -364,7 +409,7 @@ struct __align__(1024) DkvSmem {
     uint8_t v[kKvTile];
     uint8_t q[kKvStages][kTileBytes];
     uint8_t dout[kKvStages][kTileBytes];
-    float2 stats[kKvStages][kKvQ];
+    BwdRowStat stats[kKvStages][kKvQ];
     uint64_t kv_full, st_full[kKvStages], st_empty[kKvStages];
     uint64_t s_full[2], s_free[2], pds_full[2], acc_done[2], mma_done;
     uint32_t tmem_base;
@@ -381,8 +426,12 @@ __global__ void __launch_bounds__(kKvThreads, 1)
     const int k0 = kt * kKvKeys;
     const int G = p.Hq / p.Hk;
     const int nq = p.S_pad / kKvQ;
-    const int qj0 = p.causal ? k0 / kKvQ : 0; // earlier query tiles see none of these keys
-    const int n_qt = nq - qj0;
+    // the query tiles whose rows allow a key of this tile (row intervals never
+    // decrease with the row, so those rows form one interval)
+    int qa, qb;
+    key_block_query_range(p.mask, b, k0, min(k0 + kKvKeys, p.S), qa, qb);
+    const int qj0 = qa / kKvQ;
+    const int n_qt = max((qb + kKvQ - 1) / kKvQ - qj0, 0);
     const int n_it = G * n_qt;
 
     extern __shared__ uint8_t smem_raw[];
@@ -437,8 +486,7 @@ __global__ void __launch_bounds__(kKvThreads, 1)
                 ok = false;
                 break;
             }
-            const float2 *src = reinterpret_cast<const float2 *>(p.ws_stats) +
-                                (static_cast<int64_t>(b) * p.Hq + h) * p.S_pad + q0;
+            const BwdRowStat *src = p.ws_stats + (static_cast<int64_t>(b) * p.Hq + h) * p.S_pad + q0;
             sm.stats[s][lane] = src[lane];
             sm.stats[s][lane + 32] = src[lane + 32];
             __syncwarp();
@@ -527,12 +575,17 @@ __global__ void __launch_bounds__(kKvThreads, 1)
         for (int i = wg; i < n_it; i += 2) {
             const int s = i % kKvStages, u = i & 1;
             const int q0 = (qj0 + i % n_qt) * kKvQ;
-            if (!warp_wait(bar(sm.s_full[u]), (i >> 1) & 1, wc, W_S_FULL)) {
+            // the stage's row statistics (written by the producer warp before
+            // it armed st_full) and the tile's S^T, dP^T
+            if (!warp_wait(bar(sm.st_full[s]), (i / kKvStages) & 1, wc, W_KV_FULL) ||
+                !warp_wait(bar(sm.s_full[u]), (i >> 1) & 1, wc, W_S_FULL)) {
                 ok = false;
                 break;
             }
             ptx::tc_fence_after();
-            const bool edge = p.causal && q0 < k0 + kKvKeys; // holds pairs with query < key
+            // no masked pair in the tile iff its first row allows keys up to the
+            // tile's end and its last row allows keys from the tile's start
+            const bool edge = !(sm.stats[s][0].hi >= k0 + kKvKeys && sm.stats[s][kKvQ - 1].lo <= k0);
             uint32_t pa[32], da[32];
 #pragma unroll
             for (int half = 0; half < 2; ++half) {
@@ -548,12 +601,12 @@ __global__ void __launch_bounds__(kKvThreads, 1)
 #pragma unroll
                     for (int e = 0; e < 2; ++e) {
                         const int c = 32 * half + 2 * c2 + e;
-                        const float2 st = sm.stats[s][c];
-                        float pr = ptx::ex2(fmaf(__uint_as_float(sv[2 * c2 + e]), sl2, -st.x));
-                        if (edge && q0 + c < key)
+                        const BwdRowStat st = sm.stats[s][c];
+                        float pr = ptx::ex2(fmaf(__uint_as_float(sv[2 * c2 + e]), sl2, -st.lse2));
+                        if (edge && (key < st.lo || key >= st.hi))
                             pr = 0.f;
                         pp[e] = pr;
-                        dd[e] = pr * (__uint_as_float(pv[2 * c2 + e]) - st.y);
+                        dd[e] = pr * (__uint_as_float(pv[2 * c2 + e]) - st.d);
                     }
                     pa[16 * half + c2] = ptx::pack_bf16(pp[0], pp[1]);
                     da[16 * half + c2] = ptx::pack_bf16(dd[0], dd[1]);
@@ -585,7 +638,7 @@ __global__ void __launch_bounds__(kKvThreads, 1)
             ptx::tmem_ld32(tmem + lane_off + col + 32, o + 32);
             ptx::tmem_wait_ld();
             ptx::reg_fence<64>(o);
-            const float f = wg == 0 ? 1.f : p.scale;
+            const float f = n_it > 0 ? (wg == 0 ? 1.f : p.scale) : 0.f; // no visited tile: 0
             __nv_bfloat16 *dst = wg == 0 ? p.dv + b * p.dv_sb + static_cast<int64_t>(key) * p.dv_ss + hk * p.dv_sh
                                          : p.dk + b * p.dk_sb + static_cast<int64_t>(key) * p.dk_ss + hk * p.dk_sh;
 #pragma unroll

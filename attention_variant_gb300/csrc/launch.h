@@ -84,9 +84,16 @@ struct EvoParams {
 // ---- backward of the standard kind (bwd_standard.cu)
 constexpr int kBwdBlock = 64; // query / key rows per tile
 
+// Per query row of the backward's workspace: LSE log2 e, rowsum(dO O) and the
+// row's allowed key interval [lo, hi).
+struct BwdRowStat {
+    float lse2, d;
+    int lo, hi;
+};
+
 struct BwdParams {
     int B, Hq, Hk, S, S_pad;      // S_pad: S rounded up to 128 (a multiple of kBwdBlock)
-    int causal;
+    MaskSpec mask;
     float scale;
     const __nv_bfloat16 *q, *k, *v, *o, *dout; // element strides (batch, position, head):
     int64_t q_sb, q_ss, q_sh, k_sb, k_ss, k_sh, v_sb, v_ss, v_sh;
@@ -95,7 +102,7 @@ struct BwdParams {
     int64_t l_sb, l_sh;
     __nv_bfloat16 *dq, *dk, *dv;
     int64_t dq_sb, dq_ss, dq_sh, dk_sb, dk_ss, dk_sh, dv_sb, dv_ss, dv_sh;
-    float *ws_stats;              // [B][Hq][S_pad] x (LSE log2 e, rowsum(dO O))
+    BwdRowStat *ws_stats;         // [B][Hq][S_pad]
     uint32_t *err_user;
     uint64_t timeout_ns;
 };

@@ -253,10 +253,31 @@ if __name__ == "__main__":  # pragma: no cover
     print(build(force="--force" in sys.argv))
 
 
-def attention_bwd(q, k, v, dout, *, mask="none", scale=0.0):
+def _allowed(mask, S, b, window, prefix, doc_offsets):
+    """Boolean [S, S] matrix of allowed (query i, key j) pairs, from the mask
+    predicates (the same definitions fl_oracle.c states)."""
+    i = np.arange(S)[:, None]
+    j = np.arange(S)[None, :]
+    if mask == "none":
+        return np.ones((S, S), dtype=bool)
+    if mask == "causal":
+        return j <= i
+    if mask == "window":
+        return (j <= i) & (i - j < window)
+    if mask == "prefix":
+        return (j <= i) | (j < prefix)
+    if mask == "doc":
+        starts = np.asarray(doc_offsets)[b]
+        doc = np.searchsorted(starts, np.arange(S), side="right") - 1  # starts <= x, minus one
+        return (j <= i) & (doc[:, None] == doc[None, :])
+    raise ValueError(mask)
+
+
+def attention_bwd(q, k, v, dout, *, mask="none", window=0, prefix=0, doc_offsets=None, scale=0.0):
     """Gradients dQ, dK, dV (float64) of ``O = softmax(scale Q K^T + mask) V``
     for ``q [B,S,Hq,D]``, ``k, v [B,S,Hk,D]`` and the output gradient
-    ``dout [B,S,Hq,D]`` (all bf16 bits), mask ``none`` or ``causal``.
+    ``dout [B,S,Hq,D]`` (all bf16 bits), with any mask of ``attention``
+    (none, causal, window, prefix, doc).
 
     The plain definition per (batch, query head): the full probability matrix
     P (two-pass softmax), dV = P^T dO, dP = dO V^T, dS_ij = P_ij (dP_ij -
@@ -264,8 +285,6 @@ def attention_bwd(q, k, v, dout, *, mask="none", scale=0.0):
     a K/V head add their dK and dV (gist.science summary, "Limitations and
     future work": the backward pass is the fused kernels' next step).
     """
-    if mask not in ("none", "causal"):
-        raise ValueError("mask must be none or causal")
     wid = lambda x: (np.asarray(x, dtype=np.uint16).astype(np.uint32) << 16).view(np.float32) \
         .astype(np.float64)
     Q, K, V, dO = wid(q), wid(k), wid(v), wid(dout)
@@ -276,13 +295,12 @@ def attention_bwd(q, k, v, dout, *, mask="none", scale=0.0):
     dQ = np.zeros_like(Q)
     dK = np.zeros_like(K)
     dV = np.zeros_like(V)
-    causal = np.tril(np.ones((S, S), dtype=bool))
     for b in range(B):
+        allowed = _allowed(mask, S, b, window, prefix, doc_offsets)
         for h in range(Hq):
             kh = h // G
             z = s * (Q[b, :, h] @ K[b, :, kh].T)
-            if mask == "causal":
-                z = np.where(causal, z, -np.inf)
+            z = np.where(allowed, z, -np.inf)
             m = z.max(axis=1, keepdims=True)
             e = np.exp(z - m)
             P = e / e.sum(axis=1, keepdims=True)

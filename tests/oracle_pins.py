@@ -477,6 +477,29 @@ def pin_backward(lib):
         o.backward(torch.from_numpy(_f64(do)).permute(0, 2, 1, 3))
         for name, mine, ref in (("dQ", dq, Q.grad), ("dK", dk, K.grad), ("dV", dv, V.grad)):
             _close(mine, ref.permute(0, 2, 1, 3).numpy(), atol=1e-10, what=f"backward {name} {mask}")
+    # the other masks against autograd of SDPA with the same boolean mask
+    B, S, Hq, Hk, D = 2, 70, 2, 1, 32
+    q, k, v = _rand((B, S, Hq, D), "mq2"), _rand((B, S, Hk, D), "mk2"), _rand((B, S, Hk, D), "mv2")
+    do = _rand((B, S, Hq, D), "mdo2")
+    doc = np.array([[0, 13, 14, 50, S], [0, 40, S, S, S]], dtype=np.int32)
+    for mask, kw in (("window", dict(window=9)), ("prefix", dict(prefix=21)), ("doc", dict(doc_offsets=doc))):
+        dq, dk, dv = oracle.attention_bwd(q, k, v, do, mask=mask, **kw)
+        allowed = np.stack([oracle._allowed(mask, S, b, kw.get("window", 0), kw.get("prefix", 0),
+                                            kw.get("doc_offsets")) for b in range(B)])[:, None]
+        Q, K, V = (torch.from_numpy(_f64(x)).permute(0, 2, 1, 3).requires_grad_(True) for x in (q, k, v))
+        o = torch.nn.functional.scaled_dot_product_attention(Q, K, V, attn_mask=torch.from_numpy(allowed),
+                                                             enable_gqa=True)
+        o.backward(torch.from_numpy(_f64(do)).permute(0, 2, 1, 3))
+        for name, mine, ref in (("dQ", dq, Q.grad), ("dK", dk, K.grad), ("dV", dv, V.grad)):
+            _close(mine, ref.permute(0, 2, 1, 3).numpy(), atol=1e-10, what=f"backward {name} {mask}")
+        # the mask matrix itself from the interval form of each mask
+        for b in range(B):
+            for i in (0, 9, 21, 40, 69):
+                lo, hi = _allowed_range(mask, i, S, kw.get("window", 0), kw.get("prefix", 0),
+                                        list(doc[b][doc[b] < S]) if mask == "doc" else None)
+                row = np.zeros(S, dtype=bool)
+                row[lo:hi] = True
+                assert np.array_equal(allowed[b, 0, i], row), f"{mask} row {i}"
     # finite differences of L = sum(dO * O) with respect to one entry of each input
     B, S, Hq, Hk, D = 1, 6, 2, 1, 8
     q, k, v = _rand((B, S, Hq, D), "fq"), _rand((B, S, Hk, D), "fk"), _rand((B, S, Hk, D), "fv")

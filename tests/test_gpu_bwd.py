@@ -25,7 +25,7 @@ from tests import gpu_util as gu  # noqa: E402
 import attention_variant_gb300 as fa  # noqa: E402
 
 
-def _run(tag, B, S, Hq, Hk, mask):
+def _run(tag, B, S, Hq, Hk, mask, **mkw):
     q = testdata.normal_bf16((B, S, Hq, 64), f"bwd_{tag}", "q")
     k = testdata.normal_bf16((B, S, Hk, 64), f"bwd_{tag}", "k")
     v = testdata.normal_bf16((B, S, Hk, 64), f"bwd_{tag}", "v")
@@ -34,7 +34,9 @@ def _run(tag, B, S, Hq, Hk, mask):
     out = torch.empty((B, S, Hq, 64), dtype=torch.bfloat16, device="cuda")
     lse = torch.empty((B, Hq, S), dtype=torch.float32, device="cuda")
     err = torch.zeros(1, dtype=torch.int32, device="cuda")
-    d = fa.make_desc(mask=mask, error_word=err)
+    doc = mkw.pop("doc_offsets", None)
+    doc_t = torch.from_numpy(doc).cuda() if doc is not None else None
+    d = fa.make_desc(mask=mask, error_word=err, doc_offsets=doc_t, **mkw)
     fa.fl_attn_fwd(qd, kd, vd, out, lse, d)
     dq = torch.full_like(qd, float("nan"))
     dk = torch.full_like(kd, float("nan"))
@@ -44,7 +46,7 @@ def _run(tag, B, S, Hq, Hk, mask):
     fa.fl_attn_bwd(qd, kd, vd, out, lse, dod, dq, dk, dv, d, ws)
     torch.cuda.synchronize()
     assert int(err.item()) == 0
-    ref = oracle.attention_bwd(q, k, v, do, mask=mask)
+    ref = oracle.attention_bwd(q, k, v, do, mask=mask, doc_offsets=doc, **mkw)
     return (gu.f64(dq), gu.f64(dk), gu.f64(dv)), ref
 
 
@@ -63,6 +65,16 @@ def _check(got, ref, what):
                                        (3, 5, 2, 2)])
 def test_backward_matches_oracle(B, S, Hq, Hk, mask):
     got, ref = _run(f"{B}_{S}_{Hq}_{Hk}_{mask}", B, S, Hq, Hk, mask)
+    _check(got, ref, f"B{B} S{S} Hq{Hq} Hk{Hk} {mask}")
+
+
+@pytest.mark.parametrize("mask,kw", [("window", dict(window=100)), ("prefix", dict(prefix=150)),
+                                     ("doc", None)])
+@pytest.mark.parametrize("B,S,Hq,Hk", [(2, 333, 2, 2), (1, 700, 4, 2)])
+def test_backward_other_masks(B, S, Hq, Hk, mask, kw):
+    if mask == "doc":
+        kw = dict(doc_offsets=testdata.doc_offsets(S, B, f"bwd_doc_{S}", 20, 200))
+    got, ref = _run(f"{B}_{S}_{Hq}_{Hk}_{mask}", B, S, Hq, Hk, mask, **kw)
     _check(got, ref, f"B{B} S{S} Hq{Hq} Hk{Hk} {mask}")
 
 

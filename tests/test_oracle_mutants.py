@@ -114,3 +114,25 @@ def test_bwd_mutant_is_caught(name, monkeypatch):
     monkeypatch.setattr(oracle, "attention_bwd", ns["attention_bwd"])
     with pytest.raises((AssertionError, ValueError, IndexError)):
         oracle_pins.pin_backward(oracle.load())
+
+
+ALLOWED_MUTANTS = {
+    "allowed_window_inclusive": ("(i - j < window)", "(i - j <= window)"),
+    "allowed_prefix_inclusive": ("(j < prefix)", "(j <= prefix)"),
+    "allowed_doc_side_left": ('side="right"', 'side="left"'),
+}
+
+
+@pytest.mark.parametrize("name", sorted(ALLOWED_MUTANTS))
+def test_allowed_mutant_is_caught(name, monkeypatch):
+    import inspect
+    import textwrap
+
+    src = textwrap.dedent(inspect.getsource(oracle._allowed))
+    a, b = ALLOWED_MUTANTS[name]
+    assert a in src, name
+    ns = dict(vars(oracle))
+    exec(compile(src.replace(a, b), "<mutant>", "exec"), ns)
+    monkeypatch.setattr(oracle, "_allowed", ns["_allowed"])
+    with pytest.raises(AssertionError):
+        oracle_pins.pin_backward(oracle.load())
