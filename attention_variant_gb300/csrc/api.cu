@@ -815,8 +815,10 @@ fl_status bwd_plan(const fl_tensor *q, const fl_tensor *k, const fl_tensor *v,
                     (long long)pl.Hq, (long long)pl.Hk);
     if (d->kind != FL_KIND_STANDARD)
         return fail(FL_ERR_UNSUPPORTED, "the backward supports the standard kind");
-    if (d->score_mod != FL_MOD_NONE)
-        return fail(FL_ERR_UNSUPPORTED, "the backward supports score_mod none");
+    if (d->score_mod != FL_MOD_NONE && d->score_mod != FL_MOD_ALIBI && d->score_mod != FL_MOD_SOFTCAP)
+        return fail(FL_ERR_UNSUPPORTED, "the backward supports score_mod none, ALiBi or softcap");
+    if (d->score_mod == FL_MOD_SOFTCAP && !(d->softcap > 0.f && std::isfinite(d->softcap)))
+        return fail(FL_ERR_INVALID_ARG, "softcap must be positive and finite");
     if ((s = check_mask(d)) != FL_OK)
         return s;
     if (d->gqa_group != 0 && d->gqa_group != pl.Hq / pl.Hk)
@@ -903,6 +905,10 @@ fl_status fl_attn_bwd(const fl_tensor *q, const fl_tensor *k, const fl_tensor *v
     p.Hk = int(pl.Hk);
     p.S = int(pl.S);
     p.S_pad = int(pl.S_pad);
+    p.score_mod = desc->score_mod;
+    p.softcap = desc->score_mod == FL_MOD_SOFTCAP ? desc->softcap : 0.f;
+    p.alibi_slopes = desc->alibi_slopes;
+    p.alibi_exp_coef = -8.0f / float(pl.Hq);
     p.mask.kind = desc->mask;
     p.mask.S = int(pl.S);
     p.mask.window = desc->window;

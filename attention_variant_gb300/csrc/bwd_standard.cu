@@ -79,6 +79,44 @@ __device__ __forceinline__ void key_block_query_range(const MaskSpec &m, int b, 
     }
 }
 
+// The score_mod in the backward: the logit (log2 units) of raw score x = q.k
+// for query i and key j, and the chain factor dz/du turning dL/dz into dL/du
+// (u = scale x): 1 for none and ALiBi (an additive bias), 1 - tanh^2(u / cap)
+// for softcap.  tanh(v) = 1 - 2 / (1 + e^(2v)) as in the forward.
+struct ModCtx {
+    float sl2;     // scale log2 e
+    float alibi_c; // slope_h log2 e
+    float cap_in;  // 2 scale log2 e / cap
+    float cap_out; // cap log2 e
+};
+
+template <int MOD>
+__device__ __forceinline__ float mod_logit2(const ModCtx &m, float x, int i, int j, float &chain)
+{
+    if constexpr (MOD == MOD_SOFTCAP) {
+        const float th = 1.f - 2.f * ptx::rcp_approx(1.f + ptx::ex2(x * m.cap_in));
+        chain = 1.f - th * th;
+        return m.cap_out * th;
+    } else if constexpr (MOD == MOD_ALIBI) {
+        chain = 1.f;
+        return fmaf(x, m.sl2, -m.alibi_c * fabsf(static_cast<float>(i - j)));
+    } else {
+        chain = 1.f;
+        return x * m.sl2;
+    }
+}
+
+__device__ __forceinline__ ModCtx mod_ctx(const BwdParams &p, int h)
+{
+    ModCtx m;
+    m.sl2 = p.scale * kLog2e;
+    const float slope = p.alibi_slopes ? __ldg(p.alibi_slopes + h) : exp2f(p.alibi_exp_coef * static_cast<float>(h + 1));
+    m.alibi_c = slope * kLog2e;
+    m.cap_in = p.softcap > 0.f ? 2.f * p.scale * kLog2e / p.softcap : 0.f;
+    m.cap_out = p.softcap * kLog2e;
+    return m;
+}
+
 // ---------------------------------------------------------------- prep
 
 __global__ void __launch_bounds__(128) bwd_prep_kernel(const BwdParams p)
@@ -151,6 +189,7 @@ struct __align__(1024) DqSmem {
     uint32_t abort_flag;
 };
 
+template <int MOD>
 __global__ void __launch_bounds__(kDqThreads, 1)
     bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_do,
                   const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
@@ -300,7 +339,7 @@ __global__ void __launch_bounds__(kDqThreads, 1)
         const int row = q0 + r;
         const uint32_t lane_off = static_cast<uint32_t>(32 * (warp & 3)) << 16;
         const BwdRowStat st = p.ws_stats[(static_cast<int64_t>(b) * p.Hq + h) * p.S_pad + row];
-        const float sl2 = p.scale * kLog2e;
+        const ModCtx mc = mod_ctx(p, h);
         for (int j = wg; j < n_it; j += 2) {
             const int u = j & 1;
             if (!warp_wait(bar(sm.s_full[u]), (j >> 1) & 1, wc, W_S_FULL)) {
@@ -327,8 +366,10 @@ __global__ void __launch_bounds__(kDqThreads, 1)
 #pragma unroll
                 for (int e = 0; e < 2; ++e) {
                     const int col = 2 * c + e;
-                    const float pr = ptx::ex2(fmaf(__uint_as_float(sv[col]), sl2, -st.lse2));
-                    float dsv = pr * (__uint_as_float(pv[col]) - st.d);
+                    float chain;
+                    const float t = mod_logit2<MOD>(mc, __uint_as_float(sv[col]), row, j0 + col, chain);
+                    const float pr = ptx::ex2(t - st.lse2);
+                    float dsv = pr * (__uint_as_float(pv[col]) - st.d) * chain;
                     if (edge && (j0 + col < st.lo || j0 + col >= st.hi))
                         dsv = 0.f;
                     d2[e] = dsv;
@@ -416,6 +457,7 @@ struct __align__(1024) DkvSmem {
     uint32_t abort_flag;
 };
 
+template <int MOD>
 __global__ void __launch_bounds__(kKvThreads, 1)
     bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
                     const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_do,
@@ -571,10 +613,10 @@ __global__ void __launch_bounds__(kKvThreads, 1)
         const int r = 32 * (warp & 3) + lane;
         const int key = k0 + r;
         const uint32_t lane_off = static_cast<uint32_t>(32 * (warp & 3)) << 16;
-        const float sl2 = p.scale * kLog2e;
         for (int i = wg; i < n_it; i += 2) {
             const int s = i % kKvStages, u = i & 1;
             const int q0 = (qj0 + i % n_qt) * kKvQ;
+            const ModCtx mc = mod_ctx(p, hk * G + i / n_qt);
             // the stage's row statistics (written by the producer warp before
             // it armed st_full) and the tile's S^T, dP^T
             if (!warp_wait(bar(sm.st_full[s]), (i / kKvStages) & 1, wc, W_KV_FULL) ||
@@ -602,11 +644,13 @@ __global__ void __launch_bounds__(kKvThreads, 1)
                     for (int e = 0; e < 2; ++e) {
                         const int c = 32 * half + 2 * c2 + e;
                         const BwdRowStat st = sm.stats[s][c];
-                        float pr = ptx::ex2(fmaf(__uint_as_float(sv[2 * c2 + e]), sl2, -st.lse2));
+                        float chain;
+                        const float t = mod_logit2<MOD>(mc, __uint_as_float(sv[2 * c2 + e]), q0 + c, key, chain);
+                        float pr = ptx::ex2(t - st.lse2);
                         if (edge && (key < st.lo || key >= st.hi))
                             pr = 0.f;
                         pp[e] = pr;
-                        dd[e] = pr * (__uint_as_float(pv[2 * c2 + e]) - st.d);
+                        dd[e] = pr * (__uint_as_float(pv[2 * c2 + e]) - st.d) * chain;
                     }
                     pa[16 * half + c2] = ptx::pack_bf16(pp[0], pp[1]);
                     da[16 * half + c2] = ptx::pack_bf16(dd[0], dd[1]);
@@ -668,6 +712,35 @@ constexpr size_t kKvSmemBytes = sizeof(DkvSmem) + 1024 > 120 * 1024 ? sizeof(Dkv
 
 } // namespace
 
+namespace {
+
+template <int MOD>
+cudaError_t launch_bwd_mod(const CUtensorMap &tq, const CUtensorMap &tdo, const CUtensorMap &tk,
+                           const CUtensorMap &tv, const CUtensorMap &tq128, const CUtensorMap &tdo128,
+                           const CUtensorMap &tk128, const CUtensorMap &tv128, const BwdParams &p,
+                           cudaStream_t stream)
+{
+    cudaError_t e;
+    static bool configured = false; // benign race: the calls are idempotent
+    if (!configured) {
+        if ((e = cudaFuncSetAttribute(bwd_dkdv_kernel<MOD>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                      static_cast<int>(kKvSmemBytes))) != cudaSuccess ||
+            (e = cudaFuncSetAttribute(bwd_dq_kernel<MOD>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                      static_cast<int>(kDqSmemBytes))) != cudaSuccess)
+            return e;
+        configured = true;
+    }
+    bwd_dkdv_kernel<MOD><<<dim3((p.S + kKvKeys - 1) / kKvKeys, p.Hk, p.B), kKvThreads, kKvSmemBytes, stream>>>(
+        tk128, tv128, tq, tdo, p);
+    if ((e = cudaGetLastError()) != cudaSuccess)
+        return e;
+    bwd_dq_kernel<MOD><<<dim3((p.S + kDqRows - 1) / kDqRows, p.Hq, p.B), kDqThreads, kDqSmemBytes, stream>>>(
+        tq128, tdo128, tk, tv, p);
+    return cudaGetLastError();
+}
+
+} // namespace
+
 cudaError_t launch_bwd(const CUtensorMap &tq, const CUtensorMap &tdo, const CUtensorMap &tk,
                        const CUtensorMap &tv, const CUtensorMap &tq128, const CUtensorMap &tdo128,
                        const CUtensorMap &tk128, const CUtensorMap &tv128, const BwdParams &p,
@@ -675,25 +748,17 @@ cudaError_t launch_bwd(const CUtensorMap &tq, const CUtensorMap &tdo, const CUte
 {
     const int64_t rows = static_cast<int64_t>(p.B) * p.Hq * p.S_pad;
     bwd_prep_kernel<<<static_cast<unsigned>((rows + 127) / 128), 128, 0, stream>>>(p);
-    cudaError_t e = cudaGetLastError();
+    const cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess)
         return e;
-    static bool configured = false; // benign race: the calls are idempotent
-    if (!configured) {
-        if ((e = cudaFuncSetAttribute(bwd_dkdv_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                      static_cast<int>(kKvSmemBytes))) != cudaSuccess ||
-            (e = cudaFuncSetAttribute(bwd_dq_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                      static_cast<int>(kDqSmemBytes))) != cudaSuccess)
-            return e;
-        configured = true;
+    switch (p.score_mod) {
+    case MOD_ALIBI:
+        return launch_bwd_mod<MOD_ALIBI>(tq, tdo, tk, tv, tq128, tdo128, tk128, tv128, p, stream);
+    case MOD_SOFTCAP:
+        return launch_bwd_mod<MOD_SOFTCAP>(tq, tdo, tk, tv, tq128, tdo128, tk128, tv128, p, stream);
+    default:
+        return launch_bwd_mod<MOD_NONE>(tq, tdo, tk, tv, tq128, tdo128, tk128, tv128, p, stream);
     }
-    bwd_dkdv_kernel<<<dim3((p.S + kKvKeys - 1) / kKvKeys, p.Hk, p.B), kKvThreads, kKvSmemBytes, stream>>>(
-        tk128, tv128, tq, tdo, p);
-    if ((e = cudaGetLastError()) != cudaSuccess)
-        return e;
-    bwd_dq_kernel<<<dim3((p.S + kDqRows - 1) / kDqRows, p.Hq, p.B), kDqThreads, kDqSmemBytes, stream>>>(
-        tq128, tdo128, tk, tv, p);
-    return cudaGetLastError();
 }
 
 } // namespace fl

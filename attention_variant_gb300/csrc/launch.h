@@ -95,6 +95,10 @@ struct BwdParams {
     int B, Hq, Hk, S, S_pad;      // S_pad: S rounded up to 128 (a multiple of kBwdBlock)
     MaskSpec mask;
     float scale;
+    int score_mod;                // MOD_NONE, MOD_ALIBI or MOD_SOFTCAP
+    float softcap;                // cap (softcap)
+    const float *alibi_slopes;    // [Hq] or null: 2^(alibi_exp_coef (h + 1))
+    float alibi_exp_coef;
     const __nv_bfloat16 *q, *k, *v, *o, *dout; // element strides (batch, position, head):
     int64_t q_sb, q_ss, q_sh, k_sb, k_ss, k_sh, v_sb, v_ss, v_sh;
     int64_t o_sb, o_ss, o_sh, do_sb, do_ss, do_sh;

@@ -226,7 +226,8 @@ fl_status fl_attn_evoformer(const fl_tensor *q, const fl_tensor *k, const fl_ten
  * (gist.science summary, "Limitations and future work").  P is recomputed
  * from Q, K and the LSE; dS = P (dP - D) with D_i = sum_d dout_id out_id.
  *   q, out, dout, dq [B, S, Hq, 64]; k, v, dk, dv [B, S, Hk, 64]; lse [B, Hq, S] fp32
- *   desc: kind FL_KIND_STANDARD, score_mod FL_MOD_NONE, any mask of the
+ *   desc: kind FL_KIND_STANDARD, score_mod FL_MOD_NONE, FL_MOD_ALIBI or
+ *   FL_MOD_SOFTCAP (with its softcap / alibi_slopes), any mask of the
  *   standard kind (with its window / prefix / doc_offsets), scale (0: 1/8).
  *   GQA heads are summed into dk, dv.
  * `workspace`: device memory of at least fl_attn_bwd_workspace_size bytes,

@@ -273,11 +273,14 @@ def _allowed(mask, S, b, window, prefix, doc_offsets):
     raise ValueError(mask)
 
 
-def attention_bwd(q, k, v, dout, *, mask="none", window=0, prefix=0, doc_offsets=None, scale=0.0):
+def attention_bwd(q, k, v, dout, *, mod="none", softcap=20.0, alibi_slopes=None, mask="none", window=0,
+                  prefix=0, doc_offsets=None, scale=0.0):
     """Gradients dQ, dK, dV (float64) of ``O = softmax(scale Q K^T + mask) V``
     for ``q [B,S,Hq,D]``, ``k, v [B,S,Hk,D]`` and the output gradient
     ``dout [B,S,Hq,D]`` (all bf16 bits), with any mask of ``attention``
-    (none, causal, window, prefix, doc).
+    (none, causal, window, prefix, doc) and score_mod none, ALiBi or softcap:
+    z = score_mod(u), u = scale q.k, and the chain rule takes dL/dz to dL/du
+    (1 for ALiBi, an additive bias; 1 - tanh^2(u / cap) for softcap).
 
     The plain definition per (batch, query head): the full probability matrix
     P (two-pass softmax), dV = P^T dO, dP = dO V^T, dS_ij = P_ij (dP_ij -
@@ -295,18 +298,29 @@ def attention_bwd(q, k, v, dout, *, mask="none", window=0, prefix=0, doc_offsets
     dQ = np.zeros_like(Q)
     dK = np.zeros_like(K)
     dV = np.zeros_like(V)
+    slopes = alibi_slopes if alibi_slopes is not None else globals()["alibi_slopes"](Hq)
+    dist = np.abs(np.arange(S)[:, None] - np.arange(S)[None, :]).astype(np.float64)
     for b in range(B):
         allowed = _allowed(mask, S, b, window, prefix, doc_offsets)
         for h in range(Hq):
             kh = h // G
-            z = s * (Q[b, :, h] @ K[b, :, kh].T)
+            u = s * (Q[b, :, h] @ K[b, :, kh].T)
+            chain = 1.0
+            if mod == "alibi":
+                z = u - slopes[h] * dist
+            elif mod == "softcap":
+                th = np.tanh(u / softcap)
+                z = softcap * th
+                chain = 1.0 - th * th
+            else:
+                z = u
             z = np.where(allowed, z, -np.inf)
             m = z.max(axis=1, keepdims=True)
             e = np.exp(z - m)
             P = e / e.sum(axis=1, keepdims=True)
             dV[b, :, kh] += P.T @ dO[b, :, h]
             dP = dO[b, :, h] @ V[b, :, kh].T
-            dS = P * (dP - (P * dP).sum(axis=1, keepdims=True))
+            dS = P * (dP - (P * dP).sum(axis=1, keepdims=True)) * chain
             dQ[b, :, h] = s * (dS @ K[b, :, kh])
             dK[b, :, kh] += s * (dS.T @ Q[b, :, h])
     return dQ, dK, dV

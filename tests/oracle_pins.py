@@ -500,6 +500,26 @@ def pin_backward(lib):
                 row = np.zeros(S, dtype=bool)
                 row[lo:hi] = True
                 assert np.array_equal(allowed[b, 0, i], row), f"{mask} row {i}"
+    # ALiBi and softcap against autograd of the same forward written in torch
+    B, S, Hq, Hk, D = 1, 50, 4, 2, 64
+    q, k, v = _rand((B, S, Hq, D), "aq"), _rand((B, S, Hk, D), "ak"), _rand((B, S, Hk, D), "av")
+    do = _rand((B, S, Hq, D), "ado")
+    for mod in ("alibi", "softcap"):
+        dq, dk, dv = oracle.attention_bwd(q, k, v, do, mod=mod, softcap=20.0, mask="causal")
+        Q, K, V = (torch.from_numpy(_f64(x)).permute(0, 2, 1, 3).requires_grad_(True) for x in (q, k, v))
+        Kr, Vr = K.repeat_interleave(Hq // Hk, dim=1), V.repeat_interleave(Hq // Hk, dim=1)
+        u = (Q @ Kr.transpose(-1, -2)) / math.sqrt(D)
+        if mod == "alibi":
+            sl = torch.tensor([2.0 ** (-8.0 * (h + 1) / Hq) for h in range(Hq)], dtype=torch.float64)
+            dist = (torch.arange(S)[:, None] - torch.arange(S)[None, :]).abs().double()
+            z = u - sl[None, :, None, None] * dist
+        else:
+            z = 20.0 * torch.tanh(u / 20.0)
+        z = z.masked_fill(~torch.ones(S, S, dtype=torch.bool).tril(), float("-inf"))
+        o = torch.softmax(z, dim=-1) @ Vr
+        o.backward(torch.from_numpy(_f64(do)).permute(0, 2, 1, 3))
+        for name, mine, ref in (("dQ", dq, Q.grad), ("dK", dk, K.grad), ("dV", dv, V.grad)):
+            _close(mine, ref.permute(0, 2, 1, 3).numpy(), atol=1e-10, what=f"backward {name} {mod}")
     # finite differences of L = sum(dO * O) with respect to one entry of each input
     B, S, Hq, Hk, D = 1, 6, 2, 1, 8
     q, k, v = _rand((B, S, Hq, D), "fq"), _rand((B, S, Hk, D), "fk"), _rand((B, S, Hk, D), "fv")

@@ -25,7 +25,7 @@ from tests import gpu_util as gu  # noqa: E402
 import attention_variant_gb300 as fa  # noqa: E402
 
 
-def _run(tag, B, S, Hq, Hk, mask, **mkw):
+def _run(tag, B, S, Hq, Hk, mask, mod="none", **mkw):
     q = testdata.normal_bf16((B, S, Hq, 64), f"bwd_{tag}", "q")
     k = testdata.normal_bf16((B, S, Hk, 64), f"bwd_{tag}", "k")
     v = testdata.normal_bf16((B, S, Hk, 64), f"bwd_{tag}", "v")
@@ -36,7 +36,7 @@ def _run(tag, B, S, Hq, Hk, mask, **mkw):
     err = torch.zeros(1, dtype=torch.int32, device="cuda")
     doc = mkw.pop("doc_offsets", None)
     doc_t = torch.from_numpy(doc).cuda() if doc is not None else None
-    d = fa.make_desc(mask=mask, error_word=err, doc_offsets=doc_t, **mkw)
+    d = fa.make_desc(mask=mask, score_mod=mod, softcap=20.0, error_word=err, doc_offsets=doc_t, **mkw)
     fa.fl_attn_fwd(qd, kd, vd, out, lse, d)
     dq = torch.full_like(qd, float("nan"))
     dk = torch.full_like(kd, float("nan"))
@@ -46,7 +46,7 @@ def _run(tag, B, S, Hq, Hk, mask, **mkw):
     fa.fl_attn_bwd(qd, kd, vd, out, lse, dod, dq, dk, dv, d, ws)
     torch.cuda.synchronize()
     assert int(err.item()) == 0
-    ref = oracle.attention_bwd(q, k, v, do, mask=mask, doc_offsets=doc, **mkw)
+    ref = oracle.attention_bwd(q, k, v, do, mod=mod, softcap=20.0, mask=mask, doc_offsets=doc, **mkw)
     return (gu.f64(dq), gu.f64(dk), gu.f64(dv)), ref
 
 
@@ -76,6 +76,13 @@ def test_backward_other_masks(B, S, Hq, Hk, mask, kw):
         kw = dict(doc_offsets=testdata.doc_offsets(S, B, f"bwd_doc_{S}", 20, 200))
     got, ref = _run(f"{B}_{S}_{Hq}_{Hk}_{mask}", B, S, Hq, Hk, mask, **kw)
     _check(got, ref, f"B{B} S{S} Hq{Hq} Hk{Hk} {mask}")
+
+
+@pytest.mark.parametrize("mod,mask,kw", [("alibi", "causal", {}), ("alibi", "none", {}),
+                                         ("softcap", "none", {}), ("softcap", "window", dict(window=90))])
+def test_backward_score_mods(mod, mask, kw):
+    got, ref = _run(f"mod_{mod}_{mask}", 2, 333, 4, 2, mask, mod=mod, **kw)
+    _check(got, ref, f"{mod} {mask}")
 
 
 def test_backward_is_deterministic():

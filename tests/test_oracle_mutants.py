@@ -98,6 +98,8 @@ BWD_MUTANTS = {
     "bwd_dv_overwritten": ("dV[b, :, kh] += P.T @ dO[b, :, h]", "dV[b, :, kh] = P.T @ dO[b, :, h]"),
     "bwd_gqa_modulo": ("kh = h // G", "kh = h % Hk"),
     "bwd_dq_transposed_ds": ("dQ[b, :, h] = s * (dS @ K[b, :, kh])", "dQ[b, :, h] = s * (dS.T @ K[b, :, kh])"),
+    "bwd_softcap_no_chain": ("chain = 1.0 - th * th", "chain = 1.0"),
+    "bwd_alibi_sign": ("z = u - slopes[h] * dist", "z = u + slopes[h] * dist"),
 }
 
 
