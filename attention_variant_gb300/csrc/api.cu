@@ -473,10 +473,13 @@ fl_status fwd_diff(const fl_tensor *q, const fl_tensor *k, const fl_tensor *v,
 
 // ------------------------------------------------------------------ Evoformer
 
+// bias_rows > 0: q, k, v, gate, out (and lse, msa_mask) are a batch of
+// stacks folded along the MSA-row axis (bias_rows rows per stack) and bias is
+// [stacks, H, N_res, N_res], one per stack.
 fl_status fwd_evo(bool row_pass, const fl_tensor *q, const fl_tensor *k, const fl_tensor *v,
                   const fl_tensor *out, const fl_tensor *lse, const fl_attn_variant_desc *d,
                   const fl_tensor *bias, const fl_tensor *gate, const fl_tensor *msa_mask,
-                  cudaStream_t stream)
+                  cudaStream_t stream, int64_t bias_rows = 0)
 {
     View Q, K, V, O, G, Bz{}, L{}, M{};
     fl_status s;
@@ -489,7 +492,21 @@ fl_status fwd_evo(bool row_pass, const fl_tensor *q, const fl_tensor *k, const f
     for (const View *t : {&K, &V, &O, &G})
         if (!same(*t, {Ns, Nr, H, C}))
             return fail(FL_ERR_INVALID_ARG, "q, k, v, gate and out must all be [N_seq, N_res, H, c]");
-    if (row_pass) {
+    if (row_pass && bias_rows > 0) {
+        // a per-stack bias as [stacks, H, N_res, N_res], viewed below as
+        // (j, i, h, stack) with the rank-3 view's strides in the first axes
+        View B4;
+        if ((s = check_tensor(bias, "bias", 4, FL_BF16, B4)) != FL_OK) return s;
+        if (Ns % bias_rows != 0 || !same(B4, {Ns / bias_rows, H, Nr, Nr}))
+            return fail(FL_ERR_INVALID_ARG, "bias must be [B, H, N_res, N_res]");
+        Bz.ptr = B4.ptr;
+        Bz.ndim = 3;
+        for (int a = 0; a < 3; ++a) {
+            Bz.size[a] = B4.size[a + 1];
+            Bz.stride[a] = B4.stride[a + 1];
+        }
+        Bz.stride[3] = B4.stride[0];
+    } else if (row_pass) {
         if ((s = check_tensor(bias, "bias", 3, FL_BF16, Bz)) != FL_OK) return s;
         if (!same(Bz, {H, Nr, Nr}))
             return fail(FL_ERR_INVALID_ARG, "bias must be [H, N_res, N_res]");
@@ -542,10 +559,12 @@ fl_status fwd_evo(bool row_pass, const fl_tensor *q, const fl_tensor *k, const f
         if (Nr > fl::evo_max_bias_keys())
             return fail(FL_ERR_UNSUPPORTED, "the row pass keeps the bias rows of a query block in "
                         "shared memory: N_res <= %d", fl::evo_max_bias_keys());
-        // bias[h, i, j] as (j, i, h, 1); boxes of 64 keys x 128 query rows
-        const uint64_t dims[4] = {uint64_t(Nr), uint64_t(Nr), uint64_t(H), 1};
+        // bias[stack, h, i, j] as (j, i, h, stack); boxes of 64 keys x 128 query rows
+        const uint64_t stacks = bias_rows > 0 ? uint64_t(Ns / bias_rows) : 1;
+        const uint64_t dims[4] = {uint64_t(Nr), uint64_t(Nr), uint64_t(H), stacks};
         const uint64_t st[3] = {uint64_t(Bz.stride[1]) * 2, uint64_t(Bz.stride[0]) * 2,
-                                uint64_t(Bz.stride[0]) * 2 * uint64_t(H)};
+                                bias_rows > 0 ? uint64_t(Bz.stride[3]) * 2
+                                              : uint64_t(Bz.stride[0]) * 2 * uint64_t(H)};
         const uint32_t bbox[4] = {64, 128, 1, 1};
         if ((s = make_map(tb, Bz.ptr, 4, dims, st, bbox, CU_TENSOR_MAP_SWIZZLE_128B, "bias")) != FL_OK)
             return s;
@@ -565,8 +584,10 @@ fl_status fwd_evo(bool row_pass, const fl_tensor *q, const fl_tensor *k, const f
     // (more items to spread over the SMs)
     {
         int64_t best_cost = -1;
-        int best_chunk = int(B);
+        int best_chunk = 1;
         for (int64_t chunk = 1; chunk <= B; ++chunk) {
+            if (bias_rows > 0 && bias_rows % chunk != 0)
+                continue; // an item's rows share one stack's bias
             const int64_t items = ((B + chunk - 1) / chunk) * H * nq;
             const int64_t waves = (items + info.sm_count - 1) / info.sm_count;
             const int64_t cost = waves * (2 * ((chunk + 1) / 2) + 1);
@@ -583,8 +604,10 @@ fl_status fwd_evo(bool row_pass, const fl_tensor *q, const fl_tensor *k, const f
     const float scale = d->scale != 0.f ? d->scale : 1.0f / std::sqrt(float(C));
     p.qk_scale = scale;
     p.qk_log2 = scale * 1.4426950408889634f;
-    if (row_pass)
+    if (row_pass) {
         p.bias = static_cast<const __nv_bfloat16 *>(Bz.ptr);
+        p.bias_rows = int(bias_rows);
+    }
     p.gate = static_cast<const __nv_bfloat16 *>(G.ptr);
     p.g_sb = G.stride[ab];
     p.g_si = G.stride[ai];
@@ -964,11 +987,10 @@ fl_status fl_attn_bwd(const fl_tensor *q, const fl_tensor *k, const fl_tensor *v
     return ok();
 }
 
-// Stacks of a batch run one launch each (every launch alone fills the GPU at
-// AlphaFold2 sizes: N_seq x H x ceil(N_res / 128) work items for the row pass).
-// The per-stack tensors are views of the caller's: only the base pointer moves
-// by the stack stride, so validating the stack-stride rules and the first
-// stack validates them all before anything is launched.
+// Otherwise (the column pass, or strides that do not merge) stacks run one
+// launch each: the per-stack tensors are views of the caller's, only the base
+// pointer moving by the stack stride, so validating the stack-stride rules and
+// the first stack validates them all before anything is launched.
 fl_status fl_attn_evoformer(const fl_tensor *q, const fl_tensor *k, const fl_tensor *v,
                             const fl_tensor *out, const fl_tensor *lse,
                             const fl_attn_variant_desc *desc, const fl_tensor *bias,
@@ -1002,6 +1024,41 @@ fl_status fl_attn_evoformer(const fl_tensor *q, const fl_tensor *k, const fl_ten
                         {v, "v", 5, false},       {out, "out", 5, false},
                         {gate, "gate", 5, false}, {lse, "lse", 4, false},
                         {bias, "bias", 4, true},  {msa_mask, "msa_mask", 3, true}};
+    // The row pass runs as ONE launch over all stacks when each batched
+    // tensor's stack stride is N_seq times its MSA-row stride (the stacks then
+    // form one longer MSA-row axis), the mask (if any) is per stack, and the
+    // bias is shared or per stack (work items then never straddle a stack).
+    if (row && Bt > 1) {
+        const int64_t Ns = q->sizes[1];
+        auto merges = [&](const fl_tensor *t, int rank) {
+            return t && t->ndim == rank && t->sizes[0] == Bt && t->strides[0] == Ns * t->strides[1] &&
+                   t->sizes[1] == Ns;
+        };
+        const bool fold = merges(q, 5) && merges(k, 5) && merges(v, 5) && merges(out, 5) &&
+                          merges(gate, 5) && (!lse || merges(lse, 4)) &&
+                          (!msa_mask || merges(msa_mask, 3)) && bias && (bias->ndim == 3 || bias->ndim == 4);
+        if (fold) {
+            auto merged = [&](const fl_tensor *t) {
+                fl_tensor m = *t;
+                m.ndim = t->ndim - 1;
+                m.sizes[0] = Bt * Ns;
+                m.strides[0] = t->strides[1];
+                for (int d = 1; d < m.ndim; ++d) {
+                    m.sizes[d] = t->sizes[d + 1];
+                    m.strides[d] = t->strides[d + 1];
+                }
+                return m;
+            };
+            const fl_tensor fq = merged(q), fk = merged(k), fv = merged(v), fo = merged(out), fg = merged(gate);
+            fl_tensor fl{}, fm{};
+            if (lse)
+                fl = merged(lse);
+            if (msa_mask)
+                fm = merged(msa_mask);
+            return fwd_evo(true, &fq, &fk, &fv, &fo, lse ? &fl : nullptr, desc, bias, &fg,
+                           msa_mask ? &fm : nullptr, st, bias->ndim == 4 ? Ns : 0);
+        }
+    }
     fl_tensor views[8];
     const fl_tensor *per_stack[8];
     bool batched[8];

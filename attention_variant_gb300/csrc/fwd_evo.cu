@@ -145,7 +145,7 @@ __device__ void producer_role(const Ctx<BIAS> &cx, const EvoParams &p, const CUt
                 ptx::mbar_arrive_expect_tx(bar(sm.bias_full), nbox * kBiasBox);
                 for (int jb = 0; jb < nbox; ++jb)
                     ptx::tma_load_4d(ptx::smem_u32(sm.bias[jb]), tm_b, bar(sm.bias_full), 64 * jb,
-                                     it.qb * BM, it.h, 0);
+                                     it.qb * BM, it.h, p.bias_rows ? it.b0 / p.bias_rows : 0);
             }
             __syncwarp();
         }

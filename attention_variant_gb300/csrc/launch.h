@@ -67,6 +67,9 @@ struct EvoParams {
     float qk_log2;          // scale * log2(e)
     float qk_scale;         // scale
     const __nv_bfloat16 *bias; // row pass only (its TMA map is passed separately)
+    int bias_rows;          // 0: one bias for every batch index; else a bias per stack of
+                            //   bias_rows consecutive batch indices (work items never
+                            //   straddle two stacks)
     const __nv_bfloat16 *gate;
     int64_t g_sb, g_si, g_sh;
     __nv_bfloat16 *out;
