@@ -245,11 +245,14 @@ def fl_attn_evoformer(q, k, v, out, lse, desc: FlDesc, bias=None, gate=None, msa
         raise FlAttnError(st, fl_attn_last_error())
 
 
-def fl_attn_score_expr_check(expr: str, compile: bool = False) -> None:
-    """Check a score_mod expression against the grammar (and, with ``compile``,
-    run its runtime compilation, which needs no GPU); raises FlAttnError."""
+def fl_attn_score_expr_check(expr: str, compile=False) -> None:
+    """Check a score_mod expression against the grammar; with ``compile`` true
+    also run the runtime compilation of its forward kernel, with
+    ``compile="backward"`` also that of its backward kernels (no GPU needed).
+    Raises FlAttnError."""
     lib = load_library()
-    st = lib.fl_attn_score_expr_check(expr.encode(), int(bool(compile)))
+    level = 2 if compile == "backward" else int(bool(compile))
+    st = lib.fl_attn_score_expr_check(expr.encode(), level)
     if st != FL_OK:
         raise FlAttnError(st, fl_attn_last_error())
 

@@ -13,6 +13,8 @@
 #include <cstdio>
 #include <cstring>
 #include <mutex>
+#include <string>
+#include <vector>
 
 #include "fl_attn.h"
 #include "launch.h"
@@ -810,6 +812,7 @@ struct BwdPlan {
     View Q, K, V;
     int64_t B, S, Hq, Hk, S_pad;
     size_t total;
+    std::string expr, expr_grad; // FL_MOD_EXPR: the translated expression and its derivative
 };
 
 fl_status bwd_plan(const fl_tensor *q, const fl_tensor *k, const fl_tensor *v,
@@ -838,8 +841,17 @@ fl_status bwd_plan(const fl_tensor *q, const fl_tensor *k, const fl_tensor *v,
                     (long long)pl.Hq, (long long)pl.Hk);
     if (d->kind != FL_KIND_STANDARD)
         return fail(FL_ERR_UNSUPPORTED, "the backward supports the standard kind");
-    if (d->score_mod != FL_MOD_NONE && d->score_mod != FL_MOD_ALIBI && d->score_mod != FL_MOD_SOFTCAP)
-        return fail(FL_ERR_UNSUPPORTED, "the backward supports score_mod none, ALiBi or softcap");
+    if (d->score_mod < FL_MOD_NONE || d->score_mod > FL_MOD_EXPR)
+        return fail(FL_ERR_INVALID_ARG, "unknown score_mod %d", d->score_mod);
+    if (d->score_mod == FL_MOD_EXPR) {
+        std::vector<char> v(kExprCudaMax), g(kExprCudaMax);
+        char err[256];
+        if (!fl::score_expr_translate_grad(d->score_mod_expr, v.data(), v.size(), g.data(), g.size(), err,
+                                           sizeof err))
+            return fail(FL_ERR_INVALID_ARG, "score_mod_expr: %s", err);
+        pl.expr = v.data();
+        pl.expr_grad = g.data();
+    }
     if (d->score_mod == FL_MOD_SOFTCAP && !(d->softcap > 0.f && std::isfinite(d->softcap)))
         return fail(FL_ERR_INVALID_ARG, "softcap must be positive and finite");
     if ((s = check_mask(d)) != FL_OK)
@@ -980,8 +992,23 @@ fl_status fl_attn_bwd(const fl_tensor *q, const fl_tensor *k, const fl_tensor *v
             FL_OK)
             return s;
     }
-    const cudaError_t e = fl::launch_bwd(tq, tdo, tk, tv, tq128, tdo128, tk128, tv128, p,
-                                         reinterpret_cast<cudaStream_t>(stream));
+    const cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    if (desc->score_mod == FL_MOD_EXPR) {
+        cudaError_t e = fl::launch_bwd_prep(p, st);
+        char err[1024] = "";
+        if (e == cudaSuccess)
+            e = fl::launch_bwd_expr(tq, tdo, tk, tv, tq128, tdo128, tk128, tv128, p, st, pl.expr.c_str(),
+                                    pl.expr_grad.c_str(), err, sizeof err);
+        if (e == cudaErrorInvalidSource)
+            return fail(FL_ERR_INVALID_ARG, "score_mod_expr: %s", err);
+        if (e == cudaErrorNotSupported)
+            return fail(FL_ERR_UNSUPPORTED, "score_mod_expr: %s", err);
+        if (e != cudaSuccess)
+            return fail(FL_ERR_CUDA, "score_mod_expr backward: %s%s%s", cudaGetErrorString(e), err[0] ? ": " : "",
+                        err);
+        return ok();
+    }
+    const cudaError_t e = fl::launch_bwd(tq, tdo, tk, tv, tq128, tdo128, tk128, tv128, p, st);
     if (e != cudaSuccess)
         return fail(FL_ERR_CUDA, "kernel launch failed: %s", cudaGetErrorString(e));
     return ok();
@@ -1106,10 +1133,11 @@ fl_status fl_attn_evoformer(const fl_tensor *q, const fl_tensor *k, const fl_ten
 
 fl_status fl_attn_score_expr_check(const char *expr, int32_t compile)
 {
-    char cuda[kExprCudaMax], err[1024];
-    if (!fl::score_expr_translate(expr, cuda, sizeof cuda, err, sizeof err))
+    std::vector<char> cuda(kExprCudaMax), grad(kExprCudaMax);
+    char err[1024];
+    if (!fl::score_expr_translate_grad(expr, cuda.data(), cuda.size(), grad.data(), grad.size(), err, sizeof err))
         return fail(FL_ERR_INVALID_ARG, "score_mod_expr: %s", err);
-    if (compile && !fl::score_expr_compile_only(cuda, err, sizeof err))
+    if (compile && !fl::score_expr_compile_only(cuda.data(), compile > 1 ? grad.data() : nullptr, err, sizeof err))
         return fail(strstr(err, "not found") ? FL_ERR_UNSUPPORTED : FL_ERR_INVALID_ARG,
                     "score_mod_expr: %s", err);
     return ok();

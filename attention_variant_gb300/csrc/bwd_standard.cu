@@ -31,7 +31,6 @@
 // and dP in the dQ kernel costs two more of the seven products than an atomic
 // dQ accumulation would, and buys determinism and no dQ workspace.
 #include <cuda_bf16.h>
-#include <cstdint>
 
 #include "common.cuh"
 #include "launch.h"
@@ -88,6 +87,8 @@ struct ModCtx {
     float alibi_c; // slope_h log2 e
     float cap_in;  // 2 scale log2 e / cap
     float cap_out; // cap log2 e
+    float scale;   // scale                      (expression)
+    float fb, fh;  // batch index and query head (expression)
 };
 
 template <int MOD>
@@ -100,15 +101,29 @@ __device__ __forceinline__ float mod_logit2(const ModCtx &m, float x, int i, int
     } else if constexpr (MOD == MOD_ALIBI) {
         chain = 1.f;
         return fmaf(x, m.sl2, -m.alibi_c * fabsf(static_cast<float>(i - j)));
+    } else if constexpr (MOD == MOD_EXPR) {
+#ifdef FL_SCORE_EXPR
+        // the run-time expression and its derivative with respect to the
+        // score (defined ahead of this file by the runtime compilation)
+        const float u = x * m.scale, fi = static_cast<float>(i), fj = static_cast<float>(j);
+        chain = fl_score_expr_du(u, m.fb, m.fh, fi, fj);
+        return kLog2e * fl_score_expr(u, m.fb, m.fh, fi, fj);
+#else
+        chain = 1.f;
+        return 0.f;
+#endif
     } else {
         chain = 1.f;
         return x * m.sl2;
     }
 }
 
-__device__ __forceinline__ ModCtx mod_ctx(const BwdParams &p, int h)
+__device__ __forceinline__ ModCtx mod_ctx(const BwdParams &p, int b, int h)
 {
     ModCtx m;
+    m.scale = p.scale;
+    m.fb = static_cast<float>(b);
+    m.fh = static_cast<float>(h);
     m.sl2 = p.scale * kLog2e;
     const float slope = p.alibi_slopes ? __ldg(p.alibi_slopes + h) : exp2f(p.alibi_exp_coef * static_cast<float>(h + 1));
     m.alibi_c = slope * kLog2e;
@@ -174,7 +189,7 @@ __global__ void __launch_bounds__(128) bwd_prep_kernel(const BwdParams p)
 //              at the end dQ (fp32, TMEM) * scale -> bf16.
 // TMEM columns: S[2] at 0 / 64, dP[2] at 128 / 192, dS[2] (bf16 pairs) at
 // 256 / 288, dQ at 320.
-constexpr int kDqRows = 128, kDqKeys = 64, kDqStages = 4, kDqThreads = 384;
+constexpr int kDqRows = kBwdDqRows, kDqKeys = 64, kDqStages = 4, kDqThreads = kBwdThreads;
 constexpr uint32_t kDqTile = kDqRows * 64 * 2;   // Q or dO tile, 16 KB
 constexpr uint32_t kColDqS = 0, kColDqP = 128, kColDqDs = 256, kColDq = 320;
 
@@ -339,7 +354,7 @@ __global__ void __launch_bounds__(kDqThreads, 1)
         const int row = q0 + r;
         const uint32_t lane_off = static_cast<uint32_t>(32 * (warp & 3)) << 16;
         const BwdRowStat st = p.ws_stats[(static_cast<int64_t>(b) * p.Hq + h) * p.S_pad + row];
-        const ModCtx mc = mod_ctx(p, h);
+        const ModCtx mc = mod_ctx(p, b, h);
         for (int j = wg; j < n_it; j += 2) {
             const int u = j & 1;
             if (!warp_wait(bar(sm.s_full[u]), (j >> 1) & 1, wc, W_S_FULL)) {
@@ -370,6 +385,8 @@ __global__ void __launch_bounds__(kDqThreads, 1)
                     const float t = mod_logit2<MOD>(mc, __uint_as_float(sv[col]), row, j0 + col, chain);
                     const float pr = ptx::ex2(t - st.lse2);
                     float dsv = pr * (__uint_as_float(pv[col]) - st.d) * chain;
+                    if constexpr (MOD == MOD_EXPR)
+                        dsv = pr > 0.f ? dsv : 0.f; // a removed pair's derivative may be inf or NaN
                     if (edge && (j0 + col < st.lo || j0 + col >= st.hi))
                         dsv = 0.f;
                     d2[e] = dsv;
@@ -441,7 +458,7 @@ __global__ void __launch_bounds__(kDqThreads, 1)
 //              end warpgroup 0 writes dV and warpgroup 1 scale * dK.
 // TMEM columns: S^T[2] at 0 / 64, dP^T[2] at 128 / 192, P^T[2] at 256 / 288,
 // dS^T[2] at 320 / 352, dV at 384, dK at 448.
-constexpr int kKvKeys = 128, kKvQ = 64, kKvStages = 4, kKvThreads = 384;
+constexpr int kKvKeys = kBwdKvKeys, kKvQ = 64, kKvStages = 4, kKvThreads = kBwdThreads;
 constexpr uint32_t kKvTile = kKvKeys * 64 * 2;   // K or V tile, 16 KB
 constexpr uint32_t kColTS = 0, kColTP = 128, kColTPb = 256, kColTDs = 320, kColDv = 384, kColDk = 448;
 
@@ -616,7 +633,7 @@ __global__ void __launch_bounds__(kKvThreads, 1)
         for (int i = wg; i < n_it; i += 2) {
             const int s = i % kKvStages, u = i & 1;
             const int q0 = (qj0 + i % n_qt) * kKvQ;
-            const ModCtx mc = mod_ctx(p, hk * G + i / n_qt);
+            const ModCtx mc = mod_ctx(p, b, hk * G + i / n_qt);
             // the stage's row statistics (written by the producer warp before
             // it armed st_full) and the tile's S^T, dP^T
             if (!warp_wait(bar(sm.st_full[s]), (i / kKvStages) & 1, wc, W_KV_FULL) ||
@@ -651,6 +668,8 @@ __global__ void __launch_bounds__(kKvThreads, 1)
                             pr = 0.f;
                         pp[e] = pr;
                         dd[e] = pr * (__uint_as_float(pv[2 * c2 + e]) - st.d) * chain;
+                        if constexpr (MOD == MOD_EXPR)
+                            dd[e] = pr > 0.f ? dd[e] : 0.f; // a removed pair's derivative may be inf or NaN
                     }
                     pa[16 * half + c2] = ptx::pack_bf16(pp[0], pp[1]);
                     da[16 * half + c2] = ptx::pack_bf16(dd[0], dd[1]);
@@ -712,6 +731,7 @@ constexpr size_t kKvSmemBytes = sizeof(DkvSmem) + 1024 > 120 * 1024 ? sizeof(Dkv
 
 } // namespace
 
+#ifndef __CUDACC_RTC__
 namespace {
 
 template <int MOD>
@@ -741,14 +761,22 @@ cudaError_t launch_bwd_mod(const CUtensorMap &tq, const CUtensorMap &tdo, const 
 
 } // namespace
 
+cudaError_t launch_bwd_prep(const BwdParams &p, cudaStream_t stream)
+{
+    const int64_t rows = static_cast<int64_t>(p.B) * p.Hq * p.S_pad;
+    bwd_prep_kernel<<<static_cast<unsigned>((rows + 127) / 128), 128, 0, stream>>>(p);
+    return cudaGetLastError();
+}
+
+size_t bwd_dkdv_smem_bytes() { return kKvSmemBytes; }
+size_t bwd_dq_smem_bytes() { return kDqSmemBytes; }
+
 cudaError_t launch_bwd(const CUtensorMap &tq, const CUtensorMap &tdo, const CUtensorMap &tk,
                        const CUtensorMap &tv, const CUtensorMap &tq128, const CUtensorMap &tdo128,
                        const CUtensorMap &tk128, const CUtensorMap &tv128, const BwdParams &p,
                        cudaStream_t stream)
 {
-    const int64_t rows = static_cast<int64_t>(p.B) * p.Hq * p.S_pad;
-    bwd_prep_kernel<<<static_cast<unsigned>((rows + 127) / 128), 128, 0, stream>>>(p);
-    const cudaError_t e = cudaGetLastError();
+    const cudaError_t e = launch_bwd_prep(p, stream);
     if (e != cudaSuccess)
         return e;
     switch (p.score_mod) {
@@ -760,5 +788,7 @@ cudaError_t launch_bwd(const CUtensorMap &tq, const CUtensorMap &tdo, const CUte
         return launch_bwd_mod<MOD_NONE>(tq, tdo, tk, tv, tq128, tdo128, tk128, tv128, p, stream);
     }
 }
+
+#endif // !__CUDACC_RTC__
 
 } // namespace fl

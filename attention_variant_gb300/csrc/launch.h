@@ -85,7 +85,10 @@ struct EvoParams {
 };
 
 // ---- backward of the standard kind (bwd_standard.cu)
-constexpr int kBwdBlock = 64; // query / key rows per tile
+constexpr int kBwdBlock = 64;   // query / key rows per streamed tile
+constexpr int kBwdDqRows = 128; // query rows per dQ CTA
+constexpr int kBwdKvKeys = 128; // keys per dK / dV CTA
+constexpr int kBwdThreads = 384;
 
 // Per query row of the backward's workspace: LSE log2 e, rowsum(dO O) and the
 // row's allowed key interval [lo, hi).
@@ -154,6 +157,16 @@ cudaError_t decode_static_scratch(void **ptr);
 cudaError_t launch_evo(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
                        const CUtensorMap &tb, const EvoParams &p, int grid, cudaStream_t stream);
 int evo_max_bias_keys();
+cudaError_t launch_bwd_prep(const BwdParams &p, cudaStream_t stream);
+size_t bwd_dkdv_smem_bytes();
+size_t bwd_dq_smem_bytes();
+// The main backward kernels specialised for a translated expression `cuda`
+// with derivative `grad` (run-time compiled, like launch_standard_expr);
+// launch_bwd_prep must have run first on the same stream.
+cudaError_t launch_bwd_expr(const CUtensorMap &tq, const CUtensorMap &tdo, const CUtensorMap &tk,
+                            const CUtensorMap &tv, const CUtensorMap &tq128, const CUtensorMap &tdo128,
+                            const CUtensorMap &tk128, const CUtensorMap &tv128, const BwdParams &p,
+                            cudaStream_t stream, const char *cuda, const char *grad, char *err, size_t err_n);
 cudaError_t launch_bwd(const CUtensorMap &tq, const CUtensorMap &tdo, const CUtensorMap &tk,
                        const CUtensorMap &tv, const CUtensorMap &tq128, const CUtensorMap &tdo128,
                        const CUtensorMap &tk128, const CUtensorMap &tv128, const BwdParams &p,
@@ -176,9 +189,14 @@ size_t standard_smem_bytes();
 // equivalent fp32 CUDA expression to `cuda` (NUL-terminated, at most `n`
 // bytes); false with a message in `err` otherwise.
 bool score_expr_translate(const char *expr, char *cuda, size_t n, char *err, size_t err_n);
+// The same, also writing the derivative of the expression with respect to
+// `score` (forward-mode differentiation through the grammar) to `grad`.
+bool score_expr_translate_grad(const char *expr, char *cuda, size_t n, char *grad, size_t grad_n, char *err,
+                               size_t err_n);
 // Runs the runtime compilation of the standard kernel for the translated
-// expression `cuda` without loading it (needs no device).
-bool score_expr_compile_only(const char *cuda, char *err, size_t err_n);
+// expression `cuda`, and of the backward kernels for it and its derivative
+// `grad` (unless null), without loading them (needs no device).
+bool score_expr_compile_only(const char *cuda, const char *grad, char *err, size_t err_n);
 // The standard kernel specialised for the translated expression `cuda`:
 // compiled at run time on first use (per device and expression), then
 // launched like launch_standard.  Errors other than CUDA ones are described

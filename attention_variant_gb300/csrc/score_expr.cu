@@ -71,17 +71,33 @@ constexpr const char *kVars[] = {"score", "b", "h", "q_idx", "kv_idx"};
 constexpr int kMaxDepth = 64;
 constexpr size_t kMaxLen = 4096;
 
+// A translated subexpression: its fp32 CUDA value and its derivative with
+// respect to `score` (forward-mode differentiation carried through the
+// parse), `zero` when the derivative is identically 0.
+struct Dual {
+    std::string v, d;
+    bool zero = true;
+};
+
+Dual constant(const std::string &v)
+{
+    Dual r;
+    r.v = v;
+    r.d = "0.0f";
+    return r;
+}
+
 class Translator {
   public:
     explicit Translator(const char *src) : s_(src) {}
 
-    bool run(std::string &out, std::string &err)
+    bool run(Dual &out, std::string &err)
     {
         if (strlen(s_) > kMaxLen) {
             err = "expression longer than 4096 characters";
             return false;
         }
-        std::string o;
+        Dual o;
         if (expr(o)) {
             skip();
             if (s_[i_] == '\0') {
@@ -127,23 +143,23 @@ class Translator {
         return nullptr;
     }
 
-    bool expr(std::string &o)
+    bool expr(Dual &o)
     {
         if (++depth_ > kMaxDepth)
             return fail("expression nested too deeply");
-        std::string a;
+        Dual a;
         if (!sum(a))
             return false;
         skip();
         if (const char *op = relop()) {
             i_ += strlen(op);
-            std::string b;
+            Dual b;
             if (!sum(b))
                 return false;
             skip();
             if (relop())
                 return fail("comparisons do not chain (parenthesise one side)");
-            o = "fl_x_bool(" + a + " " + op + " " + b + ")";
+            o = constant("fl_x_bool(" + a.v + " " + op + " " + b.v + ")"); // piecewise constant
         } else {
             o = a;
         }
@@ -151,7 +167,7 @@ class Translator {
         return true;
     }
 
-    bool sum(std::string &o)
+    bool sum(Dual &o)
     {
         if (!term(o))
             return false;
@@ -161,14 +177,18 @@ class Translator {
             if (c != '+' && c != '-')
                 return true;
             ++i_;
-            std::string b;
+            Dual b;
             if (!term(b))
                 return false;
-            o = "(" + o + " " + c + " " + b + ")";
+            Dual r;
+            r.v = "(" + o.v + " " + c + " " + b.v + ")";
+            r.zero = o.zero && b.zero;
+            r.d = r.zero ? "0.0f" : "(" + o.d + " " + c + " " + b.d + ")";
+            o = r;
         }
     }
 
-    bool term(std::string &o)
+    bool term(Dual &o)
     {
         if (!unary(o))
             return false;
@@ -180,14 +200,23 @@ class Translator {
             if (s_[i_ + 1] == '*' || s_[i_ + 1] == '/')
                 return fail("'**', '//' and comments are not part of the grammar");
             ++i_;
-            std::string b;
+            Dual b;
             if (!unary(b))
                 return false;
-            o = "(" + o + " " + c + " " + b + ")";
+            Dual r;
+            r.v = "(" + o.v + " " + c + " " + b.v + ")";
+            r.zero = o.zero && b.zero;
+            if (r.zero)
+                r.d = "0.0f";
+            else if (c == '*')
+                r.d = "(" + o.d + " * " + b.v + " + " + o.v + " * " + b.d + ")";
+            else
+                r.d = "((" + o.d + " * " + b.v + " - " + o.v + " * " + b.d + ") / (" + b.v + " * " + b.v + "))";
+            o = r;
         }
     }
 
-    bool unary(std::string &o)
+    bool unary(Dual &o)
     {
         skip();
         const char c = s_[i_];
@@ -195,17 +224,19 @@ class Translator {
             ++i_;
             if (++depth_ > kMaxDepth)
                 return fail("expression nested too deeply");
-            std::string a;
+            Dual a;
             if (!unary(a))
                 return false;
             --depth_;
-            o = std::string("(") + c + a + ")";
+            o.v = std::string("(") + c + a.v + ")";
+            o.zero = a.zero;
+            o.d = a.zero ? "0.0f" : std::string("(") + c + a.d + ")";
             return true;
         }
         return primary(o);
     }
 
-    bool number(std::string &o)
+    bool number(Dual &o)
     {
         const size_t start = i_;
         bool dot = false, exp = false;
@@ -231,16 +262,60 @@ class Translator {
         }
         if (is_alpha(s_[i_]) || s_[i_] == '.')
             return fail("malformed number");
-        o.assign(s_ + start, i_ - start);
+        std::string t(s_ + start, i_ - start);
         if (!dot && !exp)
-            o += ".0";
-        else if (o.back() == '.')
-            o += "0";
-        o = "(" + o + "f)";
+            t += ".0";
+        else if (t.back() == '.')
+            t += "0";
+        o = constant("(" + t + "f)");
         return true;
     }
 
-    bool primary(std::string &o)
+    // f(args) with its derivative: the chain rule through each function
+    static Dual apply(const std::string &name, const std::vector<Dual> &a)
+    {
+        Dual r;
+        std::string call = "fl_x_" + name + "(";
+        for (size_t k = 0; k < a.size(); ++k)
+            call += a[k].v + (k + 1 < a.size() ? ", " : ")");
+        r.v = call;
+        bool z = true;
+        for (const Dual &x : a)
+            z = z && x.zero;
+        if (name == "floor")
+            z = true;               // piecewise constant
+        if (name == "where")
+            z = a[1].zero && a[2].zero; // the condition is piecewise constant
+        r.zero = z;
+        if (z) {
+            r.d = "0.0f";
+            return r;
+        }
+        const std::string &u = a[0].v, &du = a[0].d;
+        if (name == "tanh")
+            r.d = "fl_dx_tanh(" + u + ", " + du + ")";
+        else if (name == "exp")
+            r.d = "(" + r.v + " * " + du + ")";
+        else if (name == "exp2")
+            r.d = "(" + r.v + " * 0.6931471805599453f * " + du + ")";
+        else if (name == "log")
+            r.d = "(" + du + " / " + u + ")";
+        else if (name == "log2")
+            r.d = "(" + du + " / (" + u + " * 0.6931471805599453f))";
+        else if (name == "sqrt")
+            r.d = "(" + du + " / (2.0f * " + r.v + "))";
+        else if (name == "abs")
+            r.d = "fl_x_where(fl_x_bool(" + u + " >= 0.0f), " + du + ", -" + du + ")";
+        else if (name == "min")
+            r.d = "fl_x_where(fl_x_bool(" + u + " <= " + a[1].v + "), " + du + ", " + a[1].d + ")";
+        else if (name == "max")
+            r.d = "fl_x_where(fl_x_bool(" + u + " >= " + a[1].v + "), " + du + ", " + a[1].d + ")";
+        else // where(c, x, y)
+            r.d = "fl_x_where(" + a[0].v + ", " + a[1].d + ", " + a[2].d + ")";
+        return r;
+    }
+
+    bool primary(Dual &o)
     {
         skip();
         const char c = s_[i_];
@@ -248,14 +323,16 @@ class Translator {
             return number(o);
         if (c == '(') {
             ++i_;
-            std::string a;
+            Dual a;
             if (!expr(a))
                 return false;
             skip();
             if (s_[i_] != ')')
                 return fail("expected ')'");
             ++i_;
-            o = "(" + a + ")";
+            o.v = "(" + a.v + ")";
+            o.d = a.zero ? "0.0f" : "(" + a.d + ")";
+            o.zero = a.zero;
             return true;
         }
         if (!is_alpha(c))
@@ -266,11 +343,15 @@ class Translator {
         const std::string name(s_ + start, i_ - start);
         for (const char *v : kVars)
             if (name == v) {
-                o = name;
+                o = constant(name);
+                if (name == "score") {
+                    o.d = "1.0f";
+                    o.zero = false;
+                }
                 return true;
             }
         if (name == "inf") {
-            o = "fl_x_inf()";
+            o = constant("fl_x_inf()");
             return true;
         }
         for (const Func &f : kFuncs) {
@@ -280,9 +361,9 @@ class Translator {
             if (s_[i_] != '(')
                 return fail("expected '(' after a function name");
             ++i_;
-            o = std::string("fl_x_") + f.name + "(";
+            std::vector<Dual> args;
             for (int a = 0; a < f.arity; ++a) {
-                std::string arg;
+                Dual arg;
                 if (!expr(arg))
                     return false;
                 skip();
@@ -290,8 +371,9 @@ class Translator {
                     return fail(a + 1 < f.arity ? "expected ',' (too few arguments)"
                                                 : "expected ')' (too many arguments)");
                 ++i_;
-                o += arg + (a + 1 < f.arity ? ", " : ")");
+                args.push_back(arg);
             }
+            o = apply(name, args);
             return true;
         }
         i_ = start;
@@ -359,48 +441,66 @@ const Nvrtc &nvrtc()
     return n;
 }
 
-// The helpers every translated expression calls, then the expression as the
-// score_mod the kernel source applies when FL_SCORE_EXPR is defined.
-std::string program_source(const std::string &cuda)
+// The helpers every translated expression calls.
+const char *kHelpers =
+    "#define FL_SCORE_EXPR 1\n"
+    "__device__ __forceinline__ float fl_x_bool(bool c) { return c ? 1.f : 0.f; }\n"
+    "__device__ __forceinline__ float fl_x_inf() { return __int_as_float(0x7f800000); }\n"
+    // exponentials on the hardware 2^x (relative error ~2^-22);
+    // tanh(x) = 1 - 2 / (1 + e^(2x)) on it and the hardware
+    // reciprocal (absolute error ~1e-7; +-1 at the extremes)
+    "__device__ __forceinline__ float fl_x_exp2(float x)\n"
+    "{ float y; asm(\"ex2.approx.ftz.f32 %0, %1;\" : \"=f\"(y) : \"f\"(x)); return y; }\n"
+    "__device__ __forceinline__ float fl_x_exp(float x) { return fl_x_exp2(x * 1.4426950408889634f); }\n"
+    "__device__ __forceinline__ float fl_x_tanh(float x)\n"
+    "{\n"
+    "    float r;\n"
+    "    asm(\"rcp.approx.ftz.f32 %0, %1;\" : \"=f\"(r) : \"f\"(1.f + fl_x_exp2(x * 2.8853900817779268f)));\n"
+    "    return 1.f - 2.f * r;\n"
+    "}\n"
+    "__device__ __forceinline__ float fl_x_log(float x) { return logf(x); }\n"
+    "__device__ __forceinline__ float fl_x_log2(float x) { return log2f(x); }\n"
+    "__device__ __forceinline__ float fl_x_sqrt(float x) { return sqrtf(x); }\n"
+    "__device__ __forceinline__ float fl_x_abs(float x) { return fabsf(x); }\n"
+    "__device__ __forceinline__ float fl_x_floor(float x) { return floorf(x); }\n"
+    "__device__ __forceinline__ float fl_x_min(float x, float y) { return fminf(x, y); }\n"
+    "__device__ __forceinline__ float fl_x_max(float x, float y) { return fmaxf(x, y); }\n"
+    "__device__ __forceinline__ float fl_x_where(float c, float x, float y) { return c != 0.f ? x : y; }\n"
+    "__device__ __forceinline__ float fl_dx_tanh(float x, float dx)\n"
+    "{ const float t = fl_x_tanh(x); return (1.f - t * t) * dx; }\n";
+
+std::string expr_function(const char *name, const std::string &body)
 {
-    return "#define FL_SCORE_EXPR 1\n"
-           "__device__ __forceinline__ float fl_x_bool(bool c) { return c ? 1.f : 0.f; }\n"
-           "__device__ __forceinline__ float fl_x_inf() { return __int_as_float(0x7f800000); }\n"
-           // exponentials on the hardware 2^x (relative error ~2^-22);
-           // tanh(x) = 1 - 2 / (1 + e^(2x)) on it and the hardware
-           // reciprocal (absolute error ~1e-7; +-1 at the extremes)
-           "__device__ __forceinline__ float fl_x_exp2(float x)\n"
-           "{ float y; asm(\"ex2.approx.ftz.f32 %0, %1;\" : \"=f\"(y) : \"f\"(x)); return y; }\n"
-           "__device__ __forceinline__ float fl_x_exp(float x) { return fl_x_exp2(x * 1.4426950408889634f); }\n"
-           "__device__ __forceinline__ float fl_x_tanh(float x)\n"
-           "{\n"
-           "    float r;\n"
-           "    asm(\"rcp.approx.ftz.f32 %0, %1;\" : \"=f\"(r) : \"f\"(1.f + fl_x_exp2(x * 2.8853900817779268f)));\n"
-           "    return 1.f - 2.f * r;\n"
-           "}\n"
-           "__device__ __forceinline__ float fl_x_log(float x) { return logf(x); }\n"
-           "__device__ __forceinline__ float fl_x_log2(float x) { return log2f(x); }\n"
-           "__device__ __forceinline__ float fl_x_sqrt(float x) { return sqrtf(x); }\n"
-           "__device__ __forceinline__ float fl_x_abs(float x) { return fabsf(x); }\n"
-           "__device__ __forceinline__ float fl_x_floor(float x) { return floorf(x); }\n"
-           "__device__ __forceinline__ float fl_x_min(float x, float y) { return fminf(x, y); }\n"
-           "__device__ __forceinline__ float fl_x_max(float x, float y) { return fmaxf(x, y); }\n"
-           "__device__ __forceinline__ float fl_x_where(float c, float x, float y) { return c != 0.f ? x : y; }\n"
-           "__device__ __forceinline__ float fl_score_expr(float score, float b, float h, float q_idx,\n"
-           "                                               float kv_idx)\n"
+    return std::string("__device__ __forceinline__ float ") + name +
+           "(float score, float b, float h, float q_idx, float kv_idx)\n"
            "{\n"
            "    (void)score; (void)b; (void)h; (void)q_idx; (void)kv_idx;\n"
-           "    return " + cuda + ";\n"
-           "}\n"
-           "#include \"fwd_standard.cu\"\n";
+           "    return " + body + ";\n"
+           "}\n";
 }
 
-constexpr const char *kKernelName = "fl::std_fwd_kernel<3>"; // MOD_EXPR
+// The forward: the standard kernel's source with the expression as its
+// score_mod.
+std::string forward_source(const std::string &cuda)
+{
+    return std::string(kHelpers) + expr_function("fl_score_expr", cuda) + "#include \"fwd_standard.cu\"\n";
+}
 
-// Compiles the standard kernel for the translated expression; the cubin and
-// the kernel's mangled name on success.
-bool compile(const std::string &cuda, std::vector<char> &cubin, std::string &name, char *err,
-             size_t err_n)
+// The backward: the backward kernels' source with the expression and its
+// derivative with respect to the score.
+std::string backward_source(const std::string &cuda, const std::string &grad)
+{
+    return std::string(kHelpers) + expr_function("fl_score_expr", cuda) +
+           expr_function("fl_score_expr_du", grad) + "#include \"bwd_standard.cu\"\n";
+}
+
+const std::vector<std::string> kForwardKernels = {"fl::std_fwd_kernel<3>"}; // MOD_EXPR
+const std::vector<std::string> kBackwardKernels = {"fl::bwd_dkdv_kernel<3>", "fl::bwd_dq_kernel<3>"};
+
+// Compiles `src` (which includes the embedded kernel sources) for sm_103a;
+// the cubin and the mangled names of `kernels` on success.
+bool compile(const std::string &src, const std::vector<std::string> &kernels, std::vector<char> &cubin,
+             std::vector<std::string> &names, char *err, size_t err_n)
 {
     const Nvrtc &n = nvrtc();
     if (!n.ok) {
@@ -412,14 +512,14 @@ bool compile(const std::string &cuda, std::vector<char> &cubin, std::string &nam
         hnames.push_back(s.name);
         htexts.push_back(s.text);
     }
-    const std::string src = program_source(cuda);
     nvrtcProgram_t prog = nullptr;
     if (n.create(&prog, src.c_str(), "score_expr_kernel.cu", int(hnames.size()), htexts.data(),
                  hnames.data()) != 0) {
         put(err, err_n, "nvrtcCreateProgram failed");
         return false;
     }
-    n.add_name(prog, kKernelName);
+    for (const std::string &k : kernels)
+        n.add_name(prog, k.c_str());
     const std::string inc = "--include-path=" + cuda_home() + "/include";
     // --prec-div=false: '/' is the fast division (within 2 ulp), not the
     // IEEE-rounded one, whose slow path would cost ~10 instructions a score
@@ -436,13 +536,17 @@ bool compile(const std::string &cuda, std::vector<char> &cubin, std::string &nam
         put(err, err_n, "runtime compilation failed: %.900s", log.c_str());
     } else {
         size_t cs = 0;
-        const char *lowered = nullptr;
-        good = n.cubin_size(prog, &cs) == 0 && cs > 0 && n.lowered(prog, kKernelName, &lowered) == 0 &&
-               lowered;
+        good = n.cubin_size(prog, &cs) == 0 && cs > 0;
+        names.clear();
+        for (const std::string &k : kernels) {
+            const char *lowered = nullptr;
+            good = good && n.lowered(prog, k.c_str(), &lowered) == 0 && lowered;
+            if (good)
+                names.push_back(lowered);
+        }
         if (good) {
             cubin.resize(cs);
             good = n.cubin(prog, cubin.data()) == 0;
-            name = lowered;
         }
         if (!good)
             put(err, err_n, "reading the compiled kernel failed");
@@ -494,28 +598,38 @@ std::map<std::pair<int, std::string>, CUfunction> g_kernels;
 
 bool score_expr_translate(const char *expr, char *cuda, size_t n, char *err, size_t err_n)
 {
+    return score_expr_translate_grad(expr, cuda, n, nullptr, 0, err, err_n);
+}
+
+bool score_expr_translate_grad(const char *expr, char *cuda, size_t n, char *grad, size_t grad_n, char *err,
+                               size_t err_n)
+{
     if (!expr) {
         put(err, err_n, "no expression");
         return false;
     }
-    std::string out, e;
+    Dual out;
+    std::string e;
     if (!Translator(expr).run(out, e)) {
         put(err, err_n, "%s", e.c_str());
         return false;
     }
-    if (out.size() + 1 > n) {
+    if (out.v.size() + 1 > n || (grad && out.d.size() + 1 > grad_n)) {
         put(err, err_n, "translated expression too long");
         return false;
     }
-    memcpy(cuda, out.c_str(), out.size() + 1);
+    memcpy(cuda, out.v.c_str(), out.v.size() + 1);
+    if (grad)
+        memcpy(grad, out.d.c_str(), out.d.size() + 1);
     return true;
 }
 
-bool score_expr_compile_only(const char *cuda, char *err, size_t err_n)
+bool score_expr_compile_only(const char *cuda, const char *grad, char *err, size_t err_n)
 {
     std::vector<char> cubin;
-    std::string name;
-    return compile(cuda, cubin, name, err, err_n);
+    std::vector<std::string> names;
+    return compile(forward_source(cuda), kForwardKernels, cubin, names, err, err_n) &&
+           (!grad || compile(backward_source(cuda, grad), kBackwardKernels, cubin, names, err, err_n));
 }
 
 cudaError_t launch_standard_expr(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
@@ -540,14 +654,14 @@ cudaError_t launch_standard_expr(const CUtensorMap &tq, const CUtensorMap &tk, c
             fn = it->second;
         } else {
             std::vector<char> cubin;
-            std::string name;
-            if (!compile(cuda, cubin, name, err, err_n))
+            std::vector<std::string> names;
+            if (!compile(forward_source(cuda), kForwardKernels, cubin, names, err, err_n))
                 return cudaErrorInvalidSource;
             // the runtime has made the device's primary context current
             if ((e = cudaFree(nullptr)) != cudaSuccess)
                 return e;
             CUmodule mod = nullptr;
-            if (d.load(&mod, cubin.data()) != CUDA_SUCCESS || d.get(&fn, mod, name.c_str()) != CUDA_SUCCESS) {
+            if (d.load(&mod, cubin.data()) != CUDA_SUCCESS || d.get(&fn, mod, names[0].c_str()) != CUDA_SUCCESS) {
                 put(err, err_n, "loading the compiled kernel failed");
                 return cudaErrorInvalidKernelImage;
             }
@@ -569,6 +683,67 @@ cudaError_t launch_standard_expr(const CUtensorMap &tq, const CUtensorMap &tk, c
     if (d.launch(fn, unsigned(grid), 1, 1, unsigned(kStdThreads), 1, 1, unsigned(smem),
                  reinterpret_cast<CUstream>(stream), args, nullptr) != CUDA_SUCCESS) {
         put(err, err_n, "launching the compiled kernel failed");
+        return cudaErrorLaunchFailure;
+    }
+    return cudaSuccess;
+}
+
+// One loaded pair of backward kernels per (device, expression).
+std::map<std::pair<int, std::string>, std::pair<CUfunction, CUfunction>> g_bwd_kernels;
+
+cudaError_t launch_bwd_expr(const CUtensorMap &tq, const CUtensorMap &tdo, const CUtensorMap &tk,
+                            const CUtensorMap &tv, const CUtensorMap &tq128, const CUtensorMap &tdo128,
+                            const CUtensorMap &tk128, const CUtensorMap &tv128, const BwdParams &p,
+                            cudaStream_t stream, const char *cuda, const char *grad, char *err, size_t err_n)
+{
+    const Driver &d = driver();
+    if (!d.ok) {
+        put(err, err_n, "driver entry points for module loading are unavailable");
+        return cudaErrorNotSupported;
+    }
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess)
+        return e;
+    const size_t smem_kv = bwd_dkdv_smem_bytes(), smem_q = bwd_dq_smem_bytes();
+    std::pair<CUfunction, CUfunction> fns{nullptr, nullptr};
+    {
+        std::lock_guard<std::mutex> lock(g_mutex);
+        const std::string key = std::string(cuda) + "\n" + grad;
+        auto it = g_bwd_kernels.find({dev, key});
+        if (it != g_bwd_kernels.end()) {
+            fns = it->second;
+        } else {
+            std::vector<char> cubin;
+            std::vector<std::string> names;
+            if (!compile(backward_source(cuda, grad), kBackwardKernels, cubin, names, err, err_n))
+                return cudaErrorInvalidSource;
+            if ((e = cudaFree(nullptr)) != cudaSuccess)
+                return e;
+            CUmodule mod = nullptr;
+            if (d.load(&mod, cubin.data()) != CUDA_SUCCESS || d.get(&fns.first, mod, names[0].c_str()) != CUDA_SUCCESS ||
+                d.get(&fns.second, mod, names[1].c_str()) != CUDA_SUCCESS) {
+                put(err, err_n, "loading the compiled backward kernels failed");
+                return cudaErrorInvalidKernelImage;
+            }
+            if (d.set(fns.first, CU_FUNC_ATTRIBUTE_MAX_DYNAMIC_SHARED_SIZE_BYTES, int(smem_kv)) != CUDA_SUCCESS ||
+                d.set(fns.second, CU_FUNC_ATTRIBUTE_MAX_DYNAMIC_SHARED_SIZE_BYTES, int(smem_q)) != CUDA_SUCCESS) {
+                put(err, err_n, "setting the backward kernels' shared-memory size failed");
+                return cudaErrorInvalidConfiguration;
+            }
+            g_bwd_kernels[{dev, key}] = fns;
+        }
+    }
+    void *kv_args[] = {const_cast<CUtensorMap *>(&tk128), const_cast<CUtensorMap *>(&tv128),
+                       const_cast<CUtensorMap *>(&tq), const_cast<CUtensorMap *>(&tdo), const_cast<BwdParams *>(&p)};
+    void *q_args[] = {const_cast<CUtensorMap *>(&tq128), const_cast<CUtensorMap *>(&tdo128),
+                      const_cast<CUtensorMap *>(&tk), const_cast<CUtensorMap *>(&tv), const_cast<BwdParams *>(&p)};
+    const CUstream cs = reinterpret_cast<CUstream>(stream);
+    if (d.launch(fns.first, unsigned((p.S + kBwdKvKeys - 1) / kBwdKvKeys), unsigned(p.Hk), unsigned(p.B),
+                 unsigned(kBwdThreads), 1, 1, unsigned(smem_kv), cs, kv_args, nullptr) != CUDA_SUCCESS ||
+        d.launch(fns.second, unsigned((p.S + kBwdDqRows - 1) / kBwdDqRows), unsigned(p.Hq), unsigned(p.B),
+                 unsigned(kBwdThreads), 1, 1, unsigned(smem_q), cs, q_args, nullptr) != CUDA_SUCCESS) {
+        put(err, err_n, "launching the compiled backward kernels failed");
         return cudaErrorLaunchFailure;
     }
     return cudaSuccess;

@@ -226,10 +226,11 @@ fl_status fl_attn_evoformer(const fl_tensor *q, const fl_tensor *k, const fl_ten
  * (gist.science summary, "Limitations and future work").  P is recomputed
  * from Q, K and the LSE; dS = P (dP - D) with D_i = sum_d dout_id out_id.
  *   q, out, dout, dq [B, S, Hq, 64]; k, v, dk, dv [B, S, Hk, 64]; lse [B, Hq, S] fp32
- *   desc: kind FL_KIND_STANDARD, score_mod FL_MOD_NONE, FL_MOD_ALIBI or
- *   FL_MOD_SOFTCAP (with its softcap / alibi_slopes), any mask of the
- *   standard kind (with its window / prefix / doc_offsets), scale (0: 1/8).
- *   GQA heads are summed into dk, dv.
+ *   desc: kind FL_KIND_STANDARD, any score_mod (FL_MOD_EXPR included: the
+ *   backward kernels are compiled at run time with the expression and its
+ *   derivative with respect to `score`, derived through the grammar), any
+ *   mask of the standard kind, scale (0: 1/8).  GQA heads are summed into
+ *   dk, dv.
  * `workspace`: device memory of at least fl_attn_bwd_workspace_size bytes,
  * 256-byte aligned, owned by the caller, no initialisation needed.  Three
  * kernel launches on `stream`; every output element is written once (no
@@ -250,8 +251,9 @@ fl_status fl_attn_tile_shape(const fl_attn_variant_desc *desc, int32_t head_dim,
 
 /* Checks a score_mod expression against the FL_MOD_EXPR grammar (FL_OK or
  * FL_ERR_INVALID_ARG, with the position in fl_attn_last_error()).  With
- * `compile` nonzero it also runs the runtime compilation of the kernel for it
- * (no device needed; FL_ERR_UNSUPPORTED without NVRTC). */
+ * `compile` 1 it also runs the runtime compilation of the forward kernel for
+ * it, with 2 also that of the backward kernels for it and its derivative (no
+ * device needed; FL_ERR_UNSUPPORTED without NVRTC). */
 fl_status fl_attn_score_expr_check(const char *expr, int32_t compile);
 
 /* Static text for a status code. */

@@ -273,14 +273,16 @@ def _allowed(mask, S, b, window, prefix, doc_offsets):
     raise ValueError(mask)
 
 
-def attention_bwd(q, k, v, dout, *, mod="none", softcap=20.0, alibi_slopes=None, mask="none", window=0,
-                  prefix=0, doc_offsets=None, scale=0.0):
+def attention_bwd(q, k, v, dout, *, mod="none", softcap=20.0, alibi_slopes=None, expr=None, mask="none",
+                  window=0, prefix=0, doc_offsets=None, scale=0.0):
     """Gradients dQ, dK, dV (float64) of ``O = softmax(scale Q K^T + mask) V``
     for ``q [B,S,Hq,D]``, ``k, v [B,S,Hk,D]`` and the output gradient
     ``dout [B,S,Hq,D]`` (all bf16 bits), with any mask of ``attention``
     (none, causal, window, prefix, doc) and score_mod none, ALiBi or softcap:
     z = score_mod(u), u = scale q.k, and the chain rule takes dL/dz to dL/du
-    (1 for ALiBi, an additive bias; 1 - tanh^2(u / cap) for softcap).
+    (1 for ALiBi, an additive bias; 1 - tanh^2(u / cap) for softcap; for
+    ``mod="expr"`` the derivative of the score_mod expression ``expr``, from
+    :func:`oracle.score_expr.evaluate_with_grad`).
 
     The plain definition per (batch, query head): the full probability matrix
     P (two-pass softmax), dV = P^T dO, dP = dO V^T, dS_ij = P_ij (dP_ij -
@@ -312,6 +314,12 @@ def attention_bwd(q, k, v, dout, *, mod="none", softcap=20.0, alibi_slopes=None,
                 th = np.tanh(u / softcap)
                 z = softcap * th
                 chain = 1.0 - th * th
+            elif mod == "expr":
+                from oracle import score_expr
+                z, chain = score_expr.evaluate_with_grad(
+                    expr, score=u, b=float(b), h=float(h), q_idx=np.arange(S, dtype=np.float64)[:, None],
+                    kv_idx=np.arange(S, dtype=np.float64)[None, :])
+                z, chain = np.broadcast_to(z, u.shape), np.broadcast_to(chain, u.shape)
             else:
                 z = u
             z = np.where(allowed, z, -np.inf)
@@ -320,7 +328,8 @@ def attention_bwd(q, k, v, dout, *, mod="none", softcap=20.0, alibi_slopes=None,
             P = e / e.sum(axis=1, keepdims=True)
             dV[b, :, kh] += P.T @ dO[b, :, h]
             dP = dO[b, :, h] @ V[b, :, kh].T
-            dS = P * (dP - (P * dP).sum(axis=1, keepdims=True)) * chain
+            with np.errstate(invalid="ignore"):
+                dS = np.where(P > 0, P * (dP - (P * dP).sum(axis=1, keepdims=True)) * chain, 0.0)
             dQ[b, :, h] = s * (dS @ K[b, :, kh])
             dK[b, :, kh] += s * (dS.T @ Q[b, :, h])
     return dQ, dK, dV

@@ -92,6 +92,77 @@ def evaluate(expr: str, **env) -> np.ndarray:
         return ev(tree)
 
 
+def evaluate_with_grad(expr: str, **env):
+    """Value of ``expr`` and its derivative with respect to ``score``
+    (forward-mode differentiation: every node carries (value, derivative)),
+    float64.  Comparisons, ``floor`` and the condition of ``where`` are
+    piecewise constant (derivative 0); ``abs`` takes the derivative +1 at 0."""
+    tree = parse(expr)
+    ln2 = np.log(2.0)
+
+    def ev(n):
+        if isinstance(n, ast.Expression):
+            return ev(n.body)
+        if isinstance(n, ast.Constant):
+            return np.float64(n.value), np.float64(0.0)
+        if isinstance(n, ast.Name):
+            if n.id == "inf":
+                return np.float64(np.inf), np.float64(0.0)
+            x = np.asarray(env[n.id], dtype=np.float64)
+            return x, (np.ones_like(x) if n.id == "score" else np.zeros_like(x))
+        if isinstance(n, ast.UnaryOp):
+            v, d = ev(n.operand)
+            return (-v, -d) if isinstance(n.op, ast.USub) else (v, d)
+        if isinstance(n, ast.BinOp):
+            (a, da), (b, db) = ev(n.left), ev(n.right)
+            if isinstance(n.op, ast.Add):
+                return a + b, da + db
+            if isinstance(n.op, ast.Sub):
+                return a - b, da - db
+            if isinstance(n.op, ast.Mult):
+                return a * b, da * b + a * db
+            return a / b, (da * b - a * db) / (b * b)
+        if isinstance(n, ast.Compare):
+            (a, _), (b, _) = ev(n.left), ev(n.comparators[0])
+            v = _CMP[type(n.ops[0])](a, b).astype(np.float64)
+            return v, np.zeros_like(v)
+        if isinstance(n, ast.Call):
+            args = [ev(x) for x in n.args]
+            f = n.func.id
+            (a, da) = args[0]
+            if f == "tanh":
+                t = np.tanh(a)
+                return t, (1.0 - t * t) * da
+            if f == "exp":
+                e = np.exp(a)
+                return e, e * da
+            if f == "exp2":
+                e = np.exp2(a)
+                return e, e * ln2 * da
+            if f == "log":
+                return np.log(a), da / a
+            if f == "log2":
+                return np.log2(a), da / (a * ln2)
+            if f == "sqrt":
+                r = np.sqrt(a)
+                return r, da / (2.0 * r)
+            if f == "abs":
+                return np.abs(a), np.where(a >= 0, da, -da)
+            if f == "floor":
+                return np.floor(a), np.zeros_like(np.asarray(a, dtype=np.float64))
+            if f in ("min", "max"):
+                (b, db) = args[1]
+                pick_a = (a <= b) if f == "min" else (a >= b)
+                return (np.minimum(a, b) if f == "min" else np.maximum(a, b)), np.where(pick_a, da, db)
+            (x, dx), (y, dy) = args[1], args[2]   # where(c, x, y)
+            c = np.asarray(a) != 0
+            return np.where(c, x, y), np.where(c, dx, dy)
+        raise ValueError(type(n).__name__)
+
+    with np.errstate(all="ignore"):
+        return ev(tree)
+
+
 def _widen(bits: np.ndarray) -> np.ndarray:
     """bf16 bit patterns -> float64 (exact)."""
     return (np.asarray(bits, dtype=np.uint16).astype(np.uint32) << 16).view(np.float32).astype(np.float64)

@@ -548,6 +548,38 @@ def pin_backward(lib):
         _close(grad[idx], (up - down) / (2 * eps), atol=1e-7, what=f"finite difference {name}")
 
 
+def pin_backward_expr(lib):
+    """The backward with a score_mod expression: expressions that restate the
+    built-in variants give the built-in backward, and the forward-mode
+    derivative matches central differences of the expression's value."""
+    from oracle import score_expr as se
+
+    B, S, Hq, Hk, D = 1, 40, 4, 2, 32
+    q, k, v = _rand((B, S, Hq, D), "eq"), _rand((B, S, Hk, D), "ek"), _rand((B, S, Hk, D), "ev")
+    do = _rand((B, S, Hq, D), "edo")
+    cases = [("score", "none", dict(mod="none")), ("20 * tanh(score / 20)", "none", dict(mod="softcap")),
+             ("score - exp2(-8 * (h + 1) / 4) * abs(q_idx - kv_idx)", "causal", dict(mod="alibi")),
+             ("where(kv_idx <= q_idx, score, -inf)", "none", dict(mod="none", mask="causal"))]
+    for expr, mask, kw in cases:
+        got = oracle.attention_bwd(q, k, v, do, mod="expr", expr=expr, mask=mask)
+        kw = dict(kw)
+        ref = oracle.attention_bwd(q, k, v, do, mask=kw.pop("mask", mask), **kw)
+        for name, a, b in zip(("dQ", "dK", "dV"), got, ref):
+            _close(a, b, atol=1e-10, what=f"expr backward {name} {expr!r}")
+    rng = np.random.default_rng(9)
+    x = rng.normal(size=200) * 3
+    for expr in ["max(score, -2) * exp2(-h) + sqrt(abs(score) + 1) + log(2 + score * score) / (1 + score * score)",
+                 "where(score > 0, tanh(score), exp(score) - 1) * (1 + 0.1 * floor(kv_idx / 3))",
+                 "min(score, 1.5) - abs(score - 0.3) + log2(1 + exp(score))",
+                 "exp2(score / 4) * sqrt(2 + score * score)"]:
+        env = dict(b=1.0, h=2.0, q_idx=7.0, kv_idx=np.arange(200.0))
+        _, d = se.evaluate_with_grad(expr, score=x, **env)
+        eps = 1e-6
+        fd = (se.evaluate(expr, score=x + eps, **env) - se.evaluate(expr, score=x - eps, **env)) / (2 * eps)
+        kink = np.abs(x[:, None] - np.array([-2.0, 0.0, 0.3, 1.5])[None, :]).min(axis=1) < 1e-4
+        _close(d[~kink], fd[~kink], atol=1e-5, what=f"derivative of {expr!r}")
+
+
 def pin_score_expr(lib):
     """The score_mod-expression oracle (numpy, float64) against the C oracle's
     built-in variants written as expressions, against a closed form, on rows
@@ -596,4 +628,4 @@ def pin_score_expr(lib):
 ALL_PINS = [pin_constant_scores, pin_alibi_geometric, pin_softcap_two_keys, pin_one_hot,
             pin_rows_sum_to_one, pin_shift_invariance, pin_permutation, pin_causal_row0,
             pin_sdpa, pin_reductions, pin_rows_api, pin_diff, pin_evo, pin_fully_masked_row,
-            pin_decode, pin_key_mask, pin_score_expr, pin_backward]
+            pin_decode, pin_key_mask, pin_score_expr, pin_backward, pin_backward_expr]

@@ -25,7 +25,7 @@ from tests import gpu_util as gu  # noqa: E402
 import attention_variant_gb300 as fa  # noqa: E402
 
 
-def _run(tag, B, S, Hq, Hk, mask, mod="none", **mkw):
+def _run(tag, B, S, Hq, Hk, mask, mod="none", expr=None, **mkw):
     q = testdata.normal_bf16((B, S, Hq, 64), f"bwd_{tag}", "q")
     k = testdata.normal_bf16((B, S, Hk, 64), f"bwd_{tag}", "k")
     v = testdata.normal_bf16((B, S, Hk, 64), f"bwd_{tag}", "v")
@@ -36,7 +36,8 @@ def _run(tag, B, S, Hq, Hk, mask, mod="none", **mkw):
     err = torch.zeros(1, dtype=torch.int32, device="cuda")
     doc = mkw.pop("doc_offsets", None)
     doc_t = torch.from_numpy(doc).cuda() if doc is not None else None
-    d = fa.make_desc(mask=mask, score_mod=mod, softcap=20.0, error_word=err, doc_offsets=doc_t, **mkw)
+    d = fa.make_desc(mask=mask, score_mod=mod, softcap=20.0, error_word=err, doc_offsets=doc_t, score_expr=expr,
+                     **mkw)
     fa.fl_attn_fwd(qd, kd, vd, out, lse, d)
     dq = torch.full_like(qd, float("nan"))
     dk = torch.full_like(kd, float("nan"))
@@ -46,7 +47,8 @@ def _run(tag, B, S, Hq, Hk, mask, mod="none", **mkw):
     fa.fl_attn_bwd(qd, kd, vd, out, lse, dod, dq, dk, dv, d, ws)
     torch.cuda.synchronize()
     assert int(err.item()) == 0
-    ref = oracle.attention_bwd(q, k, v, do, mod=mod, softcap=20.0, mask=mask, doc_offsets=doc, **mkw)
+    ref = oracle.attention_bwd(q, k, v, do, mod="expr" if expr else mod, expr=expr, softcap=20.0, mask=mask,
+                               doc_offsets=doc, **mkw)
     return (gu.f64(dq), gu.f64(dk), gu.f64(dv)), ref
 
 
@@ -83,6 +85,20 @@ def test_backward_other_masks(B, S, Hq, Hk, mask, kw):
 def test_backward_score_mods(mod, mask, kw):
     got, ref = _run(f"mod_{mod}_{mask}", 2, 333, 4, 2, mask, mod=mod, **kw)
     _check(got, ref, f"{mod} {mask}")
+
+
+@pytest.mark.parametrize("expr,mask", [
+    ("20 * tanh(score / 20)", "none"),
+    ("score - 0.25 * abs(q_idx - kv_idx)", "causal"),
+    ("where(kv_idx <= q_idx, score, -inf)", "none"),
+    ("max(score, -1) + 0.5 * tanh(score) * (1 + 0.1 * h) + where(b == 1, 0.2, -0.1) * sqrt(abs(score) + 1)", "none"),
+])
+def test_backward_score_expressions(expr, mask):
+    # the backward kernels compiled at run time with the expression and its
+    # derivative (forward-mode, from the translator), against the oracle's
+    # own forward-mode derivative
+    got, ref = _run(f"expr_{testdata.fnv1a64(expr) % 997}", 2, 300, 4, 2, mask, expr=expr)
+    _check(got, ref, f"expr {expr!r} {mask}")
 
 
 def test_backward_is_deterministic():

@@ -93,7 +93,7 @@ def test_expr_mutant_is_caught(name, monkeypatch):
 # Mistakes planted in the backward oracle (oracle.attention_bwd): its source
 # is edited in memory, compiled, and swapped in for the duration of the test.
 BWD_MUTANTS = {
-    "bwd_no_D_term": ("dS = P * (dP - (P * dP).sum(axis=1, keepdims=True))", "dS = P * dP"),
+    "bwd_no_D_term": ("P * (dP - (P * dP).sum(axis=1, keepdims=True)) * chain", "P * dP * chain"),
     "bwd_dk_no_scale": ("dK[b, :, kh] += s * (dS.T @ Q[b, :, h])", "dK[b, :, kh] += dS.T @ Q[b, :, h]"),
     "bwd_dv_overwritten": ("dV[b, :, kh] += P.T @ dO[b, :, h]", "dV[b, :, kh] = P.T @ dO[b, :, h]"),
     "bwd_gqa_modulo": ("kh = h // G", "kh = h % Hk"),
@@ -138,3 +138,30 @@ def test_allowed_mutant_is_caught(name, monkeypatch):
     monkeypatch.setattr(oracle, "_allowed", ns["_allowed"])
     with pytest.raises(AssertionError):
         oracle_pins.pin_backward(oracle.load())
+
+
+# Mistakes planted in the oracle's forward-mode derivatives of expressions.
+EXPR_GRAD_MUTANTS = {
+    "grad_tanh_sign": ("return t, (1.0 - t * t) * da", "return t, (1.0 + t * t) * da"),
+    "grad_div_sign": ("(da * b - a * db) / (b * b)", "(da * b + a * db) / (b * b)"),
+    "grad_exp2_no_ln2": ("return e, e * ln2 * da", "return e, e * da"),
+    "grad_min_picks_other": ("pick_a = (a <= b) if f == \"min\" else (a >= b)",
+                             "pick_a = (a >= b) if f == \"min\" else (a >= b)"),
+}
+
+
+@pytest.mark.parametrize("name", sorted(EXPR_GRAD_MUTANTS))
+def test_expr_grad_mutant_is_caught(name, monkeypatch):
+    import inspect
+    import textwrap
+
+    from oracle import score_expr as se
+
+    src = textwrap.dedent(inspect.getsource(se.evaluate_with_grad))
+    a, b = EXPR_GRAD_MUTANTS[name]
+    assert a in src, name
+    ns = dict(vars(se))
+    exec(compile(src.replace(a, b), "<mutant>", "exec"), ns)
+    monkeypatch.setattr(se, "evaluate_with_grad", ns["evaluate_with_grad"])
+    with pytest.raises(AssertionError):
+        oracle_pins.pin_backward_expr(oracle.load())
