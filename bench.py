@@ -167,11 +167,14 @@ def evo_batched_entry(row):
                 bytes=5 * tensor_bytes + (Bt * H * Nr * Nr * 2 if row else 0) + mask.size * 4)
 
 
-def bwd_entry(mask):
+def bwd_entry(mask, expr=None, mod="none"):
     """The backward (dQ, dK, dV) on the headline MHA workload; algorithmic
-    flops 10 D per unmasked pair (the five products of the gradient)."""
+    flops 10 D per unmasked pair (the five products of the gradient).  With
+    ``expr`` the score_mod is that run-time expression."""
     e = entry("mha", HEADLINE["S"], "causal" if mask == "causal" else "vanilla")
-    e.update(kind="bwd", variant="bwd_" + ("causal" if mask == "causal" else "vanilla"),
+    name = ("bwd_expr_softcap" if expr is not None else "bwd_softcap" if mod == "softcap"
+            else "bwd_" + ("causal" if mask == "causal" else "vanilla"))
+    e.update(kind="bwd", variant=name, expr=expr, mod=mod,
              flops=10 * e["D"] * e["pairs"],
              bytes=2 * e["B"] * e["S"] * e["D"] * (4 * e["Hq"] + 4 * e["Hk"]) + 4 * e["B"] * e["Hq"] * e["S"])
     return e
@@ -186,7 +189,7 @@ def time_bwd(e, torch, fa, device, steps, warmup, flush, stream):
         .view(torch.bfloat16).to(device)
     out = torch.empty_like(q)
     lse = torch.empty((B, Hq, S), dtype=torch.float32, device=device)
-    desc = fa.make_desc(mask=e["mask"])
+    desc = fa.make_desc(mask=e["mask"], score_mod=e["mod"], softcap=workloads.SOFTCAP, score_expr=e.get("expr"))
     fa.fl_attn_fwd(q, k, v, out, lse, desc)
     dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
     ws = torch.empty(fa.fl_attn_bwd_workspace_size(q, k, desc), dtype=torch.uint8, device=device)
@@ -596,7 +599,9 @@ ONLY = {"diff": lambda: diff_entry("none"), "diff_causal": lambda: diff_entry("c
         "expr_softcap": lambda: expr_entry(2048, "expr_softcap"),
         "expr_alibi": lambda: expr_entry(2048, "expr_alibi"),
         "evo_af2_row": lambda: evo_batched_entry(True), "evo_af2_col": lambda: evo_batched_entry(False),
-        "bwd": lambda: bwd_entry("none"), "bwd_causal": lambda: bwd_entry("causal")}
+        "bwd": lambda: bwd_entry("none"), "bwd_causal": lambda: bwd_entry("causal"),
+        "bwd_expr_softcap": lambda: bwd_entry("none", EXPR_VARIANTS["expr_softcap"][1]),
+        "bwd_softcap": lambda: bwd_entry("none", mod="softcap")}
 
 
 def run_only(args):
@@ -681,7 +686,8 @@ def run_ours(args):
             variants[f"{e['name']}/{e['variant']}"] = dict(
                 tflops=round(e["flops"] / (vm * 1e-3) / 1e12, 1), ms=round(vm, 4), gbs=round(gbs, 1),
                 frac_hbm=round(gbs / peaks["hbm_gbs"], 4), l2=l2_policy(e))
-        for e in (bwd_entry("none"), bwd_entry("causal")):
+        for e in (bwd_entry("none"), bwd_entry("causal"), bwd_entry("none", mod="softcap"),
+                  bwd_entry("none", EXPR_VARIANTS["expr_softcap"][1])):
             vm = statistics.mean(time_bwd(e, torch, fa, device, args.variant_steps, 2, flush, stream))
             tf = e["flops"] / (vm * 1e-3) / 1e12
             variants[f"{e['name']}/{e['variant']}"] = dict(
