@@ -5,6 +5,7 @@
 
 #include "rtc_compat.cuh"
 
+#include "fastdiv.h"
 #include "ptx.cuh"
 
 namespace fl {
@@ -120,13 +121,22 @@ __device__ __forceinline__ TileRange q_block_range(const MaskSpec &m, int b, int
 //           heads run fastest, then rows, so concurrently running CTAs share
 //           the K/V of at most `group` heads in L2 (talk notes,
 //           "Implementation details": L2 cache optimisation).
+// The divisions of the decoding use multipliers the host computes once per
+// launch (fastdiv.h); the host keeps n_items below 2^31.
 struct GridSpec {
     int B, Hq, Hk, G, nq;
     int R, Hx;
     int64_t n_items;
     int lpt;
-    int group;
+    int group;      // strip width, at most Hx
     int pair_heads;
+    FastDiv div_hx;    // Hx
+    FastDiv div_strip; // group * R, the items of one strip
+    FastDiv div_group; // group (every strip but a narrower last one)
+    FastDiv div_last;  // the last strip's width, Hx - (strips - 1) * group
+    FastDiv div_hq;    // Hq
+    FastDiv div_pairs; // (G + 1) / 2, the head pairs of a KV group
+    FastDiv div_hk;    // Hk
 };
 
 struct Item {
@@ -136,25 +146,31 @@ struct Item {
     bool valid[2];
 };
 
-__device__ __forceinline__ Item decode_item(const GridSpec &g, int64_t L)
+__device__ __forceinline__ Item decode_item(const GridSpec &g, int64_t L64)
 {
+    const int L = static_cast<int>(L64); // < n_items < 2^31
     int r, hx;
     if (g.lpt) {
-        r = g.R - 1 - static_cast<int>(L / g.Hx);
-        hx = static_cast<int>(L % g.Hx);
+        const int q = fast_div(L, g.div_hx);
+        r = g.R - 1 - q;
+        hx = L - q * g.Hx;
     } else {
-        const int64_t per_strip = static_cast<int64_t>(g.group) * g.R;
-        const int strip = static_cast<int>(L / per_strip);
+        const int strip = fast_div(L, g.div_strip);
         const int h0 = strip * g.group;
-        const int gs = min(g.group, g.Hx - h0);
-        const int w = static_cast<int>(L - strip * per_strip);
-        r = w / gs;
-        hx = h0 + w % gs;
+        const int w = L - strip * g.div_strip.d;
+        // the strip's width: group, or what is left for the last strip
+        const bool full = h0 + g.group <= g.Hx;
+        FastDiv gs;
+        gs.d = full ? g.div_group.d : g.div_last.d;
+        gs.m = full ? g.div_group.m : g.div_last.m;
+        gs.p = full ? g.div_group.p : g.div_last.p;
+        r = fast_div(w, gs);
+        hx = h0 + (w - r * gs.d);
     }
     Item it;
     if (!g.pair_heads) {
-        it.b = hx / g.Hq;
-        const int h = hx % g.Hq;
+        it.b = fast_div(hx, g.div_hq);
+        const int h = hx - it.b * g.Hq;
         it.kvh = h;
 #pragma unroll
         for (int t = 0; t < 2; ++t) {
@@ -163,11 +179,10 @@ __device__ __forceinline__ Item decode_item(const GridSpec &g, int64_t L)
             it.valid[t] = it.qb[t] < g.nq;
         }
     } else {
-        const int P = (g.G + 1) / 2;
-        const int hp = hx % P;
-        const int bk = hx / P;
-        it.b = bk / g.Hk;
-        it.kvh = bk % g.Hk;
+        const int bk = fast_div(hx, g.div_pairs);
+        const int hp = hx - bk * g.div_pairs.d;
+        it.b = fast_div(bk, g.div_hk);
+        it.kvh = bk - it.b * g.Hk;
 #pragma unroll
         for (int t = 0; t < 2; ++t) {
             const int gi = 2 * hp + t;
