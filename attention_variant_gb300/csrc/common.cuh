@@ -264,7 +264,8 @@ __device__ __forceinline__ bool mbar_wait_drain(uint32_t bar, uint32_t parity, c
 // Where-codes recorded in bits 8..15 of the error word.
 enum : uint32_t {
     W_Q_EMPTY = 1, W_KV_EMPTY = 2, W_Q_FULL = 3, W_KV_FULL = 4, W_P_FULL = 5,
-    W_S_FULL = 6, W_O_FULL = 7, W_FINAL = 8, W_DRAIN = 9, W_BIAS = 10, W_TURN = 11
+    W_S_FULL = 6, W_O_FULL = 7, W_FINAL = 8, W_DRAIN = 9, W_BIAS = 10, W_TURN = 11,
+    W_INFO_FULL = 12, W_INFO_EMPTY = 13
 };
 
 } // namespace fl

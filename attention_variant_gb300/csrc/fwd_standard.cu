@@ -11,7 +11,12 @@
 // CTA organisation (persistent: one CTA per SM, 384 threads):
 //   warp  0    TMA producer: Q tiles once per work item, K/V tiles through an
 //              NS-stage mbarrier ring
-//   warp  1    issues S = Q K^T for both slots (one thread); TMEM owner
+//   warp  1    issues S = Q K^T for both slots (one thread); TMEM owner; also
+//              decodes each work item once for both softmax warpgroups and
+//              publishes it through a two-entry ring in shared memory
+//              (info_full / info_empty), so that the softmax warps, whose
+//              item set-up sits between one item's epilogue and the next
+//              item's first turn, only read a few words
 //   warp  2    issues O += P V for slot 0
 //   warp  3    issues O += P V for slot 1
 //   warps 4-7  softmax warpgroup of slot 0 (one thread per query row)
@@ -68,6 +73,14 @@ static_assert(kBN == kStdKeyTile, "the host encodes K/V tensor maps with kStdKey
 constexpr uint32_t kColS = 0, kColO = 224, kColP = 384;
 constexpr uint32_t kStrideS = kBN, kStrideO = kDvExt, kStrideP = 64;
 
+// A work item as decoded by the S warp for both softmax warpgroups: its batch
+// index and, per slot, head, query block and key-tile range (TileRange).
+struct ItemInfo {
+    int32_t b, valid; // valid: bit t set when slot t holds a query block
+    int32_t h[2], qb[2];
+    int32_t lo[2], hi[2], full_lo[2], full_hi[2];
+};
+
 struct __align__(1024) StdSmem {
     uint8_t q[2][2][kTileBytes]; // [Q buffer][slot]
     uint8_t k[kStages][kKVBytes];
@@ -78,6 +91,8 @@ struct __align__(1024) StdSmem {
     uint64_t s_full[2], s_free[2], p_full[2], pv_done[2];
     uint64_t turn[2];            // exponential-phase token of each softmax warpgroup
     uint64_t final_bar[3];
+    uint64_t info_full[2], info_empty[2];
+    ItemInfo info[2];            // work items in flight, published by the S warp
     uint32_t tmem_base;
     uint32_t abort_flag;
 };
@@ -205,7 +220,7 @@ __device__ void s_role(const KernelCtx &cx, const StdParams &p)
     bool ok = true;
     for (int64_t L = blockIdx.x; L < p.grid.n_items && ok; L += gridDim.x) {
         const Item it = decode_item(p.grid, L);
-        int lo = 1 << 30, hi = 0, rlo[2] = {0, 0}, rhi[2] = {0, 0};
+        int lo = 1 << 30, hi = 0, rlo[2] = {0, 0}, rhi[2] = {0, 0}, rflo[2] = {0, 0}, rfhi[2] = {0, 0};
 #pragma unroll
         for (int u = 0; u < 2; ++u) {
             if (!it.valid[u])
@@ -213,10 +228,34 @@ __device__ void s_role(const KernelCtx &cx, const StdParams &p)
             const TileRange r = q_block_range<kBN>(p.mask, it.b, it.qb[u] * BM);
             rlo[u] = r.lo;
             rhi[u] = r.hi;
+            rflo[u] = r.full_lo;
+            rfhi[u] = r.full_hi;
             lo = min(lo, r.lo);
             hi = max(hi, r.hi);
         }
         const uint32_t qbuf = item_count & 1;
+        // publish the item to the softmax warpgroups (ring of two)
+        if (item_count >= 2) {
+            ok = warp_wait(bar(sm.info_empty[qbuf]), ((item_count - 2) >> 1) & 1, cx.wc, W_INFO_EMPTY);
+            if (!ok)
+                break;
+        }
+        if (lane == 0) {
+            ItemInfo &inf = sm.info[qbuf];
+            inf.b = it.b;
+            inf.valid = (it.valid[0] ? 1 : 0) | (it.valid[1] ? 2 : 0);
+#pragma unroll
+            for (int u = 0; u < 2; ++u) {
+                inf.h[u] = it.h[u];
+                inf.qb[u] = it.qb[u];
+                inf.lo[u] = rlo[u];
+                inf.hi[u] = rhi[u];
+                inf.full_lo[u] = rflo[u];
+                inf.full_hi[u] = rfhi[u];
+            }
+            ptx::mbar_arrive(bar(sm.info_full[qbuf])); // release: the fields above first
+        }
+        __syncwarp();
         const uint32_t b_qe = bar(sm.q_empty[qbuf]);
         ok = warp_wait(bar(sm.q_full[qbuf]), (item_count >> 1) & 1, cx.wc, W_Q_FULL);
         if (!ok)
@@ -430,18 +469,31 @@ __device__ void softmax_role(const KernelCtx &cx, const StdParams &p, int t)
         if (t == 1)
             nb_pass(t); // warpgroup 0 takes the first turn
 
-    for (int64_t L = blockIdx.x; L < p.grid.n_items; L += gridDim.x) {
-        const Item it = decode_item(p.grid, L);
-        const bool mine = it.valid[t];
-        const int b = it.b, h = it.h[t], qb = it.qb[t];
-        const int i = qb * BM + r;
-        const TileRange tr = q_block_range<kBN>(p.mask, b, qb * BM);
-        const int n_mine = mine ? tr.hi - tr.lo : 0;
-        int n_other = 0;
-        if (it.valid[t ^ 1]) {
-            const TileRange to = q_block_range<kBN>(p.mask, b, it.qb[t ^ 1] * BM);
-            n_other = to.hi - to.lo;
+    uint32_t items = 0;
+    for (int64_t L = blockIdx.x; L < p.grid.n_items; L += gridDim.x, ++items) {
+        // the item as the S warp decoded it
+        if (!warp_wait(bar(sm.info_full[items & 1]), (items >> 1) & 1, cx.wc, W_INFO_FULL)) {
+            if constexpr (!kNamed)
+                return;
+            fail_L = L;
+            fail_k = 0;
+            goto aborted;
         }
+        const ItemInfo &inf = sm.info[items & 1];
+        const int vbits = inf.valid;
+        const bool mine = (vbits >> t) & 1;
+        const int b = inf.b, h = inf.h[t], qb = inf.qb[t];
+        TileRange tr;
+        tr.lo = inf.lo[t];
+        tr.hi = inf.hi[t];
+        tr.full_lo = inf.full_lo[t];
+        tr.full_hi = inf.full_hi[t];
+        const int n_other = ((vbits >> (t ^ 1)) & 1) ? inf.hi[t ^ 1] - inf.lo[t ^ 1] : 0;
+        __syncwarp();
+        if (ptx::lane_id() == 0)
+            ptx::mbar_arrive(bar(sm.info_empty[items & 1]));
+        const int i = qb * BM + r;
+        const int n_mine = mine ? tr.hi - tr.lo : 0;
         const int n_turns = max(n_mine, n_other);
         int row_lo = 0, row_hi = 0;
         if (mine)
@@ -616,6 +668,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         for (int b = 0; b < 3; ++b)
             ptx::mbar_init(bar(sm->final_bar[b]), 1);
+        for (int b = 0; b < 2; ++b) {
+            ptx::mbar_init(bar(sm->info_full[b]), 1);
+            ptx::mbar_init(bar(sm->info_empty[b]), 8); // one arrival per softmax warp
+        }
         sm->abort_flag = 0;
         ptx::fence_mbarrier_init();
         ptx::fence_proxy_async_smem();
