@@ -56,7 +56,8 @@ def l2_policy(e):
 KERNEL_SOURCES = ["attention_variant_gb300/csrc/fwd_standard.cu",
                   "attention_variant_gb300/csrc/softmax_tile.cuh",
                   "attention_variant_gb300/csrc/common.cuh",
-                  "attention_variant_gb300/csrc/ptx.cuh"]
+                  "attention_variant_gb300/csrc/ptx.cuh",
+                  "attention_variant_gb300/csrc/fastdiv.h"]
 
 
 # ---------------------------------------------------------------- workload accounting
