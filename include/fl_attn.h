@@ -186,6 +186,8 @@ typedef struct {
  * [H,N_res,N_res]).  Evoformer sequence lengths must keep every stride a
  * multiple of 16 bytes (c = 32 bf16 rows always do; the bias row stride must
  * be a multiple of 8 elements: pad N_res or the bias rows otherwise).
+ * STANDARD launches of 2^31 or more work items (pairs of 128-row query
+ * blocks per batch and head) also return FL_ERR_UNSUPPORTED.
  *
  * Returns FL_OK when enqueued.  Device-side failures (a wait that ran out)
  * are reported asynchronously through desc->error_word.
