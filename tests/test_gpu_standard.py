@@ -97,6 +97,16 @@ def test_gqa(Hq, Hk, mask):
     _check(q, k, v, "none", mask, f"gqa{Hq}_{Hk}")
 
 
+@pytest.mark.parametrize("B,Hq,Hk,mask", [(3, 4, 4, "none"), (3, 4, 4, "window"), (3, 6, 2, "none"),
+                                          (5, 3, 3, "none"), (3, 4, 4, "causal")])
+def test_partial_last_head_strip(B, Hq, Hk, mask):
+    # 12 or 15 head positions: the work items of the last strip of 8 head
+    # positions span a narrower strip (non-causal orders), every (batch, head,
+    # query block) still visited once with its own tile count
+    q, k, v = _inputs(f"strip{B}_{Hq}_{Hk}", B, 300, Hq, Hk)
+    _check(q, k, v, "none", mask, f"strip{B}_{Hq}_{Hk}")
+
+
 @pytest.mark.parametrize("S", [1, 127, 128, 129, 257])
 def test_edge_lengths(S):
     q, k, v = _inputs(f"edge{S}", 1, S, 2)
