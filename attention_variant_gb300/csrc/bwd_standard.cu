@@ -11,18 +11,19 @@
 //     dQ  = scale dS K,      dK = scale dS^T Q
 // with GQA heads summed into their shared K/V head.
 //
-// Three kernels, no atomics (every output element has one writer):
+// Two launches, no atomics (every output element has one writer):
 //   bwd_prep_kernel  per query row: D_i, LSE_i * log2 e and the row's allowed
 //                    key interval [lo_i, hi_i) into the workspace (padded
 //                    rows get LSE +inf, so their P is 0, and the empty
 //                    interval [S, S));
-//   bwd_dkdv_kernel  one CTA per (128-key tile, KV head, batch): dK and dV
-//                    accumulate in TMEM over every 64-row query tile of every
-//                    query head of the group whose rows allow a key of the
-//                    tile;
-//   bwd_dq_kernel    one CTA per (128-row query tile, query head, batch): dQ
-//                    accumulates in TMEM over the 64-key tiles.
-// Both main kernels run on the tcgen05 tensor cores with the same layout of
+//   bwd_fused_kernel one CTA per tile, of two kinds in one grid:
+//     dK/dV tiles (bwd_dkdv_body), one per (128-key tile, KV head, batch):
+//                    dK and dV accumulate in TMEM over every 64-row query
+//                    tile of every query head of the group whose rows allow
+//                    a key of the tile;
+//     dQ tiles (bwd_dq_body), one per (128-row query tile, query head,
+//                    batch): dQ accumulates in TMEM over the 64-key tiles.
+// Both tile kinds run on the tcgen05 tensor cores with the same layout of
 // roles: a TMA producer warp, one MMA-issuing warp per product chain (an MMA
 // returns to its thread only when the tensor core accepts it, so separate
 // issuers let independent chains interleave), and two warpgroups of one
@@ -204,13 +205,13 @@ struct __align__(1024) DqSmem {
     uint32_t abort_flag;
 };
 
+// dQ of query tile qt of head h, batch b (one CTA; the maps are kernel
+// parameters, so their addresses stay in the parameter space).
 template <int MOD>
-__global__ void __launch_bounds__(kDqThreads, 1)
-    bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_do,
-                  const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
-                  const BwdParams p)
+__device__ __forceinline__ void bwd_dq_body(const CUtensorMap &tm_q, const CUtensorMap &tm_do,
+                                            const CUtensorMap &tm_k, const CUtensorMap &tm_v,
+                                            const BwdParams &p, const int qt, const int h, const int b)
 {
-    const int qt = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int q0 = qt * kDqRows;
     const int hk = h / (p.Hq / p.Hk);
@@ -474,13 +475,12 @@ struct __align__(1024) DkvSmem {
     uint32_t abort_flag;
 };
 
+// dK and dV of key tile kt of KV head hk, batch b (one CTA).
 template <int MOD>
-__global__ void __launch_bounds__(kKvThreads, 1)
-    bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
-                    const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_do,
-                    const BwdParams p)
+__device__ __forceinline__ void bwd_dkdv_body(const CUtensorMap &tm_k, const CUtensorMap &tm_v,
+                                              const CUtensorMap &tm_q, const CUtensorMap &tm_do,
+                                              const BwdParams &p, const int kt, const int hk, const int b)
 {
-    const int kt = blockIdx.x, hk = blockIdx.y, b = blockIdx.z;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int k0 = kt * kKvKeys;
     const int G = p.Hq / p.Hk;
@@ -726,6 +726,35 @@ __global__ void __launch_bounds__(kKvThreads, 1)
 
 // more than half an SM's shared memory: one dQ CTA per SM, so that no second
 // CTA waits in tcgen05.alloc for the 512 TMEM columns the first one holds
+// Both gradients in one launch: blocks [0, n_kv) take the dK/dV tiles (key
+// tile fastest, then KV head, then batch), the others the dQ tiles (query
+// tile fastest, then head, then batch).  With one CTA per SM, two launches
+// each end in a partly filled wave and the second cannot start on the SMs
+// the first leaves idle; one grid shares a single last wave.
+template <int MOD>
+__global__ void __launch_bounds__(kBwdThreads, 1)
+    bwd_fused_kernel(const __grid_constant__ CUtensorMap tm_k128, const __grid_constant__ CUtensorMap tm_v128,
+                     const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_do,
+                     const __grid_constant__ CUtensorMap tm_q128, const __grid_constant__ CUtensorMap tm_do128,
+                     const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
+                     const BwdParams p)
+{
+    const int nkt = (p.S + kKvKeys - 1) / kKvKeys;
+    const int n_kv = nkt * p.Hk * p.B;
+    int x = static_cast<int>(blockIdx.x);
+    if (x < n_kv) {
+        const int kt = x % nkt;
+        x /= nkt;
+        bwd_dkdv_body<MOD>(tm_k128, tm_v128, tm_q, tm_do, p, kt, x % p.Hk, x / p.Hk);
+    } else {
+        x -= n_kv;
+        const int nqt = (p.S + kDqRows - 1) / kDqRows;
+        const int qt = x % nqt;
+        x /= nqt;
+        bwd_dq_body<MOD>(tm_q128, tm_do128, tm_k, tm_v, p, qt, x % p.Hq, x / p.Hq);
+    }
+}
+
 constexpr size_t kDqSmemBytes = sizeof(DqSmem) + 1024 > 120 * 1024 ? sizeof(DqSmem) + 1024 : 120 * 1024;
 constexpr size_t kKvSmemBytes = sizeof(DkvSmem) + 1024 > 120 * 1024 ? sizeof(DkvSmem) + 1024 : 120 * 1024;
 
@@ -740,22 +769,18 @@ cudaError_t launch_bwd_mod(const CUtensorMap &tq, const CUtensorMap &tdo, const 
                            const CUtensorMap &tk128, const CUtensorMap &tv128, const BwdParams &p,
                            cudaStream_t stream)
 {
-    cudaError_t e;
-    static bool configured = false; // benign race: the calls are idempotent
+    const size_t smem = bwd_smem_bytes();
+    static bool configured = false; // benign race: the call is idempotent
     if (!configured) {
-        if ((e = cudaFuncSetAttribute(bwd_dkdv_kernel<MOD>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                      static_cast<int>(kKvSmemBytes))) != cudaSuccess ||
-            (e = cudaFuncSetAttribute(bwd_dq_kernel<MOD>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                      static_cast<int>(kDqSmemBytes))) != cudaSuccess)
+        const cudaError_t e = cudaFuncSetAttribute(bwd_fused_kernel<MOD>,
+                                                   cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                   static_cast<int>(smem));
+        if (e != cudaSuccess)
             return e;
         configured = true;
     }
-    bwd_dkdv_kernel<MOD><<<dim3((p.S + kKvKeys - 1) / kKvKeys, p.Hk, p.B), kKvThreads, kKvSmemBytes, stream>>>(
-        tk128, tv128, tq, tdo, p);
-    if ((e = cudaGetLastError()) != cudaSuccess)
-        return e;
-    bwd_dq_kernel<MOD><<<dim3((p.S + kDqRows - 1) / kDqRows, p.Hq, p.B), kDqThreads, kDqSmemBytes, stream>>>(
-        tq128, tdo128, tk, tv, p);
+    bwd_fused_kernel<MOD><<<static_cast<unsigned>(bwd_fused_blocks(p)), kBwdThreads, smem, stream>>>(
+        tk128, tv128, tq, tdo, tq128, tdo128, tk, tv, p);
     return cudaGetLastError();
 }
 
@@ -768,8 +793,13 @@ cudaError_t launch_bwd_prep(const BwdParams &p, cudaStream_t stream)
     return cudaGetLastError();
 }
 
-size_t bwd_dkdv_smem_bytes() { return kKvSmemBytes; }
-size_t bwd_dq_smem_bytes() { return kDqSmemBytes; }
+size_t bwd_smem_bytes() { return kKvSmemBytes > kDqSmemBytes ? kKvSmemBytes : kDqSmemBytes; }
+
+int64_t bwd_fused_blocks(const BwdParams &p)
+{
+    return int64_t((p.S + kKvKeys - 1) / kKvKeys) * p.Hk * p.B +
+           int64_t((p.S + kDqRows - 1) / kDqRows) * p.Hq * p.B;
+}
 
 cudaError_t launch_bwd(const CUtensorMap &tq, const CUtensorMap &tdo, const CUtensorMap &tk,
                        const CUtensorMap &tv, const CUtensorMap &tq128, const CUtensorMap &tdo128,

@@ -158,9 +158,10 @@ cudaError_t launch_evo(const CUtensorMap &tq, const CUtensorMap &tk, const CUten
                        const CUtensorMap &tb, const EvoParams &p, int grid, cudaStream_t stream);
 int evo_max_bias_keys();
 cudaError_t launch_bwd_prep(const BwdParams &p, cudaStream_t stream);
-size_t bwd_dkdv_smem_bytes();
-size_t bwd_dq_smem_bytes();
-// The main backward kernels specialised for a translated expression `cuda`
+// Dynamic shared memory and block count of the fused dK/dV + dQ launch.
+size_t bwd_smem_bytes();
+int64_t bwd_fused_blocks(const BwdParams &p);
+// The main backward kernel specialised for a translated expression `cuda`
 // with derivative `grad` (run-time compiled, like launch_standard_expr);
 // launch_bwd_prep must have run first on the same stream.
 cudaError_t launch_bwd_expr(const CUtensorMap &tq, const CUtensorMap &tdo, const CUtensorMap &tk,

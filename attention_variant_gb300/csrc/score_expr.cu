@@ -495,7 +495,7 @@ std::string backward_source(const std::string &cuda, const std::string &grad)
 }
 
 const std::vector<std::string> kForwardKernels = {"fl::std_fwd_kernel<3>"}; // MOD_EXPR
-const std::vector<std::string> kBackwardKernels = {"fl::bwd_dkdv_kernel<3>", "fl::bwd_dq_kernel<3>"};
+const std::vector<std::string> kBackwardKernels = {"fl::bwd_fused_kernel<3>"}; // dK/dV and dQ tiles
 
 // Compiles `src` (which includes the embedded kernel sources) for sm_103a;
 // the cubin and the mangled names of `kernels` on success.
@@ -688,8 +688,8 @@ cudaError_t launch_standard_expr(const CUtensorMap &tq, const CUtensorMap &tk, c
     return cudaSuccess;
 }
 
-// One loaded pair of backward kernels per (device, expression).
-std::map<std::pair<int, std::string>, std::pair<CUfunction, CUfunction>> g_bwd_kernels;
+// One loaded backward kernel per (device, expression).
+std::map<std::pair<int, std::string>, CUfunction> g_bwd_kernels;
 
 cudaError_t launch_bwd_expr(const CUtensorMap &tq, const CUtensorMap &tdo, const CUtensorMap &tk,
                             const CUtensorMap &tv, const CUtensorMap &tq128, const CUtensorMap &tdo128,
@@ -705,14 +705,14 @@ cudaError_t launch_bwd_expr(const CUtensorMap &tq, const CUtensorMap &tdo, const
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess)
         return e;
-    const size_t smem_kv = bwd_dkdv_smem_bytes(), smem_q = bwd_dq_smem_bytes();
-    std::pair<CUfunction, CUfunction> fns{nullptr, nullptr};
+    const size_t smem = bwd_smem_bytes();
+    CUfunction fn = nullptr;
     {
         std::lock_guard<std::mutex> lock(g_mutex);
         const std::string key = std::string(cuda) + "\n" + grad;
         auto it = g_bwd_kernels.find({dev, key});
         if (it != g_bwd_kernels.end()) {
-            fns = it->second;
+            fn = it->second;
         } else {
             std::vector<char> cubin;
             std::vector<std::string> names;
@@ -721,29 +721,26 @@ cudaError_t launch_bwd_expr(const CUtensorMap &tq, const CUtensorMap &tdo, const
             if ((e = cudaFree(nullptr)) != cudaSuccess)
                 return e;
             CUmodule mod = nullptr;
-            if (d.load(&mod, cubin.data()) != CUDA_SUCCESS || d.get(&fns.first, mod, names[0].c_str()) != CUDA_SUCCESS ||
-                d.get(&fns.second, mod, names[1].c_str()) != CUDA_SUCCESS) {
-                put(err, err_n, "loading the compiled backward kernels failed");
+            if (d.load(&mod, cubin.data()) != CUDA_SUCCESS || d.get(&fn, mod, names[0].c_str()) != CUDA_SUCCESS) {
+                put(err, err_n, "loading the compiled backward kernel failed");
                 return cudaErrorInvalidKernelImage;
             }
-            if (d.set(fns.first, CU_FUNC_ATTRIBUTE_MAX_DYNAMIC_SHARED_SIZE_BYTES, int(smem_kv)) != CUDA_SUCCESS ||
-                d.set(fns.second, CU_FUNC_ATTRIBUTE_MAX_DYNAMIC_SHARED_SIZE_BYTES, int(smem_q)) != CUDA_SUCCESS) {
-                put(err, err_n, "setting the backward kernels' shared-memory size failed");
+            if (d.set(fn, CU_FUNC_ATTRIBUTE_MAX_DYNAMIC_SHARED_SIZE_BYTES, int(smem)) != CUDA_SUCCESS) {
+                put(err, err_n, "setting the backward kernel's shared-memory size failed");
                 return cudaErrorInvalidConfiguration;
             }
-            g_bwd_kernels[{dev, key}] = fns;
+            g_bwd_kernels[{dev, key}] = fn;
         }
     }
-    void *kv_args[] = {const_cast<CUtensorMap *>(&tk128), const_cast<CUtensorMap *>(&tv128),
-                       const_cast<CUtensorMap *>(&tq), const_cast<CUtensorMap *>(&tdo), const_cast<BwdParams *>(&p)};
-    void *q_args[] = {const_cast<CUtensorMap *>(&tq128), const_cast<CUtensorMap *>(&tdo128),
-                      const_cast<CUtensorMap *>(&tk), const_cast<CUtensorMap *>(&tv), const_cast<BwdParams *>(&p)};
-    const CUstream cs = reinterpret_cast<CUstream>(stream);
-    if (d.launch(fns.first, unsigned((p.S + kBwdKvKeys - 1) / kBwdKvKeys), unsigned(p.Hk), unsigned(p.B),
-                 unsigned(kBwdThreads), 1, 1, unsigned(smem_kv), cs, kv_args, nullptr) != CUDA_SUCCESS ||
-        d.launch(fns.second, unsigned((p.S + kBwdDqRows - 1) / kBwdDqRows), unsigned(p.Hq), unsigned(p.B),
-                 unsigned(kBwdThreads), 1, 1, unsigned(smem_q), cs, q_args, nullptr) != CUDA_SUCCESS) {
-        put(err, err_n, "launching the compiled backward kernels failed");
+    // the parameter order of bwd_fused_kernel
+    void *args[] = {const_cast<CUtensorMap *>(&tk128), const_cast<CUtensorMap *>(&tv128),
+                    const_cast<CUtensorMap *>(&tq), const_cast<CUtensorMap *>(&tdo),
+                    const_cast<CUtensorMap *>(&tq128), const_cast<CUtensorMap *>(&tdo128),
+                    const_cast<CUtensorMap *>(&tk), const_cast<CUtensorMap *>(&tv), const_cast<BwdParams *>(&p)};
+    const int64_t blocks = bwd_fused_blocks(p);
+    if (d.launch(fn, unsigned(blocks), 1, 1, unsigned(kBwdThreads), 1, 1, unsigned(smem),
+                 reinterpret_cast<CUstream>(stream), args, nullptr) != CUDA_SUCCESS) {
+        put(err, err_n, "launching the compiled backward kernel failed");
         return cudaErrorLaunchFailure;
     }
     return cudaSuccess;
