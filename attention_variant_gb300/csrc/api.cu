@@ -303,31 +303,10 @@ fl_status fwd_standard(const fl_tensor *q, const fl_tensor *k, const fl_tensor *
 
     fl::StdParams p{};
     const int nq = static_cast<int>((S + fl::BM - 1) / fl::BM);
-    p.grid.B = int(B);
-    p.grid.Hq = int(Hq);
-    p.grid.Hk = int(Hk);
-    p.grid.G = int(G);
-    p.grid.nq = nq;
-    p.grid.pair_heads = G >= 2 ? 1 : 0;
-    const int64_t R = G >= 2 ? nq : (nq + 1) / 2;
-    const int64_t Hx = G >= 2 ? int64_t(B) * Hk * ((G + 1) / 2) : int64_t(B) * Hq;
-    if (R * Hx >= (int64_t(1) << 31))
+    if (!fl::make_grid_spec(int(B), int(Hq), int(Hk), nq,
+                            d->mask == FL_MASK_CAUSAL || d->mask == FL_MASK_PREFIX || d->mask == FL_MASK_DOC,
+                            p.grid))
         return fail(FL_ERR_UNSUPPORTED, "more than 2^31 - 1 work items (B * heads * query tiles)");
-    p.grid.R = int(R);
-    p.grid.Hx = int(Hx);
-    p.grid.n_items = R * Hx;
-    p.grid.lpt = (d->mask == FL_MASK_CAUSAL || d->mask == FL_MASK_PREFIX || d->mask == FL_MASK_DOC);
-    p.grid.group = p.grid.Hx < 8 ? p.grid.Hx : 8;
-    {
-        const int strips = (p.grid.Hx + p.grid.group - 1) / p.grid.group;
-        p.grid.div_hx = fl::make_fastdiv(p.grid.Hx);
-        p.grid.div_strip = fl::make_fastdiv(p.grid.group * p.grid.R);
-        p.grid.div_group = fl::make_fastdiv(p.grid.group);
-        p.grid.div_last = fl::make_fastdiv(p.grid.Hx - (strips - 1) * p.grid.group);
-        p.grid.div_hq = fl::make_fastdiv(p.grid.Hq);
-        p.grid.div_pairs = fl::make_fastdiv((p.grid.G + 1) / 2);
-        p.grid.div_hk = fl::make_fastdiv(p.grid.Hk);
-    }
     p.mask.kind = d->mask;
     p.mask.S = int(S);
     p.mask.window = d->window;

@@ -146,7 +146,41 @@ struct Item {
     bool valid[2];
 };
 
-__device__ __forceinline__ Item decode_item(const GridSpec &g, int64_t L64)
+#ifndef __CUDACC_RTC__
+// The work-item grid for B batches, Hq query heads sharing Hk KV heads (G =
+// Hq / Hk per KV head) and nq query blocks, in the LPT order or in strips;
+// false (nothing set) when the items would number 2^31 or more.
+inline bool make_grid_spec(int B, int Hq, int Hk, int nq, bool lpt, GridSpec &g)
+{
+    const int G = Hq / Hk;
+    const int64_t R = G >= 2 ? nq : (nq + 1) / 2;
+    const int64_t Hx = G >= 2 ? int64_t(B) * Hk * ((G + 1) / 2) : int64_t(B) * Hq;
+    if (R * Hx >= (int64_t(1) << 31))
+        return false;
+    g.B = B;
+    g.Hq = Hq;
+    g.Hk = Hk;
+    g.G = G;
+    g.nq = nq;
+    g.pair_heads = G >= 2 ? 1 : 0;
+    g.R = int(R);
+    g.Hx = int(Hx);
+    g.n_items = R * Hx;
+    g.lpt = lpt ? 1 : 0;
+    g.group = g.Hx < 8 ? g.Hx : 8;
+    const int strips = (g.Hx + g.group - 1) / g.group;
+    g.div_hx = make_fastdiv(g.Hx);
+    g.div_strip = make_fastdiv(g.group * g.R);
+    g.div_group = make_fastdiv(g.group);
+    g.div_last = make_fastdiv(g.Hx - (strips - 1) * g.group);
+    g.div_hq = make_fastdiv(g.Hq);
+    g.div_pairs = make_fastdiv((G + 1) / 2);
+    g.div_hk = make_fastdiv(g.Hk);
+    return true;
+}
+#endif // !__CUDACC_RTC__
+
+__host__ __device__ __forceinline__ Item decode_item(const GridSpec &g, int64_t L64)
 {
     const int L = static_cast<int>(L64); // < n_items < 2^31
     int r, hx;
