@@ -271,6 +271,12 @@ fl_status fwd_standard(const fl_tensor *q, const fl_tensor *k, const fl_tensor *
     if (D != 64 || Dv != 64)
         return fail(FL_ERR_UNSUPPORTED, "standard kind supports D = Dv = 64 (got %lld, %lld)",
                     (long long)D, (long long)Dv);
+    const int nq = static_cast<int>((S + fl::BM - 1) / fl::BM);
+    fl::GridSpec work{};
+    if (!fl::make_grid_spec(int(B), int(Hq), int(Hk), nq,
+                            d->mask == FL_MASK_CAUSAL || d->mask == FL_MASK_PREFIX || d->mask == FL_MASK_DOC,
+                            work))
+        return fail(FL_ERR_UNSUPPORTED, "more than 2^31 - 1 work items (B * heads * query tiles)");
 
     int dev;
     DeviceInfo info;
@@ -302,11 +308,7 @@ fl_status fwd_standard(const fl_tensor *q, const fl_tensor *k, const fl_tensor *
     }
 
     fl::StdParams p{};
-    const int nq = static_cast<int>((S + fl::BM - 1) / fl::BM);
-    if (!fl::make_grid_spec(int(B), int(Hq), int(Hk), nq,
-                            d->mask == FL_MASK_CAUSAL || d->mask == FL_MASK_PREFIX || d->mask == FL_MASK_DOC,
-                            p.grid))
-        return fail(FL_ERR_UNSUPPORTED, "more than 2^31 - 1 work items (B * heads * query tiles)");
+    p.grid = work;
     p.mask.kind = d->mask;
     p.mask.S = int(S);
     p.mask.window = d->window;

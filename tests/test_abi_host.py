@@ -76,6 +76,11 @@ def test_validation_before_device(lib):
     assert _call(lib, notinner, good(), good(), good()) == fa.FL_ERR_INVALID_ARG
     assert _call(lib, _t((B, S, H, 128)), _t((B, S, H, 128)), _t((B, S, H, 128)),
                  _t((B, S, H, 128))) == fa.FL_ERR_UNSUPPORTED
+    # 2^31 work items or more (the kernel decodes item indices in 32 bits):
+    # 2^20 batches x 16 heads x 256 pairs of query blocks
+    huge = lambda: _t((1 << 20, 1 << 16, 16, D))
+    assert _call(lib, huge(), huge(), huge(), huge()) == fa.FL_ERR_UNSUPPORTED
+    assert "work items" in fa.fl_attn_last_error()
     assert _call(lib, _t((B, S, 3, D)), _t((B, S, 2, D)), _t((B, S, 2, D)),
                  _t((B, S, 3, D))) == fa.FL_ERR_INVALID_ARG  # Hq % Hk
     assert _call(lib, good(), good(), good(), good(),
