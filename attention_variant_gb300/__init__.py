@@ -13,7 +13,6 @@ The names mirror the C ABI: :func:`fl_attn_fwd`, :func:`fl_attn_tile_shape`,
 from __future__ import annotations
 
 import ctypes
-import math
 import os
 
 HERE = os.path.dirname(os.path.abspath(__file__))
@@ -356,8 +355,8 @@ def fl_attn_decode_static(q, k_cache, v_cache, out, lse, desc: FlDecodeDesc, str
     """fl_attn_decode with the library's own static scratch instead of a
     workspace: for callers that cannot allocate device memory.  Allocates
     nothing; calls that overlap on the GPU race (they share the scratch); the
-    first call on a device sets up the scratch address, so make it before any
-    stream capture."""
+    first call in a CUDA context (per device, and again after a device reset)
+    sets up the scratch address, so make it before any stream capture."""
     lib = load_library()
     if stream is None:
         import torch
@@ -371,6 +370,3 @@ def fl_attn_decode_static(q, k_cache, v_cache, out, lse, desc: FlDecodeDesc, str
     if st != FL_OK:
         raise FlAttnError(st, fl_attn_last_error())
 
-
-def default_scale(head_dim: int) -> float:
-    return 1.0 / math.sqrt(head_dim)

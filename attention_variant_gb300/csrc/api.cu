@@ -1134,7 +1134,7 @@ fl_status fl_attn_score_expr_check(const char *expr, int32_t compile)
 }
 
 // No workspace argument: the scratch is the library's own static device
-// array (fl::decode_static_scratch), looked up on the first call per device.
+// array (fl::decode_static_scratch), looked up on the first call per context.
 // Nothing is allocated.
 fl_status fl_attn_decode_static(const fl_tensor *q, const fl_tensor *k_cache,
                                 const fl_tensor *v_cache, const fl_tensor *out,

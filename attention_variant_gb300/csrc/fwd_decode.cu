@@ -41,6 +41,8 @@
 #include <cstdint>
 #include <mutex>
 
+#include <cuda.h>
+
 #include "common.cuh"
 #include "launch.h"
 #include "warp_mma.cuh"
@@ -479,30 +481,75 @@ __global__ void __launch_bounds__(kThreads, 2)
 namespace {
 static __device__ __align__(256) uint8_t g_decode_scratch[kDecodeStaticScratch];
 
+// The array's device address belongs to a CUDA context: a device's primary
+// context, a context the caller made current, or the new primary context a
+// cudaDeviceReset leads to all hold it at their own address.  Addresses are
+// therefore cached per context, under the context's process-unique id (a
+// handle value can be reused by a later context; the id cannot).
+struct ScratchEntry {
+    unsigned long long ctx_id;
+    void *ptr;
+};
+constexpr int kScratchEntries = 64;
 std::mutex g_scratch_mutex;
-void *g_scratch_ptr[64];
+ScratchEntry g_scratch[kScratchEntries];
+int g_scratch_used = 0, g_scratch_next = 0;
+
+using CtxGetCurrentFn = CUresult (*)(CUcontext *);
+using CtxGetIdFn = CUresult (*)(CUcontext, unsigned long long *);
+
+template <class Fn>
+Fn driver_fn(const char *name)
+{
+    void *f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion(name, &f, 12000, cudaEnableDefault, &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess) {
+        cudaGetLastError();
+        return nullptr;
+    }
+    return reinterpret_cast<Fn>(f);
 }
 
-// Device address of the scratch array on the current device.  The first call
-// on a device looks it up (host code cannot use the array's name as a device
-// address); later calls return the cached pointer.
+// Unique id of the calling thread's current context; false when there is
+// none yet (the runtime creates the primary context on its first use).
+bool current_ctx_id(unsigned long long &id)
+{
+    static CtxGetCurrentFn get_current = driver_fn<CtxGetCurrentFn>("cuCtxGetCurrent");
+    static CtxGetIdFn get_id = driver_fn<CtxGetIdFn>("cuCtxGetId");
+    if (!get_current || !get_id)
+        return false;
+    CUcontext ctx = nullptr;
+    if (get_current(&ctx) != CUDA_SUCCESS || !ctx)
+        return false;
+    return get_id(ctx, &id) == CUDA_SUCCESS;
+}
+} // namespace
+
+// Device address of the scratch array in the current context.  The first call
+// in a context looks it up (host code cannot use the array's name as a device
+// address); later calls in that context return the cached pointer.
 cudaError_t decode_static_scratch(void **ptr)
 {
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
+    std::lock_guard<std::mutex> lock(g_scratch_mutex);
+    unsigned long long id = 0;
+    if (current_ctx_id(id))
+        for (int n = 0; n < g_scratch_used; ++n)
+            if (g_scratch[n].ctx_id == id) {
+                *ptr = g_scratch[n].ptr;
+                return cudaSuccess;
+            }
+    void *p = nullptr;
+    cudaError_t e = cudaGetSymbolAddress(&p, g_decode_scratch); // makes a context current if none was
     if (e != cudaSuccess)
         return e;
-    if (dev < 0 || dev >= 64)
-        return cudaErrorInvalidDevice;
-    std::lock_guard<std::mutex> lock(g_scratch_mutex);
-    if (!g_scratch_ptr[dev]) {
-        void *p = nullptr;
-        e = cudaGetSymbolAddress(&p, g_decode_scratch);
-        if (e != cudaSuccess)
-            return e;
-        g_scratch_ptr[dev] = p;
+    if (current_ctx_id(id)) {
+        ScratchEntry &slot = g_scratch_used < kScratchEntries ? g_scratch[g_scratch_used++]
+                                                              : g_scratch[g_scratch_next++ % kScratchEntries];
+        slot.ctx_id = id;
+        slot.ptr = p;
     }
-    *ptr = g_scratch_ptr[dev];
+    *ptr = p;
     return cudaSuccess;
 }
 

@@ -332,9 +332,11 @@ fl_status fl_attn_decode(const fl_tensor *q, const fl_tensor *k_cache, const fl_
  * FL_DECODE_STATIC_SCRATCH_BYTES (64 MiB) inside this library, which every GPU
  * that loads the library holds until the process exits; shapes that need more
  * (see fl_attn_decode_workspace_size) return FL_ERR_UNSUPPORTED.  The first
- * call on each device looks up the array's device address (which may load
- * the library's device code on that device): make that first call before any
- * stream capture.  Every call shares the one array and finds the previous
+ * call in each CUDA context -- a device's primary context, a context the
+ * caller made current, or the new primary context after cudaDeviceReset --
+ * looks up the array's device address in that context (which may load the
+ * library's device code there): make that first call before any stream
+ * capture.  Every call shares the one array and finds the previous
  * call's contents; the call clears what must start at zero, but calls that
  * overlap on the GPU race: issue them on one stream, or order them.
  * Arguments, layouts and results are those of fl_attn_decode.

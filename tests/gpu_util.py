@@ -107,3 +107,20 @@ def sample_rows(B, H, S, n, seed=0):
         i = fixed[t] if t < len(fixed) else int(rng.integers(0, S))
         rows.append((int(rng.integers(0, B)), int(rng.integers(0, H)), i))
     return np.array(rows, dtype=np.int64)
+
+
+def block_edge_rows(B, H, S, n_random=0, seed=0, bm=128):
+    """(b, h, i) triples: the first and the last query row of every
+    (batch, head, 128-row query block), plus `n_random` seeded rows."""
+    rows = []
+    for b in range(B):
+        for h in range(H):
+            for q0 in range(0, S, bm):
+                rows.append((b, h, q0))
+                last = min(q0 + bm, S) - 1
+                if last != q0:
+                    rows.append((b, h, last))
+    rng = np.random.default_rng(seed)
+    for _ in range(n_random):
+        rows.append((int(rng.integers(0, B)), int(rng.integers(0, H)), int(rng.integers(0, S))))
+    return np.array(rows, dtype=np.int64)

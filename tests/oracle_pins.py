@@ -349,6 +349,48 @@ def pin_evo(lib):
     _close(lc, lrow, atol=1e-12, what="evo col LSE")
 
 
+def pin_composed_rows(lib):
+    """The composed forms' sampled-row paths (Evoformer row and column passes,
+    differential attention) equal the same rows of their full-tensor results,
+    which the closed forms above pin.  N_seq = N_res = H here, so a gate gathered with
+    its residue and head axes exchanged stays in bounds and gives other values;
+    a second, larger shape has distinct extents on every axis.  The
+    differential LSE of stream 0 is also compared with the plain attention of
+    stream 0, which fixes the stream order."""
+    for Ns, Nr, H in ((4, 4, 4), (7, 45, 3)):
+        c = 32
+        q, k, v, g = (_rand((Ns, Nr, H, c), n + f"cr{Nr}") for n in ("q", "k", "v", "g"))
+        bias = _rand((H, Nr, Nr), f"bcr{Nr}")
+        o, lse = oracle.evo_row(q, k, v, bias, g, lib=lib)
+        rows = np.array([[s, h, i] for s in range(Ns) for h in range(H) for i in range(Nr)
+                         if (s + 2 * h + 3 * i) % 4 == 0 or Nr == H])
+        o2, l2 = oracle.evo_row(q, k, v, bias, g, rows=rows, lib=lib)
+        for n, (s, h, i) in enumerate(rows):
+            _close(o2[n], o[s, i, h], atol=0, what="evo row rows= O")
+            _close(l2[n], lse[s, h, i], atol=0, what="evo row rows= LSE")
+        oc, lc = oracle.evo_col(q, k, v, g, lib=lib)
+        crow = np.array([[r, h, s] for r in range(Nr) for h in range(H) for s in range(Ns)
+                         if (r + h + 2 * s) % 3 == 0 or Nr == H])
+        oc2, lc2 = oracle.evo_col(q, k, v, g, rows=crow, lib=lib)
+        for n, (r, h, s) in enumerate(crow):
+            _close(oc2[n], oc[r, s, h], atol=0, what="evo col rows= O")
+            _close(lc2[n], lc[r, h, s], atol=0, what="evo col rows= LSE")
+    B, S, Hd = 2, 70, 3
+    q = _rand((2, B, S, Hd, 64), "qcr")
+    k = _rand((2, B, S, Hd, 64), "kcr")
+    v = _rand((B, S, Hd, 128), "vcr")
+    for mask in ("none", "causal"):
+        o, lse = oracle.diff_attention(q, k, v, 0.8, mask=mask, lib=lib)
+        _, l0 = oracle.attention(q[0], k[0], v, mask=mask, lib=lib)
+        _close(lse[0], l0, atol=0, what="diff LSE stream 0")
+        rows = np.array([[b, h, i] for b in range(B) for h in range(Hd) for i in range(0, S, 7)])
+        o2, l2 = oracle.diff_attention(q, k, v, 0.8, mask=mask, rows=rows, lib=lib)
+        for n, (b, h, i) in enumerate(rows):
+            _close(o2[n], o[b, i, h], atol=0, what="diff rows= O")
+            for st in range(2):
+                _close(l2[st, n], lse[st, b, h, i], atol=0, what="diff rows= LSE")
+
+
 def pin_fully_masked_row(lib):
     """A row with no allowed key (a document table whose first document starts
     after row 0 cannot occur in the workloads, so use prefix on Sq > Sk via a
@@ -627,5 +669,5 @@ def pin_score_expr(lib):
 
 ALL_PINS = [pin_constant_scores, pin_alibi_geometric, pin_softcap_two_keys, pin_one_hot,
             pin_rows_sum_to_one, pin_shift_invariance, pin_permutation, pin_causal_row0,
-            pin_sdpa, pin_reductions, pin_rows_api, pin_diff, pin_evo, pin_fully_masked_row,
+            pin_sdpa, pin_reductions, pin_rows_api, pin_composed_rows, pin_diff, pin_evo, pin_fully_masked_row,
             pin_decode, pin_key_mask, pin_score_expr, pin_backward, pin_backward_expr]

@@ -95,14 +95,11 @@ def test_evo_full_size(row):
     o, lse, cnt, err = run_evo(row, q, k, v, g, bias)
     assert err == 0
     B, S = (Ns, Nr) if row else (Nr, Ns)
-    rows = gu.sample_rows(B, H, S, 64, seed=11)
+    # the whole output against the oracle
     if row:
-        oref, lref = oracle.evo_row(q, k, v, bias, g, rows=rows)
-        o_s = np.stack([o[b, i, h] for b, h, i in rows])
+        oref, lref = oracle.evo_row(q, k, v, bias, g)
     else:
-        oref, lref = oracle.evo_col(q, k, v, g, rows=rows)
-        o_s = np.stack([o[i, b, h] for b, h, i in rows])
-    l_s = np.array([lse[b, h, i] for b, h, i in rows])
-    gu.compare(o_s, l_s, oref, lref, what="evo full " + ("row" if row else "col"))
+        oref, lref = oracle.evo_col(q, k, v, g)
+        oref = np.swapaxes(oref, 0, 1)
+    gu.compare(o, lse, oref, lref, what="evo full " + ("row" if row else "col"))
     assert np.array_equal(cnt, gu.expected_tile_counts("none", B, H, S))
-    assert np.all(np.isfinite(o))

@@ -107,6 +107,17 @@ def test_partial_last_head_strip(B, Hq, Hk, mask):
     _check(q, k, v, "none", mask, f"strip{B}_{Hq}_{Hk}")
 
 
+# more work items than SMs, so every CTA of the persistent grid runs two or more
+# items (Q double buffer across items, the S warp's item ring, the longest-
+# first order of the causal-family masks), compared everywhere
+@pytest.mark.parametrize("B,S,Hq,Hk,mask", [(4, 640, 16, 16, "none"), (4, 640, 16, 16, "causal"),
+                                            (4, 640, 16, 16, "doc"), (8, 384, 16, 2, "window"),
+                                            (8, 384, 16, 2, "prefix")])
+def test_persistent_items_everywhere(B, S, Hq, Hk, mask):
+    q, k, v = _inputs(f"persist{B}_{S}_{Hq}_{Hk}", B, S, Hq, Hk)
+    _check(q, k, v, "softcap" if mask == "doc" else "none", mask, f"persist{B}_{S}_{Hq}_{Hk}")
+
+
 @pytest.mark.parametrize("S", [1, 127, 128, 129, 257])
 def test_edge_lengths(S):
     q, k, v = _inputs(f"edge{S}", 1, S, 2)
@@ -139,7 +150,10 @@ def _full_size(S, B, Hq, Hk, mod, mask, tag, n_rows=96, **kw):
     okw = dict(kw)
     o, lse, cnt, err = gu.run_standard(q, k, v, score_mod=mod, mask=mask, **kw)
     assert err == 0
-    rows = gu.sample_rows(B, Hq, S, n_rows, seed=S)
+    # the first and last row of every (batch, head, query block) -- every work
+    # item of the persistent grid, and both ends of each item's key range --
+    # plus seeded random rows
+    rows = gu.block_edge_rows(B, Hq, S, n_random=n_rows, seed=S)
     oref, lref = oracle.attention(q, k, v, mod=mod, mask=mask, rows=rows, **okw)
     o_s = np.stack([o[b, i, h] for b, h, i in rows])
     l_s = np.array([lse[b, h, i] for b, h, i in rows])

@@ -165,3 +165,34 @@ def test_expr_grad_mutant_is_caught(name, monkeypatch):
     monkeypatch.setattr(se, "evaluate_with_grad", ns["evaluate_with_grad"])
     with pytest.raises(AssertionError):
         oracle_pins.pin_backward_expr(oracle.load())
+
+
+# Mistakes planted in the composed forms' sampled-row paths (the gate gather of
+# the Evoformer passes, the order of the differential streams): the source of
+# the one function is edited in memory and swapped in for the test.
+COMPOSED_MUTANTS = {
+    "evo_row_gate_axes_exchanged": ("evo_row", "gate[r[:, 0], r[:, 2], r[:, 1], :]",
+                                    "gate[r[:, 0], r[:, 1], r[:, 2], :]"),
+    "evo_row_gate_msa_row_from_head": ("evo_row", "gate[r[:, 0], r[:, 2], r[:, 1], :]",
+                                       "gate[r[:, 1], r[:, 2], r[:, 1], :]"),
+    "evo_col_gate_axes_exchanged": ("evo_col", "gt[r[:, 0], r[:, 2], r[:, 1], :]",
+                                    "gt[r[:, 0], r[:, 1], r[:, 2], :]"),
+    "evo_col_gate_not_swapped": ("evo_col", "gt[r[:, 0], r[:, 2], r[:, 1], :]",
+                                 "gate[r[:, 0] % gate.shape[0], r[:, 2] % gate.shape[1], r[:, 1], :]"),
+    "diff_streams_stacked_reversed": ("diff_attention", "np.stack([l1, l2])", "np.stack([l2, l1])"),
+}
+
+
+@pytest.mark.parametrize("name", sorted(COMPOSED_MUTANTS))
+def test_composed_mutant_is_caught(name, monkeypatch):
+    import inspect
+    import textwrap
+
+    fn, a, b = COMPOSED_MUTANTS[name]
+    src = textwrap.dedent(inspect.getsource(getattr(oracle, fn)))
+    assert src.count(a) == 1, name
+    ns = dict(vars(oracle))
+    exec(compile(src.replace(a, b), "<mutant>", "exec"), ns)
+    monkeypatch.setattr(oracle, fn, ns[fn])
+    with pytest.raises(AssertionError):
+        oracle_pins.pin_composed_rows(oracle.load())
