@@ -268,8 +268,8 @@ fl_status fwd_standard(const fl_tensor *q, const fl_tensor *k, const fl_tensor *
         return fail(FL_ERR_INVALID_ARG, "scale must be finite and positive (0 selects 1/sqrt(D))");
     if (d->mask == FL_MASK_DOC && d->doc_stride < 2)
         return fail(FL_ERR_INVALID_ARG, "doc_stride must be >= 2");
-    if (D != 64 || Dv != 64)
-        return fail(FL_ERR_UNSUPPORTED, "standard kind supports D = Dv = 64 (got %lld, %lld)",
+    if (D != Dv || (D != 32 && D != 64 && D != 128))
+        return fail(FL_ERR_UNSUPPORTED, "standard kind supports D = Dv in {32, 64, 128} (got %lld, %lld)",
                     (long long)D, (long long)Dv);
     const int nq = static_cast<int>((S + fl::BM - 1) / fl::BM);
     fl::GridSpec work{};
@@ -283,32 +283,37 @@ fl_status fwd_standard(const fl_tensor *q, const fl_tensor *k, const fl_tensor *
     if ((s = device_info(dev, info)) != FL_OK) return s;
 
     CUtensorMap tq, tk, tv;
-    const uint32_t box[4] = {64, 128, 1, 1};
-    const uint32_t kvbox[4] = {64, uint32_t(fl::kStdKeyTile), 1, 1};
+    // rows of up to 128 bytes per TMA box (D = 128: two boxes per row, the
+    // kernel loads both halves); the swizzle is the box row's width
+    const uint32_t box_cols = D == 128 ? 64u : uint32_t(D);
+    const CUtensorMapSwizzle swz = D == 32 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_128B;
+    const uint32_t box[4] = {box_cols, 128, 1, 1};
+    const uint32_t kvbox[4] = {box_cols, uint32_t(fl::std_key_tile(int(D))), 1, 1};
     {
         const uint64_t dims[4] = {uint64_t(D), uint64_t(S), uint64_t(Hq), uint64_t(B)};
         const uint64_t st[3] = {uint64_t(Q.stride[1]) * 2, uint64_t(Q.stride[2]) * 2,
                                 uint64_t(Q.stride[0]) * 2};
-        if ((s = make_map(tq, Q.ptr, 4, dims, st, box, CU_TENSOR_MAP_SWIZZLE_128B, "q")) != FL_OK)
+        if ((s = make_map(tq, Q.ptr, 4, dims, st, box, swz, "q")) != FL_OK)
             return s;
     }
     {
         const uint64_t dims[4] = {uint64_t(D), uint64_t(S), uint64_t(Hk), uint64_t(B)};
         const uint64_t st[3] = {uint64_t(K.stride[1]) * 2, uint64_t(K.stride[2]) * 2,
                                 uint64_t(K.stride[0]) * 2};
-        if ((s = make_map(tk, K.ptr, 4, dims, st, kvbox, CU_TENSOR_MAP_SWIZZLE_128B, "k")) != FL_OK)
+        if ((s = make_map(tk, K.ptr, 4, dims, st, kvbox, swz, "k")) != FL_OK)
             return s;
     }
     {
         const uint64_t dims[4] = {uint64_t(Dv), uint64_t(S), uint64_t(Hk), uint64_t(B)};
         const uint64_t st[3] = {uint64_t(V.stride[1]) * 2, uint64_t(V.stride[2]) * 2,
                                 uint64_t(V.stride[0]) * 2};
-        if ((s = make_map(tv, V.ptr, 4, dims, st, kvbox, CU_TENSOR_MAP_SWIZZLE_128B, "v")) != FL_OK)
+        if ((s = make_map(tv, V.ptr, 4, dims, st, kvbox, swz, "v")) != FL_OK)
             return s;
     }
 
     fl::StdParams p{};
     p.grid = work;
+    p.head_dim = int(D);
     p.mask.kind = d->mask;
     p.mask.S = int(S);
     p.mask.window = d->window;
@@ -399,8 +404,8 @@ fl_status fwd_diff(const fl_tensor *q, const fl_tensor *k, const fl_tensor *v,
         return fail(FL_ERR_UNSUPPORTED, "differential attention takes no score_mod");
     if (!std::isfinite(d->scale) || d->scale < 0.f || !std::isfinite(d->diff_lambda))
         return fail(FL_ERR_INVALID_ARG, "scale must be finite and positive, diff_lambda finite");
-    if (D != 64 || Dv != 128)
-        return fail(FL_ERR_UNSUPPORTED, "differential kind supports D = 64, Dv = 128");
+    if (D != 64 || (Dv != 64 && Dv != 128))
+        return fail(FL_ERR_UNSUPPORTED, "differential kind supports D = 64, Dv = 64 or 128");
 
     int dev;
     DeviceInfo info;
@@ -431,6 +436,7 @@ fl_status fwd_diff(const fl_tensor *q, const fl_tensor *k, const fl_tensor *v,
             return s;
     }
     fl::DiffParams p{};
+    p.dv = int(Dv);
     p.B = int(B);
     p.H = int(H);
     p.Hk = int(Hk);
@@ -1225,6 +1231,10 @@ fl_status fl_attn_tile_shape(const fl_attn_variant_desc *desc, int32_t head_dim,
         return fail(FL_ERR_INVALID_ARG, "NULL argument");
     switch (desc->kind) {
     case FL_KIND_STANDARD:
+        if (head_dim != 32 && head_dim != 64 && head_dim != 128)
+            return fail(FL_ERR_UNSUPPORTED, "head_dim %d not supported for kind %d", head_dim,
+                        desc->kind);
+        break;
     case FL_KIND_DIFF:
         if (head_dim != 64)
             return fail(FL_ERR_UNSUPPORTED, "head_dim %d not supported for kind %d", head_dim,
@@ -1240,7 +1250,7 @@ fl_status fl_attn_tile_shape(const fl_attn_variant_desc *desc, int32_t head_dim,
         return fail(FL_ERR_INVALID_ARG, "unknown kind %d", desc->kind);
     }
     *block_m = fl::BM;
-    *block_n = desc->kind == FL_KIND_STANDARD ? fl::kStdKeyTile : fl::BN;
+    *block_n = desc->kind == FL_KIND_STANDARD ? fl::std_key_tile(head_dim) : fl::BN;
     return ok();
 }
 

@@ -1,4 +1,4 @@
-// fwd_diff.cu -- differential attention forward, D = 64, Dv = 128:
+// fwd_diff.cu -- differential attention forward, D = 64, Dv = 64 or 128:
 //     O = softmax(scale Q1 K1^T) V - lambda softmax(scale Q2 K2^T) V
 // with both softmax streams fused in one kernel and sharing every V tile
 // (the pages name differential attention among the variants that template
@@ -7,12 +7,13 @@
 //
 // CTA organisation (persistent, 384 threads):
 //   warpgroup 0  online softmax of stream 1 (one thread per query row), then
-//                output columns 0..63
-//   warpgroup 1  online softmax of stream 2, then output columns 64..127
+//                output columns [0, Dv / 2)
+//   warpgroup 1  online softmax of stream 2, then output columns [Dv / 2, Dv)
 //   warp 8       TMA producer (Q1, Q2 once per work item; K1, K2, V per key tile)
 //   warp 9       MMA issuer and TMEM owner
 // TMEM: S_s at columns 128 s (P_s written over the first 64 of them),
-// O_s (Dv = 128 fp32) at 256 + 128 s.  Per key tile j the MMA thread issues,
+// O_s (Dv fp32 columns) at 256 + 128 s.  V tiles arrive as Dv / 64 halves of
+// 64 columns, each the B operand of its own N = 64 P V product.  Per key tile j the MMA thread issues,
 // for s = 1, 2: [O_s += P_s V_{j-1}] then S_s = Q_s K_{s,j}^T, so the tensor
 // core works on one stream while the other stream's softmax runs.  P_s may
 // reuse S_s's columns because tcgen05.mma operations issued by one thread
@@ -37,10 +38,12 @@ constexpr uint32_t kRegsOther = 72;
 static_assert(2 * 128 * kRegsSoftmax + 128 * kRegsOther == kThreads * kRegsLaunch,
               "register split must equal the launch allocation");
 
+template <int DV>
 struct __align__(1024) DiffSmem {
+    static constexpr int kVHalves = DV / 64;
     uint8_t q[2][kTile];
     uint8_t k[kStages][2][kTile];
-    uint8_t v[kStages][2][kTile]; // the two 64-column halves of a 128 x 128 V tile
+    uint8_t v[kStages][kVHalves][kTile]; // the 64-column halves of a 128 x Dv V tile
     float lx[2][BM];              // each stream's row sums for the combined epilogue
     uint64_t q_full, q_empty;
     uint64_t kv_full[kStages], kv_empty[kStages];
@@ -54,8 +57,9 @@ __device__ uint32_t g_lib_error_word;
 
 __device__ __forceinline__ uint32_t bar(const uint64_t &b) { return ptx::smem_u32(&b); }
 
+template <int DV>
 struct Ctx {
-    DiffSmem *sm;
+    DiffSmem<DV> *sm;
     uint32_t tmem;
     WaitCtl wc;
 };
@@ -88,10 +92,12 @@ __device__ __forceinline__ DiffItem decode(const DiffParams &p, int64_t L)
     return it;
 }
 
-__device__ void producer_role(const Ctx &cx, const DiffParams &p, const CUtensorMap *tm_q,
+template <int DV>
+__device__ void producer_role(const Ctx<DV> &cx, const DiffParams &p, const CUtensorMap *tm_q,
                               const CUtensorMap *tm_k, const CUtensorMap *tm_v)
 {
-    DiffSmem &sm = *cx.sm;
+    constexpr int kVHalves = DiffSmem<DV>::kVHalves;
+    DiffSmem<DV> &sm = *cx.sm;
     const uint32_t lane = ptx::lane_id();
     uint32_t kv_count = 0, item_count = 0;
     bool ok = true;
@@ -116,11 +122,11 @@ __device__ void producer_role(const Ctx &cx, const DiffParams &p, const CUtensor
             if (!ok)
                 break;
             if (lane == 0) {
-                ptx::mbar_arrive_expect_tx(bar(sm.kv_full[st]), 4 * kTile);
+                ptx::mbar_arrive_expect_tx(bar(sm.kv_full[st]), (2 + kVHalves) * kTile);
                 for (int s = 0; s < 2; ++s)
                     ptx::tma_load_5d(ptx::smem_u32(sm.k[st][s]), tm_k, bar(sm.kv_full[st]), 0,
                                      j * BN, it.kvh, it.b, s);
-                for (int half = 0; half < 2; ++half)
+                for (int half = 0; half < kVHalves; ++half)
                     ptx::tma_load_4d(ptx::smem_u32(sm.v[st][half]), tm_v, bar(sm.kv_full[st]),
                                      64 * half, j * BN, it.kvh, it.b);
             }
@@ -137,9 +143,11 @@ __device__ void producer_role(const Ctx &cx, const DiffParams &p, const CUtensor
     }
 }
 
-__device__ void mma_role(const Ctx &cx, const DiffParams &p)
+template <int DV>
+__device__ void mma_role(const Ctx<DV> &cx, const DiffParams &p)
 {
-    DiffSmem &sm = *cx.sm;
+    constexpr int kVHalves = DiffSmem<DV>::kVHalves;
+    DiffSmem<DV> &sm = *cx.sm;
     const uint32_t lane = ptx::lane_id();
     constexpr uint32_t idesc_qk = umma_idesc_bf16(BM, BN, false);
     constexpr uint32_t idesc_pv = umma_idesc_bf16(BM, 64, true);
@@ -174,7 +182,7 @@ __device__ void mma_role(const Ctx &cx, const DiffParams &p)
                     ptx::tc_fence_after();
                     if (lane == 0) {
 #pragma unroll
-                        for (int half = 0; half < 2; ++half) {
+                        for (int half = 0; half < kVHalves; ++half) {
                             const uint32_t vb = ptx::smem_u32(sm.v[prev][half]);
 #pragma unroll
                             for (int kk = 0; kk < BN / 16; ++kk)
@@ -225,9 +233,10 @@ __device__ void mma_role(const Ctx &cx, const DiffParams &p)
     mbar_wait_drain(bar(sm.final_bar), 0, cx.wc, W_FINAL);
 }
 
-__device__ void softmax_role(const Ctx &cx, const DiffParams &p, int s)
+template <int DV>
+__device__ void softmax_role(const Ctx<DV> &cx, const DiffParams &p, int s)
 {
-    DiffSmem &sm = *cx.sm;
+    DiffSmem<DV> &sm = *cx.sm;
     const int r = threadIdx.x & 127;
     const uint32_t lane_off = (((threadIdx.x >> 5) & 3u) * 32u) << 16;
     const uint32_t tS = cx.tmem + lane_off + 128 * s;
@@ -254,12 +263,13 @@ __device__ void softmax_role(const Ctx &cx, const DiffParams &p, int s)
             apply_score_mod<MOD_NONE>(x, smod, i, j0);
             if (!((j0 >= tr.full_lo) && (j0 + BN <= tr.full_hi)))
                 apply_row_mask(x, j0, row_lo, row_hi);
-            online_update_and_store_p<128>(x, p.qk_log2, st, j == tr.lo, tO[s], tS);
+            online_update_and_store_p<DV>(x, p.qk_log2, st, j == tr.lo, tO[s], tS);
             ptx::tc_fence_before();
             ptx::mbar_arrive(bar(sm.p_full[s]));
         }
 
-        // epilogue: share l, then this warpgroup writes output columns [64 s, 64 s + 64)
+        // epilogue: share l, then this warpgroup writes output columns
+        // [Dv / 2 s, Dv / 2 (s + 1))
         sm.lx[s][r] = st.l_round;
         ptx::mbar_arrive(bar(sm.l_full));
         if (p.lse && i < p.mask.S)
@@ -275,12 +285,12 @@ __device__ void softmax_role(const Ctx &cx, const DiffParams &p, int s)
         const float c0 = l0 > 0.f ? 1.f / l0 : 0.f;
         const float c1 = l1 > 0.f ? -p.lambda / l1 : 0.f;
         __nv_bfloat16 *dst = p.out + it.b * p.o_sb + static_cast<int64_t>(i) * p.o_ss +
-                             it.h * p.o_sh + 64 * s;
+                             it.h * p.o_sh + (DV / 2) * s;
 #pragma unroll 1
-        for (int c = 0; c < 4; ++c) {
+        for (int c = 0; c < DV / 32; ++c) {
             uint32_t a[16], bb[16];
-            ptx::tmem_ld16(tO[0] + 64 * s + 16 * c, a);
-            ptx::tmem_ld16(tO[1] + 64 * s + 16 * c, bb);
+            ptx::tmem_ld16(tO[0] + (DV / 2) * s + 16 * c, a);
+            ptx::tmem_ld16(tO[1] + (DV / 2) * s + 16 * c, bb);
             ptx::tmem_wait_ld();
             ptx::reg_fence<16>(a);
             ptx::reg_fence<16>(bb);
@@ -303,13 +313,14 @@ __device__ void softmax_role(const Ctx &cx, const DiffParams &p, int s)
     }
 }
 
+template <int DV>
 __global__ void __launch_bounds__(kThreads, 1)
     diff_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                     const __grid_constant__ CUtensorMap tm_v, const DiffParams p)
 {
     extern __shared__ uint8_t smem_raw[];
     const uint32_t base = ptx::smem_u32(smem_raw);
-    DiffSmem *sm = reinterpret_cast<DiffSmem *>(smem_raw + ((1024u - (base & 1023u)) & 1023u));
+    DiffSmem<DV> *sm = reinterpret_cast<DiffSmem<DV> *>(smem_raw + ((1024u - (base & 1023u)) & 1023u));
     const int warp = threadIdx.x >> 5;
     if (threadIdx.x == 0) {
         ptx::mbar_init(bar(sm->q_full), 1);
@@ -342,7 +353,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     ptx::tc_fence_before();
     __syncthreads();
     ptx::tc_fence_after();
-    Ctx cx;
+    Ctx<DV> cx;
     cx.sm = sm;
     cx.tmem = sm->tmem_base;
     cx.wc.abort_flag = &sm->abort_flag;
@@ -351,15 +362,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     cx.wc.err_lib = &g_lib_error_word;
     if (warp < 8) {
         ptx::setmaxnreg_inc<kRegsSoftmax>();
-        softmax_role(cx, p, warp >> 2);
+        softmax_role<DV>(cx, p, warp >> 2);
         ptx::tc_fence_before();
         ptx::named_barrier_sync(1, kThreads);
     } else {
         ptx::setmaxnreg_dec<kRegsOther>();
         if (warp == 8)
-            producer_role(cx, p, &tm_q, &tm_k, &tm_v);
+            producer_role<DV>(cx, p, &tm_q, &tm_k, &tm_v);
         else if (warp == 9)
-            mma_role(cx, p);
+            mma_role<DV>(cx, p);
         ptx::tc_fence_before();
         ptx::named_barrier_sync(1, kThreads);
         if (warp == 9) {
@@ -369,28 +380,36 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 }
 
-} // namespace
-
-cudaError_t launch_diff(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
-                        const DiffParams &p, int grid, cudaStream_t stream)
+template <int DV>
+cudaError_t launch_dv(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
+                      const DiffParams &p, int grid, cudaStream_t stream)
 {
-    const size_t smem = sizeof(DiffSmem) + 1024;
+    const size_t smem = sizeof(DiffSmem<DV>) + 1024;
     static bool configured = false;
     if (!configured) {
         cudaFuncAttributes attr;
-        cudaError_t e = cudaFuncGetAttributes(&attr, diff_fwd_kernel);
+        cudaError_t e = cudaFuncGetAttributes(&attr, diff_fwd_kernel<DV>);
         if (e != cudaSuccess)
             return e;
         if (attr.numRegs != static_cast<int>(kRegsLaunch))
             return cudaErrorInvalidConfiguration;
-        e = cudaFuncSetAttribute(diff_fwd_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        e = cudaFuncSetAttribute(diff_fwd_kernel<DV>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  static_cast<int>(smem));
         if (e != cudaSuccess)
             return e;
         configured = true;
     }
-    diff_fwd_kernel<<<grid, kThreads, smem, stream>>>(tq, tk, tv, p);
+    diff_fwd_kernel<DV><<<grid, kThreads, smem, stream>>>(tq, tk, tv, p);
     return cudaGetLastError();
+}
+
+} // namespace
+
+cudaError_t launch_diff(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
+                        const DiffParams &p, int grid, cudaStream_t stream)
+{
+    return p.dv == 64 ? launch_dv<64>(tq, tk, tv, p, grid, stream)
+                      : launch_dv<128>(tq, tk, tv, p, grid, stream);
 }
 
 } // namespace fl

@@ -1,4 +1,5 @@
-// fwd_standard.cu -- fused attention forward for MHA / GQA, D = Dv = 64,
+// fwd_standard.cu -- fused attention forward for MHA / GQA, D = Dv in
+// {32, 64, 128},
 // with the ALiBi and softcap score_mods and the causal, window, prefix and
 // document masks (sm_103a: TMA + mbarrier ring + tcgen05.mma into TMEM).
 //
@@ -28,12 +29,20 @@
 // register count before launching).
 // Each work item is two 128-row query tiles ("slots") sharing every K/V tile.
 //
-// Key tiles are kBN = 112 keys wide, so that TMEM (512 columns x 128 lanes,
-// lane = query row) holds, for slots t = 0, 1: S[t] fp32 at 112 t, O[t] fp32 at
-// 224 + 80 t with 80 columns -- 64 output columns and 16 columns of sum_j P_j
-// (P V multiplies P by V extended with a tile of ones, so the tensor core sums
-// the exact bf16 P it used: the normaliser of O) -- and P[t] bf16 pairs at
-// 384 + 64 t.  The softmax then keeps only the exact sum (for the LSE).
+// TMEM (512 columns x 128 lanes, lane = query row) per head dimension, for
+// slots t = 0, 1 (StdCfg below):
+//   D = 32, 64:  key tiles of 112 keys; S[t] fp32 at 112 t, O[t] at 224 + (D + 16) t
+//                with D output columns and 16 columns of sum_j P_j (P V
+//                multiplies P by V extended with a tile of ones, so the tensor
+//                core sums the exact bf16 P it used: the normaliser of O), P[t]
+//                bf16 pairs at 384 + 64 t; the softmax keeps only the exact sum
+//                (for the LSE);
+//   D = 128:     key tiles of 64 keys; S[t] at 64 t, O[t] at 128 + 128 t (two
+//                128-column accumulators leave no room for sum columns), P[t]
+//                at 384 + 32 t; the softmax keeps both sums in registers (the
+//                sum of the bf16-rounded P normalises O).
+// Q, K and V rows of D = 128 are 256 bytes: each tile is two 64-column halves
+// (two TMA boxes, 128-byte swizzle), and Q K^T walks both.
 //
 // Hand-off protocol for slot t and key tile j (all mbarriers):
 //   softmax: wait s_full(t); S[t] -> registers; arrive s_free(t); take the
@@ -63,15 +72,31 @@ constexpr uint32_t kRegsSoftmax = 200;
 constexpr uint32_t kRegsOther = 104;
 static_assert(2 * 128 * kRegsSoftmax + 128 * kRegsOther == kThreads * kRegsLaunch,
               "register split must equal the launch allocation");
-constexpr int kStages = 4;
-constexpr int kBN = 112;                        // keys per K/V tile
-constexpr uint32_t kTileBytes = BM * 64 * 2;    // one 128 x 64 bf16 Q tile
-constexpr uint32_t kKVBytes = kBN * 64 * 2;     // one 112 x 64 bf16 K or V tile
-constexpr uint32_t kDvExt = 80;                 // 64 output columns + 16 sum columns
-constexpr uint32_t kColSum = 64;
-static_assert(kBN == kStdKeyTile, "the host encodes K/V tensor maps with kStdKeyTile rows");
-constexpr uint32_t kColS = 0, kColO = 224, kColP = 384;
-constexpr uint32_t kStrideS = kBN, kStrideO = kDvExt, kStrideP = 64;
+// Tile shapes, shared-memory layout and TMEM columns per head dimension.
+template <int D>
+struct StdCfg {
+    static_assert(D == 32 || D == 64 || D == 128, "head dimension");
+    static constexpr int kBN = std_key_tile(D);           // keys per K/V tile
+    static constexpr int kStages = D == 128 ? 3 : 4;       // K/V ring depth
+    static constexpr bool kOnes = D <= 64;                 // row sum from a ones column block
+    static constexpr int kHalves = D == 128 ? 2 : 1;       // 64-column halves of a row
+    static constexpr int kBoxCols = D / kHalves;           // columns per TMA box (32 or 64)
+    static constexpr uint32_t kRowBytes = kBoxCols * 2;    // swizzle width: 64 or 128 bytes
+    static constexpr uint32_t kSwz = kRowBytes == 128 ? kSwizzle128B : kSwizzle64B;
+    static constexpr uint32_t kGroupBytes = 8 * kRowBytes; // 8-row core group
+    static constexpr uint32_t kQHalf = BM * kRowBytes;     // one half of a Q tile
+    static constexpr uint32_t kKVHalf = kBN * kRowBytes;   // one half of a K or V tile
+    static constexpr uint32_t kTileBytes = kHalves * kQHalf;  // one 128 x D bf16 Q tile
+    static constexpr uint32_t kKVBytes = kHalves * kKVHalf;   // one kBN x D bf16 K or V tile
+    static constexpr uint32_t kOnesBytes = kOnes ? kTileBytes : 16;
+    static constexpr uint32_t kDvExt = kOnes ? D + 16 : D; // O columns (with the sum block)
+    static constexpr uint32_t kColSum = D;                 // first sum column (D <= 64)
+    static constexpr uint32_t kColS = 0, kStrideS = kBN;
+    static constexpr uint32_t kColO = 2 * kBN, kStrideO = kDvExt;
+    static constexpr uint32_t kColP = 384, kStrideP = kBN / 2;
+    static_assert(kColO + 2 * kDvExt <= kColP && kColP + 2 * kStrideP <= 512, "TMEM budget");
+    static_assert(kBN % 16 == 0 && kBN <= 128, "key tile");
+};
 
 // A work item as decoded by the S warp for both softmax warpgroups: its batch
 // index and, per slot, head, query block and key-tile range (TileRange).
@@ -81,13 +106,16 @@ struct ItemInfo {
     int32_t lo[2], hi[2], full_lo[2], full_hi[2];
 };
 
+template <int D>
 struct __align__(1024) StdSmem {
-    uint8_t q[2][2][kTileBytes]; // [Q buffer][slot]
-    uint8_t k[kStages][kKVBytes];
-    uint8_t v[kStages][kKVBytes];
-    uint8_t ones[kTileBytes];    // bf16 1.0 everywhere: V's extra columns (after every V stage)
+    using C = StdCfg<D>;
+    uint8_t q[2][2][C::kTileBytes]; // [Q buffer][slot]
+    uint8_t k[C::kStages][C::kKVBytes];
+    uint8_t v[C::kStages][C::kKVBytes];
+    uint8_t ones[C::kOnesBytes];    // bf16 1.0 everywhere: V's extra columns (after every V
+                                    // stage; used for D <= 64)
     uint64_t q_full[2], q_empty[2];
-    uint64_t kv_full[kStages], kv_empty[kStages];
+    uint64_t kv_full[C::kStages], kv_empty[C::kStages];
     uint64_t s_full[2], s_free[2], p_full[2], pv_done[2];
     uint64_t turn[2];            // exponential-phase token of each softmax warpgroup
     uint64_t final_bar[3];
@@ -99,8 +127,9 @@ struct __align__(1024) StdSmem {
 
 __device__ uint32_t g_lib_error_word;
 
+template <int D>
 struct KernelCtx {
-    StdSmem *sm;
+    StdSmem<D> *sm;
     uint32_t tmem;
     WaitCtl wc;
 };
@@ -108,10 +137,13 @@ struct KernelCtx {
 __device__ __forceinline__ uint32_t bar(const uint64_t &b) { return ptx::smem_u32(&b); }
 
 // ------------------------------------------------------------------ producer
-__device__ void producer_role(const KernelCtx &cx, const StdParams &p, const CUtensorMap *tm_q,
+template <int D>
+__device__ void producer_role(const KernelCtx<D> &cx, const StdParams &p, const CUtensorMap *tm_q,
                               const CUtensorMap *tm_k, const CUtensorMap *tm_v)
 {
-    StdSmem &sm = *cx.sm;
+    using C = StdCfg<D>;
+    constexpr int kBN = C::kBN, kStages = C::kStages;
+    StdSmem<D> &sm = *cx.sm;
     const uint32_t lane = ptx::lane_id();
     uint32_t kv_count = 0, item_count = 0;
     int64_t dropped = -1;
@@ -136,12 +168,15 @@ __device__ void producer_role(const KernelCtx &cx, const StdParams &p, const CUt
                 break;
         }
         if (lane == 0) {
-            ptx::mbar_arrive_expect_tx(bar(sm.q_full[qbuf]), nvalid * kTileBytes);
+            ptx::mbar_arrive_expect_tx(bar(sm.q_full[qbuf]), nvalid * C::kTileBytes);
 #pragma unroll
             for (int t = 0; t < 2; ++t)
                 if (it.valid[t])
-                    ptx::tma_load_4d(ptx::smem_u32(sm.q[qbuf][t]), tm_q, bar(sm.q_full[qbuf]), 0,
-                                     it.qb[t] * BM, it.h[t], it.b);
+#pragma unroll
+                    for (int hf = 0; hf < C::kHalves; ++hf)
+                        ptx::tma_load_4d(ptx::smem_u32(sm.q[qbuf][t]) + hf * C::kQHalf, tm_q,
+                                         bar(sm.q_full[qbuf]), hf * C::kBoxCols, it.qb[t] * BM, it.h[t],
+                                         it.b);
         }
         __syncwarp();
         for (int j = lo; j < hi; ++j, ++kv_count) {
@@ -155,11 +190,14 @@ __device__ void producer_role(const KernelCtx &cx, const StdParams &p, const CUt
                 if (drop) {
                     dropped = kv_count;
                 } else {
-                    ptx::mbar_arrive_expect_tx(bar(sm.kv_full[s]), 2 * kKVBytes);
-                    ptx::tma_load_4d(ptx::smem_u32(sm.k[s]), tm_k, bar(sm.kv_full[s]), 0, j * kBN,
-                                     it.kvh, it.b);
-                    ptx::tma_load_4d(ptx::smem_u32(sm.v[s]), tm_v, bar(sm.kv_full[s]), 0, j * kBN,
-                                     it.kvh, it.b);
+                    ptx::mbar_arrive_expect_tx(bar(sm.kv_full[s]), 2 * C::kKVBytes);
+#pragma unroll
+                    for (int hf = 0; hf < C::kHalves; ++hf) {
+                        ptx::tma_load_4d(ptx::smem_u32(sm.k[s]) + hf * C::kKVHalf, tm_k, bar(sm.kv_full[s]),
+                                         hf * C::kBoxCols, j * kBN, it.kvh, it.b);
+                        ptx::tma_load_4d(ptx::smem_u32(sm.v[s]) + hf * C::kKVHalf, tm_v, bar(sm.kv_full[s]),
+                                         hf * C::kBoxCols, j * kBN, it.kvh, it.b);
+                    }
                 }
             }
             __syncwarp();
@@ -200,16 +238,21 @@ __device__ void producer_role(const KernelCtx &cx, const StdParams &p, const CUt
 // stage's previous phase complete).  q_empty takes one arrival per slot from
 // the S warp (a commit after the slot's last S of the item, or an arrival for
 // an absent slot).
-__device__ __forceinline__ uint32_t kv_stage(uint32_t idx) { return idx % kStages; }
-__device__ __forceinline__ uint32_t kv_parity(uint32_t idx) { return (idx / kStages) & 1; }
+template <int NS>
+__device__ __forceinline__ uint32_t kv_stage(uint32_t idx) { return idx % NS; }
+template <int NS>
+__device__ __forceinline__ uint32_t kv_parity(uint32_t idx) { return (idx / NS) & 1; }
 
-__device__ void s_role(const KernelCtx &cx, const StdParams &p)
+template <int D>
+__device__ void s_role(const KernelCtx<D> &cx, const StdParams &p)
 {
-    StdSmem &sm = *cx.sm;
+    using C = StdCfg<D>;
+    constexpr int kBN = C::kBN, kStages = C::kStages;
+    StdSmem<D> &sm = *cx.sm;
     const uint32_t lane = ptx::lane_id();
     constexpr uint32_t idesc_qk = umma_idesc_bf16(BM, kBN, false);
-    constexpr uint64_t kHiK = umma_desc_hi(16, 1024, kSwizzle128B); // Q, K: K-major
-    constexpr uint32_t kTileLo = kTileBytes >> 4, kKVLo = kKVBytes >> 4;
+    constexpr uint64_t kHiK = umma_desc_hi(16, C::kGroupBytes, C::kSwz); // Q, K: K-major
+    constexpr uint32_t kTileLo = C::kTileBytes >> 4, kKVLo = C::kKVBytes >> 4;
     constexpr uint32_t kBarStride = sizeof(uint64_t);
     const uint32_t q_lo0 = ptx::smem_u32(sm.q[0][0]) >> 4;
     const uint32_t k_lo0 = ptx::smem_u32(sm.k[0]) >> 4;
@@ -262,10 +305,11 @@ __device__ void s_role(const KernelCtx &cx, const StdParams &p)
             break;
         for (int j = lo; j < hi && ok; ++j) {
             const uint32_t idx = kv_base + static_cast<uint32_t>(j - lo);
-            ok = warp_wait(b_kvf0 + kv_stage(idx) * kBarStride, kv_parity(idx), cx.wc, W_KV_FULL);
+            ok = warp_wait(b_kvf0 + kv_stage<kStages>(idx) * kBarStride, kv_parity<kStages>(idx), cx.wc,
+                           W_KV_FULL);
             if (!ok)
                 break;
-            const uint32_t klo = k_lo0 + kv_stage(idx) * kKVLo;
+            const uint32_t klo = k_lo0 + kv_stage<kStages>(idx) * kKVLo;
 #pragma unroll
             for (int t = 0; t < 2; ++t) {
                 if (!it.valid[t] || j < rlo[t] || j >= rhi[t])
@@ -280,11 +324,16 @@ __device__ void s_role(const KernelCtx &cx, const StdParams &p)
                 ptx::tc_fence_after();
                 if (lane == 0) {
                     const uint32_t qlo = q_lo0 + (2 * qbuf + t) * kTileLo;
-                    const uint32_t tS = cx.tmem + kColS + kStrideS * t;
+                    const uint32_t tS = cx.tmem + C::kColS + C::kStrideS * t;
+                    // K steps of 16 features (32 bytes) inside a swizzle row,
+                    // then the next 64-column half
 #pragma unroll
-                    for (int kk = 0; kk < 4; ++kk)
-                        ptx::mma_ss(tS, kHiK | (qlo + 2 * kk), kHiK | (klo + 2 * kk), idesc_qk,
-                                    kk > 0 ? 1u : 0u);
+                    for (int kk = 0; kk < D / 16; ++kk) {
+                        constexpr int kSteps = C::kBoxCols / 16;
+                        const uint32_t qo = (kk / kSteps) * (C::kQHalf >> 4) + 2 * (kk % kSteps);
+                        const uint32_t ko = (kk / kSteps) * (C::kKVHalf >> 4) + 2 * (kk % kSteps);
+                        ptx::mma_ss(tS, kHiK | (qlo + qo), kHiK | (klo + ko), idesc_qk, kk > 0 ? 1u : 0u);
+                    }
                     ptx::mma_commit(bar(sm.s_full[t]));
                     if (j + 1 == rhi[t])
                         ptx::mma_commit(b_qe); // the slot's last read of this Q buffer
@@ -312,17 +361,20 @@ __device__ void s_role(const KernelCtx &cx, const StdParams &p)
     mbar_wait_drain(b_final, 0, cx.wc, W_FINAL);
 }
 
-__device__ void pv_role(const KernelCtx &cx, const StdParams &p, int t)
+template <int D>
+__device__ void pv_role(const KernelCtx<D> &cx, const StdParams &p, int t)
 {
-    StdSmem &sm = *cx.sm;
+    using C = StdCfg<D>;
+    constexpr int kBN = C::kBN, kStages = C::kStages;
+    StdSmem<D> &sm = *cx.sm;
     const uint32_t lane = ptx::lane_id();
-    constexpr uint32_t idesc_pv = umma_idesc_bf16(BM, kDvExt, true);
-    constexpr uint32_t kKVLo = kKVBytes >> 4;
+    constexpr uint32_t idesc_pv = umma_idesc_bf16(BM, C::kDvExt, true);
+    constexpr uint32_t kKVLo = C::kKVBytes >> 4;
     constexpr uint32_t kBarStride = sizeof(uint64_t);
     const uint32_t v_lo0 = ptx::smem_u32(sm.v[0]) >> 4;
     const uint32_t ones_lo = ptx::smem_u32(sm.ones) >> 4;
-    const uint32_t tO = cx.tmem + kColO + kStrideO * t;
-    const uint32_t tP = cx.tmem + kColP + kStrideP * t;
+    const uint32_t tO = cx.tmem + C::kColO + C::kStrideO * t;
+    const uint32_t tP = cx.tmem + C::kColP + C::kStrideP * t;
     const uint32_t b_pfull = bar(sm.p_full[t]), b_pvdone = bar(sm.pv_done[t]);
     const uint32_t b_kvf0 = bar(sm.kv_full[0]), b_kve0 = bar(sm.kv_empty[0]);
 
@@ -346,10 +398,10 @@ __device__ void pv_role(const KernelCtx &cx, const StdParams &p, int t)
         const bool active = it.valid[t];
         for (int j = lo; j < hi && ok; ++j) {
             const uint32_t idx = kv_base + static_cast<uint32_t>(j - lo);
-            const uint32_t stage = kv_stage(idx);
+            const uint32_t stage = kv_stage<kStages>(idx);
             if (!active || j < lot || j >= hit) {
                 // tile not used by this slot: release it once it has landed
-                ok = warp_wait(b_kvf0 + stage * kBarStride, kv_parity(idx), cx.wc, W_KV_FULL);
+                ok = warp_wait(b_kvf0 + stage * kBarStride, kv_parity<kStages>(idx), cx.wc, W_KV_FULL);
                 if (!ok)
                     break;
                 if (lane == 0)
@@ -364,13 +416,16 @@ __device__ void pv_role(const KernelCtx &cx, const StdParams &p, int t)
             ++pcount;
             ptx::tc_fence_after();
             if (lane == 0) {
-                // O += P [V_j | 1]: V's second 64-column block (of which the
-                // MMA reads 16 columns) is the ones tile, LBO bytes away
+                // D <= 64: O += P [V_j | 1]: V's second swizzle-width column
+                // block (of which the MMA reads 16 columns) is the ones tile,
+                // LBO bytes away.  D = 128: O += P V_j, V's two 64-column
+                // halves one half-tile apart.
                 const uint32_t vlo = v_lo0 + stage * kKVLo;
-                const uint64_t hi_v = umma_desc_hi((ones_lo - vlo) << 4, 1024, kSwizzle128B);
+                const uint32_t lbo = C::kOnes ? (ones_lo - vlo) << 4 : C::kKVHalf;
+                const uint64_t hi_v = umma_desc_hi(lbo, C::kGroupBytes, C::kSwz);
 #pragma unroll
                 for (int kk = 0; kk < kBN / 16; ++kk)
-                    ptx::mma_ts(tO, tP + 8 * kk, hi_v | (vlo + 128 * kk), idesc_pv,
+                    ptx::mma_ts(tO, tP + 8 * kk, hi_v | (vlo + kk * (16 * C::kRowBytes >> 4)), idesc_pv,
                                 (j > lot || kk > 0) ? 1u : 0u);
                 ptx::mma_commit(b_pvdone);
                 ptx::mma_commit(b_kve0 + stage * kBarStride); // this slot is done with tile j
@@ -430,6 +485,7 @@ __device__ __forceinline__ void nb_pass(int t)
 
 // Abort path (named-barrier turns): take and pass every turn of the CTA that
 // remains, from turn k_from of item L on, then (warpgroup 0) the final take.
+template <int kBN>
 __device__ __forceinline__ void drain_turns(const StdParams &p, int t, int64_t L, int k_from)
 {
     for (; L < p.grid.n_items; L += gridDim.x, k_from = 0) {
@@ -450,17 +506,19 @@ __device__ __forceinline__ void drain_turns(const StdParams &p, int t, int64_t L
         nb_take(t);
 }
 
-template <int MOD>
-__device__ void softmax_role(const KernelCtx &cx, const StdParams &p, int t)
+template <int MOD, int D>
+__device__ void softmax_role(const KernelCtx<D> &cx, const StdParams &p, int t)
 {
+    using C = StdCfg<D>;
+    constexpr int kBN = C::kBN;
     constexpr bool kNamed = MOD != MOD_NONE; // how the turn is passed (see above)
-    StdSmem &sm = *cx.sm;
+    StdSmem<D> &sm = *cx.sm;
     const int r = threadIdx.x & 127;             // row of the query tile = TMEM lane
     const uint32_t wq = (threadIdx.x >> 5) & 3;  // warp's quarter of the lanes
     const uint32_t lane_off = (wq * 32u) << 16;
-    const uint32_t tS = cx.tmem + lane_off + kColS + kStrideS * t;
-    const uint32_t tO = cx.tmem + lane_off + kColO + kStrideO * t;
-    const uint32_t tP = cx.tmem + lane_off + kColP + kStrideP * t;
+    const uint32_t tS = cx.tmem + lane_off + C::kColS + C::kStrideS * t;
+    const uint32_t tO = cx.tmem + lane_off + C::kColO + C::kStrideO * t;
+    const uint32_t tP = cx.tmem + lane_off + C::kColP + C::kStrideP * t;
     const uint32_t b_turn_mine = bar(sm.turn[t]), b_turn_other = bar(sm.turn[t ^ 1]);
     uint32_t scount = 0, pvcount = 0, turns = 0;
     int64_t fail_L = 0;
@@ -559,8 +617,11 @@ __device__ void softmax_role(const KernelCtx &cx, const StdParams &p, int t)
                 apply_row_mask<kBN>(x, j0, row_lo, row_hi);
             uint32_t pk[kBN / 2];
             bool rescale;
-            const float alpha = softmax_compute_p_exact_sum<kBN>(
-                x, MOD == MOD_NONE ? p.qk_log2 : 1.f, st, k == 0, pk, rescale);
+            const float alpha =
+                C::kOnes ? softmax_compute_p_exact_sum<kBN>(x, MOD == MOD_NONE ? p.qk_log2 : 1.f, st, k == 0,
+                                                            pk, rescale)
+                         : softmax_compute_p<kBN>(x, MOD == MOD_NONE ? p.qk_log2 : 1.f, st, k == 0, pk,
+                                                  rescale);
             if constexpr (kNamed) {
                 ptx::reg_fence<kBN / 2>(pk);
                 ptx::reg_fence_f<1>(&st.l);
@@ -580,7 +641,7 @@ __device__ void softmax_role(const KernelCtx &cx, const StdParams &p, int t)
                 ++pvcount;
                 ptx::tc_fence_after();
                 if (rescale)
-                    rescale_o<kDvExt>(tO, alpha);
+                    rescale_o<C::kDvExt>(tO, alpha);
             }
             store_p<kBN>(tP, pk);
             ptx::tc_fence_before();
@@ -599,31 +660,41 @@ __device__ void softmax_role(const KernelCtx &cx, const StdParams &p, int t)
         }
         ++pvcount;
         ptx::tc_fence_after();
-        uint32_t o[64], sum[1];
-        ptx::tmem_ld32(tO, o);
-        ptx::tmem_ld32(tO + 32, o + 32);
-        ptx::tmem_ld1(tO + kColSum, sum);
-        ptx::tmem_wait_ld();
-        ptx::reg_fence<32>(o);
-        ptx::reg_fence<32>(o + 32);
-        ptx::reg_fence<1>(sum);
-        const float l_round = __uint_as_float(sum[0]);
-        const float inv = l_round > 0.f ? 1.f / l_round : 0.f;
-        if (i < p.mask.S) {
-            __nv_bfloat16 *dst = p.out + b * p.o_sb + static_cast<int64_t>(i) * p.o_ss + h * p.o_sh;
-            uint4 *d4 = reinterpret_cast<uint4 *>(dst);
-#pragma unroll
-            for (int c = 0; c < 8; ++c) {
-                uint4 w;
-                w.x = ptx::pack_bf16(__uint_as_float(o[8 * c + 0]) * inv, __uint_as_float(o[8 * c + 1]) * inv);
-                w.y = ptx::pack_bf16(__uint_as_float(o[8 * c + 2]) * inv, __uint_as_float(o[8 * c + 3]) * inv);
-                w.z = ptx::pack_bf16(__uint_as_float(o[8 * c + 4]) * inv, __uint_as_float(o[8 * c + 5]) * inv);
-                w.w = ptx::pack_bf16(__uint_as_float(o[8 * c + 6]) * inv, __uint_as_float(o[8 * c + 7]) * inv);
-                d4[c] = w;
-            }
-            if (p.lse)
-                p.lse[b * p.l_sb + h * p.l_sh + i] = row_lse(st);
+        float inv;
+        if constexpr (C::kOnes) {
+            uint32_t sum[1];
+            ptx::tmem_ld1(tO + C::kColSum, sum);
+            ptx::tmem_wait_ld();
+            ptx::reg_fence<1>(sum);
+            const float l_round = __uint_as_float(sum[0]);
+            inv = l_round > 0.f ? 1.f / l_round : 0.f;
+        } else {
+            inv = row_inv_norm(st);
         }
+        // 32 output columns at a time (the TMEM loads are warp-collective, so
+        // every thread takes them; only rows inside the sequence store)
+        uint4 *d4 = reinterpret_cast<uint4 *>(p.out + b * p.o_sb + static_cast<int64_t>(i) * p.o_ss +
+                                              h * p.o_sh);
+#pragma unroll
+        for (int c32 = 0; c32 < D / 32; ++c32) {
+            uint32_t o[32];
+            ptx::tmem_ld32(tO + 32 * c32, o);
+            ptx::tmem_wait_ld();
+            ptx::reg_fence<32>(o);
+            if (i < p.mask.S) {
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    uint4 w;
+                    w.x = ptx::pack_bf16(__uint_as_float(o[8 * c + 0]) * inv, __uint_as_float(o[8 * c + 1]) * inv);
+                    w.y = ptx::pack_bf16(__uint_as_float(o[8 * c + 2]) * inv, __uint_as_float(o[8 * c + 3]) * inv);
+                    w.z = ptx::pack_bf16(__uint_as_float(o[8 * c + 4]) * inv, __uint_as_float(o[8 * c + 5]) * inv);
+                    w.w = ptx::pack_bf16(__uint_as_float(o[8 * c + 6]) * inv, __uint_as_float(o[8 * c + 7]) * inv);
+                    d4[4 * c32 + c] = w;
+                }
+            }
+        }
+        if (i < p.mask.S && p.lse)
+            p.lse[b * p.l_sb + h * p.l_sh + i] = row_lse(st);
         if (p.tile_counts && r == 0)
             p.tile_counts[(static_cast<int64_t>(b) * p.grid.Hq + h) * p.grid.nq + qb] = n_mine;
     }
@@ -633,21 +704,23 @@ __device__ void softmax_role(const KernelCtx &cx, const StdParams &p, int t)
     return;
 aborted:
     // (named-barrier turns only) match the other warpgroup's remaining turns
-    drain_turns(p, t, fail_L, fail_k);
+    drain_turns<kBN>(p, t, fail_L, fail_k);
 }
 
-template <int MOD>
+template <int MOD, int D>
 __global__ void __launch_bounds__(kThreads, 1)
     std_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                    const __grid_constant__ CUtensorMap tm_v, const StdParams p)
 {
+    using C = StdCfg<D>;
+    constexpr int kStages = C::kStages;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t base = ptx::smem_u32(smem_raw);
-    StdSmem *sm = reinterpret_cast<StdSmem *>(smem_raw + ((1024u - (base & 1023u)) & 1023u));
+    StdSmem<D> *sm = reinterpret_cast<StdSmem<D> *>(smem_raw + ((1024u - (base & 1023u)) & 1023u));
     const int warp = threadIdx.x >> 5;
 
     // the ones tile (bf16 1.0 pairs), read by the tensor core through the async proxy
-    for (uint32_t w = threadIdx.x; w < kTileBytes / 4; w += kThreads)
+    for (uint32_t w = threadIdx.x; w < C::kOnesBytes / 4; w += kThreads)
         reinterpret_cast<uint32_t *>(sm->ones)[w] = 0x3F803F80u;
     ptx::fence_proxy_async_smem();
     if (threadIdx.x == 0) {
@@ -689,7 +762,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncthreads();
     ptx::tc_fence_after();
 
-    KernelCtx cx;
+    KernelCtx<D> cx;
     cx.sm = sm;
     cx.tmem = sm->tmem_base;
     cx.wc.abort_flag = &sm->abort_flag;
@@ -701,7 +774,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // runs under both register limits.
     if (warp >= 4) {
         ptx::setmaxnreg_inc<kRegsSoftmax>();
-        softmax_role<MOD>(cx, p, (warp >> 2) - 1);
+        softmax_role<MOD, D>(cx, p, (warp >> 2) - 1);
         ptx::tc_fence_before();
         ptx::named_barrier_sync(1, kThreads);
     } else {
@@ -722,28 +795,44 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 #ifndef __CUDACC_RTC__
-template <int MOD>
+template <int MOD, int D>
 cudaError_t launch_mod(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
                        const StdParams &p, int grid, cudaStream_t stream)
 {
-    const size_t smem = sizeof(StdSmem) + 1024;
+    // the layout plus the worst-case alignment pad within 227 KB per CTA
+    static_assert(sizeof(StdSmem<D>) + 1024 <= 232448, "shared memory per CTA");
+    const size_t smem = sizeof(StdSmem<D>) + 1024;
     static bool configured = false; // benign race: both calls are idempotent
     if (!configured) {
         cudaFuncAttributes attr;
-        cudaError_t e = cudaFuncGetAttributes(&attr, std_fwd_kernel<MOD>);
+        cudaError_t e = cudaFuncGetAttributes(&attr, std_fwd_kernel<MOD, D>);
         if (e != cudaSuccess)
             return e;
         // The setmaxnreg split assumes exactly kRegsLaunch registers at launch.
         if (attr.numRegs != static_cast<int>(kRegsLaunch))
             return cudaErrorInvalidConfiguration;
-        e = cudaFuncSetAttribute(std_fwd_kernel<MOD>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        e = cudaFuncSetAttribute(std_fwd_kernel<MOD, D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  static_cast<int>(smem));
         if (e != cudaSuccess)
             return e;
         configured = true;
     }
-    std_fwd_kernel<MOD><<<grid, kThreads, smem, stream>>>(tq, tk, tv, p);
+    std_fwd_kernel<MOD, D><<<grid, kThreads, smem, stream>>>(tq, tk, tv, p);
     return cudaGetLastError();
+}
+
+template <int D>
+cudaError_t launch_dim(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
+                       const StdParams &p, int grid, cudaStream_t stream)
+{
+    switch (p.score_mod) {
+    case MOD_ALIBI:
+        return launch_mod<MOD_ALIBI, D>(tq, tk, tv, p, grid, stream);
+    case MOD_SOFTCAP:
+        return launch_mod<MOD_SOFTCAP, D>(tq, tk, tv, p, grid, stream);
+    default:
+        return launch_mod<MOD_NONE, D>(tq, tk, tv, p, grid, stream);
+    }
 }
 #endif // !__CUDACC_RTC__
 
@@ -753,17 +842,21 @@ cudaError_t launch_mod(const CUtensorMap &tq, const CUtensorMap &tk, const CUten
 cudaError_t launch_standard(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
                             const StdParams &p, int grid, cudaStream_t stream)
 {
-    switch (p.score_mod) {
-    case MOD_ALIBI:
-        return launch_mod<MOD_ALIBI>(tq, tk, tv, p, grid, stream);
-    case MOD_SOFTCAP:
-        return launch_mod<MOD_SOFTCAP>(tq, tk, tv, p, grid, stream);
+    switch (p.head_dim) {
+    case 32:
+        return launch_dim<32>(tq, tk, tv, p, grid, stream);
+    case 128:
+        return launch_dim<128>(tq, tk, tv, p, grid, stream);
     default:
-        return launch_mod<MOD_NONE>(tq, tk, tv, p, grid, stream);
+        return launch_dim<64>(tq, tk, tv, p, grid, stream);
     }
 }
 
-size_t standard_smem_bytes() { return sizeof(StdSmem) + 1024; }
+size_t standard_smem_bytes(int head_dim)
+{
+    return head_dim == 32 ? sizeof(StdSmem<32>) + 1024
+                          : head_dim == 128 ? sizeof(StdSmem<128>) + 1024 : sizeof(StdSmem<64>) + 1024;
+}
 #endif // !__CUDACC_RTC__
 
 } // namespace fl

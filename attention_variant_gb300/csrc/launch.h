@@ -17,6 +17,7 @@ namespace fl {
 struct StdParams {
     GridSpec grid;
     MaskSpec mask;
+    int head_dim;         // D = Dv: 32, 64 or 128
     int score_mod;
     float qk_log2;        // scale * log2(e)
     float softcap_in;     // 2 * scale * log2(e) / cap
@@ -34,15 +35,16 @@ struct StdParams {
     uint64_t timeout_ns;
 };
 
-// Parameters of the differential-attention kernel (D = 64, Dv = 128).
+// Parameters of the differential-attention kernel (D = 64, Dv = 64 or 128).
 struct DiffParams {
     int B, H, Hk, G, nq;
+    int dv;               // 64 or 128
     int64_t n_items;
     int lpt, group;
     MaskSpec mask;        // none or causal
     float qk_log2;        // scale * log2(e)
     float lambda;
-    __nv_bfloat16 *out;   // [B, S, H, 128]
+    __nv_bfloat16 *out;   // [B, S, H, Dv]
     int64_t o_sb, o_ss, o_sh;
     float *lse;           // [2, B, H, S] or null
     int64_t l_s2, l_sb, l_sh;
@@ -174,16 +176,17 @@ cudaError_t launch_bwd(const CUtensorMap &tq, const CUtensorMap &tdo, const CUte
                        cudaStream_t stream);
 #endif
 
-// Keys per K/V tile of the standard kernel (its TMEM budget: see fwd_standard.cu),
-// its threads per CTA and the registers per thread it must be compiled to.
-constexpr int kStdKeyTile = 112;
+// Keys per K/V tile of the standard kernel for head dimension D (its TMEM
+// budget: see fwd_standard.cu), its threads per CTA and the registers per
+// thread it must be compiled to.
+__host__ __device__ constexpr int std_key_tile(int D) { return D == 128 ? 64 : 112; }
 constexpr int kStdThreads = 384;
 constexpr int kStdRegs = 168;
 
 #ifndef __CUDACC_RTC__
 cudaError_t launch_standard(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
                             const StdParams &p, int grid, cudaStream_t stream);
-size_t standard_smem_bytes();
+size_t standard_smem_bytes(int head_dim);
 
 // ---- score_mod expressions (score_expr.cu)
 // Checks `expr` against the expression grammar of fl_attn.h and writes the

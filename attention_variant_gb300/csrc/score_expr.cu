@@ -494,7 +494,11 @@ std::string backward_source(const std::string &cuda, const std::string &grad)
            expr_function("fl_score_expr_du", grad) + "#include \"bwd_standard.cu\"\n";
 }
 
-const std::vector<std::string> kForwardKernels = {"fl::std_fwd_kernel<3>"}; // MOD_EXPR
+// MOD_EXPR at head dimension D
+std::vector<std::string> forward_kernels(int D)
+{
+    return {"fl::std_fwd_kernel<3, " + std::to_string(D) + ">"};
+}
 const std::vector<std::string> kBackwardKernels = {"fl::bwd_fused_kernel<3>"}; // dK/dV and dQ tiles
 
 // Compiles `src` (which includes the embedded kernel sources) for sm_103a;
@@ -628,7 +632,7 @@ bool score_expr_compile_only(const char *cuda, const char *grad, char *err, size
 {
     std::vector<char> cubin;
     std::vector<std::string> names;
-    return compile(forward_source(cuda), kForwardKernels, cubin, names, err, err_n) &&
+    return compile(forward_source(cuda), forward_kernels(64), cubin, names, err, err_n) &&
            (!grad || compile(backward_source(cuda, grad), kBackwardKernels, cubin, names, err, err_n));
 }
 
@@ -645,17 +649,18 @@ cudaError_t launch_standard_expr(const CUtensorMap &tq, const CUtensorMap &tk, c
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess)
         return e;
-    const size_t smem = standard_smem_bytes();
+    const size_t smem = standard_smem_bytes(p.head_dim);
+    const std::string key = std::to_string(p.head_dim) + ":" + cuda;
     CUfunction fn = nullptr;
     {
         std::lock_guard<std::mutex> lock(g_mutex);
-        auto it = g_kernels.find({dev, cuda});
+        auto it = g_kernels.find({dev, key});
         if (it != g_kernels.end()) {
             fn = it->second;
         } else {
             std::vector<char> cubin;
             std::vector<std::string> names;
-            if (!compile(forward_source(cuda), kForwardKernels, cubin, names, err, err_n))
+            if (!compile(forward_source(cuda), forward_kernels(p.head_dim), cubin, names, err, err_n))
                 return cudaErrorInvalidSource;
             // the runtime has made the device's primary context current
             if ((e = cudaFree(nullptr)) != cudaSuccess)
@@ -675,7 +680,7 @@ cudaError_t launch_standard_expr(const CUtensorMap &tq, const CUtensorMap &tk, c
                 put(err, err_n, "setting the kernel's shared-memory size failed");
                 return cudaErrorInvalidConfiguration;
             }
-            g_kernels[{dev, cuda}] = fn;
+            g_kernels[{dev, key}] = fn;
         }
     }
     void *args[] = {const_cast<CUtensorMap *>(&tq), const_cast<CUtensorMap *>(&tk),

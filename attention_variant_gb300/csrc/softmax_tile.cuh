@@ -181,8 +181,9 @@ __device__ __forceinline__ void online_update_and_store_p(float (&x)[BN], float 
 //                      and both sums; O is not touched;
 //   rescale_o + store_p: once the previous P V has completed.
 // Returns the O rescale factor (1 when no rescale is needed for this warp).
-__device__ __forceinline__ float softmax_compute_p(float (&x)[BN], float c, RowState &st,
-                                                   bool first, uint32_t (&pk)[BN / 2],
+template <int N = BN>
+__device__ __forceinline__ float softmax_compute_p(float (&x)[N], float c, RowState &st,
+                                                   bool first, uint32_t (&pk)[N / 2],
                                                    bool &rescale)
 {
     float mc[4];
@@ -190,7 +191,7 @@ __device__ __forceinline__ float softmax_compute_p(float (&x)[BN], float c, RowS
     for (int q = 0; q < 4; ++q)
         mc[q] = fmaxf(x[2 * q], x[2 * q + 1]);
 #pragma unroll
-    for (int e = 8; e < BN; e += 8) {
+    for (int e = 8; e < N; e += 8) {
 #pragma unroll
         for (int q = 0; q < 4; ++q)
             mc[q] = ptx::max3(mc[q], x[e + 2 * q], x[e + 2 * q + 1]);
@@ -215,7 +216,7 @@ __device__ __forceinline__ float softmax_compute_p(float (&x)[BN], float c, RowS
     float le[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
     float lr[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-    for (int e = 0; e < BN / 2; ++e) {
+    for (int e = 0; e < N / 2; ++e) {
         float a0, a1;
         ptx::fma2(a0, a1, x[2 * e], x[2 * e + 1], c, c, nmu, nmu);
         const float p0 = ptx::ex2(a0);

@@ -89,8 +89,9 @@ def unmasked_pairs(mask, B, H, S, window=0, prefix=0, doc=None):
     return total
 
 
-def entry(kind, S, variant):
-    """One benchmark entry of the MHA sweep ("mha") or GQA mask sweep ("gqa")."""
+def entry(kind, S, variant, D=workloads.HEAD_DIM):
+    """One benchmark entry of the MHA sweep ("mha") or GQA mask sweep ("gqa");
+    D other than the sweep's 64 names a head-dimension variant of its shape."""
     if kind == "mha":
         w = workloads.mha_workload(S)
         B, Hq, Hk = w["B"], w["H"], w["H"]
@@ -98,7 +99,8 @@ def entry(kind, S, variant):
         B = dict(workloads.GQA_SHAPES)[S]
         w = workloads.gqa_workload(S, B)
         Hq, Hk = w["Hq"], w["Hk"]
-    D = workloads.HEAD_DIM
+    if D != workloads.HEAD_DIM:
+        w = dict(w, name=f"{w['name']}_d{D}")
     mod = {"vanilla": "none", "alibi": "alibi", "softcap": "softcap"}.get(variant, "none")
     mask = variant if variant in ("causal", "window", "prefix", "doc") else "none"
     kw = {}
@@ -130,12 +132,14 @@ def expr_entry(S, name):
     return e
 
 
-def diff_entry(mask):
+def diff_entry(mask, Dv=None):
     w = workloads.DIFF
-    B, S, H, D, Dv = w["B"], w["S"], w["H"], w["D"], w["Dv"]
+    B, S, H, D = w["B"], w["S"], w["H"], w["D"]
+    Dv = Dv or w["Dv"]
+    name = w["name"] if Dv == w["Dv"] else f"{w['name']}_dv{Dv}"
     pairs = unmasked_pairs(mask, B, H, S)
     # per pair: two Q K^T (2 D each) and two P V (2 Dv each)
-    return dict(name=w["name"], kind="diff", B=B, S=S, H=H, D=D, Dv=Dv, mask=mask,
+    return dict(name=name, kind="diff", B=B, S=S, H=H, D=D, Dv=Dv, mask=mask,
                 variant="causal" if mask == "causal" else "non-causal", pairs=pairs,
                 flops=pairs * (2 * 2 * D + 2 * 2 * Dv),
                 bytes=2 * (2 * 2 * B * S * H * D + B * S * H * Dv + B * S * H * Dv) + 4 * 2 * B * H * S)
@@ -220,6 +224,11 @@ def decode_entry(mod):
                 mod=mod, B=B, Sq=Sq, Hq=Hq, Hk=Hk, D=D, lens=lens, page=w["page"],
                 flops=4 * D * Sq * Hq * keys,
                 bytes=2 * 2 * keys * Hk * D + 2 * 2 * B * Sq * Hq * D + 4 * B * Hq * Sq)
+
+
+def head_dim_entries():
+    """The MHA S = 2048 shape at head dimensions 32 and 128."""
+    return [entry("mha", 2048, v, D=D) for D in (32, 128) for v in ("vanilla", "causal")]
 
 
 def all_entries():
@@ -625,6 +634,8 @@ ONLY = {"diff": lambda: diff_entry("none"), "diff_causal": lambda: diff_entry("c
         "evo_row": lambda: evo_entry(True), "evo_col": lambda: evo_entry(False),
         "decode": lambda: decode_entry("none"), "decode_softcap": lambda: decode_entry("softcap"),
         "vanilla": lambda: entry("mha", 2048, "vanilla"), "causal": lambda: entry("mha", 2048, "causal"),
+        "d128": lambda: entry("mha", 2048, "vanilla", D=128), "d32": lambda: entry("mha", 2048, "vanilla", D=32),
+        "diff_dv64": lambda: diff_entry("none", Dv=64),
         "softcap": lambda: entry("mha", 2048, "softcap"), "alibi": lambda: entry("mha", 2048, "alibi"),
         "s512_vanilla": lambda: entry("mha", 512, "vanilla"), "s512_causal": lambda: entry("mha", 512, "causal"),
         "gqa16k_window": lambda: entry("gqa", 16384, "window"), "gqa16k_doc": lambda: entry("gqa", 16384, "doc"),
@@ -704,7 +715,8 @@ def run_ours(args):
 
     variants = {}
     if not args.headline_only:
-        for e in [diff_entry("none"), diff_entry("causal"), evo_entry(True), evo_entry(False)]:
+        for e in [diff_entry("none"), diff_entry("causal"), diff_entry("none", Dv=64), evo_entry(True),
+                  evo_entry(False)]:
             vms = time_other(e, torch, fa, device, args.variant_steps, 2, flush, stream)
             vm = statistics.mean(vms)
             tf = e["flops"] / (vm * 1e-3) / 1e12
@@ -735,7 +747,7 @@ def run_ours(args):
             variants[f"{e['name']}/{e['variant']}"] = dict(
                 tflops=round(e["flops"] / (vm * 1e-3) / 1e12, 1), ms=round(vm, 4), gbs=round(gbs, 1),
                 frac_hbm=round(gbs / peaks["hbm_gbs"], 4), l2=l2_policy(e))
-        for e in all_entries() + [expr_entry(head["S"], n) for n in EXPR_VARIANTS]:
+        for e in all_entries() + [expr_entry(head["S"], n) for n in EXPR_VARIANTS] + head_dim_entries():
             h = gpu_inputs(e, torch, device) if (e["S"], e["kind"]) != (head["S"], "mha") else host
             vms, _ = time_entry(e, h, torch, fa, device, args.variant_steps, 2, flush, stream)
             vm = statistics.mean(vms)

@@ -152,7 +152,8 @@ typedef struct {
     int32_t *debug_tile_counts; /* NULL, or device int32 [batch][heads][ceil(S/128)]: the
                                    number of key tiles each 128-row query block visited
                                    (key-tile width from fl_attn_tile_shape: 112 for the
-                                   standard kind, 128 for the others) */
+                                   standard kind at D = 32 and 64, 64 at D = 128, 128 for
+                                   the other kinds) */
     uint32_t *error_word;    /* NULL, or a device word the kernel ORs FL_DEVERR_* into */
     int32_t debug_inject;    /* fl_inject; 0 in normal use */
     uint32_t wait_timeout_us; /* bound of every device-side wait; 0 means 2,000,000 */
@@ -178,9 +179,9 @@ typedef struct {
  *                     lse [N_res,H,N_seq] or NULL.
  * lse is natural-log; its innermost stride must be 1.
  *
- * Supported shapes: STANDARD D = Dv = 64; DIFF D = 64, Dv = 128 with mask
- * none or causal; EVO c = 32, and for FL_KIND_EVO_ROW N_res <= 384 (the bias
- * rows of a query block are kept in shared memory).  Other shapes return
+ * Supported shapes: STANDARD D = Dv in {32, 64, 128}; DIFF D = 64, Dv = 64
+ * or 128 with mask none or causal; EVO c = 32, and for FL_KIND_EVO_ROW
+ * N_res <= 384 (the bias rows of a query block are kept in shared memory).  Other shapes return
  * FL_ERR_UNSUPPORTED.  The bias may be passed with any strides obeying the
  * fl_tensor rules (for example a [N_res,N_res,H] tensor viewed as
  * [H,N_res,N_res]).  Evoformer sequence lengths must keep every stride a

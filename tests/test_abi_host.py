@@ -74,8 +74,10 @@ def test_validation_before_device(lib):
     assert _call(lib, odd, good(), good(), good()) == fa.FL_ERR_ALIGNMENT
     notinner = _t((B, S, H, D), strides=(S * H * D, H * D, D, 2))
     assert _call(lib, notinner, good(), good(), good()) == fa.FL_ERR_INVALID_ARG
-    assert _call(lib, _t((B, S, H, 128)), _t((B, S, H, 128)), _t((B, S, H, 128)),
-                 _t((B, S, H, 128))) == fa.FL_ERR_UNSUPPORTED
+    assert _call(lib, _t((B, S, H, 96)), _t((B, S, H, 96)), _t((B, S, H, 96)),
+                 _t((B, S, H, 96))) == fa.FL_ERR_UNSUPPORTED  # head dimension
+    assert _call(lib, _t((B, S, H, 64)), _t((B, S, H, 64)), _t((B, S, H, 128)),
+                 _t((B, S, H, 128))) == fa.FL_ERR_UNSUPPORTED  # D != Dv
     # 2^31 work items or more (the kernel decodes item indices in 32 bits):
     # 2^20 batches x 16 heads x 256 pairs of query blocks
     huge = lambda: _t((1 << 20, 1 << 16, 16, D))
@@ -107,6 +109,8 @@ def test_size_one_axes_take_any_stride(lib):
 
 def test_tile_shape(lib):
     assert fa.fl_attn_tile_shape(fa.make_desc(), 64) == (128, 112)
+    assert fa.fl_attn_tile_shape(fa.make_desc(), 32) == (128, 112)
+    assert fa.fl_attn_tile_shape(fa.make_desc(), 128) == (128, 64)
     assert fa.fl_attn_tile_shape(fa.make_desc(kind="diff"), 64) == (128, 128)
     assert fa.fl_attn_tile_shape(fa.make_desc(kind="evo_row"), 32) == (128, 128)
     with pytest.raises(fa.FlAttnError):

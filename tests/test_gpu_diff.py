@@ -59,6 +59,33 @@ def test_diff_small(S, mask):
     assert np.array_equal(cnt, exp)
 
 
+@pytest.mark.parametrize("mask", ["none", "causal"])
+def test_diff_dv64(mask):
+    # value head dimension 64 (one 64-column V half per key tile); 333 rows
+    # leave a ragged last tile
+    q, k, v = _inputs("diffdv64", 2, 333, 3, Dv=64)
+    o, lse, cnt, err = run_diff(q, k, v, 0.8, mask)
+    assert err == 0
+    oref, lref = oracle.diff_attention(q, k, v, 0.8, mask=mask)
+    gu.compare(o, lse, oref, lref, what=f"diff dv64 {mask}")
+    assert np.array_equal(cnt, gu.expected_tile_counts(mask, 2, 3, 333))
+
+
+def test_diff_dv64_full_size():
+    """The differential workload's shape (B 4, S 4096, H 16) with Dv = 64,
+    causal, rows at both ends of every query block against the oracle."""
+    w = workloads.DIFF
+    q, k, v = _inputs(w["name"] + "_dv64", w["B"], w["S"], w["H"], Dv=64)
+    o, lse, cnt, err = run_diff(q, k, v, w["lam"], "causal")
+    assert err == 0
+    rows = gu.block_edge_rows(w["B"], w["H"], w["S"], n_random=64, seed=3)
+    oref, lref = oracle.diff_attention(q, k, v, w["lam"], mask="causal", rows=rows)
+    o_s = np.stack([o[b, i, h] for b, h, i in rows])
+    l_s = np.stack([[lse[s, b, h, i] for b, h, i in rows] for s in range(2)])
+    gu.compare(o_s, l_s, oref, lref, what="diff dv64 full causal")
+    assert np.array_equal(cnt, gu.expected_tile_counts("causal", w["B"], w["H"], w["S"]))
+
+
 def test_diff_gqa_and_lambda_zero():
     q, k, v = _inputs("diffgqa", 1, 300, 4, 2)
     o, lse, _, _ = run_diff(q, k, v, 0.0, "causal")

