@@ -529,8 +529,8 @@ fl_status fwd_evo(bool row_pass, const fl_tensor *q, const fl_tensor *k, const f
         return fail(FL_ERR_UNSUPPORTED, "the Evoformer kinds take no mask and no score_mod");
     if (!std::isfinite(d->scale) || d->scale < 0.f)
         return fail(FL_ERR_INVALID_ARG, "scale must be finite and positive (0 selects 1/sqrt(c))");
-    if (C != 32)
-        return fail(FL_ERR_UNSUPPORTED, "the Evoformer kinds support c = 32 (got %lld)", (long long)C);
+    if (C != 32 && C != 64)
+        return fail(FL_ERR_UNSUPPORTED, "the Evoformer kinds support c = 32 or 64 (got %lld)", (long long)C);
 
     int dev;
     DeviceInfo info;
@@ -539,7 +539,8 @@ fl_status fwd_evo(bool row_pass, const fl_tensor *q, const fl_tensor *k, const f
     // [batch, sequence, head, c] view: which tensor axis plays batch and sequence
     const int ab = row_pass ? 0 : 1, ai = row_pass ? 1 : 0;
     CUtensorMap tq, tk, tv;
-    const uint32_t box[4] = {32, 128, 1, 1};
+    const uint32_t box[4] = {uint32_t(C), 128, 1, 1};
+    const CUtensorMapSwizzle swz = C == 32 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_128B;
     const View *src[3] = {&Q, &K, &V};
     CUtensorMap *dst[3] = {&tq, &tk, &tv};
     const char *names[3] = {"q", "k", "v"};
@@ -548,16 +549,15 @@ fl_status fwd_evo(bool row_pass, const fl_tensor *q, const fl_tensor *k, const f
         const uint64_t dims[4] = {uint64_t(C), uint64_t(S), uint64_t(H), uint64_t(B)};
         const uint64_t st[3] = {uint64_t(T.stride[ai]) * 2, uint64_t(T.stride[2]) * 2,
                                 uint64_t(T.stride[ab]) * 2};
-        if ((s = make_map(*dst[m], T.ptr, 4, dims, st, box, CU_TENSOR_MAP_SWIZZLE_64B, names[m])) != FL_OK)
+        if ((s = make_map(*dst[m], T.ptr, 4, dims, st, box, swz, names[m])) != FL_OK)
             return s;
     }
     CUtensorMap tb;
     std::memset(&tb, 0, sizeof tb);
     if (row_pass) {
-        if (Nr > fl::evo_max_bias_keys())
-            return fail(FL_ERR_UNSUPPORTED, "the row pass keeps the bias rows of a query block in "
-                        "shared memory: N_res <= %d", fl::evo_max_bias_keys());
-        // bias[stack, h, i, j] as (j, i, h, stack); boxes of 64 keys x 128 query rows
+        // bias[stack, h, i, j] as (j, i, h, stack); boxes of 64 keys x 128 query
+        // rows (kept for a whole work item, or streamed per key tile when
+        // N_res > 384 or c = 64)
         const uint64_t stacks = bias_rows > 0 ? uint64_t(Ns / bias_rows) : 1;
         const uint64_t dims[4] = {uint64_t(Nr), uint64_t(Nr), uint64_t(H), stacks};
         const uint64_t st[3] = {uint64_t(Bz.stride[1]) * 2, uint64_t(Bz.stride[0]) * 2,
@@ -568,6 +568,7 @@ fl_status fwd_evo(bool row_pass, const fl_tensor *q, const fl_tensor *k, const f
             return s;
     }
     fl::EvoParams p{};
+    p.head_dim = int(C);
     const int nq = int((S + fl::BM - 1) / fl::BM);
     p.grid.B = int(B);
     p.grid.Hq = int(H);
@@ -1242,7 +1243,7 @@ fl_status fl_attn_tile_shape(const fl_attn_variant_desc *desc, int32_t head_dim,
         break;
     case FL_KIND_EVO_ROW:
     case FL_KIND_EVO_COL:
-        if (head_dim != 32)
+        if (head_dim != 32 && head_dim != 64)
             return fail(FL_ERR_UNSUPPORTED, "head_dim %d not supported for kind %d", head_dim,
                         desc->kind);
         break;

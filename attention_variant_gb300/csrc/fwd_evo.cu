@@ -1,11 +1,12 @@
-// fwd_evo.cu -- Evoformer MSA gated self-attention forward, c = 32 per head:
+// fwd_evo.cu -- Evoformer MSA gated self-attention forward, c = 32 or 64 per head:
 //     O = sigmoid(g) * softmax(scale q k^T + b) v
 // row-wise (attention over residues for each MSA row, pair bias b[h, i, j]
 // shared by every MSA row) and column-wise (attention over MSA rows for each
 // residue, no bias).  The pages evaluate both as complex variants template
 // systems cannot express (talk notes, "Evaluation: complex variants" and
-// "End-to-end: AlphaFold2": Evoformer with 8 heads of dimension 32); here the
-// gate is fused into the epilogue and the bias into the online softmax.
+// "End-to-end: AlphaFold2": Evoformer with 8 heads of dimension 32; the
+// kernel benchmark with 4 heads of dimension 64); here the gate is fused into
+// the epilogue and the bias into the online softmax.
 //
 // Both passes run over a [batch, sequence, head, c] view: the row pass takes
 // batch = MSA row and sequence = residue, the column pass the reverse (the
@@ -13,33 +14,44 @@
 //
 // Work item = (head h, query block qb, a chunk of batch indices).  The CTA's
 // two slots take alternate batch indices of the chunk; a slot's "steps" are
-// its (batch index, key tile) pairs in order.  In the row pass the bias rows
-// of (h, qb) are loaded once per item into shared memory (128 rows x up to
-// 384 keys) and read by every MSA row of the chunk: the pair-bias tile is
-// reused across MSA rows instead of being re-read from L2 for each of them.
+// its (batch index, key tile) pairs in order, and the two slots' steps are
+// interleaved (step s of slot 0, then of slot 1) in one K/V ring.  The pair
+// bias of (h, qb) is the same for every MSA row of the chunk:
+//   BIAS_RESIDENT (c = 32, N_res <= 384): its 128 rows x N_res keys are
+//     loaded once per item into shared memory and read by every MSA row;
+//   BIAS_STREAM (N_res > 384, or c = 64 whose K/V tiles leave no room): the
+//     128 x 128 bias tile of each step is loaded into a two-stage ring shared
+//     by both slots (both slots are at the same key tile in a step).
 //
-// Warps: 0 TMA producer for both slots (Q double-buffered per slot, K/V
-// through one ring per slot, and the bias), 1 issues S = Q K^T for both slots
-// (TMEM owner), 2 and 3 issue O += P V for slot 0 and slot 1, 4-7 softmax of
-// slot 0, 8-11 softmax of slot 1.  The producer and the S warp walk the steps
-// of both slots interleaved (step s of slot 0, then of slot 1), the order in
-// which the slots consume them.  Q K^T and P V are issued by different warps
-// because a tcgen05.mma returns to its issuing thread only once the tensor
-// core has accepted it: one thread issuing both chains of a slot spends most
-// of a tile blocked in issue.
-
-// TMEM per slot t: S[t] fp32 at 128 t; O[t] at 256 + 64 t with 48 columns:
-// 32 output columns and 16 columns of sum_j P_j (P V multiplies P by V
-// extended with a tile of ones, so the tensor core also sums the exact bf16 P
-// it used: the normaliser of O); P[t] bf16 pairs at 384 + 64 t.
+// Warps: 0 TMA producer, 1 issues S = Q K^T for both slots (TMEM owner), 2
+// and 3 issue O += P V for slot 0 and slot 1, 4-11 softmax of slot 0, 12-19
+// softmax of slot 1.  Q K^T and P V are issued by different warps because a
+// tcgen05.mma returns to its issuing thread only once the tensor core has
+// accepted it.
 //
-// Per slot and key tile j: softmax waits s_full, copies S out of TMEM and
-// arrives s_free (the MMA warp then issues the next Q K^T at once), computes P
-// in registers, waits pv_done (the previous P V), rescales O if the reference
-// max moved, writes P, arrives p_full (the MMA warp then issues P V).  The
-// epilogue of one batch index (O / sum, times the prefetched gate) runs inside
-// the first key tile of the slot's next batch index, where the latency of the
-// last P V is hidden behind the exponentials.
+// Softmax: two threads per query row.  Each of a slot's eight softmax warps
+// owns 16 TMEM lanes (query rows) and reads a 128-key score tile through the
+// 16-lane TMEM shapes: thread t holds rows t/4 and t/4 + 8 of its 16 and, of
+// every 8-key group, keys 2 (t % 4) and 2 (t % 4) + 1 -- 32 keys of each of
+// two rows.  A row's max and sums are combined across the four threads of a
+// quad by two shuffles.  Twice as many softmax warps as one thread per row
+// would allow (16 instead of 8) keep the per-score instruction chain
+// (bias, max, exponent, pack) issuing: with one thread per row a step was
+// latency-bound at about half the issue rate.
+//
+// TMEM per slot t: S[t] fp32 at 128 t; O[t] at 256 + 64 t (c = 32: 32 output
+// columns and 16 columns of sum_j P_j -- P V multiplies P by V extended with a
+// tile of ones, so the tensor core also sums the exact bf16 P it used, the
+// normaliser of O; c = 64: 64 output columns, the sum of the rounded P kept
+// in registers); P[t] bf16 pairs at 384 + 64 t.
+//
+// Per slot and key tile j: the softmax waits s_full, copies S out of TMEM and
+// arrives s_free (the S warp then issues the next Q K^T), adds the bias,
+// computes P in registers, waits pv_done (the previous P V), rescales O if a
+// row's reference max moved, writes P, arrives p_full (the P V warp then
+// issues P V).  The epilogue of one batch index (O / sum, times sigmoid of
+// the gate) runs inside the first key tile of the slot's next batch index,
+// where the latency of the last P V is hidden behind the exponentials.
 #include <cuda_bf16.h>
 #include <cstdint>
 
@@ -50,47 +62,63 @@
 namespace fl {
 namespace {
 
-constexpr int kThreads = 384;
-constexpr uint32_t kRegsLaunch = 168;
-constexpr uint32_t kRegsSoftmax = 200;
-constexpr uint32_t kRegsOther = 104;
-static_assert(2 * 128 * kRegsSoftmax + 128 * kRegsOther == kThreads * kRegsLaunch,
+constexpr int kThreads = 640;
+constexpr uint32_t kRegsLaunch = 96;
+constexpr uint32_t kRegsSoftmax = 104;
+constexpr uint32_t kRegsOther = 64;
+static_assert(16 * 32 * kRegsSoftmax + 4 * 32 * kRegsOther == kThreads * kRegsLaunch,
               "register split must equal the launch allocation");
-constexpr uint32_t kTile = BM * 32 * 2;       // one 128 x 32 bf16 tile (8 KB)
-constexpr uint32_t kBiasBox = BM * 64 * 2;    // 128 rows x 64 keys of bias (16 KB)
-constexpr int kMaxBiasBoxes = 6;              // resident bias covers up to 384 keys
+
+enum : int { BIAS_NONE = 0, BIAS_RESIDENT = 1, BIAS_STREAM = 2 };
+
+constexpr uint32_t kBiasBox = BM * 64 * 2; // 128 query rows x 64 keys of bias (16 KB)
+constexpr int kMaxBiasBoxes = 6;           // resident bias: up to 384 keys
+constexpr int kBiasStages = 2;             // streamed bias: 128-key tiles in flight
 constexpr uint32_t kColS = 0, kColO = 256, kColP = 384;
-constexpr uint32_t kDvExt = 48;               // 32 output columns + 16 sum columns
-constexpr uint32_t kColSum = 32;
+constexpr uint32_t kSmemLimit = 232448;    // 227 KB per CTA
 
-
-template <bool BIAS>
+template <int C, int BIAS>
 struct EvoCfg {
-    static constexpr int kStages = BIAS ? 2 : 4; // K/V ring depth per slot
+    static_assert(C == 32 || C == 64, "head dimension");
+    static constexpr uint32_t kRowBytes = C * 2; // one swizzle row: 64 or 128 bytes
+    static constexpr uint32_t kSwz = C == 32 ? kSwizzle64B : kSwizzle128B;
+    static constexpr uint32_t kTile = BM * kRowBytes; // one 128 x c bf16 tile
+    static constexpr bool kOnes = C == 32;            // normaliser from the ones columns
+    static constexpr uint32_t kDvExt = kOnes ? C + 16 : C;
+    static constexpr uint32_t kBiasBytes =
+        BIAS == BIAS_RESIDENT ? kMaxBiasBoxes * kBiasBox : BIAS == BIAS_STREAM ? kBiasStages * 2 * kBiasBox : 1024;
+    static constexpr uint32_t kOnesBytes = kOnes ? kTile : 1024;
+    // Q (two slots, double-buffered), bias, ones, barriers and alignment pad
+    static constexpr uint32_t kFixed = 4 * kTile + kBiasBytes + kOnesBytes + 2048;
+    static constexpr int kStagesFit = int((kSmemLimit - kFixed) / (2 * kTile));
+    static constexpr int kStages = kStagesFit > 8 ? 8 : kStagesFit; // K/V ring shared by both slots
+    static_assert(kStages >= 3, "K/V ring");
 };
 
-template <bool BIAS>
+template <int C, int BIAS>
 struct __align__(1024) EvoSmem {
-    static constexpr int NS = EvoCfg<BIAS>::kStages;
-    uint8_t bias[BIAS ? kMaxBiasBoxes : 1][BIAS ? kBiasBox : 1024];
-    uint8_t q[2][2][kTile];         // [slot][Q buffer]
-    uint8_t k[2][NS][kTile];        // [slot][stage]
-    uint8_t v[2][NS][kTile];
-    uint8_t ones[kTile];            // bf16 1.0 everywhere: the extra columns of V; it must
-                                    // follow every V stage (the descriptor offset is unsigned)
+    using Cfg = EvoCfg<C, BIAS>;
+    static constexpr int NS = Cfg::kStages;
+    static constexpr int NB = BIAS == BIAS_STREAM ? kBiasStages : 1;
+    uint8_t bias[Cfg::kBiasBytes];
+    uint8_t q[2][2][Cfg::kTile];     // [slot][Q buffer]
+    uint8_t k[NS][Cfg::kTile];
+    uint8_t v[NS][Cfg::kTile];
+    uint8_t ones[Cfg::kOnesBytes];   // bf16 1.0 everywhere: the extra columns of V (c = 32); it
+                                     // must follow every V stage (the descriptor offset is unsigned)
     uint64_t q_full[2][2], q_empty[2][2];
-    uint64_t kv_full[2][NS], kv_empty[2][NS];
+    uint64_t kv_full[NS], kv_empty[NS];
     uint64_t s_full[2], s_free[2], p_full[2], pv_done[2], o_final[2], s_final;
-    uint64_t bias_full, bias_empty;
+    uint64_t bias_full[NB], bias_empty[NB];
     uint32_t tmem_base;
     uint32_t abort_flag;
 };
 
 __device__ uint32_t g_lib_error_word;
 
-template <bool BIAS>
+template <int C, int BIAS>
 struct Ctx {
-    EvoSmem<BIAS> *sm;
+    EvoSmem<C, BIAS> *sm;
     uint32_t tmem;
     WaitCtl wc;
 };
@@ -121,31 +149,33 @@ __device__ __forceinline__ int slot_rows(const EvoItem &it, int t)
 }
 
 // ------------------------------------------------------------------ producer
-template <bool BIAS>
-__device__ void producer_role(const Ctx<BIAS> &cx, const EvoParams &p, const CUtensorMap *tm_q,
+template <int C, int BIAS>
+__device__ void producer_role(const Ctx<C, BIAS> &cx, const EvoParams &p, const CUtensorMap *tm_q,
                               const CUtensorMap *tm_k, const CUtensorMap *tm_v,
                               const CUtensorMap *tm_b)
 {
-    constexpr int NS = EvoCfg<BIAS>::kStages;
-    EvoSmem<BIAS> &sm = *cx.sm;
+    using Cfg = EvoCfg<C, BIAS>;
+    constexpr int NS = Cfg::kStages;
+    EvoSmem<C, BIAS> &sm = *cx.sm;
     const uint32_t lane = ptx::lane_id();
     const int nkv = (p.mask.S + BN - 1) / BN;
     const int nbox = (p.mask.S + 63) / 64;
-    uint32_t kv_count[2] = {0u, 0u}, q_count[2] = {0u, 0u}, item_count = 0;
+    uint32_t kv_count = 0, q_count[2] = {0u, 0u}, item_count = 0, bias_count = 0;
     bool ok = true;
     for (int64_t L = blockIdx.x; L < p.n_items && ok; L += gridDim.x, ++item_count) {
         const EvoItem it = decode_evo(p, L);
-        if (BIAS) {
+        const int stack = p.bias_rows ? it.b0 / p.bias_rows : 0;
+        if constexpr (BIAS == BIAS_RESIDENT) {
             if (item_count > 0) {
-                ok = warp_wait(bar(sm.bias_empty), (item_count - 1) & 1, cx.wc, W_BIAS);
+                ok = warp_wait(bar(sm.bias_empty[0]), (item_count - 1) & 1, cx.wc, W_BIAS);
                 if (!ok)
                     break;
             }
             if (lane == 0) {
-                ptx::mbar_arrive_expect_tx(bar(sm.bias_full), nbox * kBiasBox);
+                ptx::mbar_arrive_expect_tx(bar(sm.bias_full[0]), nbox * kBiasBox);
                 for (int jb = 0; jb < nbox; ++jb)
-                    ptx::tma_load_4d(ptx::smem_u32(sm.bias[jb]), tm_b, bar(sm.bias_full), 64 * jb,
-                                     it.qb * BM, it.h, p.bias_rows ? it.b0 / p.bias_rows : 0);
+                    ptx::tma_load_4d(ptx::smem_u32(sm.bias) + jb * kBiasBox, tm_b, bar(sm.bias_full[0]),
+                                     64 * jb, it.qb * BM, it.h, stack);
             }
             __syncwarp();
         }
@@ -153,6 +183,21 @@ __device__ void producer_role(const Ctx<BIAS> &cx, const EvoParams &p, const CUt
         const int n_steps = max(steps[0], steps[1]);
         for (int st = 0; st < n_steps && ok; ++st) {
             const int j = st % nkv;
+            if constexpr (BIAS == BIAS_STREAM) {
+                // this step's 128 x 128 bias tile, for both slots
+                const uint32_t bs = bias_count % kBiasStages;
+                ok = warp_wait(bar(sm.bias_empty[bs]), ((bias_count / kBiasStages) & 1) ^ 1, cx.wc, W_BIAS);
+                if (!ok)
+                    break;
+                if (lane == 0) {
+                    ptx::mbar_arrive_expect_tx(bar(sm.bias_full[bs]), 2 * kBiasBox);
+                    for (int jb = 0; jb < 2; ++jb)
+                        ptx::tma_load_4d(ptx::smem_u32(sm.bias) + (2 * bs + jb) * kBiasBox, tm_b,
+                                         bar(sm.bias_full[bs]), 128 * j + 64 * jb, it.qb * BM, it.h, stack);
+                }
+                __syncwarp();
+                ++bias_count;
+            }
 #pragma unroll
             for (int t = 0; t < 2; ++t) {
                 if (st >= steps[t])
@@ -167,61 +212,64 @@ __device__ void producer_role(const Ctx<BIAS> &cx, const EvoParams &p, const CUt
                             break;
                     }
                     if (lane == 0) {
-                        ptx::mbar_arrive_expect_tx(bar(sm.q_full[t][qbuf]), kTile);
+                        ptx::mbar_arrive_expect_tx(bar(sm.q_full[t][qbuf]), Cfg::kTile);
                         ptx::tma_load_4d(ptx::smem_u32(sm.q[t][qbuf]), tm_q, bar(sm.q_full[t][qbuf]), 0,
                                          it.qb * BM, it.h, b);
                     }
                     __syncwarp();
                     ++q_count[t];
                 }
-                const uint32_t stage = kv_count[t] % NS;
-                ok = warp_wait(bar(sm.kv_empty[t][stage]), ((kv_count[t] / NS) & 1) ^ 1, cx.wc,
-                               W_KV_EMPTY);
+                const uint32_t stage = kv_count % NS;
+                ok = warp_wait(bar(sm.kv_empty[stage]), ((kv_count / NS) & 1) ^ 1, cx.wc, W_KV_EMPTY);
                 if (!ok)
                     break;
                 if (lane == 0) {
-                    ptx::mbar_arrive_expect_tx(bar(sm.kv_full[t][stage]), 2 * kTile);
-                    ptx::tma_load_4d(ptx::smem_u32(sm.k[t][stage]), tm_k, bar(sm.kv_full[t][stage]), 0,
-                                     j * BN, it.h, b);
-                    ptx::tma_load_4d(ptx::smem_u32(sm.v[t][stage]), tm_v, bar(sm.kv_full[t][stage]), 0,
-                                     j * BN, it.h, b);
+                    ptx::mbar_arrive_expect_tx(bar(sm.kv_full[stage]), 2 * Cfg::kTile);
+                    ptx::tma_load_4d(ptx::smem_u32(sm.k[stage]), tm_k, bar(sm.kv_full[stage]), 0, j * BN,
+                                     it.h, b);
+                    ptx::tma_load_4d(ptx::smem_u32(sm.v[stage]), tm_v, bar(sm.kv_full[stage]), 0, j * BN,
+                                     it.h, b);
                 }
                 __syncwarp();
-                ++kv_count[t];
+                ++kv_count;
             }
         }
     }
     if (!ok) {
         // wait (bounded, ignoring the abort) for this warp's own loads in flight
+        const uint32_t first = kv_count > NS ? kv_count - NS : 0;
+        for (uint32_t idx = first; idx < kv_count; ++idx)
+            mbar_wait_drain(bar(sm.kv_full[idx % NS]), (idx / NS) & 1, cx.wc, W_DRAIN);
 #pragma unroll
-        for (int t = 0; t < 2; ++t) {
-            const uint32_t first = kv_count[t] > NS ? kv_count[t] - NS : 0;
-            for (uint32_t idx = first; idx < kv_count[t]; ++idx)
-                mbar_wait_drain(bar(sm.kv_full[t][idx % NS]), (idx / NS) & 1, cx.wc, W_DRAIN);
+        for (int t = 0; t < 2; ++t)
             for (uint32_t n = q_count[t] > 2 ? q_count[t] - 2 : 0; n < q_count[t]; ++n)
                 mbar_wait_drain(bar(sm.q_full[t][n & 1]), (n >> 1) & 1, cx.wc, W_DRAIN);
-        }
-        if (BIAS && item_count > 0)
-            mbar_wait_drain(bar(sm.bias_full), (item_count - 1) & 1, cx.wc, W_DRAIN);
+        if constexpr (BIAS == BIAS_RESIDENT)
+            if (item_count > 0)
+                mbar_wait_drain(bar(sm.bias_full[0]), (item_count - 1) & 1, cx.wc, W_DRAIN);
+        if constexpr (BIAS == BIAS_STREAM)
+            for (uint32_t n = bias_count > kBiasStages ? bias_count - kBiasStages : 0; n < bias_count; ++n)
+                mbar_wait_drain(bar(sm.bias_full[n % kBiasStages]), (n / kBiasStages) & 1, cx.wc, W_DRAIN);
     }
 }
 
 // ------------------------------------------------------------------ MMA issuers
-constexpr uint64_t kHiK = umma_desc_hi(16, 512, kSwizzle64B); // Q, K: K-major, 64-byte rows
 
 // S = Q K^T for both slots, steps interleaved like the producer's.  q_empty
 // (one arrival) is committed after a batch index's last S; S(t, s) waits for
 // the softmax to have copied S(t, s-1) out of TMEM.
-template <bool BIAS>
-__device__ void s_role(const Ctx<BIAS> &cx, const EvoParams &p)
+template <int C, int BIAS>
+__device__ void s_role(const Ctx<C, BIAS> &cx, const EvoParams &p)
 {
-    constexpr int NS = EvoCfg<BIAS>::kStages;
-    EvoSmem<BIAS> &sm = *cx.sm;
+    using Cfg = EvoCfg<C, BIAS>;
+    constexpr int NS = Cfg::kStages;
+    EvoSmem<C, BIAS> &sm = *cx.sm;
     const uint32_t lane = ptx::lane_id();
     constexpr uint32_t idesc_qk = umma_idesc_bf16(BM, BN, false);
-    constexpr uint32_t kTileLo = kTile >> 4;
+    constexpr uint64_t kHiK = umma_desc_hi(16, 8 * Cfg::kRowBytes, Cfg::kSwz); // Q, K: K-major
+    constexpr uint32_t kTileLo = Cfg::kTile >> 4;
     const int nkv = (p.mask.S + BN - 1) / BN;
-    uint32_t kv_count[2] = {0u, 0u}, q_count[2] = {0u, 0u}, issued[2] = {0u, 0u};
+    uint32_t kv_count = 0, q_count[2] = {0u, 0u}, issued[2] = {0u, 0u};
     bool ok = true;
     for (int64_t L = blockIdx.x; L < p.n_items && ok; L += gridDim.x) {
         const EvoItem it = decode_evo(p, L);
@@ -244,17 +292,17 @@ __device__ void s_role(const Ctx<BIAS> &cx, const EvoParams &p)
                     if (!ok)
                         break;
                 }
-                const uint32_t stage = kv_count[t] % NS;
-                ok = warp_wait(bar(sm.kv_full[t][stage]), (kv_count[t] / NS) & 1, cx.wc, W_KV_FULL);
+                const uint32_t stage = kv_count % NS;
+                ok = warp_wait(bar(sm.kv_full[stage]), (kv_count / NS) & 1, cx.wc, W_KV_FULL);
                 if (!ok)
                     break;
                 ptx::tc_fence_after();
                 if (lane == 0) {
-                    const uint32_t qlo = (ptx::smem_u32(sm.q[t][qbuf]) >> 4);
-                    const uint32_t klo = (ptx::smem_u32(sm.k[t][0]) >> 4) + stage * kTileLo;
+                    const uint32_t qlo = ptx::smem_u32(sm.q[t][qbuf]) >> 4;
+                    const uint32_t klo = (ptx::smem_u32(sm.k[0]) >> 4) + stage * kTileLo;
                     const uint32_t tS = cx.tmem + kColS + 128 * t;
 #pragma unroll
-                    for (int kk = 0; kk < 2; ++kk)
+                    for (int kk = 0; kk < C / 16; ++kk) // 16 features (32 bytes) per step
                         ptx::mma_ss(tS, kHiK | (qlo + 2 * kk), kHiK | (klo + 2 * kk), idesc_qk,
                                     kk > 0 ? 1u : 0u);
                     ptx::mma_commit(bar(sm.s_full[t]));
@@ -263,7 +311,7 @@ __device__ void s_role(const Ctx<BIAS> &cx, const EvoParams &p)
                 }
                 __syncwarp();
                 ++issued[t];
-                ++kv_count[t];
+                ++kv_count;
                 if (j + 1 == nkv)
                     ++q_count[t];
             }
@@ -276,18 +324,20 @@ __device__ void s_role(const Ctx<BIAS> &cx, const EvoParams &p)
     mbar_wait_drain(bar(sm.s_final), 0, cx.wc, W_FINAL);
 }
 
-// O += P [V | 1] for slot t.  S(j) of a step completes before its softmax can
-// publish P(j), so the commit after P V also covers the K read: kv_empty has
-// one arrival (this warp's).
-template <bool BIAS>
-__device__ void pv_role(const Ctx<BIAS> &cx, const EvoParams &p, int t)
+// O += P [V | 1] (c = 32) or P V (c = 64) for slot t.  The ring index counts
+// both slots' steps in the producer's order; this warp acts on its own
+// slot's.  S(j) of a step completes before its softmax can publish P(j), so
+// the commit after P V also covers the K read: kv_empty has one arrival.
+template <int C, int BIAS>
+__device__ void pv_role(const Ctx<C, BIAS> &cx, const EvoParams &p, int t)
 {
-    constexpr int NS = EvoCfg<BIAS>::kStages;
-    EvoSmem<BIAS> &sm = *cx.sm;
+    using Cfg = EvoCfg<C, BIAS>;
+    constexpr int NS = Cfg::kStages;
+    EvoSmem<C, BIAS> &sm = *cx.sm;
     const uint32_t lane = ptx::lane_id();
-    constexpr uint32_t idesc_pv = umma_idesc_bf16(BM, kDvExt, true);
-    constexpr uint32_t kTileLo = kTile >> 4;
-    const uint32_t v_lo0 = ptx::smem_u32(sm.v[t][0]) >> 4;
+    constexpr uint32_t idesc_pv = umma_idesc_bf16(BM, Cfg::kDvExt, true);
+    constexpr uint32_t kTileLo = Cfg::kTile >> 4;
+    const uint32_t v_lo0 = ptx::smem_u32(sm.v[0]) >> 4;
     const uint32_t ones_lo = ptx::smem_u32(sm.ones) >> 4;
     const uint32_t tO = cx.tmem + kColO + 64 * t, tP = cx.tmem + kColP + 64 * t;
     const int nkv = (p.mask.S + BN - 1) / BN;
@@ -295,27 +345,41 @@ __device__ void pv_role(const Ctx<BIAS> &cx, const EvoParams &p, int t)
     bool ok = true;
     for (int64_t L = blockIdx.x; L < p.n_items && ok; L += gridDim.x) {
         const EvoItem it = decode_evo(p, L);
-        const int steps = slot_rows(it, t) * nkv;
-        for (int st = 0; st < steps && ok; ++st, ++kv_count) {
-            const int j = st % nkv;
-            // the softmax has written P(j) and rescaled O: O += P [V_j | 1]
-            ok = warp_wait(bar(sm.p_full[t]), pcount & 1, cx.wc, W_P_FULL);
-            if (!ok)
-                break;
-            ++pcount;
-            ptx::tc_fence_after();
-            if (lane == 0) {
-                const uint32_t stage = kv_count % NS;
-                const uint32_t vlo = v_lo0 + stage * kTileLo;
-                const uint64_t hi_v = umma_desc_hi((ones_lo - vlo) << 4, 512, kSwizzle64B);
+        const int steps[2] = {slot_rows(it, 0) * nkv, slot_rows(it, 1) * nkv};
+        const int n_steps = max(steps[0], steps[1]);
+        for (int st = 0; st < n_steps && ok; ++st) {
 #pragma unroll
-                for (int kk = 0; kk < BN / 16; ++kk)
-                    ptx::mma_ts(tO, tP + 8 * kk, hi_v | (vlo + 64 * kk), idesc_pv,
-                                (j > 0 || kk > 0) ? 1u : 0u);
-                ptx::mma_commit(bar(sm.pv_done[t]));
-                ptx::mma_commit(bar(sm.kv_empty[t][stage]));
+            for (int u = 0; u < 2; ++u) {
+                if (st >= steps[u])
+                    continue;
+                if (u != t) {
+                    ++kv_count; // the other slot's stage
+                    continue;
+                }
+                const int j = st % nkv;
+                // the softmax has written P(j) and rescaled O: O += P V_j
+                ok = warp_wait(bar(sm.p_full[t]), pcount & 1, cx.wc, W_P_FULL);
+                if (!ok)
+                    break;
+                ++pcount;
+                ptx::tc_fence_after();
+                if (lane == 0) {
+                    const uint32_t stage = kv_count % NS;
+                    const uint32_t vlo = v_lo0 + stage * kTileLo;
+                    // c = 32: V's second swizzle-width column block is the ones
+                    // tile, LBO bytes away; c = 64: N = 64 is one block
+                    const uint32_t lbo = Cfg::kOnes ? (ones_lo - vlo) << 4 : Cfg::kTile;
+                    const uint64_t hi_v = umma_desc_hi(lbo, 8 * Cfg::kRowBytes, Cfg::kSwz);
+#pragma unroll
+                    for (int kk = 0; kk < BN / 16; ++kk)
+                        ptx::mma_ts(tO, tP + 8 * kk, hi_v | (vlo + kk * (16 * Cfg::kRowBytes >> 4)), idesc_pv,
+                                    (j > 0 || kk > 0) ? 1u : 0u);
+                    ptx::mma_commit(bar(sm.pv_done[t]));
+                    ptx::mma_commit(bar(sm.kv_empty[stage]));
+                }
+                __syncwarp();
+                ++kv_count;
             }
-            __syncwarp();
         }
     }
     const uint32_t b_final = bar(sm.o_final[t]);
@@ -326,11 +390,28 @@ __device__ void pv_role(const Ctx<BIAS> &cx, const EvoParams &p, int t)
 }
 
 // ------------------------------------------------------------------ softmax
+//
+// Register layout of one thread (16x256b loads of a 128-key tile): x[4r],
+// x[4r + 1] are keys 8r + 2 jq, 8r + 2 jq + 1 of row R0 and x[4r + 2],
+// x[4r + 3] the same keys of row R1 = R0 + 8 (r = 0..15, jq = lane % 4).
 
-struct PendingRow {
-    int b, h, qb, i;
-    RowState st;
+struct Rows2 {
+    float m[2];  // reference max (log2 units) of rows R0, R1
+    float l[2];  // this thread's share of the sum of the exact P (LSE)
+    float lr[2]; // this thread's share of the sum of the rounded P (c = 64 normaliser)
 };
+
+__device__ __forceinline__ float quad_max(float v)
+{
+    v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 1));
+    return fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 2));
+}
+
+__device__ __forceinline__ float quad_sum(float v)
+{
+    v += __shfl_xor_sync(0xffffffffu, v, 1);
+    return v + __shfl_xor_sync(0xffffffffu, v, 2);
+}
 
 __device__ __forceinline__ float tanh_approx(float x)
 {
@@ -339,46 +420,166 @@ __device__ __forceinline__ float tanh_approx(float x)
     return y;
 }
 
-// sigmoid(g) * O / sum(P) -> bf16 row, LSE, visited-tile count.  O[t] must
-// hold the finished output of `pr` (its last P V has completed).
-template <bool LSE>
-__device__ __forceinline__ void store_row_output(const EvoParams &p, uint32_t tO,
-                                                 const PendingRow &pr, int r, int nkv)
+// Max update with the lazy rescale decision, then P = 2^(c x - m) packed as
+// bf16 pairs (pk[2r] row R0, pk[2r + 1] row R1) and this thread's shares of
+// the sums.  Returns whether any row of the warp rescales (alpha[k] = 1 for
+// rows that do not).
+template <bool LSE, bool RSUM>
+__device__ __forceinline__ bool evo_tile_p(const float (&x)[64], float c, Rows2 &st, bool first,
+                                           uint32_t (&pk)[32], float (&alpha)[2])
 {
-    uint32_t o[32], sum[1];
-    ptx::tmem_ld32(tO, o);
-    ptx::tmem_ld1(tO + kColSum, sum);
-    ptx::tmem_wait_ld();
-    ptx::reg_fence<32>(o);
-    ptx::reg_fence<1>(sum);
-    const float l_round = __uint_as_float(sum[0]);
-    const float inv = l_round > 0.f ? 1.f / l_round : 0.f;
-    if (pr.i < p.mask.S) {
-        uint4 *d4 = reinterpret_cast<uint4 *>(p.out + pr.b * p.o_sb +
-                                              static_cast<int64_t>(pr.i) * p.o_si + pr.h * p.o_sh);
-        const uint4 *g4 = reinterpret_cast<const uint4 *>(
-            p.gate + pr.b * p.g_sb + static_cast<int64_t>(pr.i) * p.g_si + pr.h * p.g_sh);
+    float a0 = fmaxf(x[0], x[1]), a1 = fmaxf(x[2], x[3]);
+    float b0 = fmaxf(x[4], x[5]), b1 = fmaxf(x[6], x[7]);
 #pragma unroll
-        for (int c4 = 0; c4 < 4; ++c4) {
-            const uint4 gw = __ldg(g4 + c4); // prefetched into L1 when the row started
-            const uint32_t gv[4] = {gw.x, gw.y, gw.z, gw.w};
-            uint32_t ov[4];
-#pragma unroll
-            for (int q = 0; q < 4; ++q) {
-                // sigmoid(g) = 1/2 + tanh(g / 2) / 2 (one special-function op)
-                const float g0 = __uint_as_float(gv[q] << 16);
-                const float g1 = __uint_as_float(gv[q] & 0xFFFF0000u);
-                const float s0 = fmaf(0.5f, tanh_approx(0.5f * g0), 0.5f);
-                const float s1 = fmaf(0.5f, tanh_approx(0.5f * g1), 0.5f);
-                ov[q] = ptx::pack_bf16(__uint_as_float(o[8 * c4 + 2 * q]) * inv * s0,
-                                       __uint_as_float(o[8 * c4 + 2 * q + 1]) * inv * s1);
-            }
-            d4[c4] = make_uint4(ov[0], ov[1], ov[2], ov[3]);
-        }
-        if (LSE)
-            p.lse[pr.b * p.l_sb + pr.h * p.l_sh + pr.i] = row_lse(pr.st);
+    for (int r = 2; r < 16; r += 2) {
+        a0 = ptx::max3(a0, x[4 * r], x[4 * r + 1]);
+        a1 = ptx::max3(a1, x[4 * r + 2], x[4 * r + 3]);
+        b0 = ptx::max3(b0, x[4 * r + 4], x[4 * r + 5]);
+        b1 = ptx::max3(b1, x[4 * r + 6], x[4 * r + 7]);
     }
-    if (p.tile_counts && r == 0)
+    const float mx[2] = {quad_max(fmaxf(a0, b0)) * c, quad_max(fmaxf(a1, b1)) * c}; // c > 0
+    alpha[0] = alpha[1] = 1.f;
+    bool rescale = false;
+    if (first) {
+        st.m[0] = mx[0];
+        st.m[1] = mx[1];
+    } else {
+        const bool need = mx[0] > st.m[0] + kRescaleThreshold || mx[1] > st.m[1] + kRescaleThreshold;
+        if (__any_sync(0xffffffffu, need)) {
+#pragma unroll
+            for (int k = 0; k < 2; ++k) {
+                const float m_new = fmaxf(st.m[k], mx[k]);
+                alpha[k] = (m_new == kNegInf) ? 1.f : ptx::ex2(st.m[k] - m_new);
+                st.l[k] *= alpha[k];
+                st.lr[k] *= alpha[k];
+                st.m[k] = m_new;
+            }
+            rescale = true;
+        }
+    }
+    const float n0 = (st.m[0] == kNegInf) ? 0.f : -st.m[0];
+    const float n1 = (st.m[1] == kNegInf) ? 0.f : -st.m[1];
+    float le[4] = {0.f, 0.f, 0.f, 0.f}, lq[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int r = 0; r < 16; ++r) {
+        float u0, u1, w0, w1;
+        ptx::fma2(u0, u1, x[4 * r], x[4 * r + 1], c, c, n0, n0);
+        ptx::fma2(w0, w1, x[4 * r + 2], x[4 * r + 3], c, c, n1, n1);
+        const float p0 = ptx::ex2(u0), p1 = ptx::ex2(u1);
+        const float q0 = ptx::ex2(w0), q1 = ptx::ex2(w1);
+        pk[2 * r] = ptx::pack_bf16(p0, p1);
+        pk[2 * r + 1] = ptx::pack_bf16(q0, q1);
+        if constexpr (LSE) {
+            ptx::add2(le[0], le[1], p0, p1);
+            ptx::add2(le[2], le[3], q0, q1);
+        }
+        if constexpr (RSUM) {
+            ptx::add2(lq[0], lq[1], __uint_as_float(pk[2 * r] << 16), __uint_as_float(pk[2 * r] & 0xFFFF0000u));
+            ptx::add2(lq[2], lq[3], __uint_as_float(pk[2 * r + 1] << 16),
+                      __uint_as_float(pk[2 * r + 1] & 0xFFFF0000u));
+        }
+    }
+    if constexpr (LSE) {
+        st.l[0] += le[0] + le[1];
+        st.l[1] += le[2] + le[3];
+    }
+    if constexpr (RSUM) {
+        st.lr[0] += lq[0] + lq[1];
+        st.lr[1] += lq[2] + lq[3];
+    }
+    return rescale;
+}
+
+// O[t] *= alpha for this thread's two rows (its columns of the 16x256b layout).
+template <int C>
+__device__ __forceinline__ void evo_rescale_o(uint32_t tO, const float (&alpha)[2])
+{
+    if constexpr (C == 32) {
+        uint32_t o[24]; // columns 0..31 (output) and 32..47 (sums)
+        ptx::tmem_ld_16x256b_x4(tO, o);
+        ptx::tmem_ld_16x256b_x2(tO + 32, o + 16);
+        ptx::tmem_wait_ld();
+        ptx::reg_fence<24>(o);
+#pragma unroll
+        for (int e = 0; e < 24; ++e)
+            o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha[(e >> 1) & 1]);
+        ptx::tmem_st_16x256b_x4(tO, o);
+        ptx::tmem_st_16x256b_x2(tO + 32, o + 16);
+    } else {
+        uint32_t o[32];
+        ptx::tmem_ld_16x256b_x8(tO, o);
+        ptx::tmem_wait_ld();
+        ptx::reg_fence<32>(o);
+#pragma unroll
+        for (int e = 0; e < 32; ++e)
+            o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha[(e >> 1) & 1]);
+        ptx::tmem_st_16x256b_x8(tO, o);
+    }
+}
+
+struct PendingRow {
+    int b, h, qb, r0; // r0: this thread's first row in the query block
+    Rows2 st;
+};
+
+// sigmoid(g) * O / sum(P) -> bf16, LSE, visited-tile count, for this thread's
+// two rows of `pr`.  O[t] must hold the finished output of `pr` (its last P V
+// has completed).  Warp-collective (TMEM loads, shuffles).
+template <int C, bool LSE>
+__device__ __forceinline__ void evo_epilogue(const EvoParams &p, uint32_t tO, const PendingRow &pr, int jq,
+                                             int nkv)
+{
+    constexpr int kChunks = C / 8;
+    uint32_t o[4 * kChunks];
+    float inv[2];
+    if constexpr (C == 32) {
+        uint32_t sum[4];
+        ptx::tmem_ld_16x256b_x4(tO, o);
+        ptx::tmem_ld_16x256b_x1(tO + 32, sum); // registers 0 and 2: the sums of R0 and R1
+        ptx::tmem_wait_ld();
+        ptx::reg_fence<16>(o);
+        ptx::reg_fence<4>(sum);
+        const float s0 = __uint_as_float(sum[0]), s1 = __uint_as_float(sum[2]);
+        inv[0] = s0 > 0.f ? 1.f / s0 : 0.f;
+        inv[1] = s1 > 0.f ? 1.f / s1 : 0.f;
+    } else {
+        ptx::tmem_ld_16x256b_x8(tO, o);
+        ptx::tmem_wait_ld();
+        ptx::reg_fence<32>(o);
+        const float s0 = quad_sum(pr.st.lr[0]), s1 = quad_sum(pr.st.lr[1]);
+        inv[0] = s0 > 0.f ? 1.f / s0 : 0.f;
+        inv[1] = s1 > 0.f ? 1.f / s1 : 0.f;
+    }
+    float lsum[2] = {0.f, 0.f};
+    if constexpr (LSE) {
+        lsum[0] = quad_sum(pr.st.l[0]);
+        lsum[1] = quad_sum(pr.st.l[1]);
+    }
+#pragma unroll
+    for (int k = 0; k < 2; ++k) {
+        const int i = pr.qb * BM + pr.r0 + 8 * k;
+        if (i >= p.mask.S)
+            continue;
+        const int64_t g_row = pr.b * p.g_sb + static_cast<int64_t>(i) * p.g_si + pr.h * p.g_sh;
+        const int64_t o_row = pr.b * p.o_sb + static_cast<int64_t>(i) * p.o_si + pr.h * p.o_sh;
+        const uint32_t *g32 = reinterpret_cast<const uint32_t *>(p.gate + g_row);
+        uint32_t *o32 = reinterpret_cast<uint32_t *>(p.out + o_row);
+#pragma unroll
+        for (int r = 0; r < kChunks; ++r) {
+            // columns 8r + 2 jq and 8r + 2 jq + 1: one 32-bit word of the row
+            const uint32_t gw = __ldg(g32 + 4 * r + jq); // prefetched into L1 when the row started
+            const float g0 = __uint_as_float(gw << 16), g1 = __uint_as_float(gw & 0xFFFF0000u);
+            // sigmoid(g) = 1/2 + tanh(g / 2) / 2 (one special-function op)
+            const float s0 = fmaf(0.5f, tanh_approx(0.5f * g0), 0.5f);
+            const float s1 = fmaf(0.5f, tanh_approx(0.5f * g1), 0.5f);
+            o32[4 * r + jq] = ptx::pack_bf16(__uint_as_float(o[4 * r + 2 * k]) * inv[k] * s0,
+                                             __uint_as_float(o[4 * r + 2 * k + 1]) * inv[k] * s1);
+        }
+        if (LSE && jq == 0)
+            p.lse[pr.b * p.l_sb + pr.h * p.l_sh + i] =
+                lsum[k] > 0.f ? (pr.st.m[k] + log2f(lsum[k])) * kLn2 : kNegInf;
+    }
+    if (p.tile_counts && pr.r0 == 0 && jq == 0)
         p.tile_counts[(static_cast<int64_t>(pr.b) * p.grid.Hq + pr.h) * p.grid.nq + pr.qb] = nkv;
 }
 
@@ -393,178 +594,235 @@ __device__ __forceinline__ uint32_t mask_keeps(const EvoParams &p, int b, int ke
                     : (__ldg(static_cast<const uint16_t *>(p.kmask) + off) & 0x7FFFu);
 }
 
-template <bool BIAS, bool LSE, bool KMASK>
-__device__ void softmax_role(const Ctx<BIAS> &cx, const EvoParams &p, int t)
+template <int C, int BIAS, bool LSE, bool KMASK>
+__device__ void softmax_role(const Ctx<C, BIAS> &cx, const EvoParams &p, int t, int wi)
 {
-    EvoSmem<BIAS> &sm = *cx.sm;
-    const int r = threadIdx.x & 127;             // row of the query tile = TMEM lane
-    const uint32_t wq = (threadIdx.x >> 5) & 3;  // warp's quarter of the lanes
-    const uint32_t lane_off = (wq * 32u) << 16;
+    using Cfg = EvoCfg<C, BIAS>;
+    constexpr bool kRsum = !Cfg::kOnes;
+    EvoSmem<C, BIAS> &sm = *cx.sm;
+    const int lane = threadIdx.x & 31;
+    const int jq = lane & 3;                      // key pair of every 8-key group
+    const int wq = (threadIdx.x >> 5) & 3;        // TMEM lane quarter of this warp
+    const int r0 = 32 * wq + 16 * (wi >> 2) + (lane >> 2); // rows r0 and r0 + 8 of the block
+    const uint32_t lane_off = static_cast<uint32_t>(32 * wq + 16 * (wi >> 2)) << 16;
     const uint32_t tS = cx.tmem + lane_off + kColS + 128 * t;
     const uint32_t tO = cx.tmem + lane_off + kColO + 64 * t;
     const uint32_t tP = cx.tmem + lane_off + kColP + 64 * t;
     const int S = p.mask.S;
     const int nkv = (S + BN - 1) / BN;
-    // bias smem: row r of each 64-key box is 128 bytes, 16-byte chunk c stored
-    // at position c ^ (r & 7) (the 128-byte swizzle the TMA wrote it with)
-    const uint32_t bias_row = ptx::smem_u32(sm.bias[0]) + r * 128;
-    uint32_t scount = 0, pvcount = 0, item_count = 0;
+    // bias smem: row R of a 64-key box is 128 bytes, 16-byte chunk cc (8 keys)
+    // stored at position cc ^ (R & 7) (the 128-byte swizzle the TMA wrote);
+    // this thread's 32-bit word of a chunk is at byte 4 jq, and rows r0 and
+    // r0 + 8 share the swizzle phase
+    const uint32_t bias_r0 = ptx::smem_u32(sm.bias) + r0 * 128 + 4 * jq;
+    const uint32_t swz = r0 & 7;
+    uint32_t scount = 0, pvcount = 0, item_count = 0, bias_count = 0;
     bool pending = false;
     PendingRow prev{};
 
     for (int64_t L = blockIdx.x; L < p.n_items; L += gridDim.x, ++item_count) {
         const EvoItem it = decode_evo(p, L);
-        const int i = it.qb * BM + r;
-        const TileRange tr = q_block_range(p.mask, 0, it.qb * BM);
-        int row_lo, row_hi;
-        row_interval(p.mask, 0, i, row_lo, row_hi);
-        if (BIAS && !warp_wait(bar(sm.bias_full), item_count & 1, cx.wc, W_BIAS))
+        if (BIAS == BIAS_RESIDENT && !warp_wait(bar(sm.bias_full[0]), item_count & 1, cx.wc, W_BIAS))
             return;
-        for (int b = it.b0 + t; b < it.b1; b += 2) {
-            RowState st{kNegInf, 0.f, 0.f};
-            for (int j = 0; j < nkv; ++j) {
-                // MSA mask of this batch index and key tile: lane l reads keys
-                // j0 + 32 w + l (issued before the wait, used after it)
-                uint32_t keep[4];
-                if constexpr (KMASK) {
-                    const int lane = threadIdx.x & 31;
-#pragma unroll
-                    for (int w = 0; w < 4; ++w)
-                        keep[w] = mask_keeps(p, b, j * BN + 32 * w + lane, S);
-                }
-                if (!warp_wait(bar(sm.s_full[t]), scount & 1, cx.wc, W_S_FULL))
+        const int steps[2] = {slot_rows(it, 0) * nkv, slot_rows(it, 1) * nkv};
+        const int n_steps = max(steps[0], steps[1]);
+        Rows2 st{{kNegInf, kNegInf}, {0.f, 0.f}, {0.f, 0.f}};
+        for (int stp = 0; stp < n_steps; ++stp) {
+            const int j = stp % nkv;
+            uint32_t bias_base = 0;
+            if constexpr (BIAS == BIAS_STREAM) {
+                const uint32_t bs = bias_count % kBiasStages;
+                if (!warp_wait(bar(sm.bias_full[bs]), (bias_count / kBiasStages) & 1, cx.wc, W_BIAS))
                     return;
-                ++scount;
-                ptx::tc_fence_after();
-                float x[BN];
-                load_scores(tS, x);
-                ptx::tc_fence_before();
-                ptx::mbar_arrive(bar(sm.s_free[t])); // S[t] may be overwritten
-                const int j0 = j * BN;
-                float c = p.qk_log2;
-                if constexpr (BIAS) {
-                    // natural-unit logits scale q.k + b[h, i, j]; log2 e goes
-                    // into the exponent
-                    c = kLog2e;
-#pragma unroll
-                    for (int ch = 0; ch < BN / 8; ++ch) {
-                        const int box = 2 * j + (ch >> 3), cc = ch & 7;
-                        const uint32_t addr =
-                            bias_row + box * kBiasBox + ((cc ^ (r & 7)) << 4);
-                        uint32_t w0, w1, w2, w3;
-                        asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
-                                     : "=r"(w0), "=r"(w1), "=r"(w2), "=r"(w3)
-                                     : "r"(addr));
-                        const uint32_t wv[4] = {w0, w1, w2, w3};
-#pragma unroll
-                        for (int q = 0; q < 4; ++q) {
-                            x[8 * ch + 2 * q] =
-                                fmaf(x[8 * ch + 2 * q], p.qk_scale, __uint_as_float(wv[q] << 16));
-                            x[8 * ch + 2 * q + 1] = fmaf(x[8 * ch + 2 * q + 1], p.qk_scale,
-                                                         __uint_as_float(wv[q] & 0xFFFF0000u));
-                        }
-                    }
+                ++bias_count;
+                if (stp >= steps[t]) {
+                    // no row of this slot at this step: release the stage
+                    __syncwarp();
+                    if (lane == 0)
+                        ptx::mbar_arrive(bar(sm.bias_empty[bs]));
+                    continue;
                 }
-                if (!((j0 >= tr.full_lo) && (j0 + BN <= tr.full_hi)))
-                    apply_row_mask(x, j0, row_lo, row_hi);
-                if constexpr (KMASK) {
-                    // word w bit l: key j0 + 32 w + l is kept
-                    uint32_t bits[4], all = ~0u;
-#pragma unroll
-                    for (int w = 0; w < 4; ++w) {
-                        bits[w] = __ballot_sync(0xffffffffu, keep[w] != 0u);
-                        all &= bits[w];
-                    }
-                    if (all != ~0u) {
-#pragma unroll
-                        for (int e = 0; e < BN; ++e)
-                            if (!((bits[e >> 5] >> (e & 31)) & 1u))
-                                x[e] = kNegInf;
-                    }
-                }
-                uint32_t pk[BN / 2];
-                bool rescale;
-                const float alpha =
-                    LSE ? softmax_compute_p_exact_sum(x, c, st, j == 0, pk, rescale)
-                        : softmax_compute_p_no_sum(x, c, st, j == 0, pk, rescale);
-                if (j > 0 || pending) {
-                    // the previous P V of this slot has consumed P[t] and
-                    // landed in O[t]
-                    if (!warp_wait(bar(sm.pv_done[t]), pvcount & 1, cx.wc, W_O_FULL))
-                        return;
-                    ++pvcount;
-                    ptx::tc_fence_after();
-                    if (j > 0) {
-                        if (rescale)
-                            rescale_o<kDvExt>(tO, alpha);
-                    } else {
-                        store_row_output<LSE>(p, tO, prev, r, nkv);
-                        pending = false;
-                    }
-                }
-                if (j == 0 && i < S) {
-                    // bring this row's 64 gate bytes into L1 for its (deferred) epilogue
-                    const __nv_bfloat16 *gp =
-                        p.gate + b * p.g_sb + static_cast<int64_t>(i) * p.g_si + it.h * p.g_sh;
-                    asm volatile("prefetch.global.L1 [%0];" ::"l"(gp));
-                }
-                store_p(tP, pk);
-                ptx::tc_fence_before();
-                ptx::mbar_arrive(bar(sm.p_full[t]));
+                bias_base = bias_r0 + 2 * bs * kBiasBox;
+            } else {
+                if (stp >= steps[t])
+                    break;
+                bias_base = bias_r0 + 2 * j * kBiasBox;
             }
-            prev.b = b;
-            prev.h = it.h;
-            prev.qb = it.qb;
-            prev.i = i;
-            prev.st = st;
-            pending = true;
+            const int b = it.b0 + t + 2 * (stp / nkv);
+            const int j0 = j * BN;
+            // MSA mask of this batch index and key tile: lane l reads keys
+            // j0 + 32 w + l (issued before the wait, used after it)
+            uint32_t keep[4];
+            if constexpr (KMASK) {
+#pragma unroll
+                for (int w = 0; w < 4; ++w)
+                    keep[w] = mask_keeps(p, b, j0 + 32 * w + lane, S);
+            }
+            if (!warp_wait(bar(sm.s_full[t]), scount & 1, cx.wc, W_S_FULL))
+                return;
+            ++scount;
+            ptx::tc_fence_after();
+            float x[64];
+            {
+                uint32_t raw[64];
+                ptx::tmem_ld_16x256b_x16(tS, raw);
+                ptx::tmem_wait_ld();
+                ptx::reg_fence<32>(raw);
+                ptx::reg_fence<32>(raw + 32);
+#pragma unroll
+                for (int e = 0; e < 64; ++e)
+                    x[e] = __uint_as_float(raw[e]);
+            }
+            ptx::tc_fence_before();
+            ptx::mbar_arrive(bar(sm.s_free[t])); // S[t] may be overwritten
+            float c = p.qk_log2;
+            if constexpr (BIAS != BIAS_NONE) {
+                // natural-unit logits scale q.k + b[h, i, j]; log2 e goes into
+                // the exponent
+                c = kLog2e;
+#pragma unroll
+                for (int r = 0; r < 16; ++r) {
+                    const uint32_t a = bias_base + (r >> 3) * kBiasBox + (((r & 7) ^ swz) << 4);
+                    uint32_t w0, w1;
+                    asm volatile("ld.shared.b32 %0, [%1];" : "=r"(w0) : "r"(a));
+                    asm volatile("ld.shared.b32 %0, [%1];" : "=r"(w1) : "r"(a + 8 * 128));
+                    ptx::fma2(x[4 * r], x[4 * r + 1], x[4 * r], x[4 * r + 1], p.qk_scale, p.qk_scale,
+                              __uint_as_float(w0 << 16), __uint_as_float(w0 & 0xFFFF0000u));
+                    ptx::fma2(x[4 * r + 2], x[4 * r + 3], x[4 * r + 2], x[4 * r + 3], p.qk_scale, p.qk_scale,
+                              __uint_as_float(w1 << 16), __uint_as_float(w1 & 0xFFFF0000u));
+                }
+                if constexpr (BIAS == BIAS_STREAM) {
+                    // the bias words are in registers (used above): release the stage
+                    __syncwarp();
+                    if (lane == 0)
+                        ptx::mbar_arrive(bar(sm.bias_empty[(bias_count - 1) % kBiasStages]));
+                }
+            }
+            if (j0 + BN > S) {
+                // keys past the sequence (a ragged last tile)
+#pragma unroll
+                for (int e = 0; e < 64; ++e)
+                    if (j0 + 8 * (e >> 2) + 2 * jq + (e & 1) >= S)
+                        x[e] = kNegInf;
+            }
+            if constexpr (KMASK) {
+                // word w bit l: key j0 + 32 w + l is kept
+                uint32_t bits[4], all = ~0u;
+#pragma unroll
+                for (int w = 0; w < 4; ++w) {
+                    bits[w] = __ballot_sync(0xffffffffu, keep[w] != 0u);
+                    all &= bits[w];
+                }
+                if (all != ~0u) {
+#pragma unroll
+                    for (int e = 0; e < 64; ++e) {
+                        const int key = 8 * (e >> 2) + 2 * jq + (e & 1);
+                        if (!((bits[key >> 5] >> (key & 31)) & 1u))
+                            x[e] = kNegInf;
+                    }
+                }
+            }
+            uint32_t pk[32];
+            float alpha[2];
+            const bool rescale = evo_tile_p<LSE, kRsum>(x, c, st, j == 0, pk, alpha);
+            const bool waits = j > 0 || pending;
+            if (waits) {
+                // the previous P V of this slot has consumed P[t] and landed in O[t]
+                if (!warp_wait(bar(sm.pv_done[t]), pvcount & 1, cx.wc, W_O_FULL))
+                    return;
+                ++pvcount;
+                ptx::tc_fence_after();
+            }
+            // P first (its registers are free again before O is read); the P V
+            // that overwrites O waits for p_full below
+            ptx::tmem_st_16x128b_x16(tP, pk);
+            if (waits) {
+                if (j > 0) {
+                    if (rescale)
+                        evo_rescale_o<C>(tO, alpha);
+                } else {
+                    evo_epilogue<C, LSE>(p, tO, prev, jq, nkv);
+                    pending = false;
+                }
+            }
+            if (j == 0 && jq == 0) {
+                // bring this thread's rows' gate bytes into L1 for their (deferred) epilogue
+#pragma unroll
+                for (int k = 0; k < 2; ++k) {
+                    const int i = it.qb * BM + r0 + 8 * k;
+                    if (i < S)
+                        asm volatile("prefetch.global.L1 [%0];" ::"l"(
+                            p.gate + b * p.g_sb + static_cast<int64_t>(i) * p.g_si + it.h * p.g_sh));
+                }
+            }
+            ptx::tmem_wait_st();
+            ptx::tc_fence_before();
+            ptx::mbar_arrive(bar(sm.p_full[t]));
+            if (j + 1 == nkv) {
+                prev.b = b;
+                prev.h = it.h;
+                prev.qb = it.qb;
+                prev.r0 = r0;
+                prev.st = st;
+                pending = true;
+                st = Rows2{{kNegInf, kNegInf}, {0.f, 0.f}, {0.f, 0.f}};
+            }
         }
-        if (BIAS)
-            ptx::mbar_arrive(bar(sm.bias_empty)); // this warpgroup is done with the bias rows
+        if constexpr (BIAS == BIAS_RESIDENT) {
+            __syncwarp();
+            if (lane == 0)
+                ptx::mbar_arrive(bar(sm.bias_empty[0])); // this warp is done with the bias rows
+        }
     }
     if (pending) {
         if (!warp_wait(bar(sm.o_final[t]), 0, cx.wc, W_O_FULL))
             return;
         ptx::tc_fence_after();
-        store_row_output<LSE>(p, tO, prev, r, nkv);
+        evo_epilogue<C, LSE>(p, tO, prev, jq, nkv);
     }
 }
 
-template <bool BIAS, bool LSE, bool KMASK>
+template <int C, int BIAS, bool LSE, bool KMASK>
 __global__ void __launch_bounds__(kThreads, 1)
     evo_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                    const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_b,
                    const EvoParams p)
 {
-    constexpr int NS = EvoCfg<BIAS>::kStages;
+    using Cfg = EvoCfg<C, BIAS>;
+    using Smem = EvoSmem<C, BIAS>;
+    constexpr int NS = Smem::NS, NB = Smem::NB;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t base = ptx::smem_u32(smem_raw);
-    EvoSmem<BIAS> *sm = reinterpret_cast<EvoSmem<BIAS> *>(smem_raw + ((1024u - (base & 1023u)) & 1023u));
+    Smem *sm = reinterpret_cast<Smem *>(smem_raw + ((1024u - (base & 1023u)) & 1023u));
     const int warp = threadIdx.x >> 5;
 
     // the ones tile (bf16 1.0 pairs), read by the tensor core through the async proxy
-    for (uint32_t w = threadIdx.x; w < kTile / 4; w += kThreads)
-        reinterpret_cast<uint32_t *>(sm->ones)[w] = 0x3F803F80u;
-    ptx::fence_proxy_async_smem();
+    if constexpr (Cfg::kOnes) {
+        for (uint32_t w = threadIdx.x; w < Cfg::kOnesBytes / 4; w += kThreads)
+            reinterpret_cast<uint32_t *>(sm->ones)[w] = 0x3F803F80u;
+        ptx::fence_proxy_async_smem();
+    }
     if (threadIdx.x == 0) {
         for (int t = 0; t < 2; ++t) {
             for (int b = 0; b < 2; ++b) {
                 ptx::mbar_init(bar(sm->q_full[t][b]), 1);
                 ptx::mbar_init(bar(sm->q_empty[t][b]), 1);
             }
-            for (int s = 0; s < NS; ++s) {
-                ptx::mbar_init(bar(sm->kv_full[t][s]), 1);
-                ptx::mbar_init(bar(sm->kv_empty[t][s]), 1);
-            }
             ptx::mbar_init(bar(sm->s_full[t]), 1);
-            ptx::mbar_init(bar(sm->s_free[t]), 128);
-            ptx::mbar_init(bar(sm->p_full[t]), 128);
+            ptx::mbar_init(bar(sm->s_free[t]), 256);
+            ptx::mbar_init(bar(sm->p_full[t]), 256);
             ptx::mbar_init(bar(sm->pv_done[t]), 1);
             ptx::mbar_init(bar(sm->o_final[t]), 1);
         }
+        for (int s = 0; s < NS; ++s) {
+            ptx::mbar_init(bar(sm->kv_full[s]), 1);
+            ptx::mbar_init(bar(sm->kv_empty[s]), 1);
+        }
         ptx::mbar_init(bar(sm->s_final), 1);
-        ptx::mbar_init(bar(sm->bias_full), 1);
-        ptx::mbar_init(bar(sm->bias_empty), 256);
+        for (int s = 0; s < NB; ++s) {
+            ptx::mbar_init(bar(sm->bias_full[s]), 1);
+            ptx::mbar_init(bar(sm->bias_empty[s]), 16); // one arrival per softmax warp
+        }
         sm->abort_flag = 0;
         ptx::fence_mbarrier_init();
         ptx::fence_proxy_async_smem();
@@ -573,7 +831,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         ptx::prefetch_tensormap(&tm_q);
         ptx::prefetch_tensormap(&tm_k);
         ptx::prefetch_tensormap(&tm_v);
-        if (BIAS)
+        if (BIAS != BIAS_NONE)
             ptx::prefetch_tensormap(&tm_b);
     }
     if (warp == 1) {
@@ -584,7 +842,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncthreads();
     ptx::tc_fence_after();
 
-    Ctx<BIAS> cx;
+    Ctx<C, BIAS> cx;
     cx.sm = sm;
     cx.tmem = sm->tmem_base;
     cx.wc.abort_flag = &sm->abort_flag;
@@ -596,17 +854,17 @@ __global__ void __launch_bounds__(kThreads, 1)
     // runs under both register limits.
     if (warp >= 4) {
         ptx::setmaxnreg_inc<kRegsSoftmax>();
-        softmax_role<BIAS, LSE, KMASK>(cx, p, (warp >> 2) - 1);
+        softmax_role<C, BIAS, LSE, KMASK>(cx, p, (warp - 4) >> 3, (warp - 4) & 7);
         ptx::tc_fence_before();
         ptx::named_barrier_sync(1, kThreads);
     } else {
         ptx::setmaxnreg_dec<kRegsOther>();
         if (warp == 0)
-            producer_role<BIAS>(cx, p, &tm_q, &tm_k, &tm_v, &tm_b);
+            producer_role<C, BIAS>(cx, p, &tm_q, &tm_k, &tm_v, &tm_b);
         else if (warp == 1)
-            s_role<BIAS>(cx, p);
+            s_role<C, BIAS>(cx, p);
         else
-            pv_role<BIAS>(cx, p, warp - 2);
+            pv_role<C, BIAS>(cx, p, warp - 2);
         ptx::tc_fence_before();
         ptx::named_barrier_sync(1, kThreads);
         if (warp == 1) {
@@ -616,28 +874,52 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 }
 
-template <bool BIAS, bool LSE, bool KMASK>
+template <int C, int BIAS, bool LSE, bool KMASK>
 cudaError_t launch_variant(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
                            const CUtensorMap &tb, const EvoParams &p, int grid, cudaStream_t stream)
 {
-    const size_t smem = sizeof(EvoSmem<BIAS>) + 1024;
+    // the layout plus the worst-case alignment pad within 227 KB per CTA
+    static_assert(sizeof(EvoSmem<C, BIAS>) + 1024 <= kSmemLimit, "shared memory per CTA");
+    const size_t smem = sizeof(EvoSmem<C, BIAS>) + 1024;
     static bool configured = false; // benign race: both calls are idempotent
     if (!configured) {
         cudaFuncAttributes attr;
-        cudaError_t e = cudaFuncGetAttributes(&attr, evo_fwd_kernel<BIAS, LSE, KMASK>);
+        cudaError_t e = cudaFuncGetAttributes(&attr, evo_fwd_kernel<C, BIAS, LSE, KMASK>);
         if (e != cudaSuccess)
             return e;
         // The setmaxnreg split assumes exactly kRegsLaunch registers at launch.
         if (attr.numRegs != static_cast<int>(kRegsLaunch))
             return cudaErrorInvalidConfiguration;
-        e = cudaFuncSetAttribute(evo_fwd_kernel<BIAS, LSE, KMASK>,
+        e = cudaFuncSetAttribute(evo_fwd_kernel<C, BIAS, LSE, KMASK>,
                                  cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
         if (e != cudaSuccess)
             return e;
         configured = true;
     }
-    evo_fwd_kernel<BIAS, LSE, KMASK><<<grid, kThreads, smem, stream>>>(tq, tk, tv, tb, p);
+    evo_fwd_kernel<C, BIAS, LSE, KMASK><<<grid, kThreads, smem, stream>>>(tq, tk, tv, tb, p);
     return cudaGetLastError();
+}
+
+template <int C, int BIAS>
+cudaError_t launch_flags(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
+                         const CUtensorMap &tb, const EvoParams &p, int grid, cudaStream_t stream)
+{
+    if (p.kmask)
+        return p.lse ? launch_variant<C, BIAS, true, true>(tq, tk, tv, tb, p, grid, stream)
+                     : launch_variant<C, BIAS, false, true>(tq, tk, tv, tb, p, grid, stream);
+    return p.lse ? launch_variant<C, BIAS, true, false>(tq, tk, tv, tb, p, grid, stream)
+                 : launch_variant<C, BIAS, false, false>(tq, tk, tv, tb, p, grid, stream);
+}
+
+template <int C>
+cudaError_t launch_c(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
+                     const CUtensorMap &tb, const EvoParams &p, int grid, cudaStream_t stream)
+{
+    if (!p.bias)
+        return launch_flags<C, BIAS_NONE>(tq, tk, tv, tb, p, grid, stream);
+    if (C == 32 && p.mask.S <= kMaxBiasBoxes * 64)
+        return launch_flags<C, (C == 32 ? BIAS_RESIDENT : BIAS_STREAM)>(tq, tk, tv, tb, p, grid, stream);
+    return launch_flags<C, BIAS_STREAM>(tq, tk, tv, tb, p, grid, stream);
 }
 
 } // namespace
@@ -645,20 +927,8 @@ cudaError_t launch_variant(const CUtensorMap &tq, const CUtensorMap &tk, const C
 cudaError_t launch_evo(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
                        const CUtensorMap &tb, const EvoParams &p, int grid, cudaStream_t stream)
 {
-    if (p.kmask) {
-        if (p.bias)
-            return p.lse ? launch_variant<true, true, true>(tq, tk, tv, tb, p, grid, stream)
-                         : launch_variant<true, false, true>(tq, tk, tv, tb, p, grid, stream);
-        return p.lse ? launch_variant<false, true, true>(tq, tk, tv, tb, p, grid, stream)
-                     : launch_variant<false, false, true>(tq, tk, tv, tb, p, grid, stream);
-    }
-    if (p.bias)
-        return p.lse ? launch_variant<true, true, false>(tq, tk, tv, tb, p, grid, stream)
-                     : launch_variant<true, false, false>(tq, tk, tv, tb, p, grid, stream);
-    return p.lse ? launch_variant<false, true, false>(tq, tk, tv, tb, p, grid, stream)
-                 : launch_variant<false, false, false>(tq, tk, tv, tb, p, grid, stream);
+    return p.head_dim == 64 ? launch_c<64>(tq, tk, tv, tb, p, grid, stream)
+                            : launch_c<32>(tq, tk, tv, tb, p, grid, stream);
 }
-
-int evo_max_bias_keys() { return kMaxBiasBoxes * 64; }
 
 } // namespace fl

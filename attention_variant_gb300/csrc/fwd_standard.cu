@@ -448,12 +448,18 @@ __device__ void pv_role(const KernelCtx<D> &cx, const StdParams &p, int t)
 // turn, then hands it to the other one.  Without the turns both warpgroups
 // run their exponentials at the same time on the same SM sub-partitions and
 // then both wait for their tensor-core chains; with them one slot's
-// exponentials overlap the other slot's Q K^T and P V (ping-pong).  Every work
-// item takes max(n_0, n_1) turns, n_t being slot t's tile count (0 for an
-// absent slot): the slot with fewer tiles takes empty turns, so both
-// warpgroups pass the turn the same number of times.  Turn k of warpgroup 1
-// follows warpgroup 0's turn k, turn k > 0 of warpgroup 0 follows warpgroup
-// 1's turn k - 1, and warpgroup 0's first turn is free.
+// exponentials overlap the other slot's Q K^T and P V (ping-pong).  Turn k of
+// a work item belongs to key tile lo + k of the union [lo, hi) of both slots'
+// tile ranges -- the order in which the K/V ring fills -- and every item takes
+// hi - lo turns: a slot takes an empty turn for a tile outside its own range,
+// so both warpgroups pass the turn the same number of times.  Indexing the
+// turns by the slot's own range instead deadlocks once one slot's range
+// starts at least a ring depth of tiles after the other's (a document that
+// begins in the second query block of an MHA pair): the later slot's first
+// tile could not enter the ring before the earlier slot released tiles that
+// it could only reach after the later slot's first turn.  Turn k of
+// warpgroup 1 follows warpgroup 0's turn k, turn k > 0 of warpgroup 0 follows
+// warpgroup 1's turn k - 1, and warpgroup 0's first turn is free.
 //
 // How the turn is passed depends on the score_mod (chosen by measurement):
 //  * plain scores: an mbarrier pair (a bounded wait, like every other wait);
@@ -490,13 +496,15 @@ __device__ __forceinline__ void drain_turns(const StdParams &p, int t, int64_t L
 {
     for (; L < p.grid.n_items; L += gridDim.x, k_from = 0) {
         const Item it = decode_item(p.grid, L);
-        int n_turns = 0;
+        int lo = 1 << 30, hi = 0;
 #pragma unroll
         for (int u = 0; u < 2; ++u)
             if (it.valid[u]) {
                 const TileRange r = q_block_range<kBN>(p.mask, it.b, it.qb[u] * BM);
-                n_turns = max(n_turns, r.hi - r.lo);
+                lo = min(lo, r.lo);
+                hi = max(hi, r.hi);
             }
+        const int n_turns = max(0, hi - lo);
         for (int k = k_from; k < n_turns; ++k) {
             nb_take(t);
             nb_pass(t);
@@ -546,13 +554,18 @@ __device__ void softmax_role(const KernelCtx<D> &cx, const StdParams &p, int t)
         tr.hi = inf.hi[t];
         tr.full_lo = inf.full_lo[t];
         tr.full_hi = inf.full_hi[t];
-        const int n_other = ((vbits >> (t ^ 1)) & 1) ? inf.hi[t ^ 1] - inf.lo[t ^ 1] : 0;
+        // the union of both slots' key-tile ranges: one turn per tile
+        int u_lo = mine ? tr.lo : 1 << 30, u_hi = mine ? tr.hi : 0;
+        if ((vbits >> (t ^ 1)) & 1) {
+            u_lo = min(u_lo, inf.lo[t ^ 1]);
+            u_hi = max(u_hi, inf.hi[t ^ 1]);
+        }
         __syncwarp();
         if (ptx::lane_id() == 0)
             ptx::mbar_arrive(bar(sm.info_empty[items & 1]));
         const int i = qb * BM + r;
         const int n_mine = mine ? tr.hi - tr.lo : 0;
-        const int n_turns = max(n_mine, n_other);
+        const int n_turns = max(0, u_hi - u_lo);
         int row_lo = 0, row_hi = 0;
         if (mine)
             row_interval(p.mask, b, i, row_lo, row_hi);
@@ -578,7 +591,9 @@ __device__ void softmax_role(const KernelCtx<D> &cx, const StdParams &p, int t)
         for (int k = 0; k < n_turns; ++k, ++turns) {
             const uint32_t phase = t == 1 ? turns : turns - 1;
             const bool free_turn = t == 0 && turns == 0; // warpgroup 0's first turn
-            if (k >= n_mine) {
+            const int j = u_lo + k;      // this turn's key tile
+            const int kk = j - tr.lo;    // its index in this slot's own range
+            if (!mine || kk < 0 || j >= tr.hi) {
                 // empty turn: pass the token on
                 if constexpr (kNamed) {
                     nb_take(t);
@@ -590,7 +605,6 @@ __device__ void softmax_role(const KernelCtx<D> &cx, const StdParams &p, int t)
                 }
                 continue;
             }
-            const int j = tr.lo + k;
             if (!warp_wait(bar(sm.s_full[t]), scount & 1, cx.wc, W_S_FULL)) {
                 if constexpr (!kNamed)
                     return;
@@ -618,9 +632,9 @@ __device__ void softmax_role(const KernelCtx<D> &cx, const StdParams &p, int t)
             uint32_t pk[kBN / 2];
             bool rescale;
             const float alpha =
-                C::kOnes ? softmax_compute_p_exact_sum<kBN>(x, MOD == MOD_NONE ? p.qk_log2 : 1.f, st, k == 0,
+                C::kOnes ? softmax_compute_p_exact_sum<kBN>(x, MOD == MOD_NONE ? p.qk_log2 : 1.f, st, kk == 0,
                                                             pk, rescale)
-                         : softmax_compute_p<kBN>(x, MOD == MOD_NONE ? p.qk_log2 : 1.f, st, k == 0, pk,
+                         : softmax_compute_p<kBN>(x, MOD == MOD_NONE ? p.qk_log2 : 1.f, st, kk == 0, pk,
                                                   rescale);
             if constexpr (kNamed) {
                 ptx::reg_fence<kBN / 2>(pk);
@@ -629,7 +643,7 @@ __device__ void softmax_role(const KernelCtx<D> &cx, const StdParams &p, int t)
             } else {
                 ptx::mbar_arrive(b_turn_other); // hand the turn over
             }
-            if (k > 0) {
+            if (kk > 0) {
                 // the previous tile's P V has consumed P[t] and landed in O[t]
                 if (!warp_wait(bar(sm.pv_done[t]), pvcount & 1, cx.wc, W_O_FULL)) {
                     if constexpr (!kNamed)

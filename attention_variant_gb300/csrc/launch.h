@@ -58,12 +58,13 @@ cudaError_t launch_diff(const CUtensorMap &tq, const CUtensorMap &tk, const CUte
                         const DiffParams &p, int grid, cudaStream_t stream);
 #endif
 
-// Parameters of the Evoformer kernel (c = 32) over a [batch, sequence, head, c]
+// Parameters of the Evoformer kernel (c = 32 or 64) over a [batch, sequence, head, c]
 // view: row pass batch = MSA row, sequence = residue; column pass the reverse.
 // Work items are (head, query block, chunk of `chunk` batch indices).
 struct EvoParams {
     GridSpec grid;          // B, Hq (= heads), nq used
     MaskSpec mask;          // kind NONE; S = length of the attended axis
+    int head_dim;           // c: 32 or 64
     int64_t n_items;
     int chunk;
     float qk_log2;          // scale * log2(e)
@@ -158,7 +159,6 @@ cudaError_t decode_static_scratch(void **ptr);
 
 cudaError_t launch_evo(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
                        const CUtensorMap &tb, const EvoParams &p, int grid, cudaStream_t stream);
-int evo_max_bias_keys();
 cudaError_t launch_bwd_prep(const BwdParams &p, cudaStream_t stream);
 // Dynamic shared memory and block count of the fused dK/dV + dQ launch.
 size_t bwd_smem_bytes();

@@ -145,8 +145,8 @@ def diff_entry(mask, Dv=None):
                 bytes=2 * (2 * 2 * B * S * H * D + B * S * H * Dv + B * S * H * Dv) + 4 * 2 * B * H * S)
 
 
-def evo_entry(row):
-    w = workloads.EVO
+def evo_entry(row, w=None):
+    w = w or workloads.EVO
     Ns, Nr, H, c = w["N_seq"], w["N_res"], w["H"], w["c"]
     B, S = (Ns, Nr) if row else (Nr, Ns)
     pairs = B * H * S * S
@@ -632,6 +632,8 @@ def cpu_baseline(e, seconds=12.0):
 
 ONLY = {"diff": lambda: diff_entry("none"), "diff_causal": lambda: diff_entry("causal"),
         "evo_row": lambda: evo_entry(True), "evo_col": lambda: evo_entry(False),
+        "evo_c64_row": lambda: evo_entry(True, workloads.EVO_C64),
+        "evo_c64_col": lambda: evo_entry(False, workloads.EVO_C64),
         "decode": lambda: decode_entry("none"), "decode_softcap": lambda: decode_entry("softcap"),
         "vanilla": lambda: entry("mha", 2048, "vanilla"), "causal": lambda: entry("mha", 2048, "causal"),
         "d128": lambda: entry("mha", 2048, "vanilla", D=128), "d32": lambda: entry("mha", 2048, "vanilla", D=32),
@@ -716,7 +718,7 @@ def run_ours(args):
     variants = {}
     if not args.headline_only:
         for e in [diff_entry("none"), diff_entry("causal"), diff_entry("none", Dv=64), evo_entry(True),
-                  evo_entry(False)]:
+                  evo_entry(False), evo_entry(True, workloads.EVO_C64), evo_entry(False, workloads.EVO_C64)]:
             vms = time_other(e, torch, fa, device, args.variant_steps, 2, flush, stream)
             vm = statistics.mean(vms)
             tf = e["flops"] / (vm * 1e-3) / 1e12
@@ -748,7 +750,7 @@ def run_ours(args):
                 tflops=round(e["flops"] / (vm * 1e-3) / 1e12, 1), ms=round(vm, 4), gbs=round(gbs, 1),
                 frac_hbm=round(gbs / peaks["hbm_gbs"], 4), l2=l2_policy(e))
         for e in all_entries() + [expr_entry(head["S"], n) for n in EXPR_VARIANTS] + head_dim_entries():
-            h = gpu_inputs(e, torch, device) if (e["S"], e["kind"]) != (head["S"], "mha") else host
+            h = host if e["name"] == head["name"] else gpu_inputs(e, torch, device)
             vms, _ = time_entry(e, h, torch, fa, device, args.variant_steps, 2, flush, stream)
             vm = statistics.mean(vms)
             tf = e["flops"] / (vm * 1e-3) / 1e12

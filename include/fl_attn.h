@@ -180,8 +180,9 @@ typedef struct {
  * lse is natural-log; its innermost stride must be 1.
  *
  * Supported shapes: STANDARD D = Dv in {32, 64, 128}; DIFF D = 64, Dv = 64
- * or 128 with mask none or causal; EVO c = 32, and for FL_KIND_EVO_ROW
- * N_res <= 384 (the bias rows of a query block are kept in shared memory).  Other shapes return
+ * or 128 with mask none or causal; EVO c = 32 or 64, any N_res (the row pass
+ * keeps a query block's bias rows in shared memory for c = 32 and N_res <= 384,
+ * and streams them per key tile otherwise).  Other shapes return
  * FL_ERR_UNSUPPORTED.  The bias may be passed with any strides obeying the
  * fl_tensor rules (for example a [N_res,N_res,H] tensor viewed as
  * [H,N_res,N_res]).  Evoformer sequence lengths must keep every stride a

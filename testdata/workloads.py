@@ -35,6 +35,9 @@ DIFF = dict(name="diff_b4_s4096_h16", B=4, S=4096, H=16, D=64, Dv=128, lam=0.8)
 
 # Evoformer MSA gated self-attention: N_seq=512, N_res=384, H=8, c=32.
 EVO = dict(name="evo_msa_s512_r384_h8_c32", N_seq=512, N_res=384, H=8, c=32)
+# The pages' Evoformer kernel benchmark head shape (4 heads of dimension 64; the
+# pages give no MSA size, so the c = 32 workload's MSA is used: same bytes).
+EVO_C64 = dict(name="evo_msa_s512_r384_h4_c64", N_seq=512, N_res=384, H=4, c=64)
 # A batch of AlphaFold2-sized MSA stacks (sequence length 256) with an MSA mask
 # shaped like padding: the last 26 residues and the last 12 MSA rows removed.
 EVO_AF2 = dict(name="evo_af2_b8_s128_r256_h8_c32", B=8, N_seq=128, N_res=256, H=8, c=32,

@@ -28,11 +28,11 @@ def _inputs(tag, Ns, Nr, H, c=32):
     return q, k, v, g, bias
 
 
-def run_evo(row, q, k, v, g, bias, bias_pitch=None):
+def run_evo(row, q, k, v, g, bias, bias_pitch=None, lse_on=True):
     Ns, Nr, H, c = q.shape
     B, S = (Ns, Nr) if row else (Nr, Ns)
     out = torch.full((Ns, Nr, H, c), float("nan"), dtype=torch.bfloat16, device="cuda")
-    lse = torch.full((B, H, S), float("nan"), dtype=torch.float32, device="cuda")
+    lse = torch.full((B, H, S), float("nan"), dtype=torch.float32, device="cuda") if lse_on else None
     cnt = torch.full((B, H, (S + 127) // 128), -1, dtype=torch.int32, device="cuda")
     err = torch.zeros(1, dtype=torch.int32, device="cuda")
     d = fa.make_desc(kind="evo_row" if row else "evo_col", debug_tile_counts=cnt, error_word=err)
@@ -47,7 +47,7 @@ def run_evo(row, q, k, v, g, bias, bias_pitch=None):
             bias_t = gu.dev(padded)[:, :, :Nr]
     fa.fl_attn_fwd(gu.dev(q), gu.dev(k), gu.dev(v), out, lse, d, bias=bias_t, gate=gu.dev(g))
     torch.cuda.synchronize()
-    return gu.f64(out), gu.f64(lse), cnt.cpu().numpy(), int(err.item())
+    return gu.f64(out), gu.f64(lse) if lse_on else None, cnt.cpu().numpy(), int(err.item())
 
 
 @pytest.mark.parametrize("Ns,Nr", [(4, 200), (3, 384), (5, 136)])
@@ -58,6 +58,48 @@ def test_evo_row_small(Ns, Nr):
     oref, lref = oracle.evo_row(q, k, v, bias, g)
     gu.compare(o, lse, oref, lref, what=f"evo row {Ns}x{Nr}")
     assert np.array_equal(cnt, gu.expected_tile_counts("none", Ns, 2, Nr))
+
+
+# c = 64 (the pages' Evoformer kernel benchmark: 4 heads of dimension 64;
+# bias streamed per key tile) and c = 32 with N_res > 384 (bias streamed)
+@pytest.mark.parametrize("Ns,Nr,c", [(4, 200, 64), (3, 384, 64), (3, 520, 32), (2, 712, 32),
+                                     (2, 600, 64)])
+def test_evo_row_streamed_bias(Ns, Nr, c):
+    q, k, v, g, bias = _inputs(f"evos{Ns}_{Nr}_{c}", Ns, Nr, 2, c)
+    o, lse, cnt, err = run_evo(True, q, k, v, g, bias)
+    assert err == 0
+    oref, lref = oracle.evo_row(q, k, v, bias, g)
+    gu.compare(o, lse, oref, lref, what=f"evo row {Ns}x{Nr} c{c}")
+    assert np.array_equal(cnt, gu.expected_tile_counts("none", Ns, 2, Nr))
+
+
+@pytest.mark.parametrize("Ns,Nr", [(200, 4), (130, 5)])
+def test_evo_col_c64(Ns, Nr):
+    q, k, v, g, _ = _inputs(f"evoc64_{Ns}_{Nr}", Ns, Nr, 2, 64)
+    o, lse, cnt, err = run_evo(False, q, k, v, g, None)
+    assert err == 0
+    oref, lref = oracle.evo_col(q, k, v, g)
+    gu.compare(o, lse, np.swapaxes(oref, 0, 1), lref, what=f"evo col c64 {Ns}x{Nr}")
+    assert np.array_equal(cnt, gu.expected_tile_counts("none", Nr, 2, Ns))
+
+
+@pytest.mark.parametrize("c", [32, 64])
+@pytest.mark.parametrize("row", [True, False], ids=["row", "col"])
+def test_evo_persistent_items_everywhere(row, c):
+    # several work items per CTA (odd chunks: one slot has a row fewer), and
+    # the LSE-free path the benchmark times, compared everywhere
+    Ns, Nr, H = (37, 256, 4) if row else (256, 37, 4)
+    q, k, v, g, bias = _inputs(f"evop{int(row)}_{c}", Ns, Nr, H, c)
+    for lse_on in (True, False):
+        o, lse, cnt, err = run_evo(row, q, k, v, g, bias if row else None, lse_on=lse_on)
+        assert err == 0
+        if row:
+            oref, lref = oracle.evo_row(q, k, v, bias, g)
+        else:
+            oref, lref = oracle.evo_col(q, k, v, g)
+            oref = np.swapaxes(oref, 0, 1)
+        gu.compare(o, lse, oref, lref if lse_on else None,
+                   what=f"evo persistent {'row' if row else 'col'} c{c} lse={lse_on}")
 
 
 def test_evo_row_ragged_padded_bias():
@@ -103,3 +145,21 @@ def test_evo_full_size(row):
         oref = np.swapaxes(oref, 0, 1)
     gu.compare(o, lse, oref, lref, what="evo full " + ("row" if row else "col"))
     assert np.array_equal(cnt, gu.expected_tile_counts("none", B, H, S))
+
+
+@pytest.mark.parametrize("row", [True, False], ids=["row", "col"])
+def test_evo_c64_kernel_benchmark_shape(row):
+    """The Evoformer kernel benchmark's head shape (4 heads of dimension 64)
+    at the MSA size of the c = 32 workload (N_seq 512, N_res 384), the whole
+    output against the oracle."""
+    w = workloads.EVO_C64
+    Ns, Nr, H, c = w["N_seq"], w["N_res"], w["H"], w["c"]
+    q, k, v, g, bias = _inputs(w["name"], Ns, Nr, H, c)
+    o, lse, cnt, err = run_evo(row, q, k, v, g, bias)
+    assert err == 0
+    if row:
+        oref, lref = oracle.evo_row(q, k, v, bias, g)
+    else:
+        oref, lref = oracle.evo_col(q, k, v, g)
+        oref = np.swapaxes(oref, 0, 1)
+    gu.compare(o, lse, oref, lref, what="evo c64 " + ("row" if row else "col"))

