@@ -179,10 +179,10 @@ __device__ void producer_role(const Ctx<C, BIAS> &cx, const EvoParams &p, const 
             }
             __syncwarp();
         }
-        const int steps[2] = {slot_rows(it, 0) * nkv, slot_rows(it, 1) * nkv};
-        const int n_steps = max(steps[0], steps[1]);
-        for (int st = 0; st < n_steps && ok; ++st) {
-            const int j = st % nkv;
+        const int rows[2] = {slot_rows(it, 0), slot_rows(it, 1)};
+        // steps (row n, key tile j) in order; slot 0 has at least slot 1's rows
+        for (int n = 0; n < rows[0] && ok; ++n)
+        for (int j = 0; j < nkv && ok; ++j) {
             if constexpr (BIAS == BIAS_STREAM) {
                 // this step's 128 x 128 bias tile, for both slots
                 const uint32_t bs = bias_count % kBiasStages;
@@ -200,9 +200,9 @@ __device__ void producer_role(const Ctx<C, BIAS> &cx, const EvoParams &p, const 
             }
 #pragma unroll
             for (int t = 0; t < 2; ++t) {
-                if (st >= steps[t])
+                if (n >= rows[t])
                     continue;
-                const int b = it.b0 + t + 2 * (st / nkv);
+                const int b = it.b0 + t + 2 * n;
                 if (j == 0) {
                     const uint32_t qbuf = q_count[t] & 1;
                     if (q_count[t] >= 2) {
@@ -273,13 +273,12 @@ __device__ void s_role(const Ctx<C, BIAS> &cx, const EvoParams &p)
     bool ok = true;
     for (int64_t L = blockIdx.x; L < p.n_items && ok; L += gridDim.x) {
         const EvoItem it = decode_evo(p, L);
-        const int steps[2] = {slot_rows(it, 0) * nkv, slot_rows(it, 1) * nkv};
-        const int n_steps = max(steps[0], steps[1]);
-        for (int st = 0; st < n_steps && ok; ++st) {
-            const int j = st % nkv;
+        const int rows[2] = {slot_rows(it, 0), slot_rows(it, 1)};
+        for (int n = 0; n < rows[0] && ok; ++n)
+        for (int j = 0; j < nkv && ok; ++j) {
 #pragma unroll
             for (int t = 0; t < 2; ++t) {
-                if (st >= steps[t])
+                if (n >= rows[t])
                     continue;
                 const uint32_t qbuf = q_count[t] & 1;
                 if (j == 0) {
@@ -345,18 +344,17 @@ __device__ void pv_role(const Ctx<C, BIAS> &cx, const EvoParams &p, int t)
     bool ok = true;
     for (int64_t L = blockIdx.x; L < p.n_items && ok; L += gridDim.x) {
         const EvoItem it = decode_evo(p, L);
-        const int steps[2] = {slot_rows(it, 0) * nkv, slot_rows(it, 1) * nkv};
-        const int n_steps = max(steps[0], steps[1]);
-        for (int st = 0; st < n_steps && ok; ++st) {
+        const int rows[2] = {slot_rows(it, 0), slot_rows(it, 1)};
+        for (int n = 0; n < rows[0] && ok; ++n)
+        for (int j = 0; j < nkv && ok; ++j) {
 #pragma unroll
             for (int u = 0; u < 2; ++u) {
-                if (st >= steps[u])
+                if (n >= rows[u])
                     continue;
                 if (u != t) {
                     ++kv_count; // the other slot's stage
                     continue;
                 }
-                const int j = st % nkv;
                 // the softmax has written P(j) and rescaled O: O += P V_j
                 ok = warp_wait(bar(sm.p_full[t]), pcount & 1, cx.wc, W_P_FULL);
                 if (!ok)
@@ -506,14 +504,17 @@ __device__ __forceinline__ void evo_rescale_o(uint32_t tO, const float (&alpha)[
         ptx::tmem_st_16x256b_x4(tO, o);
         ptx::tmem_st_16x256b_x2(tO + 32, o + 16);
     } else {
-        uint32_t o[32];
-        ptx::tmem_ld_16x256b_x8(tO, o);
-        ptx::tmem_wait_ld();
-        ptx::reg_fence<32>(o);
 #pragma unroll
-        for (int e = 0; e < 32; ++e)
-            o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha[(e >> 1) & 1]);
-        ptx::tmem_st_16x256b_x8(tO, o);
+        for (int h = 0; h < 2; ++h) { // 32 columns at a time
+            uint32_t o[16];
+            ptx::tmem_ld_16x256b_x4(tO + 32 * h, o);
+            ptx::tmem_wait_ld();
+            ptx::reg_fence<16>(o);
+#pragma unroll
+            for (int e = 0; e < 16; ++e)
+                o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha[(e >> 1) & 1]);
+            ptx::tmem_st_16x256b_x4(tO + 32 * h, o);
+        }
     }
 }
 
@@ -529,23 +530,16 @@ template <int C, bool LSE>
 __device__ __forceinline__ void evo_epilogue(const EvoParams &p, uint32_t tO, const PendingRow &pr, int jq,
                                              int nkv)
 {
-    constexpr int kChunks = C / 8;
-    uint32_t o[4 * kChunks];
     float inv[2];
     if constexpr (C == 32) {
         uint32_t sum[4];
-        ptx::tmem_ld_16x256b_x4(tO, o);
         ptx::tmem_ld_16x256b_x1(tO + 32, sum); // registers 0 and 2: the sums of R0 and R1
         ptx::tmem_wait_ld();
-        ptx::reg_fence<16>(o);
         ptx::reg_fence<4>(sum);
         const float s0 = __uint_as_float(sum[0]), s1 = __uint_as_float(sum[2]);
         inv[0] = s0 > 0.f ? 1.f / s0 : 0.f;
         inv[1] = s1 > 0.f ? 1.f / s1 : 0.f;
     } else {
-        ptx::tmem_ld_16x256b_x8(tO, o);
-        ptx::tmem_wait_ld();
-        ptx::reg_fence<32>(o);
         const float s0 = quad_sum(pr.st.lr[0]), s1 = quad_sum(pr.st.lr[1]);
         inv[0] = s0 > 0.f ? 1.f / s0 : 0.f;
         inv[1] = s1 > 0.f ? 1.f / s1 : 0.f;
@@ -555,27 +549,39 @@ __device__ __forceinline__ void evo_epilogue(const EvoParams &p, uint32_t tO, co
         lsum[0] = quad_sum(pr.st.l[0]);
         lsum[1] = quad_sum(pr.st.l[1]);
     }
+    // 32 output columns at a time (16 registers of the 16x256b layout)
+#pragma unroll
+    for (int c32 = 0; c32 < C / 32; ++c32) {
+        uint32_t o[16];
+        ptx::tmem_ld_16x256b_x4(tO + 32 * c32, o);
+        ptx::tmem_wait_ld();
+        ptx::reg_fence<16>(o);
+#pragma unroll
+        for (int k = 0; k < 2; ++k) {
+            const int i = pr.qb * BM + pr.r0 + 8 * k;
+            if (i >= p.mask.S)
+                continue;
+            const int64_t g_row = pr.b * p.g_sb + static_cast<int64_t>(i) * p.g_si + pr.h * p.g_sh;
+            const int64_t o_row = pr.b * p.o_sb + static_cast<int64_t>(i) * p.o_si + pr.h * p.o_sh;
+            const uint32_t *g32 = reinterpret_cast<const uint32_t *>(p.gate + g_row) + 16 * c32;
+            uint32_t *o32 = reinterpret_cast<uint32_t *>(p.out + o_row) + 16 * c32;
+#pragma unroll
+            for (int r = 0; r < 4; ++r) {
+                // columns 32 c32 + 8r + 2 jq and + 1: one 32-bit word of the row
+                const uint32_t gw = __ldg(g32 + 4 * r + jq); // prefetched into L1 when the row started
+                const float g0 = __uint_as_float(gw << 16), g1 = __uint_as_float(gw & 0xFFFF0000u);
+                // sigmoid(g) = 1/2 + tanh(g / 2) / 2 (one special-function op)
+                const float s0 = fmaf(0.5f, tanh_approx(0.5f * g0), 0.5f);
+                const float s1 = fmaf(0.5f, tanh_approx(0.5f * g1), 0.5f);
+                o32[4 * r + jq] = ptx::pack_bf16(__uint_as_float(o[4 * r + 2 * k]) * inv[k] * s0,
+                                                 __uint_as_float(o[4 * r + 2 * k + 1]) * inv[k] * s1);
+            }
+        }
+    }
 #pragma unroll
     for (int k = 0; k < 2; ++k) {
         const int i = pr.qb * BM + pr.r0 + 8 * k;
-        if (i >= p.mask.S)
-            continue;
-        const int64_t g_row = pr.b * p.g_sb + static_cast<int64_t>(i) * p.g_si + pr.h * p.g_sh;
-        const int64_t o_row = pr.b * p.o_sb + static_cast<int64_t>(i) * p.o_si + pr.h * p.o_sh;
-        const uint32_t *g32 = reinterpret_cast<const uint32_t *>(p.gate + g_row);
-        uint32_t *o32 = reinterpret_cast<uint32_t *>(p.out + o_row);
-#pragma unroll
-        for (int r = 0; r < kChunks; ++r) {
-            // columns 8r + 2 jq and 8r + 2 jq + 1: one 32-bit word of the row
-            const uint32_t gw = __ldg(g32 + 4 * r + jq); // prefetched into L1 when the row started
-            const float g0 = __uint_as_float(gw << 16), g1 = __uint_as_float(gw & 0xFFFF0000u);
-            // sigmoid(g) = 1/2 + tanh(g / 2) / 2 (one special-function op)
-            const float s0 = fmaf(0.5f, tanh_approx(0.5f * g0), 0.5f);
-            const float s1 = fmaf(0.5f, tanh_approx(0.5f * g1), 0.5f);
-            o32[4 * r + jq] = ptx::pack_bf16(__uint_as_float(o[4 * r + 2 * k]) * inv[k] * s0,
-                                             __uint_as_float(o[4 * r + 2 * k + 1]) * inv[k] * s1);
-        }
-        if (LSE && jq == 0)
+        if (LSE && jq == 0 && i < p.mask.S)
             p.lse[pr.b * p.l_sb + pr.h * p.l_sh + i] =
                 lsum[k] > 0.f ? (pr.st.m[k] + log2f(lsum[k])) * kLn2 : kNegInf;
     }
@@ -624,18 +630,18 @@ __device__ void softmax_role(const Ctx<C, BIAS> &cx, const EvoParams &p, int t, 
         const EvoItem it = decode_evo(p, L);
         if (BIAS == BIAS_RESIDENT && !warp_wait(bar(sm.bias_full[0]), item_count & 1, cx.wc, W_BIAS))
             return;
-        const int steps[2] = {slot_rows(it, 0) * nkv, slot_rows(it, 1) * nkv};
-        const int n_steps = max(steps[0], steps[1]);
+        const int rows0 = slot_rows(it, 0), my_rows = slot_rows(it, t);
         Rows2 st{{kNegInf, kNegInf}, {0.f, 0.f}, {0.f, 0.f}};
-        for (int stp = 0; stp < n_steps; ++stp) {
-            const int j = stp % nkv;
+        // the steps (row n, key tile j) of slot 0, which has at least this slot's rows
+        for (int n = 0; n < (BIAS == BIAS_STREAM ? rows0 : my_rows); ++n)
+        for (int j = 0; j < nkv; ++j) {
             uint32_t bias_base = 0;
             if constexpr (BIAS == BIAS_STREAM) {
                 const uint32_t bs = bias_count % kBiasStages;
                 if (!warp_wait(bar(sm.bias_full[bs]), (bias_count / kBiasStages) & 1, cx.wc, W_BIAS))
                     return;
                 ++bias_count;
-                if (stp >= steps[t]) {
+                if (n >= my_rows) {
                     // no row of this slot at this step: release the stage
                     __syncwarp();
                     if (lane == 0)
@@ -644,11 +650,9 @@ __device__ void softmax_role(const Ctx<C, BIAS> &cx, const EvoParams &p, int t, 
                 }
                 bias_base = bias_r0 + 2 * bs * kBiasBox;
             } else {
-                if (stp >= steps[t])
-                    break;
                 bias_base = bias_r0 + 2 * j * kBiasBox;
             }
-            const int b = it.b0 + t + 2 * (stp / nkv);
+            const int b = it.b0 + t + 2 * n;
             const int j0 = j * BN;
             // MSA mask of this batch index and key tile: lane l reads keys
             // j0 + 32 w + l (issued before the wait, used after it)

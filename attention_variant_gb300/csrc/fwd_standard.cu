@@ -588,28 +588,33 @@ __device__ void softmax_role(const KernelCtx<D> &cx, const StdParams &p, int t)
         }
 
         RowState st{kNegInf, 0.f, 0.f};
-        for (int k = 0; k < n_turns; ++k, ++turns) {
+        // Turns [k_first, k_first + n_mine) of the item's n_turns are this
+        // slot's own tiles tr.lo, tr.lo + 1, ...; the others are empty turns.
+        // The own tiles run in a loop of their own (indexed from 0, so its
+        // first iteration is the slot's first tile), the empty turns before
+        // and after it in two short loops.
+        const int k_first = mine ? tr.lo - u_lo : n_turns;
+        for (int k = 0; k < k_first; ++k, ++turns) {
+            // empty turn: pass the token on
+            if constexpr (kNamed) {
+                nb_take(t);
+                nb_pass(t);
+            } else {
+                if (!(t == 0 && turns == 0) && !warp_wait(b_turn_mine, (t == 1 ? turns : turns - 1) & 1, cx.wc,
+                                                          W_TURN))
+                    return;
+                ptx::mbar_arrive(b_turn_other);
+            }
+        }
+        for (int kk = 0; kk < n_mine; ++kk, ++turns) {
             const uint32_t phase = t == 1 ? turns : turns - 1;
             const bool free_turn = t == 0 && turns == 0; // warpgroup 0's first turn
-            const int j = u_lo + k;      // this turn's key tile
-            const int kk = j - tr.lo;    // its index in this slot's own range
-            if (!mine || kk < 0 || j >= tr.hi) {
-                // empty turn: pass the token on
-                if constexpr (kNamed) {
-                    nb_take(t);
-                    nb_pass(t);
-                } else {
-                    if (!free_turn && !warp_wait(b_turn_mine, phase & 1, cx.wc, W_TURN))
-                        return;
-                    ptx::mbar_arrive(b_turn_other);
-                }
-                continue;
-            }
+            const int j = tr.lo + kk;    // this turn's key tile
             if (!warp_wait(bar(sm.s_full[t]), scount & 1, cx.wc, W_S_FULL)) {
                 if constexpr (!kNamed)
                     return;
                 fail_L = L;
-                fail_k = k;
+                fail_k = k_first + kk;
                 goto aborted;
             }
             ++scount;
@@ -649,7 +654,7 @@ __device__ void softmax_role(const KernelCtx<D> &cx, const StdParams &p, int t)
                     if constexpr (!kNamed)
                         return;
                     fail_L = L;
-                    fail_k = k + 1;
+                    fail_k = k_first + kk + 1;
                     goto aborted;
                 }
                 ++pvcount;
@@ -660,6 +665,18 @@ __device__ void softmax_role(const KernelCtx<D> &cx, const StdParams &p, int t)
             store_p<kBN>(tP, pk);
             ptx::tc_fence_before();
             ptx::mbar_arrive(bar(sm.p_full[t]));
+        }
+        for (int k = k_first + n_mine; k < n_turns; ++k, ++turns) {
+            // empty turn: pass the token on
+            if constexpr (kNamed) {
+                nb_take(t);
+                nb_pass(t);
+            } else {
+                if (!(t == 0 && turns == 0) && !warp_wait(b_turn_mine, (t == 1 ? turns : turns - 1) & 1, cx.wc,
+                                                          W_TURN))
+                    return;
+                ptx::mbar_arrive(b_turn_other);
+            }
         }
         if (!mine)
             continue;
@@ -674,36 +691,43 @@ __device__ void softmax_role(const KernelCtx<D> &cx, const StdParams &p, int t)
         }
         ++pvcount;
         ptx::tc_fence_after();
-        float inv;
-        if constexpr (C::kOnes) {
-            uint32_t sum[1];
-            ptx::tmem_ld1(tO + C::kColSum, sum);
-            ptx::tmem_wait_ld();
-            ptx::reg_fence<1>(sum);
-            const float l_round = __uint_as_float(sum[0]);
-            inv = l_round > 0.f ? 1.f / l_round : 0.f;
-        } else {
-            inv = row_inv_norm(st);
-        }
-        // 32 output columns at a time (the TMEM loads are warp-collective, so
-        // every thread takes them; only rows inside the sequence store)
+        // up to 64 output columns per round: their TMEM loads (and, D <= 64, the
+        // sum column) issued together, one wait; the loads are warp-collective,
+        // so every thread takes them and only rows inside the sequence store
+        constexpr int kCols = D < 64 ? D : 64;
         uint4 *d4 = reinterpret_cast<uint4 *>(p.out + b * p.o_sb + static_cast<int64_t>(i) * p.o_ss +
                                               h * p.o_sh);
+        float inv = 0.f;
+        if constexpr (!C::kOnes)
+            inv = row_inv_norm(st);
 #pragma unroll
-        for (int c32 = 0; c32 < D / 32; ++c32) {
-            uint32_t o[32];
-            ptx::tmem_ld32(tO + 32 * c32, o);
-            ptx::tmem_wait_ld();
-            ptx::reg_fence<32>(o);
+        for (int round = 0; round < D / kCols; ++round) {
+            uint32_t o[kCols];
+#pragma unroll
+            for (int c32 = 0; c32 < kCols / 32; ++c32)
+                ptx::tmem_ld32(tO + round * kCols + 32 * c32, o + 32 * c32);
+            if constexpr (C::kOnes) {
+                uint32_t sum[1];
+                ptx::tmem_ld1(tO + C::kColSum, sum);
+                ptx::tmem_wait_ld();
+                ptx::reg_fence<1>(sum);
+                const float l_round = __uint_as_float(sum[0]);
+                inv = l_round > 0.f ? 1.f / l_round : 0.f;
+            } else {
+                ptx::tmem_wait_ld();
+            }
+#pragma unroll
+            for (int c32 = 0; c32 < kCols / 32; ++c32)
+                ptx::reg_fence<32>(o + 32 * c32);
             if (i < p.mask.S) {
 #pragma unroll
-                for (int c = 0; c < 4; ++c) {
+                for (int c = 0; c < kCols / 8; ++c) {
                     uint4 w;
                     w.x = ptx::pack_bf16(__uint_as_float(o[8 * c + 0]) * inv, __uint_as_float(o[8 * c + 1]) * inv);
                     w.y = ptx::pack_bf16(__uint_as_float(o[8 * c + 2]) * inv, __uint_as_float(o[8 * c + 3]) * inv);
                     w.z = ptx::pack_bf16(__uint_as_float(o[8 * c + 4]) * inv, __uint_as_float(o[8 * c + 5]) * inv);
                     w.w = ptx::pack_bf16(__uint_as_float(o[8 * c + 6]) * inv, __uint_as_float(o[8 * c + 7]) * inv);
-                    d4[4 * c32 + c] = w;
+                    d4[round * (kCols / 8) + c] = w;
                 }
             }
         }
