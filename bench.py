@@ -705,7 +705,7 @@ def run_ours(args):
     peaks = measured_peaks()
     achieved = head["flops"] / (statistics.mean(ms) * 1e-3) / 1e12
 
-    e2e_ms, h2d, d2h, copies = time_e2e(head, host, torch, fa, device, max(3, args.steps // 4),
+    e2e_ms, h2d, d2h, copies = time_e2e(head, host, torch, fa, device, max(3, args.steps),
                                         args.warmup, stream)
     e2e_ms = max_over_ranks(e2e_ms, world, device)
     # the pipelined step cannot beat its slowest stage: the upload, the
