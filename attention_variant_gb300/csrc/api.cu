@@ -423,7 +423,7 @@ fl_status fwd_diff(const fl_tensor *q, const fl_tensor *k, const fl_tensor *v,
         const uint64_t dims[5] = {uint64_t(D), uint64_t(S), uint64_t(Hk), uint64_t(B), 2};
         const uint64_t st[4] = {uint64_t(K.stride[2]) * 2, uint64_t(K.stride[3]) * 2,
                                 uint64_t(K.stride[1]) * 2, uint64_t(K.stride[0]) * 2};
-        const uint32_t box[5] = {64, 128, 1, 1, 1};
+        const uint32_t box[5] = {64, uint32_t(fl::diff_key_tile(int(Dv))), 1, 1, 1};
         if ((s = make_map(tk, K.ptr, 5, dims, st, box, CU_TENSOR_MAP_SWIZZLE_128B, "k")) != FL_OK)
             return s;
     }
@@ -431,7 +431,7 @@ fl_status fwd_diff(const fl_tensor *q, const fl_tensor *k, const fl_tensor *v,
         const uint64_t dims[4] = {uint64_t(Dv), uint64_t(S), uint64_t(Hk), uint64_t(B)};
         const uint64_t st[3] = {uint64_t(V.stride[1]) * 2, uint64_t(V.stride[2]) * 2,
                                 uint64_t(V.stride[0]) * 2};
-        const uint32_t box[4] = {64, 128, 1, 1};
+        const uint32_t box[4] = {64, uint32_t(fl::diff_key_tile(int(Dv))), 1, 1};
         if ((s = make_map(tv, V.ptr, 4, dims, st, box, CU_TENSOR_MAP_SWIZZLE_128B, "v")) != FL_OK)
             return s;
     }
@@ -1236,9 +1236,9 @@ fl_status fl_attn_tile_shape(const fl_attn_variant_desc *desc, int32_t head_dim,
             return fail(FL_ERR_UNSUPPORTED, "head_dim %d not supported for kind %d", head_dim,
                         desc->kind);
         break;
-    case FL_KIND_DIFF:
-        if (head_dim != 64)
-            return fail(FL_ERR_UNSUPPORTED, "head_dim %d not supported for kind %d", head_dim,
+    case FL_KIND_DIFF: // head_dim is the value head dimension Dv here (D is 64)
+        if (head_dim != 64 && head_dim != 128)
+            return fail(FL_ERR_UNSUPPORTED, "value head_dim %d not supported for kind %d", head_dim,
                         desc->kind);
         break;
     case FL_KIND_EVO_ROW:
@@ -1251,7 +1251,9 @@ fl_status fl_attn_tile_shape(const fl_attn_variant_desc *desc, int32_t head_dim,
         return fail(FL_ERR_INVALID_ARG, "unknown kind %d", desc->kind);
     }
     *block_m = fl::BM;
-    *block_n = desc->kind == FL_KIND_STANDARD ? fl::std_key_tile(head_dim) : fl::BN;
+    *block_n = desc->kind == FL_KIND_STANDARD ? fl::std_key_tile(head_dim)
+               : desc->kind == FL_KIND_DIFF   ? fl::diff_key_tile(head_dim)
+                                              : fl::BN;
     return ok();
 }
 

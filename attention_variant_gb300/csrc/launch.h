@@ -182,6 +182,9 @@ cudaError_t launch_bwd(const CUtensorMap &tq, const CUtensorMap &tdo, const CUte
 __host__ __device__ constexpr int std_key_tile(int D) { return D == 128 ? 64 : 112; }
 constexpr int kStdThreads = 384;
 constexpr int kStdRegs = 168;
+// Keys per K/V tile of the differential kernel for value head dimension Dv
+// (its TMEM budget: see fwd_diff.cu).
+__host__ __device__ constexpr int diff_key_tile(int dv) { return dv == 128 ? 80 : 112; }
 
 #ifndef __CUDACC_RTC__
 cudaError_t launch_standard(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,

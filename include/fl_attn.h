@@ -152,8 +152,9 @@ typedef struct {
     int32_t *debug_tile_counts; /* NULL, or device int32 [batch][heads][ceil(S/128)]: the
                                    number of key tiles each 128-row query block visited
                                    (key-tile width from fl_attn_tile_shape: 112 for the
-                                   standard kind at D = 32 and 64, 64 at D = 128, 128 for
-                                   the other kinds) */
+                                   standard kind at D = 32 and 64, 64 at D = 128; 112 for
+                                   the differential kind at Dv = 64, 80 at Dv = 128; 128
+                                   for the Evoformer kinds) */
     uint32_t *error_word;    /* NULL, or a device word the kernel ORs FL_DEVERR_* into */
     int32_t debug_inject;    /* fl_inject; 0 in normal use */
     uint32_t wait_timeout_us; /* bound of every device-side wait; 0 means 2,000,000 */
@@ -249,7 +250,9 @@ fl_status fl_attn_bwd(const fl_tensor *q, const fl_tensor *k, const fl_tensor *v
                       fl_stream_t stream);
 
 /* Query-block and key-tile sizes the kernel for `desc` uses (for the
- * visited-tile accounting).  Never touches the device. */
+ * visited-tile accounting).  `head_dim` is D for the standard and Evoformer
+ * kinds and the value head dimension Dv for FL_KIND_DIFF (whose D is 64).
+ * Never touches the device. */
 fl_status fl_attn_tile_shape(const fl_attn_variant_desc *desc, int32_t head_dim,
                              int32_t *block_m, int32_t *block_n);
 

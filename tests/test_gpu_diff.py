@@ -33,6 +33,11 @@ def _inputs(tag, B, S, H, Hk=None, D=64, Dv=128):
     return q, k, v
 
 
+def _bn(Dv):
+    """Keys per key tile of the differential kernel for value head dimension Dv."""
+    return fa.fl_attn_tile_shape(fa.make_desc(kind="diff"), Dv)[1]
+
+
 def run_diff(q, k, v, lam, mask="none"):
     _, B, S, H, D = q.shape
     Dv = v.shape[3]
@@ -55,7 +60,7 @@ def test_diff_small(S, mask):
     assert err == 0
     oref, lref = oracle.diff_attention(q, k, v, 0.8, mask=mask)
     gu.compare(o, lse, oref, lref, what=f"diff {S} {mask}")
-    exp = gu.expected_tile_counts(mask, 2, 3, S)
+    exp = gu.expected_tile_counts(mask, 2, 3, S, bn=_bn(128))
     assert np.array_equal(cnt, exp)
 
 
@@ -68,7 +73,7 @@ def test_diff_dv64(mask):
     assert err == 0
     oref, lref = oracle.diff_attention(q, k, v, 0.8, mask=mask)
     gu.compare(o, lse, oref, lref, what=f"diff dv64 {mask}")
-    assert np.array_equal(cnt, gu.expected_tile_counts(mask, 2, 3, 333))
+    assert np.array_equal(cnt, gu.expected_tile_counts(mask, 2, 3, 333, bn=_bn(64)))
 
 
 def test_diff_dv64_full_size():
@@ -83,7 +88,7 @@ def test_diff_dv64_full_size():
     o_s = np.stack([o[b, i, h] for b, h, i in rows])
     l_s = np.stack([[lse[s, b, h, i] for b, h, i in rows] for s in range(2)])
     gu.compare(o_s, l_s, oref, lref, what="diff dv64 full causal")
-    assert np.array_equal(cnt, gu.expected_tile_counts("causal", w["B"], w["H"], w["S"]))
+    assert np.array_equal(cnt, gu.expected_tile_counts("causal", w["B"], w["H"], w["S"], bn=_bn(64)))
 
 
 def test_diff_gqa_and_lambda_zero():
@@ -93,15 +98,30 @@ def test_diff_gqa_and_lambda_zero():
     gu.compare(o, lse, oref, lref, what="diff gqa lambda 0")
 
 
-def test_diff_persistent_items_everywhere():
-    # 320 work items: every CTA of the persistent grid runs two or more
-    q, k, v = _inputs("diffpersist", 4, 640, 16)
+@pytest.mark.parametrize("Dv", [64, 128])
+def test_diff_persistent_items_everywhere(Dv):
+    # 320 work items: every CTA of the persistent grid runs two or more, so the
+    # hand-over of both streams' O between items is exercised
+    q, k, v = _inputs(f"diffpersist{Dv}", 4, 640, 16, Dv=Dv)
     for mask in ("none", "causal"):
         o, lse, cnt, err = run_diff(q, k, v, 0.8, mask)
         assert err == 0
         oref, lref = oracle.diff_attention(q, k, v, 0.8, mask=mask)
-        gu.compare(o, lse, oref, lref, what=f"diff persistent {mask}")
-        assert np.array_equal(cnt, gu.expected_tile_counts(mask, 4, 16, 640))
+        gu.compare(o, lse, oref, lref, what=f"diff persistent dv{Dv} {mask}")
+        assert np.array_equal(cnt, gu.expected_tile_counts(mask, 4, 16, 640, bn=_bn(Dv)))
+
+
+@pytest.mark.parametrize("Dv", [64, 128])
+@pytest.mark.parametrize("S", [1, 80, 112, 1000])
+def test_diff_tile_edges(Dv, S):
+    # lengths at and off both key-tile widths (80 and 112 keys), a single row
+    q, k, v = _inputs(f"diffedge{S}", 1, S, 2, Dv=Dv)
+    for mask in ("none", "causal"):
+        o, lse, cnt, err = run_diff(q, k, v, 0.5, mask)
+        assert err == 0
+        oref, lref = oracle.diff_attention(q, k, v, 0.5, mask=mask)
+        gu.compare(o, lse, oref, lref, what=f"diff edge S{S} dv{Dv} {mask}")
+        assert np.array_equal(cnt, gu.expected_tile_counts(mask, 1, 2, S, bn=_bn(Dv)))
 
 
 @pytest.mark.parametrize("mask", ["none", "causal"])
@@ -113,4 +133,4 @@ def test_diff_full_size(mask):
     assert err == 0
     oref, lref = oracle.diff_attention(q, k, v, w["lam"], mask=mask)
     gu.compare(o, lse, oref, lref, what=f"diff full {mask}")
-    assert np.array_equal(cnt, gu.expected_tile_counts(mask, w["B"], w["H"], w["S"]))
+    assert np.array_equal(cnt, gu.expected_tile_counts(mask, w["B"], w["H"], w["S"], bn=_bn(128)))
