@@ -695,12 +695,6 @@ __device__ void softmax_role(const Ctx<C, BIAS> &cx, const EvoParams &p, int t, 
                     ptx::fma2(x[4 * r + 2], x[4 * r + 3], x[4 * r + 2], x[4 * r + 3], p.qk_scale, p.qk_scale,
                               __uint_as_float(w1 << 16), __uint_as_float(w1 & 0xFFFF0000u));
                 }
-                if constexpr (BIAS == BIAS_STREAM) {
-                    // the bias words are in registers (used above): release the stage
-                    __syncwarp();
-                    if (lane == 0)
-                        ptx::mbar_arrive(bar(sm.bias_empty[(bias_count - 1) % kBiasStages]));
-                }
             }
             if (j0 + BN > S) {
                 // keys past the sequence (a ragged last tile)
@@ -762,6 +756,17 @@ __device__ void softmax_role(const Ctx<C, BIAS> &cx, const EvoParams &p, int t, 
             ptx::tmem_wait_st();
             ptx::tc_fence_before();
             ptx::mbar_arrive(bar(sm.p_full[t]));
+            if constexpr (BIAS == BIAS_STREAM) {
+                // Release the bias stage only now: P, written to TMEM above,
+                // depends on every bias word this warp loaded, so those shared
+                // loads have completed.  (The arithmetic that consumes them is
+                // not ordered before a release placed right after the loads, so
+                // the loads of the last warp to arrive could still be in flight
+                // when the TMA refilled the stage.)
+                __syncwarp();
+                if (lane == 0)
+                    ptx::mbar_arrive(bar(sm.bias_empty[(bias_count - 1) % kBiasStages]));
+            }
             if (j + 1 == nkv) {
                 prev.b = b;
                 prev.h = it.h;
