@@ -142,6 +142,7 @@ def test_tile_shape(lib):
     assert fa.fl_attn_tile_shape(fa.make_desc(kind="diff"), 64) == (128, 112)
     assert fa.fl_attn_tile_shape(fa.make_desc(kind="diff"), 128) == (128, 80)
     assert fa.fl_attn_tile_shape(fa.make_desc(kind="evo_row"), 32) == (128, 128)
+    assert fa.fl_attn_tile_shape(fa.make_desc(kind="evo_col"), 64) == (128, 128)
     with pytest.raises(fa.FlAttnError):
         fa.fl_attn_tile_shape(fa.make_desc(), 48)
 
