@@ -103,80 +103,8 @@ __device__ __forceinline__ void apply_row_mask(float (&x)[N], int j0, int row_lo
             x[e] = kNegInf;
 }
 
-// Max update with lazy rescale of the DV fp32 output columns at tO, then
-// P = 2^(t - m) -> bf16 at tP (64 columns) and both sums.  `first` marks the
-// first tile of the row's range (O is not yet written: the P V product of that
-// tile overwrites it).  For MOD_NONE, x holds raw scores and `c` = scale *
-// log2 e; otherwise x holds log2-domain logits and `c` = 1.
-template <int DV>
-__device__ __forceinline__ void online_update_and_store_p(float (&x)[BN], float c, RowState &st,
-                                                          bool first, uint32_t tO, uint32_t tP)
-{
-    // four independent max chains (3-input max), then combine
-    float mc[4];
-#pragma unroll
-    for (int q = 0; q < 4; ++q)
-        mc[q] = fmaxf(x[2 * q], x[2 * q + 1]);
-#pragma unroll
-    for (int e = 8; e < BN; e += 8) {
-#pragma unroll
-        for (int q = 0; q < 4; ++q)
-            mc[q] = ptx::max3(mc[q], x[e + 2 * q], x[e + 2 * q + 1]);
-    }
-    const float mx = fmaxf(fmaxf(mc[0], mc[1]), fmaxf(mc[2], mc[3])) * c; // c > 0
-
-    if (first) {
-        st.m_ref = mx;
-    } else {
-        const bool need = mx > st.m_ref + kRescaleThreshold;
-        if (__any_sync(0xffffffffu, need)) {
-            const float m_new = fmaxf(st.m_ref, mx);
-            const float alpha = (m_new == kNegInf) ? 1.f : ptx::ex2(st.m_ref - m_new);
-#pragma unroll 1
-            for (int k = 0; k < DV / 16; ++k) {
-                uint32_t o[16];
-                ptx::tmem_ld16(tO + 16 * k, o);
-                ptx::tmem_wait_ld();
-                ptx::reg_fence<16>(o);
-#pragma unroll
-                for (int e = 0; e < 16; ++e)
-                    o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
-                ptx::tmem_st16(tO + 16 * k, o);
-            }
-            ptx::tmem_wait_st();
-            st.l *= alpha;
-            st.l_round *= alpha;
-            st.m_ref = m_new;
-        }
-    }
-    const float nmu = (st.m_ref == kNegInf) ? 0.f : -st.m_ref;
-    // four independent packed accumulators per sum keep the add chains short
-    float le[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-    float lr[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-    for (int k = 0; k < BN / 16; ++k) {
-        uint32_t pk[8];
-#pragma unroll
-        for (int e = 0; e < 8; ++e) {
-            float a0, a1;
-            ptx::fma2(a0, a1, x[16 * k + 2 * e], x[16 * k + 2 * e + 1], c, c, nmu, nmu);
-            const float p0 = ptx::ex2(a0);
-            const float p1 = ptx::ex2(a1);
-            pk[e] = ptx::pack_bf16(p0, p1);
-            const int q = 2 * (e & 3);
-            ptx::add2(le[q], le[q + 1], p0, p1);
-            ptx::add2(lr[q], lr[q + 1], __uint_as_float(pk[e] << 16),
-                      __uint_as_float(pk[e] & 0xFFFF0000u));
-        }
-        ptx::tmem_st8(tP + 8 * k, pk);
-    }
-    st.l += ((le[0] + le[1]) + (le[2] + le[3])) + ((le[4] + le[5]) + (le[6] + le[7]));
-    st.l_round += ((lr[0] + lr[1]) + (lr[2] + lr[3])) + ((lr[4] + lr[5]) + (lr[6] + lr[7]));
-    ptx::tmem_wait_st();
-}
-
-// The same step split in two so the caller can overlap the exponentials with
-// the P V product of the previous tile:
+// One tile's online-softmax step, in two parts so the caller can overlap the
+// exponentials with the P V product of the previous tile:
 //   softmax_compute_p: max, rescale decision, P (packed bf16 in registers)
 //                      and both sums; O is not touched;
 //   rescale_o + store_p: once the previous P V has completed.
@@ -278,47 +206,6 @@ __device__ __forceinline__ float softmax_compute_p_exact_sum(float (&x)[N], floa
         ptx::add2(le[q], le[q + 1], p0, p1);
     }
     st.l += ((le[0] + le[1]) + (le[2] + le[3])) + ((le[4] + le[5]) + (le[6] + le[7]));
-    return alpha;
-}
-
-// As softmax_compute_p_exact_sum, without any row sum (for kernels whose P V
-// product produces the rounded sum and whose caller needs no log-sum-exp).
-template <int N = BN>
-__device__ __forceinline__ float softmax_compute_p_no_sum(float (&x)[N], float c, RowState &st,
-                                                          bool first, uint32_t (&pk)[N / 2],
-                                                          bool &rescale)
-{
-    float mc[4];
-#pragma unroll
-    for (int q = 0; q < 4; ++q)
-        mc[q] = fmaxf(x[2 * q], x[2 * q + 1]);
-#pragma unroll
-    for (int e = 8; e < N; e += 8) {
-#pragma unroll
-        for (int q = 0; q < 4; ++q)
-            mc[q] = ptx::max3(mc[q], x[e + 2 * q], x[e + 2 * q + 1]);
-    }
-    const float mx = fmaxf(fmaxf(mc[0], mc[1]), fmaxf(mc[2], mc[3])) * c; // c > 0
-    float alpha = 1.f;
-    rescale = false;
-    if (first) {
-        st.m_ref = mx;
-    } else {
-        const bool need = mx > st.m_ref + kRescaleThreshold;
-        if (__any_sync(0xffffffffu, need)) {
-            const float m_new = fmaxf(st.m_ref, mx);
-            alpha = (m_new == kNegInf) ? 1.f : ptx::ex2(st.m_ref - m_new);
-            st.m_ref = m_new;
-            rescale = true;
-        }
-    }
-    const float nmu = (st.m_ref == kNegInf) ? 0.f : -st.m_ref;
-#pragma unroll
-    for (int e = 0; e < N / 2; ++e) {
-        float a0, a1;
-        ptx::fma2(a0, a1, x[2 * e], x[2 * e + 1], c, c, nmu, nmu);
-        pk[e] = ptx::pack_bf16(ptx::ex2(a0), ptx::ex2(a1));
-    }
     return alpha;
 }
 
