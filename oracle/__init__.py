@@ -333,3 +333,45 @@ def attention_bwd(q, k, v, dout, *, mod="none", softcap=20.0, alibi_slopes=None,
             dQ[b, :, h] = s * (dS @ K[b, :, kh])
             dK[b, :, kh] += s * (dS.T @ Q[b, :, h])
     return dQ, dK, dV
+
+
+def diff_attention_bwd(q, k, v, dout, lam, *, mask="none", scale=0.0):
+    """Gradients of differential attention, float64:
+    ``O = softmax(s Q1 K1^T + mask) V - lam softmax(s Q2 K2^T + mask) V``
+    for ``q [2,B,S,H,D]``, ``k [2,B,S,Hk,D]``, ``v [B,S,Hk,Dv]`` and
+    ``dout [B,S,H,Dv]`` (bf16 bits); returns ``dQ [2,B,S,H,D]``,
+    ``dK [2,B,S,Hk,D]``, ``dV [B,S,Hk,Dv]``.
+
+    The chain rule through both softmaxes, written out per (batch, head):
+    stream t has its own probability matrix P_t and the coefficient c_t
+    (1, then -lam) on its output, so dP_t = c_t dO V^T, dS_t = P_t (dP_t -
+    rowsum(P_t dP_t)), dQ_t = s dS_t K_t, dK_t = s dS_t^T Q_t, and the shared
+    V collects dV = sum_t c_t P_t^T dO.  (Differential attention is one of
+    the pages' complex variants, gist.science summary, "Results"; the backward
+    is the fused kernels' named next step, "Limitations and future work".)
+    """
+    wid = lambda x: (np.asarray(x, dtype=np.uint16).astype(np.uint32) << 16).view(np.float32) \
+        .astype(np.float64)
+    Q, K, V, dO = wid(q), wid(k), wid(v), wid(dout)
+    _, B, S, H, D = Q.shape
+    Hk = K.shape[3]
+    G = H // Hk
+    sc = scale if scale else 1.0 / np.sqrt(D)
+    coef = (1.0, -float(lam))
+    dQ = np.zeros_like(Q)
+    dK = np.zeros_like(K)
+    dV = np.zeros_like(V)
+    for b in range(B):
+        allowed = _allowed(mask, S, b, 0, 0, None)
+        for h in range(H):
+            kh = h // G
+            for t in range(2):
+                z = np.where(allowed, sc * (Q[t, b, :, h] @ K[t, b, :, kh].T), -np.inf)
+                e = np.exp(z - z.max(axis=1, keepdims=True))
+                P = e / e.sum(axis=1, keepdims=True)
+                dV[b, :, kh] += coef[t] * (P.T @ dO[b, :, h])
+                dP = coef[t] * (dO[b, :, h] @ V[b, :, kh].T)
+                dS = P * (dP - (P * dP).sum(axis=1, keepdims=True))
+                dQ[t, b, :, h] = sc * (dS @ K[t, b, :, kh])
+                dK[t, b, :, kh] += sc * (dS.T @ Q[t, b, :, h])
+    return dQ, dK, dV

@@ -590,6 +590,51 @@ def pin_backward(lib):
         _close(grad[idx], (up - down) / (2 * eps), atol=1e-7, what=f"finite difference {name}")
 
 
+def pin_diff_backward(lib):
+    """The differential backward against float64 autograd of the forward
+    written in torch (both softmaxes, one V; MHA and GQA, with and without the
+    causal mask, Dv 64 and 128, a non-default scale), and against two
+    reductions: lambda = 0 is the plain backward of stream one (stream two's
+    gradients vanish), and identical streams give (1 - lambda) times the plain
+    backward for dV and the two streams' dQ, dK in the ratio 1 : -lambda."""
+    for (B, S, H, Hk, D, Dv, mask, scale, lam) in [(2, 23, 2, 2, 16, 32, "none", 0.0, 0.8),
+                                                   (1, 31, 4, 2, 16, 16, "causal", 0.3, 0.5)]:
+        q, k = _rand((2, B, S, H, D), "dbq"), _rand((2, B, S, Hk, D), "dbk")
+        v, do = _rand((B, S, Hk, Dv), "dbv"), _rand((B, S, H, Dv), "dbdo")
+        dq, dk, dv = oracle.diff_attention_bwd(q, k, v, do, lam, mask=mask, scale=scale)
+        Q, K = (torch.from_numpy(_f64(x)).permute(0, 1, 3, 2, 4).requires_grad_(True) for x in (q, k))
+        V = torch.from_numpy(_f64(v)).permute(0, 2, 1, 3).requires_grad_(True)
+        sc = scale or 1.0 / math.sqrt(D)
+        Vr = V.repeat_interleave(H // Hk, dim=1)
+        out = 0
+        for t, c in ((0, 1.0), (1, -lam)):
+            z = sc * (Q[t] @ K[t].repeat_interleave(H // Hk, dim=1).transpose(-1, -2))
+            if mask == "causal":
+                z = z.masked_fill(~torch.ones(S, S, dtype=torch.bool).tril(), float("-inf"))
+            out = out + c * (torch.softmax(z, dim=-1) @ Vr)
+        out.backward(torch.from_numpy(_f64(do)).permute(0, 2, 1, 3))
+        _close(dq, Q.grad.permute(0, 1, 3, 2, 4).numpy(), atol=1e-10, what=f"diff backward dQ {mask}")
+        _close(dk, K.grad.permute(0, 1, 3, 2, 4).numpy(), atol=1e-10, what=f"diff backward dK {mask}")
+        _close(dv, V.grad.permute(0, 2, 1, 3).numpy(), atol=1e-10, what=f"diff backward dV {mask}")
+    # reductions, against the plain backward oracle
+    B, S, H, Hk, D = 1, 40, 2, 1, 16
+    q, k = _rand((2, B, S, H, D), "drq"), _rand((2, B, S, Hk, D), "drk")
+    v, do = _rand((B, S, Hk, D), "drv"), _rand((B, S, H, D), "drdo")
+    dq, dk, dv = oracle.diff_attention_bwd(q, k, v, do, 0.0, mask="causal")
+    pq, pk, pv = oracle.attention_bwd(q[0], k[0], v, do, mask="causal")
+    _close(dq[0], pq, atol=1e-12, what="diff backward lambda 0 dQ")
+    _close(dk[0], pk, atol=1e-12, what="diff backward lambda 0 dK")
+    _close(dv, pv, atol=1e-12, what="diff backward lambda 0 dV")
+    _close(dq[1], 0 * pq, atol=1e-12, what="diff backward lambda 0 stream two")
+    same_q, same_k = np.stack([q[0], q[0]]), np.stack([k[0], k[0]])
+    lam = 0.3
+    dq, dk, dv = oracle.diff_attention_bwd(same_q, same_k, v, do, lam, mask="causal")
+    _close(dv, (1 - lam) * pv, atol=1e-12, what="diff backward identical streams dV")
+    _close(dq[0], pq, atol=1e-12, what="diff backward identical streams dQ1")
+    _close(dq[1], -lam * pq, atol=1e-12, what="diff backward identical streams dQ2")
+    _close(dk[1], -lam * pk, atol=1e-12, what="diff backward identical streams dK2")
+
+
 def pin_backward_expr(lib):
     """The backward with a score_mod expression: expressions that restate the
     built-in variants give the built-in backward, and the forward-mode
@@ -670,4 +715,5 @@ def pin_score_expr(lib):
 ALL_PINS = [pin_constant_scores, pin_alibi_geometric, pin_softcap_two_keys, pin_one_hot,
             pin_rows_sum_to_one, pin_shift_invariance, pin_permutation, pin_causal_row0,
             pin_sdpa, pin_reductions, pin_rows_api, pin_composed_rows, pin_diff, pin_evo, pin_fully_masked_row,
-            pin_decode, pin_key_mask, pin_score_expr, pin_backward, pin_backward_expr]
+            pin_decode, pin_key_mask, pin_score_expr, pin_backward, pin_backward_expr,
+            pin_diff_backward]

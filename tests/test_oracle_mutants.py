@@ -118,6 +118,34 @@ def test_bwd_mutant_is_caught(name, monkeypatch):
         oracle_pins.pin_backward(oracle.load())
 
 
+# Mistakes planted in the differential backward oracle.
+DIFF_BWD_MUTANTS = {
+    "diff_bwd_lambda_sign": ("coef = (1.0, -float(lam))", "coef = (1.0, float(lam))"),
+    "diff_bwd_dv_one_stream": ("dV[b, :, kh] += coef[t] * (P.T @ dO[b, :, h])",
+                               "dV[b, :, kh] += (P.T @ dO[b, :, h]) if t == 0 else 0.0"),
+    "diff_bwd_streams_share_k": ("z = np.where(allowed, sc * (Q[t, b, :, h] @ K[t, b, :, kh].T), -np.inf)",
+                                 "z = np.where(allowed, sc * (Q[t, b, :, h] @ K[0, b, :, kh].T), -np.inf)"),
+    "diff_bwd_dk_from_other_q": ("dK[t, b, :, kh] += sc * (dS.T @ Q[t, b, :, h])",
+                                 "dK[t, b, :, kh] += sc * (dS.T @ Q[1 - t, b, :, h])"),
+    "diff_bwd_no_coef_in_dp": ("dP = coef[t] * (dO[b, :, h] @ V[b, :, kh].T)", "dP = dO[b, :, h] @ V[b, :, kh].T"),
+}
+
+
+@pytest.mark.parametrize("name", sorted(DIFF_BWD_MUTANTS))
+def test_diff_bwd_mutant_is_caught(name, monkeypatch):
+    import inspect
+    import textwrap
+
+    src = textwrap.dedent(inspect.getsource(oracle.diff_attention_bwd))
+    a, b = DIFF_BWD_MUTANTS[name]
+    assert a in src, name
+    ns = dict(vars(oracle))
+    exec(compile(src.replace(a, b), "<mutant>", "exec"), ns)
+    monkeypatch.setattr(oracle, "diff_attention_bwd", ns["diff_attention_bwd"])
+    with pytest.raises((AssertionError, ValueError, IndexError)):
+        oracle_pins.pin_diff_backward(oracle.load())
+
+
 ALLOWED_MUTANTS = {
     "allowed_window_inclusive": ("(i - j < window)", "(i - j <= window)"),
     "allowed_prefix_inclusive": ("(j < prefix)", "(j <= prefix)"),
