@@ -7,7 +7,8 @@ is missing, importing the binding's entry points raises.
 The names mirror the C ABI: :func:`fl_attn_fwd`, :func:`fl_attn_tile_shape`,
 :func:`fl_attn_status_string`, :func:`fl_attn_last_error`,
 :func:`fl_attn_version`, :func:`fl_attn_decode_workspace_size`,
-:func:`fl_attn_decode`, :func:`fl_attn_decode_static`.  Tensors are torch tensors on the current CUDA device
+:func:`fl_attn_decode`, :func:`fl_attn_decode_static`, :func:`fl_attn_bwd`,
+:func:`fl_attn_diff_bwd`.  Tensors are torch tensors on the current CUDA device
 (PyTorch provides device memory and streams; nothing else).
 """
 from __future__ import annotations
@@ -121,6 +122,12 @@ def load_library(path: str = LIB_PATH):
     lib.fl_attn_bwd.restype = ctypes.c_int
     lib.fl_attn_bwd.argtypes = [P(FlTensor)] * 9 + [P(FlDesc), ctypes.c_void_p, ctypes.c_size_t,
                                                     ctypes.c_void_p]
+    lib.fl_attn_diff_bwd_workspace_size.restype = ctypes.c_int
+    lib.fl_attn_diff_bwd_workspace_size.argtypes = [P(FlTensor), P(FlTensor), P(FlTensor), P(FlDesc),
+                                                    P(ctypes.c_size_t)]
+    lib.fl_attn_diff_bwd.restype = ctypes.c_int
+    lib.fl_attn_diff_bwd.argtypes = [P(FlTensor)] * 8 + [P(FlDesc), ctypes.c_void_p, ctypes.c_size_t,
+                                                         ctypes.c_void_p]
     lib.fl_attn_evoformer.restype = ctypes.c_int
     lib.fl_attn_evoformer.argtypes = [P(FlTensor), P(FlTensor), P(FlTensor), P(FlTensor), P(FlTensor),
                                       P(FlDesc), P(FlTensor), P(FlTensor), P(FlTensor), ctypes.c_void_p]
@@ -222,6 +229,34 @@ def fl_attn_bwd(q, k, v, out, lse, dout, dq, dk, dv, desc: FlDesc, workspace, st
     st = lib.fl_attn_bwd(*[_ref(x) for x in t], ctypes.byref(desc),
                          ctypes.c_void_p(workspace.data_ptr()),
                          workspace.numel() * workspace.element_size(), ctypes.c_void_p(stream))
+    if st != FL_OK:
+        raise FlAttnError(st, fl_attn_last_error())
+
+
+def fl_attn_diff_bwd_workspace_size(q, k, v, desc: FlDesc) -> int:
+    """Bytes of workspace fl_attn_diff_bwd needs for these shapes."""
+    lib = load_library()
+    n = ctypes.c_size_t()
+    st = lib.fl_attn_diff_bwd_workspace_size(_ref(as_fl_tensor(q)), _ref(as_fl_tensor(k)), _ref(as_fl_tensor(v)),
+                                             ctypes.byref(desc), ctypes.byref(n))
+    if st != FL_OK:
+        raise FlAttnError(st, fl_attn_last_error())
+    return n.value
+
+
+def fl_attn_diff_bwd(q, k, v, lse, dout, dq, dk, dv, desc: FlDesc, workspace, stream=None) -> None:
+    """Enqueue the differential backward (see include/fl_attn.h); workspace is
+    a device torch tensor of at least fl_attn_diff_bwd_workspace_size bytes."""
+    lib = load_library()
+    if stream is None:
+        import torch
+        stream = torch.cuda.current_stream().cuda_stream
+    elif hasattr(stream, "cuda_stream"):
+        stream = stream.cuda_stream
+    t = [as_fl_tensor(x) for x in (q, k, v, lse, dout, dq, dk, dv)]
+    st = lib.fl_attn_diff_bwd(*[_ref(x) for x in t], ctypes.byref(desc),
+                              ctypes.c_void_p(workspace.data_ptr()),
+                              workspace.numel() * workspace.element_size(), ctypes.c_void_p(stream))
     if st != FL_OK:
         raise FlAttnError(st, fl_attn_last_error())
 

@@ -863,6 +863,107 @@ fl_status bwd_plan(const fl_tensor *q, const fl_tensor *k, const fl_tensor *v,
     return FL_OK;
 }
 
+// ------------------------------------------------------------------ differential backward
+
+// A bf16 [d0, d1, d2, d3] view at `ptr` with the given element strides (the
+// innermost one 1), as the library's own entry points take it.
+fl_tensor view4(void *ptr, int dtype, const int64_t (&size)[4], const int64_t (&stride)[3])
+{
+    fl_tensor t{};
+    t.ptr = ptr;
+    t.dtype = static_cast<fl_dtype>(dtype);
+    t.ndim = 4;
+    for (int d = 0; d < 4; ++d)
+        t.sizes[d] = size[d];
+    for (int d = 0; d < 3; ++d)
+        t.strides[d] = stride[d];
+    t.strides[3] = 1;
+    return t;
+}
+
+fl_tensor view3(void *ptr, int dtype, const int64_t (&size)[3], const int64_t (&stride)[2])
+{
+    fl_tensor t{};
+    t.ptr = ptr;
+    t.dtype = static_cast<fl_dtype>(dtype);
+    t.ndim = 3;
+    for (int d = 0; d < 3; ++d)
+        t.sizes[d] = size[d];
+    t.strides[0] = stride[0];
+    t.strides[1] = stride[1];
+    t.strides[2] = 1;
+    return t;
+}
+
+// Shapes, the desc the standard kind's kernels run with, and the workspace
+// layout of the differential backward: one recomputed O half, the bf16
+// partial gradients of every (stream, value half), and the standard
+// backward's own workspace (reused by each of its runs).
+struct DiffBwdPlan {
+    View Q, K, V;
+    int64_t B, S, H, Hk, Dv, halves;
+    fl_attn_variant_desc sd; // the standard kind's desc for the inner calls
+    size_t unit_q, unit_k;   // bytes of one [B, S, H, 64] / [B, S, Hk, 64] bf16 buffer
+    size_t off_o, off_dq, off_dk, off_dv, off_ws, ws_bytes, total;
+};
+
+fl_status diff_bwd_plan(const fl_tensor *q, const fl_tensor *k, const fl_tensor *v,
+                        const fl_attn_variant_desc *d, DiffBwdPlan &pl)
+{
+    fl_status s;
+    if (!d)
+        return fail(FL_ERR_INVALID_ARG, "desc is NULL");
+    if (d->kind != FL_KIND_DIFF)
+        return fail(FL_ERR_INVALID_ARG, "fl_attn_diff_bwd takes FL_KIND_DIFF");
+    if ((s = check_tensor(q, "q", 5, FL_BF16, pl.Q)) != FL_OK) return s;
+    if ((s = check_tensor(k, "k", 5, FL_BF16, pl.K)) != FL_OK) return s;
+    if ((s = check_tensor(v, "v", 4, FL_BF16, pl.V)) != FL_OK) return s;
+    if (pl.Q.size[0] != 2 || pl.K.size[0] != 2)
+        return fail(FL_ERR_INVALID_ARG, "q and k need a leading stream axis of size 2");
+    pl.B = pl.Q.size[1];
+    pl.S = pl.Q.size[2];
+    pl.H = pl.Q.size[3];
+    pl.Hk = pl.K.size[3];
+    pl.Dv = pl.V.size[3];
+    if (!(pl.K.size[1] == pl.B && pl.K.size[2] == pl.S && pl.K.size[4] == pl.Q.size[4]))
+        return fail(FL_ERR_INVALID_ARG, "k must be [2, B, S, Hk, D] matching q");
+    if (!same(pl.V, {pl.B, pl.S, pl.Hk, pl.Dv}))
+        return fail(FL_ERR_INVALID_ARG, "v must be [B, S, Hk, Dv]");
+    if (pl.H % pl.Hk != 0)
+        return fail(FL_ERR_INVALID_ARG, "H must be a multiple of Hk");
+    if (d->gqa_group != 0 && d->gqa_group != pl.H / pl.Hk)
+        return fail(FL_ERR_INVALID_ARG, "gqa_group does not match H / Hk");
+    if (pl.Q.size[4] != 64 || (pl.Dv != 64 && pl.Dv != 128))
+        return fail(FL_ERR_UNSUPPORTED, "the differential backward supports D = 64, Dv = 64 or 128");
+    if (d->mask != FL_MASK_NONE && d->mask != FL_MASK_CAUSAL)
+        return fail(FL_ERR_UNSUPPORTED, "differential attention takes no mask or causal");
+    if (d->score_mod != FL_MOD_NONE)
+        return fail(FL_ERR_UNSUPPORTED, "differential attention takes no score_mod");
+    if (!std::isfinite(d->scale) || d->scale < 0.f || !std::isfinite(d->diff_lambda))
+        return fail(FL_ERR_INVALID_ARG, "scale must be finite and positive, diff_lambda finite");
+    pl.halves = pl.Dv / 64;
+    pl.sd = fl_attn_variant_desc{};
+    pl.sd.kind = FL_KIND_STANDARD;
+    pl.sd.score_mod = FL_MOD_NONE;
+    pl.sd.mask = d->mask;
+    pl.sd.gqa_group = 0;
+    pl.sd.scale = d->scale;
+    pl.sd.error_word = d->error_word;
+    pl.sd.wait_timeout_us = d->wait_timeout_us;
+    const auto up = [](size_t x) { return (x + 255) / 256 * 256; };
+    pl.unit_q = up(size_t(pl.B) * pl.S * pl.H * 64 * 2);
+    pl.unit_k = up(size_t(pl.B) * pl.S * pl.Hk * 64 * 2);
+    pl.off_o = 0;
+    pl.off_dq = pl.off_o + pl.unit_q;
+    pl.off_dk = pl.off_dq + 2 * pl.halves * pl.unit_q;
+    pl.off_dv = pl.off_dk + 2 * pl.halves * pl.unit_k;
+    pl.off_ws = pl.off_dv + 2 * pl.halves * pl.unit_k;
+    const int64_t S_pad = (pl.S + 127) / 128 * 128; // as the standard backward sizes its own
+    pl.ws_bytes = up(size_t(pl.B) * size_t(pl.H) * size_t(S_pad) * sizeof(fl::BwdRowStat));
+    pl.total = pl.off_ws + pl.ws_bytes;
+    return FL_OK;
+}
+
 } // namespace
 
 extern "C" {
@@ -1008,6 +1109,137 @@ fl_status fl_attn_bwd(const fl_tensor *q, const fl_tensor *k, const fl_tensor *v
     const cudaError_t e = fl::launch_bwd(tq, tdo, tk, tv, tq128, tdo128, tk128, tv128, p, st);
     if (e != cudaSuccess)
         return fail(FL_ERR_CUDA, "kernel launch failed: %s", cudaGetErrorString(e));
+    return ok();
+}
+
+fl_status fl_attn_diff_bwd_workspace_size(const fl_tensor *q, const fl_tensor *k, const fl_tensor *v,
+                                          const fl_attn_variant_desc *desc, size_t *bytes)
+{
+    if (!bytes)
+        return fail(FL_ERR_INVALID_ARG, "bytes is NULL");
+    DiffBwdPlan pl;
+    const fl_status s = diff_bwd_plan(q, k, v, desc, pl);
+    if (s != FL_OK)
+        return s;
+    *bytes = pl.total;
+    return ok();
+}
+
+fl_status fl_attn_diff_bwd(const fl_tensor *q, const fl_tensor *k, const fl_tensor *v,
+                           const fl_tensor *lse, const fl_tensor *dout, const fl_tensor *dq,
+                           const fl_tensor *dk, const fl_tensor *dv, const fl_attn_variant_desc *desc,
+                           void *workspace, size_t workspace_bytes, fl_stream_t stream)
+{
+    DiffBwdPlan pl;
+    fl_status s = diff_bwd_plan(q, k, v, desc, pl);
+    if (s != FL_OK)
+        return s;
+    View L, DO, DQ, DK, DV;
+    if ((s = check_tensor(lse, "lse", 4, FL_F32, L)) != FL_OK) return s;
+    if ((s = check_tensor(dout, "dout", 4, FL_BF16, DO)) != FL_OK) return s;
+    if ((s = check_tensor(dq, "dq", 5, FL_BF16, DQ)) != FL_OK) return s;
+    if ((s = check_tensor(dk, "dk", 5, FL_BF16, DK)) != FL_OK) return s;
+    if ((s = check_tensor(dv, "dv", 4, FL_BF16, DV)) != FL_OK) return s;
+    if (!same(L, {2, pl.B, pl.H, pl.S}))
+        return fail(FL_ERR_INVALID_ARG, "lse must be [2, B, H, S]");
+    if (!same(DO, {pl.B, pl.S, pl.H, pl.Dv}))
+        return fail(FL_ERR_INVALID_ARG, "dout must be [B, S, H, Dv]");
+    if (!same(DQ, {2, pl.B, pl.S, pl.H, 64}))
+        return fail(FL_ERR_INVALID_ARG, "dq must be [2, B, S, H, 64]");
+    if (!same(DK, {2, pl.B, pl.S, pl.Hk, 64}))
+        return fail(FL_ERR_INVALID_ARG, "dk must be [2, B, S, Hk, 64]");
+    if (!same(DV, {pl.B, pl.S, pl.Hk, pl.Dv}))
+        return fail(FL_ERR_INVALID_ARG, "dv must be [B, S, Hk, Dv]");
+    if (!workspace)
+        return fail(FL_ERR_INVALID_ARG, "workspace is NULL");
+    if (reinterpret_cast<uintptr_t>(workspace) % kWsAlign)
+        return fail(FL_ERR_ALIGNMENT, "workspace is not %zu-byte aligned", kWsAlign);
+    if (workspace_bytes < pl.total)
+        return fail(FL_ERR_INVALID_ARG, "workspace holds %zu bytes, %zu needed", workspace_bytes, pl.total);
+    int dev;
+    DeviceInfo info;
+    if ((s = device_info(dev, info)) != FL_OK)
+        return s;
+
+    uint8_t *ws = static_cast<uint8_t *>(workspace);
+    const auto bf = [](void *base, int64_t elems) {
+        return static_cast<void *>(static_cast<__nv_bfloat16 *>(base) + elems);
+    };
+    const int64_t B = pl.B, S = pl.S, H = pl.H, Hk = pl.Hk;
+    const int64_t packed_q[3] = {S * H * 64, H * 64, 64}, packed_k[3] = {S * Hk * 64, Hk * 64, 64};
+    const float coef[2] = {1.f, -desc->diff_lambda};
+    // The views below only re-address tensors validated above (a stream's
+    // slice, a 64-column half, a workspace buffer), so the inner calls cannot
+    // fail validation after an earlier one has launched.
+    for (int t = 0; t < 2; ++t) {
+        const fl_tensor qt = view4(bf(pl.Q.ptr, t * pl.Q.stride[0]), FL_BF16, {B, S, H, 64},
+                                   {pl.Q.stride[1], pl.Q.stride[2], pl.Q.stride[3]});
+        const fl_tensor kt = view4(bf(pl.K.ptr, t * pl.K.stride[0]), FL_BF16, {B, S, Hk, 64},
+                                   {pl.K.stride[1], pl.K.stride[2], pl.K.stride[3]});
+        const fl_tensor lt = view3(static_cast<float *>(L.ptr) + t * L.stride[0], FL_F32, {B, H, S},
+                                   {L.stride[1], L.stride[2]});
+        for (int64_t hv = 0; hv < pl.halves; ++hv) {
+            const fl_tensor vh = view4(bf(pl.V.ptr, 64 * hv), FL_BF16, {B, S, Hk, 64},
+                                       {pl.V.stride[0], pl.V.stride[1], pl.V.stride[2]});
+            const fl_tensor doh = view4(bf(DO.ptr, 64 * hv), FL_BF16, {B, S, H, 64},
+                                        {DO.stride[0], DO.stride[1], DO.stride[2]});
+            const fl_tensor oh = view4(ws + pl.off_o, FL_BF16, {B, S, H, 64}, packed_q);
+            const size_t part = size_t(2 * hv + t); // partial buffers in (half, stream) order
+            const fl_tensor gq = view4(ws + pl.off_dq + part * pl.unit_q, FL_BF16, {B, S, H, 64}, packed_q);
+            const fl_tensor gk = view4(ws + pl.off_dk + part * pl.unit_k, FL_BF16, {B, S, Hk, 64}, packed_k);
+            const fl_tensor gv = view4(ws + pl.off_dv + part * pl.unit_k, FL_BF16, {B, S, Hk, 64}, packed_k);
+            // this stream's output over this half of V, then its backward with dO
+            if ((s = fwd_standard(&qt, &kt, &vh, &oh, nullptr, &pl.sd, nullptr, nullptr,
+                                  reinterpret_cast<cudaStream_t>(stream))) != FL_OK)
+                return s;
+            if ((s = fl_attn_bwd(&qt, &kt, &vh, &oh, &lt, &doh, &gq, &gk, &gv, &pl.sd, ws + pl.off_ws,
+                                 pl.ws_bytes, stream)) != FL_OK)
+                return s;
+        }
+    }
+    // dQ_t = c_t sum over halves, dK_t likewise, dV half = sum_t c_t dV_t
+    const cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    const auto part_ptr = [&](size_t off, size_t unit, int64_t hv, int t) {
+        return reinterpret_cast<const __nv_bfloat16 *>(ws + off + size_t(2 * hv + t) * unit);
+    };
+    for (int t = 0; t < 2; ++t) {
+        for (int which = 0; which < 2; ++which) { // dQ, dK
+            const View &Out = which == 0 ? DQ : DK;
+            const int64_t heads = which == 0 ? H : Hk;
+            fl::DiffCombine c{};
+            c.rows = B * S * heads;
+            c.S = S;
+            c.heads = heads;
+            for (int64_t hv = 0; hv < pl.halves; ++hv) {
+                c.in[hv] = which == 0 ? part_ptr(pl.off_dq, pl.unit_q, hv, t) : part_ptr(pl.off_dk, pl.unit_k, hv, t);
+                c.coef[hv] = coef[t];
+            }
+            c.out = static_cast<__nv_bfloat16 *>(Out.ptr) + t * Out.stride[0];
+            c.o_sb = Out.stride[1];
+            c.o_ss = Out.stride[2];
+            c.o_sh = Out.stride[3];
+            const cudaError_t e = fl::launch_diff_bwd_combine(c, info.sm_count, st);
+            if (e != cudaSuccess)
+                return fail(FL_ERR_CUDA, "kernel launch failed: %s", cudaGetErrorString(e));
+        }
+    }
+    for (int64_t hv = 0; hv < pl.halves; ++hv) {
+        fl::DiffCombine c{};
+        c.rows = B * S * Hk;
+        c.S = S;
+        c.heads = Hk;
+        for (int t = 0; t < 2; ++t) {
+            c.in[t] = part_ptr(pl.off_dv, pl.unit_k, hv, t);
+            c.coef[t] = coef[t];
+        }
+        c.out = static_cast<__nv_bfloat16 *>(DV.ptr) + 64 * hv;
+        c.o_sb = DV.stride[0];
+        c.o_ss = DV.stride[1];
+        c.o_sh = DV.stride[2];
+        const cudaError_t e = fl::launch_diff_bwd_combine(c, info.sm_count, st);
+        if (e != cudaSuccess)
+            return fail(FL_ERR_CUDA, "kernel launch failed: %s", cudaGetErrorString(e));
+    }
     return ok();
 }
 

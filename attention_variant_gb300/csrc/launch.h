@@ -120,6 +120,17 @@ struct BwdParams {
     uint64_t timeout_ns;
 };
 
+// ---- backward of the differential kind (bwd_diff.cu): the combining step
+// out[row, 0:64] = sum_p coef[p] in_p[row, 0:64] (fp32 sum of bf16 partials);
+// row = (b * S + position) * heads + head of the output view.
+struct DiffCombine {
+    int64_t rows, S, heads;
+    const __nv_bfloat16 *in[2]; // contiguous [rows][64]; in[1] may be null
+    float coef[2];
+    __nv_bfloat16 *out;         // element strides (batch, position, head); 64 columns contiguous
+    int64_t o_sb, o_ss, o_sh;
+};
+
 // ---- serving with a KV cache (fwd_decode.cu)
 constexpr int kDecodeChunk = 128; // keys per pipeline stage
 constexpr int kDecodeMaxSplitChunks = 8; // chunks per CTA (split) at most
@@ -156,6 +167,8 @@ size_t decode_smem_bytes(int R);
 // Size of the library's own decode scratch array (fl_attn_decode_static).
 constexpr size_t kDecodeStaticScratch = size_t(64) << 20;
 cudaError_t decode_static_scratch(void **ptr);
+
+cudaError_t launch_diff_bwd_combine(const DiffCombine &c, int sm_count, cudaStream_t stream);
 
 cudaError_t launch_evo(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
                        const CUtensorMap &tb, const EvoParams &p, int grid, cudaStream_t stream);

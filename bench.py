@@ -214,6 +214,47 @@ def time_bwd(e, torch, fa, device, steps, warmup, flush, stream):
     return [a.elapsed_time(b) for a, b in evs]
 
 
+def diff_bwd_entry(mask):
+    """The differential backward on the differential workload; algorithmic
+    flops per unmasked pair and stream 6 D + 4 Dv (S = Q K^T, dQ and dK: 2 D
+    each; dP = dO V^T and dV: 2 Dv each)."""
+    e = diff_entry(mask)
+    e.update(kind="diff_bwd", variant="bwd_" + ("causal" if mask == "causal" else "non-causal"),
+             flops=e["pairs"] * 2 * (6 * e["D"] + 4 * e["Dv"]),
+             bytes=2 * e["B"] * e["S"] * e["H"] * (2 * 2 * 2 * e["D"] + 3 * e["Dv"]) + 4 * 2 * e["B"] * e["H"] * e["S"])
+    return e
+
+
+def time_diff_bwd(e, torch, fa, device, steps, warmup, flush, stream):
+    """Device time of fl_attn_diff_bwd (all its launches) on the workload."""
+    B, S, H, D, Dv = e["B"], e["S"], e["H"], e["D"], e["Dv"]
+    to = lambda b: torch.from_numpy(b.view(np.int16)).view(torch.bfloat16).to(device)
+    q = to(testdata.normal_bf16((2, B, S, H, D), e["name"], "q"))
+    k = to(testdata.normal_bf16((2, B, S, H, D), e["name"], "k"))
+    v = to(testdata.normal_bf16((B, S, H, Dv), e["name"], "v"))
+    do = to(testdata.normal_bf16((B, S, H, Dv), e["name"], "do"))
+    out = torch.empty((B, S, H, Dv), dtype=torch.bfloat16, device=device)
+    lse = torch.empty((2, B, H, S), dtype=torch.float32, device=device)
+    desc = fa.make_desc(kind="diff", mask=e["mask"], diff_lambda=workloads.DIFF["lam"])
+    fa.fl_attn_fwd(q, k, v, out, lse, desc)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    ws = torch.empty(fa.fl_attn_diff_bwd_workspace_size(q, k, v, desc), dtype=torch.uint8, device=device)
+    with torch.cuda.stream(stream):
+        for _ in range(warmup):
+            flush.zero_()
+            fa.fl_attn_diff_bwd(q, k, v, lse, do, dq, dk, dv, desc, ws, stream=stream)
+        torch.cuda.synchronize()
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(steps)]
+        for a, b in evs:
+            flush.zero_()
+            a.record(stream)
+            fa.fl_attn_diff_bwd(q, k, v, lse, do, dq, dk, dv, desc, ws, stream=stream)
+            b.record(stream)
+        torch.cuda.synchronize()
+    return [a.elapsed_time(b) for a, b in evs]
+
+
 def decode_entry(mod):
     """The serving workload: one new token per sequence against a paged cache."""
     w = workloads.DECODE
@@ -646,7 +687,8 @@ ONLY = {"diff": lambda: diff_entry("none"), "diff_causal": lambda: diff_entry("c
         "evo_af2_row": lambda: evo_batched_entry(True), "evo_af2_col": lambda: evo_batched_entry(False),
         "bwd": lambda: bwd_entry("none"), "bwd_causal": lambda: bwd_entry("causal"),
         "bwd_expr_softcap": lambda: bwd_entry("none", EXPR_VARIANTS["expr_softcap"][1]),
-        "bwd_softcap": lambda: bwd_entry("none", mod="softcap")}
+        "bwd_softcap": lambda: bwd_entry("none", mod="softcap"),
+        "diff_bwd": lambda: diff_bwd_entry("none"), "diff_bwd_causal": lambda: diff_bwd_entry("causal")}
 
 
 def run_only(args):
@@ -664,7 +706,7 @@ def run_only(args):
                                         args.warmup, flush, stream)[0])
     else:
         timer = {"decode": time_decode, "evo_batched": time_evo_batched,
-                 "bwd": time_bwd}.get(e["kind"], time_other)
+                 "bwd": time_bwd, "diff_bwd": time_diff_bwd}.get(e["kind"], time_other)
         ms = statistics.mean(timer(e, torch, fa, device, args.steps, args.warmup, flush, stream))
     print(json.dumps({"only": args.only, "ms": round(ms, 4),
                       "tflops": round(e["flops"] / (ms * 1e-3) / 1e12, 1),
@@ -739,6 +781,12 @@ def run_ours(args):
         for e in (bwd_entry("none"), bwd_entry("causal"), bwd_entry("none", mod="softcap"),
                   bwd_entry("none", EXPR_VARIANTS["expr_softcap"][1])):
             vm = statistics.mean(time_bwd(e, torch, fa, device, args.variant_steps, 2, flush, stream))
+            tf = e["flops"] / (vm * 1e-3) / 1e12
+            variants[f"{e['name']}/{e['variant']}"] = dict(
+                tflops=round(tf, 1), frac_peak=round(tf / peaks["bf16_tflops"], 4), ms=round(vm, 4),
+                gbs=round(e["bytes"] / (vm * 1e-3) / 1e9, 1), l2="flushed before every timed step (256 MiB write)")
+        for e in (diff_bwd_entry("none"), diff_bwd_entry("causal")):
+            vm = statistics.mean(time_diff_bwd(e, torch, fa, device, args.variant_steps, 2, flush, stream))
             tf = e["flops"] / (vm * 1e-3) / 1e12
             variants[f"{e['name']}/{e['variant']}"] = dict(
                 tflops=round(tf, 1), frac_peak=round(tf / peaks["bf16_tflops"], 4), ms=round(vm, 4),

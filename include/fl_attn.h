@@ -249,6 +249,35 @@ fl_status fl_attn_bwd(const fl_tensor *q, const fl_tensor *k, const fl_tensor *v
                       const fl_attn_variant_desc *desc, void *workspace, size_t workspace_bytes,
                       fl_stream_t stream);
 
+/*
+ * fl_attn_diff_bwd -- backward of the differential kind: dQ1, dQ2, dK1, dK2
+ * and dV of
+ *     O = softmax(scale Q1 K1^T + mask) V - lambda softmax(scale Q2 K2^T + mask) V
+ * given the forward's per-stream (natural-log) lse and the output gradient
+ * dout (the pages name differential attention among the complex variants,
+ * gist.science summary, "Results", and the backward as the fused kernels'
+ * next step, "Limitations and future work").
+ *   q, dq [2, B, S, H, 64]; k, dk [2, B, S, Hk, 64]; v, dv [B, S, Hk, Dv],
+ *   Dv 64 or 128; dout [B, S, H, Dv]; lse [2, B, H, S] fp32 (fl_attn_fwd's).
+ *   desc: kind FL_KIND_DIFF, mask none or causal, no score_mod, scale (0:
+ *   1/8), diff_lambda; GQA heads are summed into dk, dv.
+ * Stream t's gradients are those of one softmax attention whose output
+ * gradient is c_t dout (c = 1, -lambda); the library recomputes each stream's
+ * output from q, k and v and runs the standard backward on it, per 64-column
+ * half of V when Dv = 128, then adds the partial gradients with their
+ * coefficients in fp32 and rounds once to bf16.
+ * `workspace`: device memory of at least fl_attn_diff_bwd_workspace_size
+ * bytes, 256-byte aligned, owned by the caller, no initialisation needed.
+ * All launches go to `stream`, validation happens before the first one, and
+ * every output element is written exactly once (no atomics).
+ */
+fl_status fl_attn_diff_bwd_workspace_size(const fl_tensor *q, const fl_tensor *k, const fl_tensor *v,
+                                          const fl_attn_variant_desc *desc, size_t *bytes);
+fl_status fl_attn_diff_bwd(const fl_tensor *q, const fl_tensor *k, const fl_tensor *v,
+                           const fl_tensor *lse, const fl_tensor *dout, const fl_tensor *dq,
+                           const fl_tensor *dk, const fl_tensor *dv, const fl_attn_variant_desc *desc,
+                           void *workspace, size_t workspace_bytes, fl_stream_t stream);
+
 /* Query-block and key-tile sizes the kernel for `desc` uses (for the
  * visited-tile accounting).  `head_dim` is D for the standard and Evoformer
  * kinds and the value head dimension Dv for FL_KIND_DIFF (whose D is 64).

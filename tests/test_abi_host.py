@@ -297,3 +297,32 @@ def test_evoformer_batched_validation_before_device(lib):
         fa.FL_ERR_INVALID_ARG
     odd = _t((Bt, Ns, Nr, H, c), strides=(Ns * Nr * H * c + 4, Nr * H * c, H * c, c, 1))
     assert call(q=odd) == fa.FL_ERR_ALIGNMENT
+
+
+@fake_addresses
+def test_diff_bwd_validation_before_device(lib):
+    B, S, H, Hk = 2, 256, 4, 2
+    r = ctypes.byref
+
+    def args(Dv=128, do_shape=None):
+        return [_t((2, B, S, H, 64)), _t((2, B, S, Hk, 64)), _t((B, S, Hk, Dv)), _t((2, B, H, S), fa.FL_F32),
+                _t(do_shape or (B, S, H, Dv)), _t((2, B, S, H, 64)), _t((2, B, S, Hk, 64)), _t((B, S, Hk, Dv))]
+
+    def call(a, desc, ws=0x40000, nbytes=1 << 30):
+        return lib.fl_attn_diff_bwd(*[r(x) for x in a], r(desc), ws, nbytes, None)
+
+    d = fa.make_desc(kind="diff", diff_lambda=0.8)
+    n = ctypes.c_size_t()
+    a = args()
+    assert lib.fl_attn_diff_bwd_workspace_size(r(a[0]), r(a[1]), r(a[2]), r(d), r(n)) == fa.FL_OK
+    assert n.value > 0 and n.value % 256 == 0
+    # every failure below happens before any CUDA call
+    assert call(args(), fa.make_desc(kind="standard")) == fa.FL_ERR_INVALID_ARG
+    assert call(args(Dv=96), d) == fa.FL_ERR_UNSUPPORTED
+    assert call(args(), fa.make_desc(kind="diff", mask="window", window=8)) == fa.FL_ERR_UNSUPPORTED
+    assert call(args(), fa.make_desc(kind="diff", score_mod="softcap", softcap=20.0)) == fa.FL_ERR_UNSUPPORTED
+    assert call(args(do_shape=(B, S, H, 64)), d) == fa.FL_ERR_INVALID_ARG
+    assert call(args(), d, ws=0) == fa.FL_ERR_INVALID_ARG
+    assert call(args(), d, ws=0x40010) == fa.FL_ERR_ALIGNMENT
+    assert call(args(), d, nbytes=n.value - 1) == fa.FL_ERR_INVALID_ARG
+    assert "workspace holds" in fa.fl_attn_last_error()
