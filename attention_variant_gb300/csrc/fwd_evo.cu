@@ -565,16 +565,21 @@ __device__ __forceinline__ void evo_epilogue(const EvoParams &p, uint32_t tO, co
             const int64_t o_row = pr.b * p.o_sb + static_cast<int64_t>(i) * p.o_si + pr.h * p.o_sh;
             const uint32_t *g32 = reinterpret_cast<const uint32_t *>(p.gate + g_row) + 16 * c32;
             uint32_t *o32 = reinterpret_cast<uint32_t *>(p.out + o_row) + 16 * c32;
+            const float hinv = 0.5f * inv[k];
 #pragma unroll
             for (int r = 0; r < 4; ++r) {
                 // columns 32 c32 + 8r + 2 jq and + 1: one 32-bit word of the row
                 const uint32_t gw = __ldg(g32 + 4 * r + jq); // prefetched into L1 when the row started
-                const float g0 = __uint_as_float(gw << 16), g1 = __uint_as_float(gw & 0xFFFF0000u);
-                // sigmoid(g) = 1/2 + tanh(g / 2) / 2 (one special-function op)
-                const float s0 = fmaf(0.5f, tanh_approx(0.5f * g0), 0.5f);
-                const float s1 = fmaf(0.5f, tanh_approx(0.5f * g1), 0.5f);
-                o32[4 * r + jq] = ptx::pack_bf16(__uint_as_float(o[4 * r + 2 * k]) * inv[k] * s0,
-                                                 __uint_as_float(o[4 * r + 2 * k + 1]) * inv[k] * s1);
+                // sigmoid(g) o / l = a (1 + tanh(g / 2)) with a = o / (2 l): one
+                // special-function op per column, the rest as packed pairs
+                float g0, g1, a0, a1, y0, y1;
+                ptx::fma2(g0, g1, __uint_as_float(gw << 16), __uint_as_float(gw & 0xFFFF0000u), 0.5f, 0.5f,
+                          0.f, 0.f);
+                const float t0 = tanh_approx(g0), t1 = tanh_approx(g1);
+                ptx::fma2(a0, a1, __uint_as_float(o[4 * r + 2 * k]), __uint_as_float(o[4 * r + 2 * k + 1]), hinv,
+                          hinv, 0.f, 0.f);
+                ptx::fma2(y0, y1, a0, a1, t0, t1, a0, a1);
+                o32[4 * r + jq] = ptx::pack_bf16(y0, y1);
             }
         }
     }
