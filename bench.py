@@ -682,6 +682,7 @@ ONLY = {"diff": lambda: diff_entry("none"), "diff_causal": lambda: diff_entry("c
         "softcap": lambda: entry("mha", 2048, "softcap"), "alibi": lambda: entry("mha", 2048, "alibi"),
         "s512_vanilla": lambda: entry("mha", 512, "vanilla"), "s512_causal": lambda: entry("mha", 512, "causal"),
         "gqa16k_window": lambda: entry("gqa", 16384, "window"), "gqa16k_doc": lambda: entry("gqa", 16384, "doc"),
+        "gqa16k_prefix": lambda: entry("gqa", 16384, "prefix"),
         "expr_softcap": lambda: expr_entry(2048, "expr_softcap"),
         "expr_alibi": lambda: expr_entry(2048, "expr_alibi"),
         "evo_af2_row": lambda: evo_batched_entry(True), "evo_af2_col": lambda: evo_batched_entry(False),
