@@ -4,11 +4,13 @@ with the float64 oracle.
 The forward runs through the library (its per-stream fp32 LSE feeds the
 backward, as in training); the oracle differentiates the plain definition in
 float64 from the same bf16 inputs.  Tolerance: that of the standard backward
-(max |err| <= 10 * 2^-9 max |ref|, mean |err| <= 3 * 2^-9 mean |ref| per
-gradient), since each stream's partial gradients come from the standard
-backward kernels; they are summed with their coefficients in fp32 and rounded
-once, which adds at most one more bf16 rounding of a partial (2^-9 of its
-scale) where two partials meet (dV, and dQ / dK at Dv = 128).
+(max |err| <= 10 * 2^-9 max |ref|, mean |err| <= 4 * 2^-9 mean |ref| per
+gradient; the mean bound covers the rounding of D = rowsum(dO O) from the
+bf16 O, derived in tests/test_gpu_bwd.py), since each stream's partial
+gradients come from the standard backward kernels; they are summed with their
+coefficients in fp32 and rounded once, which adds at most one more bf16
+rounding of a partial (2^-9 of its scale) where two partials meet (dV, and
+dQ / dK at Dv = 128).
 """
 import numpy as np
 import pytest
@@ -56,7 +58,7 @@ def _check(got, ref, what):
         e = np.abs(g - r)
         assert e.max() <= 10 * 2.0 ** -9 * np.abs(r).max(), \
             f"{what} {name}: max err {e.max():.3e} vs max |ref| {np.abs(r).max():.3e}"
-        assert e.mean() <= 3 * 2.0 ** -9 * np.abs(r).mean(), \
+        assert e.mean() <= 4 * 2.0 ** -9 * np.abs(r).mean(), \
             f"{what} {name}: mean err {e.mean():.3e} vs mean |ref| {np.abs(r).mean():.3e}"
 
 

@@ -134,3 +134,80 @@ def test_sweep_evoformer(case):
                what=f"{tag}: {'row' if row else 'col'} Ns{Ns} Nr{Nr} H{H} c{ch}")
     bn = fa.fl_attn_tile_shape(fa.make_desc(kind="evo_row"), ch)[1]
     assert np.array_equal(cnt.cpu().numpy(), gu.expected_tile_counts("none", B, H, S, bn=bn))
+
+
+def _decode_cases(n=8):
+    rng = np.random.default_rng(SEED + 3)
+    cases = []
+    for c in range(n):
+        Sq = int(rng.integers(1, 5))
+        Hk = int(rng.choice([1, 2]))
+        G = int(rng.choice([g for g in (1, 2, 4, 8) if g * Sq <= 64]))
+        B = int(rng.integers(1, 9))
+        lens = [int(x) for x in rng.integers(Sq, 3000, size=B)]
+        page = int(rng.choice([0, 16, 64, 256]))  # 0: contiguous cache
+        cases.append((c, B, Sq, Hk * G, Hk, lens, page, str(rng.choice(["none", "softcap"])),
+                      bool(rng.integers(0, 2))))
+    return cases
+
+
+@pytest.mark.parametrize("case", _decode_cases(), ids=lambda c: f"decode{c[0]}")
+def test_sweep_decode(case):
+    from tests import test_gpu_decode as td
+
+    c, B, Sq, Hq, Hk, lens, page, mod, causal = case
+    tag = f"sweep_dec{c}"
+    if page:
+        q, kc, vc, table, k, v = td._paged(tag, B, Sq, Hq, Hk, lens, page)
+    else:
+        q, k, v = td._inputs(tag, B, Sq, Hq, Hk, max(lens))
+        kc, vc, table = k, v, None
+    (o, lse), = td._run(q, kc, vc, lens, max(lens), table=table, mod=mod, causal=causal)
+    oref, lref = td._ref(q, k, v, lens, mod, causal)
+    gu.compare(o, lse, oref, lref, what=f"{tag}: B{B} Sq{Sq} H{Hq}/{Hk} page {page} {mod} causal={causal}")
+
+
+def _bwd_cases(n=6):
+    rng = np.random.default_rng(SEED + 4)
+    cases = []
+    for c in range(n):
+        Hk = int(rng.choice([1, 2]))
+        Hq = Hk * int(rng.choice([1, 2, 4]))
+        S = int(rng.integers(1, 700))
+        mask = str(rng.choice(["none", "causal", "window", "prefix", "doc"]))
+        kw = {}
+        if mask == "window":
+            kw["window"] = int(rng.integers(1, S + 50))
+        elif mask == "prefix":
+            kw["prefix"] = int(rng.integers(0, S + 50))
+        cases.append((c, int(rng.integers(1, 3)), S, Hq, Hk, mask, str(rng.choice(["none", "alibi", "softcap"])),
+                      kw))
+    return cases
+
+
+@pytest.mark.parametrize("case", _bwd_cases(), ids=lambda c: f"bwd{c[0]}")
+def test_sweep_backward(case):
+    from tests import test_gpu_bwd as tb
+
+    c, B, S, Hq, Hk, mask, mod, kw = case
+    tag = f"sweep_bwd{c}"
+    if mask == "doc":
+        kw = dict(doc_offsets=testdata.doc_offsets(S, B, tag, lo=37, hi=400))
+    got, ref = tb._run(tag, B, S, Hq, Hk, mask, mod=mod, **kw)
+    tb._check(got, ref, f"{tag}: B{B} S{S} H{Hq}/{Hk} {mod}/{mask}")
+
+
+def _diff_bwd_cases(n=4):
+    rng = np.random.default_rng(SEED + 5)
+    return [(c, int(rng.integers(1, 3)), int(rng.integers(1, 600)), int(rng.choice([1, 2])),
+             int(rng.choice([1, 2, 3])), int(rng.choice([64, 128])), str(rng.choice(["none", "causal"])),
+             float(rng.uniform(-1.0, 1.0))) for c in range(n)]
+
+
+@pytest.mark.parametrize("case", _diff_bwd_cases(), ids=lambda c: f"diffbwd{c[0]}")
+def test_sweep_diff_backward(case):
+    from tests import test_gpu_diff_bwd as tdb
+
+    c, B, S, Hk, G, Dv, mask, lam = case
+    got, ref = tdb._run(f"sweep{c}", B, S, Hk * G, Hk, Dv, mask, lam)
+    tdb._check(got, ref, f"sweep diff backward {c}: B{B} S{S} H{Hk * G}/{Hk} Dv{Dv} {mask} lam {lam:.3f}")
