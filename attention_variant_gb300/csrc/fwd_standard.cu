@@ -31,12 +31,17 @@
 //
 // TMEM (512 columns x 128 lanes, lane = query row) per head dimension, for
 // slots t = 0, 1 (StdCfg below):
-//   D = 32, 64:  key tiles of 112 keys; S[t] fp32 at 112 t, O[t] at 224 + (D + 16) t
-//                with D output columns and 16 columns of sum_j P_j (P V
+//   D = 64:      key tiles of 112 keys; S[t] fp32 at 112 t, O[t] at 224 + 80 t
+//                with 64 output columns and 16 columns of sum_j P_j (P V
 //                multiplies P by V extended with a tile of ones, so the tensor
 //                core sums the exact bf16 P it used: the normaliser of O), P[t]
-//                bf16 pairs at 384 + 64 t; the softmax keeps only the exact sum
+//                bf16 pairs at 384 + 56 t; the softmax keeps only the exact sum
 //                (for the LSE);
+//   D = 32:      the same with key tiles of 128 keys: S[t] at 128 t, O[t] at
+//                256 + 48 t (32 output and 16 sum columns), P[t] at 384 + 64 t;
+//                128-key tiles at D = 64 would need 544 columns (or a P buffer
+//                shared by the slots, or the rounded sum in registers: both
+//                measured slower than 112-key tiles);
 //   D = 128:     key tiles of 64 keys; S[t] at 64 t, O[t] at 128 + 128 t (two
 //                128-column accumulators leave no room for sum columns), P[t]
 //                at 384 + 32 t; the softmax keeps both sums in registers (the

@@ -192,7 +192,7 @@ cudaError_t launch_bwd(const CUtensorMap &tq, const CUtensorMap &tdo, const CUte
 // Keys per K/V tile of the standard kernel for head dimension D (its TMEM
 // budget: see fwd_standard.cu), its threads per CTA and the registers per
 // thread it must be compiled to.
-__host__ __device__ constexpr int std_key_tile(int D) { return D == 128 ? 64 : 112; }
+__host__ __device__ constexpr int std_key_tile(int D) { return D == 128 ? 64 : D == 64 ? 112 : 128; }
 constexpr int kStdThreads = 384;
 constexpr int kStdRegs = 168;
 // Keys per K/V tile of the differential kernel for value head dimension Dv

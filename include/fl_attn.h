@@ -151,8 +151,8 @@ typedef struct {
     const float *alibi_slopes; /* device float [Hq], or NULL for 2^(-8 (h+1) / Hq) */
     int32_t *debug_tile_counts; /* NULL, or device int32 [batch][heads][ceil(S/128)]: the
                                    number of key tiles each 128-row query block visited
-                                   (key-tile width from fl_attn_tile_shape: 112 for the
-                                   standard kind at D = 32 and 64, 64 at D = 128; 112 for
+                                   (key-tile width from fl_attn_tile_shape: 128 for the
+                                   standard kind at D = 32, 112 at D = 64, 64 at D = 128; 112 for
                                    the differential kind at Dv = 64, 80 at Dv = 128; 128
                                    for the Evoformer kinds) */
     uint32_t *error_word;    /* NULL, or a device word the kernel ORs FL_DEVERR_* into */

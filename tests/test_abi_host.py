@@ -137,7 +137,7 @@ def test_size_one_axes_take_any_stride(lib):
 
 def test_tile_shape(lib):
     assert fa.fl_attn_tile_shape(fa.make_desc(), 64) == (128, 112)
-    assert fa.fl_attn_tile_shape(fa.make_desc(), 32) == (128, 112)
+    assert fa.fl_attn_tile_shape(fa.make_desc(), 32) == (128, 128)
     assert fa.fl_attn_tile_shape(fa.make_desc(), 128) == (128, 64)
     assert fa.fl_attn_tile_shape(fa.make_desc(kind="diff"), 64) == (128, 112)
     assert fa.fl_attn_tile_shape(fa.make_desc(kind="diff"), 128) == (128, 80)

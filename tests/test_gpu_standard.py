@@ -93,10 +93,10 @@ def test_mha_variants(mod, mask, S):
     _check(q, k, v, mod, mask, f"mha{S}")
 
 
-# head dimensions 32 (112-key tiles, 64-byte rows) and 128 (64-key tiles, two
+# head dimensions 32 (128-key tiles, 64-byte rows) and 128 (64-key tiles, two
 # 64-column halves per row, row sums in registers); every length ends in a
-# ragged last key tile for both tile widths (333 = 2*112 + 109 = 5*64 + 13,
-# 600 = 5*112 + 40 = 9*64 + 24)
+# ragged last key tile for both tile widths (333 = 2*128 + 77 = 5*64 + 13,
+# 600 = 4*128 + 88 = 9*64 + 24)
 @pytest.mark.parametrize("D", [32, 128])
 @pytest.mark.parametrize("S", [333, 600])
 @pytest.mark.parametrize("mask", ["none", "causal", "window", "prefix", "doc"])
@@ -125,7 +125,7 @@ def test_head_dims_persistent_items_everywhere(D, mask):
     _check(q, k, v, "none", mask, tag)
 
 
-@pytest.mark.parametrize("D", [64, 128])
+@pytest.mark.parametrize("D", [32, 64, 128])
 def test_doc_start_far_into_the_pair(D):
     """A document that starts in the second query block of an MHA pair while
     the first block's document began many key tiles earlier: the two slots'
@@ -188,6 +188,15 @@ def test_edge_lengths(S):
     q, k, v = _inputs(f"edge{S}", 1, S, 2)
     for mask in ("none", "causal"):
         _check(q, k, v, "alibi", mask, f"edge{S}")
+
+
+@pytest.mark.parametrize("S", [1, 128, 129, 256, 383])
+def test_edge_lengths_d32(S):
+    # D = 32 runs 128-key tiles: lengths at, one past and one short of a
+    # multiple of the tile
+    q, k, v = _inputs(f"edge32_{S}", 1, S, 2, D=32, Dv=32)
+    for mask in ("none", "causal"):
+        _check(q, k, v, "alibi", mask, f"edge32_{S}")
 
 
 def test_strided_layout_and_no_lse():
