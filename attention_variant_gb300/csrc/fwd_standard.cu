@@ -468,8 +468,13 @@ __device__ void pv_role(const KernelCtx<D> &cx, const StdParams &p, int t)
 //
 // How the turn is passed depends on the score_mod (chosen by measurement):
 //  * plain scores: an mbarrier pair (a bounded wait, like every other wait);
-//  * ALiBi and softcap, whose longer exponential phase gains from a faster
-//    hand-off: two named barriers (a woken barrier.sync resumes within a few
+//  * softcap: no turns.  Its three special-function operations per score
+//    (two exponentials and a reciprocal) keep the XU pipe the busiest unit,
+//    so the tensor core's chains hide behind the exponentials without the
+//    ping-pong, and both warpgroups exponentiating at once measured faster
+//    (MHA S = 2048: 437 against 427 TFLOP/s with named-barrier turns);
+//  * ALiBi (and run-time expressions), whose longer exponential phase gains
+//    from a faster hand-off: two named barriers (a woken barrier.sync resumes within a few
 //    cycles, an mbarrier wait took ~250).  Warpgroup 0 waits on barrier 2
 //    before each turn and warpgroup 1 arrives there once at the start and
 //    after each turn; warpgroup 1 waits on barrier 3 and warpgroup 0 arrives
@@ -524,7 +529,9 @@ __device__ void softmax_role(const KernelCtx<D> &cx, const StdParams &p, int t)
 {
     using C = StdCfg<D>;
     constexpr int kBN = C::kBN;
-    constexpr bool kNamed = MOD != MOD_NONE; // how the turn is passed (see above)
+    // how the turn is passed (see above): an mbarrier pair, named barriers or no turns
+    constexpr bool kTurns = MOD != MOD_SOFTCAP;
+    constexpr bool kNamed = kTurns && MOD != MOD_NONE;
     StdSmem<D> &sm = *cx.sm;
     const int r = threadIdx.x & 127;             // row of the query tile = TMEM lane
     const uint32_t wq = (threadIdx.x >> 5) & 3;  // warp's quarter of the lanes
@@ -604,7 +611,7 @@ __device__ void softmax_role(const KernelCtx<D> &cx, const StdParams &p, int t)
             if constexpr (kNamed) {
                 nb_take(t);
                 nb_pass(t);
-            } else {
+            } else if constexpr (kTurns) {
                 if (!(t == 0 && turns == 0) && !warp_wait(b_turn_mine, (t == 1 ? turns : turns - 1) & 1, cx.wc,
                                                           W_TURN))
                     return;
@@ -631,7 +638,7 @@ __device__ void softmax_role(const KernelCtx<D> &cx, const StdParams &p, int t)
             if constexpr (kNamed) {
                 nb_take(t);
                 ptx::reg_fence_f<kBN>(x);
-            } else {
+            } else if constexpr (kTurns) {
                 if (!free_turn && !warp_wait(b_turn_mine, phase & 1, cx.wc, W_TURN))
                     return;
             }
@@ -650,7 +657,7 @@ __device__ void softmax_role(const KernelCtx<D> &cx, const StdParams &p, int t)
                 ptx::reg_fence<kBN / 2>(pk);
                 ptx::reg_fence_f<1>(&st.l);
                 nb_pass(t);
-            } else {
+            } else if constexpr (kTurns) {
                 ptx::mbar_arrive(b_turn_other); // hand the turn over
             }
             if (kk > 0) {
@@ -676,7 +683,7 @@ __device__ void softmax_role(const KernelCtx<D> &cx, const StdParams &p, int t)
             if constexpr (kNamed) {
                 nb_take(t);
                 nb_pass(t);
-            } else {
+            } else if constexpr (kTurns) {
                 if (!(t == 0 && turns == 0) && !warp_wait(b_turn_mine, (t == 1 ? turns : turns - 1) & 1, cx.wc,
                                                           W_TURN))
                     return;

@@ -66,18 +66,32 @@ __device__ __forceinline__ void load_scores(uint32_t tS, float (&x)[N])
 template <int MOD, int N = BN>
 __device__ __forceinline__ void apply_score_mod(float (&x)[N], const ScoreMod &sm, int i, int j0)
 {
+    // Both score_mods work on pairs of keys with the packed fp32 instructions
+    // (one issue for two scores): fewer instructions in the exponential phase,
+    // which one warp per sub-partition runs.
     if constexpr (MOD == MOD_ALIBI) {
-        // z - slope |i - j|, in log2 units
-        const float d0 = static_cast<float>(j0 - i);
+        // z - slope |i - j|, in log2 units; j - i of keys 2e and 2e + 1 stepped
+        // by 2 (exact in fp32: |j - i| < 2^24)
+        const float nc = -sm.alibi_c;
+        float dA = static_cast<float>(j0 - i), dB = dA + 1.f;
 #pragma unroll
-        for (int e = 0; e < N; ++e)
-            x[e] = fmaf(x[e], sm.qk_log2, -sm.alibi_c * fabsf(d0 + static_cast<float>(e)));
+        for (int e = 0; e < N / 2; ++e) {
+            ptx::fma2(x[2 * e], x[2 * e + 1], x[2 * e], x[2 * e + 1], sm.qk_log2, sm.qk_log2, nc * fabsf(dA),
+                      nc * fabsf(dB));
+            ptx::add2(dA, dB, 2.f, 2.f);
+        }
     } else if constexpr (MOD == MOD_SOFTCAP) {
-        // cap * tanh(z / cap) with tanh(u) = 1 - 2 / (1 + e^(2u)), in log2 units
+        // cap * tanh(z / cap) with tanh(u) = 1 - 2 / (1 + e^(2u)), in log2 units:
+        // out (1 - 2 r) as out + (-2 out) r, r = 1 / (1 + 2^(z in))
+        const float m2o = -2.f * sm.softcap_out;
 #pragma unroll
-        for (int e = 0; e < N; ++e) {
-            const float ex = ptx::ex2(x[e] * sm.softcap_in);
-            x[e] = sm.softcap_out * (1.f - 2.f * ptx::rcp_approx(1.f + ex));
+        for (int e = 0; e < N / 2; ++e) {
+            float a0, a1;
+            ptx::fma2(a0, a1, x[2 * e], x[2 * e + 1], sm.softcap_in, sm.softcap_in, 0.f, 0.f);
+            float d0 = ptx::ex2(a0), d1 = ptx::ex2(a1);
+            ptx::add2(d0, d1, 1.f, 1.f);
+            const float r0 = ptx::rcp_approx(d0), r1 = ptx::rcp_approx(d1);
+            ptx::fma2(x[2 * e], x[2 * e + 1], r0, r1, m2o, m2o, sm.softcap_out, sm.softcap_out);
         }
     } else if constexpr (MOD == MOD_EXPR) {
 #ifdef FL_SCORE_EXPR
