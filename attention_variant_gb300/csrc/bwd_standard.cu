@@ -133,6 +133,35 @@ __device__ __forceinline__ ModCtx mod_ctx(const BwdParams &p, int b, int h)
     return m;
 }
 
+// The exponent arguments (logit - LSE, log2 units) and chain factors of a pair
+// of scores x0, x1 with the packed fp32 instructions (one issue for two
+// scores: the elementwise step of both tile kinds is issue-bound, and this
+// form cut its instructions enough to take the plain-score backward from 448
+// to 534 TFLOP/s at S = 2048); dA, dB: i - j of the two pairs (ALiBi; exact in
+// fp32), nl0, nl1: -LSE log2 e of their rows.  Run-time expressions keep the
+// per-score mod_logit2 above.
+template <int MOD>
+__device__ __forceinline__ void mod_args2(const ModCtx &m, float x0, float x1, float dA, float dB, float nl0,
+                                          float nl1, float &a0, float &a1, float &ch0, float &ch1)
+{
+    ch0 = ch1 = 1.f;
+    if constexpr (MOD == MOD_SOFTCAP) {
+        float g0, g1, t0, t1;
+        ptx::fma2(g0, g1, x0, x1, m.cap_in, m.cap_in, 0.f, 0.f);
+        float e0 = ptx::ex2(g0), e1 = ptx::ex2(g1);
+        ptx::add2(e0, e1, 1.f, 1.f);
+        const float r0 = ptx::rcp_approx(e0), r1 = ptx::rcp_approx(e1);
+        ptx::fma2(t0, t1, r0, r1, -2.f, -2.f, 1.f, 1.f);       // tanh
+        ptx::fma2(a0, a1, t0, t1, m.cap_out, m.cap_out, nl0, nl1);
+        ptx::fma2(ch0, ch1, -t0, -t1, t0, t1, 1.f, 1.f);      // 1 - tanh^2
+    } else if constexpr (MOD == MOD_ALIBI) {
+        const float nc = -m.alibi_c;
+        ptx::fma2(a0, a1, x0, x1, m.sl2, m.sl2, fmaf(nc, fabsf(dA), nl0), fmaf(nc, fabsf(dB), nl1));
+    } else {
+        ptx::fma2(a0, a1, x0, x1, m.sl2, m.sl2, nl0, nl1);
+    }
+}
+
 // ---------------------------------------------------------------- prep
 
 __global__ void __launch_bounds__(128) bwd_prep_kernel(const BwdParams p)
@@ -376,6 +405,43 @@ __device__ __forceinline__ void bwd_dq_body(const CUtensorMap &tm_q, const CUten
             const int j0 = (tr.lo + j) * kDqKeys;
             const bool edge = !(j0 >= tr.full_lo && j0 + kDqKeys <= tr.full_hi);
             uint32_t ds[32];
+            if constexpr (MOD != MOD_EXPR) {
+                if constexpr (MOD != MOD_SOFTCAP) {
+                    // a removed pair's score -> -inf, so its P is 0 (a softcap
+                    // score is bounded: its argument is masked below instead)
+                    if (edge) {
+#pragma unroll
+                        for (int col = 0; col < 64; ++col)
+                            if (j0 + col < st.lo || j0 + col >= st.hi)
+                                sv[col] = 0xFF800000u;
+                    }
+                }
+                const float nl = -st.lse2, nd = -st.d;
+                float dA = static_cast<float>(row - j0), dB = dA - 1.f; // i - j of keys 2c, 2c + 1
+#pragma unroll
+                for (int c = 0; c < 32; ++c) {
+                    float a0, a1, ch0, ch1, u0, u1, r0, r1;
+                    mod_args2<MOD>(mc, __uint_as_float(sv[2 * c]), __uint_as_float(sv[2 * c + 1]), dA, dB, nl, nl,
+                                   a0, a1, ch0, ch1);
+                    if constexpr (MOD == MOD_ALIBI)
+                        ptx::add2(dA, dB, -2.f, -2.f);
+                    if constexpr (MOD == MOD_SOFTCAP) {
+                        if (edge) {
+                            if (j0 + 2 * c < st.lo || j0 + 2 * c >= st.hi)
+                                a0 = kNegInf;
+                            if (j0 + 2 * c + 1 < st.lo || j0 + 2 * c + 1 >= st.hi)
+                                a1 = kNegInf;
+                        }
+                    }
+                    const float p0 = ptx::ex2(a0), p1 = ptx::ex2(a1);
+                    ptx::fma2(u0, u1, __uint_as_float(pv[2 * c]), __uint_as_float(pv[2 * c + 1]), 1.f, 1.f, nd,
+                              nd);
+                    if constexpr (MOD == MOD_SOFTCAP)
+                        ptx::fma2(u0, u1, u0, u1, ch0, ch1, 0.f, 0.f);
+                    ptx::fma2(r0, r1, p0, p1, u0, u1, 0.f, 0.f);
+                    ds[c] = ptx::pack_bf16(r0, r1);
+                }
+            } else
 #pragma unroll
             for (int c = 0; c < 32; ++c) {
                 float d2[2];
@@ -654,6 +720,47 @@ __device__ __forceinline__ void bwd_dkdv_body(const CUtensorMap &tm_k, const CUt
                 ptx::tmem_wait_ld();
                 ptx::reg_fence<32>(sv);
                 ptx::reg_fence<32>(pv);
+                if constexpr (MOD != MOD_EXPR) {
+                    if constexpr (MOD != MOD_SOFTCAP) {
+                        if (edge) {
+#pragma unroll
+                            for (int c = 0; c < 32; ++c) {
+                                const BwdRowStat &sc = sm.stats[s][32 * half + c];
+                                if (key < sc.lo || key >= sc.hi)
+                                    sv[c] = 0xFF800000u; // -inf: P = 0
+                            }
+                        }
+                    }
+                    // i - j of query rows 2 c2, 2 c2 + 1 of this half
+                    float dA = static_cast<float>(q0 + 32 * half - key), dB = dA + 1.f;
+#pragma unroll
+                    for (int c2 = 0; c2 < 16; ++c2) {
+                        const BwdRowStat s0 = sm.stats[s][32 * half + 2 * c2];
+                        const BwdRowStat s1 = sm.stats[s][32 * half + 2 * c2 + 1];
+                        float a0, a1, ch0, ch1, u0, u1, r0, r1;
+                        mod_args2<MOD>(mc, __uint_as_float(sv[2 * c2]), __uint_as_float(sv[2 * c2 + 1]), dA, dB,
+                                       -s0.lse2, -s1.lse2, a0, a1, ch0, ch1);
+                        if constexpr (MOD == MOD_ALIBI)
+                            ptx::add2(dA, dB, 2.f, 2.f);
+                        if constexpr (MOD == MOD_SOFTCAP) {
+                            if (edge) {
+                                if (key < s0.lo || key >= s0.hi)
+                                    a0 = kNegInf;
+                                if (key < s1.lo || key >= s1.hi)
+                                    a1 = kNegInf;
+                            }
+                        }
+                        const float p0 = ptx::ex2(a0), p1 = ptx::ex2(a1);
+                        ptx::fma2(u0, u1, __uint_as_float(pv[2 * c2]), __uint_as_float(pv[2 * c2 + 1]), 1.f, 1.f,
+                                  -s0.d, -s1.d);
+                        if constexpr (MOD == MOD_SOFTCAP)
+                            ptx::fma2(u0, u1, u0, u1, ch0, ch1, 0.f, 0.f);
+                        ptx::fma2(r0, r1, p0, p1, u0, u1, 0.f, 0.f);
+                        pa[16 * half + c2] = ptx::pack_bf16(p0, p1);
+                        da[16 * half + c2] = ptx::pack_bf16(r0, r1);
+                    }
+                    continue;
+                }
 #pragma unroll
                 for (int c2 = 0; c2 < 16; ++c2) {
                     float pp[2], dd[2];
