@@ -166,8 +166,7 @@ __device__ __forceinline__ float softmax_compute_p(float (&x)[N], float c, RowSt
         pk[e] = ptx::pack_bf16(p0, p1);
         const int q = 2 * (e & 3);
         ptx::add2(le[q], le[q + 1], p0, p1);
-        ptx::add2(lr[q], lr[q + 1], __uint_as_float(pk[e] << 16),
-                  __uint_as_float(pk[e] & 0xFFFF0000u));
+        ptx::add_bf16x2_to_f32(lr[q], lr[q + 1], pk[e]); // the rounded P, widened exactly
     }
     st.l += ((le[0] + le[1]) + (le[2] + le[3])) + ((le[4] + le[5]) + (le[6] + le[7]));
     st.l_round += ((lr[0] + lr[1]) + (lr[2] + lr[3])) + ((lr[4] + lr[5]) + (lr[6] + lr[7]));
