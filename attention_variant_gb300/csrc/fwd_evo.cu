@@ -472,9 +472,11 @@ __device__ __forceinline__ bool evo_tile_p(const float (&x)[64], float c, Rows2 
             ptx::add2(le[2], le[3], q0, q1);
         }
         if constexpr (RSUM) {
-            ptx::add2(lq[0], lq[1], __uint_as_float(pk[2 * r] << 16), __uint_as_float(pk[2 * r] & 0xFFFF0000u));
-            ptx::add2(lq[2], lq[3], __uint_as_float(pk[2 * r + 1] << 16),
-                      __uint_as_float(pk[2 * r + 1] & 0xFFFF0000u));
+            // the rounded P, widened exactly by mixed-precision adds (the
+            // shift-and-mask form needed registers that made the column pass
+            // at c = 64 spill: 269 against 192 us)
+            ptx::add_bf16x2_to_f32(lq[0], lq[1], pk[2 * r]);
+            ptx::add_bf16x2_to_f32(lq[2], lq[3], pk[2 * r + 1]);
         }
     }
     if constexpr (LSE) {
