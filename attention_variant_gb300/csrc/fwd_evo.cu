@@ -582,9 +582,7 @@ __device__ __forceinline__ void evo_epilogue(const EvoParams &p, uint32_t tO, co
             const int i = pr.qb * BM + pr.r0 + 8 * k;
             if (i >= p.mask.S)
                 continue;
-            const int64_t g_row = pr.b * p.g_sb + static_cast<int64_t>(i) * p.g_si + pr.h * p.g_sh;
             const int64_t o_row = pr.b * p.o_sb + static_cast<int64_t>(i) * p.o_si + pr.h * p.o_sh;
-            const uint32_t *g32 = reinterpret_cast<const uint32_t *>(p.gate + g_row) + 16 * c32;
             uint32_t *o32 = reinterpret_cast<uint32_t *>(p.out + o_row) + 16 * c32;
             const float hinv = 0.5f * inv[k];
 #pragma unroll
