@@ -401,30 +401,38 @@ __device__ void softmax_role(const Ctx<DV> &cx, const DiffParams &p, int s)
             l0 = sm.lx[0][r];
             l1 = sm.lx[1][r];
         }
-        const float c0 = l0 > 0.f ? 1.f / l0 : 0.f;
-        const float c1 = l1 > 0.f ? -p.lambda / l1 : 0.f;
+        const float c0 = l0 > 0.f ? ptx::rcp_approx(l0) : 0.f;
+        const float c1 = l1 > 0.f ? -p.lambda * ptx::rcp_approx(l1) : 0.f;
         __nv_bfloat16 *dst = p.out + it.b * p.o_sb + static_cast<int64_t>(i) * p.o_ss + it.h * p.o_sh +
                              (DV / 2) * s;
-#pragma unroll 1
-        for (int c = 0; c < DV / 32; ++c) {
-            uint32_t a[16], bb[16];
-            ptx::tmem_ld16(tO0 + (DV / 2) * s + 16 * c, a);
-            ptx::tmem_ld16(tO1 + (DV / 2) * s + 16 * c, bb);
-            ptx::tmem_wait_ld();
-            ptx::reg_fence<16>(a);
-            ptx::reg_fence<16>(bb);
-            if (i < p.mask.S) {
-                uint32_t w[8];
+        // 32 of this warpgroup's output columns per round: both streams' TMEM
+        // loads under one wait, the row written with 32-byte stores where aligned
 #pragma unroll
-                for (int e = 0; e < 8; ++e) {
+        for (int c = 0; c < DV / 64; ++c) {
+            uint32_t a[32], bb[32];
+            ptx::tmem_ld32(tO0 + (DV / 2) * s + 32 * c, a);
+            ptx::tmem_ld32(tO1 + (DV / 2) * s + 32 * c, bb);
+            ptx::tmem_wait_ld();
+            ptx::reg_fence<32>(a);
+            ptx::reg_fence<32>(bb);
+            if (i < p.mask.S) {
+                uint32_t w[16];
+#pragma unroll
+                for (int e = 0; e < 16; ++e) {
                     const float y0 = fmaf(__uint_as_float(a[2 * e]), c0, __uint_as_float(bb[2 * e]) * c1);
                     const float y1 =
                         fmaf(__uint_as_float(a[2 * e + 1]), c0, __uint_as_float(bb[2 * e + 1]) * c1);
                     w[e] = ptx::pack_bf16(y0, y1);
                 }
-                uint4 *d4 = reinterpret_cast<uint4 *>(dst + 16 * c);
-                d4[0] = make_uint4(w[0], w[1], w[2], w[3]);
-                d4[1] = make_uint4(w[4], w[5], w[6], w[7]);
+                uint4 *d4 = reinterpret_cast<uint4 *>(dst + 32 * c);
+                if ((reinterpret_cast<uint64_t>(d4) & 31u) == 0u) {
+                    ptx::st_global_v8(d4, w);
+                    ptx::st_global_v8(d4 + 2, w + 8);
+                } else {
+#pragma unroll
+                    for (int q = 0; q < 4; ++q)
+                        d4[q] = make_uint4(w[4 * q], w[4 * q + 1], w[4 * q + 2], w[4 * q + 3]);
+                }
             }
         }
         ptx::tc_fence_before();

@@ -724,7 +724,7 @@ __device__ void softmax_role(const KernelCtx<D> &cx, const StdParams &p, int t)
                 ptx::tmem_wait_ld();
                 ptx::reg_fence<1>(sum);
                 const float l_round = __uint_as_float(sum[0]);
-                inv = l_round > 0.f ? 1.f / l_round : 0.f;
+                inv = l_round > 0.f ? ptx::rcp_approx(l_round) : 0.f;
             } else {
                 ptx::tmem_wait_ld();
             }
@@ -732,14 +732,22 @@ __device__ void softmax_role(const KernelCtx<D> &cx, const StdParams &p, int t)
             for (int c32 = 0; c32 < kCols / 32; ++c32)
                 ptx::reg_fence<32>(o + 32 * c32);
             if (i < p.mask.S) {
+                uint32_t w[kCols / 2];
 #pragma unroll
-                for (int c = 0; c < kCols / 8; ++c) {
-                    uint4 w;
-                    w.x = ptx::pack_bf16(__uint_as_float(o[8 * c + 0]) * inv, __uint_as_float(o[8 * c + 1]) * inv);
-                    w.y = ptx::pack_bf16(__uint_as_float(o[8 * c + 2]) * inv, __uint_as_float(o[8 * c + 3]) * inv);
-                    w.z = ptx::pack_bf16(__uint_as_float(o[8 * c + 4]) * inv, __uint_as_float(o[8 * c + 5]) * inv);
-                    w.w = ptx::pack_bf16(__uint_as_float(o[8 * c + 6]) * inv, __uint_as_float(o[8 * c + 7]) * inv);
-                    d4[round * (kCols / 8) + c] = w;
+                for (int c = 0; c < kCols / 2; ++c)
+                    w[c] = ptx::pack_bf16(__uint_as_float(o[2 * c]) * inv, __uint_as_float(o[2 * c + 1]) * inv);
+                // the row as 32-byte stores where it is 32-byte aligned (half the
+                // store instructions and L1 wavefronts of 16-byte stores: S = 512
+                // 522 -> 543, S = 2048 876 -> 883, D = 128 1039 -> 1068 TFLOP/s)
+                uint4 *dr = d4 + round * (kCols / 8);
+                if ((reinterpret_cast<uint64_t>(dr) & 31u) == 0u) {
+#pragma unroll
+                    for (int c = 0; c < kCols / 16; ++c)
+                        ptx::st_global_v8(dr + 2 * c, w + 8 * c);
+                } else {
+#pragma unroll
+                    for (int c = 0; c < kCols / 8; ++c)
+                        dr[c] = make_uint4(w[4 * c], w[4 * c + 1], w[4 * c + 2], w[4 * c + 3]);
                 }
             }
         }

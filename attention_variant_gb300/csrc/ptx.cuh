@@ -390,6 +390,14 @@ __device__ __forceinline__ float rcp_approx(float x)
     return y;
 }
 
+// One 32-byte global store of eight words (the address must be 32-byte aligned).
+__device__ __forceinline__ void st_global_v8(void *ptr, const uint32_t *r)
+{
+    asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(ptr), "r"(r[0]), "r"(r[1]),
+                 "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7])
+                 : "memory");
+}
+
 // Packed fp32 pair arithmetic (one instruction for two lanes of work).
 __device__ __forceinline__ void fma2(float &d0, float &d1, float a0, float a1, float b0, float b1,
                                      float c0, float c1)

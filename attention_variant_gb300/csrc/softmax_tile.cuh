@@ -260,7 +260,7 @@ __device__ __forceinline__ float row_lse(const RowState &st)
 // 1 / (the normaliser of O), 0 for a row with no allowed key.
 __device__ __forceinline__ float row_inv_norm(const RowState &st)
 {
-    return st.l_round > 0.f ? 1.f / st.l_round : 0.f;
+    return st.l_round > 0.f ? ptx::rcp_approx(st.l_round) : 0.f; // l_round >= 1: the row max has P >= 1
 }
 
 } // namespace fl
