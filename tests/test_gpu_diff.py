@@ -124,6 +124,25 @@ def test_diff_tile_edges(Dv, S):
         assert np.array_equal(cnt, gu.expected_tile_counts(mask, 1, 2, S, bn=_bn(Dv)))
 
 
+@pytest.mark.parametrize("Dv", [64, 128])
+def test_diff_output_rows_off_32_byte_alignment(Dv):
+    # O in a view 16 bytes into its buffer with a row pitch of Dv + 8
+    # elements: the epilogue's 16-byte store path
+    B, S, H = 1, 200, 2
+    q, k, v = _inputs(f"diffmisal{Dv}", B, S, H, Dv=Dv)
+    big = torch.full((B, S, H, Dv + 8), float("nan"), dtype=torch.bfloat16, device="cuda")
+    out = big[..., 8:]
+    lse = torch.full((2, B, H, S), float("nan"), dtype=torch.float32, device="cuda")
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    fa.fl_attn_fwd(gu.dev(q), gu.dev(k), gu.dev(v), out, lse,
+                   fa.make_desc(kind="diff", mask="causal", diff_lambda=0.5, error_word=err))
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    oref, lref = oracle.diff_attention(q, k, v, 0.5, mask="causal")
+    gu.compare(gu.f64(out), gu.f64(lse), oref, lref, what=f"diff misaligned rows dv{Dv}")
+    assert torch.isnan(big[..., :8]).all()
+
+
 @pytest.mark.parametrize("mask", ["none", "causal"])
 def test_diff_full_size(mask):
     """The whole output of the full-size workload against the oracle."""

@@ -207,6 +207,25 @@ def test_strided_layout_and_no_lse():
     gu.compare(o, None, oref, None, what="bhsd")
 
 
+@pytest.mark.parametrize("D", [32, 64, 128])
+def test_output_rows_off_32_byte_alignment(D):
+    # O written into a view that starts 16 bytes into its buffer, with a row
+    # pitch of D + 8 elements: every row is 16-byte but not 32-byte aligned
+    # (the epilogue's 16-byte store path; aligned rows take 32-byte stores)
+    B, S, H = 2, 300, 3
+    q, k, v = _inputs(f"misal{D}", B, S, H, D=D, Dv=D)
+    big = torch.full((B, S, H, D + 8), float("nan"), dtype=torch.bfloat16, device="cuda")
+    out = big[..., 8:]
+    lse = torch.full((B, H, S), float("nan"), dtype=torch.float32, device="cuda")
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    fa.fl_attn_fwd(gu.dev(q), gu.dev(k), gu.dev(v), out, lse, fa.make_desc(mask="causal", error_word=err))
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    oref, lref = oracle.attention(q, k, v, mask="causal")
+    gu.compare(gu.f64(out), gu.f64(lse), oref, lref, what=f"misaligned rows D{D}")
+    assert torch.isnan(big[..., :8]).all()  # nothing written outside the view
+
+
 def test_custom_scale_and_slopes():
     q, k, v = _inputs("scale", 1, 256, 4)
     slopes = np.array([0.5, 0.25, 0.0, 1.0], dtype=np.float32)
