@@ -89,6 +89,47 @@ def unmasked_pairs(mask, B, H, S, window=0, prefix=0, doc=None):
     return total
 
 
+def visited_pairs(mask, B, H, S, bn, window=0, prefix=0, doc=None):
+    """Pairs inside the key tiles the kernel visits: per 128-row query block,
+    its rows times the keys of the tiles [floor(lo_first / bn), ceil(hi_last / bn))
+    (the last tile clipped to S).  Against the unmasked pairs it shows the
+    work spent on masked pairs of partial tiles."""
+    total = 0
+    for b in range(B):
+        lo, hi = row_intervals(mask, S, window, prefix, None if doc is None else doc[b])
+        q0 = np.arange(0, S, 128)
+        q1 = np.minimum(q0 + 128, S)
+        t_lo = lo[q0] // bn
+        t_hi = -(-hi[q1 - 1] // bn)
+        keys = np.minimum(t_hi * bn, S) - t_lo * bn
+        total += int(((q1 - q0) * keys).sum()) * H
+    return total
+
+
+# XU-pipe cycles per visited pair and sub-partition: a 2^x takes 4 cycles per
+# warp instruction (32 pairs), the bf16 pack of two P 2 cycles; softcap adds a
+# 2^x and a reciprocal (probed rates, 32 2^x per clock and SM).
+XU_CYCLES_PER_PAIR = {"none": (4 + 1) / 32, "alibi": (4 + 1) / 32, "softcap": (12 + 1) / 32}
+
+
+def bound_times(e, peaks, sms=152, clock_hz=2.07e9):
+    """The launch's lower bounds in us: tensor (algorithmic flops at the
+    measured bf16 peak), HBM (algorithmic bytes at the measured copy rate) and
+    XU (the special-function work of the visited pairs at the maximum clock)."""
+    out = dict(t_tc_us=round(e["flops"] / (peaks["bf16_tflops"] * 1e12) * 1e6, 1),
+               t_hbm_us=round(e["bytes"] / (peaks["hbm_gbs"] * 1e9) * 1e6, 1))
+    if "visited" in e:
+        xu = e["visited"] * XU_CYCLES_PER_PAIR.get(e.get("mod", "none"), XU_CYCLES_PER_PAIR["none"])
+        out["t_xu_us"] = round(xu / (4 * sms * clock_hz) * 1e6, 1)
+    return out
+
+
+def spread(ms):
+    """Median and standard deviation of per-step times (the mean is the value)."""
+    return dict(median_ms=round(statistics.median(ms), 4),
+                std_ms=round(statistics.pstdev(ms), 4) if len(ms) > 1 else 0.0)
+
+
 def entry(kind, S, variant, D=workloads.HEAD_DIM):
     """One benchmark entry of the MHA sweep ("mha") or GQA mask sweep ("gqa");
     D other than the sweep's 64 names a head-dimension variant of its shape."""
@@ -764,10 +805,12 @@ def run_ours(args):
                   evo_entry(False), evo_entry(True, workloads.EVO_C64), evo_entry(False, workloads.EVO_C64)]:
             vms = time_other(e, torch, fa, device, args.variant_steps, 2, flush, stream)
             vm = statistics.mean(vms)
+            if e["kind"].startswith("evo"):
+                e["visited"] = e["pairs"]  # 128-key tiles: N_res 384 and N_seq 512 leave no partial tile
             tf = e["flops"] / (vm * 1e-3) / 1e12
             gbs = e["bytes"] / (vm * 1e-3) / 1e9
             rec = dict(tflops=round(tf, 1), frac_peak=round(tf / peaks["bf16_tflops"], 4),
-                       ms=round(vm, 4), gbs=round(gbs, 1))
+                       ms=round(vm, 4), gbs=round(gbs, 1), **spread(vms), **bound_times(e, peaks))
             if e["kind"].startswith("evo"):
                 rec["frac_hbm"] = round(gbs / peaks["hbm_gbs"], 4)
             rec["l2"] = l2_policy(e)
@@ -803,9 +846,14 @@ def run_ours(args):
             vms, _ = time_entry(e, h, torch, fa, device, args.variant_steps, 2, flush, stream)
             vm = statistics.mean(vms)
             tf = e["flops"] / (vm * 1e-3) / 1e12
+            bn = fa.fl_attn_tile_shape(fa.make_desc(), e["D"])[1]
+            e["visited"] = visited_pairs(e["mask"], e["B"], e["Hq"], e["S"], bn, e["kw"].get("window", 0),
+                                         e["kw"].get("prefix", 0), e["doc"])
             variants[f"{e['name']}/{e['variant']}"] = dict(
                 tflops=round(tf, 1), frac_peak=round(tf / peaks["bf16_tflops"], 4),
-                ms=round(vm, 4), gbs=round(e["bytes"] / (vm * 1e-3) / 1e9, 1))
+                ms=round(vm, 4), gbs=round(e["bytes"] / (vm * 1e-3) / 1e9, 1), **spread(vms),
+                visited_tflops=round(4 * e["D"] * e["visited"] / (vm * 1e-3) / 1e12, 1),
+                **bound_times(e, peaks))
 
     if rank != 0:
         return
