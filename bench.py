@@ -124,6 +124,9 @@ def bound_times(e, peaks, sms=152, clock_hz=2.07e9):
     return out
 
 
+VARIANT_WARMUP = 3  # untimed launches before each variant's timed steps
+
+
 def spread(ms):
     """Median and standard deviation of per-step times (the mean is the value)."""
     return dict(median_ms=round(statistics.median(ms), 4),
@@ -803,7 +806,7 @@ def run_ours(args):
     if not args.headline_only:
         for e in [diff_entry("none"), diff_entry("causal"), diff_entry("none", Dv=64), evo_entry(True),
                   evo_entry(False), evo_entry(True, workloads.EVO_C64), evo_entry(False, workloads.EVO_C64)]:
-            vms = time_other(e, torch, fa, device, args.variant_steps, 2, flush, stream)
+            vms = time_other(e, torch, fa, device, args.variant_steps, VARIANT_WARMUP, flush, stream)
             vm = statistics.mean(vms)
             if e["kind"].startswith("evo"):
                 e["visited"] = e["pairs"]  # 128-key tiles: N_res 384 and N_seq 512 leave no partial tile
@@ -816,34 +819,40 @@ def run_ours(args):
             rec["l2"] = l2_policy(e)
             variants[f"{e['name']}/{e['variant']}"] = rec
         for e in (evo_batched_entry(True), evo_batched_entry(False)):
-            vm = statistics.mean(time_evo_batched(e, torch, fa, device, args.variant_steps, 2, flush,
-                                                  stream))
+            vms = time_evo_batched(e, torch, fa, device, args.variant_steps, VARIANT_WARMUP, flush, stream)
+            vm = statistics.mean(vms)
             gbs = e["bytes"] / (vm * 1e-3) / 1e9
             variants[f"{e['name']}/{e['variant']}"] = dict(
                 tflops=round(e["flops"] / (vm * 1e-3) / 1e12, 1), ms=round(vm, 4), gbs=round(gbs, 1),
-                frac_hbm=round(gbs / peaks["hbm_gbs"], 4), l2=l2_policy(e))
+                frac_hbm=round(gbs / peaks["hbm_gbs"], 4), **spread(vms), l2=l2_policy(e))
         for e in (bwd_entry("none"), bwd_entry("causal"), bwd_entry("none", mod="softcap"),
                   bwd_entry("none", EXPR_VARIANTS["expr_softcap"][1])):
-            vm = statistics.mean(time_bwd(e, torch, fa, device, args.variant_steps, 2, flush, stream))
+            vms = time_bwd(e, torch, fa, device, args.variant_steps, VARIANT_WARMUP, flush, stream)
+            vm = statistics.mean(vms)
             tf = e["flops"] / (vm * 1e-3) / 1e12
             variants[f"{e['name']}/{e['variant']}"] = dict(
                 tflops=round(tf, 1), frac_peak=round(tf / peaks["bf16_tflops"], 4), ms=round(vm, 4),
-                gbs=round(e["bytes"] / (vm * 1e-3) / 1e9, 1), l2="flushed before every timed step (256 MiB write)")
+                gbs=round(e["bytes"] / (vm * 1e-3) / 1e9, 1), **spread(vms), **bound_times(e, peaks),
+                l2="flushed before every timed step (256 MiB write)")
         for e in (diff_bwd_entry("none"), diff_bwd_entry("causal")):
-            vm = statistics.mean(time_diff_bwd(e, torch, fa, device, args.variant_steps, 2, flush, stream))
+            vms = time_diff_bwd(e, torch, fa, device, args.variant_steps, VARIANT_WARMUP, flush, stream)
+            vm = statistics.mean(vms)
             tf = e["flops"] / (vm * 1e-3) / 1e12
             variants[f"{e['name']}/{e['variant']}"] = dict(
                 tflops=round(tf, 1), frac_peak=round(tf / peaks["bf16_tflops"], 4), ms=round(vm, 4),
-                gbs=round(e["bytes"] / (vm * 1e-3) / 1e9, 1), l2="flushed before every timed step (256 MiB write)")
+                gbs=round(e["bytes"] / (vm * 1e-3) / 1e9, 1), **spread(vms), **bound_times(e, peaks),
+                l2="flushed before every timed step (256 MiB write)")
         for e in (decode_entry("none"), decode_entry("softcap")):
-            vm = statistics.mean(time_decode(e, torch, fa, device, args.variant_steps, 2, flush, stream))
+            vms = time_decode(e, torch, fa, device, args.variant_steps, VARIANT_WARMUP, flush, stream)
+            vm = statistics.mean(vms)
             gbs = e["bytes"] / (vm * 1e-3) / 1e9
             variants[f"{e['name']}/{e['variant']}"] = dict(
                 tflops=round(e["flops"] / (vm * 1e-3) / 1e12, 1), ms=round(vm, 4), gbs=round(gbs, 1),
-                frac_hbm=round(gbs / peaks["hbm_gbs"], 4), l2=l2_policy(e))
+                frac_hbm=round(gbs / peaks["hbm_gbs"], 4), **spread(vms), **bound_times(e, peaks),
+                l2=l2_policy(e))
         for e in all_entries() + [expr_entry(head["S"], n) for n in EXPR_VARIANTS] + head_dim_entries():
             h = host if e["name"] == head["name"] else gpu_inputs(e, torch, device)
-            vms, _ = time_entry(e, h, torch, fa, device, args.variant_steps, 2, flush, stream)
+            vms, _ = time_entry(e, h, torch, fa, device, args.variant_steps, VARIANT_WARMUP, flush, stream)
             vm = statistics.mean(vms)
             tf = e["flops"] / (vm * 1e-3) / 1e12
             bn = fa.fl_attn_tile_shape(fa.make_desc(), e["D"])[1]
