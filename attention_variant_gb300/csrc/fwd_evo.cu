@@ -58,6 +58,7 @@
 #include "common.cuh"
 #include "launch.h"
 #include "softmax_tile.cuh"
+#include "warp_mma.cuh"
 
 namespace fl {
 namespace {
@@ -641,11 +642,24 @@ __device__ void softmax_role(const Ctx<C, BIAS> &cx, const EvoParams &p, int t, 
     const int S = p.mask.S;
     const int nkv = (S + BN - 1) / BN;
     // bias smem: row R of a 64-key box is 128 bytes, 16-byte chunk cc (8 keys)
-    // stored at position cc ^ (R & 7) (the 128-byte swizzle the TMA wrote);
-    // this thread's 32-bit word of a chunk is at byte 4 jq, and rows r0 and
-    // r0 + 8 share the swizzle phase
-    const uint32_t bias_r0 = ptx::smem_u32(sm.bias) + r0 * 128 + 4 * jq;
-    const uint32_t swz = r0 & 7;
+    // stored at position cc ^ (R & 7) (the 128-byte swizzle the TMA wrote).
+    // The bias words come in with ldmatrix: its m8n8 fragment gives thread t
+    // row t / 4 and columns 2 (t % 4), 2 (t % 4) + 1 of an 8 x 8 block -- this
+    // thread's two keys of an 8-key chunk of rows r0 and r0 + 8, the layout of
+    // the scores.  One x4 load covers two chunks of both rows; lane l gives the
+    // address of row l % 8 of block l / 8 (rows rb + 8 (block % 2) + l % 8,
+    // chunk 2q + block / 2), so boff[q] is this lane's offset for chunk pair q
+    // of a 64-key box.  Eight x4 loads replace 32 four-byte loads and their
+    // swizzled addresses per tile (row pass 243 -> 222 us).
+    const uint32_t bias_s0 = ptx::smem_u32(sm.bias);
+    uint32_t boff[4];
+    {
+        const uint32_t lm = static_cast<uint32_t>(lane) >> 3, li = static_cast<uint32_t>(lane) & 7u;
+        const uint32_t lrow = static_cast<uint32_t>(32 * wq + 16 * (wi >> 2)) + 8u * (lm & 1u) + li;
+#pragma unroll
+        for (int q = 0; q < 4; ++q)
+            boff[q] = lrow * 128u + (((2u * q + (lm >> 1)) ^ li) << 4);
+    }
     uint32_t scount = 0, pvcount = 0, item_count = 0, bias_count = 0;
     bool pending = false;
     PendingRow prev{};
@@ -672,9 +686,9 @@ __device__ void softmax_role(const Ctx<C, BIAS> &cx, const EvoParams &p, int t, 
                         ptx::mbar_arrive(bar(sm.bias_empty[bs]));
                     continue;
                 }
-                bias_base = bias_r0 + 2 * bs * kBiasBox;
+                bias_base = bias_s0 + 2 * bs * kBiasBox;
             } else {
-                bias_base = bias_r0 + 2 * j * kBiasBox;
+                bias_base = bias_s0 + 2 * j * kBiasBox;
             }
             const int b = it.b0 + t + 2 * n;
             const int j0 = j * BN;
@@ -709,15 +723,18 @@ __device__ void softmax_role(const Ctx<C, BIAS> &cx, const EvoParams &p, int t, 
                 // the exponent
                 c = kLog2e;
 #pragma unroll
-                for (int r = 0; r < 16; ++r) {
-                    const uint32_t a = bias_base + (r >> 3) * kBiasBox + (((r & 7) ^ swz) << 4);
-                    uint32_t w0, w1;
-                    asm volatile("ld.shared.b32 %0, [%1];" : "=r"(w0) : "r"(a));
-                    asm volatile("ld.shared.b32 %0, [%1];" : "=r"(w1) : "r"(a + 8 * 128));
-                    ptx::fma2(x[4 * r], x[4 * r + 1], x[4 * r], x[4 * r + 1], p.qk_scale, p.qk_scale,
-                              __uint_as_float(w0 << 16), __uint_as_float(w0 & 0xFFFF0000u));
-                    ptx::fma2(x[4 * r + 2], x[4 * r + 3], x[4 * r + 2], x[4 * r + 3], p.qk_scale, p.qk_scale,
-                              __uint_as_float(w1 << 16), __uint_as_float(w1 & 0xFFFF0000u));
+                for (int q = 0; q < 8; ++q) {
+                    uint32_t w[4]; // chunk 2q rows r0, r0 + 8; chunk 2q + 1 rows r0, r0 + 8
+                    wm::ldsm_x4(bias_base + (q >> 2) * kBiasBox + boff[q & 3], w[0], w[1], w[2], w[3]);
+#pragma unroll
+                    for (int h = 0; h < 2; ++h) {
+                        const int r = 2 * q + h;
+                        const uint32_t w0 = w[2 * h], w1 = w[2 * h + 1];
+                        ptx::fma2(x[4 * r], x[4 * r + 1], x[4 * r], x[4 * r + 1], p.qk_scale, p.qk_scale,
+                                  __uint_as_float(w0 << 16), __uint_as_float(w0 & 0xFFFF0000u));
+                        ptx::fma2(x[4 * r + 2], x[4 * r + 3], x[4 * r + 2], x[4 * r + 3], p.qk_scale,
+                                  p.qk_scale, __uint_as_float(w1 << 16), __uint_as_float(w1 & 0xFFFF0000u));
+                    }
                 }
             }
             if (j0 + BN > S) {
